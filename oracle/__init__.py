@@ -1,0 +1,268 @@
+"""CPU oracle for the NVFP4 / FP8 paged KV cache (numpy front end).
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / reference leg of ``bench.py`` may import this package.  The
+CUDA library never loads it and shares no code with it; the two meet only
+through the seeded input generators, which hold none of the method's
+arithmetic.
+
+The arithmetic lives in ``nvfp4kv_oracle.c`` (scalar C, one thread, FP32
+quantizer steps without FMA contraction, FP64 attention); this module only
+marshals numpy arrays.  Every function cites the page passage it follows:
+
+  [P1] "SOAR Weekly Champion Notes 05 | Zhisuan Team One: NVFP4 KV Cache and
+       Mixed-Precision Practice", sections 02 and 03.
+  [P2] "SGLang x Qwen x NVIDIA Collaboration: NVFP4 KV Cache Breaks
+       Long-Context and Agentic Inference Bottlenecks", sections "The Core of
+       the Ledger: 4-bit Does Not Equal 2x" and "Three Paths".
+
+Parity pins live in ``tests/test_oracle_*.py``.  Functions whose result the
+pages' throughput figures would pin (end-to-end serving speed-ups) are not
+implemented: parity unpinned, out of scope.
+"""
+import ctypes
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_f32p = ctypes.POINTER(ctypes.c_float)
+_f64p = ctypes.POINTER(ctypes.c_double)
+
+PREC_NVFP4 = 0
+PREC_FP8 = 1
+
+NVFP4_GLOBAL_DIVISOR = 6.0 * 448.0  # largest E2M1 magnitude x largest E4M3 value
+FP8_GLOBAL_DIVISOR = 448.0
+
+
+def lib():
+    global _LIB
+    if _LIB is None:
+        L = ctypes.CDLL(_build.build())
+        L.orc_e2m1_value.restype = ctypes.c_double
+        L.orc_e2m1_value.argtypes = [ctypes.c_uint8]
+        L.orc_e4m3_value.restype = ctypes.c_double
+        L.orc_e4m3_value.argtypes = [ctypes.c_uint8]
+        L.orc_e2m1_encode.restype = ctypes.c_uint8
+        L.orc_e2m1_encode.argtypes = [ctypes.c_float]
+        L.orc_e4m3_encode.restype = ctypes.c_uint8
+        L.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        for n in ("orc_e2m1_encode_bits", "orc_e4m3_encode_bits"):
+            f = getattr(L, n)
+            f.restype = None
+            f.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _u8p]
+        L.orc_global_scale.restype = ctypes.c_float
+        L.orc_global_scale.argtypes = [_f32p, ctypes.c_int64, ctypes.c_float]
+        L.orc_nvfp4_quantize_write.restype = ctypes.c_int
+        L.orc_nvfp4_quantize_write.argtypes = [_f32p, _f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _i64p,
+                                               _f32p, ctypes.c_int, ctypes.c_int64, _u8p, _u8p, _u8p, _u8p]
+        L.orc_fp8_quantize_write.restype = ctypes.c_int
+        L.orc_fp8_quantize_write.argtypes = [_f32p, _f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _i64p,
+                                             _f32p, ctypes.c_int, ctypes.c_int64, _u8p, _u8p]
+        L.orc_gather_dequant.restype = ctypes.c_int
+        L.orc_gather_dequant.argtypes = [ctypes.c_int, _u8p, _u8p, ctypes.c_float, _i32p, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                         _f64p]
+        L.orc_paged_decode_attention.restype = ctypes.c_int
+        L.orc_paged_decode_attention.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_int, _u8p, _u8p, _u8p, _u8p, _f32p, _i32p,
+                                                 ctypes.c_int, _i32p, ctypes.c_int64, ctypes.c_double,
+                                                 ctypes.c_int, _f64p]
+        L.orc_dequant_to_fp8_workspace.restype = ctypes.c_int
+        L.orc_dequant_to_fp8_workspace.argtypes = [_i32p, ctypes.c_int, _i32p, _i32p, _i64p, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                                   _u8p, _u8p, _u8p, _u8p, _f32p, _f32p, _u8p, _u8p]
+        _LIB = L
+    return _LIB
+
+
+def _p(a, t):
+    return a.ctypes.data_as(t)
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+# --------------------------------------------------------------------------
+# Element formats ([P1] 02; [P2] Core of the Ledger)
+# --------------------------------------------------------------------------
+
+def e2m1_value(code: int) -> float:
+    """Value of a 4-bit E2M1 code (1 sign, 2 exponent, 1 mantissa bit)."""
+    return lib().orc_e2m1_value(code)
+
+
+def e4m3_value(b: int) -> float:
+    """Value of an E4M3 byte (OCP 'fn' variant); NaN for 0x7F / 0xFF."""
+    return lib().orc_e4m3_value(b)
+
+
+def e2m1_encode(y: float) -> int:
+    """Round-to-nearest-even E2M1 code of an FP32 value, saturating at 6."""
+    return lib().orc_e2m1_encode(y)
+
+
+def e4m3_encode(y: float) -> int:
+    """Round-to-nearest-even E4M3 byte of an FP32 value, saturating at 448."""
+    return lib().orc_e4m3_encode(y)
+
+
+def e2m1_encode_bits(start: int, count: int) -> np.ndarray:
+    out = np.empty(count, np.uint8)
+    lib().orc_e2m1_encode_bits(start, count, _p(out, _u8p))
+    return out
+
+
+def e4m3_encode_bits(start: int, count: int) -> np.ndarray:
+    out = np.empty(count, np.uint8)
+    lib().orc_e4m3_encode_bits(start, count, _p(out, _u8p))
+    return out
+
+
+def e2m1_encode_array(y: np.ndarray) -> np.ndarray:
+    y = _c(y, np.float32).ravel()
+    return np.array([lib().orc_e2m1_encode(float(v)) for v in y], np.uint8)
+
+
+def e4m3_encode_array(y: np.ndarray) -> np.ndarray:
+    y = _c(y, np.float32).ravel()
+    bits = y.view(np.uint32)
+    out = np.empty(y.size, np.uint8)
+    L = lib()
+    for i, u in enumerate(bits):
+        L.orc_e4m3_encode_bits(int(u), 1, _p(out[i:i + 1], _u8p))
+    return out
+
+
+# --------------------------------------------------------------------------
+# Global scale ([P2] Core of the Ledger: one FP32 global scale per tensor)
+# --------------------------------------------------------------------------
+
+def global_scale(x: np.ndarray, divisor: float = NVFP4_GLOBAL_DIVISOR) -> np.float32:
+    x = _c(x, np.float32)
+    return np.float32(lib().orc_global_scale(_p(x, _f32p), x.size, divisor))
+
+
+# --------------------------------------------------------------------------
+# Paged cache ([P1] 02 "FP4 memory pool"; [P2] Three Paths, paged KV cache)
+# --------------------------------------------------------------------------
+
+class Cache:
+    """One layer's paged cache planes (head-major inside a page).
+
+    NVFP4: ``k_data``/``v_data`` [num_pages, Hkv, P, D/2] codes, ``k_scale``/
+    ``v_scale`` [num_pages, Hkv, P, D/16] E4M3 bytes.  FP8: data
+    [num_pages, Hkv, P, D], no scale planes.  ``g`` = float32[2] (K, V)
+    global (NVFP4) or per-tensor (FP8) scale.
+    """
+
+    def __init__(self, prec, num_pages, Hkv, P, D, g, fill=0):
+        self.prec, self.num_pages, self.Hkv, self.P, self.D = prec, num_pages, Hkv, P, D
+        self.g = np.asarray(g, np.float32).reshape(2).copy()
+        if prec == PREC_NVFP4:
+            self.k_data = np.full((num_pages, Hkv, P, D // 2), fill, np.uint8)
+            self.v_data = np.full((num_pages, Hkv, P, D // 2), fill, np.uint8)
+            self.k_scale = np.full((num_pages, Hkv, P, D // 16), fill, np.uint8)
+            self.v_scale = np.full((num_pages, Hkv, P, D // 16), fill, np.uint8)
+        else:
+            self.k_data = np.full((num_pages, Hkv, P, D), fill, np.uint8)
+            self.v_data = np.full((num_pages, Hkv, P, D), fill, np.uint8)
+            self.k_scale = np.zeros(1, np.uint8)
+            self.v_scale = np.zeros(1, np.uint8)
+
+
+def quantize_write(cache: Cache, k: np.ndarray, v: np.ndarray, slot_mapping: np.ndarray) -> None:
+    """Quantized write of new K/V [T, Hkv, D] into the cache slots.
+
+    NVFP4 follows [P2] Core of the Ledger (two-level scaling) and [P1] 02
+    (two codes per byte); FP8 follows [P1] 01/03 (FP8 KV cache layers).
+    """
+    k = _c(k, np.float32)
+    v = _c(v, np.float32)
+    assert np.isfinite(k).all() and np.isfinite(v).all()
+    sm = _c(slot_mapping, np.int64)
+    T = sm.shape[0]
+    assert k.shape == (T, cache.Hkv, cache.D) and v.shape == k.shape
+    L = lib()
+    if cache.prec == PREC_NVFP4:
+        rc = L.orc_nvfp4_quantize_write(_p(k, _f32p), _p(v, _f32p), T, cache.Hkv, cache.D, _p(sm, _i64p),
+                                        _p(cache.g, _f32p), cache.P, cache.num_pages, _p(cache.k_data, _u8p),
+                                        _p(cache.k_scale, _u8p), _p(cache.v_data, _u8p), _p(cache.v_scale, _u8p))
+    else:
+        rc = L.orc_fp8_quantize_write(_p(k, _f32p), _p(v, _f32p), T, cache.Hkv, cache.D, _p(sm, _i64p),
+                                      _p(cache.g, _f32p), cache.P, cache.num_pages, _p(cache.k_data, _u8p),
+                                      _p(cache.v_data, _u8p))
+    if rc != 0:
+        raise ValueError("slot out of range")
+
+
+def gather_dequant(cache: Cache, which: str, block_row: np.ndarray, L: int, h: int) -> np.ndarray:
+    """Exact FP64 values of tokens [0, L) of one (sequence, KV head)."""
+    br = _c(block_row, np.int32)
+    out = np.empty((L, cache.D), np.float64)
+    data, sc, g = ((cache.k_data, cache.k_scale, cache.g[0]) if which == "k"
+                   else (cache.v_data, cache.v_scale, cache.g[1]))
+    rc = lib().orc_gather_dequant(cache.prec, _p(data, _u8p), _p(sc, _u8p), float(g), _p(br, _i32p), L,
+                                  cache.Hkv, h, cache.D, cache.P, cache.num_pages, _p(out, _f64p))
+    if rc != 0:
+        raise ValueError("page out of range")
+    return out
+
+
+def paged_decode_attention(cache: Cache, q_bf16_bits: np.ndarray, block_table: np.ndarray,
+                           seq_lens: np.ndarray, sm_scale: float = 0.0, num_splits: int = 0) -> np.ndarray:
+    """Paged GQA decode attention in FP64 ([P2] Three Paths, decode).
+
+    ``q_bf16_bits``: uint16 [B, Hq, D] BF16 bit patterns.  Returns FP64
+    [B, Hq, D].  ``num_splits > 1`` evaluates the split / log-sum-exp merge
+    form, which must equal the plain softmax.
+    """
+    q = _c(q_bf16_bits, np.uint16)
+    B, Hq, D = q.shape
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    if sm_scale == 0.0:
+        sm_scale = 1.0 / np.sqrt(D)
+    out = np.empty((B, Hq, D), np.float64)
+    rc = lib().orc_paged_decode_attention(_p(q, _u16p), B, Hq, cache.Hkv, D, cache.P, cache.prec,
+                                          _p(cache.k_data, _u8p), _p(cache.k_scale, _u8p), _p(cache.v_data, _u8p),
+                                          _p(cache.v_scale, _u8p), _p(cache.g, _f32p), _p(bt, _i32p), bt.shape[1],
+                                          _p(sl, _i32p), cache.num_pages, float(sm_scale), int(num_splits),
+                                          _p(out, _f64p))
+    if rc != 0:
+        raise ValueError("bad block table / sequence length")
+    return out
+
+
+def dequant_to_fp8_workspace(cache: Cache, block_table: np.ndarray, seq_ids, prefix_lens,
+                             ws_scale) -> tuple:
+    """Chunked-extend prefix dequant into the FP8 workspace ([P2] Three Paths).
+
+    Returns (ws_k, ws_v), uint8 [sum(prefix_lens), Hkv, D] E4M3.
+    """
+    assert cache.prec == PREC_NVFP4
+    bt = _c(block_table, np.int32)
+    ids = _c(seq_ids, np.int32)
+    pl = _c(prefix_lens, np.int32)
+    cu = np.zeros(len(pl) + 1, np.int64)
+    cu[1:] = np.cumsum(pl)
+    ws = _c(ws_scale, np.float32).reshape(2)
+    rows = int(cu[-1])
+    wk = np.zeros((rows, cache.Hkv, cache.D), np.uint8)
+    wv = np.zeros((rows, cache.Hkv, cache.D), np.uint8)
+    rc = lib().orc_dequant_to_fp8_workspace(_p(bt, _i32p), bt.shape[1], _p(ids, _i32p), _p(pl, _i32p),
+                                            _p(cu, _i64p), len(pl), cache.Hkv, cache.D, cache.P, cache.num_pages,
+                                            _p(cache.k_data, _u8p), _p(cache.k_scale, _u8p),
+                                            _p(cache.v_data, _u8p), _p(cache.v_scale, _u8p), _p(cache.g, _f32p),
+                                            _p(ws, _f32p), _p(wk, _u8p), _p(wv, _u8p))
+    if rc != 0:
+        raise ValueError("bad arguments")
+    return wk, wv

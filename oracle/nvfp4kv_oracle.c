@@ -1,0 +1,404 @@
+/*
+ * nvfp4kv oracle: a plain, scalar, single-threaded CPU statement of what the
+ * NVFP4 / FP8 paged KV-cache hot path computes.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header, table or helper with the
+ * CUDA library and includes nothing from it.
+ *
+ * Sources (page title, section):
+ *   [P1] "SOAR Weekly Champion Notes 05 | Zhisuan Team One: NVFP4 KV Cache and
+ *        Mixed-Precision Practice", sections 02 (NVFP4 KV Cache) and
+ *        03 (Mixed-precision KV Cache).
+ *   [P2] "SGLang x Qwen x NVIDIA Collaboration: NVFP4 KV Cache Breaks
+ *        Long-Context and Agentic Inference Bottlenecks", sections
+ *        "The Core of the Ledger: 4-bit Does Not Equal 2x" and
+ *        "Three Paths: Putting the Quantization Cost on the Compute-Bound Side".
+ *
+ * The pages fix the structure (E2M1 = 1 sign + 2 exponent + 1 mantissa bits,
+ * two codes per byte, one E4M3 scale per 16 values, one FP32 global scale per
+ * tensor, 9 bytes per 16 values) but give no formula.  The formulas below are
+ * the plainest reading, stated once here and followed literally:
+ *
+ *   global g      = amax|x over the tensor| / (6 * 448)        (FP32 divide)
+ *   per 16-block  : amax_b; d = 6*g; sf = amax_b / d; sbyte = E4M3_RNE_sat(sf)
+ *                   S = E4M3 value of sbyte (exact); den = S*g
+ *   per element   : code = E2M1_RNE_sat(x / den); byte j = code[2j] | code[2j+1]<<4
+ *   zero cases    : g == 0 or den == 0  ->  scale byte 0x00 (g == 0) and codes 0x0
+ *   FP8 layers    : s8 = amax / 448; byte = E4M3_RNE_sat(x / s8); s8 == 0 -> 0x00
+ *
+ * Every FP32 step is one IEEE-754 binary32 operation with round-to-nearest-even
+ * and no fused multiply-add (build with -ffp-contract=off).  Attention runs in
+ * FP64 over values dequantized exactly.
+ *
+ * Parity pins (tests, not here): the E2M1 code table, brute-force nearest-value
+ * rounding over every FP32 bit pattern, the 9-byte ledger, exact round trips,
+ * brute-force dense attention and the split / log-sum-exp merge identity.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* E2M1 ([P1] 02, [P2] Core of the Ledger: 1 sign + 2 exponent + 1 mantissa). */
+/* Exponent bias 1; exponent field 0 is subnormal (0 or 0.5).                 */
+/* ------------------------------------------------------------------------ */
+
+double orc_e2m1_value(uint8_t code) {
+  int e = (code >> 1) & 3, m = code & 1;
+  double mag = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return (code & 8) ? -mag : mag;
+}
+
+/* Round to nearest E2M1 value, ties to the even code, saturating at 6.
+ * Magnitude grid 0, .5, 1, 1.5, 2, 3, 4, 6; the decision points are the
+ * midpoints between neighbours, and at a midpoint the even code wins. */
+uint8_t orc_e2m1_encode(float y) {
+  uint8_t sign = signbit(y) ? 8 : 0;
+  double a = fabs((double)y);
+  uint8_t mag;
+  if (isnan(y)) return 0; /* undefined; inputs are finite */
+  if (a <= 0.25) mag = 0;
+  else if (a < 0.75) mag = 1;
+  else if (a <= 1.25) mag = 2;
+  else if (a < 1.75) mag = 3;
+  else if (a <= 2.5) mag = 4;
+  else if (a < 3.5) mag = 5;
+  else if (a <= 5.0) mag = 6;
+  else mag = 7;
+  return sign | mag;
+}
+
+/* ------------------------------------------------------------------------ */
+/* E4M3, the OCP 8-bit "fn" variant ([P2] Core of the Ledger: "FP8 (E4M3)     */
+/* block-level scale"; [P1] 01: FP8 KV cache): bias 7, 3 mantissa bits,       */
+/* subnormals m*2^-9, no infinities, 0x7F/0xFF = NaN, largest finite 448.     */
+/* ------------------------------------------------------------------------ */
+
+double orc_e4m3_value(uint8_t b) {
+  int e = (b >> 3) & 15, m = b & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  v = (e == 0) ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+  return (b & 0x80) ? -v : v;
+}
+
+/* Round to nearest E4M3 value, ties to even mantissa; finite values above
+ * 448 and infinity saturate to 448 (sign kept). */
+uint8_t orc_e4m3_encode(float y) {
+  uint8_t sign = signbit(y) ? 0x80 : 0;
+  double a, quantum, n, v;
+  int ex, e, m;
+  if (isnan(y)) return sign | 0x7F;
+  a = fabs((double)y);
+  if (a > 448.0) return sign | 0x7E;
+  if (a < ldexp(1.0, -6)) {
+    quantum = ldexp(1.0, -9); /* subnormal spacing */
+  } else {
+    frexp(a, &ex);                   /* a in [2^(ex-1), 2^ex) */
+    quantum = ldexp(1.0, ex - 1 - 3); /* 3 mantissa bits */
+  }
+  n = nearbyint(a / quantum); /* exact quotient; default mode = ties-to-even */
+  v = n * quantum;
+  if (v == 0.0) return sign;
+  if (v < ldexp(1.0, -6)) return sign | (uint8_t)n;
+  frexp(v, &ex);
+  e = ex - 1 + 7;
+  m = (int)(v / ldexp(1.0, ex - 1) * 8.0) - 8;
+  return sign | (uint8_t)(e << 3) | (uint8_t)m;
+}
+
+/* Bulk forms over raw FP32 bit patterns, for exhaustive sweeps. */
+void orc_e2m1_encode_bits(uint32_t start, uint32_t count, uint8_t *out) {
+  uint32_t i;
+  for (i = 0; i < count; ++i) {
+    uint32_t u = start + i;
+    float f;
+    memcpy(&f, &u, 4);
+    out[i] = orc_e2m1_encode(f);
+  }
+}
+
+void orc_e4m3_encode_bits(uint32_t start, uint32_t count, uint8_t *out) {
+  uint32_t i;
+  for (i = 0; i < count; ++i) {
+    uint32_t u = start + i;
+    float f;
+    memcpy(&f, &u, 4);
+    out[i] = orc_e4m3_encode(f);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Global scale ([P2] Core of the Ledger: "the whole tensor gets one FP32     */
+/* global scale").  g = amax / divisor, divisor 2688 = 6*448 for NVFP4 and    */
+/* 448 for the FP8 per-tensor scale.                                          */
+/* ------------------------------------------------------------------------ */
+
+float orc_global_scale(const float *x, int64_t n, float divisor) {
+  float amax = 0.0f;
+  int64_t i;
+  for (i = 0; i < n; ++i) {
+    float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  return amax / divisor;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Quantizers                                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* One head vector x[D] -> D/2 code bytes and D/16 E4M3 scale bytes. */
+static void nvfp4_quantize_vector(const float *x, int D, float g, uint8_t *codes, uint8_t *scales) {
+  int b, i;
+  for (b = 0; b < D / 16; ++b) {
+    const float *blk = x + 16 * b;
+    uint8_t q[16];
+    float amax = 0.0f, d, sf, S, den;
+    uint8_t sbyte;
+    for (i = 0; i < 16; ++i) {
+      float a = fabsf(blk[i]);
+      if (a > amax) amax = a;
+    }
+    if (g == 0.0f) {
+      sbyte = 0;
+      den = 0.0f;
+    } else {
+      d = 6.0f * g;
+      sf = amax / d;
+      sbyte = orc_e4m3_encode(sf);
+      S = (float)orc_e4m3_value(sbyte);
+      den = S * g;
+    }
+    for (i = 0; i < 16; ++i) q[i] = (den == 0.0f) ? 0 : orc_e2m1_encode(blk[i] / den);
+    for (i = 0; i < 8; ++i) codes[8 * b + i] = (uint8_t)(q[2 * i] | (q[2 * i + 1] << 4));
+    scales[b] = sbyte;
+  }
+}
+
+static void fp8_quantize_vector(const float *x, int D, float s8, uint8_t *out) {
+  int i;
+  for (i = 0; i < D; ++i) out[i] = (s8 == 0.0f) ? 0 : orc_e4m3_encode(x[i] / s8);
+}
+
+/* Quantized write into paged slots ([P1] 02 "quantized write"; [P2] Three
+ * Paths: the current chunk "is quantized into the NVFP4 cache").
+ * k, v: [T][Hkv][D] FP32.  slot = page*P + offset; slot < 0 skips the token.
+ * Cache planes (head-major inside a page):
+ *   codes  [num_pages][Hkv][P][D/2],  scales [num_pages][Hkv][P][D/16].
+ * g[0], g[1] = global scales of K and V.  Returns 0, or -1 on a bad slot. */
+int orc_nvfp4_quantize_write(const float *k, const float *v, int64_t T, int Hkv, int D,
+                             const int64_t *slot_mapping, const float *g, int P, int64_t num_pages,
+                             uint8_t *k_codes, uint8_t *k_scales, uint8_t *v_codes, uint8_t *v_scales) {
+  int64_t t;
+  int h;
+  for (t = 0; t < T; ++t) {
+    int64_t slot = slot_mapping[t], page, off;
+    if (slot < 0) continue;
+    if (slot >= num_pages * P) return -1;
+    page = slot / P;
+    off = slot % P;
+    for (h = 0; h < Hkv; ++h) {
+      int64_t row = (page * Hkv + h) * P + off;
+      const int64_t src = (t * Hkv + h) * D;
+      nvfp4_quantize_vector(k + src, D, g[0], k_codes + row * (D / 2), k_scales + row * (D / 16));
+      nvfp4_quantize_vector(v + src, D, g[1], v_codes + row * (D / 2), v_scales + row * (D / 16));
+    }
+  }
+  return 0;
+}
+
+/* FP8 E4M3 write for the FP8 layers ([P1] 03: sensitive layers keep FP8):
+ * planes [num_pages][Hkv][P][D]; s8[0], s8[1] = per-tensor scales of K, V. */
+int orc_fp8_quantize_write(const float *k, const float *v, int64_t T, int Hkv, int D,
+                           const int64_t *slot_mapping, const float *s8, int P, int64_t num_pages,
+                           uint8_t *k_data, uint8_t *v_data) {
+  int64_t t;
+  int h;
+  for (t = 0; t < T; ++t) {
+    int64_t slot = slot_mapping[t], page, off;
+    if (slot < 0) continue;
+    if (slot >= num_pages * P) return -1;
+    page = slot / P;
+    off = slot % P;
+    for (h = 0; h < Hkv; ++h) {
+      int64_t row = (page * Hkv + h) * P + off;
+      const int64_t src = (t * Hkv + h) * D;
+      fp8_quantize_vector(k + src, D, s8[0], k_data + row * D);
+      fp8_quantize_vector(v + src, D, s8[1], v_data + row * D);
+    }
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dequantization of one cached head vector to FP64 (exact).                 */
+/* prec 0 = NVFP4: x = e2m1(code) * E4M3(scale) * g                           */
+/* prec 1 = FP8:   x = E4M3(byte) * s8                                        */
+/* ------------------------------------------------------------------------ */
+
+static void dequant_row(int prec, const uint8_t *data, const uint8_t *scales, int64_t row, int D, float g,
+                        double *out) {
+  int d;
+  if (prec == 0) {
+    const uint8_t *c = data + row * (D / 2);
+    const uint8_t *s = scales + row * (D / 16);
+    for (d = 0; d < D; ++d) {
+      uint8_t code = (d & 1) ? (uint8_t)(c[d / 2] >> 4) : (uint8_t)(c[d / 2] & 15);
+      out[d] = orc_e2m1_value(code) * orc_e4m3_value(s[d / 16]) * (double)g;
+    }
+  } else {
+    const uint8_t *c = data + row * D;
+    for (d = 0; d < D; ++d) out[d] = orc_e4m3_value(c[d]) * (double)g;
+  }
+}
+
+/* Dequantize tokens [0, L) of one (sequence, KV head) into dense [L][D]. */
+int orc_gather_dequant(int prec, const uint8_t *data, const uint8_t *scales, float g, const int32_t *block_row,
+                       int L, int Hkv, int h, int D, int P, int64_t num_pages, double *out) {
+  int t;
+  for (t = 0; t < L; ++t) {
+    int64_t page = block_row[t / P];
+    if (page < 0 || page >= num_pages) return -1;
+    dequant_row(prec, data, scales, (page * Hkv + h) * P + t % P, D, g, out + (int64_t)t * D);
+  }
+  return 0;
+}
+
+static double bf16_bits_to_double(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Paged GQA decode attention ([P2] Three Paths: decode reads the NVFP4 cache */
+/* directly).  Plain dense softmax in FP64 over the gathered tokens of each   */
+/* sequence; query head h reads KV head h / (Hq/Hkv); every token in [0, L)   */
+/* is visible; L == 0 gives zeros.                                            */
+/*   q   [B][Hq][D] BF16 bits;  out [B][Hq][D] FP64.                          */
+/*   num_splits <= 1: one softmax over all L tokens.  num_splits > 1: the L   */
+/*   tokens are cut into num_splits equal contiguous ranges (the last ones    */
+/*   may be empty), each range gives (o_k = sum p v, m_k, l_k) and the ranges */
+/*   are merged with the log-sum-exp rule M = max m_k,                        */
+/*   out = sum e^(m_k - M) o_k / sum e^(m_k - M) l_k.                         */
+/* ------------------------------------------------------------------------ */
+int orc_paged_decode_attention(const uint16_t *q, int B, int Hq, int Hkv, int D, int P, int prec,
+                               const uint8_t *k_data, const uint8_t *k_scales, const uint8_t *v_data,
+                               const uint8_t *v_scales, const float *g, const int32_t *block_table,
+                               int max_pages, const int32_t *seq_lens, int64_t num_pages, double sm_scale,
+                               int num_splits, double *out) {
+  int b, h, G = Hq / Hkv;
+  int rc = 0;
+  for (b = 0; b < B && rc == 0; ++b) {
+    int L = seq_lens[b];
+    for (h = 0; h < Hkv && rc == 0; ++h) {
+      double *K, *V, *s;
+      int j;
+      if (L <= 0) {
+        for (j = 0; j < G; ++j) memset(out + ((int64_t)b * Hq + h * G + j) * D, 0, sizeof(double) * D);
+        continue;
+      }
+      if ((L + P - 1) / P > max_pages) return -1;
+      K = (double *)malloc(sizeof(double) * (size_t)L * D);
+      V = (double *)malloc(sizeof(double) * (size_t)L * D);
+      s = (double *)malloc(sizeof(double) * (size_t)L);
+      rc |= orc_gather_dequant(prec, k_data, k_scales, g[0], block_table + (int64_t)b * max_pages, L, Hkv, h, D, P,
+                               num_pages, K);
+      rc |= orc_gather_dequant(prec, v_data, v_scales, g[1], block_table + (int64_t)b * max_pages, L, Hkv, h, D, P,
+                               num_pages, V);
+      for (j = 0; j < G && rc == 0; ++j) {
+        int qh = h * G + j, t, d, nsp = num_splits > 1 ? num_splits : 1, sp;
+        const uint16_t *qv = q + ((int64_t)b * Hq + qh) * D;
+        double *o = out + ((int64_t)b * Hq + qh) * D;
+        double M = -INFINITY, lsum = 0.0;
+        double *ms = (double *)malloc(sizeof(double) * nsp), *ls = (double *)malloc(sizeof(double) * nsp);
+        double *os = (double *)calloc((size_t)nsp * D, sizeof(double));
+        for (t = 0; t < L; ++t) {
+          double acc = 0.0;
+          for (d = 0; d < D; ++d) acc += bf16_bits_to_double(qv[d]) * K[(int64_t)t * D + d];
+          s[t] = acc * sm_scale;
+        }
+        for (sp = 0; sp < nsp; ++sp) {
+          int chunk = (L + nsp - 1) / nsp, t0 = sp * chunk, t1 = t0 + chunk < L ? t0 + chunk : L;
+          double m = -INFINITY, l = 0.0;
+          for (t = t0; t < t1; ++t)
+            if (s[t] > m) m = s[t];
+          for (t = t0; t < t1; ++t) {
+            double p = exp(s[t] - m);
+            l += p;
+            for (d = 0; d < D; ++d) os[(int64_t)sp * D + d] += p * V[(int64_t)t * D + d];
+          }
+          ms[sp] = m;
+          ls[sp] = l;
+          if (m > M) M = m;
+        }
+        for (d = 0; d < D; ++d) o[d] = 0.0;
+        for (sp = 0; sp < nsp; ++sp) {
+          double w;
+          if (ls[sp] == 0.0) continue; /* empty range */
+          w = exp(ms[sp] - M);
+          lsum += w * ls[sp];
+          for (d = 0; d < D; ++d) o[d] += w * os[(int64_t)sp * D + d];
+        }
+        for (d = 0; d < D; ++d) o[d] /= lsum;
+        free(ms);
+        free(ls);
+        free(os);
+      }
+      free(K);
+      free(V);
+      free(s);
+    }
+  }
+  return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Chunked-extend dequant into the shared FP8 workspace ([P2] Three Paths:    */
+/* "the cached prefix is gathered out and dequantized into a cross-layer      */
+/* shared FP8 workspace").  For sequence seq_ids[i], tokens [0, prefix_lens[i]) */
+/* go to workspace rows cu_prefix[i] + t, layout [rows][Hkv][D] E4M3:          */
+/*   w = e2m1(code) * S       (exact in FP32)                                 */
+/*   r = g / ws_scale         (FP32 divide, once per K and V)                  */
+/*   byte = E4M3_RNE_sat(w * r)                                               */
+/* ------------------------------------------------------------------------ */
+int orc_dequant_to_fp8_workspace(const int32_t *block_table, int max_pages, const int32_t *seq_ids,
+                                 const int32_t *prefix_lens, const int64_t *cu_prefix, int n, int Hkv, int D,
+                                 int P, int64_t num_pages, const uint8_t *k_codes, const uint8_t *k_scales,
+                                 const uint8_t *v_codes, const uint8_t *v_scales, const float *g,
+                                 const float *ws_scale, uint8_t *ws_k, uint8_t *ws_v) {
+  int i, pass;
+  for (pass = 0; pass < 2; ++pass) {
+    const uint8_t *codes = pass ? v_codes : k_codes;
+    const uint8_t *scales = pass ? v_scales : k_scales;
+    uint8_t *ws = pass ? ws_v : ws_k;
+    float r;
+    if (!(ws_scale[pass] > 0.0f)) return -1;
+    r = g[pass] / ws_scale[pass];
+    for (i = 0; i < n; ++i) {
+      const int32_t *brow = block_table + (int64_t)seq_ids[i] * max_pages;
+      int t, h, d;
+      for (t = 0; t < prefix_lens[i]; ++t) {
+        int64_t page = brow[t / P];
+        if (page < 0 || page >= num_pages) return -1;
+        for (h = 0; h < Hkv; ++h) {
+          int64_t row = (page * Hkv + h) * P + t % P;
+          const uint8_t *c = codes + row * (D / 2);
+          const uint8_t *s = scales + row * (D / 16);
+          uint8_t *dst = ws + ((cu_prefix[i] + t) * Hkv + h) * D;
+          for (d = 0; d < D; ++d) {
+            uint8_t code = (d & 1) ? (uint8_t)(c[d / 2] >> 4) : (uint8_t)(c[d / 2] & 15);
+            float w = (float)(orc_e2m1_value(code) * orc_e4m3_value(s[d / 16]));
+            dst[d] = orc_e4m3_encode(w * r);
+          }
+        }
+      }
+    }
+  }
+  return 0;
+}
