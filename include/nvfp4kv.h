@@ -1,0 +1,198 @@
+/*
+ * nvfp4kv: NVFP4 (and FP8 E4M3) paged KV cache for LLM decode on one GB300
+ * (sm_103a).  C ABI: plain pointers and sizes; no framework types.
+ *
+ * Sources (page title, section):
+ *   [P1] "SOAR Weekly Champion Notes 05 | Zhisuan Team One: NVFP4 KV Cache and
+ *        Mixed-Precision Practice": 02 NVFP4 KV Cache (E2M1 = 1 sign + 2
+ *        exponent + 1 mantissa bit, two values per byte, quantized write and
+ *        dequantized read paths, FP4 memory pool); 03 Mixed-precision KV
+ *        Cache (FP8 for the sensitive first/last layers, NVFP4 elsewhere).
+ *   [P2] "SGLang x Qwen x NVIDIA Collaboration: NVFP4 KV Cache Breaks
+ *        Long-Context and Agentic Inference Bottlenecks": The Core of the
+ *        Ledger (one E4M3 block scale per 16 values, one FP32 global scale per
+ *        tensor, 9 bytes per 16 values); Three Paths (decode reads NVFP4 from
+ *        the paged cache and dequantizes inside the kernel; chunked extend
+ *        dequantizes the cached prefix into a shared FP8 workspace and
+ *        quantizes the new chunk into the cache).
+ *
+ * Number formats.  E2M1 codes: magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6, bit 3 =
+ * sign; byte j of a row holds element 2j in its low nibble and 2j+1 in its
+ * high nibble.  E4M3: the OCP "fn" byte (bias 7, largest finite 448).
+ *
+ * Quantizer (FP32, IEEE round-to-nearest-even, no fused multiply-add):
+ *   g     = amax(|x|) / 2688                    per tensor (K and V separately)
+ *   sbyte = E4M3_rne_satfinite(amax16 / (6*g))  per 16 consecutive head_dim values
+ *   code  = E2M1_rne_satfinite(x / (E4M3(sbyte) * g))
+ *   g == 0 -> scale byte 0 and codes 0; a block whose E4M3(sbyte)*g is 0 has
+ *   codes 0.  FP8 layers: s8 = amax / 448, byte = E4M3_rne_satfinite(x / s8),
+ *   s8 == 0 -> byte 0.
+ *
+ * Cache layout (one layer; every pointer is device memory owned by the caller):
+ *   NVFP4: k_data, v_data   [num_pages][num_kv_heads][page_size][head_dim/2]
+ *          k_scale, v_scale [num_pages][num_kv_heads][page_size][head_dim/16]
+ *   FP8:   k_data, v_data   [num_pages][num_kv_heads][page_size][head_dim]
+ *   A token at slot s lives at page s / page_size, offset s % page_size.
+ *   Supported: head_dim 128; page_size 16, 32, 64 or 128; every pointer
+ *   16-byte aligned.  Anything else -> NVKV_ERR_UNSUPPORTED.
+ *
+ * Conventions.  Every call is asynchronous on `stream` (a cudaStream_t, NULL
+ * = the legacy default stream) and returns after launching.  Argument errors
+ * are found on the host before any launch (nothing is written).  Launch
+ * failures return NVKV_ERR_CUDA.  Out-of-range device-side indices (a slot,
+ * a block-table entry, a sequence longer than its block-table row) never fault:
+ * the element is skipped or clamped and a nonzero code is stored into
+ * cache->err_flag when that pointer is non-NULL.  The library allocates no
+ * memory; scratch comes from the caller's workspace.  Calls on the same
+ * stream are ordered; calls that share a workspace must not overlap.
+ */
+#ifndef NVFP4KV_H
+#define NVFP4KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NVKV_OK = 0,
+  NVKV_ERR_INVALID_ARG = 1,
+  NVKV_ERR_UNSUPPORTED = 2,
+  NVKV_ERR_CUDA = 3,
+  NVKV_ERR_WORKSPACE_TOO_SMALL = 4
+} nvkv_status;
+
+typedef enum { NVKV_PREC_NVFP4 = 0, NVKV_PREC_FP8_E4M3 = 1 } nvkv_precision;
+
+typedef enum { NVKV_DTYPE_F32 = 0, NVKV_DTYPE_BF16 = 1 } nvkv_dtype;
+
+/* Device error codes written to cache->err_flag (first one wins). */
+#define NVKV_DEVERR_SLOT 1       /* slot >= num_pages * page_size            */
+#define NVKV_DEVERR_PAGE 2       /* block-table entry outside [0, num_pages) */
+#define NVKV_DEVERR_SEQLEN 3     /* seq_len > max_pages * page_size or < 0   */
+#define NVKV_DEVERR_TIMEOUT 4    /* a bounded wait inside a kernel ran out   */
+#define NVKV_DEVERR_WS_ROWS 5    /* workspace rows smaller than the prefixes */
+
+/* One layer's cache.  The struct itself is host memory read during the call. */
+typedef struct {
+  int32_t prec;                /* nvkv_precision                               */
+  int32_t num_pages;
+  int32_t page_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t reserved;
+  uint8_t *k_data, *v_data;    /* codes (NVFP4) or E4M3 bytes (FP8)            */
+  uint8_t *k_scale, *v_scale;  /* E4M3 block scales (NVFP4); NULL for FP8      */
+  const float *kv_scale;       /* device float[2] {K, V}: NVFP4 global g, FP8 s8 */
+  int32_t *err_flag;           /* optional device int32, 0 = no error          */
+} nvkv_cache;
+
+/* Readable name of a status. */
+const char *nvkv_status_string(nvkv_status s);
+
+/* Global scale of one tensor ([P2] The Core of the Ledger: "the whole tensor
+ * gets one FP32 global scale"): out[0] = max|x[i]| / divisor, FP32 divide.
+ * divisor 2688 (= 6 * 448) gives the NVFP4 g, 448 the FP8 s8.  x: n values of
+ * `dtype`, device.  out: device float.  n == 0 gives 0.  Three stream operations
+ * (a memset and two kernels). */
+nvkv_status nvkv_global_scale(const void *x, nvkv_dtype dtype, int64_t n, float divisor, float *out,
+                              void *stream);
+
+/* Running maximum for a global scale computed over a tensor stored in pieces:
+ * amax[0] = max(amax[0], max|x[i]|).  amax: device float, >= 0, set to 0 by
+ * the caller before the first piece; the global scale is then
+ * nvkv_global_scale(amax, F32, 1, divisor, out) (division is monotonic, so
+ * this equals the scale of the whole tensor). */
+nvkv_status nvkv_amax_update(const void *x, nvkv_dtype dtype, int64_t n, float *amax, void *stream);
+
+/* NVFP4 quantized write into paged slots ([P1] 02 "quantized write"; [P2] Three
+ * Paths: new KV "is quantized into the NVFP4 cache").
+ *   k, v          [num_tokens][num_kv_heads][head_dim] of `dtype` (BF16 widens exactly)
+ *   slot_mapping  [num_tokens] int64 device; a negative slot skips the token
+ *   global_scale  device float[2] {g_K, g_V}; NULL -> cache->kv_scale
+ *   cache         prec must be NVKV_PREC_NVFP4
+ * Bytes are identical to the quantizer stated at the top of this file. */
+nvkv_status nvfp4_kv_quantize_write(const void *k, const void *v, nvkv_dtype dtype, int64_t num_tokens,
+                                    const int64_t *slot_mapping, const float *global_scale,
+                                    const nvkv_cache *cache, void *stream);
+
+/* FP8 E4M3 write for the FP8 layers ([P1] 03: sensitive layers keep an FP8 KV
+ * cache).  Same arguments; global_scale = per-tensor {s8_K, s8_V}; cache->prec
+ * must be NVKV_PREC_FP8_E4M3. */
+nvkv_status fp8_kv_quantize_write(const void *k, const void *v, nvkv_dtype dtype, int64_t num_tokens,
+                                  const int64_t *slot_mapping, const float *global_scale,
+                                  const nvkv_cache *cache, void *stream);
+
+/* Bytes of decode workspace for this problem size: num_splits > 0 as passed to
+ * the decode call, 0 for the library's choice on the current device.  The
+ * workspace must be zero-filled once before its first use (for example with
+ * nvkv_decode_workspace_init); every completed decode call leaves its counters
+ * at zero again.  Returns 0 for unsupported sizes. */
+size_t nvkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t num_splits);
+
+/* Zero `bytes` of workspace on `stream` (a cudaMemsetAsync). */
+nvkv_status nvkv_decode_workspace_init(void *workspace, size_t bytes, void *stream);
+
+/* Paged GQA decode attention over the NVFP4 or FP8 cache ([P2] Three Paths:
+ * decode "reads NVFP4 directly and dequantizes on the fly"; [P1] 03 per-layer
+ * precision).
+ *   q               [batch][num_q_heads][head_dim] BF16, device
+ *   block_table     [batch][max_pages] int32 page ids, device
+ *   seq_lens        [batch] int32 visible tokens per sequence (the token written
+ *                   in this step included), device; 0 gives a zero output row
+ *   layer_precision must equal cache->prec (else NVKV_ERR_INVALID_ARG)
+ *   sm_scale        softmax scale; 0 -> 1/sqrt(head_dim)
+ *   num_splits      0: balance the work over the GPU (split-KV wherever it
+ *                   helps); > 0: cut every sequence into that many partitions
+ *                   (exactly so when all sequences have equal length)
+ *   workspace       scratch of nvkv_decode_workspace_size(...) bytes, device
+ *   out             [batch][num_q_heads][head_dim] BF16, device
+ * Query head h reads KV head h / (num_q_heads / num_kv_heads); every token in
+ * [0, seq_len) is visible.  out = softmax(q k^T * sm_scale) v with the FP32
+ * result rounded to BF16.  Split partitions are merged with the log-sum-exp
+ * rule inside the same kernel.  Requires num_q_heads / num_kv_heads <= 8 and
+ * batch <= 1024. */
+nvkv_status nvfp4_paged_decode_attention(const void *q, const nvkv_cache *cache, const int32_t *block_table,
+                                         int32_t max_pages, const int32_t *seq_lens, int32_t batch,
+                                         int32_t num_q_heads, int32_t layer_precision, float sm_scale,
+                                         int32_t num_splits, void *workspace, size_t workspace_bytes, void *out,
+                                         void *stream);
+
+/* The FP8 E4M3 variant: the same call for a cache with prec == NVKV_PREC_FP8_E4M3. */
+nvkv_status fp8_paged_decode_attention(const void *q, const nvkv_cache *cache, const int32_t *block_table,
+                                       int32_t max_pages, const int32_t *seq_lens, int32_t batch,
+                                       int32_t num_q_heads, float sm_scale, int32_t num_splits, void *workspace,
+                                       size_t workspace_bytes, void *out, void *stream);
+
+/* Chunked-extend prefix dequant into the shared FP8 workspace ([P2] Three
+ * Paths: "the cached prefix is gathered out and dequantized into a cross-layer
+ * shared FP8 workspace").  For i < n, tokens [0, prefix_lens[i]) of sequence
+ * seq_ids[i] land in rows cu_prefix[i] + t of ws_k / ws_v, layout
+ * [rows][num_kv_heads][head_dim] E4M3:
+ *   byte = E4M3_rne_satfinite((e2m1 * S) * (g / ws_scale))   (FP32, per K and V)
+ *   seq_ids, prefix_lens  [n] int32 device; cu_prefix [n+1] int64 device
+ *                         exclusive prefix sums of prefix_lens
+ *   ws_scale              device float[2] {K, V}, > 0 (e.g. 6 * g)
+ *   ws_rows               rows allocated in ws_k and ws_v (host value); rows
+ *                         past it are skipped and NVKV_DEVERR_WS_ROWS raised
+ * cache->prec must be NVKV_PREC_NVFP4. */
+nvkv_status nvfp4_kv_dequant_to_fp8_workspace(const int32_t *block_table, int32_t max_pages,
+                                              const int32_t *seq_ids, const int32_t *prefix_lens,
+                                              const int64_t *cu_prefix, int32_t n, const nvkv_cache *cache,
+                                              const float *ws_scale, uint8_t *ws_k, uint8_t *ws_v,
+                                              int64_t ws_rows, void *stream);
+
+/* Element encoders of the quantizer, one output byte per FP32 input: E2M1
+ * code (low nibble, round-to-nearest-even, saturating at 6) and E4M3 byte
+ * (round-to-nearest-even, saturating at 448).  x, out: device. */
+nvkv_status nvkv_encode_e2m1(const float *x, int64_t n, uint8_t *out, void *stream);
+nvkv_status nvkv_encode_e4m3(const float *x, int64_t n, uint8_t *out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4KV_H */

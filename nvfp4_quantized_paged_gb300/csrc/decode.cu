@@ -1,0 +1,798 @@
+// Paged GQA decode attention reading the NVFP4 (or FP8 E4M3) cache straight
+// from HBM ("SGLang x Qwen x NVIDIA ...", Three Paths: decode is memory-bound,
+// so the kernel reads NVFP4 directly and dequantizes on the fly; it must read
+// exactly as much as it computes).  The per-layer FP8 variant serves the
+// sensitive layers ("SOAR Weekly Champion Notes 05", 03).
+//
+// Design (sm_103a, one GPU):
+//   * Work unit = one 64-token tile of one (sequence, KV head).  The units of
+//     the whole batch are laid end to end and cut into equal contiguous shares,
+//     one per CTA of a persistent grid (about SMs x resident CTAs), so every
+//     CTA streams the same number of bytes whatever the sequence lengths.  A
+//     (sequence, KV head) cut between CTAs yields split-KV partials that the
+//     last-arriving CTA merges with the log-sum-exp rule (no second kernel,
+//     no spin: an atomic arrival counter).
+//   * One producer warp streams tiles into a shared-memory ring with 1-D bulk
+//     copies (cp.async.bulk + mbarrier transaction counts): per page run, the
+//     K codes, K scales, V codes and V scales planes (NVFP4: 144 B per token
+//     and KV head) or the two E4M3 planes (FP8: 256 B).  An L2 evict-first
+//     hint keeps the streamed cache from flushing reused data.
+//   * Four consumer warps each own whole tiles.  E2M1 pairs become f16x2 with
+//     one cvt.rn.f16x2.e2m1x2 and are scaled by their E4M3 block scale with
+//     one f16x2 multiply; code * scale has at most 6 significant bits and lies
+//     in [2^-10, 2688], so it is exact in FP16.  Scores and P.V run on the
+//     tensor cores as m16n8k16 FP16 MMAs with FP32 accumulation: tokens form
+//     M, the GQA query group (<= 8 heads) forms N.  The global scale g_K,
+//     sm_scale, log2(e) and a per-head power of two that brings the BF16
+//     query into FP16 range are folded into one FP32 factor per score; g_V is
+//     applied once to the output.  Online softmax in FP32 with exp2 and a
+//     lazily raised running max (rescale only when the max grows by > 2^8).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "nvkv_device.cuh"
+#include "nvkv_host.h"
+
+namespace nvkv {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kTile = 64;          // tokens per work unit / ring stage
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxBatch = 1024;    // sequences per call (prefix sums live in shared memory)
+constexpr int kMaxGroup = 8;       // query heads per KV head (MMA N)
+constexpr int kSlotFloats = kMaxGroup * kD + 2 * kMaxGroup;  // one partial (o, m, l)
+constexpr float kRescaleThreshold = 8.0f;                   // log2 units
+
+template <int PREC>
+struct Layout;
+template <>
+struct Layout<NVKV_PREC_NVFP4> {
+  static constexpr int kRowBytes = kD / 2;
+  static constexpr int kKc = 0;
+  static constexpr int kKs = kKc + kTile * kRowBytes;
+  static constexpr int kVc = kKs + kTile * (kD / 16);
+  static constexpr int kVs = kVc + kTile * kRowBytes;
+  static constexpr int kStageBytes = kVs + kTile * (kD / 16);  // 9216
+  static constexpr int kStages = 6;
+  static constexpr int kMinBlocks = 3;
+};
+template <>
+struct Layout<NVKV_PREC_FP8_E4M3> {
+  static constexpr int kRowBytes = kD;
+  static constexpr int kKc = 0;
+  static constexpr int kVc = kTile * kRowBytes;
+  static constexpr int kStageBytes = 2 * kTile * kRowBytes;  // 16384
+  static constexpr int kStages = 6;
+  static constexpr int kMinBlocks = 2;
+};
+
+struct DecodeArgs {
+  const __nv_bfloat16 *q;
+  CacheDev c;
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  int32_t max_pages;
+  int32_t B, Hq, G;
+  float sm_scale;
+  int32_t num_ctas;
+  int32_t *counters;  // [B * Hkv]
+  float *partials;    // [num_ctas][2][kSlotFloats]
+  __nv_bfloat16 *out;
+};
+
+template <int PREC>
+constexpr int smem_bytes_for(int G) {
+  return Layout<PREC>::kStages * Layout<PREC>::kStageBytes  // ring
+         + 2 * Layout<PREC>::kStages * 8                       // full/empty barriers
+         + (kMaxBatch + 1) * 4                                 // tile prefix sums
+         + kConsumerWarps * G * kD * 4                         // warp merge: o
+         + kConsumerWarps * kMaxGroup * 2 * 4                  // warp merge: m, l
+         + 64;                                                 // flags
+}
+
+// Segment = run of consecutive units of one (sequence, KV head).
+struct Seg {
+  int b, h, t0, t1;  // tiles [t0, t1) of (b, h)
+};
+
+// cum[b] = tiles of sequences before b; units before sequence b = Hkv * cum[b].
+__device__ __forceinline__ Seg seg_at(int64_t u, int64_t u_end, const int32_t *cum, int B, int Hkv) {
+  int lo = 0, hi = B - 1;  // last b with Hkv*cum[b] <= u (sequences without tiles are skipped)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<int64_t>(cum[mid]) * Hkv <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  const int nb = cum[lo + 1] - cum[lo];
+  const int64_t r = u - static_cast<int64_t>(cum[lo]) * Hkv;
+  Seg s;
+  s.b = lo;
+  s.h = static_cast<int>(r / nb);
+  s.t0 = static_cast<int>(r % nb);
+  const int64_t left = u_end - u;
+  s.t1 = static_cast<int>(left < nb - s.t0 ? s.t0 + left : nb);
+  return s;
+}
+
+// Shares: CTA c owns units [floor(c W / NC), floor((c+1) W / NC)); with W >= NC
+// every share is non-empty.  owner_of(u) = the CTA whose share holds unit u.
+__device__ __forceinline__ int64_t share_begin(int64_t c, int64_t W, int64_t NC) { return c * W / NC; }
+__device__ __forceinline__ int64_t owner_of(int64_t u, int64_t W, int64_t NC) {
+  return ((u + 1) * NC + W - 1) / W - 1;
+}
+
+__device__ __forceinline__ int clamped_len(const DecodeArgs &a, int b) {
+  const int64_t cap = static_cast<int64_t>(a.max_pages) * a.c.P;
+  const int64_t L = a.seq_lens[b];
+  return static_cast<int>(L < 0 ? 0 : (L > cap ? cap : L));
+}
+
+// ---------------------------------------------------------------------------
+// Producer warp: bulk copies of the tiles of this CTA's share into the ring.
+// Lane j*nplanes + plane copies plane `plane` of page run j of the tile.
+// ---------------------------------------------------------------------------
+template <int PREC>
+__device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uint64_t *empty, const int32_t *cum,
+                         int64_t u0, int64_t u1, volatile int *abort, int *fills) {
+  using Lay = Layout<PREC>;
+  const int lane = threadIdx.x & 31;
+  const int Hkv = a.c.Hkv, P = a.c.P;
+  const uint64_t policy = policy_evict_first();
+  constexpr int nplanes = (PREC == NVKV_PREC_NVFP4) ? 4 : 2;
+  constexpr uint32_t bytes_per_tok = (PREC == NVKV_PREC_NVFP4) ? 144u : 256u;
+  const int run = P < kTile ? P : kTile;  // tokens per copy
+  int64_t i = 0;                          // stage counter
+  for (int64_t u = u0; u < u1;) {
+    const Seg s = seg_at(u, u1, cum, a.B, Hkv);
+    const int len = clamped_len(a, s.b);
+    const int32_t *brow = a.block_table + static_cast<int64_t>(s.b) * a.max_pages;
+    for (int t = s.t0; t < s.t1; ++t, ++i) {
+      const int slot = static_cast<int>(i % Lay::kStages);
+      const uint32_t fill = static_cast<uint32_t>(i / Lay::kStages);
+      if (*abort) return;
+      if (lane == 0 && fill > 0) mbar_wait_bounded(&empty[slot], (fill - 1) & 1u, abort);
+      __syncwarp();
+      if (*abort) return;
+      const int tok0 = t * kTile;
+      const int ntok = min(kTile, len - tok0);
+      const int nrun = (ntok + run - 1) / run;
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nrun * run) * bytes_per_tok);
+      __syncwarp();
+      if (lane < nrun * nplanes) {
+        const int j = lane / nplanes, plane = lane % nplanes;
+        const int tok = tok0 + j * run;
+        int64_t page = brow[tok / P];
+        if (page < 0 || page >= a.c.num_pages) {
+          set_err(a.c.err, NVKV_DEVERR_PAGE);
+          page = 0;  // a valid address; the output of this sequence is then undefined
+        }
+        const int64_t row = (page * Hkv + s.h) * P + tok % P;
+        uint8_t *stage = ring + static_cast<size_t>(slot) * Lay::kStageBytes;
+        if constexpr (PREC == NVKV_PREC_NVFP4) {
+          const uint8_t *src;
+          uint8_t *dst;
+          uint32_t nb;
+          if (plane == 0) {
+            src = a.c.kd + row * (kD / 2); dst = stage + Lay::kKc + j * run * (kD / 2); nb = run * (kD / 2);
+          } else if (plane == 1) {
+            src = a.c.ks + row * (kD / 16); dst = stage + Lay::kKs + j * run * (kD / 16); nb = run * (kD / 16);
+          } else if (plane == 2) {
+            src = a.c.vd + row * (kD / 2); dst = stage + Lay::kVc + j * run * (kD / 2); nb = run * (kD / 2);
+          } else {
+            src = a.c.vs + row * (kD / 16); dst = stage + Lay::kVs + j * run * (kD / 16); nb = run * (kD / 16);
+          }
+          bulk_g2s(dst, src, nb, &full[slot], policy);
+        } else {
+          const uint8_t *src = (plane == 0 ? a.c.kd : a.c.vd) + row * kD;
+          uint8_t *dst = stage + (plane == 0 ? Lay::kKc : Lay::kVc) + j * run * kD;
+          bulk_g2s(dst, src, static_cast<uint32_t>(run * kD), &full[slot], policy);
+        }
+      }
+      if (lane == 0) fills[slot] = static_cast<int>(fill) + 1;
+    }
+    u += s.t1 - s.t0;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Consumer warps.  Lane = 4r + c.  Scores: MMA rows = tokens 16k + r, 16k + r + 8
+// of sub-tile k; head_dim order inside one MMA k-step s is permuted so that a
+// thread reads 16 contiguous code bytes (d in [32c, 32c+32), step s covers
+// d = 32c + 4s + {0,1,2,3}); the query fragment uses the same order.  P.V:
+// MMA rows = head_dim (thread r owns block r: d in [16r, 16r+16)), k = tokens
+// 16k + {2c, 2c+1, 2c+8, 2c+9}, n = query head.  O for heads 2c, 2c+1 of the
+// group and d in [16r, 16r+16) stays in 32 FP32 registers.
+// ---------------------------------------------------------------------------
+struct WarpState {
+  float o[8][4];
+  float m[2];
+  float l[2];
+};
+
+template <int PREC>
+__device__ __forceinline__ void qk_subtile(const uint8_t *stage, int k, int r, int c, const uint32_t (&qf)[8][2],
+                                           float (&acc)[4]) {
+  using Lay = Layout<PREC>;
+  acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
+  const int row0 = 16 * k + r, row1 = row0 + 8;
+  if constexpr (PREC == NVKV_PREC_NVFP4) {
+    const uint4 c0 = *reinterpret_cast<const uint4 *>(stage + Lay::kKc + row0 * Lay::kRowBytes + 16 * c);
+    const uint4 c1 = *reinterpret_cast<const uint4 *>(stage + Lay::kKc + row1 * Lay::kRowBytes + 16 * c);
+    const uint32_t s0 = *reinterpret_cast<const uint16_t *>(stage + Lay::kKs + row0 * 8 + 2 * c);
+    const uint32_t s1 = *reinterpret_cast<const uint16_t *>(stage + Lay::kKs + row1 * 8 + 2 * c);
+    const uint32_t sc0 = f16x2_from_e4m3x2<0>(s0), sc1 = f16x2_from_e4m3x2<0>(s1);
+    const uint32_t lo0 = prmt(sc0, 0, 0x1010), hi0 = prmt(sc0, 0, 0x3232);  // {S_2c,S_2c}, {S_2c+1,S_2c+1}
+    const uint32_t lo1 = prmt(sc1, 0, 0x1010), hi1 = prmt(sc1, 0, 0x3232);
+    const uint32_t w0[4] = {c0.x, c0.y, c0.z, c0.w};
+    const uint32_t w1[4] = {c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const uint32_t m0 = s < 4 ? lo0 : hi0, m1 = s < 4 ? lo1 : hi1;
+      uint32_t a0, a1, a2, a3;
+      if ((s & 1) == 0) {
+        a0 = f16x2_from_e2m1x2<0>(w0[s >> 1]);
+        a2 = f16x2_from_e2m1x2<1>(w0[s >> 1]);
+        a1 = f16x2_from_e2m1x2<0>(w1[s >> 1]);
+        a3 = f16x2_from_e2m1x2<1>(w1[s >> 1]);
+      } else {
+        a0 = f16x2_from_e2m1x2<2>(w0[s >> 1]);
+        a2 = f16x2_from_e2m1x2<3>(w0[s >> 1]);
+        a1 = f16x2_from_e2m1x2<2>(w1[s >> 1]);
+        a3 = f16x2_from_e2m1x2<3>(w1[s >> 1]);
+      }
+      mma_f16_16816(acc, hmul2_u32(a0, m0), hmul2_u32(a1, m1), hmul2_u32(a2, m0), hmul2_u32(a3, m1), qf[s][0],
+                    qf[s][1]);
+    }
+  } else {
+    const uint4 *p0 = reinterpret_cast<const uint4 *>(stage + Lay::kKc + row0 * Lay::kRowBytes + 32 * c);
+    const uint4 *p1 = reinterpret_cast<const uint4 *>(stage + Lay::kKc + row1 * Lay::kRowBytes + 32 * c);
+    const uint4 x0 = p0[0], y0 = p0[1], x1 = p1[0], y1 = p1[1];
+    const uint32_t w0[8] = {x0.x, x0.y, x0.z, x0.w, y0.x, y0.y, y0.z, y0.w};
+    const uint32_t w1[8] = {x1.x, x1.y, x1.z, x1.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      mma_f16_16816(acc, f16x2_from_e4m3x2<0>(w0[s]), f16x2_from_e4m3x2<0>(w1[s]), f16x2_from_e4m3x2<1>(w0[s]),
+                    f16x2_from_e4m3x2<1>(w1[s]), qf[s][0], qf[s][1]);
+    }
+  }
+}
+
+template <int I>
+__device__ __forceinline__ void pv_mma_nvfp4(float (&o)[4], uint32_t xAB, uint32_t yAB, uint32_t xCD, uint32_t yCD,
+                                             uint32_t sAB, uint32_t sCD, uint32_t b0, uint32_t b1) {
+  mma_f16_16816(o, hmul2_u32(f16x2_from_e2m1x2<I>(xAB), sAB), hmul2_u32(f16x2_from_e2m1x2<I>(yAB), sAB),
+                hmul2_u32(f16x2_from_e2m1x2<I>(xCD), sCD), hmul2_u32(f16x2_from_e2m1x2<I>(yCD), sCD), b0, b1);
+}
+
+template <int PREC>
+__device__ __forceinline__ void pv_subtile(const uint8_t *stage, int k, int r, int c, int nvalid, uint32_t b0,
+                                           uint32_t b1, WarpState &st) {
+  using Lay = Layout<PREC>;
+  const int tA = 16 * k + 2 * c, tB = tA + 1, tC = tA + 8, tD = tA + 9;
+  if constexpr (PREC == NVKV_PREC_NVFP4) {
+    const uint2 vA = *reinterpret_cast<const uint2 *>(stage + Lay::kVc + tA * Lay::kRowBytes + 8 * r);
+    const uint2 vB = *reinterpret_cast<const uint2 *>(stage + Lay::kVc + tB * Lay::kRowBytes + 8 * r);
+    const uint2 vC = *reinterpret_cast<const uint2 *>(stage + Lay::kVc + tC * Lay::kRowBytes + 8 * r);
+    const uint2 vD = *reinterpret_cast<const uint2 *>(stage + Lay::kVc + tD * Lay::kRowBytes + 8 * r);
+    const uint8_t *vs = stage + Lay::kVs;
+    uint32_t sA = vs[tA * 8 + r], sB = vs[tB * 8 + r], sC = vs[tC * 8 + r], sD = vs[tD * 8 + r];
+    if (nvalid < kTile) {  // masked tokens get scale 0 -> value 0 (codes are finite)
+      if (tA >= nvalid) sA = 0;
+      if (tB >= nvalid) sB = 0;
+      if (tC >= nvalid) sC = 0;
+      if (tD >= nvalid) sD = 0;
+    }
+    const uint32_t sAB = f16x2_from_e4m3x2<0>(sA | (sB << 8));
+    const uint32_t sCD = f16x2_from_e4m3x2<0>(sC | (sD << 8));
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const uint32_t a = w ? vA.y : vA.x, bb = w ? vB.y : vB.x, cc = w ? vC.y : vC.x, dd = w ? vD.y : vD.x;
+      // byte j of x: token pair's low nibbles (d = 16r + 2j); of y: high nibbles (d + 1)
+      const uint32_t xAB = (a & 0x0F0F0F0Fu) | ((bb & 0x0F0F0F0Fu) << 4);
+      const uint32_t yAB = ((a >> 4) & 0x0F0F0F0Fu) | (bb & 0xF0F0F0F0u);
+      const uint32_t xCD = (cc & 0x0F0F0F0Fu) | ((dd & 0x0F0F0F0Fu) << 4);
+      const uint32_t yCD = ((cc >> 4) & 0x0F0F0F0Fu) | (dd & 0xF0F0F0F0u);
+      pv_mma_nvfp4<0>(st.o[4 * w + 0], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
+      pv_mma_nvfp4<1>(st.o[4 * w + 1], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
+      pv_mma_nvfp4<2>(st.o[4 * w + 2], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
+      pv_mma_nvfp4<3>(st.o[4 * w + 3], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
+    }
+  } else {
+    uint4 vA = *reinterpret_cast<const uint4 *>(stage + Lay::kVc + tA * Lay::kRowBytes + 16 * r);
+    uint4 vB = *reinterpret_cast<const uint4 *>(stage + Lay::kVc + tB * Lay::kRowBytes + 16 * r);
+    uint4 vC = *reinterpret_cast<const uint4 *>(stage + Lay::kVc + tC * Lay::kRowBytes + 16 * r);
+    uint4 vD = *reinterpret_cast<const uint4 *>(stage + Lay::kVc + tD * Lay::kRowBytes + 16 * r);
+    if (nvalid < kTile) {  // masked tokens -> E4M3 zero (stale bytes could be NaN)
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      if (tA >= nvalid) vA = z;
+      if (tB >= nvalid) vB = z;
+      if (tC >= nvalid) vC = z;
+      if (tD >= nvalid) vD = z;
+    }
+    const uint32_t A[4] = {vA.x, vA.y, vA.z, vA.w}, Bv[4] = {vB.x, vB.y, vB.z, vB.w};
+    const uint32_t C[4] = {vC.x, vC.y, vC.z, vC.w}, Dv[4] = {vD.x, vD.y, vD.z, vD.w};
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {
+      const uint32_t ab01 = prmt(A[qd], Bv[qd], 0x5140), ab23 = prmt(A[qd], Bv[qd], 0x7362);
+      const uint32_t cd01 = prmt(C[qd], Dv[qd], 0x5140), cd23 = prmt(C[qd], Dv[qd], 0x7362);
+      mma_f16_16816(st.o[2 * qd], f16x2_from_e4m3x2<0>(ab01), f16x2_from_e4m3x2<1>(ab01),
+                    f16x2_from_e4m3x2<0>(cd01), f16x2_from_e4m3x2<1>(cd01), b0, b1);
+      mma_f16_16816(st.o[2 * qd + 1], f16x2_from_e4m3x2<0>(ab23), f16x2_from_e4m3x2<1>(ab23),
+                    f16x2_from_e4m3x2<0>(cd23), f16x2_from_e4m3x2<1>(cd23), b0, b1);
+    }
+  }
+}
+
+// One 64-token tile: 4 sub-tiles of 16 tokens.
+template <int PREC>
+__device__ __forceinline__ void consume_tile(const uint8_t *stage, int nvalid, int r, int c,
+                                             const uint32_t (&qf)[8][2], const float (&cs)[2], WarpState &st) {
+  float x[4][4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    qk_subtile<PREC>(stage, k, r, c, qf, x[k]);
+    x[k][0] *= cs[0];
+    x[k][1] *= cs[1];
+    x[k][2] *= cs[0];
+    x[k][3] *= cs[1];
+    if (nvalid < kTile) {
+      const int t0 = 16 * k + r, t1 = t0 + 8;
+      if (t0 >= nvalid) x[k][0] = x[k][1] = -INFINITY;
+      if (t1 >= nvalid) x[k][2] = x[k][3] = -INFINITY;
+    }
+  }
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    mx0 = fmaxf(mx0, fmaxf(x[k][0], x[k][2]));
+    mx1 = fmaxf(mx1, fmaxf(x[k][1], x[k][3]));
+  }
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+  }
+  const bool need = (mx0 > st.m[0] + kRescaleThreshold) || (mx1 > st.m[1] + kRescaleThreshold);
+  if (__any_sync(0xffffffffu, need)) {
+    const float n0 = fmaxf(st.m[0], mx0), n1 = fmaxf(st.m[1], mx1);
+    const float al0 = ex2(st.m[0] - n0), al1 = ex2(st.m[1] - n1);
+    st.m[0] = n0;
+    st.m[1] = n1;
+    st.l[0] *= al0;
+    st.l[1] *= al1;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      st.o[j][0] *= al0;
+      st.o[j][1] *= al1;
+      st.o[j][2] *= al0;
+      st.o[j][3] *= al1;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float p0 = ex2(x[k][0] - st.m[0]), p1 = ex2(x[k][1] - st.m[1]);
+    const float p2 = ex2(x[k][2] - st.m[0]), p3 = ex2(x[k][3] - st.m[1]);
+    st.l[0] += p0 + p2;
+    st.l[1] += p1 + p3;
+    const uint32_t b0 = movmatrix_trans(pack_f16x2(p0, p1));  // P[tok 16k+2c, +1][head r]
+    const uint32_t b1 = movmatrix_trans(pack_f16x2(p2, p3));  // P[tok 16k+8+2c, +1][head r]
+    pv_subtile<PREC>(stage, k, r, c, nvalid, b0, b1, st);
+  }
+}
+
+template <int PREC>
+__global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_kernel(const DecodeArgs a) {
+  using Lay = Layout<PREC>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t *ring = smem;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::kStages * Lay::kStageBytes);
+  uint64_t *empty = full + Lay::kStages;
+  int32_t *cum = reinterpret_cast<int32_t *>(empty + Lay::kStages);
+  float *mrg_o = reinterpret_cast<float *>(cum + kMaxBatch + 1);
+  float *mrg_ml = mrg_o + kConsumerWarps * a.G * kD;
+  int *flags = reinterpret_cast<int *>(mrg_ml + kConsumerWarps * kMaxGroup * 2);
+  volatile int *abort = flags;  // flags[0]
+  int *fills = flags + 1;       // flags[1 .. kStages]
+  int *bcast = flags + 1 + Lay::kStages;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Hkv = a.c.Hkv, B = a.B, G = a.G;
+  const int64_t cap = static_cast<int64_t>(a.max_pages) * a.c.P;
+
+  // ---- prologue: tiles per sequence -> prefix sums (warp 0), barriers ----
+  if (tid == 0) {
+    flags[0] = 0;
+    for (int s = 0; s < Lay::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      fills[s] = 0;
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    int carry = 0;
+    if (lane == 0) cum[0] = 0;
+    for (int base = 0; base < B; base += 32) {
+      const int b = base + lane;
+      int n = 0;
+      if (b < B) {
+        int64_t Lb = a.seq_lens[b];
+        if (Lb < 0 || Lb > cap) {
+          if (blockIdx.x == 0) set_err(a.c.err, NVKV_DEVERR_SEQLEN);
+          Lb = Lb < 0 ? 0 : cap;
+        }
+        n = static_cast<int>((Lb + kTile - 1) / kTile);
+      }
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (b < B) cum[b + 1] = carry + incl;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  __syncthreads();
+
+  const int64_t W = static_cast<int64_t>(cum[B]) * Hkv;
+  // never more shares than units: every active CTA owns at least one unit,
+  // which the contributor count of the merge relies on
+  const int64_t NC = W < a.num_ctas ? (W > 0 ? W : 1) : a.num_ctas;
+  const bool active = blockIdx.x < NC;
+  const int64_t u0 = active ? share_begin(blockIdx.x, W, NC) : 0;
+  const int64_t u1 = active ? share_begin(blockIdx.x + 1, W, NC) : 0;
+
+  // zero rows of empty sequences (spread over CTAs)
+  for (int b = blockIdx.x; b < B; b += a.num_ctas) {
+    if (cum[b + 1] == cum[b]) {
+      uint4 *o = reinterpret_cast<uint4 *>(a.out + static_cast<int64_t>(b) * a.Hq * kD);
+      for (int i = tid; i < a.Hq * kD / 8; i += kThreads) o[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
+
+  if (warp == kConsumerWarps) {
+    producer<PREC>(a, ring, full, empty, cum, u0, u1, abort, fills);
+  } else {
+    const int r = lane >> 2, c = lane & 3;
+    const float kscale = __fmul_rn(a.c.scale[0], a.sm_scale * 1.4426950408889634f);
+    const float vscale = a.c.scale[1];
+    int64_t i = 0;
+    for (int64_t u = u0; u < u1;) {
+      const Seg s = seg_at(u, u1, cum, B, Hkv);
+      const int64_t Lb = clamped_len(a, s.b);
+      // query of head j = r of the group, d in [32c, 32c+32), scaled by 2^-e_j into FP16
+      uint32_t qf[8][2];
+      float cs[2];
+      {
+        float qv[32];
+        if (r < G) {
+          const uint4 *qp =
+              reinterpret_cast<const uint4 *>(a.q + (static_cast<int64_t>(s.b) * a.Hq + s.h * G + r) * kD + 32 * c);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const uint4 w = __ldg(qp + v4);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              qv[8 * v4 + 2 * e] = __uint_as_float(ww[e] << 16);
+              qv[8 * v4 + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) qv[e] = 0.0f;
+        }
+        float am = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) am = fmaxf(am, fabsf(qv[e]));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+        // ex = exponent of the head's max minus 14: the scaled max lies in [2^14, 2^15)
+        int ex = 0;
+        if (am > 0.0f) ex = static_cast<int>((__float_as_uint(am) >> 23) & 0xFF) - 127 - 14;
+        ex = max(-110, min(110, ex));
+        const float down = __uint_as_float(static_cast<uint32_t>(127 - ex) << 23);
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) {
+          qf[s2][0] = pack_f16x2(qv[4 * s2] * down, qv[4 * s2 + 1] * down);
+          qf[s2][1] = pack_f16x2(qv[4 * s2 + 2] * down, qv[4 * s2 + 3] * down);
+        }
+        const int e0 = __shfl_sync(0xffffffffu, ex, 8 * c);
+        const int e1 = __shfl_sync(0xffffffffu, ex, 8 * c + 4);
+        cs[0] = __fmul_rn(kscale, __uint_as_float(static_cast<uint32_t>(127 + e0) << 23));
+        cs[1] = __fmul_rn(kscale, __uint_as_float(static_cast<uint32_t>(127 + e1) << 23));
+      }
+      WarpState st;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) st.o[j][0] = st.o[j][1] = st.o[j][2] = st.o[j][3] = 0.0f;
+      st.m[0] = st.m[1] = -INFINITY;
+      st.l[0] = st.l[1] = 0.0f;
+
+      const int ntiles = s.t1 - s.t0;
+      for (int k = 0; k < ntiles; ++k) {
+        const int64_t gi = i + k;
+        if (static_cast<int>(gi % kConsumerWarps) != warp) continue;
+        const int slot = static_cast<int>(gi % Lay::kStages);
+        const uint32_t fill = static_cast<uint32_t>(gi / Lay::kStages);
+        if (mbar_wait_bounded(&full[slot], fill & 1u, abort)) {
+          const int64_t rem = Lb - static_cast<int64_t>(s.t0 + k) * kTile;
+          const int nvalid = rem < kTile ? static_cast<int>(rem) : kTile;
+          consume_tile<PREC>(ring + static_cast<size_t>(slot) * Lay::kStageBytes, nvalid, r, c, qf, cs, st);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+      }
+      i += ntiles;
+
+      // ---- merge the four warps: (m, l) per head, O per (head, d) ----
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        st.l[0] += __shfl_xor_sync(0xffffffffu, st.l[0], o);
+        st.l[1] += __shfl_xor_sync(0xffffffffu, st.l[1], o);
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int hd = 2 * c + e;
+        if (hd < G) {
+          float *dst = mrg_o + (warp * G + hd) * kD + 16 * r;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            dst[2 * j] = st.o[j][e];
+            dst[2 * j + 1] = st.o[j][2 + e];
+          }
+          if (r == 0) {
+            mrg_ml[(warp * kMaxGroup + hd) * 2 + 0] = st.m[e];
+            mrg_ml[(warp * kMaxGroup + hd) * 2 + 1] = st.l[e];
+          }
+        }
+      }
+      named_bar_sync(1, kConsumerWarps * 32);
+
+      const int nb = cum[s.b + 1] - cum[s.b];
+      const bool complete = (s.t0 == 0) && (s.t1 == nb);
+      const int64_t ubh0 = static_cast<int64_t>(cum[s.b]) * Hkv + static_cast<int64_t>(s.h) * nb;
+      const int slot_id = (u == u0) ? 0 : 1;
+      float *part = a.partials + (static_cast<int64_t>(blockIdx.x) * 2 + slot_id) * kSlotFloats;
+      for (int e = tid; e < G * kD; e += kConsumerWarps * 32) {
+        const int hd = e / kD, d = e % kD;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg_ml[(w * kMaxGroup + hd) * 2]);
+        float o = 0.0f, l = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float mw = mrg_ml[(w * kMaxGroup + hd) * 2];
+          const float f = (mw == -INFINITY) ? 0.0f : ex2(mw - M);
+          o += f * mrg_o[(w * G + hd) * kD + d];
+          l += f * mrg_ml[(w * kMaxGroup + hd) * 2 + 1];
+        }
+        if (complete) {
+          a.out[(static_cast<int64_t>(s.b) * a.Hq + s.h * G + hd) * kD + d] = __float2bfloat16_rn(o * (vscale / l));
+        } else {
+          part[hd * kD + d] = o;
+          if (d == 0) {
+            part[kMaxGroup * kD + hd] = M;
+            part[kMaxGroup * kD + kMaxGroup + hd] = l;
+          }
+        }
+      }
+      if (!complete) {
+        __threadfence();
+        named_bar_sync(1, kConsumerWarps * 32);
+        if (tid == 0) {
+          const int64_t c_first = owner_of(ubh0, W, NC), c_last = owner_of(ubh0 + nb - 1, W, NC);
+          const int contributors = static_cast<int>(c_last - c_first + 1);
+          const int old = atomicAdd(&a.counters[s.b * Hkv + s.h], 1);
+          bcast[0] = (old == contributors - 1) ? 1 : 0;
+          bcast[1] = static_cast<int>(c_first);
+          bcast[2] = contributors;
+          __threadfence();
+        }
+        named_bar_sync(1, kConsumerWarps * 32);
+        if (bcast[0]) {
+          // last arriver: merge every contributor's partial
+          const int64_t c_first = bcast[1];
+          const int ncontrib = bcast[2];
+          for (int e = tid; e < G * kD; e += kConsumerWarps * 32) {
+            const int hd = e / kD, d = e % kD;
+            float M = -INFINITY;
+            for (int q = 0; q < ncontrib; ++q) {
+              const int64_t cc = c_first + q;
+              const int sl = share_begin(cc, W, NC) >= ubh0 ? 0 : 1;
+              M = fmaxf(M, __ldcg(a.partials + (cc * 2 + sl) * kSlotFloats + kMaxGroup * kD + hd));
+            }
+            float o = 0.0f, l = 0.0f;
+            for (int q = 0; q < ncontrib; ++q) {
+              const int64_t cc = c_first + q;
+              const int sl = share_begin(cc, W, NC) >= ubh0 ? 0 : 1;
+              const float *pp = a.partials + (cc * 2 + sl) * kSlotFloats;
+              const float mq = __ldcg(pp + kMaxGroup * kD + hd);
+              const float f = (mq == -INFINITY) ? 0.0f : ex2(mq - M);
+              o += f * __ldcg(pp + hd * kD + d);
+              l += f * __ldcg(pp + kMaxGroup * kD + kMaxGroup + hd);
+            }
+            a.out[(static_cast<int64_t>(s.b) * a.Hq + s.h * G + hd) * kD + d] = __float2bfloat16_rn(o * (vscale / l));
+          }
+          if (tid == 0) a.counters[s.b * Hkv + s.h] = 0;
+        }
+      }
+      named_bar_sync(1, kConsumerWarps * 32);
+      u += ntiles;
+    }
+  }
+
+  __syncthreads();
+  // after a timeout, wait (bounded) for copies still in flight before the CTA exits
+  if (*abort) {
+    if (tid == 0) set_err(a.c.err, NVKV_DEVERR_TIMEOUT);
+    if (tid == kConsumerWarps * 32) {
+      volatile int never = 0;
+      for (int s = 0; s < Lay::kStages; ++s)
+        if (fills[s] > 0) mbar_wait_bounded(&full[s], static_cast<uint32_t>(fills[s] - 1) & 1u, &never);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+struct DevInfo {
+  int sms = 0;
+  int occ[2][kMaxGroup + 1] = {};
+};
+
+DevInfo g_info[64];
+std::once_flag g_once[64];
+
+template <int PREC>
+int occupancy_for(int G) {
+  const int smem = smem_bytes_for<PREC>(G);
+  if (cudaFuncSetAttribute(decode_kernel<PREC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<PREC>, kThreads, smem) != cudaSuccess) return 0;
+  return n;
+}
+
+const DevInfo *dev_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::call_once(g_once[dev], [dev] {
+    DevInfo &d = g_info[dev];
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    for (int G = 1; G <= kMaxGroup; ++G) {
+      d.occ[0][G] = occupancy_for<NVKV_PREC_NVFP4>(G);
+      d.occ[1][G] = occupancy_for<NVKV_PREC_FP8_E4M3>(G);
+    }
+  });
+  return g_info[dev].sms > 0 ? &g_info[dev] : nullptr;
+}
+
+// CTAs of the persistent grid.  num_splits > 0: batch * Hkv * num_splits, so
+// equal-length sequences are cut into exactly num_splits shares each.
+int64_t num_ctas_for(int prec, int32_t batch, int32_t Hkv, int32_t G, int64_t max_units, int32_t num_splits) {
+  int64_t n;
+  if (num_splits > 0) {
+    n = static_cast<int64_t>(batch) * Hkv * num_splits;
+  } else {
+    const DevInfo *d = dev_info();
+    if (!d) return -1;
+    const int occ = d->occ[prec][G] > 0 ? d->occ[prec][G] : 1;
+    n = static_cast<int64_t>(d->sms) * occ;
+  }
+  if (n > max_units) n = max_units;
+  return n < 1 ? 1 : n;
+}
+
+size_t counters_bytes(int32_t batch, int32_t Hkv) { return (static_cast<size_t>(batch) * Hkv * 4 + 255) / 256 * 256; }
+
+size_t workspace_bytes_for(int32_t batch, int32_t Hkv, int64_t nctas) {
+  return counters_bytes(batch, Hkv) + static_cast<size_t>(nctas) * 2 * kSlotFloats * sizeof(float);
+}
+
+nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t *block_table, int32_t max_pages,
+                          const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, int32_t prec, float sm_scale,
+                          int32_t num_splits, void *workspace, size_t workspace_bytes, void *out, void *stream) {
+  nvkv_status st = check_cache(cache, prec);
+  if (st != NVKV_OK) return st;
+  if (batch < 0 || num_q_heads <= 0 || max_pages <= 0 || num_splits < 0) return NVKV_ERR_INVALID_ARG;
+  if (batch == 0) return NVKV_OK;
+  if (batch > kMaxBatch) return NVKV_ERR_UNSUPPORTED;
+  const int Hkv = cache->num_kv_heads;
+  if (num_q_heads % Hkv != 0) return NVKV_ERR_INVALID_ARG;
+  const int G = num_q_heads / Hkv;
+  if (G > kMaxGroup) return NVKV_ERR_UNSUPPORTED;
+  if (!q || !block_table || !seq_lens || !out || !workspace) return NVKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return NVKV_ERR_UNSUPPORTED;
+  if (!(sm_scale >= 0.0f)) return NVKV_ERR_INVALID_ARG;
+  const int64_t max_units = static_cast<int64_t>(batch) * Hkv *
+                            ((static_cast<int64_t>(max_pages) * cache->page_size + kTile - 1) / kTile);
+  const int64_t nctas = num_ctas_for(prec, batch, Hkv, G, max_units, num_splits);
+  if (nctas < 0) return NVKV_ERR_CUDA;
+  if (nctas > 0x7fffffff) return NVKV_ERR_UNSUPPORTED;
+  if (workspace_bytes < workspace_bytes_for(batch, Hkv, nctas)) return NVKV_ERR_WORKSPACE_TOO_SMALL;
+  if (!dev_info()) return NVKV_ERR_CUDA;
+
+  DecodeArgs a;
+  a.q = static_cast<const __nv_bfloat16 *>(q);
+  a.c = to_dev(cache);
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.max_pages = max_pages;
+  a.B = batch;
+  a.Hq = num_q_heads;
+  a.G = G;
+  a.sm_scale = sm_scale > 0.0f ? sm_scale : 1.0f / sqrtf(static_cast<float>(cache->head_dim));
+  a.num_ctas = static_cast<int32_t>(nctas);
+  a.counters = static_cast<int32_t *>(workspace);
+  a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + counters_bytes(batch, Hkv));
+  a.out = static_cast<__nv_bfloat16 *>(out);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (prec == NVKV_PREC_NVFP4)
+    decode_kernel<NVKV_PREC_NVFP4><<<static_cast<int>(nctas), kThreads, smem_bytes_for<NVKV_PREC_NVFP4>(G), s>>>(a);
+  else
+    decode_kernel<NVKV_PREC_FP8_E4M3>
+        <<<static_cast<int>(nctas), kThreads, smem_bytes_for<NVKV_PREC_FP8_E4M3>(G), s>>>(a);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace nvkv
+
+using namespace nvkv;
+
+extern "C" {
+
+size_t nvkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t num_splits) {
+  if (batch <= 0 || batch > kMaxBatch || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim != kD ||
+      num_splits < 0)
+    return 0;
+  if (num_q_heads % num_kv_heads != 0) return 0;
+  const int G = num_q_heads / num_kv_heads;
+  if (G > kMaxGroup) return 0;
+  int64_t nctas;
+  if (num_splits > 0) {
+    nctas = static_cast<int64_t>(batch) * num_kv_heads * num_splits;
+  } else {
+    const DevInfo *d = dev_info();
+    if (!d) return 0;
+    int occ = 1;
+    for (int p = 0; p < 2; ++p) occ = d->occ[p][G] > occ ? d->occ[p][G] : occ;
+    nctas = static_cast<int64_t>(d->sms) * occ;
+  }
+  return workspace_bytes_for(batch, num_kv_heads, nctas);
+}
+
+nvkv_status nvkv_decode_workspace_init(void *workspace, size_t bytes, void *stream) {
+  if (!workspace && bytes) return NVKV_ERR_INVALID_ARG;
+  if (bytes == 0) return NVKV_OK;
+  return cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess ? NVKV_OK
+                                                                                               : NVKV_ERR_CUDA;
+}
+
+nvkv_status nvfp4_paged_decode_attention(const void *q, const nvkv_cache *cache, const int32_t *block_table,
+                                         int32_t max_pages, const int32_t *seq_lens, int32_t batch,
+                                         int32_t num_q_heads, int32_t layer_precision, float sm_scale,
+                                         int32_t num_splits, void *workspace, size_t workspace_bytes, void *out,
+                                         void *stream) {
+  if (!cache || layer_precision != cache->prec) return NVKV_ERR_INVALID_ARG;
+  if (layer_precision != NVKV_PREC_NVFP4 && layer_precision != NVKV_PREC_FP8_E4M3) return NVKV_ERR_INVALID_ARG;
+  return decode_common(q, cache, block_table, max_pages, seq_lens, batch, num_q_heads, layer_precision, sm_scale,
+                       num_splits, workspace, workspace_bytes, out, stream);
+}
+
+nvkv_status fp8_paged_decode_attention(const void *q, const nvkv_cache *cache, const int32_t *block_table,
+                                       int32_t max_pages, const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                       float sm_scale, int32_t num_splits, void *workspace, size_t workspace_bytes,
+                                       void *out, void *stream) {
+  return decode_common(q, cache, block_table, max_pages, seq_lens, batch, num_q_heads, NVKV_PREC_FP8_E4M3, sm_scale,
+                       num_splits, workspace, workspace_bytes, out, stream);
+}
+
+}  // extern "C"
