@@ -173,8 +173,11 @@ nvkv_status fp8_paged_decode_attention(const void *q, const nvkv_cache *cache, c
  * seq_ids[i] land in rows cu_prefix[i] + t of ws_k / ws_v, layout
  * [rows][num_kv_heads][head_dim] E4M3:
  *   byte = E4M3_rne_satfinite((e2m1 * S) * (g / ws_scale))   (FP32, per K and V)
- *   seq_ids, prefix_lens  [n] int32 device; cu_prefix [n+1] int64 device
- *                         exclusive prefix sums of prefix_lens
+ *   seq_ids, prefix_lens  [n] int32 device; each seq_ids[i] must index a row
+ *                         of block_table; cu_prefix [n+1] int64 device,
+ *                         exclusive prefix sums of prefix_lens; a prefix longer
+ *                         than its row (max_pages * page_size) is skipped and
+ *                         NVKV_DEVERR_SEQLEN raised
  *   ws_scale              device float[2] {K, V}, > 0 (e.g. 6 * g)
  *   ws_rows               rows allocated in ws_k and ws_v (host value); rows
  *                         past it are skipped and NVKV_DEVERR_WS_ROWS raised

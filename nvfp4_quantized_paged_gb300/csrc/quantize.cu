@@ -220,6 +220,10 @@ __global__ void __launch_bounds__(256)
   }
   const int64_t t = r - cu_prefix[lo];
   if (t >= prefix_lens[lo]) return;
+  if (t / c.P >= max_pages) {  // prefix longer than its block-table row
+    set_err(c.err, NVKV_DEVERR_SEQLEN);
+    return;
+  }
   const int64_t page = block_table[static_cast<int64_t>(seq_ids[lo]) * max_pages + t / c.P];
   if (page < 0 || page >= c.num_pages) {
     set_err(c.err, NVKV_DEVERR_PAGE);

@@ -1,0 +1,128 @@
+"""Device-side driver of the decode hot path for one workload.
+
+Builds a layer's paged cache on the GPU from a seeded workload, using only
+this library's kernels for every step of the method (global scale, quantized
+write, decode attention, workspace dequant), and exposes ``step()``: the work
+of one serving step for that layer, i.e. the quantized write of the step's new
+tokens, the paged decode attention over the batch and, for workloads with a
+chunked-extend pass, the prefix dequant into the shared FP8 workspace plus the
+write of the new chunk.  PyTorch only allocates memory and orders streams.
+"""
+from __future__ import annotations
+
+from typing import List, Optional
+
+import numpy as np
+import torch
+
+from . import (Cache, FP8_GLOBAL_DIVISOR, NVFP4_GLOBAL_DIVISOR, PREC_FP8, PREC_NVFP4, alloc_decode_workspace,
+               fp8_kv_quantize_write, nvfp4_kv_dequant_to_fp8_workspace, nvfp4_kv_quantize_write,
+               nvfp4_paged_decode_attention, nvkv_amax_update, nvkv_global_scale)
+from .workloads import Workload
+
+
+class Layer:
+    """One layer of a workload: cache, scales and step inputs on the device.
+
+    ``prec`` overrides the workload's precision map (the FP8 comparator runs
+    the same workload with every layer in FP8).
+    """
+
+    def __init__(self, wl: Workload, layer: int, device="cuda", prec: Optional[int] = None,
+                 num_splits: Optional[int] = None):
+        s = wl.spec
+        self.wl, self.layer, self.device = wl, layer, torch.device(device)
+        self.prec = prec if prec is not None else (PREC_FP8 if wl.is_fp8(layer) else PREC_NVFP4)
+        self.num_splits = s.num_splits if num_splits is None else num_splits
+        div = FP8_GLOBAL_DIVISOR if self.prec == PREC_FP8 else NVFP4_GLOBAL_DIVISOR
+        # global scale over every token the layer will hold (prefix, step and
+        # extend tokens), K and V separately
+        self.amax = torch.zeros(2, dtype=torch.float32, device=self.device)
+        for b in range(s.B):
+            for kind in (0, 1):
+                nvkv_amax_update(wl.kv(layer, kind, b), self.amax[kind:kind + 1])
+        self.scale = torch.zeros(2, dtype=torch.float32, device=self.device)
+        for kind in (0, 1):
+            nvkv_global_scale(self.amax[kind:kind + 1], self.scale[kind:kind + 1], div)
+        self.cache = Cache(self.prec, wl.num_pages, s.Hkv, s.P, device=self.device, kv_scale=self.scale)
+        for b in range(s.B):  # initial fill of each sequence's visible prefix
+            L = int(wl.seq_lens[b])
+            if L:
+                self.write(wl.kv(layer, 0, b, 0, L), wl.kv(layer, 1, b, 0, L),
+                           torch.from_numpy(wl.slots(b, 0, L)).to(self.device))
+        self.block_table = torch.from_numpy(wl.block_table).to(self.device)
+        self.seq_lens = torch.from_numpy(wl.seq_lens).to(self.device)
+        self.q = wl.q_bf16(layer)
+        self.k_new = self.v_new = self.slots_new = None
+        if wl.step_seqs():  # tokens re-written inside each step (the last ones of each sequence)
+            ks, vs = [], []
+            for b in wl.step_seqs():
+                L = int(wl.seq_lens[b])
+                ks.append(wl.kv(layer, 0, b, L - s.step_write, L))
+                vs.append(wl.kv(layer, 1, b, L - s.step_write, L))
+            self.k_new, self.v_new = torch.cat(ks).contiguous(), torch.cat(vs).contiguous()
+            self.slots_new = torch.from_numpy(wl.step_slots()).to(self.device)
+        self.ext = None
+        if s.extend_seqs and self.prec == PREC_NVFP4:
+            ids = [b for b in s.extend_seqs if b < s.B]
+            pref = [int(wl.seq_lens[b]) for b in ids]
+            cu = np.zeros(len(ids) + 1, np.int64)
+            cu[1:] = np.cumsum(pref)
+            n_ext = s.extend_tokens
+            ws_scale = torch.zeros(2, dtype=torch.float32, device=self.device)
+            for kind in (0, 1):  # FP8 per-tensor convention: amax / 448
+                nvkv_global_scale(self.amax[kind:kind + 1], ws_scale[kind:kind + 1], FP8_GLOBAL_DIVISOR)
+            self.ext = dict(
+                seq_ids=torch.tensor(ids, dtype=torch.int32, device=self.device),
+                prefix_lens=torch.tensor(pref, dtype=torch.int32, device=self.device),
+                cu_prefix=torch.from_numpy(cu).to(self.device),
+                ws_scale=ws_scale,
+                ws_k=torch.empty(int(cu[-1]), s.Hkv, s.D, dtype=torch.uint8, device=self.device),
+                ws_v=torch.empty(int(cu[-1]), s.Hkv, s.D, dtype=torch.uint8, device=self.device),
+                k=torch.cat([wl.kv(layer, 0, b, pref[i], pref[i] + n_ext) for i, b in enumerate(ids)]).contiguous(),
+                v=torch.cat([wl.kv(layer, 1, b, pref[i], pref[i] + n_ext) for i, b in enumerate(ids)]).contiguous(),
+                slots=torch.from_numpy(np.concatenate([wl.slots(b, pref[i], pref[i] + n_ext)
+                                                       for i, b in enumerate(ids)])).to(self.device),
+            )
+        self.out = torch.empty(s.B, s.Hq, s.D, dtype=torch.bfloat16, device=self.device)
+        self.workspace = alloc_decode_workspace(s.B, s.Hq, s.Hkv, self.num_splits, device=self.device)
+
+    # ------------------------------------------------------------------ steps
+    def write(self, k, v, slots):
+        if self.prec == PREC_NVFP4:
+            nvfp4_kv_quantize_write(k, v, slots, self.scale, self.cache)
+        else:
+            fp8_kv_quantize_write(k, v, slots, self.scale, self.cache)
+
+    def decode(self, q=None, out=None):
+        nvfp4_paged_decode_attention(q if q is not None else self.q, self.cache, self.block_table, self.seq_lens,
+                                     self.prec, out if out is not None else self.out, self.workspace,
+                                     num_splits=self.num_splits)
+
+    def extend(self):
+        e = self.ext
+        nvfp4_kv_dequant_to_fp8_workspace(self.block_table, e["seq_ids"], e["prefix_lens"], e["cu_prefix"],
+                                          self.cache, e["ws_scale"], e["ws_k"], e["ws_v"])
+        self.write(e["k"], e["v"], e["slots"])
+
+    def step(self):
+        if self.k_new is not None:
+            self.write(self.k_new, self.v_new, self.slots_new)
+        self.decode()
+        if self.ext is not None:
+            self.extend()
+
+    # ------------------------------------------------------------ bookkeeping
+    def kv_bytes_read(self) -> int:
+        """Algorithmic bytes decode reads: K/V codes and scales of every visible token."""
+        per_tok = 144 if self.prec == PREC_NVFP4 else 256
+        return int(self.wl.seq_lens.astype(np.int64).sum()) * self.wl.spec.Hkv * per_tok
+
+    def qo_bytes(self) -> int:
+        s = self.wl.spec
+        return 2 * s.B * s.Hq * s.D * 2
+
+
+def build_layers(wl: Workload, device="cuda", layers: Optional[List[int]] = None, prec=None) -> List[Layer]:
+    idx = layers if layers is not None else list(range(wl.spec.layers))
+    return [Layer(wl, l, device, prec=prec) for l in idx]

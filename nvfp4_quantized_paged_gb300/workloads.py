@@ -50,6 +50,7 @@ class Spec:
     D: int
     P: int
     L: int = 0                      # fixed length (0: drawn, see lens_lognormal)
+    lens: Optional[Tuple[int, ...]] = None  # explicit per-sequence lengths (ragged test cases)
     lens_lognormal: Optional[Tuple[float, float, int, int]] = None  # median, sigma, lo, hi
     dist: str = "normal"            # normal | channel_outliers | element_outliers | lognormal_channels
     outlier_scale: float = 1.0
@@ -106,7 +107,9 @@ class Workload:
     def __init__(self, spec: Spec, seed: int = 0, device="cpu"):
         self.spec, self.seed, self.device = spec, seed, torch.device(device)
         s = spec
-        if s.lens_lognormal is not None:
+        if s.lens is not None:
+            self.seq_lens = np.array(s.lens, np.int32)
+        elif s.lens_lognormal is not None:
             med, sig, lo, hi = s.lens_lognormal
             g = _gen("cpu", seed, 1, 0xA11)
             z = torch.randn(s.B, generator=g, dtype=torch.float64)
@@ -120,7 +123,7 @@ class Workload:
             if b < s.B:
                 self.ext[b] = s.extend_tokens
         need = (self.seq_lens + self.ext + s.P - 1) // s.P
-        self.max_pages = int(need.max()) if s.B else 1
+        self.max_pages = max(1, int(need.max())) if s.B else 1
         self.num_pages = int(need.sum())
         if s.table == "contiguous":
             order = np.arange(self.num_pages, dtype=np.int64)
@@ -143,7 +146,12 @@ class Workload:
         """Slots of the tokens re-written inside one step, sequence-major."""
         s = self.spec
         return np.concatenate([self.slots(b, int(self.seq_lens[b]) - s.step_write, int(self.seq_lens[b]))
-                               for b in range(s.B)]) if s.step_write else np.zeros(0, np.int64)
+                               for b in self.step_seqs()] + [np.zeros(0, np.int64)])
+
+    def step_seqs(self):
+        """Sequences that re-write their last tokens inside a step."""
+        s = self.spec
+        return [b for b in range(s.B) if s.step_write and self.seq_lens[b] >= s.step_write]
 
     def is_fp8(self, layer: int) -> bool:
         return layer in self.spec.fp8_layers
