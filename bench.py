@@ -1,0 +1,423 @@
+"""Benchmark of the NVFP4 paged-KV decode hot path on GB300.
+
+One step = the hot path of one serving step over one batch: the NVFP4
+quantized write of the step's new tokens and the paged GQA decode attention
+over the whole batch (plus the chunked-extend pass where the workload has one).
+Default workload: decode_b16_ctx8k (16 sequences x 8192 tokens, 32 q / 8 KV
+heads, head_dim 128, page 64, permuted block table, 1% x20 outliers).
+
+Prints ONE JSON line (rank 0).  ``value`` is the algorithmic HBM throughput of
+the step (GB/s; bytes of NVFP4 K/V codes + scales read, Q read, output
+written, new tokens read and their codes written) over the device-timed step;
+``e2e`` is the same metric with the step's inputs copied from pinned host
+memory and the output copied back inside the timed region.  The FP8-KV
+variant of the same workload is timed beside it as the comparator.  Between
+timed steps the caches rotate over replicas whose total exceeds L2.
+
+Multi-GPU: replicas only (one independent copy of the workload per rank, no
+collective on the data path); the barrier and max-over-ranks timing use
+torch.distributed.
+
+--impl reference: the CPU oracle (scalar C, one thread) on a bounded sample of
+the same workload, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 paged decode attn: HBM GB/s & % of 8 TB/s peak; decode tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+DEFAULT_WORKLOAD = "decode_b16_ctx8k"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        return dist, rank, ws, local
+    return None, rank, ws, local
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def _max_over_ranks(dist, x, device):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _sum_over_ranks(dist, x, device):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.path = index, None, None
+
+    def __enter__(self):
+        self.path = os.path.join("/tmp", f"nvkv_clocks_{os.getpid()}.csv")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "100"], stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": []}
+        try:
+            rows = [l.split(",") for l in open(self.path).read().strip().splitlines() if l.strip()]
+            sm = [float(r[0]) for r in rows]
+            out["sm_mhz"] = statistics.median(sm) if sm else None
+            out["sm_max_mhz"] = float(rows[0][1]) if rows else None
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for j, n in enumerate(names):
+                if any(r[2 + j].strip().lower() == "active" for r in rows):
+                    out["reasons"].append(n)
+            out["samples"] = len(rows)
+        except Exception:
+            pass
+        return out
+
+
+def step_bytes(lay) -> dict:
+    """Algorithmic bytes of one step of one layer."""
+    s = lay.wl.spec
+    kv = lay.kv_bytes_read()
+    qo = lay.qo_bytes()
+    per_tok_write = (144 if lay.prec == 0 else 256)
+    w = 0
+    if lay.k_new is not None:
+        n = lay.k_new.shape[0] * s.Hkv
+        w += n * (2 * 128 * 4 + per_tok_write)
+    if lay.ext is not None:
+        rows = lay.ext["ws_k"].shape[0] * s.Hkv
+        w += rows * (144 + 256)                                    # workspace dequant: read NVFP4, write FP8
+        n = lay.ext["k"].shape[0] * s.Hkv
+        w += n * (2 * 128 * 4 + per_tok_write)
+    return dict(kv=kv, qo=qo, write=w, total=kv + qo + w)
+
+
+def run_ours(args):
+    dist, rank, ws, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import nvfp4_quantized_paged_gb300 as nv
+    from nvfp4_quantized_paged_gb300.runner import Layer
+    from nvfp4_quantized_paged_gb300.workloads import SPECS, Workload
+    nv.lib()
+    spec = SPECS[args.workload]
+    wl = Workload(spec, seed=0, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    layers = list(range(spec.layers))
+
+    def build(prec=None):
+        first = [Layer(wl, l, dev, prec=prec) for l in layers]
+        per = sum(step_bytes(x)["kv"] for x in first)
+        reps = max(1, -(-3 * l2 // max(per, 1)))
+        sets = [first] + [[Layer(wl, l, dev, prec=prec) for l in layers] for _ in range(reps - 1)]
+        return sets
+
+    sets = build()
+    bytes_step = sum(step_bytes(x)["total"] for x in sets[0])
+    kv_step = sum(step_bytes(x)["kv"] + step_bytes(x)["qo"] for x in sets[0])
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        for lay in sets[i % len(sets)]:
+            lay.step()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    # per-launch events around every decode call (same stream) for the roofline
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps * len(layers))]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(dist)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t0.record(stream)
+        j = 0
+        for i in range(args.steps):
+            for lay in sets[i % len(sets)]:
+                if lay.k_new is not None:
+                    lay.write(lay.k_new, lay.v_new, lay.slots_new)
+                ev[j][0].record(stream)
+                lay.decode()
+                ev[j][1].record(stream)
+                j += 1
+                if lay.ext is not None:
+                    lay.extend()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    _barrier(dist)
+    ms = t0.elapsed_time(t1) / args.steps
+    ms = _max_over_ranks(dist, ms, dev)
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    launches_per_step = sum((1 if x.k_new is not None else 0) + 1 + (2 if x.ext is not None else 0)
+                            for x in sets[0])
+
+    # e2e: inputs from pinned host memory, output back to the host, through the C ABI
+    host = []
+    for lay in sets[0]:
+        h = dict(q=lay.q.cpu().pin_memory(), out=torch.empty(lay.out.shape, dtype=lay.out.dtype).pin_memory())
+        if lay.k_new is not None:
+            h.update(k=lay.k_new.cpu().pin_memory(), v=lay.v_new.cpu().pin_memory(),
+                     s=lay.slots_new.cpu().pin_memory())
+        host.append(h)
+    h2d = sum(h["q"].numel() * 2 + (h["k"].numel() * 8 + h["s"].numel() * 8 if "k" in h else 0) for h in host)
+    d2h = sum(h["out"].numel() * 2 for h in host)
+
+    def e2e_step(i):
+        for lay, h in zip(sets[i % len(sets)], host):
+            lay.q.copy_(h["q"], non_blocking=True)
+            if "k" in h:
+                lay.k_new.copy_(h["k"], non_blocking=True)
+                lay.v_new.copy_(h["v"], non_blocking=True)
+                lay.slots_new.copy_(h["s"], non_blocking=True)
+                lay.write(lay.k_new, lay.v_new, lay.slots_new)
+            lay.decode()
+            if lay.ext is not None:
+                lay.extend()
+            h["out"].copy_(lay.out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    _barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, dev)
+
+    # FP8-KV comparator: the same workload with every layer in FP8
+    fp8_ms = None
+    if not args.no_fp8:
+        del sets
+        torch.cuda.empty_cache()
+        fsets = build(prec=nv.PREC_FP8)
+
+        def fstep(i):
+            for lay in fsets[i % len(fsets)]:
+                lay.step()
+        for i in range(args.warmup):
+            fstep(i)
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for i in range(args.steps):
+            fstep(i)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        fp8_ms = _max_over_ranks(dist, f0.elapsed_time(f1) / args.steps, dev)
+
+    total_bytes = _sum_over_ranks(dist, float(bytes_step), dev)
+    gbs = total_bytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    dec_gbs = kv_step / len(layers) / (dec_avg_ms * 1e-3) / 1e9 if len(layers) else 0.0
+    traffic = _traffic_from_profile(args.workload)
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(gbs, 1),
+            "unit": "GB/s",
+            "n_gpus": ws,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f16xf16->f32 (NVFP4/E4M3 dequantized exactly to f16)",
+            "data": "synthetic (seeded; no dataset or weights)",
+            "config": {
+                "workload": args.workload, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv, "D": spec.D,
+                "L": spec.L or "ragged", "page": spec.P, "layers": spec.layers,
+                "l2": f"inputs rotate over cache replicas totalling >= 3x L2 ({l2 >> 20} MiB)",
+                "parallelism": f"replicas x{ws}",
+            },
+            "pct_of_8TBps": round(100.0 * gbs / ws / NOMINAL_HBM_GBS, 2),
+            "pct_of_measured_hbm": round(100.0 * gbs / ws / peak, 2),
+            "decode_tokens_per_s": round(_sum_over_ranks(dist, spec.B, dev) / (ms * 1e-3), 1),
+            "us_per_layer": round(ms * 1e3 / spec.layers, 2),
+            "e2e": {"value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                    "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": int(launches_per_step * args.steps),
+            "roofline": {"bound": "hbm", "kernel": "decode_kernel<NVFP4>", "achieved": round(dec_gbs, 1),
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(dec_gbs / peak, 4), "traffic": traffic,
+                         "algorithmic_bytes_per_launch": int(kv_step / len(layers)),
+                         "avg_launch_us": round(dec_avg_ms * 1e3, 3)},
+            "fp8_comparator": None if fp8_ms is None else {
+                "ms_per_step": round(fp8_ms, 5), "speedup_nvfp4_over_fp8": round(fp8_ms / ms, 3)},
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(spec, args.workload, budget_s=args.cpu_budget)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def _traffic_from_profile(workload):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"decode_nvfp4_{workload}.json")
+    try:
+        prof = json.load(open(path))
+        src = open(os.path.join(ROOT, "nvfp4_quantized_paged_gb300", "csrc", "decode.cu"), "rb").read()
+        if prof.get("decode_cu_sha256") != hashlib.sha256(src).hexdigest():
+            return None
+        return prof.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def cpu_baseline(spec, workload, budget_s=15.0):
+    """The oracle (scalar C, 1 thread) on a bounded sample: whole sequences of
+    the workload, each = its step write + decode attention over all heads."""
+    import oracle
+    from nvfp4_quantized_paged_gb300.workloads import Workload
+    wl = Workload(spec, seed=0, device="cpu")
+    per_tok = 144
+    done_bytes, t_total, seqs = 0, 0.0, 0
+    for b in range(spec.B):
+        L = int(wl.seq_lens[b])
+        k = wl.kv(0, 0, b).numpy()
+        v = wl.kv(0, 1, b).numpy()
+        g = np.array([oracle.global_scale(k), oracle.global_scale(v)], np.float32)
+        npages = (L + spec.P - 1) // spec.P
+        c = oracle.Cache(oracle.PREC_NVFP4, npages, spec.Hkv, spec.P, spec.D, g)
+        t = np.arange(L)
+        oracle.quantize_write(c, k[:L], v[:L], (t // spec.P) * spec.P + t % spec.P)
+        bt = np.arange(npages, dtype=np.int32)[None]
+        q = wl.q_bf16(0)[b:b + 1].view(torch.int16).numpy().view(np.uint16)
+        nw = max(spec.step_write, 0)
+        t0 = time.perf_counter()
+        if nw:
+            tt = np.arange(L - nw, L)
+            oracle.quantize_write(c, k[L - nw:L], v[L - nw:L], (tt // spec.P) * spec.P + tt % spec.P)
+        oracle.paged_decode_attention(c, q, bt, np.array([L], np.int32))
+        t_total += time.perf_counter() - t0
+        done_bytes += L * spec.Hkv * per_tok + 2 * spec.Hq * spec.D * 2 + nw * spec.Hkv * (2 * 128 * 4 + per_tok)
+        seqs += 1
+        if t_total >= budget_s:
+            break
+    return {"value": round(done_bytes / t_total / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{seqs} of {spec.B} sequences (step write + decode of all heads), {t_total:.1f} s",
+            "cpu": _cpu_name(), "host_cores": os.cpu_count()}
+
+
+def _cpu_name():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from nvfp4_quantized_paged_gb300.workloads import SPECS
+    spec = SPECS[args.workload]
+    # each step: a bounded oracle sample of the workload
+    for _ in range(args.warmup):
+        pass
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cb = cpu_baseline(spec, args.workload, budget_s=args.cpu_budget / max(1, args.steps))
+        vals.append(cb["value"])
+    elapsed = time.perf_counter() - t0
+    v = statistics.median(vals)
+    line = {"metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * elapsed / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (oracle attention), f32 (oracle quantizer)",
+            "data": "synthetic (seeded)", "impl": "reference",
+            "config": {"workload": args.workload, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv, "D": spec.D,
+                       "L": spec.L, "page": spec.P},
+            "cpu_baseline": dict(cb, value=v),
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-fp8", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

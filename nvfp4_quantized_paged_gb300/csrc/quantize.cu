@@ -59,10 +59,11 @@ __device__ __forceinline__ void load16(const __nv_bfloat16 *src, float (&x)[16])
 // non-negative float), then one FP32 divide.
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(256) amax_kernel(const T *__restrict__ x, int64_t n, uint32_t *out_bits) {
+__global__ void __launch_bounds__(256) amax_kernel(const T *__restrict__ x, int64_t n, bool vec,
+                                                   uint32_t *out_bits) {
   float m = 0.0f;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int64_t n16 = n / 16;
+  const int64_t n16 = vec ? n / 16 : 0;  // 128-bit loads need a 16-byte aligned base
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) {
     float v[16];
     load16(x + 16 * i, v);
@@ -267,10 +268,12 @@ int amax_grid(int64_t n) {
 
 nvkv_status launch_amax(const void *x, nvkv_dtype dtype, int64_t n, float *acc, cudaStream_t s) {
   const int grid = amax_grid(n);
+  const bool vec = aligned16(x);
   if (dtype == NVKV_DTYPE_F32)
-    amax_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(x), n, reinterpret_cast<uint32_t *>(acc));
+    amax_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(x), n, vec,
+                                             reinterpret_cast<uint32_t *>(acc));
   else
-    amax_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x), n,
+    amax_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x), n, vec,
                                                      reinterpret_cast<uint32_t *>(acc));
   return launch_status();
 }
@@ -332,7 +335,6 @@ nvkv_status nvkv_global_scale(const void *x, nvkv_dtype dtype, int64_t n, float 
                               void *stream) {
   if (!out || n < 0 || (n > 0 && !x) || !(divisor > 0.0f)) return NVKV_ERR_INVALID_ARG;
   if (dtype != NVKV_DTYPE_F32 && dtype != NVKV_DTYPE_BF16) return NVKV_ERR_INVALID_ARG;
-  if (n > 0 && !aligned16(x)) return NVKV_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(out, 0, sizeof(float), s) != cudaSuccess) return NVKV_ERR_CUDA;
   if (n > 0) {
@@ -347,7 +349,6 @@ nvkv_status nvkv_amax_update(const void *x, nvkv_dtype dtype, int64_t n, float *
   if (!amax || n < 0 || (n > 0 && !x)) return NVKV_ERR_INVALID_ARG;
   if (dtype != NVKV_DTYPE_F32 && dtype != NVKV_DTYPE_BF16) return NVKV_ERR_INVALID_ARG;
   if (n == 0) return NVKV_OK;
-  if (!aligned16(x)) return NVKV_ERR_UNSUPPORTED;
   return launch_amax(x, dtype, n, amax, static_cast<cudaStream_t>(stream));
 }
 
