@@ -184,7 +184,11 @@ def run_ours(args):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _barrier(dist)
     torch.cuda.synchronize()
-    with Clocks(local) as clk:
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    with Clocks(gpu_id) as clk:
         t0.record(stream)
         j = 0
         for i in range(args.steps):
