@@ -167,6 +167,31 @@ nvkv_status fp8_paged_decode_attention(const void *q, const nvkv_cache *cache, c
                                        int32_t num_q_heads, float sm_scale, int32_t num_splits, void *workspace,
                                        size_t workspace_bytes, void *out, void *stream);
 
+/* Decode attention that allocates nothing and takes no workspace (no
+ * counterpart in the pages: this is a convenience of this library).  For
+ * callers that cannot hand out device memory per call: serving engines that
+ * give all free HBM to their KV page pool at start-up and keep no allocator
+ * for scratch, and plugin hosts that pass a kernel only its input and output
+ * pointers.  Same arguments and result as nvfp4_paged_decode_attention without
+ * workspace/workspace_bytes; the split-KV scratch lives in a fixed array of
+ * NVKV_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the
+ * library keeps until the process exits.  A problem whose scratch (see
+ * nvkv_decode_workspace_size) exceeds that size is rejected with
+ * NVKV_ERR_WORKSPACE_TOO_SMALL before any launch.  The first call on a device
+ * looks up the array's device address (set-up, once per device, with that
+ * device current); make that first call before any stream capture.  Each call
+ * clears the array's counters on `stream` before its kernel.  All calls share
+ * the one array and it keeps the last call's contents, so calls that can
+ * overlap on the GPU (different streams, different host threads without
+ * ordering) race and give wrong results: order them on one stream.  No
+ * cudaMalloc, cudaFree or allocating library routine is called. */
+#define NVKV_NOALLOC_SCRATCH_BYTES (8u << 20)
+nvkv_status nvfp4_paged_decode_attention_noalloc(const void *q, const nvkv_cache *cache,
+                                                 const int32_t *block_table, int32_t max_pages,
+                                                 const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                                 int32_t layer_precision, float sm_scale, int32_t num_splits,
+                                                 void *out, void *stream);
+
 /* Chunked-extend prefix dequant into the shared FP8 workspace ([P2] Three
  * Paths: "the cached prefix is gathered out and dequantized into a cross-layer
  * shared FP8 workspace").  For i < n, tokens [0, prefix_lens[i]) of sequence

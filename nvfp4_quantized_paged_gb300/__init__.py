@@ -87,6 +87,8 @@ SIGNATURES = {
                                             _vp, _vp]),
     "fp8_paged_decode_attention": (_i32, [_vp, _cachep, _vp, _i32, _vp, _i32, _i32, _f32, _i32, _vp, _sz, _vp,
                                           _vp]),
+    "nvfp4_paged_decode_attention_noalloc": (_i32, [_vp, _cachep, _vp, _i32, _vp, _i32, _i32, _i32, _f32, _i32,
+                                                    _vp, _vp]),
     "nvfp4_kv_dequant_to_fp8_workspace": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _cachep, _vp, _vp, _vp, _i64,
                                                  _vp]),
     "nvkv_encode_e2m1": (_i32, [_vp, _i64, _vp, _vp]),
@@ -261,6 +263,18 @@ def fp8_paged_decode_attention(q, cache: Cache, block_table, seq_lens, out, work
                                             _ptr(seq_lens), q.shape[0], q.shape[1], sm_scale, num_splits,
                                             _ptr(workspace), workspace.numel() * workspace.element_size(),
                                             _ptr(out), _stream(stream)))
+
+
+def nvfp4_paged_decode_attention_noalloc(q, cache: Cache, block_table, seq_lens, layer_precision, out,
+                                         sm_scale=0.0, num_splits=0, stream=None):
+    """Decode attention with the library's fixed scratch array instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    d = cache.desc()
+    _check("nvfp4_paged_decode_attention_noalloc",
+           lib().nvfp4_paged_decode_attention_noalloc(_ptr(q), ctypes.byref(d), _ptr(block_table),
+                                                      block_table.shape[1], _ptr(seq_lens), q.shape[0], q.shape[1],
+                                                      layer_precision, sm_scale, num_splits, _ptr(out),
+                                                      _stream(stream)))
 
 
 def nvfp4_kv_dequant_to_fp8_workspace(block_table, seq_ids, prefix_lens, cu_prefix, cache: Cache, ws_scale, ws_k,

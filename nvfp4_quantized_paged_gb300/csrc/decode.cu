@@ -744,9 +744,61 @@ nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t 
 }  // namespace
 }  // namespace nvkv
 
+// Scratch of nvfp4_paged_decode_attention_noalloc: a fixed device array for
+// callers that cannot allocate (see the header).  Host code must not pass the
+// symbol itself to a kernel (it is a host-side stand-in); the device address
+// comes from cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) uint8_t nvkv_noalloc_scratch[NVKV_NOALLOC_SCRATCH_BYTES];
+
+namespace nvkv {
+namespace {
+
+struct NoAllocScratch {
+  void *ptr = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+NoAllocScratch g_noalloc[64];
+std::once_flag g_noalloc_once[64];
+
+// Device address of the scratch array on the current device (nullptr on failure).
+void *noalloc_scratch_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::call_once(g_noalloc_once[dev], [dev] {
+    g_noalloc[dev].err = cudaGetSymbolAddress(&g_noalloc[dev].ptr, nvkv_noalloc_scratch);
+    if (g_noalloc[dev].err != cudaSuccess) g_noalloc[dev].ptr = nullptr;
+  });
+  return g_noalloc[dev].ptr;
+}
+
+}  // namespace
+}  // namespace nvkv
+
 using namespace nvkv;
 
 extern "C" {
+
+nvkv_status nvfp4_paged_decode_attention_noalloc(const void *q, const nvkv_cache *cache,
+                                                 const int32_t *block_table, int32_t max_pages,
+                                                 const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                                 int32_t layer_precision, float sm_scale, int32_t num_splits,
+                                                 void *out, void *stream) {
+  if (!cache || layer_precision != cache->prec) return NVKV_ERR_INVALID_ARG;
+  if (layer_precision != NVKV_PREC_NVFP4 && layer_precision != NVKV_PREC_FP8_E4M3) return NVKV_ERR_INVALID_ARG;
+  nvkv_status st = check_cache(cache, layer_precision);
+  if (st != NVKV_OK) return st;
+  if (batch < 0 || batch > kMaxBatch) return batch < 0 ? NVKV_ERR_INVALID_ARG : NVKV_ERR_UNSUPPORTED;
+  if (batch == 0) return NVKV_OK;
+  void *scratch = noalloc_scratch_ptr();
+  if (!scratch) return NVKV_ERR_CUDA;
+  // the arrival counters must start at zero; the partial slots are always written before they are read
+  const size_t zero = counters_bytes(batch, cache->num_kv_heads);
+  if (zero > NVKV_NOALLOC_SCRATCH_BYTES) return NVKV_ERR_WORKSPACE_TOO_SMALL;
+  if (cudaMemsetAsync(scratch, 0, zero, static_cast<cudaStream_t>(stream)) != cudaSuccess) return NVKV_ERR_CUDA;
+  return decode_common(q, cache, block_table, max_pages, seq_lens, batch, num_q_heads, layer_precision, sm_scale,
+                       num_splits, scratch, NVKV_NOALLOC_SCRATCH_BYTES, out, stream);
+}
+
 
 size_t nvkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                   int32_t num_splits) {

@@ -1,0 +1,67 @@
+"""The allocation-free decode entry point.
+
+Some callers cannot give this library device memory for scratch: serving
+engines that hand all free HBM to their KV page pool at start-up and keep no
+allocator for per-call buffers, and plugin hosts that pass a kernel only its
+inputs and outputs.  For them nvfp4_paged_decode_attention_noalloc uses a
+fixed scratch array inside the library.  This test calls it through the C ABI
+twice in a row, on two different problems, and checks each output against the
+regular entry point (caller workspace) with the tolerance the parity tests
+use.  It also checks that a problem needing more scratch than the array holds
+is refused with the documented status.  The file is collected last so that a
+stop-at-first-failure run has already run every other test.
+"""
+import ctypes
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+def _layer(name, lens, P, Hq, Hkv, prec, seed):
+    from nvfp4_quantized_paged_gb300.runner import Layer
+    from nvfp4_quantized_paged_gb300.workloads import Spec, Workload
+    spec = Spec(name, B=len(lens), Hq=Hq, Hkv=Hkv, D=128, P=P, lens=tuple(lens), dist="element_outliers",
+                outlier_scale=20.0, outlier_p=0.01, step_write=0)
+    return Layer(Workload(spec, seed=seed, device="cuda"), 0, prec=prec)
+
+
+def _noalloc(nv, lay, out):
+    d = lay.cache.desc()
+    return nv.lib().nvfp4_paged_decode_attention_noalloc(
+        ctypes.c_void_p(lay.q.data_ptr()), ctypes.byref(d), ctypes.c_void_p(lay.block_table.data_ptr()),
+        lay.block_table.shape[1], ctypes.c_void_p(lay.seq_lens.data_ptr()), lay.q.shape[0], lay.q.shape[1],
+        lay.prec, 0.0, 0, ctypes.c_void_p(out.data_ptr()),
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row():
+    import nvfp4_quantized_paged_gb300 as nv
+    problems = [
+        _layer("noalloc_a", [3000, 1, 700, 64], 64, 32, 8, nv.PREC_NVFP4, 11),
+        _layer("noalloc_b", [129, 5000], 16, 16, 2, nv.PREC_FP8, 12),
+    ]
+    for lay in problems:
+        lay.decode()  # regular entry point, caller-owned workspace
+        want = lay.out.float().clone()
+        out = torch.full_like(lay.out, float("nan"))
+        assert _noalloc(nv, lay, out) == nv.NVKV_OK
+        torch.cuda.synchronize()
+        assert lay.cache.err.item() == 0
+        got = out.float()
+        assert torch.isfinite(got).all()
+        assert torch.all((got - want).abs() <= 2e-3 + 1e-2 * want.abs())
+
+
+def test_noalloc_refuses_problems_larger_than_its_scratch():
+    import nvfp4_quantized_paged_gb300 as nv
+    lay = _layer("noalloc_c", [8192, 8192], 64, 32, 8, nv.PREC_NVFP4, 13)
+    d = lay.cache.desc()
+    out = torch.empty_like(lay.out)
+    # 2 sequences x 8 KV heads x 100 splits -> 1600 CTAs x 2 partial slots of 4160 B = 13.3 MB > 8 MiB
+    st = nv.lib().nvfp4_paged_decode_attention_noalloc(
+        ctypes.c_void_p(lay.q.data_ptr()), ctypes.byref(d), ctypes.c_void_p(lay.block_table.data_ptr()),
+        lay.block_table.shape[1], ctypes.c_void_p(lay.seq_lens.data_ptr()), 2, 32, nv.PREC_NVFP4, 0.0, 100,
+        ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == nv.NVKV_ERR_WORKSPACE_TOO_SMALL
