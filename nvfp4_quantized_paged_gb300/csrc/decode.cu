@@ -91,7 +91,7 @@ constexpr int smem_bytes_for(int G) {
          + (kMaxBatch + 1) * 4                                 // tile prefix sums
          + kConsumerWarps * G * kD * 4                         // warp merge: o
          + kConsumerWarps * kMaxGroup * 2 * 4                  // warp merge: m, l
-         + 64;                                                 // flags
+         + 4 * (4 + 2 * Layout<PREC>::kStages);                // flags, fills, bcast, consumed
 }
 
 // Segment = run of consecutive units of one (sequence, KV head).
@@ -125,6 +125,22 @@ __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t W, int64_t NC) {
   return ((u + 1) * NC + W - 1) / W - 1;
 }
 
+// Bounded wait until *cnt >= want (a shared-memory counter another warp of
+// the CTA advances); false on abort or after ~2 s (then *abort is raised).
+__device__ __forceinline__ bool wait_consumed(volatile int *cnt, int want, volatile int *abort) {
+  if (*cnt >= want) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (*cnt >= want) return true;
+    if (*abort) return false;
+    if ((it & 255u) == 0 && global_timer_ns() - t0 > 2000000000ull) {
+      *abort = 1;
+      return false;
+    }
+    __nanosleep(32);
+  }
+}
+
 __device__ __forceinline__ int clamped_len(const DecodeArgs &a, int b) {
   const int64_t cap = static_cast<int64_t>(a.max_pages) * a.c.P;
   const int64_t L = a.seq_lens[b];
@@ -150,22 +166,34 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
     const Seg s = seg_at(u, u1, cum, a.B, Hkv);
     const int len = clamped_len(a, s.b);
     const int32_t *brow = a.block_table + static_cast<int64_t>(s.b) * a.max_pages;
+    // Block-table window: lane l holds the entry of page index wbase + l; the
+    // next window is requested as soon as the current one is in use, so its
+    // load latency hides behind 32 pages of copies.
+    int wbase = (s.t0 * kTile) / P;
+    int32_t pg = wbase + lane < a.max_pages ? brow[wbase + lane] : 0;
+    int32_t pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
     for (int t = s.t0; t < s.t1; ++t, ++i) {
       const int slot = static_cast<int>(i % Lay::kStages);
       const uint32_t fill = static_cast<uint32_t>(i / Lay::kStages);
-      if (*abort) return;
+      if (__any_sync(0xffffffffu, *abort)) return;
       if (lane == 0 && fill > 0) mbar_wait_bounded(&empty[slot], (fill - 1) & 1u, abort);
-      __syncwarp();
-      if (*abort) return;
+      if (__any_sync(0xffffffffu, *abort)) return;  // warp-uniform exit
       const int tok0 = t * kTile;
       const int ntok = min(kTile, len - tok0);
       const int nrun = (ntok + run - 1) / run;
+      if ((tok0 + ntok - 1) / P >= wbase + 32) {  // tile leaves the window (warp-uniform)
+        wbase += 32;
+        pg = pg_next;
+        pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
+      }
       if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nrun * run) * bytes_per_tok);
-      __syncwarp();
+      const int jl = lane / nplanes;
+      const int pidx = lane < nrun * nplanes ? (tok0 + jl * run) / P - wbase : 0;
+      const int64_t page_w = __shfl_sync(0xffffffffu, pg, pidx & 31);
       if (lane < nrun * nplanes) {
-        const int j = lane / nplanes, plane = lane % nplanes;
+        const int j = jl, plane = lane % nplanes;
         const int tok = tok0 + j * run;
-        int64_t page = brow[tok / P];
+        int64_t page = page_w;
         if (page < 0 || page >= a.c.num_pages) {
           set_err(a.c.err, NVKV_DEVERR_PAGE);
           page = 0;  // a valid address; the output of this sequence is then undefined
@@ -213,51 +241,80 @@ struct WarpState {
   float l[2];
 };
 
+// A fragments of MMA k-step s for rows (row0, row0 + 8): code bytes of the
+// two rows (16 each, d in [32c, 32c+32)) and, for NVFP4, the block scales of
+// blocks 2c and 2c+1 duplicated into f16x2 (lo = block 2c, hi = block 2c+1).
 template <int PREC>
-__device__ __forceinline__ void qk_subtile(const uint8_t *stage, int k, int r, int c, const uint32_t (&qf)[8][2],
-                                           float (&acc)[4]) {
+struct KRows {
+  uint32_t w0[PREC == NVKV_PREC_NVFP4 ? 4 : 8], w1[PREC == NVKV_PREC_NVFP4 ? 4 : 8];
+  uint32_t lo0, hi0, lo1, hi1;
+};
+
+template <int PREC>
+__device__ __forceinline__ void load_k_rows(const uint8_t *stage, int row0, int c, KRows<PREC> &kr) {
   using Lay = Layout<PREC>;
-  acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
-  const int row0 = 16 * k + r, row1 = row0 + 8;
+  const int row1 = row0 + 8;
   if constexpr (PREC == NVKV_PREC_NVFP4) {
     const uint4 c0 = *reinterpret_cast<const uint4 *>(stage + Lay::kKc + row0 * Lay::kRowBytes + 16 * c);
     const uint4 c1 = *reinterpret_cast<const uint4 *>(stage + Lay::kKc + row1 * Lay::kRowBytes + 16 * c);
+    kr.w0[0] = c0.x; kr.w0[1] = c0.y; kr.w0[2] = c0.z; kr.w0[3] = c0.w;
+    kr.w1[0] = c1.x; kr.w1[1] = c1.y; kr.w1[2] = c1.z; kr.w1[3] = c1.w;
     const uint32_t s0 = *reinterpret_cast<const uint16_t *>(stage + Lay::kKs + row0 * 8 + 2 * c);
     const uint32_t s1 = *reinterpret_cast<const uint16_t *>(stage + Lay::kKs + row1 * 8 + 2 * c);
     const uint32_t sc0 = f16x2_from_e4m3x2<0>(s0), sc1 = f16x2_from_e4m3x2<0>(s1);
-    const uint32_t lo0 = prmt(sc0, 0, 0x1010), hi0 = prmt(sc0, 0, 0x3232);  // {S_2c,S_2c}, {S_2c+1,S_2c+1}
-    const uint32_t lo1 = prmt(sc1, 0, 0x1010), hi1 = prmt(sc1, 0, 0x3232);
-    const uint32_t w0[4] = {c0.x, c0.y, c0.z, c0.w};
-    const uint32_t w1[4] = {c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const uint32_t m0 = s < 4 ? lo0 : hi0, m1 = s < 4 ? lo1 : hi1;
-      uint32_t a0, a1, a2, a3;
-      if ((s & 1) == 0) {
-        a0 = f16x2_from_e2m1x2<0>(w0[s >> 1]);
-        a2 = f16x2_from_e2m1x2<1>(w0[s >> 1]);
-        a1 = f16x2_from_e2m1x2<0>(w1[s >> 1]);
-        a3 = f16x2_from_e2m1x2<1>(w1[s >> 1]);
-      } else {
-        a0 = f16x2_from_e2m1x2<2>(w0[s >> 1]);
-        a2 = f16x2_from_e2m1x2<3>(w0[s >> 1]);
-        a1 = f16x2_from_e2m1x2<2>(w1[s >> 1]);
-        a3 = f16x2_from_e2m1x2<3>(w1[s >> 1]);
-      }
-      mma_f16_16816(acc, hmul2_u32(a0, m0), hmul2_u32(a1, m1), hmul2_u32(a2, m0), hmul2_u32(a3, m1), qf[s][0],
-                    qf[s][1]);
-    }
+    kr.lo0 = prmt(sc0, 0, 0x1010);  // {S_2c, S_2c}
+    kr.hi0 = prmt(sc0, 0, 0x3232);  // {S_2c+1, S_2c+1}
+    kr.lo1 = prmt(sc1, 0, 0x1010);
+    kr.hi1 = prmt(sc1, 0, 0x3232);
   } else {
     const uint4 *p0 = reinterpret_cast<const uint4 *>(stage + Lay::kKc + row0 * Lay::kRowBytes + 32 * c);
     const uint4 *p1 = reinterpret_cast<const uint4 *>(stage + Lay::kKc + row1 * Lay::kRowBytes + 32 * c);
     const uint4 x0 = p0[0], y0 = p0[1], x1 = p1[0], y1 = p1[1];
-    const uint32_t w0[8] = {x0.x, x0.y, x0.z, x0.w, y0.x, y0.y, y0.z, y0.w};
-    const uint32_t w1[8] = {x1.x, x1.y, x1.z, x1.w, y1.x, y1.y, y1.z, y1.w};
+    kr.w0[0] = x0.x; kr.w0[1] = x0.y; kr.w0[2] = x0.z; kr.w0[3] = x0.w;
+    kr.w0[4] = y0.x; kr.w0[5] = y0.y; kr.w0[6] = y0.z; kr.w0[7] = y0.w;
+    kr.w1[0] = x1.x; kr.w1[1] = x1.y; kr.w1[2] = x1.z; kr.w1[3] = x1.w;
+    kr.w1[4] = y1.x; kr.w1[5] = y1.y; kr.w1[6] = y1.z; kr.w1[7] = y1.w;
+  }
+}
+
+template <int PREC, int S>
+__device__ __forceinline__ void qk_step(const KRows<PREC> &kr, const uint32_t (&qf)[8][2], float (&acc)[4]) {
+  if constexpr (PREC == NVKV_PREC_NVFP4) {
+    const uint32_t m0 = S < 4 ? kr.lo0 : kr.hi0, m1 = S < 4 ? kr.lo1 : kr.hi1;
+    constexpr int B0 = (S & 1) ? 2 : 0, B1 = B0 + 1;
+    const uint32_t a0 = hmul2_u32(f16x2_from_e2m1x2<B0>(kr.w0[S >> 1]), m0);
+    const uint32_t a2 = hmul2_u32(f16x2_from_e2m1x2<B1>(kr.w0[S >> 1]), m0);
+    const uint32_t a1 = hmul2_u32(f16x2_from_e2m1x2<B0>(kr.w1[S >> 1]), m1);
+    const uint32_t a3 = hmul2_u32(f16x2_from_e2m1x2<B1>(kr.w1[S >> 1]), m1);
+    mma_f16_16816(acc, a0, a1, a2, a3, qf[S][0], qf[S][1]);
+  } else {
+    mma_f16_16816(acc, f16x2_from_e4m3x2<0>(kr.w0[S]), f16x2_from_e4m3x2<0>(kr.w1[S]),
+                  f16x2_from_e4m3x2<1>(kr.w0[S]), f16x2_from_e4m3x2<1>(kr.w1[S]), qf[S][0], qf[S][1]);
+  }
+}
+
+// Scores of sub-tiles k0 and k0+1 (tokens 16k + r, 16k + r + 8): four
+// independent MMA chains (two sub-tiles x even/odd k-steps) instead of one.
+template <int PREC>
+__device__ __forceinline__ void qk_pair(const uint8_t *stage, int k0, int r, int c, const uint32_t (&qf)[8][2],
+                                        float (&xa)[4], float (&xb)[4]) {
+  KRows<PREC> ka, kb;
+  load_k_rows<PREC>(stage, 16 * k0 + r, c, ka);
+  load_k_rows<PREC>(stage, 16 * (k0 + 1) + r, c, kb);
+  float ea[4] = {0.f, 0.f, 0.f, 0.f}, oa[4] = {0.f, 0.f, 0.f, 0.f};
+  float eb[4] = {0.f, 0.f, 0.f, 0.f}, ob[4] = {0.f, 0.f, 0.f, 0.f};
+  qk_step<PREC, 0>(ka, qf, ea); qk_step<PREC, 0>(kb, qf, eb);
+  qk_step<PREC, 1>(ka, qf, oa); qk_step<PREC, 1>(kb, qf, ob);
+  qk_step<PREC, 2>(ka, qf, ea); qk_step<PREC, 2>(kb, qf, eb);
+  qk_step<PREC, 3>(ka, qf, oa); qk_step<PREC, 3>(kb, qf, ob);
+  qk_step<PREC, 4>(ka, qf, ea); qk_step<PREC, 4>(kb, qf, eb);
+  qk_step<PREC, 5>(ka, qf, oa); qk_step<PREC, 5>(kb, qf, ob);
+  qk_step<PREC, 6>(ka, qf, ea); qk_step<PREC, 6>(kb, qf, eb);
+  qk_step<PREC, 7>(ka, qf, oa); qk_step<PREC, 7>(kb, qf, ob);
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      mma_f16_16816(acc, f16x2_from_e4m3x2<0>(w0[s]), f16x2_from_e4m3x2<0>(w1[s]), f16x2_from_e4m3x2<1>(w0[s]),
-                    f16x2_from_e4m3x2<1>(w1[s]), qf[s][0], qf[s][1]);
-    }
+  for (int e = 0; e < 4; ++e) {
+    xa[e] = ea[e] + oa[e];
+    xb[e] = eb[e] + ob[e];
   }
 }
 
@@ -332,9 +389,10 @@ template <int PREC>
 __device__ __forceinline__ void consume_tile(const uint8_t *stage, int nvalid, int r, int c,
                                              const uint32_t (&qf)[8][2], const float (&cs)[2], WarpState &st) {
   float x[4][4];
+  qk_pair<PREC>(stage, 0, r, c, qf, x[0], x[1]);
+  qk_pair<PREC>(stage, 2, r, c, qf, x[2], x[3]);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    qk_subtile<PREC>(stage, k, r, c, qf, x[k]);
     x[k][0] *= cs[0];
     x[k][1] *= cs[1];
     x[k][2] *= cs[0];
@@ -396,8 +454,9 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
   float *mrg_ml = mrg_o + kConsumerWarps * a.G * kD;
   int *flags = reinterpret_cast<int *>(mrg_ml + kConsumerWarps * kMaxGroup * 2);
   volatile int *abort = flags;  // flags[0]
-  int *fills = flags + 1;       // flags[1 .. kStages]
-  int *bcast = flags + 1 + Lay::kStages;
+  int *fills = flags + 1;       // flags[1 .. kStages]: fills issued per slot
+  int *bcast = flags + 1 + Lay::kStages;            // 3 ints
+  volatile int *consumed = flags + 4 + Lay::kStages;  // kStages ints: fills consumed per slot
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = a.c.Hkv, B = a.B, G = a.G;
@@ -410,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
       fills[s] = 0;
+      consumed[s] = 0;
     }
     fence_mbar_init();
   }
@@ -519,13 +579,22 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
         if (static_cast<int>(gi % kConsumerWarps) != warp) continue;
         const int slot = static_cast<int>(gi % Lay::kStages);
         const uint32_t fill = static_cast<uint32_t>(gi / Lay::kStages);
-        if (mbar_wait_bounded(&full[slot], fill & 1u, abort)) {
+        // Consecutive fills of a slot go to different warps.  Wait until the
+        // slot's previous fill has been consumed: only then is the fill this
+        // warp needs the slot's current phase, so the parity wait below
+        // cannot match an older completed phase.
+        bool ready = wait_consumed(consumed + slot, static_cast<int>(fill), abort);
+        ready = ready && mbar_wait_bounded(&full[slot], fill & 1u, abort);
+        if (__all_sync(0xffffffffu, ready)) {  // warp-uniform: the MMAs below are .aligned
           const int64_t rem = Lb - static_cast<int64_t>(s.t0 + k) * kTile;
           const int nvalid = rem < kTile ? static_cast<int>(rem) : kTile;
           consume_tile<PREC>(ring + static_cast<size_t>(slot) * Lay::kStageBytes, nvalid, r, c, qf, cs, st);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (lane == 0) {
+          mbar_arrive(&empty[slot]);
+          consumed[slot] = static_cast<int>(fill) + 1;
+        }
       }
       i += ntiles;
 
@@ -798,7 +867,6 @@ nvkv_status nvfp4_paged_decode_attention_noalloc(const void *q, const nvkv_cache
   return decode_common(q, cache, block_table, max_pages, seq_lens, batch, num_q_heads, layer_precision, sm_scale,
                        num_splits, scratch, NVKV_NOALLOC_SCRATCH_BYTES, out, stream);
 }
-
 
 size_t nvkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                   int32_t num_splits) {
