@@ -28,13 +28,16 @@
  *   codes 0.  FP8 layers: s8 = amax / 448, byte = E4M3_rne_satfinite(x / s8),
  *   s8 == 0 -> byte 0.
  *
- * Cache layout (one layer; every pointer is device memory owned by the caller):
- *   NVFP4: k_data, v_data   [num_pages][num_kv_heads][page_size][head_dim/2]
- *          k_scale, v_scale [num_pages][num_kv_heads][page_size][head_dim/16]
- *   FP8:   k_data, v_data   [num_pages][num_kv_heads][page_size][head_dim]
- *   A token at slot s lives at page s / page_size, offset s % page_size.
- *   Supported: head_dim 128; page_size 16, 32, 64 or 128; every pointer
- *   16-byte aligned.  Anything else -> NVKV_ERR_UNSUPPORTED.
+ * Cache layout (one layer, device memory owned by the caller): one contiguous
+ * block per (page, KV head), pages outermost: data[num_pages][num_kv_heads][block]
+ *   NVFP4 block (P * 144 bytes at head_dim 128, P = page_size):
+ *     [K codes P x D/2 | K scales P x D/16 | V codes P x D/2 | V scales P x D/16]
+ *   FP8 block (P * 256 bytes): [K P x D | V P x D]
+ * Row `off` of a plane holds the token at page offset `off`; a token at slot s
+ * lives at page s / P, offset s % P.  A page of one KV head is therefore one
+ * contiguous run of bytes, which decode fetches with a single bulk copy.
+ *   Supported: head_dim 128; page_size 16, 32 or 64; every pointer 16-byte
+ *   aligned.  Anything else -> NVKV_ERR_UNSUPPORTED.
  *
  * Conventions.  Every call is asynchronous on `stream` (a cudaStream_t, NULL
  * = the legacy default stream) and returns after launching.  Argument errors
@@ -83,8 +86,7 @@ typedef struct {
   int32_t num_kv_heads;
   int32_t head_dim;
   int32_t reserved;
-  uint8_t *k_data, *v_data;    /* codes (NVFP4) or E4M3 bytes (FP8)            */
-  uint8_t *k_scale, *v_scale;  /* E4M3 block scales (NVFP4); NULL for FP8      */
+  uint8_t *data;               /* [num_pages][num_kv_heads][block], see above  */
   const float *kv_scale;       /* device float[2] {K, V}: NVFP4 global g, FP8 s8 */
   int32_t *err_flag;           /* optional device int32, 0 = no error          */
 } nvkv_cache;

@@ -58,10 +58,7 @@ class nvkv_cache(ctypes.Structure):
         ("num_kv_heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32),
         ("reserved", ctypes.c_int32),
-        ("k_data", ctypes.c_void_p),
-        ("v_data", ctypes.c_void_p),
-        ("k_scale", ctypes.c_void_p),
-        ("v_scale", ctypes.c_void_p),
+        ("data", ctypes.c_void_p),
         ("kv_scale", ctypes.c_void_p),
         ("err_flag", ctypes.c_void_p),
     ]
@@ -151,26 +148,34 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 class Cache:
-    """One layer's paged cache planes in device memory (head-major in a page).
+    """One layer's paged cache in device memory: one contiguous block per
+    (page, KV head), ``data`` uint8 [num_pages, Hkv, block].
 
-    NVFP4: k_data/v_data uint8 [num_pages, Hkv, P, 64], k_scale/v_scale uint8
-    [num_pages, Hkv, P, 8].  FP8: k_data/v_data uint8 [num_pages, Hkv, P, 128].
-    ``kv_scale`` float32[2] (K, V): the NVFP4 global scales or FP8 per-tensor
-    scales.  ``err`` int32[1]: device error word (0 = none).
+    NVFP4 block = [K codes P x 64 | K scales P x 8 | V codes P x 64 |
+    V scales P x 8] (P * 144 bytes); FP8 block = [K P x 128 | V P x 128].
+    ``k_data``/``k_scale``/``v_data``/``v_scale`` are views of the planes
+    shaped [num_pages, Hkv, P, 64] / [num_pages, Hkv, P, 8] (FP8:
+    [num_pages, Hkv, P, 128], no scales).  ``kv_scale`` float32[2] (K, V): the
+    NVFP4 global scales or FP8 per-tensor scales.  ``err`` int32[1]: device
+    error word (0 = none).
     """
 
     def __init__(self, prec: int, num_pages: int, num_kv_heads: int, page_size: int, device="cuda",
                  head_dim: int = HEAD_DIM, kv_scale: Optional[torch.Tensor] = None):
         self.prec, self.num_pages, self.Hkv, self.P, self.D = prec, num_pages, num_kv_heads, page_size, head_dim
-        u8 = dict(dtype=torch.uint8, device=device)
+        P, D = page_size, head_dim
         if prec == PREC_NVFP4:
-            self.k_data = torch.zeros(num_pages, num_kv_heads, page_size, head_dim // 2, **u8)
-            self.v_data = torch.zeros(num_pages, num_kv_heads, page_size, head_dim // 2, **u8)
-            self.k_scale = torch.zeros(num_pages, num_kv_heads, page_size, head_dim // 16, **u8)
-            self.v_scale = torch.zeros(num_pages, num_kv_heads, page_size, head_dim // 16, **u8)
+            half = P * (D // 2 + D // 16)
+            self.data = torch.zeros(num_pages, num_kv_heads, 2 * half, dtype=torch.uint8, device=device)
+            cs = P * (D // 2)
+            self.k_data = self.data[:, :, :cs].unflatten(-1, (P, D // 2))
+            self.k_scale = self.data[:, :, cs:half].unflatten(-1, (P, D // 16))
+            self.v_data = self.data[:, :, half:half + cs].unflatten(-1, (P, D // 2))
+            self.v_scale = self.data[:, :, half + cs:].unflatten(-1, (P, D // 16))
         else:
-            self.k_data = torch.zeros(num_pages, num_kv_heads, page_size, head_dim, **u8)
-            self.v_data = torch.zeros(num_pages, num_kv_heads, page_size, head_dim, **u8)
+            self.data = torch.zeros(num_pages, num_kv_heads, 2 * P * D, dtype=torch.uint8, device=device)
+            self.k_data = self.data[:, :, :P * D].unflatten(-1, (P, D))
+            self.v_data = self.data[:, :, P * D:].unflatten(-1, (P, D))
             self.k_scale = self.v_scale = None
         self.kv_scale = kv_scale if kv_scale is not None else torch.zeros(2, dtype=torch.float32, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
@@ -179,19 +184,14 @@ class Cache:
         d = nvkv_cache()
         d.prec, d.num_pages, d.page_size, d.num_kv_heads, d.head_dim = (self.prec, self.num_pages, self.P, self.Hkv,
                                                                          self.D)
-        d.k_data, d.v_data = self.k_data.data_ptr(), self.v_data.data_ptr()
-        d.k_scale = self.k_scale.data_ptr() if self.k_scale is not None else None
-        d.v_scale = self.v_scale.data_ptr() if self.v_scale is not None else None
+        d.data = self.data.data_ptr()
         d.kv_scale = self.kv_scale.data_ptr()
         d.err_flag = self.err.data_ptr()
         return d
 
     @property
     def nbytes(self) -> int:
-        n = self.k_data.numel() + self.v_data.numel()
-        if self.k_scale is not None:
-            n += self.k_scale.numel() + self.v_scale.numel()
-        return n
+        return self.data.numel()
 
 
 # ---------------------------------------------------------------------------

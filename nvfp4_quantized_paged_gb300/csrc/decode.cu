@@ -13,20 +13,23 @@
 //     last-arriving CTA merges with the log-sum-exp rule (no second kernel,
 //     no spin: an atomic arrival counter).
 //   * One producer warp streams tiles into a shared-memory ring with 1-D bulk
-//     copies (cp.async.bulk + mbarrier transaction counts): per page run, the
-//     K codes, K scales, V codes and V scales planes (NVFP4: 144 B per token
-//     and KV head) or the two E4M3 planes (FP8: 256 B).  An L2 evict-first
-//     hint keeps the streamed cache from flushing reused data.
-//   * Four consumer warps each own whole tiles.  E2M1 pairs become f16x2 with
-//     one cvt.rn.f16x2.e2m1x2 and are scaled by their E4M3 block scale with
-//     one f16x2 multiply; code * scale has at most 6 significant bits and lies
-//     in [2^-10, 2688], so it is exact in FP16.  Scores and P.V run on the
-//     tensor cores as m16n8k16 FP16 MMAs with FP32 accumulation: tokens form
-//     M, the GQA query group (<= 8 heads) forms N.  The global scale g_K,
-//     sm_scale, log2(e) and a per-head power of two that brings the BF16
-//     query into FP16 range are folded into one FP32 factor per score; g_V is
-//     applied once to the output.  Online softmax in FP32 with exp2 and a
-//     lazily raised running max (rescale only when the max grows by > 2^8).
+//     copies (cp.async.bulk + mbarrier transaction counts).  The cache keeps
+//     each (page, KV head) as one contiguous block, so a 64-token tile is one
+//     9216-byte copy at page size 64 (NVFP4; 16 KB for FP8), or 64/P copies of
+//     whole page blocks.  Block-table entries are fetched 32 at a time, one
+//     window ahead.  An L2 evict-first hint marks the stream.
+//   * Four consumer warps share every tile: warp w takes tokens [16w, 16w+16),
+//     copies its slice into registers and releases the stage at once, so the
+//     ring stays almost entirely in flight while the warps compute.
+//   * E2M1 pairs become f16x2 with one cvt.rn.f16x2.e2m1x2 and are scaled by
+//     their E4M3 block scale with one f16x2 multiply; code * scale has at most
+//     6 significant bits and lies in [2^-10, 2688], so it is exact in FP16.
+//     Scores and P.V run on the tensor cores as m16n8k16 FP16 MMAs with FP32
+//     accumulation: tokens form M, the GQA query group (<= 8 heads) forms N.
+//     g_K, sm_scale, log2(e) and a per-head power of two that brings the BF16
+//     query into FP16 range form one FP32 factor per score; g_V is applied
+//     once to the output.  Online softmax in FP32 with exp2 and a lazily raised
+//     running max (rescale only when the max grows by more than 2^8).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -40,7 +43,8 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kTile = 64;          // tokens per work unit / ring stage
-constexpr int kConsumerWarps = 4;
+constexpr int kSub = 16;           // tokens per consumer warp per stage
+constexpr int kConsumerWarps = kTile / kSub;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxBatch = 1024;    // sequences per call (prefix sums live in shared memory)
 constexpr int kMaxGroup = 8;       // query heads per KV head (MMA N)
@@ -51,21 +55,15 @@ template <int PREC>
 struct Layout;
 template <>
 struct Layout<NVKV_PREC_NVFP4> {
-  static constexpr int kRowBytes = kD / 2;
-  static constexpr int kKc = 0;
-  static constexpr int kKs = kKc + kTile * kRowBytes;
-  static constexpr int kVc = kKs + kTile * (kD / 16);
-  static constexpr int kVs = kVc + kTile * kRowBytes;
-  static constexpr int kStageBytes = kVs + kTile * (kD / 16);  // 9216
+  static constexpr int kTokBytes = kNvTokBytes;                // 144
+  static constexpr int kStageBytes = kTile * kTokBytes;        // 9216
   static constexpr int kStages = 6;
   static constexpr int kMinBlocks = 3;
 };
 template <>
 struct Layout<NVKV_PREC_FP8_E4M3> {
-  static constexpr int kRowBytes = kD;
-  static constexpr int kKc = 0;
-  static constexpr int kVc = kTile * kRowBytes;
-  static constexpr int kStageBytes = 2 * kTile * kRowBytes;  // 16384
+  static constexpr int kTokBytes = kF8TokBytes;                // 256
+  static constexpr int kStageBytes = kTile * kTokBytes;        // 16384
   static constexpr int kStages = 6;
   static constexpr int kMinBlocks = 2;
 };
@@ -91,7 +89,7 @@ constexpr int smem_bytes_for(int G) {
          + (kMaxBatch + 1) * 4                                 // tile prefix sums
          + kConsumerWarps * G * kD * 4                         // warp merge: o
          + kConsumerWarps * kMaxGroup * 2 * 4                  // warp merge: m, l
-         + 4 * (4 + 2 * Layout<PREC>::kStages);                // flags, fills, bcast, consumed
+         + 4 * (4 + Layout<PREC>::kStages);                    // abort, fills, bcast
 }
 
 // Segment = run of consecutive units of one (sequence, KV head).
@@ -125,22 +123,6 @@ __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t W, int64_t NC) {
   return ((u + 1) * NC + W - 1) / W - 1;
 }
 
-// Bounded wait until *cnt >= want (a shared-memory counter another warp of
-// the CTA advances); false on abort or after ~2 s (then *abort is raised).
-__device__ __forceinline__ bool wait_consumed(volatile int *cnt, int want, volatile int *abort) {
-  if (*cnt >= want) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (*cnt >= want) return true;
-    if (*abort) return false;
-    if ((it & 255u) == 0 && global_timer_ns() - t0 > 2000000000ull) {
-      *abort = 1;
-      return false;
-    }
-    __nanosleep(32);
-  }
-}
-
 __device__ __forceinline__ int clamped_len(const DecodeArgs &a, int b) {
   const int64_t cap = static_cast<int64_t>(a.max_pages) * a.c.P;
   const int64_t L = a.seq_lens[b];
@@ -148,8 +130,8 @@ __device__ __forceinline__ int clamped_len(const DecodeArgs &a, int b) {
 }
 
 // ---------------------------------------------------------------------------
-// Producer warp: bulk copies of the tiles of this CTA's share into the ring.
-// Lane j*nplanes + plane copies plane `plane` of page run j of the tile.
+// Producer warp: one bulk copy per page block of each tile of this CTA's
+// share (a tile spans 64 / P whole page blocks).  Lane j copies block j.
 // ---------------------------------------------------------------------------
 template <int PREC>
 __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uint64_t *empty, const int32_t *cum,
@@ -158,17 +140,14 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
   const int lane = threadIdx.x & 31;
   const int Hkv = a.c.Hkv, P = a.c.P;
   const uint64_t policy = policy_evict_first();
-  constexpr int nplanes = (PREC == NVKV_PREC_NVFP4) ? 4 : 2;
-  constexpr uint32_t bytes_per_tok = (PREC == NVKV_PREC_NVFP4) ? 144u : 256u;
-  const int run = P < kTile ? P : kTile;  // tokens per copy
-  int64_t i = 0;                          // stage counter
+  const uint32_t block_bytes = static_cast<uint32_t>(P) * Lay::kTokBytes;
+  int64_t i = 0;  // stage counter
   for (int64_t u = u0; u < u1;) {
     const Seg s = seg_at(u, u1, cum, a.B, Hkv);
     const int len = clamped_len(a, s.b);
     const int32_t *brow = a.block_table + static_cast<int64_t>(s.b) * a.max_pages;
     // Block-table window: lane l holds the entry of page index wbase + l; the
-    // next window is requested as soon as the current one is in use, so its
-    // load latency hides behind 32 pages of copies.
+    // next window is requested when the current one comes into use.
     int wbase = (s.t0 * kTile) / P;
     int32_t pg = wbase + lane < a.max_pages ? brow[wbase + lane] : 0;
     int32_t pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
@@ -180,45 +159,23 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
       if (__any_sync(0xffffffffu, *abort)) return;  // warp-uniform exit
       const int tok0 = t * kTile;
       const int ntok = min(kTile, len - tok0);
-      const int nrun = (ntok + run - 1) / run;
-      if ((tok0 + ntok - 1) / P >= wbase + 32) {  // tile leaves the window (warp-uniform)
+      const int nblk = (ntok + P - 1) / P;  // page blocks holding the tile's tokens
+      if ((tok0 + ntok - 1) / P >= wbase + 32) {  // the tile leaves the window (warp-uniform)
         wbase += 32;
         pg = pg_next;
         pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nrun * run) * bytes_per_tok);
-      const int jl = lane / nplanes;
-      const int pidx = lane < nrun * nplanes ? (tok0 + jl * run) / P - wbase : 0;
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nblk) * block_bytes);
+      const int pidx = lane < nblk ? tok0 / P + lane - wbase : 0;
       const int64_t page_w = __shfl_sync(0xffffffffu, pg, pidx & 31);
-      if (lane < nrun * nplanes) {
-        const int j = jl, plane = lane % nplanes;
-        const int tok = tok0 + j * run;
+      if (lane < nblk) {
         int64_t page = page_w;
         if (page < 0 || page >= a.c.num_pages) {
           set_err(a.c.err, NVKV_DEVERR_PAGE);
           page = 0;  // a valid address; the output of this sequence is then undefined
         }
-        const int64_t row = (page * Hkv + s.h) * P + tok % P;
-        uint8_t *stage = ring + static_cast<size_t>(slot) * Lay::kStageBytes;
-        if constexpr (PREC == NVKV_PREC_NVFP4) {
-          const uint8_t *src;
-          uint8_t *dst;
-          uint32_t nb;
-          if (plane == 0) {
-            src = a.c.kd + row * (kD / 2); dst = stage + Lay::kKc + j * run * (kD / 2); nb = run * (kD / 2);
-          } else if (plane == 1) {
-            src = a.c.ks + row * (kD / 16); dst = stage + Lay::kKs + j * run * (kD / 16); nb = run * (kD / 16);
-          } else if (plane == 2) {
-            src = a.c.vd + row * (kD / 2); dst = stage + Lay::kVc + j * run * (kD / 2); nb = run * (kD / 2);
-          } else {
-            src = a.c.vs + row * (kD / 16); dst = stage + Lay::kVs + j * run * (kD / 16); nb = run * (kD / 16);
-          }
-          bulk_g2s(dst, src, nb, &full[slot], policy);
-        } else {
-          const uint8_t *src = (plane == 0 ? a.c.kd : a.c.vd) + row * kD;
-          uint8_t *dst = stage + (plane == 0 ? Lay::kKc : Lay::kVc) + j * run * kD;
-          bulk_g2s(dst, src, static_cast<uint32_t>(run * kD), &full[slot], policy);
-        }
+        bulk_g2s(ring + static_cast<size_t>(slot) * Lay::kStageBytes + static_cast<size_t>(lane) * block_bytes,
+                 a.c.data + a.c.block(page, s.h, Lay::kTokBytes), block_bytes, &full[slot], policy);
       }
       if (lane == 0) fills[slot] = static_cast<int>(fill) + 1;
     }
@@ -227,13 +184,13 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
 }
 
 // ---------------------------------------------------------------------------
-// Consumer warps.  Lane = 4r + c.  Scores: MMA rows = tokens 16k + r, 16k + r + 8
-// of sub-tile k; head_dim order inside one MMA k-step s is permuted so that a
-// thread reads 16 contiguous code bytes (d in [32c, 32c+32), step s covers
-// d = 32c + 4s + {0,1,2,3}); the query fragment uses the same order.  P.V:
-// MMA rows = head_dim (thread r owns block r: d in [16r, 16r+16)), k = tokens
-// 16k + {2c, 2c+1, 2c+8, 2c+9}, n = query head.  O for heads 2c, 2c+1 of the
-// group and d in [16r, 16r+16) stays in 32 FP32 registers.
+// Consumer warps.  Lane = 4r + c.  Warp w owns tokens [16w, 16w+16) of every
+// stage.  Scores: MMA rows = tokens r, r + 8 of the slice; head_dim order
+// inside one MMA k-step s is permuted so that a thread reads 16 contiguous code
+// bytes (d in [32c, 32c+32), step s covers d = 32c + 4s + {0,1,2,3}); the
+// query fragment uses the same order.  P.V: MMA rows = head_dim (thread r owns
+// d in [16r, 16r+16)), k = tokens 2c, 2c+1, 2c+8, 2c+9, n = query head.  O for
+// heads 2c, 2c+1 of the group and d in [16r, 16r+16) lives in 32 registers.
 // ---------------------------------------------------------------------------
 struct WarpState {
   float o[8][4];
@@ -241,80 +198,92 @@ struct WarpState {
   float l[2];
 };
 
-// A fragments of MMA k-step s for rows (row0, row0 + 8): code bytes of the
-// two rows (16 each, d in [32c, 32c+32)) and, for NVFP4, the block scales of
-// blocks 2c and 2c+1 duplicated into f16x2 (lo = block 2c, hi = block 2c+1).
+// Offsets of a warp's slice inside a stage (block layout of the header).
 template <int PREC>
-struct KRows {
-  uint32_t w0[PREC == NVKV_PREC_NVFP4 ? 4 : 8], w1[PREC == NVKV_PREC_NVFP4 ? 4 : 8];
-  uint32_t lo0, hi0, lo1, hi1;
+struct SliceOffsets {
+  int kc, ks, vc, vs;  // row 0 of K codes, K scales, V codes, V scales (NVFP4); kc, vc for FP8
+  __device__ SliceOffsets(int warp, int P) {
+    const int blk = (kSub * warp) / P, row0 = (kSub * warp) % P;
+    const int base = blk * P * Layout<PREC>::kTokBytes;
+    if constexpr (PREC == NVKV_PREC_NVFP4) {
+      kc = base + row0 * kNvCodeRow;
+      ks = base + P * kNvCodeRow + row0 * kNvScaleRow;
+      vc = base + P * (kNvCodeRow + kNvScaleRow) + row0 * kNvCodeRow;
+      vs = base + P * (2 * kNvCodeRow + kNvScaleRow) + row0 * kNvScaleRow;
+    } else {
+      kc = base + row0 * kF8Row;
+      vc = base + P * kF8Row + row0 * kF8Row;
+      ks = vs = 0;
+    }
+  }
+};
+
+// A warp's 16-token slice, copied out of the stage.
+template <int PREC>
+struct Slice {
+  uint32_t k0[PREC == NVKV_PREC_NVFP4 ? 4 : 8], k1[PREC == NVKV_PREC_NVFP4 ? 4 : 8];  // K rows r, r+8
+  uint32_t ks0, ks1;                                                                 // their scales (NVFP4)
+  uint32_t va[PREC == NVKV_PREC_NVFP4 ? 2 : 4], vb[PREC == NVKV_PREC_NVFP4 ? 2 : 4];  // V tokens 2c, 2c+1
+  uint32_t vc[PREC == NVKV_PREC_NVFP4 ? 2 : 4], vd[PREC == NVKV_PREC_NVFP4 ? 2 : 4];  // V tokens 2c+8, 2c+9
+  uint32_t vsc;                                                                      // 4 V scale bytes
 };
 
 template <int PREC>
-__device__ __forceinline__ void load_k_rows(const uint8_t *stage, int row0, int c, KRows<PREC> &kr) {
-  using Lay = Layout<PREC>;
-  const int row1 = row0 + 8;
+__device__ __forceinline__ void load_slice(const uint8_t *stage, const SliceOffsets<PREC> &o, int r, int c,
+                                           Slice<PREC> &x) {
   if constexpr (PREC == NVKV_PREC_NVFP4) {
-    const uint4 c0 = *reinterpret_cast<const uint4 *>(stage + Lay::kKc + row0 * Lay::kRowBytes + 16 * c);
-    const uint4 c1 = *reinterpret_cast<const uint4 *>(stage + Lay::kKc + row1 * Lay::kRowBytes + 16 * c);
-    kr.w0[0] = c0.x; kr.w0[1] = c0.y; kr.w0[2] = c0.z; kr.w0[3] = c0.w;
-    kr.w1[0] = c1.x; kr.w1[1] = c1.y; kr.w1[2] = c1.z; kr.w1[3] = c1.w;
-    const uint32_t s0 = *reinterpret_cast<const uint16_t *>(stage + Lay::kKs + row0 * 8 + 2 * c);
-    const uint32_t s1 = *reinterpret_cast<const uint16_t *>(stage + Lay::kKs + row1 * 8 + 2 * c);
-    const uint32_t sc0 = f16x2_from_e4m3x2<0>(s0), sc1 = f16x2_from_e4m3x2<0>(s1);
-    kr.lo0 = prmt(sc0, 0, 0x1010);  // {S_2c, S_2c}
-    kr.hi0 = prmt(sc0, 0, 0x3232);  // {S_2c+1, S_2c+1}
-    kr.lo1 = prmt(sc1, 0, 0x1010);
-    kr.hi1 = prmt(sc1, 0, 0x3232);
+    const uint4 a = *reinterpret_cast<const uint4 *>(stage + o.kc + r * kNvCodeRow + 16 * c);
+    const uint4 b = *reinterpret_cast<const uint4 *>(stage + o.kc + (r + 8) * kNvCodeRow + 16 * c);
+    x.k0[0] = a.x; x.k0[1] = a.y; x.k0[2] = a.z; x.k0[3] = a.w;
+    x.k1[0] = b.x; x.k1[1] = b.y; x.k1[2] = b.z; x.k1[3] = b.w;
+    x.ks0 = *reinterpret_cast<const uint16_t *>(stage + o.ks + r * kNvScaleRow + 2 * c);
+    x.ks1 = *reinterpret_cast<const uint16_t *>(stage + o.ks + (r + 8) * kNvScaleRow + 2 * c);
+    const int tA = 2 * c;
+    const uint2 A = *reinterpret_cast<const uint2 *>(stage + o.vc + tA * kNvCodeRow + 8 * r);
+    const uint2 B = *reinterpret_cast<const uint2 *>(stage + o.vc + (tA + 1) * kNvCodeRow + 8 * r);
+    const uint2 C = *reinterpret_cast<const uint2 *>(stage + o.vc + (tA + 8) * kNvCodeRow + 8 * r);
+    const uint2 D = *reinterpret_cast<const uint2 *>(stage + o.vc + (tA + 9) * kNvCodeRow + 8 * r);
+    x.va[0] = A.x; x.va[1] = A.y; x.vb[0] = B.x; x.vb[1] = B.y;
+    x.vc[0] = C.x; x.vc[1] = C.y; x.vd[0] = D.x; x.vd[1] = D.y;
+    const uint8_t *vs = stage + o.vs + r;
+    x.vsc = static_cast<uint32_t>(vs[tA * kNvScaleRow]) | (static_cast<uint32_t>(vs[(tA + 1) * kNvScaleRow]) << 8) |
+            (static_cast<uint32_t>(vs[(tA + 8) * kNvScaleRow]) << 16) |
+            (static_cast<uint32_t>(vs[(tA + 9) * kNvScaleRow]) << 24);
   } else {
-    const uint4 *p0 = reinterpret_cast<const uint4 *>(stage + Lay::kKc + row0 * Lay::kRowBytes + 32 * c);
-    const uint4 *p1 = reinterpret_cast<const uint4 *>(stage + Lay::kKc + row1 * Lay::kRowBytes + 32 * c);
-    const uint4 x0 = p0[0], y0 = p0[1], x1 = p1[0], y1 = p1[1];
-    kr.w0[0] = x0.x; kr.w0[1] = x0.y; kr.w0[2] = x0.z; kr.w0[3] = x0.w;
-    kr.w0[4] = y0.x; kr.w0[5] = y0.y; kr.w0[6] = y0.z; kr.w0[7] = y0.w;
-    kr.w1[0] = x1.x; kr.w1[1] = x1.y; kr.w1[2] = x1.z; kr.w1[3] = x1.w;
-    kr.w1[4] = y1.x; kr.w1[5] = y1.y; kr.w1[6] = y1.z; kr.w1[7] = y1.w;
+    const uint4 *p0 = reinterpret_cast<const uint4 *>(stage + o.kc + r * kF8Row + 32 * c);
+    const uint4 *p1 = reinterpret_cast<const uint4 *>(stage + o.kc + (r + 8) * kF8Row + 32 * c);
+    const uint4 a0 = p0[0], a1 = p0[1], b0 = p1[0], b1 = p1[1];
+    x.k0[0] = a0.x; x.k0[1] = a0.y; x.k0[2] = a0.z; x.k0[3] = a0.w;
+    x.k0[4] = a1.x; x.k0[5] = a1.y; x.k0[6] = a1.z; x.k0[7] = a1.w;
+    x.k1[0] = b0.x; x.k1[1] = b0.y; x.k1[2] = b0.z; x.k1[3] = b0.w;
+    x.k1[4] = b1.x; x.k1[5] = b1.y; x.k1[6] = b1.z; x.k1[7] = b1.w;
+    const int tA = 2 * c;
+    const uint4 A = *reinterpret_cast<const uint4 *>(stage + o.vc + tA * kF8Row + 16 * r);
+    const uint4 B = *reinterpret_cast<const uint4 *>(stage + o.vc + (tA + 1) * kF8Row + 16 * r);
+    const uint4 C = *reinterpret_cast<const uint4 *>(stage + o.vc + (tA + 8) * kF8Row + 16 * r);
+    const uint4 D = *reinterpret_cast<const uint4 *>(stage + o.vc + (tA + 9) * kF8Row + 16 * r);
+    x.va[0] = A.x; x.va[1] = A.y; x.va[2] = A.z; x.va[3] = A.w;
+    x.vb[0] = B.x; x.vb[1] = B.y; x.vb[2] = B.z; x.vb[3] = B.w;
+    x.vc[0] = C.x; x.vc[1] = C.y; x.vc[2] = C.z; x.vc[3] = C.w;
+    x.vd[0] = D.x; x.vd[1] = D.y; x.vd[2] = D.z; x.vd[3] = D.w;
+    x.ks0 = x.ks1 = x.vsc = 0;
   }
 }
 
 template <int PREC, int S>
-__device__ __forceinline__ void qk_step(const KRows<PREC> &kr, const uint32_t (&qf)[8][2], float (&acc)[4]) {
+__device__ __forceinline__ void qk_step(const Slice<PREC> &x, uint32_t lo0, uint32_t hi0, uint32_t lo1, uint32_t hi1,
+                                        const uint32_t (&qf)[8][2], float (&acc)[4]) {
   if constexpr (PREC == NVKV_PREC_NVFP4) {
-    const uint32_t m0 = S < 4 ? kr.lo0 : kr.hi0, m1 = S < 4 ? kr.lo1 : kr.hi1;
+    const uint32_t m0 = S < 4 ? lo0 : hi0, m1 = S < 4 ? lo1 : hi1;
     constexpr int B0 = (S & 1) ? 2 : 0, B1 = B0 + 1;
-    const uint32_t a0 = hmul2_u32(f16x2_from_e2m1x2<B0>(kr.w0[S >> 1]), m0);
-    const uint32_t a2 = hmul2_u32(f16x2_from_e2m1x2<B1>(kr.w0[S >> 1]), m0);
-    const uint32_t a1 = hmul2_u32(f16x2_from_e2m1x2<B0>(kr.w1[S >> 1]), m1);
-    const uint32_t a3 = hmul2_u32(f16x2_from_e2m1x2<B1>(kr.w1[S >> 1]), m1);
+    const uint32_t a0 = hmul2_u32(f16x2_from_e2m1x2<B0>(x.k0[S >> 1]), m0);
+    const uint32_t a2 = hmul2_u32(f16x2_from_e2m1x2<B1>(x.k0[S >> 1]), m0);
+    const uint32_t a1 = hmul2_u32(f16x2_from_e2m1x2<B0>(x.k1[S >> 1]), m1);
+    const uint32_t a3 = hmul2_u32(f16x2_from_e2m1x2<B1>(x.k1[S >> 1]), m1);
     mma_f16_16816(acc, a0, a1, a2, a3, qf[S][0], qf[S][1]);
   } else {
-    mma_f16_16816(acc, f16x2_from_e4m3x2<0>(kr.w0[S]), f16x2_from_e4m3x2<0>(kr.w1[S]),
-                  f16x2_from_e4m3x2<1>(kr.w0[S]), f16x2_from_e4m3x2<1>(kr.w1[S]), qf[S][0], qf[S][1]);
-  }
-}
-
-// Scores of sub-tiles k0 and k0+1 (tokens 16k + r, 16k + r + 8): four
-// independent MMA chains (two sub-tiles x even/odd k-steps) instead of one.
-template <int PREC>
-__device__ __forceinline__ void qk_pair(const uint8_t *stage, int k0, int r, int c, const uint32_t (&qf)[8][2],
-                                        float (&xa)[4], float (&xb)[4]) {
-  KRows<PREC> ka, kb;
-  load_k_rows<PREC>(stage, 16 * k0 + r, c, ka);
-  load_k_rows<PREC>(stage, 16 * (k0 + 1) + r, c, kb);
-  float ea[4] = {0.f, 0.f, 0.f, 0.f}, oa[4] = {0.f, 0.f, 0.f, 0.f};
-  float eb[4] = {0.f, 0.f, 0.f, 0.f}, ob[4] = {0.f, 0.f, 0.f, 0.f};
-  qk_step<PREC, 0>(ka, qf, ea); qk_step<PREC, 0>(kb, qf, eb);
-  qk_step<PREC, 1>(ka, qf, oa); qk_step<PREC, 1>(kb, qf, ob);
-  qk_step<PREC, 2>(ka, qf, ea); qk_step<PREC, 2>(kb, qf, eb);
-  qk_step<PREC, 3>(ka, qf, oa); qk_step<PREC, 3>(kb, qf, ob);
-  qk_step<PREC, 4>(ka, qf, ea); qk_step<PREC, 4>(kb, qf, eb);
-  qk_step<PREC, 5>(ka, qf, oa); qk_step<PREC, 5>(kb, qf, ob);
-  qk_step<PREC, 6>(ka, qf, ea); qk_step<PREC, 6>(kb, qf, eb);
-  qk_step<PREC, 7>(ka, qf, oa); qk_step<PREC, 7>(kb, qf, ob);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    xa[e] = ea[e] + oa[e];
-    xb[e] = eb[e] + ob[e];
+    mma_f16_16816(acc, f16x2_from_e4m3x2<0>(x.k0[S]), f16x2_from_e4m3x2<0>(x.k1[S]), f16x2_from_e4m3x2<1>(x.k0[S]),
+                  f16x2_from_e4m3x2<1>(x.k1[S]), qf[S][0], qf[S][1]);
   }
 }
 
@@ -325,90 +294,37 @@ __device__ __forceinline__ void pv_mma_nvfp4(float (&o)[4], uint32_t xAB, uint32
                 hmul2_u32(f16x2_from_e2m1x2<I>(xCD), sCD), hmul2_u32(f16x2_from_e2m1x2<I>(yCD), sCD), b0, b1);
 }
 
+// One warp's 16-token slice: scores, online-softmax update, P.V.
+// nvalid = valid tokens of the slice (1..16).
 template <int PREC>
-__device__ __forceinline__ void pv_subtile(const uint8_t *stage, int k, int r, int c, int nvalid, uint32_t b0,
-                                           uint32_t b1, WarpState &st) {
-  using Lay = Layout<PREC>;
-  const int tA = 16 * k + 2 * c, tB = tA + 1, tC = tA + 8, tD = tA + 9;
+__device__ __forceinline__ void consume_slice(Slice<PREC> &x, int nvalid, int r, int c, const uint32_t (&qf)[8][2],
+                                              const float (&cs)[2], WarpState &st) {
+  // ---- scores: two independent MMA chains (even / odd k-steps) ----
+  float e[4] = {0.f, 0.f, 0.f, 0.f}, od[4] = {0.f, 0.f, 0.f, 0.f};
+  uint32_t lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
   if constexpr (PREC == NVKV_PREC_NVFP4) {
-    const uint2 vA = *reinterpret_cast<const uint2 *>(stage + Lay::kVc + tA * Lay::kRowBytes + 8 * r);
-    const uint2 vB = *reinterpret_cast<const uint2 *>(stage + Lay::kVc + tB * Lay::kRowBytes + 8 * r);
-    const uint2 vC = *reinterpret_cast<const uint2 *>(stage + Lay::kVc + tC * Lay::kRowBytes + 8 * r);
-    const uint2 vD = *reinterpret_cast<const uint2 *>(stage + Lay::kVc + tD * Lay::kRowBytes + 8 * r);
-    const uint8_t *vs = stage + Lay::kVs;
-    uint32_t sA = vs[tA * 8 + r], sB = vs[tB * 8 + r], sC = vs[tC * 8 + r], sD = vs[tD * 8 + r];
-    if (nvalid < kTile) {  // masked tokens get scale 0 -> value 0 (codes are finite)
-      if (tA >= nvalid) sA = 0;
-      if (tB >= nvalid) sB = 0;
-      if (tC >= nvalid) sC = 0;
-      if (tD >= nvalid) sD = 0;
-    }
-    const uint32_t sAB = f16x2_from_e4m3x2<0>(sA | (sB << 8));
-    const uint32_t sCD = f16x2_from_e4m3x2<0>(sC | (sD << 8));
-#pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      const uint32_t a = w ? vA.y : vA.x, bb = w ? vB.y : vB.x, cc = w ? vC.y : vC.x, dd = w ? vD.y : vD.x;
-      // byte j of x: token pair's low nibbles (d = 16r + 2j); of y: high nibbles (d + 1)
-      const uint32_t xAB = (a & 0x0F0F0F0Fu) | ((bb & 0x0F0F0F0Fu) << 4);
-      const uint32_t yAB = ((a >> 4) & 0x0F0F0F0Fu) | (bb & 0xF0F0F0F0u);
-      const uint32_t xCD = (cc & 0x0F0F0F0Fu) | ((dd & 0x0F0F0F0Fu) << 4);
-      const uint32_t yCD = ((cc >> 4) & 0x0F0F0F0Fu) | (dd & 0xF0F0F0F0u);
-      pv_mma_nvfp4<0>(st.o[4 * w + 0], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
-      pv_mma_nvfp4<1>(st.o[4 * w + 1], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
-      pv_mma_nvfp4<2>(st.o[4 * w + 2], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
-      pv_mma_nvfp4<3>(st.o[4 * w + 3], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
-    }
-  } else {
-    uint4 vA = *reinterpret_cast<const uint4 *>(stage + Lay::kVc + tA * Lay::kRowBytes + 16 * r);
-    uint4 vB = *reinterpret_cast<const uint4 *>(stage + Lay::kVc + tB * Lay::kRowBytes + 16 * r);
-    uint4 vC = *reinterpret_cast<const uint4 *>(stage + Lay::kVc + tC * Lay::kRowBytes + 16 * r);
-    uint4 vD = *reinterpret_cast<const uint4 *>(stage + Lay::kVc + tD * Lay::kRowBytes + 16 * r);
-    if (nvalid < kTile) {  // masked tokens -> E4M3 zero (stale bytes could be NaN)
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      if (tA >= nvalid) vA = z;
-      if (tB >= nvalid) vB = z;
-      if (tC >= nvalid) vC = z;
-      if (tD >= nvalid) vD = z;
-    }
-    const uint32_t A[4] = {vA.x, vA.y, vA.z, vA.w}, Bv[4] = {vB.x, vB.y, vB.z, vB.w};
-    const uint32_t C[4] = {vC.x, vC.y, vC.z, vC.w}, Dv[4] = {vD.x, vD.y, vD.z, vD.w};
-#pragma unroll
-    for (int qd = 0; qd < 4; ++qd) {
-      const uint32_t ab01 = prmt(A[qd], Bv[qd], 0x5140), ab23 = prmt(A[qd], Bv[qd], 0x7362);
-      const uint32_t cd01 = prmt(C[qd], Dv[qd], 0x5140), cd23 = prmt(C[qd], Dv[qd], 0x7362);
-      mma_f16_16816(st.o[2 * qd], f16x2_from_e4m3x2<0>(ab01), f16x2_from_e4m3x2<1>(ab01),
-                    f16x2_from_e4m3x2<0>(cd01), f16x2_from_e4m3x2<1>(cd01), b0, b1);
-      mma_f16_16816(st.o[2 * qd + 1], f16x2_from_e4m3x2<0>(ab23), f16x2_from_e4m3x2<1>(ab23),
-                    f16x2_from_e4m3x2<0>(cd23), f16x2_from_e4m3x2<1>(cd23), b0, b1);
-    }
+    const uint32_t sc0 = f16x2_from_e4m3x2<0>(x.ks0), sc1 = f16x2_from_e4m3x2<0>(x.ks1);
+    lo0 = prmt(sc0, 0, 0x1010);  // {S_2c, S_2c}
+    hi0 = prmt(sc0, 0, 0x3232);  // {S_2c+1, S_2c+1}
+    lo1 = prmt(sc1, 0, 0x1010);
+    hi1 = prmt(sc1, 0, 0x3232);
   }
-}
-
-// One 64-token tile: 4 sub-tiles of 16 tokens.
-template <int PREC>
-__device__ __forceinline__ void consume_tile(const uint8_t *stage, int nvalid, int r, int c,
-                                             const uint32_t (&qf)[8][2], const float (&cs)[2], WarpState &st) {
-  float x[4][4];
-  qk_pair<PREC>(stage, 0, r, c, qf, x[0], x[1]);
-  qk_pair<PREC>(stage, 2, r, c, qf, x[2], x[3]);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    x[k][0] *= cs[0];
-    x[k][1] *= cs[1];
-    x[k][2] *= cs[0];
-    x[k][3] *= cs[1];
-    if (nvalid < kTile) {
-      const int t0 = 16 * k + r, t1 = t0 + 8;
-      if (t0 >= nvalid) x[k][0] = x[k][1] = -INFINITY;
-      if (t1 >= nvalid) x[k][2] = x[k][3] = -INFINITY;
-    }
+  qk_step<PREC, 0>(x, lo0, hi0, lo1, hi1, qf, e);
+  qk_step<PREC, 1>(x, lo0, hi0, lo1, hi1, qf, od);
+  qk_step<PREC, 2>(x, lo0, hi0, lo1, hi1, qf, e);
+  qk_step<PREC, 3>(x, lo0, hi0, lo1, hi1, qf, od);
+  qk_step<PREC, 4>(x, lo0, hi0, lo1, hi1, qf, e);
+  qk_step<PREC, 5>(x, lo0, hi0, lo1, hi1, qf, od);
+  qk_step<PREC, 6>(x, lo0, hi0, lo1, hi1, qf, e);
+  qk_step<PREC, 7>(x, lo0, hi0, lo1, hi1, qf, od);
+  float s0 = (e[0] + od[0]) * cs[0], s1 = (e[1] + od[1]) * cs[1];  // token r
+  float s2 = (e[2] + od[2]) * cs[0], s3 = (e[3] + od[3]) * cs[1];  // token r + 8
+  if (nvalid < kSub) {
+    if (r >= nvalid) s0 = s1 = -INFINITY;
+    if (r + 8 >= nvalid) s2 = s3 = -INFINITY;
   }
-  float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    mx0 = fmaxf(mx0, fmaxf(x[k][0], x[k][2]));
-    mx1 = fmaxf(mx1, fmaxf(x[k][1], x[k][3]));
-  }
+  // ---- online softmax: max over the slice's 16 tokens, per head ----
+  float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
@@ -430,16 +346,144 @@ __device__ __forceinline__ void consume_tile(const uint8_t *stage, int nvalid, i
       st.o[j][3] *= al1;
     }
   }
+  const float p0 = ex2(s0 - st.m[0]), p1 = ex2(s1 - st.m[1]);
+  const float p2 = ex2(s2 - st.m[0]), p3 = ex2(s3 - st.m[1]);
+  st.l[0] += p0 + p2;
+  st.l[1] += p1 + p3;
+  const uint32_t b0 = movmatrix_trans(pack_f16x2(p0, p1));  // P[tok 2c, 2c+1][head r]
+  const uint32_t b1 = movmatrix_trans(pack_f16x2(p2, p3));  // P[tok 2c+8, 2c+9][head r]
+
+  // ---- P.V ----
+  const int tA = 2 * c;
+  if constexpr (PREC == NVKV_PREC_NVFP4) {
+    uint32_t sv = x.vsc;
+    if (nvalid < kSub) {  // masked tokens get scale 0 -> value 0 (codes are finite)
+      if (tA >= nvalid) sv &= 0xFFFFFF00u;
+      if (tA + 1 >= nvalid) sv &= 0xFFFF00FFu;
+      if (tA + 8 >= nvalid) sv &= 0xFF00FFFFu;
+      if (tA + 9 >= nvalid) sv &= 0x00FFFFFFu;
+    }
+    const uint32_t sAB = f16x2_from_e4m3x2<0>(sv), sCD = f16x2_from_e4m3x2<1>(sv);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float p0 = ex2(x[k][0] - st.m[0]), p1 = ex2(x[k][1] - st.m[1]);
-    const float p2 = ex2(x[k][2] - st.m[0]), p3 = ex2(x[k][3] - st.m[1]);
-    st.l[0] += p0 + p2;
-    st.l[1] += p1 + p3;
-    const uint32_t b0 = movmatrix_trans(pack_f16x2(p0, p1));  // P[tok 16k+2c, +1][head r]
-    const uint32_t b1 = movmatrix_trans(pack_f16x2(p2, p3));  // P[tok 16k+8+2c, +1][head r]
-    pv_subtile<PREC>(stage, k, r, c, nvalid, b0, b1, st);
+    for (int w = 0; w < 2; ++w) {
+      const uint32_t a = x.va[w], bb = x.vb[w], cc = x.vc[w], dd = x.vd[w];
+      // byte j of x*: the token pair's low nibbles (d = 16r + 2j'); of y*: high nibbles (d + 1)
+      const uint32_t xAB = (a & 0x0F0F0F0Fu) | ((bb & 0x0F0F0F0Fu) << 4);
+      const uint32_t yAB = ((a >> 4) & 0x0F0F0F0Fu) | (bb & 0xF0F0F0F0u);
+      const uint32_t xCD = (cc & 0x0F0F0F0Fu) | ((dd & 0x0F0F0F0Fu) << 4);
+      const uint32_t yCD = ((cc >> 4) & 0x0F0F0F0Fu) | (dd & 0xF0F0F0F0u);
+      pv_mma_nvfp4<0>(st.o[4 * w + 0], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
+      pv_mma_nvfp4<1>(st.o[4 * w + 1], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
+      pv_mma_nvfp4<2>(st.o[4 * w + 2], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
+      pv_mma_nvfp4<3>(st.o[4 * w + 3], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
+    }
+  } else {
+    if (nvalid < kSub) {  // masked tokens -> E4M3 zero (stale bytes could be NaN)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (tA >= nvalid) x.va[q] = 0;
+        if (tA + 1 >= nvalid) x.vb[q] = 0;
+        if (tA + 8 >= nvalid) x.vc[q] = 0;
+        if (tA + 9 >= nvalid) x.vd[q] = 0;
+      }
+    }
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {
+      const uint32_t ab01 = prmt(x.va[qd], x.vb[qd], 0x5140), ab23 = prmt(x.va[qd], x.vb[qd], 0x7362);
+      const uint32_t cd01 = prmt(x.vc[qd], x.vd[qd], 0x5140), cd23 = prmt(x.vc[qd], x.vd[qd], 0x7362);
+      mma_f16_16816(st.o[2 * qd], f16x2_from_e4m3x2<0>(ab01), f16x2_from_e4m3x2<1>(ab01),
+                    f16x2_from_e4m3x2<0>(cd01), f16x2_from_e4m3x2<1>(cd01), b0, b1);
+      mma_f16_16816(st.o[2 * qd + 1], f16x2_from_e4m3x2<0>(ab23), f16x2_from_e4m3x2<1>(ab23),
+                    f16x2_from_e4m3x2<0>(cd23), f16x2_from_e4m3x2<1>(cd23), b0, b1);
+    }
   }
+}
+
+// Merge of the split-KV partials of one (sequence, KV head) by the 128
+// consumer threads of the last-arriving CTA.  Contributor k's partial is
+// (o_k[G][128], m_k[G], l_k[G]) in log2 units; out = sum_k 2^(m_k - M) o_k /
+// sum_k 2^(m_k - M) l_k with M = max_k m_k, times g_V.  `wbuf` (>= 4 * G * 128
+// floats) and `red` (>= 64 floats) are free shared memory.
+__device__ __forceinline__ void merge_partials(const DecodeArgs &a, int64_t c_first, int ncontrib, int64_t W, int64_t NC,
+                                            int64_t ubh0, int b, int h, float vscale, float *wbuf, float *red) {
+  constexpr int kT = kConsumerWarps * 32;
+  const int G = a.G, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hd = tid % G;     // kT % G == 0: a thread always serves the same head
+  const int kstep = kT / G;   // contributors visited per pass step
+  const int cap = kConsumerWarps * kD;  // contributors whose weights fit in wbuf per chunk
+  auto stats = [&](int k) -> const float * {
+    const int64_t cc = c_first + k;
+    const int sl = share_begin(cc, W, NC) >= ubh0 ? 0 : 1;
+    return a.partials + (cc * 2 + sl) * kSlotFloats;
+  };
+  auto reduce = [&](float v, bool is_max) -> float {  // over threads with the same head
+    for (int o = G; o < 32; o <<= 1) {
+      const float y = __shfl_xor_sync(0xffffffffu, v, o);
+      v = is_max ? fmaxf(v, y) : v + y;
+    }
+    named_bar_sync(1, kT);
+    if (lane < G) red[warp * kMaxGroup + lane] = v;
+    named_bar_sync(1, kT);
+    float t = red[hd];
+#pragma unroll
+    for (int w = 1; w < kConsumerWarps; ++w) t = is_max ? fmaxf(t, red[w * kMaxGroup + hd]) : t + red[w * kMaxGroup + hd];
+    return t;
+  };
+  // pass A: M per head
+  float m = -INFINITY;
+  for (int k = tid / G; k < ncontrib; k += kstep) m = fmaxf(m, __ldcg(stats(k) + kMaxGroup * kD + hd));
+  const float M = reduce(m, true);
+  float acc[kMaxGroup];
+#pragma unroll
+  for (int j = 0; j < kMaxGroup; ++j) acc[j] = 0.0f;
+  float lsum = 0.0f;
+  for (int k0 = 0; k0 < ncontrib; k0 += cap) {
+    const int kn = min(cap, ncontrib - k0);
+    // pass B: weights of this chunk into shared memory, l partial sums
+    named_bar_sync(1, kT);
+    for (int k = tid / G; k < kn; k += kstep) {
+      const float *st = stats(k0 + k);
+      const float mk = __ldcg(st + kMaxGroup * kD + hd);
+      const float w = mk == -INFINITY ? 0.0f : ex2(mk - M);
+      wbuf[k * G + hd] = w;
+      lsum += w * __ldcg(st + kMaxGroup * kD + kMaxGroup + hd);
+    }
+    named_bar_sync(1, kT);
+    // pass C: thread = d; heads in groups of four, eight contributors per batch in flight
+    for (int j0 = 0; j0 < G; j0 += 4) {
+      for (int k = 0; k < kn; k += 8) {
+        float v[8][4];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            v[q][j] = (j0 + j < G && k + q < kn) ? __ldcg(stats(k0 + k + q) + (j0 + j) * kD + tid) : 0.0f;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (j0 + j < G && k + q < kn) {
+              const float w = wbuf[(k + q) * G + j0 + j] * v[q][j];
+              if (j0 == 0) acc[j] += w;
+              else acc[4 + j] += w;
+            }
+        }
+      }
+    }
+  }
+  const float L = reduce(lsum, false);  // every thread now holds L of head `hd`
+  // thread d writes all heads; the L of head j sits in red after the reduce
+#pragma unroll
+  for (int j = 0; j < kMaxGroup; ++j) {
+    if (j < G) {
+      float Lj = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) Lj += red[w * kMaxGroup + j];
+      a.out[(static_cast<int64_t>(b) * a.Hq + h * G + j) * kD + tid] = __float2bfloat16_rn(acc[j] * (vscale / Lj));
+    }
+  }
+  (void)L;
 }
 
 template <int PREC>
@@ -453,10 +497,9 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
   float *mrg_o = reinterpret_cast<float *>(cum + kMaxBatch + 1);
   float *mrg_ml = mrg_o + kConsumerWarps * a.G * kD;
   int *flags = reinterpret_cast<int *>(mrg_ml + kConsumerWarps * kMaxGroup * 2);
-  volatile int *abort = flags;  // flags[0]
-  int *fills = flags + 1;       // flags[1 .. kStages]: fills issued per slot
-  int *bcast = flags + 1 + Lay::kStages;            // 3 ints
-  volatile int *consumed = flags + 4 + Lay::kStages;  // kStages ints: fills consumed per slot
+  volatile int *abort = flags;              // flags[0]
+  int *fills = flags + 1;                   // flags[1 .. kStages]: fills issued per slot
+  int *bcast = flags + 1 + Lay::kStages;    // 3 ints
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = a.c.Hkv, B = a.B, G = a.G;
@@ -467,9 +510,8 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
     flags[0] = 0;
     for (int s = 0; s < Lay::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);  // every consumer warp reads every stage
       fills[s] = 0;
-      consumed[s] = 0;
     }
     fence_mbar_init();
   }
@@ -519,6 +561,7 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
     producer<PREC>(a, ring, full, empty, cum, u0, u1, abort, fills);
   } else {
     const int r = lane >> 2, c = lane & 3;
+    const SliceOffsets<PREC> so(warp, a.c.P);
     const float kscale = __fmul_rn(a.c.scale[0], a.sm_scale * 1.4426950408889634f);
     const float vscale = a.c.scale[1];
     int64_t i = 0;
@@ -576,25 +619,18 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
       const int ntiles = s.t1 - s.t0;
       for (int k = 0; k < ntiles; ++k) {
         const int64_t gi = i + k;
-        if (static_cast<int>(gi % kConsumerWarps) != warp) continue;
         const int slot = static_cast<int>(gi % Lay::kStages);
         const uint32_t fill = static_cast<uint32_t>(gi / Lay::kStages);
-        // Consecutive fills of a slot go to different warps.  Wait until the
-        // slot's previous fill has been consumed: only then is the fill this
-        // warp needs the slot's current phase, so the parity wait below
-        // cannot match an older completed phase.
-        bool ready = wait_consumed(consumed + slot, static_cast<int>(fill), abort);
-        ready = ready && mbar_wait_bounded(&full[slot], fill & 1u, abort);
-        if (__all_sync(0xffffffffu, ready)) {  // warp-uniform: the MMAs below are .aligned
-          const int64_t rem = Lb - static_cast<int64_t>(s.t0 + k) * kTile;
-          const int nvalid = rem < kTile ? static_cast<int>(rem) : kTile;
-          consume_tile<PREC>(ring + static_cast<size_t>(slot) * Lay::kStageBytes, nvalid, r, c, qf, cs, st);
-        }
+        // Every consumer warp reads every stage in order, so the phase this
+        // warp waits for is always the slot's current one.
+        const bool ready = mbar_wait_bounded(&full[slot], fill & 1u, abort);
+        const int64_t rem = Lb - static_cast<int64_t>(s.t0 + k) * kTile - kSub * warp;
+        const int nvalid = rem < kSub ? static_cast<int>(rem) : kSub;
+        Slice<PREC> x;
+        if (nvalid > 0) load_slice<PREC>(ring + static_cast<size_t>(slot) * Lay::kStageBytes, so, r, c, x);
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&empty[slot]);
-          consumed[slot] = static_cast<int>(fill) + 1;
-        }
+        if (lane == 0) mbar_arrive(&empty[slot]);  // the slice is in registers: release the stage
+        if (__all_sync(0xffffffffu, ready) && nvalid > 0) consume_slice<PREC>(x, nvalid, r, c, qf, cs, st);
       }
       i += ntiles;
 
@@ -664,29 +700,11 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
         }
         named_bar_sync(1, kConsumerWarps * 32);
         if (bcast[0]) {
-          // last arriver: merge every contributor's partial
-          const int64_t c_first = bcast[1];
-          const int ncontrib = bcast[2];
-          for (int e = tid; e < G * kD; e += kConsumerWarps * 32) {
-            const int hd = e / kD, d = e % kD;
-            float M = -INFINITY;
-            for (int q = 0; q < ncontrib; ++q) {
-              const int64_t cc = c_first + q;
-              const int sl = share_begin(cc, W, NC) >= ubh0 ? 0 : 1;
-              M = fmaxf(M, __ldcg(a.partials + (cc * 2 + sl) * kSlotFloats + kMaxGroup * kD + hd));
-            }
-            float o = 0.0f, l = 0.0f;
-            for (int q = 0; q < ncontrib; ++q) {
-              const int64_t cc = c_first + q;
-              const int sl = share_begin(cc, W, NC) >= ubh0 ? 0 : 1;
-              const float *pp = a.partials + (cc * 2 + sl) * kSlotFloats;
-              const float mq = __ldcg(pp + kMaxGroup * kD + hd);
-              const float f = (mq == -INFINITY) ? 0.0f : ex2(mq - M);
-              o += f * __ldcg(pp + hd * kD + d);
-              l += f * __ldcg(pp + kMaxGroup * kD + kMaxGroup + hd);
-            }
-            a.out[(static_cast<int64_t>(s.b) * a.Hq + s.h * G + hd) * kD + d] = __float2bfloat16_rn(o * (vscale / l));
-          }
+          // Last arriver: merge every contributor's partial with the
+          // log-sum-exp rule.  Statistics are fetched in parallel and the
+          // weighted sum keeps all contributors' loads in flight, so the merge
+          // costs a few L2 round trips instead of one per contributor.
+          merge_partials(a, bcast[1], bcast[2], W, NC, ubh0, s.b, s.h, vscale, mrg_o, mrg_ml);
           if (tid == 0) a.counters[s.b * Hkv + s.h] = 0;
         }
       }

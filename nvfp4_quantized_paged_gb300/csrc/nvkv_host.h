@@ -20,14 +20,9 @@ inline nvkv_status check_cache(const nvkv_cache *c, int32_t want_prec) {
   if (c->num_pages <= 0 || c->num_kv_heads <= 0 || c->page_size <= 0 || c->head_dim <= 0)
     return NVKV_ERR_INVALID_ARG;
   if (c->head_dim != 128) return NVKV_ERR_UNSUPPORTED;
-  if (c->page_size != 16 && c->page_size != 32 && c->page_size != 64 && c->page_size != 128)
-    return NVKV_ERR_UNSUPPORTED;
-  if (!c->k_data || !c->v_data || !c->kv_scale) return NVKV_ERR_INVALID_ARG;
-  if (!aligned16(c->k_data) || !aligned16(c->v_data)) return NVKV_ERR_UNSUPPORTED;
-  if (c->prec == NVKV_PREC_NVFP4) {
-    if (!c->k_scale || !c->v_scale) return NVKV_ERR_INVALID_ARG;
-    if (!aligned16(c->k_scale) || !aligned16(c->v_scale)) return NVKV_ERR_UNSUPPORTED;
-  }
+  if (c->page_size != 16 && c->page_size != 32 && c->page_size != 64) return NVKV_ERR_UNSUPPORTED;
+  if (!c->data || !c->kv_scale) return NVKV_ERR_INVALID_ARG;
+  if (!aligned16(c->data)) return NVKV_ERR_UNSUPPORTED;
   return NVKV_OK;
 }
 
@@ -37,19 +32,35 @@ inline nvkv_status launch_status() {
 }
 
 // Device-side view of a cache descriptor (passed by value to kernels).
+// Byte layout of one (page, KV head) block at head_dim 128 (see the header).
+constexpr int kNvCodeRow = 64, kNvScaleRow = 8, kNvTokBytes = 144;  // NVFP4: per token, K+V
+constexpr int kF8Row = 128, kF8TokBytes = 256;                      // FP8
+
 struct CacheDev {
-  uint8_t *kd, *vd, *ks, *vs;
+  uint8_t *data;
   const float *scale;
   int32_t *err;
   int32_t num_pages, P, Hkv;
+  // NVFP4 plane offsets inside a block: kind 0 = K, 1 = V
+  __host__ __device__ int64_t block(int64_t page, int h, int tok_bytes) const {
+    return (page * Hkv + h) * static_cast<int64_t>(P) * tok_bytes;
+  }
+  __host__ __device__ int64_t nv_codes(int64_t page, int h, int kind, int off) const {
+    return block(page, h, kNvTokBytes) + static_cast<int64_t>(kind) * P * (kNvCodeRow + kNvScaleRow) +
+           static_cast<int64_t>(off) * kNvCodeRow;
+  }
+  __host__ __device__ int64_t nv_scales(int64_t page, int h, int kind, int off) const {
+    return block(page, h, kNvTokBytes) + static_cast<int64_t>(kind) * P * (kNvCodeRow + kNvScaleRow) +
+           static_cast<int64_t>(P) * kNvCodeRow + static_cast<int64_t>(off) * kNvScaleRow;
+  }
+  __host__ __device__ int64_t f8_row(int64_t page, int h, int kind, int off) const {
+    return block(page, h, kF8TokBytes) + static_cast<int64_t>(kind) * P * kF8Row + static_cast<int64_t>(off) * kF8Row;
+  }
 };
 
 inline CacheDev to_dev(const nvkv_cache *c) {
   CacheDev d;
-  d.kd = c->k_data;
-  d.vd = c->v_data;
-  d.ks = c->k_scale;
-  d.vs = c->v_scale;
+  d.data = c->data;
   d.scale = c->kv_scale;
   d.err = c->err_flag;
   d.num_pages = c->num_pages;

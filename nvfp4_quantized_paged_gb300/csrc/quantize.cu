@@ -113,7 +113,8 @@ __global__ void __launch_bounds__(256)
     if (kind == 0 && h == 0 && blk == 0) set_err(c.err, NVKV_DEVERR_SLOT);
     return;
   }
-  const int64_t row = (slot / c.P * c.Hkv + h) * c.P + slot % c.P;
+  const int64_t page = slot / c.P;
+  const int off = static_cast<int>(slot % c.P);
   float x[16];
   load16((kind == 0 ? k : v) + th * kD + 16 * blk, x);
   const float g = gs[kind];
@@ -136,9 +137,8 @@ __global__ void __launch_bounds__(256)
       hi |= e2m1x2_from_f32(__fdiv_rn(x[8 + 2 * j], den), __fdiv_rn(x[8 + 2 * j + 1], den)) << (8 * j);
     }
   }
-  uint8_t *codes = (kind == 0 ? c.kd : c.vd) + row * (kD / 2) + 8 * blk;
-  *reinterpret_cast<uint2 *>(codes) = make_uint2(lo, hi);
-  (kind == 0 ? c.ks : c.vs)[row * kBlocksPerRow + blk] = static_cast<uint8_t>(sbyte);
+  *reinterpret_cast<uint2 *>(c.data + c.nv_codes(page, h, kind, off) + 8 * blk) = make_uint2(lo, hi);
+  c.data[c.nv_scales(page, h, kind, off) + blk] = static_cast<uint8_t>(sbyte);
 }
 
 // ---------------------------------------------------------------------------
@@ -162,7 +162,8 @@ __global__ void __launch_bounds__(256)
     if (kind == 0 && h == 0 && blk == 0) set_err(c.err, NVKV_DEVERR_SLOT);
     return;
   }
-  const int64_t row = (slot / c.P * c.Hkv + h) * c.P + slot % c.P;
+  const int64_t page = slot / c.P;
+  const int off = static_cast<int>(slot % c.P);
   float x[16];
   load16((kind == 0 ? k : v) + th * kD + 16 * blk, x);
   const float s8 = gs[kind];
@@ -174,8 +175,7 @@ __global__ void __launch_bounds__(256)
              (e4m3x2_from_f32(__fdiv_rn(x[4 * j + 2], s8), __fdiv_rn(x[4 * j + 3], s8)) << 16);
     }
   }
-  uint8_t *dst = (kind == 0 ? c.kd : c.vd) + row * kD + 16 * blk;
-  *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4 *>(c.data + c.f8_row(page, h, kind, off) + 16 * blk) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // ---------------------------------------------------------------------------
@@ -230,9 +230,9 @@ __global__ void __launch_bounds__(256)
     set_err(c.err, NVKV_DEVERR_PAGE);
     return;
   }
-  const int64_t row = (page * c.Hkv + h) * c.P + t % c.P;
-  const uint2 cw = *reinterpret_cast<const uint2 *>((kind == 0 ? c.kd : c.vd) + row * (kD / 2) + 8 * blk);
-  const float S = f32_from_e4m3((kind == 0 ? c.ks : c.vs)[row * kBlocksPerRow + blk]);
+  const int off = static_cast<int>(t % c.P);
+  const uint2 cw = *reinterpret_cast<const uint2 *>(c.data + c.nv_codes(page, h, kind, off) + 8 * blk);
+  const float S = f32_from_e4m3(c.data[c.nv_scales(page, h, kind, off) + blk]);
   const float ratio = __fdiv_rn(c.scale[kind], ws_scale[kind]);
   const uint32_t words[2] = {cw.x, cw.y};
   uint32_t out[4];

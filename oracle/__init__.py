@@ -61,23 +61,23 @@ def lib():
         L.orc_global_scale.argtypes = [_f32p, ctypes.c_int64, ctypes.c_float]
         L.orc_nvfp4_quantize_write.restype = ctypes.c_int
         L.orc_nvfp4_quantize_write.argtypes = [_f32p, _f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _i64p,
-                                               _f32p, ctypes.c_int, ctypes.c_int64, _u8p, _u8p, _u8p, _u8p]
+                                               _f32p, ctypes.c_int, ctypes.c_int64, _u8p]
         L.orc_fp8_quantize_write.restype = ctypes.c_int
         L.orc_fp8_quantize_write.argtypes = [_f32p, _f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _i64p,
-                                             _f32p, ctypes.c_int, ctypes.c_int64, _u8p, _u8p]
+                                             _f32p, ctypes.c_int, ctypes.c_int64, _u8p]
         L.orc_gather_dequant.restype = ctypes.c_int
-        L.orc_gather_dequant.argtypes = [ctypes.c_int, _u8p, _u8p, ctypes.c_float, _i32p, ctypes.c_int,
+        L.orc_gather_dequant.argtypes = [ctypes.c_int, _u8p, ctypes.c_int, ctypes.c_float, _i32p, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                          _f64p]
         L.orc_paged_decode_attention.restype = ctypes.c_int
         L.orc_paged_decode_attention.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                                 ctypes.c_int, ctypes.c_int, _u8p, _u8p, _u8p, _u8p, _f32p, _i32p,
+                                                 ctypes.c_int, ctypes.c_int, _u8p, _f32p, _i32p,
                                                  ctypes.c_int, _i32p, ctypes.c_int64, ctypes.c_double,
                                                  ctypes.c_int, _f64p]
         L.orc_dequant_to_fp8_workspace.restype = ctypes.c_int
         L.orc_dequant_to_fp8_workspace.argtypes = [_i32p, ctypes.c_int, _i32p, _i32p, _i64p, ctypes.c_int,
                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
-                                                   _u8p, _u8p, _u8p, _u8p, _f32p, _f32p, _u8p, _u8p]
+                                                   _u8p, _f32p, _f32p, _u8p, _u8p]
         _LIB = L
     return _LIB
 
@@ -156,27 +156,39 @@ def global_scale(x: np.ndarray, divisor: float = NVFP4_GLOBAL_DIVISOR) -> np.flo
 # --------------------------------------------------------------------------
 
 class Cache:
-    """One layer's paged cache planes (head-major inside a page).
+    """One layer's paged cache: one contiguous block per (page, KV head).
 
-    NVFP4: ``k_data``/``v_data`` [num_pages, Hkv, P, D/2] codes, ``k_scale``/
-    ``v_scale`` [num_pages, Hkv, P, D/16] E4M3 bytes.  FP8: data
-    [num_pages, Hkv, P, D], no scale planes.  ``g`` = float32[2] (K, V)
-    global (NVFP4) or per-tensor (FP8) scale.
+    ``data`` uint8 [num_pages, Hkv, block]: NVFP4 block = [K codes P*D/2 |
+    K scales P*D/16 | V codes P*D/2 | V scales P*D/16] (P*144 bytes at
+    D = 128); FP8 block = [K P*D | V P*D].  ``k_data``/``k_scale``/``v_data``/
+    ``v_scale`` are numpy views of the planes, shaped [num_pages, Hkv, P, D/2]
+    and [num_pages, Hkv, P, D/16] (FP8: [num_pages, Hkv, P, D], no scales).
+    ``g`` = float32[2] (K, V) global (NVFP4) or per-tensor (FP8) scale.
     """
 
     def __init__(self, prec, num_pages, Hkv, P, D, g, fill=0):
         self.prec, self.num_pages, self.Hkv, self.P, self.D = prec, num_pages, Hkv, P, D
         self.g = np.asarray(g, np.float32).reshape(2).copy()
         if prec == PREC_NVFP4:
-            self.k_data = np.full((num_pages, Hkv, P, D // 2), fill, np.uint8)
-            self.v_data = np.full((num_pages, Hkv, P, D // 2), fill, np.uint8)
-            self.k_scale = np.full((num_pages, Hkv, P, D // 16), fill, np.uint8)
-            self.v_scale = np.full((num_pages, Hkv, P, D // 16), fill, np.uint8)
+            half = P * (D // 2 + D // 16)
+            self.data = np.full((num_pages, Hkv, 2 * half), fill, np.uint8)
+            cs, ss = P * (D // 2), P * (D // 16)
+            self.k_data = self.data[:, :, :cs].reshape(num_pages, Hkv, P, D // 2)
+            self.k_scale = self.data[:, :, cs:half].reshape(num_pages, Hkv, P, D // 16)
+            self.v_data = self.data[:, :, half:half + cs].reshape(num_pages, Hkv, P, D // 2)
+            self.v_scale = self.data[:, :, half + cs:].reshape(num_pages, Hkv, P, D // 16)
+            del ss
         else:
-            self.k_data = np.full((num_pages, Hkv, P, D), fill, np.uint8)
-            self.v_data = np.full((num_pages, Hkv, P, D), fill, np.uint8)
-            self.k_scale = np.zeros(1, np.uint8)
-            self.v_scale = np.zeros(1, np.uint8)
+            self.data = np.full((num_pages, Hkv, 2 * P * D), fill, np.uint8)
+            self.k_data = self.data[:, :, :P * D].reshape(num_pages, Hkv, P, D)
+            self.v_data = self.data[:, :, P * D:].reshape(num_pages, Hkv, P, D)
+            self.k_scale = self.v_scale = None
+        for v in (self.k_data, self.v_data, self.k_scale, self.v_scale):
+            assert v is None or np.shares_memory(v, self.data)
+
+    @property
+    def nbytes(self):
+        return self.data.nbytes
 
 
 def quantize_write(cache: Cache, k: np.ndarray, v: np.ndarray, slot_mapping: np.ndarray) -> None:
@@ -194,12 +206,10 @@ def quantize_write(cache: Cache, k: np.ndarray, v: np.ndarray, slot_mapping: np.
     L = lib()
     if cache.prec == PREC_NVFP4:
         rc = L.orc_nvfp4_quantize_write(_p(k, _f32p), _p(v, _f32p), T, cache.Hkv, cache.D, _p(sm, _i64p),
-                                        _p(cache.g, _f32p), cache.P, cache.num_pages, _p(cache.k_data, _u8p),
-                                        _p(cache.k_scale, _u8p), _p(cache.v_data, _u8p), _p(cache.v_scale, _u8p))
+                                        _p(cache.g, _f32p), cache.P, cache.num_pages, _p(cache.data, _u8p))
     else:
         rc = L.orc_fp8_quantize_write(_p(k, _f32p), _p(v, _f32p), T, cache.Hkv, cache.D, _p(sm, _i64p),
-                                      _p(cache.g, _f32p), cache.P, cache.num_pages, _p(cache.k_data, _u8p),
-                                      _p(cache.v_data, _u8p))
+                                      _p(cache.g, _f32p), cache.P, cache.num_pages, _p(cache.data, _u8p))
     if rc != 0:
         raise ValueError("slot out of range")
 
@@ -208,9 +218,8 @@ def gather_dequant(cache: Cache, which: str, block_row: np.ndarray, L: int, h: i
     """Exact FP64 values of tokens [0, L) of one (sequence, KV head)."""
     br = _c(block_row, np.int32)
     out = np.empty((L, cache.D), np.float64)
-    data, sc, g = ((cache.k_data, cache.k_scale, cache.g[0]) if which == "k"
-                   else (cache.v_data, cache.v_scale, cache.g[1]))
-    rc = lib().orc_gather_dequant(cache.prec, _p(data, _u8p), _p(sc, _u8p), float(g), _p(br, _i32p), L,
+    kind = 0 if which == "k" else 1
+    rc = lib().orc_gather_dequant(cache.prec, _p(cache.data, _u8p), kind, float(cache.g[kind]), _p(br, _i32p), L,
                                   cache.Hkv, h, cache.D, cache.P, cache.num_pages, _p(out, _f64p))
     if rc != 0:
         raise ValueError("page out of range")
@@ -233,8 +242,7 @@ def paged_decode_attention(cache: Cache, q_bf16_bits: np.ndarray, block_table: n
         sm_scale = 1.0 / np.sqrt(D)
     out = np.empty((B, Hq, D), np.float64)
     rc = lib().orc_paged_decode_attention(_p(q, _u16p), B, Hq, cache.Hkv, D, cache.P, cache.prec,
-                                          _p(cache.k_data, _u8p), _p(cache.k_scale, _u8p), _p(cache.v_data, _u8p),
-                                          _p(cache.v_scale, _u8p), _p(cache.g, _f32p), _p(bt, _i32p), bt.shape[1],
+                                          _p(cache.data, _u8p), _p(cache.g, _f32p), _p(bt, _i32p), bt.shape[1],
                                           _p(sl, _i32p), cache.num_pages, float(sm_scale), int(num_splits),
                                           _p(out, _f64p))
     if rc != 0:
@@ -260,8 +268,7 @@ def dequant_to_fp8_workspace(cache: Cache, block_table: np.ndarray, seq_ids, pre
     wv = np.zeros((rows, cache.Hkv, cache.D), np.uint8)
     rc = lib().orc_dequant_to_fp8_workspace(_p(bt, _i32p), bt.shape[1], _p(ids, _i32p), _p(pl, _i32p),
                                             _p(cu, _i64p), len(pl), cache.Hkv, cache.D, cache.P, cache.num_pages,
-                                            _p(cache.k_data, _u8p), _p(cache.k_scale, _u8p),
-                                            _p(cache.v_data, _u8p), _p(cache.v_scale, _u8p), _p(cache.g, _f32p),
+                                            _p(cache.data, _u8p), _p(cache.g, _f32p),
                                             _p(ws, _f32p), _p(wk, _u8p), _p(wv, _u8p))
     if rc != 0:
         raise ValueError("bad arguments")

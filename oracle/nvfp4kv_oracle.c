@@ -28,6 +28,11 @@
  *   zero cases    : g == 0 or den == 0  ->  scale byte 0x00 (g == 0) and codes 0x0
  *   FP8 layers    : s8 = amax / 448; byte = E4M3_RNE_sat(x / s8); s8 == 0 -> 0x00
  *
+ * Cache layout (the pages give none): one contiguous block per (page, KV
+ * head), pages then heads: NVFP4 block = [K codes P*D/2 | K scales P*D/16 |
+ * V codes P*D/2 | V scales P*D/16]; FP8 block = [K P*D | V P*D].  Inside a
+ * plane, slot `off` of the page is row `off`.
+ *
  * Every FP32 step is one IEEE-754 binary32 operation with round-to-nearest-even
  * and no fused multiply-add (build with -ffp-contract=off).  Attention runs in
  * FP64 over values dequantized exactly.
@@ -184,52 +189,64 @@ static void fp8_quantize_vector(const float *x, int D, float s8, uint8_t *out) {
   for (i = 0; i < D; ++i) out[i] = (s8 == 0.0f) ? 0 : orc_e4m3_encode(x[i] / s8);
 }
 
+/* Byte offsets inside the cache (one contiguous block per page and KV head). */
+static int64_t nv_block_bytes(int P, int D) { return (int64_t)P * 2 * (D / 2 + D / 16); }
+static int64_t fp8_block_bytes(int P, int D) { return (int64_t)P * 2 * D; }
+
+/* NVFP4: plane 0 = codes, 1 = scales; kind 0 = K, 1 = V. */
+static int64_t nv_offset(int64_t page, int Hkv, int h, int P, int D, int kind, int plane, int off) {
+  int64_t base = (page * Hkv + h) * nv_block_bytes(P, D) + (int64_t)kind * P * (D / 2 + D / 16);
+  return plane == 0 ? base + (int64_t)off * (D / 2) : base + (int64_t)P * (D / 2) + (int64_t)off * (D / 16);
+}
+
+static int64_t fp8_offset(int64_t page, int Hkv, int h, int P, int D, int kind, int off) {
+  return (page * Hkv + h) * fp8_block_bytes(P, D) + (int64_t)kind * P * D + (int64_t)off * D;
+}
+
 /* Quantized write into paged slots ([P1] 02 "quantized write"; [P2] Three
  * Paths: the current chunk "is quantized into the NVFP4 cache").
  * k, v: [T][Hkv][D] FP32.  slot = page*P + offset; slot < 0 skips the token.
- * Cache planes (head-major inside a page):
- *   codes  [num_pages][Hkv][P][D/2],  scales [num_pages][Hkv][P][D/16].
  * g[0], g[1] = global scales of K and V.  Returns 0, or -1 on a bad slot. */
 int orc_nvfp4_quantize_write(const float *k, const float *v, int64_t T, int Hkv, int D,
                              const int64_t *slot_mapping, const float *g, int P, int64_t num_pages,
-                             uint8_t *k_codes, uint8_t *k_scales, uint8_t *v_codes, uint8_t *v_scales) {
+                             uint8_t *cache) {
   int64_t t;
-  int h;
+  int h, kind;
   for (t = 0; t < T; ++t) {
-    int64_t slot = slot_mapping[t], page, off;
+    int64_t slot = slot_mapping[t], page;
+    int off;
     if (slot < 0) continue;
     if (slot >= num_pages * P) return -1;
     page = slot / P;
-    off = slot % P;
-    for (h = 0; h < Hkv; ++h) {
-      int64_t row = (page * Hkv + h) * P + off;
-      const int64_t src = (t * Hkv + h) * D;
-      nvfp4_quantize_vector(k + src, D, g[0], k_codes + row * (D / 2), k_scales + row * (D / 16));
-      nvfp4_quantize_vector(v + src, D, g[1], v_codes + row * (D / 2), v_scales + row * (D / 16));
-    }
+    off = (int)(slot % P);
+    for (h = 0; h < Hkv; ++h)
+      for (kind = 0; kind < 2; ++kind) {
+        const float *src = (kind ? v : k) + (t * Hkv + h) * D;
+        nvfp4_quantize_vector(src, D, g[kind], cache + nv_offset(page, Hkv, h, P, D, kind, 0, off),
+                              cache + nv_offset(page, Hkv, h, P, D, kind, 1, off));
+      }
   }
   return 0;
 }
 
-/* FP8 E4M3 write for the FP8 layers ([P1] 03: sensitive layers keep FP8):
- * planes [num_pages][Hkv][P][D]; s8[0], s8[1] = per-tensor scales of K, V. */
+/* FP8 E4M3 write for the FP8 layers ([P1] 03: sensitive layers keep FP8);
+ * s8[0], s8[1] = per-tensor scales of K, V. */
 int orc_fp8_quantize_write(const float *k, const float *v, int64_t T, int Hkv, int D,
                            const int64_t *slot_mapping, const float *s8, int P, int64_t num_pages,
-                           uint8_t *k_data, uint8_t *v_data) {
+                           uint8_t *cache) {
   int64_t t;
-  int h;
+  int h, kind;
   for (t = 0; t < T; ++t) {
-    int64_t slot = slot_mapping[t], page, off;
+    int64_t slot = slot_mapping[t], page;
+    int off;
     if (slot < 0) continue;
     if (slot >= num_pages * P) return -1;
     page = slot / P;
-    off = slot % P;
-    for (h = 0; h < Hkv; ++h) {
-      int64_t row = (page * Hkv + h) * P + off;
-      const int64_t src = (t * Hkv + h) * D;
-      fp8_quantize_vector(k + src, D, s8[0], k_data + row * D);
-      fp8_quantize_vector(v + src, D, s8[1], v_data + row * D);
-    }
+    off = (int)(slot % P);
+    for (h = 0; h < Hkv; ++h)
+      for (kind = 0; kind < 2; ++kind)
+        fp8_quantize_vector((kind ? v : k) + (t * Hkv + h) * D, D, s8[kind],
+                            cache + fp8_offset(page, Hkv, h, P, D, kind, off));
   }
   return 0;
 }
@@ -240,30 +257,31 @@ int orc_fp8_quantize_write(const float *k, const float *v, int64_t T, int Hkv, i
 /* prec 1 = FP8:   x = E4M3(byte) * s8                                        */
 /* ------------------------------------------------------------------------ */
 
-static void dequant_row(int prec, const uint8_t *data, const uint8_t *scales, int64_t row, int D, float g,
-                        double *out) {
+static void dequant_row(int prec, const uint8_t *cache, int64_t page, int Hkv, int h, int P, int D, int kind,
+                        int off, float g, double *out) {
   int d;
   if (prec == 0) {
-    const uint8_t *c = data + row * (D / 2);
-    const uint8_t *s = scales + row * (D / 16);
+    const uint8_t *c = cache + nv_offset(page, Hkv, h, P, D, kind, 0, off);
+    const uint8_t *s = cache + nv_offset(page, Hkv, h, P, D, kind, 1, off);
     for (d = 0; d < D; ++d) {
       uint8_t code = (d & 1) ? (uint8_t)(c[d / 2] >> 4) : (uint8_t)(c[d / 2] & 15);
       out[d] = orc_e2m1_value(code) * orc_e4m3_value(s[d / 16]) * (double)g;
     }
   } else {
-    const uint8_t *c = data + row * D;
+    const uint8_t *c = cache + fp8_offset(page, Hkv, h, P, D, kind, off);
     for (d = 0; d < D; ++d) out[d] = orc_e4m3_value(c[d]) * (double)g;
   }
 }
 
-/* Dequantize tokens [0, L) of one (sequence, KV head) into dense [L][D]. */
-int orc_gather_dequant(int prec, const uint8_t *data, const uint8_t *scales, float g, const int32_t *block_row,
-                       int L, int Hkv, int h, int D, int P, int64_t num_pages, double *out) {
+/* Dequantize K (kind 0) or V (kind 1) of tokens [0, L) of one (sequence, KV
+ * head) into dense [L][D]. */
+int orc_gather_dequant(int prec, const uint8_t *cache, int kind, float g, const int32_t *block_row, int L, int Hkv,
+                       int h, int D, int P, int64_t num_pages, double *out) {
   int t;
   for (t = 0; t < L; ++t) {
     int64_t page = block_row[t / P];
     if (page < 0 || page >= num_pages) return -1;
-    dequant_row(prec, data, scales, (page * Hkv + h) * P + t % P, D, g, out + (int64_t)t * D);
+    dequant_row(prec, cache, page, Hkv, h, P, D, kind, t % P, g, out + (int64_t)t * D);
   }
   return 0;
 }
@@ -288,8 +306,7 @@ static double bf16_bits_to_double(uint16_t b) {
 /*   out = sum e^(m_k - M) o_k / sum e^(m_k - M) l_k.                         */
 /* ------------------------------------------------------------------------ */
 int orc_paged_decode_attention(const uint16_t *q, int B, int Hq, int Hkv, int D, int P, int prec,
-                               const uint8_t *k_data, const uint8_t *k_scales, const uint8_t *v_data,
-                               const uint8_t *v_scales, const float *g, const int32_t *block_table,
+                               const uint8_t *cache, const float *g, const int32_t *block_table,
                                int max_pages, const int32_t *seq_lens, int64_t num_pages, double sm_scale,
                                int num_splits, double *out) {
   int b, h, G = Hq / Hkv;
@@ -307,9 +324,9 @@ int orc_paged_decode_attention(const uint16_t *q, int B, int Hq, int Hkv, int D,
       K = (double *)malloc(sizeof(double) * (size_t)L * D);
       V = (double *)malloc(sizeof(double) * (size_t)L * D);
       s = (double *)malloc(sizeof(double) * (size_t)L);
-      rc |= orc_gather_dequant(prec, k_data, k_scales, g[0], block_table + (int64_t)b * max_pages, L, Hkv, h, D, P,
+      rc |= orc_gather_dequant(prec, cache, 0, g[0], block_table + (int64_t)b * max_pages, L, Hkv, h, D, P,
                                num_pages, K);
-      rc |= orc_gather_dequant(prec, v_data, v_scales, g[1], block_table + (int64_t)b * max_pages, L, Hkv, h, D, P,
+      rc |= orc_gather_dequant(prec, cache, 1, g[1], block_table + (int64_t)b * max_pages, L, Hkv, h, D, P,
                                num_pages, V);
       for (j = 0; j < G && rc == 0; ++j) {
         int qh = h * G + j, t, d, nsp = num_splits > 1 ? num_splits : 1, sp;
@@ -369,13 +386,10 @@ int orc_paged_decode_attention(const uint16_t *q, int B, int Hq, int Hkv, int D,
 /* ------------------------------------------------------------------------ */
 int orc_dequant_to_fp8_workspace(const int32_t *block_table, int max_pages, const int32_t *seq_ids,
                                  const int32_t *prefix_lens, const int64_t *cu_prefix, int n, int Hkv, int D,
-                                 int P, int64_t num_pages, const uint8_t *k_codes, const uint8_t *k_scales,
-                                 const uint8_t *v_codes, const uint8_t *v_scales, const float *g,
+                                 int P, int64_t num_pages, const uint8_t *cache, const float *g,
                                  const float *ws_scale, uint8_t *ws_k, uint8_t *ws_v) {
   int i, pass;
   for (pass = 0; pass < 2; ++pass) {
-    const uint8_t *codes = pass ? v_codes : k_codes;
-    const uint8_t *scales = pass ? v_scales : k_scales;
     uint8_t *ws = pass ? ws_v : ws_k;
     float r;
     if (!(ws_scale[pass] > 0.0f)) return -1;
@@ -387,9 +401,8 @@ int orc_dequant_to_fp8_workspace(const int32_t *block_table, int max_pages, cons
         int64_t page = brow[t / P];
         if (page < 0 || page >= num_pages) return -1;
         for (h = 0; h < Hkv; ++h) {
-          int64_t row = (page * Hkv + h) * P + t % P;
-          const uint8_t *c = codes + row * (D / 2);
-          const uint8_t *s = scales + row * (D / 16);
+          const uint8_t *c = cache + nv_offset(page, Hkv, h, P, D, pass, 0, t % P);
+          const uint8_t *s = cache + nv_offset(page, Hkv, h, P, D, pass, 1, t % P);
           uint8_t *dst = ws + ((cu_prefix[i] + t) * Hkv + h) * D;
           for (d = 0; d < D; ++d) {
             uint8_t code = (d & 1) ? (uint8_t)(c[d / 2] >> 4) : (uint8_t)(c[d / 2] & 15);

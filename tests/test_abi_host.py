@@ -24,7 +24,7 @@ def test_library_exports_every_header_function(nv):
 def _desc(nv, **kw):
     d = nv.nvkv_cache()
     d.prec, d.num_pages, d.page_size, d.num_kv_heads, d.head_dim = 0, 4, 16, 2, 128
-    d.k_data = d.v_data = d.k_scale = d.v_scale = 0x10000
+    d.data = 0x10000
     d.kv_scale = 0x20000
     for k, v in kw.items():
         setattr(d, k, v)
@@ -40,10 +40,11 @@ def test_write_argument_checks(nv):
     assert L.nvfp4_kv_quantize_write(None, None, 0, 1, None, None, None, None) == nv.NVKV_ERR_INVALID_ARG
     assert _write(nv, _desc(nv, head_dim=64)) == nv.NVKV_ERR_UNSUPPORTED
     assert _write(nv, _desc(nv, page_size=48)) == nv.NVKV_ERR_UNSUPPORTED
+    assert _write(nv, _desc(nv, page_size=128)) == nv.NVKV_ERR_UNSUPPORTED
     assert _write(nv, _desc(nv, prec=1)) == nv.NVKV_ERR_INVALID_ARG           # precision mismatch
     assert _write(nv, _desc(nv, prec=0), "fp8_kv_quantize_write") == nv.NVKV_ERR_INVALID_ARG
-    assert _write(nv, _desc(nv, k_scale=None)) == nv.NVKV_ERR_INVALID_ARG     # NVFP4 needs scale planes
-    assert _write(nv, _desc(nv, k_data=0x10008)) == nv.NVKV_ERR_UNSUPPORTED   # 16-byte alignment
+    assert _write(nv, _desc(nv, data=None)) == nv.NVKV_ERR_INVALID_ARG
+    assert _write(nv, _desc(nv, data=0x10008)) == nv.NVKV_ERR_UNSUPPORTED     # 16-byte alignment
     assert _write(nv, _desc(nv), n=0) == nv.NVKV_OK                           # nothing to do
     assert _write(nv, _desc(nv), n=-1) == nv.NVKV_ERR_INVALID_ARG
 
@@ -82,7 +83,7 @@ def test_other_entry_points_reject_bad_arguments(nv):
     assert L.nvkv_amax_update(0x10000, 3, 5, 0x20000, None) == nv.NVKV_ERR_INVALID_ARG
     assert L.nvkv_encode_e2m1(None, 4, None, None) == nv.NVKV_ERR_INVALID_ARG
     assert L.nvkv_encode_e4m3(None, 0, None, None) == nv.NVKV_OK
-    d = _desc(nv, prec=1, k_scale=None, v_scale=None)
+    d = _desc(nv, prec=1)
     assert L.nvfp4_kv_dequant_to_fp8_workspace(0x1000, 4, 0x1000, 0x1000, 0x1000, 2, ctypes.byref(d), 0x1000,
                                                0x2000, 0x3000, 10, None) == nv.NVKV_ERR_INVALID_ARG
     assert L.nvkv_status_string(4) == b"workspace too small"

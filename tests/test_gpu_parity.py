@@ -5,7 +5,7 @@ bit for bit; attention outputs (BF16) must satisfy
 |gpu - oracle| <= 2e-3 + 1e-2 * |oracle| element by element, the oracle being
 FP64 attention over the identical quantized bytes.  Cases are small enough for
 the oracle to finish in seconds yet span several 64-token tiles, ragged tails,
-empty sequences, page sizes 16..128, GQA groups 1..8 and forced splits.
+empty sequences, page sizes 16, 32 and 64, GQA groups 1..8 and forced splits.
 """
 import zlib
 
@@ -38,7 +38,6 @@ CASES = {
     "ragged_p64": dict(B=6, lens=(1, 63, 64, 65, 200, 1000)),
     "ragged_p16": dict(B=5, P=16, lens=(5, 16, 17, 100, 300)),
     "ragged_p32": dict(B=3, P=32, lens=(31, 33, 700)),
-    "ragged_p128": dict(B=3, P=128, lens=(127, 129, 640)),
     "empty_seqs": dict(B=4, lens=(0, 100, 0, 64)),
     "gqa8": dict(B=3, Hq=16, Hkv=2, lens=(70, 300, 129)),
     "gqa1": dict(B=2, Hq=4, Hkv=4, lens=(90, 257)),

@@ -194,3 +194,22 @@ def test_planted_mistakes_are_caught(orc):
     a = (x / den)
     b = (x * (np.float32(1) / den)).astype(np.float32)
     assert np.any(a != b)  # operation order matters in FP32
+
+
+def test_block_layout_offsets(orc):
+    """One contiguous block per (page, KV head): NVFP4 [K codes | K scales |
+    V codes | V scales], FP8 [K | V]; row = page offset."""
+    Hkv, P, D = 2, 4, 32
+    c = orc.Cache(orc.PREC_NVFP4, 3, Hkv, P, D, [1.0, 1.0])
+    x = np.zeros((1, Hkv, D), np.float32)
+    x[0, 1, 0] = 6.0  # head 1, element 0 -> code 7, scale 1.0 (0x38)
+    orc.quantize_write(c, x, 0.5 * x, np.array([2 * P + 3], np.int64))  # page 2, offset 3
+    blk = c.data[2, 1]
+    cb, sb = P * D // 2, P * D // 16
+    assert blk[3 * (D // 2)] == 0x07 and blk[cb + 3 * (D // 16)] == 0x38              # K: code 7, scale 1
+    assert blk[cb + sb + 3 * (D // 2)] == 0x07 and blk[2 * cb + sb + 3 * (D // 16)] == 0x30  # V: 3 = 6 x 0.5
+    assert np.count_nonzero(c.data) == 4
+    f = orc.Cache(orc.PREC_FP8, 3, Hkv, P, D, [1.0, 1.0])
+    orc.quantize_write(f, x, 0.5 * x, np.array([2 * P + 3], np.int64))
+    assert f.data[2, 1, 3 * D] == 0x4C and f.data[2, 1, P * D + 3 * D] == 0x44      # E4M3(6), E4M3(3)
+    assert np.count_nonzero(f.data) == 2
