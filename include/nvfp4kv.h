@@ -129,13 +129,13 @@ nvkv_status fp8_kv_quantize_write(const void *k, const void *v, nvkv_dtype dtype
 
 /* Bytes of decode workspace for this problem size: num_splits > 0 as passed to
  * the decode call, 0 for the library's choice on the current device.  The
- * workspace must be zero-filled once before its first use (for example with
- * nvkv_decode_workspace_init); every completed decode call leaves its counters
- * at zero again.  Returns 0 for unsupported sizes. */
+ * workspace holds the split-KV schedule and partial results; every decode call
+ * writes all of it that it later reads, so it needs no initialisation.
+ * Returns 0 for unsupported sizes. */
 size_t nvkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                   int32_t num_splits);
 
-/* Zero `bytes` of workspace on `stream` (a cudaMemsetAsync). */
+/* Zero `bytes` of workspace on `stream` (a cudaMemsetAsync); optional. */
 nvkv_status nvkv_decode_workspace_init(void *workspace, size_t bytes, void *stream);
 
 /* Paged GQA decode attention over the NVFP4 or FP8 cache ([P2] Three Paths:
@@ -155,8 +155,9 @@ nvkv_status nvkv_decode_workspace_init(void *workspace, size_t bytes, void *stre
  * Query head h reads KV head h / (num_q_heads / num_kv_heads); every token in
  * [0, seq_len) is visible.  out = softmax(q k^T * sm_scale) v with the FP32
  * result rounded to BF16.  Split partitions are merged with the log-sum-exp
- * rule inside the same kernel.  Requires num_q_heads / num_kv_heads <= 8 and
- * batch <= 1024. */
+ * rule by a second, small kernel chained to the first with programmatic
+ * dependent launch (two launches on `stream`).  Requires num_q_heads /
+ * num_kv_heads <= 8 and batch <= 1024. */
 nvkv_status nvfp4_paged_decode_attention(const void *q, const nvkv_cache *cache, const int32_t *block_table,
                                          int32_t max_pages, const int32_t *seq_lens, int32_t batch,
                                          int32_t num_q_heads, int32_t layer_precision, float sm_scale,
@@ -182,8 +183,8 @@ nvkv_status fp8_paged_decode_attention(const void *q, const nvkv_cache *cache, c
  * NVKV_ERR_WORKSPACE_TOO_SMALL before any launch.  The first call on a device
  * looks up the array's device address (set-up, once per device, with that
  * device current); make that first call before any stream capture.  Each call
- * clears the array's counters on `stream` before its kernel.  All calls share
- * the one array and it keeps the last call's contents, so calls that can
+ * writes all of the array it reads, so nothing needs clearing between calls.
+ * All calls share the one array and it keeps the last call's contents, so calls that can
  * overlap on the GPU (different streams, different host threads without
  * ordering) race and give wrong results: order them on one stream.  No
  * cudaMalloc, cudaFree or allocating library routine is called. */

@@ -77,7 +77,7 @@ struct DecodeArgs {
   int32_t B, Hq, G;
   float sm_scale;
   int32_t num_ctas;
-  int32_t *counters;  // [B * Hkv]
+  int32_t *meta;      // written by CTA 0: cum[0..B] (tiles before each sequence), then NC
   float *partials;    // [num_ctas][2][kSlotFloats]
   __nv_bfloat16 *out;
 };
@@ -89,7 +89,7 @@ constexpr int smem_bytes_for(int G) {
          + (kMaxBatch + 1) * 4                                 // tile prefix sums
          + kConsumerWarps * G * kD * 4                         // warp merge: o
          + kConsumerWarps * kMaxGroup * 2 * 4                  // warp merge: m, l
-         + 4 * (4 + Layout<PREC>::kStages);                    // abort, fills, bcast
+         + 4 * (1 + Layout<PREC>::kStages);                    // abort, fills
 }
 
 // Segment = run of consecutive units of one (sequence, KV head).
@@ -294,13 +294,12 @@ __device__ __forceinline__ void pv_mma_nvfp4(float (&o)[4], uint32_t xAB, uint32
                 hmul2_u32(f16x2_from_e2m1x2<I>(xCD), sCD), hmul2_u32(f16x2_from_e2m1x2<I>(yCD), sCD), b0, b1);
 }
 
-// One warp's 16-token slice: scores, online-softmax update, P.V.
-// nvalid = valid tokens of the slice (1..16).
+// Scores of one 16-token slice for this thread: rows r (s[0], s[1]) and r + 8
+// (s[2], s[3]), heads 2c, 2c+1; scaled to log2 units; -inf past nvalid.
 template <int PREC>
-__device__ __forceinline__ void consume_slice(Slice<PREC> &x, int nvalid, int r, int c, const uint32_t (&qf)[8][2],
-                                              const float (&cs)[2], WarpState &st) {
-  // ---- scores: two independent MMA chains (even / odd k-steps) ----
-  float e[4] = {0.f, 0.f, 0.f, 0.f}, od[4] = {0.f, 0.f, 0.f, 0.f};
+__device__ __forceinline__ void slice_scores(const Slice<PREC> &x, int nvalid, int r, const uint32_t (&qf)[8][2],
+                                             const float (&cs)[2], float (&sc)[4]) {
+  float e[4] = {0.f, 0.f, 0.f, 0.f}, od[4] = {0.f, 0.f, 0.f, 0.f};  // even / odd k-step chains
   uint32_t lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
   if constexpr (PREC == NVKV_PREC_NVFP4) {
     const uint32_t sc0 = f16x2_from_e4m3x2<0>(x.ks0), sc1 = f16x2_from_e4m3x2<0>(x.ks1);
@@ -317,43 +316,16 @@ __device__ __forceinline__ void consume_slice(Slice<PREC> &x, int nvalid, int r,
   qk_step<PREC, 5>(x, lo0, hi0, lo1, hi1, qf, od);
   qk_step<PREC, 6>(x, lo0, hi0, lo1, hi1, qf, e);
   qk_step<PREC, 7>(x, lo0, hi0, lo1, hi1, qf, od);
-  float s0 = (e[0] + od[0]) * cs[0], s1 = (e[1] + od[1]) * cs[1];  // token r
-  float s2 = (e[2] + od[2]) * cs[0], s3 = (e[3] + od[3]) * cs[1];  // token r + 8
-  if (nvalid < kSub) {
-    if (r >= nvalid) s0 = s1 = -INFINITY;
-    if (r + 8 >= nvalid) s2 = s3 = -INFINITY;
-  }
-  // ---- online softmax: max over the slice's 16 tokens, per head ----
-  float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-  }
-  const bool need = (mx0 > st.m[0] + kRescaleThreshold) || (mx1 > st.m[1] + kRescaleThreshold);
-  if (__any_sync(0xffffffffu, need)) {
-    const float n0 = fmaxf(st.m[0], mx0), n1 = fmaxf(st.m[1], mx1);
-    const float al0 = ex2(st.m[0] - n0), al1 = ex2(st.m[1] - n1);
-    st.m[0] = n0;
-    st.m[1] = n1;
-    st.l[0] *= al0;
-    st.l[1] *= al1;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      st.o[j][0] *= al0;
-      st.o[j][1] *= al1;
-      st.o[j][2] *= al0;
-      st.o[j][3] *= al1;
-    }
-  }
-  const float p0 = ex2(s0 - st.m[0]), p1 = ex2(s1 - st.m[1]);
-  const float p2 = ex2(s2 - st.m[0]), p3 = ex2(s3 - st.m[1]);
-  st.l[0] += p0 + p2;
-  st.l[1] += p1 + p3;
-  const uint32_t b0 = movmatrix_trans(pack_f16x2(p0, p1));  // P[tok 2c, 2c+1][head r]
-  const uint32_t b1 = movmatrix_trans(pack_f16x2(p2, p3));  // P[tok 2c+8, 2c+9][head r]
+  const bool v0 = r < nvalid, v1 = r + 8 < nvalid;
+  sc[0] = v0 ? (e[0] + od[0]) * cs[0] : -INFINITY;
+  sc[1] = v0 ? (e[1] + od[1]) * cs[1] : -INFINITY;
+  sc[2] = v1 ? (e[2] + od[2]) * cs[0] : -INFINITY;
+  sc[3] = v1 ? (e[3] + od[3]) * cs[1] : -INFINITY;
+}
 
-  // ---- P.V ----
+// O += V^T P^T for one slice (b0, b1: the P fragments of its tokens).
+template <int PREC>
+__device__ __forceinline__ void slice_pv(Slice<PREC> &x, int nvalid, int c, uint32_t b0, uint32_t b1, WarpState &st) {
   const int tA = 2 * c;
   if constexpr (PREC == NVKV_PREC_NVFP4) {
     uint32_t sv = x.vsc;
@@ -399,91 +371,75 @@ __device__ __forceinline__ void consume_slice(Slice<PREC> &x, int nvalid, int r,
   }
 }
 
-// Merge of the split-KV partials of one (sequence, KV head) by the 128
-// consumer threads of the last-arriving CTA.  Contributor k's partial is
-// (o_k[G][128], m_k[G], l_k[G]) in log2 units; out = sum_k 2^(m_k - M) o_k /
-// sum_k 2^(m_k - M) l_k with M = max_k m_k, times g_V.  `wbuf` (>= 4 * G * 128
-// floats) and `red` (>= 64 floats) are free shared memory.
-__device__ __forceinline__ void merge_partials(const DecodeArgs &a, int64_t c_first, int ncontrib, int64_t W, int64_t NC,
-                                            int64_t ubh0, int b, int h, float vscale, float *wbuf, float *red) {
-  constexpr int kT = kConsumerWarps * 32;
-  const int G = a.G, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int hd = tid % G;     // kT % G == 0: a thread always serves the same head
-  const int kstep = kT / G;   // contributors visited per pass step
-  const int cap = kConsumerWarps * kD;  // contributors whose weights fit in wbuf per chunk
-  auto stats = [&](int k) -> const float * {
-    const int64_t cc = c_first + k;
-    const int sl = share_begin(cc, W, NC) >= ubh0 ? 0 : 1;
-    return a.partials + (cc * 2 + sl) * kSlotFloats;
-  };
-  auto reduce = [&](float v, bool is_max) -> float {  // over threads with the same head
-    for (int o = G; o < 32; o <<= 1) {
-      const float y = __shfl_xor_sync(0xffffffffu, v, o);
-      v = is_max ? fmaxf(v, y) : v + y;
-    }
-    named_bar_sync(1, kT);
-    if (lane < G) red[warp * kMaxGroup + lane] = v;
-    named_bar_sync(1, kT);
-    float t = red[hd];
+// NS slices of consecutive stages: scores, one online-softmax update over all
+// 16 * NS tokens, P.V.  nvalid[i] = valid tokens of slice i (0..16).  The
+// kernel uses NS = 1: two slices per update hold twice the operand registers
+// and ran slower (spills at three CTAs per SM).
+template <int PREC, int NS>
+__device__ __forceinline__ void consume(Slice<PREC> (&x)[NS], const int (&nvalid)[NS], int r, int c,
+                                        const uint32_t (&qf)[8][2], const float (&cs)[2], WarpState &st) {
+  float sc[NS][4];
 #pragma unroll
-    for (int w = 1; w < kConsumerWarps; ++w) t = is_max ? fmaxf(t, red[w * kMaxGroup + hd]) : t + red[w * kMaxGroup + hd];
-    return t;
-  };
-  // pass A: M per head
-  float m = -INFINITY;
-  for (int k = tid / G; k < ncontrib; k += kstep) m = fmaxf(m, __ldcg(stats(k) + kMaxGroup * kD + hd));
-  const float M = reduce(m, true);
-  float acc[kMaxGroup];
+  for (int i = 0; i < NS; ++i) slice_scores<PREC>(x[i], nvalid[i], r, qf, cs, sc[i]);
+  float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < kMaxGroup; ++j) acc[j] = 0.0f;
-  float lsum = 0.0f;
-  for (int k0 = 0; k0 < ncontrib; k0 += cap) {
-    const int kn = min(cap, ncontrib - k0);
-    // pass B: weights of this chunk into shared memory, l partial sums
-    named_bar_sync(1, kT);
-    for (int k = tid / G; k < kn; k += kstep) {
-      const float *st = stats(k0 + k);
-      const float mk = __ldcg(st + kMaxGroup * kD + hd);
-      const float w = mk == -INFINITY ? 0.0f : ex2(mk - M);
-      wbuf[k * G + hd] = w;
-      lsum += w * __ldcg(st + kMaxGroup * kD + kMaxGroup + hd);
-    }
-    named_bar_sync(1, kT);
-    // pass C: thread = d; heads in groups of four, eight contributors per batch in flight
-    for (int j0 = 0; j0 < G; j0 += 4) {
-      for (int k = 0; k < kn; k += 8) {
-        float v[8][4];
+  for (int i = 0; i < NS; ++i) {
+    mx0 = fmaxf(mx0, fmaxf(sc[i][0], sc[i][2]));
+    mx1 = fmaxf(mx1, fmaxf(sc[i][1], sc[i][3]));
+  }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+  for (int o = 4; o < 32; o <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+  }
+  const bool need = (mx0 > st.m[0] + kRescaleThreshold) || (mx1 > st.m[1] + kRescaleThreshold);
+  if (__any_sync(0xffffffffu, need)) {
+    const float n0 = fmaxf(st.m[0], mx0), n1 = fmaxf(st.m[1], mx1);
+    const float al0 = ex2(st.m[0] - n0), al1 = ex2(st.m[1] - n1);
+    st.m[0] = n0;
+    st.m[1] = n1;
+    st.l[0] *= al0;
+    st.l[1] *= al1;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            v[q][j] = (j0 + j < G && k + q < kn) ? __ldcg(stats(k0 + k + q) + (j0 + j) * kD + tid) : 0.0f;
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (j0 + j < G && k + q < kn) {
-              const float w = wbuf[(k + q) * G + j0 + j] * v[q][j];
-              if (j0 == 0) acc[j] += w;
-              else acc[4 + j] += w;
-            }
-        }
-      }
+    for (int j = 0; j < 8; ++j) {
+      st.o[j][0] *= al0;
+      st.o[j][1] *= al1;
+      st.o[j][2] *= al0;
+      st.o[j][3] *= al1;
     }
   }
-  const float L = reduce(lsum, false);  // every thread now holds L of head `hd`
-  // thread d writes all heads; the L of head j sits in red after the reduce
+  uint32_t b[NS][2];
 #pragma unroll
-  for (int j = 0; j < kMaxGroup; ++j) {
-    if (j < G) {
-      float Lj = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) Lj += red[w * kMaxGroup + j];
-      a.out[(static_cast<int64_t>(b) * a.Hq + h * G + j) * kD + tid] = __float2bfloat16_rn(acc[j] * (vscale / Lj));
-    }
+  for (int i = 0; i < NS; ++i) {
+    const float p0 = ex2(sc[i][0] - st.m[0]), p1 = ex2(sc[i][1] - st.m[1]);
+    const float p2 = ex2(sc[i][2] - st.m[0]), p3 = ex2(sc[i][3] - st.m[1]);
+    st.l[0] += p0 + p2;
+    st.l[1] += p1 + p3;
+    b[i][0] = movmatrix_trans(pack_f16x2(p0, p1));  // P[tok 2c, 2c+1][head r]
+    b[i][1] = movmatrix_trans(pack_f16x2(p2, p3));  // P[tok 2c+8, 2c+9][head r]
   }
-  (void)L;
+#pragma unroll
+  for (int i = 0; i < NS; ++i) slice_pv<PREC>(x[i], nvalid[i], c, b[i][0], b[i][1], st);
+}
+
+// The warp's 16-token slice of the next stage: wait for it, copy it to
+// registers, release the stage and advance the ring position.  rem = tokens of
+// the sequence from the slice's first token on.
+template <int PREC>
+__device__ __forceinline__ bool fetch_slice(uint64_t *full, uint64_t *empty, const uint8_t *ring,
+                                            const SliceOffsets<PREC> &so, int &slot, uint32_t &phase,
+                                            volatile int *abort, int64_t rem, int r, int c, int lane, Slice<PREC> &x,
+                                            int &nvalid) {
+  const bool ready = mbar_wait_bounded(&full[slot], phase, abort);
+  nvalid = rem < kSub ? (rem > 0 ? static_cast<int>(rem) : 0) : kSub;
+  if (nvalid > 0) load_slice<PREC>(ring + static_cast<size_t>(slot) * Layout<PREC>::kStageBytes, so, r, c, x);
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&empty[slot]);
+  if (++slot == Layout<PREC>::kStages) {
+    slot = 0;
+    phase ^= 1u;
+  }
+  return __all_sync(0xffffffffu, ready);
 }
 
 template <int PREC>
@@ -499,7 +455,6 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
   int *flags = reinterpret_cast<int *>(mrg_ml + kConsumerWarps * kMaxGroup * 2);
   volatile int *abort = flags;              // flags[0]
   int *fills = flags + 1;                   // flags[1 .. kStages]: fills issued per slot
-  int *bcast = flags + 1 + Lay::kStages;    // 3 ints
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = a.c.Hkv, B = a.B, G = a.G;
@@ -549,6 +504,12 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
   const int64_t u0 = active ? share_begin(blockIdx.x, W, NC) : 0;
   const int64_t u1 = active ? share_begin(blockIdx.x + 1, W, NC) : 0;
 
+  // the combine kernel needs the same schedule: CTA 0 publishes it
+  if (blockIdx.x == 0) {
+    for (int b = tid; b <= B; b += kThreads) a.meta[b] = cum[b];
+    if (tid == 0) a.meta[B + 1] = static_cast<int32_t>(NC);
+  }
+
   // zero rows of empty sequences (spread over CTAs)
   for (int b = blockIdx.x; b < B; b += a.num_ctas) {
     if (cum[b + 1] == cum[b]) {
@@ -564,7 +525,8 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
     const SliceOffsets<PREC> so(warp, a.c.P);
     const float kscale = __fmul_rn(a.c.scale[0], a.sm_scale * 1.4426950408889634f);
     const float vscale = a.c.scale[1];
-    int64_t i = 0;
+    int slot = 0;          // ring position and parity of the next stage this warp reads
+    uint32_t phase = 0;
     for (int64_t u = u0; u < u1;) {
       const Seg s = seg_at(u, u1, cum, B, Hkv);
       const int64_t Lb = clamped_len(a, s.b);
@@ -618,21 +580,13 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
 
       const int ntiles = s.t1 - s.t0;
       for (int k = 0; k < ntiles; ++k) {
-        const int64_t gi = i + k;
-        const int slot = static_cast<int>(gi % Lay::kStages);
-        const uint32_t fill = static_cast<uint32_t>(gi / Lay::kStages);
-        // Every consumer warp reads every stage in order, so the phase this
-        // warp waits for is always the slot's current one.
-        const bool ready = mbar_wait_bounded(&full[slot], fill & 1u, abort);
-        const int64_t rem = Lb - static_cast<int64_t>(s.t0 + k) * kTile - kSub * warp;
-        const int nvalid = rem < kSub ? static_cast<int>(rem) : kSub;
-        Slice<PREC> x;
-        if (nvalid > 0) load_slice<PREC>(ring + static_cast<size_t>(slot) * Lay::kStageBytes, so, r, c, x);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);  // the slice is in registers: release the stage
-        if (__all_sync(0xffffffffu, ready) && nvalid > 0) consume_slice<PREC>(x, nvalid, r, c, qf, cs, st);
+        Slice<PREC> x[1];
+        int nv[1];
+        const bool ok = fetch_slice<PREC>(full, empty, ring, so, slot, phase, abort,
+                                          Lb - static_cast<int64_t>(s.t0 + k) * kTile - kSub * warp, r, c, lane, x[0],
+                                          nv[0]);
+        if (ok && nv[0] > 0) consume<PREC, 1>(x, nv, r, c, qf, cs, st);
       }
-      i += ntiles;
 
       // ---- merge the four warps: (m, l) per head, O per (head, d) ----
 #pragma unroll
@@ -660,7 +614,6 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
 
       const int nb = cum[s.b + 1] - cum[s.b];
       const bool complete = (s.t0 == 0) && (s.t1 == nb);
-      const int64_t ubh0 = static_cast<int64_t>(cum[s.b]) * Hkv + static_cast<int64_t>(s.h) * nb;
       const int slot_id = (u == u0) ? 0 : 1;
       float *part = a.partials + (static_cast<int64_t>(blockIdx.x) * 2 + slot_id) * kSlotFloats;
       for (int e = tid; e < G * kD; e += kConsumerWarps * 32) {
@@ -686,33 +639,13 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
           }
         }
       }
-      if (!complete) {
-        __threadfence();
-        named_bar_sync(1, kConsumerWarps * 32);
-        if (tid == 0) {
-          const int64_t c_first = owner_of(ubh0, W, NC), c_last = owner_of(ubh0 + nb - 1, W, NC);
-          const int contributors = static_cast<int>(c_last - c_first + 1);
-          const int old = atomicAdd(&a.counters[s.b * Hkv + s.h], 1);
-          bcast[0] = (old == contributors - 1) ? 1 : 0;
-          bcast[1] = static_cast<int>(c_first);
-          bcast[2] = contributors;
-          __threadfence();
-        }
-        named_bar_sync(1, kConsumerWarps * 32);
-        if (bcast[0]) {
-          // Last arriver: merge every contributor's partial with the
-          // log-sum-exp rule.  Statistics are fetched in parallel and the
-          // weighted sum keeps all contributors' loads in flight, so the merge
-          // costs a few L2 round trips instead of one per contributor.
-          merge_partials(a, bcast[1], bcast[2], W, NC, ubh0, s.b, s.h, vscale, mrg_o, mrg_ml);
-          if (tid == 0) a.counters[s.b * Hkv + s.h] = 0;
-        }
-      }
       named_bar_sync(1, kConsumerWarps * 32);
       u += ntiles;
     }
   }
 
+  // this CTA's partials are written: the combine grid may start launching
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __syncthreads();
   // after a timeout, wait (bounded) for copies still in flight before the CTA exits
   if (*abort) {
@@ -723,6 +656,76 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
         if (fills[s] > 0) mbar_wait_bounded(&full[s], static_cast<uint32_t>(fills[s] - 1) & 1u, &never);
     }
   }
+}
+
+
+// ---------------------------------------------------------------------------
+// Split-KV merge (log-sum-exp rule), one CTA per (sequence, KV head, query
+// head of the group), thread = head_dim element.  Runs after the decode grid
+// (programmatic dependent launch: griddepcontrol.wait returns once the decode
+// grid has completed and its writes are visible).  Contributor k of a
+// (sequence, KV head) left (o_k, m_k, l_k) in log2 units; out = sum_k
+// 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k * g_V, M = max_k m_k.  (Sequence,
+// head) pairs that one CTA covered entirely were written by the decode grid.
+// ---------------------------------------------------------------------------
+struct CombineArgs {
+  const int32_t *meta;
+  const float *partials;
+  const float *scale;
+  int32_t B, Hkv, Hq, G;
+  __nv_bfloat16 *out;
+};
+
+constexpr int kCombineThreads = kD;
+constexpr int kCombineBatch = 16;  // contributors whose loads are in flight together
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
+  const int tid = threadIdx.x;
+  const int hd = blockIdx.x % a.G, bh = blockIdx.x / a.G, h = bh % a.Hkv, b = bh / a.Hkv;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int32_t c0 = a.meta[b], c1 = a.meta[b + 1];
+  const int nb = c1 - c0;
+  if (nb == 0) return;
+  const int64_t W = static_cast<int64_t>(a.meta[a.B]) * a.Hkv, NC = a.meta[a.B + 1];
+  const int64_t ubh0 = static_cast<int64_t>(c0) * a.Hkv + static_cast<int64_t>(h) * nb;
+  const int64_t c_first = owner_of(ubh0, W, NC);
+  const int n = static_cast<int>(owner_of(ubh0 + nb - 1, W, NC) - c_first + 1);
+  if (n == 1) return;  // written directly by the decode grid
+  // Every thread (one head_dim element) loads the statistics and its element
+  // of a batch of contributors at once and folds them into a running
+  // (max, sum, acc) triple: one round trip per batch, no block reductions.
+  float M = -INFINITY, L = 0.0f, acc = 0.0f;
+  for (int k0 = 0; k0 < n; k0 += kCombineBatch) {
+    float m[kCombineBatch], l[kCombineBatch], o[kCombineBatch];
+#pragma unroll
+    for (int q = 0; q < kCombineBatch; ++q) {
+      if (k0 + q < n) {
+        const int64_t cc = c_first + k0 + q;
+        const float *st = a.partials + (cc * 2 + (share_begin(cc, W, NC) >= ubh0 ? 0 : 1)) * kSlotFloats;
+        m[q] = st[kMaxGroup * kD + hd];
+        l[q] = st[kMaxGroup * kD + kMaxGroup + hd];
+        o[q] = st[hd * kD + tid];
+      } else {
+        m[q] = -INFINITY;
+        l[q] = 0.0f;
+        o[q] = 0.0f;
+      }
+    }
+    float mb = M;
+#pragma unroll
+    for (int q = 0; q < kCombineBatch; ++q) mb = fmaxf(mb, m[q]);
+    const float r = M == -INFINITY ? 0.0f : ex2(M - mb);
+    L *= r;
+    acc *= r;
+#pragma unroll
+    for (int q = 0; q < kCombineBatch; ++q) {
+      const float w = m[q] == -INFINITY ? 0.0f : ex2(m[q] - mb);
+      L += w * l[q];
+      acc += w * o[q];
+    }
+    M = mb;
+  }
+  a.out[(static_cast<int64_t>(b) * a.Hq + h * a.G + hd) * kD + tid] = __float2bfloat16_rn(acc * (a.scale[1] / L));
 }
 
 // ---------------------------------------------------------------------------
@@ -776,10 +779,12 @@ int64_t num_ctas_for(int prec, int32_t batch, int32_t Hkv, int32_t G, int64_t ma
   return n < 1 ? 1 : n;
 }
 
-size_t counters_bytes(int32_t batch, int32_t Hkv) { return (static_cast<size_t>(batch) * Hkv * 4 + 255) / 256 * 256; }
+// Workspace = schedule (cum[0..B], NC) + two partial slots per CTA.
+size_t meta_bytes(int32_t batch) { return (static_cast<size_t>(batch + 2) * 4 + 255) / 256 * 256; }
 
 size_t workspace_bytes_for(int32_t batch, int32_t Hkv, int64_t nctas) {
-  return counters_bytes(batch, Hkv) + static_cast<size_t>(nctas) * 2 * kSlotFloats * sizeof(float);
+  (void)Hkv;
+  return meta_bytes(batch) + static_cast<size_t>(nctas) * 2 * kSlotFloats * sizeof(float);
 }
 
 nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t *block_table, int32_t max_pages,
@@ -816,8 +821,8 @@ nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t 
   a.G = G;
   a.sm_scale = sm_scale > 0.0f ? sm_scale : 1.0f / sqrtf(static_cast<float>(cache->head_dim));
   a.num_ctas = static_cast<int32_t>(nctas);
-  a.counters = static_cast<int32_t *>(workspace);
-  a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + counters_bytes(batch, Hkv));
+  a.meta = static_cast<int32_t *>(workspace);
+  a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + meta_bytes(batch));
   a.out = static_cast<__nv_bfloat16 *>(out);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (prec == NVKV_PREC_NVFP4)
@@ -825,6 +830,33 @@ nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t 
   else
     decode_kernel<NVKV_PREC_FP8_E4M3>
         <<<static_cast<int>(nctas), kThreads, smem_bytes_for<NVKV_PREC_FP8_E4M3>(G), s>>>(a);
+  st = launch_status();
+  if (st != NVKV_OK) return st;
+  // split-KV merge, launched as a programmatic dependent of the decode grid
+  CombineArgs ca;
+  ca.meta = a.meta;
+  ca.partials = a.partials;
+  ca.scale = a.c.scale;
+  ca.B = batch;
+  ca.Hkv = Hkv;
+  ca.Hq = num_q_heads;
+  ca.G = G;
+  ca.out = a.out;
+  const int64_t cgrid = static_cast<int64_t>(batch) * Hkv * G;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cgrid));
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, combine_kernel, ca) != cudaSuccess) {
+    cudaGetLastError();  // clear, then fall back to an ordinary stream-ordered launch
+    combine_kernel<<<static_cast<unsigned>(cgrid), kCombineThreads, 0, s>>>(ca);
+  }
   return launch_status();
 }
 
@@ -878,10 +910,7 @@ nvkv_status nvfp4_paged_decode_attention_noalloc(const void *q, const nvkv_cache
   if (batch == 0) return NVKV_OK;
   void *scratch = noalloc_scratch_ptr();
   if (!scratch) return NVKV_ERR_CUDA;
-  // the arrival counters must start at zero; the partial slots are always written before they are read
-  const size_t zero = counters_bytes(batch, cache->num_kv_heads);
-  if (zero > NVKV_NOALLOC_SCRATCH_BYTES) return NVKV_ERR_WORKSPACE_TOO_SMALL;
-  if (cudaMemsetAsync(scratch, 0, zero, static_cast<cudaStream_t>(stream)) != cudaSuccess) return NVKV_ERR_CUDA;
+  // every call rewrites the scratch it later reads (schedule and partials): nothing needs clearing
   return decode_common(q, cache, block_table, max_pages, seq_lens, batch, num_q_heads, layer_precision, sm_scale,
                        num_splits, scratch, NVKV_NOALLOC_SCRATCH_BYTES, out, stream);
 }
