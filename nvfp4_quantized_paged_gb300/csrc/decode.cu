@@ -191,6 +191,12 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
 // query fragment uses the same order.  P.V: MMA rows = head_dim (thread r owns
 // d in [16r, 16r+16)), k = tokens 2c, 2c+1, 2c+8, 2c+9, n = query head.  O for
 // heads 2c, 2c+1 of the group and d in [16r, 16r+16) lives in 32 registers.
+//
+// The warp runs its slices as a two-deep software pipeline: while the P.V
+// MMAs of slice i issue, the score MMAs of slice i+1 issue between them (the
+// two chains are independent), and the softmax of slice i+1 follows.  K of a
+// slice is read from shared memory when its scores start, V when its P.V
+// starts; the stage is released after both.
 // ---------------------------------------------------------------------------
 struct WarpState {
   float o[8][4];
@@ -218,37 +224,39 @@ struct SliceOffsets {
   }
 };
 
-// A warp's 16-token slice, copied out of the stage.
+// K operand of a slice: code words of rows r, r + 8 and (NVFP4) their block
+// scales as f16x2 pairs {S, S} for d blocks 2c (lo) and 2c + 1 (hi).
 template <int PREC>
-struct Slice {
-  uint32_t k0[PREC == NVKV_PREC_NVFP4 ? 4 : 8], k1[PREC == NVKV_PREC_NVFP4 ? 4 : 8];  // K rows r, r+8
-  uint32_t ks0, ks1;                                                                 // their scales (NVFP4)
-  uint32_t va[PREC == NVKV_PREC_NVFP4 ? 2 : 4], vb[PREC == NVKV_PREC_NVFP4 ? 2 : 4];  // V tokens 2c, 2c+1
-  uint32_t vc[PREC == NVKV_PREC_NVFP4 ? 2 : 4], vd[PREC == NVKV_PREC_NVFP4 ? 2 : 4];  // V tokens 2c+8, 2c+9
-  uint32_t vsc;                                                                      // 4 V scale bytes
+struct KOps {
+  uint32_t k0[PREC == NVKV_PREC_NVFP4 ? 4 : 8], k1[PREC == NVKV_PREC_NVFP4 ? 4 : 8];
+  uint32_t lo0, hi0, lo1, hi1;
+};
+
+// V operand of a slice.  NVFP4: per 8-byte half w, the e2m1 pairs of tokens
+// (2c, 2c+1) at d and d + 1 (x, y) and of tokens (2c+8, 2c+9) (z, t), and the
+// f16x2 block scales of those token pairs; masked tokens carry scale 0.  FP8:
+// the raw code words of tokens 2c, 2c+1, 2c+8, 2c+9, masked tokens zeroed.
+template <int PREC>
+struct VOps {
+  uint32_t w[PREC == NVKV_PREC_NVFP4 ? 2 : 4][4];
+  uint32_t sAB, sCD;
 };
 
 template <int PREC>
-__device__ __forceinline__ void load_slice(const uint8_t *stage, const SliceOffsets<PREC> &o, int r, int c,
-                                           Slice<PREC> &x) {
+__device__ __forceinline__ void load_k(const uint8_t *stage, const SliceOffsets<PREC> &o, int r, int c,
+                                       KOps<PREC> &x) {
   if constexpr (PREC == NVKV_PREC_NVFP4) {
     const uint4 a = *reinterpret_cast<const uint4 *>(stage + o.kc + r * kNvCodeRow + 16 * c);
     const uint4 b = *reinterpret_cast<const uint4 *>(stage + o.kc + (r + 8) * kNvCodeRow + 16 * c);
     x.k0[0] = a.x; x.k0[1] = a.y; x.k0[2] = a.z; x.k0[3] = a.w;
     x.k1[0] = b.x; x.k1[1] = b.y; x.k1[2] = b.z; x.k1[3] = b.w;
-    x.ks0 = *reinterpret_cast<const uint16_t *>(stage + o.ks + r * kNvScaleRow + 2 * c);
-    x.ks1 = *reinterpret_cast<const uint16_t *>(stage + o.ks + (r + 8) * kNvScaleRow + 2 * c);
-    const int tA = 2 * c;
-    const uint2 A = *reinterpret_cast<const uint2 *>(stage + o.vc + tA * kNvCodeRow + 8 * r);
-    const uint2 B = *reinterpret_cast<const uint2 *>(stage + o.vc + (tA + 1) * kNvCodeRow + 8 * r);
-    const uint2 C = *reinterpret_cast<const uint2 *>(stage + o.vc + (tA + 8) * kNvCodeRow + 8 * r);
-    const uint2 D = *reinterpret_cast<const uint2 *>(stage + o.vc + (tA + 9) * kNvCodeRow + 8 * r);
-    x.va[0] = A.x; x.va[1] = A.y; x.vb[0] = B.x; x.vb[1] = B.y;
-    x.vc[0] = C.x; x.vc[1] = C.y; x.vd[0] = D.x; x.vd[1] = D.y;
-    const uint8_t *vs = stage + o.vs + r;
-    x.vsc = static_cast<uint32_t>(vs[tA * kNvScaleRow]) | (static_cast<uint32_t>(vs[(tA + 1) * kNvScaleRow]) << 8) |
-            (static_cast<uint32_t>(vs[(tA + 8) * kNvScaleRow]) << 16) |
-            (static_cast<uint32_t>(vs[(tA + 9) * kNvScaleRow]) << 24);
+    const uint32_t s0 = *reinterpret_cast<const uint16_t *>(stage + o.ks + r * kNvScaleRow + 2 * c);
+    const uint32_t s1 = *reinterpret_cast<const uint16_t *>(stage + o.ks + (r + 8) * kNvScaleRow + 2 * c);
+    const uint32_t h0 = f16x2_from_e4m3x2<0>(s0), h1 = f16x2_from_e4m3x2<0>(s1);
+    x.lo0 = prmt(h0, 0, 0x1010);  // {S_2c, S_2c}
+    x.hi0 = prmt(h0, 0, 0x3232);  // {S_2c+1, S_2c+1}
+    x.lo1 = prmt(h1, 0, 0x1010);
+    x.hi1 = prmt(h1, 0, 0x3232);
   } else {
     const uint4 *p0 = reinterpret_cast<const uint4 *>(stage + o.kc + r * kF8Row + 32 * c);
     const uint4 *p1 = reinterpret_cast<const uint4 *>(stage + o.kc + (r + 8) * kF8Row + 32 * c);
@@ -257,24 +265,70 @@ __device__ __forceinline__ void load_slice(const uint8_t *stage, const SliceOffs
     x.k0[4] = a1.x; x.k0[5] = a1.y; x.k0[6] = a1.z; x.k0[7] = a1.w;
     x.k1[0] = b0.x; x.k1[1] = b0.y; x.k1[2] = b0.z; x.k1[3] = b0.w;
     x.k1[4] = b1.x; x.k1[5] = b1.y; x.k1[6] = b1.z; x.k1[7] = b1.w;
-    const int tA = 2 * c;
+    x.lo0 = x.hi0 = x.lo1 = x.hi1 = 0;
+  }
+}
+
+// nvalid = valid tokens of the slice (0..16): tokens past it are masked.
+template <int PREC>
+__device__ __forceinline__ void load_v(const uint8_t *stage, const SliceOffsets<PREC> &o, int r, int c, int nvalid,
+                                       VOps<PREC> &x) {
+  const int tA = 2 * c;
+  if constexpr (PREC == NVKV_PREC_NVFP4) {
+    const uint2 A = *reinterpret_cast<const uint2 *>(stage + o.vc + tA * kNvCodeRow + 8 * r);
+    const uint2 B = *reinterpret_cast<const uint2 *>(stage + o.vc + (tA + 1) * kNvCodeRow + 8 * r);
+    const uint2 C = *reinterpret_cast<const uint2 *>(stage + o.vc + (tA + 8) * kNvCodeRow + 8 * r);
+    const uint2 D = *reinterpret_cast<const uint2 *>(stage + o.vc + (tA + 9) * kNvCodeRow + 8 * r);
+    const uint8_t *vs = stage + o.vs + r;
+    uint32_t sv = static_cast<uint32_t>(vs[tA * kNvScaleRow]) | (static_cast<uint32_t>(vs[(tA + 1) * kNvScaleRow]) << 8) |
+                  (static_cast<uint32_t>(vs[(tA + 8) * kNvScaleRow]) << 16) |
+                  (static_cast<uint32_t>(vs[(tA + 9) * kNvScaleRow]) << 24);
+    if (nvalid < kSub) {  // masked tokens get scale 0 -> value 0 (codes are finite)
+      if (tA >= nvalid) sv &= 0xFFFFFF00u;
+      if (tA + 1 >= nvalid) sv &= 0xFFFF00FFu;
+      if (tA + 8 >= nvalid) sv &= 0xFF00FFFFu;
+      if (tA + 9 >= nvalid) sv &= 0x00FFFFFFu;
+    }
+    x.sAB = f16x2_from_e4m3x2<0>(sv);
+    x.sCD = f16x2_from_e4m3x2<1>(sv);
+    const uint32_t a[2] = {A.x, A.y}, b[2] = {B.x, B.y}, cc[2] = {C.x, C.y}, dd[2] = {D.x, D.y};
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      // byte j: the token pair's low nibbles (d = 16r + 2j') or high nibbles (d + 1)
+      x.w[w][0] = (a[w] & 0x0F0F0F0Fu) | ((b[w] & 0x0F0F0F0Fu) << 4);
+      x.w[w][1] = ((a[w] >> 4) & 0x0F0F0F0Fu) | (b[w] & 0xF0F0F0F0u);
+      x.w[w][2] = (cc[w] & 0x0F0F0F0Fu) | ((dd[w] & 0x0F0F0F0Fu) << 4);
+      x.w[w][3] = ((cc[w] >> 4) & 0x0F0F0F0Fu) | (dd[w] & 0xF0F0F0F0u);
+    }
+  } else {
     const uint4 A = *reinterpret_cast<const uint4 *>(stage + o.vc + tA * kF8Row + 16 * r);
     const uint4 B = *reinterpret_cast<const uint4 *>(stage + o.vc + (tA + 1) * kF8Row + 16 * r);
     const uint4 C = *reinterpret_cast<const uint4 *>(stage + o.vc + (tA + 8) * kF8Row + 16 * r);
     const uint4 D = *reinterpret_cast<const uint4 *>(stage + o.vc + (tA + 9) * kF8Row + 16 * r);
-    x.va[0] = A.x; x.va[1] = A.y; x.va[2] = A.z; x.va[3] = A.w;
-    x.vb[0] = B.x; x.vb[1] = B.y; x.vb[2] = B.z; x.vb[3] = B.w;
-    x.vc[0] = C.x; x.vc[1] = C.y; x.vc[2] = C.z; x.vc[3] = C.w;
-    x.vd[0] = D.x; x.vd[1] = D.y; x.vd[2] = D.z; x.vd[3] = D.w;
-    x.ks0 = x.ks1 = x.vsc = 0;
+    x.w[0][0] = A.x; x.w[1][0] = A.y; x.w[2][0] = A.z; x.w[3][0] = A.w;
+    x.w[0][1] = B.x; x.w[1][1] = B.y; x.w[2][1] = B.z; x.w[3][1] = B.w;
+    x.w[0][2] = C.x; x.w[1][2] = C.y; x.w[2][2] = C.z; x.w[3][2] = C.w;
+    x.w[0][3] = D.x; x.w[1][3] = D.y; x.w[2][3] = D.z; x.w[3][3] = D.w;
+    if (nvalid < kSub) {  // masked tokens -> E4M3 zero (stale bytes could be NaN)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (tA >= nvalid) x.w[q][0] = 0;
+        if (tA + 1 >= nvalid) x.w[q][1] = 0;
+        if (tA + 8 >= nvalid) x.w[q][2] = 0;
+        if (tA + 9 >= nvalid) x.w[q][3] = 0;
+      }
+    }
+    x.sAB = x.sCD = 0;
   }
 }
 
+// Score MMA k-step S (even steps accumulate into e, odd into od).
 template <int PREC, int S>
-__device__ __forceinline__ void qk_step(const Slice<PREC> &x, uint32_t lo0, uint32_t hi0, uint32_t lo1, uint32_t hi1,
-                                        const uint32_t (&qf)[8][2], float (&acc)[4]) {
+__device__ __forceinline__ void qk_step(const KOps<PREC> &x, const uint32_t (&qf)[8][2], float (&e)[4],
+                                        float (&od)[4]) {
+  float(&acc)[4] = (S & 1) ? od : e;
   if constexpr (PREC == NVKV_PREC_NVFP4) {
-    const uint32_t m0 = S < 4 ? lo0 : hi0, m1 = S < 4 ? lo1 : hi1;
+    const uint32_t m0 = S < 4 ? x.lo0 : x.hi0, m1 = S < 4 ? x.lo1 : x.hi1;
     constexpr int B0 = (S & 1) ? 2 : 0, B1 = B0 + 1;
     const uint32_t a0 = hmul2_u32(f16x2_from_e2m1x2<B0>(x.k0[S >> 1]), m0);
     const uint32_t a2 = hmul2_u32(f16x2_from_e2m1x2<B1>(x.k0[S >> 1]), m0);
@@ -287,113 +341,73 @@ __device__ __forceinline__ void qk_step(const Slice<PREC> &x, uint32_t lo0, uint
   }
 }
 
-template <int I>
-__device__ __forceinline__ void pv_mma_nvfp4(float (&o)[4], uint32_t xAB, uint32_t yAB, uint32_t xCD, uint32_t yCD,
-                                             uint32_t sAB, uint32_t sCD, uint32_t b0, uint32_t b1) {
-  mma_f16_16816(o, hmul2_u32(f16x2_from_e2m1x2<I>(xAB), sAB), hmul2_u32(f16x2_from_e2m1x2<I>(yAB), sAB),
-                hmul2_u32(f16x2_from_e2m1x2<I>(xCD), sCD), hmul2_u32(f16x2_from_e2m1x2<I>(yCD), sCD), b0, b1);
-}
-
-// Scores of one 16-token slice for this thread: rows r (s[0], s[1]) and r + 8
-// (s[2], s[3]), heads 2c, 2c+1; scaled to log2 units; -inf past nvalid.
-template <int PREC>
-__device__ __forceinline__ void slice_scores(const Slice<PREC> &x, int nvalid, int r, const uint32_t (&qf)[8][2],
-                                             const float (&cs)[2], float (&sc)[4]) {
-  float e[4] = {0.f, 0.f, 0.f, 0.f}, od[4] = {0.f, 0.f, 0.f, 0.f};  // even / odd k-step chains
-  uint32_t lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
+// P.V MMA for output tile J (NVFP4: half w = J / 4, byte J % 4 of each pair
+// word; FP8: token-pair word J / 2, byte pair J % 2).
+template <int PREC, int J>
+__device__ __forceinline__ void pv_tile(const VOps<PREC> &x, uint32_t b0, uint32_t b1, WarpState &st) {
   if constexpr (PREC == NVKV_PREC_NVFP4) {
-    const uint32_t sc0 = f16x2_from_e4m3x2<0>(x.ks0), sc1 = f16x2_from_e4m3x2<0>(x.ks1);
-    lo0 = prmt(sc0, 0, 0x1010);  // {S_2c, S_2c}
-    hi0 = prmt(sc0, 0, 0x3232);  // {S_2c+1, S_2c+1}
-    lo1 = prmt(sc1, 0, 0x1010);
-    hi1 = prmt(sc1, 0, 0x3232);
-  }
-  qk_step<PREC, 0>(x, lo0, hi0, lo1, hi1, qf, e);
-  qk_step<PREC, 1>(x, lo0, hi0, lo1, hi1, qf, od);
-  qk_step<PREC, 2>(x, lo0, hi0, lo1, hi1, qf, e);
-  qk_step<PREC, 3>(x, lo0, hi0, lo1, hi1, qf, od);
-  qk_step<PREC, 4>(x, lo0, hi0, lo1, hi1, qf, e);
-  qk_step<PREC, 5>(x, lo0, hi0, lo1, hi1, qf, od);
-  qk_step<PREC, 6>(x, lo0, hi0, lo1, hi1, qf, e);
-  qk_step<PREC, 7>(x, lo0, hi0, lo1, hi1, qf, od);
-  const bool v0 = r < nvalid, v1 = r + 8 < nvalid;
-  sc[0] = v0 ? (e[0] + od[0]) * cs[0] : -INFINITY;
-  sc[1] = v0 ? (e[1] + od[1]) * cs[1] : -INFINITY;
-  sc[2] = v1 ? (e[2] + od[2]) * cs[0] : -INFINITY;
-  sc[3] = v1 ? (e[3] + od[3]) * cs[1] : -INFINITY;
-}
-
-// O += V^T P^T for one slice (b0, b1: the P fragments of its tokens).
-template <int PREC>
-__device__ __forceinline__ void slice_pv(Slice<PREC> &x, int nvalid, int c, uint32_t b0, uint32_t b1, WarpState &st) {
-  const int tA = 2 * c;
-  if constexpr (PREC == NVKV_PREC_NVFP4) {
-    uint32_t sv = x.vsc;
-    if (nvalid < kSub) {  // masked tokens get scale 0 -> value 0 (codes are finite)
-      if (tA >= nvalid) sv &= 0xFFFFFF00u;
-      if (tA + 1 >= nvalid) sv &= 0xFFFF00FFu;
-      if (tA + 8 >= nvalid) sv &= 0xFF00FFFFu;
-      if (tA + 9 >= nvalid) sv &= 0x00FFFFFFu;
-    }
-    const uint32_t sAB = f16x2_from_e4m3x2<0>(sv), sCD = f16x2_from_e4m3x2<1>(sv);
-#pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      const uint32_t a = x.va[w], bb = x.vb[w], cc = x.vc[w], dd = x.vd[w];
-      // byte j of x*: the token pair's low nibbles (d = 16r + 2j'); of y*: high nibbles (d + 1)
-      const uint32_t xAB = (a & 0x0F0F0F0Fu) | ((bb & 0x0F0F0F0Fu) << 4);
-      const uint32_t yAB = ((a >> 4) & 0x0F0F0F0Fu) | (bb & 0xF0F0F0F0u);
-      const uint32_t xCD = (cc & 0x0F0F0F0Fu) | ((dd & 0x0F0F0F0Fu) << 4);
-      const uint32_t yCD = ((cc >> 4) & 0x0F0F0F0Fu) | (dd & 0xF0F0F0F0u);
-      pv_mma_nvfp4<0>(st.o[4 * w + 0], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
-      pv_mma_nvfp4<1>(st.o[4 * w + 1], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
-      pv_mma_nvfp4<2>(st.o[4 * w + 2], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
-      pv_mma_nvfp4<3>(st.o[4 * w + 3], xAB, yAB, xCD, yCD, sAB, sCD, b0, b1);
-    }
+    constexpr int w = J >> 2, I = J & 3;
+    mma_f16_16816(st.o[J], hmul2_u32(f16x2_from_e2m1x2<I>(x.w[w][0]), x.sAB),
+                  hmul2_u32(f16x2_from_e2m1x2<I>(x.w[w][1]), x.sAB), hmul2_u32(f16x2_from_e2m1x2<I>(x.w[w][2]), x.sCD),
+                  hmul2_u32(f16x2_from_e2m1x2<I>(x.w[w][3]), x.sCD), b0, b1);
   } else {
-    if (nvalid < kSub) {  // masked tokens -> E4M3 zero (stale bytes could be NaN)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (tA >= nvalid) x.va[q] = 0;
-        if (tA + 1 >= nvalid) x.vb[q] = 0;
-        if (tA + 8 >= nvalid) x.vc[q] = 0;
-        if (tA + 9 >= nvalid) x.vd[q] = 0;
-      }
-    }
-#pragma unroll
-    for (int qd = 0; qd < 4; ++qd) {
-      const uint32_t ab01 = prmt(x.va[qd], x.vb[qd], 0x5140), ab23 = prmt(x.va[qd], x.vb[qd], 0x7362);
-      const uint32_t cd01 = prmt(x.vc[qd], x.vd[qd], 0x5140), cd23 = prmt(x.vc[qd], x.vd[qd], 0x7362);
-      mma_f16_16816(st.o[2 * qd], f16x2_from_e4m3x2<0>(ab01), f16x2_from_e4m3x2<1>(ab01),
-                    f16x2_from_e4m3x2<0>(cd01), f16x2_from_e4m3x2<1>(cd01), b0, b1);
-      mma_f16_16816(st.o[2 * qd + 1], f16x2_from_e4m3x2<0>(ab23), f16x2_from_e4m3x2<1>(ab23),
-                    f16x2_from_e4m3x2<0>(cd23), f16x2_from_e4m3x2<1>(cd23), b0, b1);
-    }
+    constexpr int qd = J >> 1;
+    constexpr uint32_t sel = (J & 1) ? 0x7362u : 0x5140u;
+    const uint32_t ab = prmt(x.w[qd][0], x.w[qd][1], sel), cd = prmt(x.w[qd][2], x.w[qd][3], sel);
+    mma_f16_16816(st.o[J], f16x2_from_e4m3x2<0>(ab), f16x2_from_e4m3x2<1>(ab), f16x2_from_e4m3x2<0>(cd),
+                  f16x2_from_e4m3x2<1>(cd), b0, b1);
   }
 }
 
-// NS slices of consecutive stages: scores, one online-softmax update over all
-// 16 * NS tokens, P.V.  nvalid[i] = valid tokens of slice i (0..16).  The
-// kernel uses NS = 1: two slices per update hold twice the operand registers
-// and ran slower (spills at three CTAs per SM).
-template <int PREC, int NS>
-__device__ __forceinline__ void consume(Slice<PREC> (&x)[NS], const int (&nvalid)[NS], int r, int c,
-                                        const uint32_t (&qf)[8][2], const float (&cs)[2], WarpState &st) {
-  float sc[NS][4];
-#pragma unroll
-  for (int i = 0; i < NS; ++i) slice_scores<PREC>(x[i], nvalid[i], r, qf, cs, sc[i]);
-  float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < NS; ++i) {
-    mx0 = fmaxf(mx0, fmaxf(sc[i][0], sc[i][2]));
-    mx1 = fmaxf(mx1, fmaxf(sc[i][1], sc[i][3]));
+// Step J of the pipeline: score k-step J of the next slice and P.V tile J of
+// the current one, each only when asked for.
+template <int PREC, int J, bool QK, bool PV>
+__device__ __forceinline__ void pipe_step(const KOps<PREC> &kx, const uint32_t (&qf)[8][2], float (&e)[4],
+                                          float (&od)[4], const VOps<PREC> &vx, uint32_t b0, uint32_t b1,
+                                          WarpState &st) {
+  if constexpr (QK) qk_step<PREC, J>(kx, qf, e, od);
+  if constexpr (PV) pv_tile<PREC, J>(vx, b0, b1, st);
+}
+
+template <int PREC, bool QK, bool PV>
+__device__ __forceinline__ void pipe_all(const KOps<PREC> &kx, const uint32_t (&qf)[8][2], float (&e)[4],
+                                         float (&od)[4], const VOps<PREC> &vx, uint32_t b0, uint32_t b1,
+                                         WarpState &st) {
+  pipe_step<PREC, 0, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
+  pipe_step<PREC, 1, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
+  pipe_step<PREC, 2, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
+  pipe_step<PREC, 3, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
+  pipe_step<PREC, 4, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
+  pipe_step<PREC, 5, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
+  pipe_step<PREC, 6, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
+  pipe_step<PREC, 7, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
+}
+
+// Online softmax of one slice's scores (e + od, rows r / r + 8, heads 2c,
+// 2c+1, scaled by cs into log2 units; rows at or past nvalid masked): raises
+// the running max only when a score exceeds it by more than the threshold
+// (then O and l are rescaled), and returns P as the two f16x2 B fragments of
+// the P.V MMA (zero for a slice without valid tokens): b0 = P[tok 2c, 2c+1][head r], b1 = P[tok 2c+8, 2c+9][head r].
+__device__ __forceinline__ void softmax_slice(const float (&e)[4], const float (&od)[4], int nvalid, int r,
+                                              const float (&cs)[2], WarpState &st, uint32_t &b0, uint32_t &b1) {
+  if (nvalid <= 0) {  // warp-uniform: a slice past the end of the sequence adds nothing
+    b0 = b1 = 0;
+    return;
   }
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-  }
-  const bool need = (mx0 > st.m[0] + kRescaleThreshold) || (mx1 > st.m[1] + kRescaleThreshold);
+  const bool v0 = r < nvalid, v1 = r + 8 < nvalid;
+  const float s0 = v0 ? (e[0] + od[0]) * cs[0] : -INFINITY;
+  const float s1 = v0 ? (e[1] + od[1]) * cs[1] : -INFINITY;
+  const float s2 = v1 ? (e[2] + od[2]) * cs[0] : -INFINITY;
+  const float s3 = v1 ? (e[3] + od[3]) * cs[1] : -INFINITY;
+  const bool need = (s0 > st.m[0] + kRescaleThreshold) | (s2 > st.m[0] + kRescaleThreshold) |
+                    (s1 > st.m[1] + kRescaleThreshold) | (s3 > st.m[1] + kRescaleThreshold);
   if (__any_sync(0xffffffffu, need)) {
+    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
     const float n0 = fmaxf(st.m[0], mx0), n1 = fmaxf(st.m[1], mx1);
     const float al0 = ex2(st.m[0] - n0), al1 = ex2(st.m[1] - n1);
     st.m[0] = n0;
@@ -408,38 +422,35 @@ __device__ __forceinline__ void consume(Slice<PREC> (&x)[NS], const int (&nvalid
       st.o[j][3] *= al1;
     }
   }
-  uint32_t b[NS][2];
-#pragma unroll
-  for (int i = 0; i < NS; ++i) {
-    const float p0 = ex2(sc[i][0] - st.m[0]), p1 = ex2(sc[i][1] - st.m[1]);
-    const float p2 = ex2(sc[i][2] - st.m[0]), p3 = ex2(sc[i][3] - st.m[1]);
-    st.l[0] += p0 + p2;
-    st.l[1] += p1 + p3;
-    b[i][0] = movmatrix_trans(pack_f16x2(p0, p1));  // P[tok 2c, 2c+1][head r]
-    b[i][1] = movmatrix_trans(pack_f16x2(p2, p3));  // P[tok 2c+8, 2c+9][head r]
-  }
-#pragma unroll
-  for (int i = 0; i < NS; ++i) slice_pv<PREC>(x[i], nvalid[i], c, b[i][0], b[i][1], st);
+  const float p0 = ex2(s0 - st.m[0]), p1 = ex2(s1 - st.m[1]);
+  const float p2 = ex2(s2 - st.m[0]), p3 = ex2(s3 - st.m[1]);
+  st.l[0] += p0 + p2;
+  st.l[1] += p1 + p3;
+  b0 = movmatrix_trans(pack_f16x2(p0, p1));
+  b1 = movmatrix_trans(pack_f16x2(p2, p3));
 }
 
-// The warp's 16-token slice of the next stage: wait for it, copy it to
-// registers, release the stage and advance the ring position.  rem = tokens of
-// the sequence from the slice's first token on.
-template <int PREC>
-__device__ __forceinline__ bool fetch_slice(uint64_t *full, uint64_t *empty, const uint8_t *ring,
-                                            const SliceOffsets<PREC> &so, int &slot, uint32_t &phase,
-                                            volatile int *abort, int64_t rem, int r, int c, int lane, Slice<PREC> &x,
-                                            int &nvalid) {
-  const bool ready = mbar_wait_bounded(&full[slot], phase, abort);
-  nvalid = rem < kSub ? (rem > 0 ? static_cast<int>(rem) : 0) : kSub;
-  if (nvalid > 0) load_slice<PREC>(ring + static_cast<size_t>(slot) * Layout<PREC>::kStageBytes, so, r, c, x);
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&empty[slot]);
-  if (++slot == Layout<PREC>::kStages) {
-    slot = 0;
-    phase ^= 1u;
+// Ring position of the next stage a consumer warp reads.
+struct RingPos {
+  int slot = 0;
+  uint32_t phase = 0;
+  template <int PREC>
+  __device__ __forceinline__ void advance() {
+    if (++slot == Layout<PREC>::kStages) {
+      slot = 0;
+      phase ^= 1u;
+    }
   }
+};
+
+// Wait for the stage at `p`; false (warp-uniform) after a timeout.
+__device__ __forceinline__ bool wait_stage(uint64_t *full, const RingPos &p, volatile int *abort) {
+  const bool ready = mbar_wait_bounded(&full[p.slot], p.phase, abort);
   return __all_sync(0xffffffffu, ready);
+}
+
+__device__ __forceinline__ int slice_valid(int64_t rem) {
+  return rem < kSub ? (rem > 0 ? static_cast<int>(rem) : 0) : kSub;
 }
 
 template <int PREC>
@@ -525,8 +536,7 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
     const SliceOffsets<PREC> so(warp, a.c.P);
     const float kscale = __fmul_rn(a.c.scale[0], a.sm_scale * 1.4426950408889634f);
     const float vscale = a.c.scale[1];
-    int slot = 0;          // ring position and parity of the next stage this warp reads
-    uint32_t phase = 0;
+    RingPos pos;  // ring position and parity of the next stage this warp reads
     for (int64_t u = u0; u < u1;) {
       const Seg s = seg_at(u, u1, cum, B, Hkv);
       const int64_t Lb = clamped_len(a, s.b);
@@ -578,14 +588,46 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
       st.m[0] = st.m[1] = -INFINITY;
       st.l[0] = st.l[1] = 0.0f;
 
+      // two-deep pipeline over the segment's slices (see the consumer notes)
       const int ntiles = s.t1 - s.t0;
-      for (int k = 0; k < ntiles; ++k) {
-        Slice<PREC> x[1];
-        int nv[1];
-        const bool ok = fetch_slice<PREC>(full, empty, ring, so, slot, phase, abort,
-                                          Lb - static_cast<int64_t>(s.t0 + k) * kTile - kSub * warp, r, c, lane, x[0],
-                                          nv[0]);
-        if (ok && nv[0] > 0) consume<PREC, 1>(x, nv, r, c, qf, cs, st);
+      const int64_t rem0 = Lb - static_cast<int64_t>(s.t0) * kTile - kSub * warp;
+      bool ok = wait_stage(full, pos, abort);
+      RingPos cur = pos;
+      int nv_cur = slice_valid(rem0);
+      uint32_t b0 = 0, b1 = 0;
+      {
+        KOps<PREC> kx;
+        VOps<PREC> vx;
+        float e[4] = {0.f, 0.f, 0.f, 0.f}, od[4] = {0.f, 0.f, 0.f, 0.f};
+        load_k<PREC>(ring + static_cast<size_t>(cur.slot) * Lay::kStageBytes, so, r, c, kx);
+        pipe_all<PREC, true, false>(kx, qf, e, od, vx, 0, 0, st);
+        softmax_slice(e, od, nv_cur, r, cs, st, b0, b1);
+      }
+      pos.template advance<PREC>();
+      for (int k = 0; k < ntiles && ok; ++k) {
+        const uint8_t *stage_cur = ring + static_cast<size_t>(cur.slot) * Lay::kStageBytes;
+        VOps<PREC> vx;
+        load_v<PREC>(stage_cur, so, r, c, nv_cur, vx);
+        if (k + 1 < ntiles) {
+          ok = wait_stage(full, pos, abort);
+          const int nv_next = slice_valid(rem0 - static_cast<int64_t>(k + 1) * kTile);
+          KOps<PREC> kx;
+          load_k<PREC>(ring + static_cast<size_t>(pos.slot) * Lay::kStageBytes, so, r, c, kx);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[cur.slot]);
+          float e[4] = {0.f, 0.f, 0.f, 0.f}, od[4] = {0.f, 0.f, 0.f, 0.f};
+          pipe_all<PREC, true, true>(kx, qf, e, od, vx, b0, b1, st);
+          softmax_slice(e, od, nv_next, r, cs, st, b0, b1);
+          cur = pos;
+          nv_cur = nv_next;
+          pos.template advance<PREC>();
+        } else {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[cur.slot]);
+          KOps<PREC> kx;
+          float e[4], od[4];
+          pipe_all<PREC, false, true>(kx, qf, e, od, vx, b0, b1, st);
+        }
       }
 
       // ---- merge the four warps: (m, l) per head, O per (head, d) ----
