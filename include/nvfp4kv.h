@@ -29,13 +29,21 @@
  *   s8 == 0 -> byte 0.
  *
  * Cache layout (one layer, device memory owned by the caller): one contiguous
- * block per (page, KV head), pages outermost: data[num_pages][num_kv_heads][block]
- *   NVFP4 block (P * 144 bytes at head_dim 128, P = page_size):
- *     [K codes P x D/2 | K scales P x D/16 | V codes P x D/2 | V scales P x D/16]
- *   FP8 block (P * 256 bytes): [K P x D | V P x D]
- * Row `off` of a plane holds the token at page offset `off`; a token at slot s
- * lives at page s / P, offset s % P.  A page of one KV head is therefore one
- * contiguous run of bytes, which decode fetches with a single bulk copy.
+ * block per (page, KV head), pages outermost: data[num_pages][num_kv_heads][block],
+ * block = P * 144 bytes (NVFP4) or P * 256 bytes (FP8) at head_dim 128,
+ * P = page_size.  A token at slot s lives at page s / P, offset off = s % P,
+ * in group off / 8 (eight consecutive offsets), row r = off % 8.  Groups:
+ *   NVFP4 (1152 bytes): [K codes 8 x 64 | K scales 8 x 8 | V codes 8 x 64 |
+ *                        V scales 8 x 8]
+ *   FP8 (2048 bytes):   [K 8 x 128 | V 8 x 128]
+ * K bytes are stored in 16-byte chunks, chunk-major: byte j of row r at
+ * (j / 16) * 128 + r * 16 + j % 16 (the K-major core-matrix order of a
+ * tensor-core operand, so a staged tile of K codes is an MMA operand as it
+ * stands).  V rows are stored in the order 0, 2, 4, 6, 1, 3, 5, 7 (row r at
+ * position (r % 2) * 4 + r / 2; bank-conflict-free operand loads); scales
+ * row-major.  A page of one KV head is one contiguous run of bytes, which
+ * decode fetches with a single bulk copy.  The byte contents are the
+ * quantizer's output above; only their positions are fixed here.
  *   Supported: head_dim 128; page_size 16, 32 or 64; every pointer 16-byte
  *   aligned.  Anything else -> NVKV_ERR_UNSUPPORTED.
  *

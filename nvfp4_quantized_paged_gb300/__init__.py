@@ -149,34 +149,19 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 class Cache:
     """One layer's paged cache in device memory: one contiguous block per
-    (page, KV head), ``data`` uint8 [num_pages, Hkv, block].
-
-    NVFP4 block = [K codes P x 64 | K scales P x 8 | V codes P x 64 |
-    V scales P x 8] (P * 144 bytes); FP8 block = [K P x 128 | V P x 128].
-    ``k_data``/``k_scale``/``v_data``/``v_scale`` are views of the planes
-    shaped [num_pages, Hkv, P, 64] / [num_pages, Hkv, P, 8] (FP8:
-    [num_pages, Hkv, P, 128], no scales).  ``kv_scale`` float32[2] (K, V): the
-    NVFP4 global scales or FP8 per-tensor scales.  ``err`` int32[1]: device
-    error word (0 = none).
+    (page, KV head), ``data`` uint8 [num_pages, Hkv, block], block = P * 144
+    bytes (NVFP4) or P * 256 (FP8).  Inside a block the page's slots form
+    groups of eight (the byte positions are stated in include/nvfp4kv.h).
+    ``kv_scale`` float32[2] (K, V): the NVFP4 global scales or FP8 per-tensor
+    scales.  ``err`` int32[1]: device error word (0 = none).
     """
 
     def __init__(self, prec: int, num_pages: int, num_kv_heads: int, page_size: int, device="cuda",
                  head_dim: int = HEAD_DIM, kv_scale: Optional[torch.Tensor] = None):
         self.prec, self.num_pages, self.Hkv, self.P, self.D = prec, num_pages, num_kv_heads, page_size, head_dim
         P, D = page_size, head_dim
-        if prec == PREC_NVFP4:
-            half = P * (D // 2 + D // 16)
-            self.data = torch.zeros(num_pages, num_kv_heads, 2 * half, dtype=torch.uint8, device=device)
-            cs = P * (D // 2)
-            self.k_data = self.data[:, :, :cs].unflatten(-1, (P, D // 2))
-            self.k_scale = self.data[:, :, cs:half].unflatten(-1, (P, D // 16))
-            self.v_data = self.data[:, :, half:half + cs].unflatten(-1, (P, D // 2))
-            self.v_scale = self.data[:, :, half + cs:].unflatten(-1, (P, D // 16))
-        else:
-            self.data = torch.zeros(num_pages, num_kv_heads, 2 * P * D, dtype=torch.uint8, device=device)
-            self.k_data = self.data[:, :, :P * D].unflatten(-1, (P, D))
-            self.v_data = self.data[:, :, P * D:].unflatten(-1, (P, D))
-            self.k_scale = self.v_scale = None
+        block = P * 2 * (D // 2 + D // 16) if prec == PREC_NVFP4 else 2 * P * D
+        self.data = torch.zeros(num_pages, num_kv_heads, block, dtype=torch.uint8, device=device)
         self.kv_scale = kv_scale if kv_scale is not None else torch.zeros(2, dtype=torch.float32, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
 

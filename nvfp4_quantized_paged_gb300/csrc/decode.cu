@@ -5,31 +5,36 @@
 // sensitive layers ("SOAR Weekly Champion Notes 05", 03).
 //
 // Design (sm_103a, one GPU):
-//   * Work unit = one 64-token tile of one (sequence, KV head).  The units of
+//   * Work unit = one 128-token tile of one (sequence, KV head).  The units of
 //     the whole batch are laid end to end and cut into equal contiguous shares,
-//     one per CTA of a persistent grid (about SMs x resident CTAs), so every
-//     CTA streams the same number of bytes whatever the sequence lengths.  A
-//     (sequence, KV head) cut between CTAs yields split-KV partials that the
-//     last-arriving CTA merges with the log-sum-exp rule (no second kernel,
-//     no spin: an atomic arrival counter).
-//   * One producer warp streams tiles into a shared-memory ring with 1-D bulk
-//     copies (cp.async.bulk + mbarrier transaction counts).  The cache keeps
-//     each (page, KV head) as one contiguous block, so a 64-token tile is one
-//     9216-byte copy at page size 64 (NVFP4; 16 KB for FP8), or 64/P copies of
-//     whole page blocks.  Block-table entries are fetched 32 at a time, one
-//     window ahead.  An L2 evict-first hint marks the stream.
-//   * Four consumer warps share every tile: warp w takes tokens [16w, 16w+16),
-//     copies its slice into registers and releases the stage at once, so the
-//     ring stays almost entirely in flight while the warps compute.
-//   * E2M1 pairs become f16x2 with one cvt.rn.f16x2.e2m1x2 and are scaled by
-//     their E4M3 block scale with one f16x2 multiply; code * scale has at most
-//     6 significant bits and lies in [2^-10, 2688], so it is exact in FP16.
-//     Scores and P.V run on the tensor cores as m16n8k16 FP16 MMAs with FP32
-//     accumulation: tokens form M, the GQA query group (<= 8 heads) forms N.
-//     g_K, sm_scale, log2(e) and a per-head power of two that brings the BF16
-//     query into FP16 range form one FP32 factor per score; g_V is applied
-//     once to the output.  Online softmax in FP32 with exp2 and a lazily raised
-//     running max (rescale only when the max grows by more than 2^8).
+//     one per CTA of a persistent grid (SMs x resident CTAs), so every CTA
+//     streams the same number of bytes whatever the sequence lengths.  A
+//     (sequence, KV head) cut between CTAs leaves split-KV partials that a
+//     second kernel merges with the log-sum-exp rule.
+//   * Warp roles: a producer warp streams tiles into a shared-memory ring with
+//     1-D bulk copies (one per page block, mbarrier transaction counts); an MMA
+//     warp computes the scores of each tile on the 5th-generation tensor cores;
+//     four consumer warps (one per TMEM lane quadrant, 32 tokens each) run the
+//     softmax and P.V.
+//   * Scores S = K Q^T straight from the packed cache: the K codes of a staged
+//     tile are the A operand of one block-scaled MMA (kind::mxf4nvf4, M = 128
+//     tokens, K = 64 per instruction) and the E4M3 block scales of K are its
+//     scale factors, so K is never dequantized by a thread.  The BF16 query
+//     enters as the B operand in the same format: each query head is written
+//     as a sum of four NVFP4 terms (E2M1 codes, one E4M3 scale per 16 values),
+//     stacked along N, and the score is the sum of the four columns.  The FP8
+//     variant does the same with kind::f8f6f4 and four E4M3 terms.  Scores land
+//     in TMEM (double-buffered) and are read with tcgen05.ld, one token per
+//     consumer thread.
+//   * P.V on warp MMAs (m16n8k16 FP16 -> FP32; tokens = K, GQA heads = N):
+//     E2M1 pairs -> f16x2 by cvt.rn.f16x2.e2m1x2, times the E4M3 block scale
+//     (f16x2 multiply; code * scale has at most 6 significant bits in
+//     [2^-10, 2688], exact in FP16).  P goes to the MMA operand layout through
+//     a small per-warp shared-memory transpose.
+//   * g_K, sm_scale, log2(e) and the power of two that scales each query head
+//     before its decomposition form one FP32 factor per head; g_V is applied to
+//     the output.  Online softmax in FP32 with exp2 and a lazily raised running
+//     max (rescale only when the max grows by more than 2^8).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -42,30 +47,70 @@ namespace nvkv {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kTile = 64;          // tokens per work unit / ring stage
-constexpr int kSub = 16;           // tokens per consumer warp per stage
-constexpr int kConsumerWarps = kTile / kSub;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kTile = 128;         // tokens per work unit / ring stage (the MMA M)
+constexpr int kGroups = 3;         // consumer groups: group g takes the tiles i = g (mod 3) of the CTA
+constexpr int kGroupWarps = 4;     // warp w of a group owns tokens [32w, 32w+32) of a tile = TMEM lane quadrant w
+constexpr int kConsumerWarps = kGroups * kGroupWarps;
+constexpr int kProducerWarp = kConsumerWarps, kMmaWarp = kConsumerWarps + 1;
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kMaxBatch = 1024;    // sequences per call (prefix sums live in shared memory)
-constexpr int kMaxGroup = 8;       // query heads per KV head (MMA N)
+constexpr int kMaxGroup = 8;       // query heads per KV head
+constexpr int kTerms = 4;          // query terms of the score MMA
+constexpr int kQBufs = 3;          // query images in flight (segments)
 constexpr int kSlotFloats = kMaxGroup * kD + 2 * kMaxGroup;  // one partial (o, m, l)
 constexpr float kRescaleThreshold = 8.0f;                   // log2 units
 
+// Per-precision tile geometry (groups of 8 tokens, see nvkv_host.h).
 template <int PREC>
-struct Layout;
+struct Prec;
 template <>
-struct Layout<NVKV_PREC_NVFP4> {
-  static constexpr int kTokBytes = kNvTokBytes;                // 144
-  static constexpr int kStageBytes = kTile * kTokBytes;        // 9216
-  static constexpr int kStages = 6;
-  static constexpr int kMinBlocks = 3;
+struct Prec<NVKV_PREC_NVFP4> {
+  static constexpr int kTokBytes = kNvTokBytes;       // 144
+  static constexpr int kGroup = kNvGroup;             // 1152
+  static constexpr int kKRow = 64;                    // K bytes per token
+  static constexpr int kMmas = 2;                     // K = 64 values per instruction
+  static constexpr int kRing = 10;                    // stages at 4 heads per group
 };
 template <>
-struct Layout<NVKV_PREC_FP8_E4M3> {
-  static constexpr int kTokBytes = kF8TokBytes;                // 256
-  static constexpr int kStageBytes = kTile * kTokBytes;        // 16384
-  static constexpr int kStages = 6;
-  static constexpr int kMinBlocks = 2;
+struct Prec<NVKV_PREC_FP8_E4M3> {
+  static constexpr int kTokBytes = kF8TokBytes;       // 256
+  static constexpr int kGroup = kF8Group;             // 2048
+  static constexpr int kKRow = 128;
+  static constexpr int kMmas = 4;                     // K = 32 values per instruction
+  static constexpr int kRing = 6;
+};
+
+// NH = heads per group slot set (4 or 8), N = NH * kTerms columns of the score MMA.
+template <int PREC, int NH>
+struct Cfg {
+  using P = Prec<PREC>;
+  static constexpr bool kNv = PREC == NVKV_PREC_NVFP4;
+  static constexpr int N = NH * kTerms;
+  static constexpr int kStageBytes = kTile / kGroupRows * P::kGroup;     // 18432 / 32768
+  static constexpr int kStages = NH == 4 ? P::kRing : P::kRing - 1;
+  static constexpr int kQRow = P::kKRow;                                 // B row bytes
+  static constexpr int kQImg = N * kQRow;                                // one query image
+  static constexpr int kQSbo = 8 * kQRow;                                // 8-row group stride of B
+  // TMEM columns: scores (one buffer of N per consumer group) from 0; NVFP4
+  // scale factors at 16-column boundaries: A (K scales of the group's next
+  // tile) at 128 + 32 * group + 16 * mma, B at 256 + 32 * query image + 16 * mma.
+  // One CTA per SM holds all 512.
+  static constexpr uint32_t kTmemCols = kNv ? 512 : 128;
+  __host__ __device__ static constexpr uint32_t sfa_col(int buf, int k) { return 128 + 32 * buf + 16 * k; }
+  __host__ __device__ static constexpr uint32_t sfb_col(int qb, int k) { return 256 + 32 * qb + 16 * k; }
+  // shared memory (bytes)
+  static constexpr int oRing = 0;
+  static constexpr int oQImg = oRing + kStages * kStageBytes;
+  static constexpr int oSfb = oQImg + kQBufs * kQImg;                       // [3][2][32][16] (NVFP4)
+  static constexpr int oPt = oSfb + (kNv ? kQBufs * 2 * 512 : 0);          // [12 warps][NH][32] f16
+  static constexpr int oCs = oPt + kConsumerWarps * NH * 32 * 2;           // [3][8] f32
+  static constexpr int oMrgO = oCs + kQBufs * 8 * 4;                       // [12 warps][2][128] f32
+  static constexpr int oMrgMl = oMrgO + kConsumerWarps * 2 * kD * 4;       // [12 warps][8][2] f32
+  static constexpr int oCum = oMrgMl + kConsumerWarps * kMaxGroup * 2 * 4;  // [kMaxBatch + 1] i32
+  static constexpr int oBars = (oCum + (kMaxBatch + 1) * 4 + 15) / 16 * 16;
+  static constexpr int kBars = 2 * kStages + 3 * kGroups + kQBufs;  // full, empty, sready, sempty, sfready, qready
+  static constexpr int oFlags = oBars + kBars * 8;                          // tmem holder, abort, fills[kStages]
+  static constexpr int kSmem = oFlags + 4 * (2 + kStages);
 };
 
 struct DecodeArgs {
@@ -81,16 +126,6 @@ struct DecodeArgs {
   float *partials;    // [num_ctas][2][kSlotFloats]
   __nv_bfloat16 *out;
 };
-
-template <int PREC>
-constexpr int smem_bytes_for(int G) {
-  return Layout<PREC>::kStages * Layout<PREC>::kStageBytes  // ring
-         + 2 * Layout<PREC>::kStages * 8                       // full/empty barriers
-         + (kMaxBatch + 1) * 4                                 // tile prefix sums
-         + kConsumerWarps * G * kD * 4                         // warp merge: o
-         + kConsumerWarps * kMaxGroup * 2 * 4                  // warp merge: m, l
-         + 4 * (1 + Layout<PREC>::kStages);                    // abort, fills
-}
 
 // Segment = run of consecutive units of one (sequence, KV head).
 struct Seg {
@@ -129,18 +164,25 @@ __device__ __forceinline__ int clamped_len(const DecodeArgs &a, int b) {
   return static_cast<int>(L < 0 ? 0 : (L > cap ? cap : L));
 }
 
+// Wait for `parity` of `bar`; false (warp-uniform) after a timeout or abort.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  const bool ok = mbar_wait_bounded(bar, parity, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------------------
 // Producer warp: one bulk copy per page block of each tile of this CTA's
-// share (a tile spans 64 / P whole page blocks).  Lane j copies block j.
+// share (a tile spans 128 / P whole page blocks, placed back to back, so the
+// stage is 16 groups of 8 tokens at a uniform stride).  Lane j copies block j.
 // ---------------------------------------------------------------------------
-template <int PREC>
+template <int PREC, int NH>
 __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uint64_t *empty, const int32_t *cum,
                          int64_t u0, int64_t u1, volatile int *abort, int *fills) {
-  using Lay = Layout<PREC>;
+  using C = Cfg<PREC, NH>;
   const int lane = threadIdx.x & 31;
   const int Hkv = a.c.Hkv, P = a.c.P;
   const uint64_t policy = policy_evict_first();
-  const uint32_t block_bytes = static_cast<uint32_t>(P) * Lay::kTokBytes;
+  const uint32_t block_bytes = static_cast<uint32_t>(P) * C::P::kTokBytes;
   int64_t i = 0;  // stage counter
   for (int64_t u = u0; u < u1;) {
     const Seg s = seg_at(u, u1, cum, a.B, Hkv);
@@ -152,8 +194,8 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
     int32_t pg = wbase + lane < a.max_pages ? brow[wbase + lane] : 0;
     int32_t pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
     for (int t = s.t0; t < s.t1; ++t, ++i) {
-      const int slot = static_cast<int>(i % Lay::kStages);
-      const uint32_t fill = static_cast<uint32_t>(i / Lay::kStages);
+      const int slot = static_cast<int>(i % C::kStages);
+      const uint32_t fill = static_cast<uint32_t>(i / C::kStages);
       if (__any_sync(0xffffffffu, *abort)) return;
       if (lane == 0 && fill > 0) mbar_wait_bounded(&empty[slot], (fill - 1) & 1u, abort);
       if (__any_sync(0xffffffffu, *abort)) return;  // warp-uniform exit
@@ -174,8 +216,8 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
           set_err(a.c.err, NVKV_DEVERR_PAGE);
           page = 0;  // a valid address; the output of this sequence is then undefined
         }
-        bulk_g2s(ring + static_cast<size_t>(slot) * Lay::kStageBytes + static_cast<size_t>(lane) * block_bytes,
-                 a.c.data + a.c.block(page, s.h, Lay::kTokBytes), block_bytes, &full[slot], policy);
+        bulk_g2s(ring + static_cast<size_t>(slot) * C::kStageBytes + static_cast<size_t>(lane) * block_bytes,
+                 a.c.data + a.c.block(page, s.h, C::P::kTokBytes), block_bytes, &full[slot], policy);
       }
       if (lane == 0) fills[slot] = static_cast<int>(fill) + 1;
     }
@@ -184,106 +226,222 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
 }
 
 // ---------------------------------------------------------------------------
-// Consumer warps.  Lane = 4r + c.  Warp w owns tokens [16w, 16w+16) of every
-// stage.  Scores: MMA rows = tokens r, r + 8 of the slice; head_dim order
-// inside one MMA k-step s is permuted so that a thread reads 16 contiguous code
-// bytes (d in [32c, 32c+32), step s covers d = 32c + 4s + {0,1,2,3}); the
-// query fragment uses the same order.  P.V: MMA rows = head_dim (thread r owns
-// d in [16r, 16r+16)), k = tokens 2c, 2c+1, 2c+8, 2c+9, n = query head.  O for
-// heads 2c, 2c+1 of the group and d in [16r, 16r+16) lives in 32 registers.
-//
-// The warp runs its slices as a two-deep software pipeline: while the P.V
-// MMAs of slice i issue, the score MMAs of slice i+1 issue between them (the
-// two chains are independent), and the softmax of slice i+1 follows.  K of a
-// slice is read from shared memory when its scores start, V when its P.V
-// starts; the stage is released after both.
+// Query images.  Lane (j, kb) of the MMA warp takes head j of the group and
+// values [16 kb, 16 kb + 16); the head is scaled by 2^-e (its max lands in
+// [2^7, 2^8)) and written as kTerms terms, each the residual of the previous
+// ones rounded to the operand format:
+//   NVFP4: term = E2M1 codes x one E4M3 scale per 16 values (scale = residual
+//          max / 6, rounded to E4M3); the codes fill B row n = 4 j + term in
+//          the MMA's K-major core-matrix order, the scale goes to the
+//          scale-factor atom of MMA kb / 4, row n, byte kb % 4.
+//   FP8:   term = E4M3(residual), 16 bytes per lane and term.
+// cs[j] = g_K * sm_scale * log2(e) * 2^e turns a score column sum into log2
+// units.  Heads j >= G get zero terms and cs = 0.
 // ---------------------------------------------------------------------------
-struct WarpState {
-  float o[8][4];
-  float m[2];
-  float l[2];
-};
-
-// Offsets of a warp's slice inside a stage (block layout of the header).
-template <int PREC>
-struct SliceOffsets {
-  int kc, ks, vc, vs;  // row 0 of K codes, K scales, V codes, V scales (NVFP4); kc, vc for FP8
-  __device__ SliceOffsets(int warp, int P) {
-    const int blk = (kSub * warp) / P, row0 = (kSub * warp) % P;
-    const int base = blk * P * Layout<PREC>::kTokBytes;
-    if constexpr (PREC == NVKV_PREC_NVFP4) {
-      kc = base + row0 * kNvCodeRow;
-      ks = base + P * kNvCodeRow + row0 * kNvScaleRow;
-      vc = base + P * (kNvCodeRow + kNvScaleRow) + row0 * kNvCodeRow;
-      vs = base + P * (2 * kNvCodeRow + kNvScaleRow) + row0 * kNvScaleRow;
+template <int PREC, int NH>
+__device__ void prepare_query(const DecodeArgs &a, const Seg &s, uint8_t *img, uint8_t *sfb, float *cs,
+                              float kscale) {
+  using C = Cfg<PREC, NH>;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int pass = 0; pass < NH / 4; ++pass) {
+    const int j = (lane >> 3) + 4 * pass, kb = lane & 7;
+    float v[16];
+    if (j < a.G) {
+      const uint4 *qp = reinterpret_cast<const uint4 *>(a.q + (static_cast<int64_t>(s.b) * a.Hq + s.h * a.G + j) * kD +
+                                                        16 * kb);
+#pragma unroll
+      for (int v4 = 0; v4 < 2; ++v4) {
+        const uint4 w = __ldg(qp + v4);
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[8 * v4 + 2 * e] = __uint_as_float(ww[e] << 16);
+          v[8 * v4 + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+        }
+      }
     } else {
-      kc = base + row0 * kF8Row;
-      vc = base + P * kF8Row + row0 * kF8Row;
-      ks = vs = 0;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = 0.0f;
     }
+    float am = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) am = fmaxf(am, fabsf(v[e]));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
+    int ex = 0;
+    if (am > 0.0f) ex = static_cast<int>((__float_as_uint(am) >> 23) & 0xFF) - 127 - 7;
+    ex = max(-100, min(100, ex));
+    const float down = __uint_as_float(static_cast<uint32_t>(127 - ex) << 23);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] *= down;  // exact (power of two)
+#pragma unroll
+    for (int t = 0; t < kTerms; ++t) {
+      const int n = kTerms * j + t;
+      if constexpr (C::kNv) {
+        float m = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[e]));
+        const uint32_t sb = e4m3x2_from_f32(m * (1.0f / 6.0f), 0.0f) & 0xFFu;
+        const float sv = f32_from_e4m3(sb);
+        uint32_t w[2] = {0u, 0u};
+        if (sv > 0.0f) {
+          const float inv = 1.0f / sv;
+#pragma unroll
+          for (int p = 0; p < 8; ++p) {
+            const uint32_t byte = e2m1x2_from_f32(v[2 * p] * inv, v[2 * p + 1] * inv);
+            w[p >> 2] |= byte << (8 * (p & 3));
+            const uint32_t h2 = f16x2_from_e2m1x2<0>(byte);
+            v[2 * p] -= f32_lo(h2) * sv;  // exact: at most 6 significant bits
+            v[2 * p + 1] -= f32_hi(h2) * sv;
+          }
+        }
+        *reinterpret_cast<uint2 *>(img + (n >> 3) * C::kQSbo + (kb >> 1) * 128 + (n & 7) * 16 + (kb & 1) * 8) =
+            make_uint2(w[0], w[1]);
+        sfb[(kb >> 2) * 512 + n * 16 + (kb & 3)] = static_cast<uint8_t>(sb);
+      } else {
+        uint32_t w[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const uint32_t lo = e4m3x2_from_f32(v[4 * p], v[4 * p + 1]);
+          const uint32_t hi = e4m3x2_from_f32(v[4 * p + 2], v[4 * p + 3]);
+          w[p] = lo | (hi << 16);
+          const uint32_t h0 = f16x2_from_e4m3x2<0>(w[p]), h1 = f16x2_from_e4m3x2<1>(w[p]);
+          v[4 * p] -= f32_lo(h0);
+          v[4 * p + 1] -= f32_hi(h0);
+          v[4 * p + 2] -= f32_lo(h1);
+          v[4 * p + 3] -= f32_hi(h1);
+        }
+        *reinterpret_cast<uint4 *>(img + (n >> 3) * C::kQSbo + kb * 128 + (n & 7) * 16) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+    if (kb == 0) cs[j] = j < a.G ? __fmul_rn(kscale, __uint_as_float(static_cast<uint32_t>(127 + ex) << 23)) : 0.0f;
   }
-};
+  fence_proxy_async_smem();  // the images are read by the tensor cores (async proxy)
+  __syncwarp();
+}
 
-// K operand of a slice: code words of rows r, r + 8 and (NVFP4) their block
-// scales as f16x2 pairs {S, S} for d blocks 2c (lo) and 2c + 1 (hi).
-template <int PREC>
-struct KOps {
-  uint32_t k0[PREC == NVKV_PREC_NVFP4 ? 4 : 8], k1[PREC == NVKV_PREC_NVFP4 ? 4 : 8];
-  uint32_t lo0, hi0, lo1, hi1;
+// ---------------------------------------------------------------------------
+// MMA warp.  Per tile i: once consumer group g = i % 3 has read its previous
+// tile's scores and written this tile's K block scales into its TMEM
+// scale-factor columns, issue the score MMAs into group g's score buffer and
+// commit them to sready[g].  The query image of a segment is prepared one
+// segment ahead (ring of three), right after the first MMA of the current
+// segment issues.
+// ---------------------------------------------------------------------------
+template <int PREC, int NH>
+__device__ void mma_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uint64_t *full, uint64_t *sready,
+                         uint64_t *sempty, uint64_t *sfready, uint64_t *qready, const int32_t *cum, int64_t u0,
+                         int64_t u1, volatile int *abort, float kscale, int64_t &issued) {
+  using C = Cfg<PREC, NH>;
+  const int lane = threadIdx.x & 31;
+  uint8_t *ring = smem + C::oRing;
+  uint8_t *qimg = smem + C::oQImg;
+  uint8_t *sfb = smem + C::oSfb;
+  float *cs = reinterpret_cast<float *>(smem + C::oCs);
+  const int Hkv = a.c.Hkv;
+  issued = 0;
+  if (u0 >= u1) return;
+  {
+    const Seg s0 = seg_at(u0, u1, cum, a.B, Hkv);
+    prepare_query<PREC, NH>(a, s0, qimg, sfb, cs, kscale);
+    if (lane == 0) {
+      if constexpr (C::kNv) {
+        tc_fence_after();
+        tmem_cp_32x128b_x4(tmem + C::sfb_col(0, 0), umma_desc(smem_u32(sfb), 128, 128));
+        tmem_cp_32x128b_x4(tmem + C::sfb_col(0, 1), umma_desc(smem_u32(sfb + 512), 128, 128));
+      }
+      mbar_arrive(&qready[0]);
+    }
+    __syncwarp();
+  }
+  int64_t i = 0;  // tile counter
+  int sidx = 0;   // segment counter
+  for (int64_t u = u0; u < u1; ++sidx) {
+    const Seg s = seg_at(u, u1, cum, a.B, Hkv);
+    const int qb = sidx % kQBufs;
+    const int ntiles = s.t1 - s.t0;
+    for (int k = 0; k < ntiles; ++k, ++i) {
+      const int slot = static_cast<int>(i % C::kStages), buf = static_cast<int>(i % kGroups);
+      const uint8_t *stage = ring + static_cast<size_t>(slot) * C::kStageBytes;
+      if (i >= kGroups && !warp_wait(&sempty[buf], static_cast<uint32_t>(i / kGroups - 1) & 1u, abort)) return;
+      if (!warp_wait(&full[slot], static_cast<uint32_t>(i / C::kStages) & 1u, abort)) return;
+      if (C::kNv && !warp_wait(&sfready[buf], static_cast<uint32_t>(i / kGroups) & 1u, abort)) return;
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(buf * C::N);
+        const uint32_t a0 = smem_u32(stage), b0 = smem_u32(qimg + qb * C::kQImg);
+        if constexpr (C::kNv) {
+#pragma unroll
+          for (int kk = 0; kk < C::P::kMmas; ++kk)
+            umma_nvfp4(d, umma_desc(a0 + kk * 256, 128, kNvGroup), umma_desc(b0 + kk * 256, 128, C::kQSbo),
+                       idesc_nvfp4(C::N), tmem + C::sfa_col(buf, kk), tmem + C::sfb_col(qb, kk), kk > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < C::P::kMmas; ++kk)
+            umma_e4m3(d, umma_desc(a0 + kk * 256, 128, kF8Group), umma_desc(b0 + kk * 256, 128, C::kQSbo),
+                      idesc_e4m3(C::N), kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&sready[buf]);
+      }
+      __syncwarp();
+      issued = i + 1;
+      if (k == 0 && u + ntiles < u1) {  // the next segment's query image
+        const int nq = (sidx + 1) % kQBufs;
+        const Seg ns = seg_at(u + ntiles, u1, cum, a.B, Hkv);
+        prepare_query<PREC, NH>(a, ns, qimg + nq * C::kQImg, sfb + nq * 1024, cs + nq * 8, kscale);
+        if (lane == 0) {
+          if constexpr (C::kNv) {
+            tc_fence_after();
+            tmem_cp_32x128b_x4(tmem + C::sfb_col(nq, 0), umma_desc(smem_u32(sfb + nq * 1024), 128, 128));
+            tmem_cp_32x128b_x4(tmem + C::sfb_col(nq, 1), umma_desc(smem_u32(sfb + nq * 1024 + 512), 128, 128));
+          }
+          mbar_arrive(&qready[nq]);
+        }
+      }
+    }
+    u += ntiles;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Consumer warps: P.V of a 16-token slice.  Lane = 4r + c.  MMA rows = head_dim
+// (thread r owns d in [16r, 16r+16): tile J covers d = 16r + 2J, +1), k =
+// tokens 2c, 2c+1, 2c+8, 2c+9 of the slice, n = query head.  O for heads
+// 2c, 2c+1 of the group and d in [16r, 16r+16) lives in 32 registers.
+// ---------------------------------------------------------------------------
+struct WarpO {
+  float o[8][4];
 };
 
 // V operand of a slice.  NVFP4: per 8-byte half w, the e2m1 pairs of tokens
-// (2c, 2c+1) at d and d + 1 (x, y) and of tokens (2c+8, 2c+9) (z, t), and the
-// f16x2 block scales of those token pairs; masked tokens carry scale 0.  FP8:
-// the raw code words of tokens 2c, 2c+1, 2c+8, 2c+9, masked tokens zeroed.
+// (2c, 2c+1) at d and d + 1 and of tokens (2c+8, 2c+9), and the f16x2 block
+// scales of those token pairs; masked tokens carry scale 0.  FP8: the raw code
+// words of tokens 2c, 2c+1, 2c+8, 2c+9, masked tokens zeroed.
 template <int PREC>
 struct VOps {
   uint32_t w[PREC == NVKV_PREC_NVFP4 ? 2 : 4][4];
   uint32_t sAB, sCD;
 };
 
+// g0 = the slice's first group (two groups of 8 tokens); nvalid = valid tokens (1..16).
 template <int PREC>
-__device__ __forceinline__ void load_k(const uint8_t *stage, const SliceOffsets<PREC> &o, int r, int c,
-                                       KOps<PREC> &x) {
-  if constexpr (PREC == NVKV_PREC_NVFP4) {
-    const uint4 a = *reinterpret_cast<const uint4 *>(stage + o.kc + r * kNvCodeRow + 16 * c);
-    const uint4 b = *reinterpret_cast<const uint4 *>(stage + o.kc + (r + 8) * kNvCodeRow + 16 * c);
-    x.k0[0] = a.x; x.k0[1] = a.y; x.k0[2] = a.z; x.k0[3] = a.w;
-    x.k1[0] = b.x; x.k1[1] = b.y; x.k1[2] = b.z; x.k1[3] = b.w;
-    const uint32_t s0 = *reinterpret_cast<const uint16_t *>(stage + o.ks + r * kNvScaleRow + 2 * c);
-    const uint32_t s1 = *reinterpret_cast<const uint16_t *>(stage + o.ks + (r + 8) * kNvScaleRow + 2 * c);
-    const uint32_t h0 = f16x2_from_e4m3x2<0>(s0), h1 = f16x2_from_e4m3x2<0>(s1);
-    x.lo0 = prmt(h0, 0, 0x1010);  // {S_2c, S_2c}
-    x.hi0 = prmt(h0, 0, 0x3232);  // {S_2c+1, S_2c+1}
-    x.lo1 = prmt(h1, 0, 0x1010);
-    x.hi1 = prmt(h1, 0, 0x3232);
-  } else {
-    const uint4 *p0 = reinterpret_cast<const uint4 *>(stage + o.kc + r * kF8Row + 32 * c);
-    const uint4 *p1 = reinterpret_cast<const uint4 *>(stage + o.kc + (r + 8) * kF8Row + 32 * c);
-    const uint4 a0 = p0[0], a1 = p0[1], b0 = p1[0], b1 = p1[1];
-    x.k0[0] = a0.x; x.k0[1] = a0.y; x.k0[2] = a0.z; x.k0[3] = a0.w;
-    x.k0[4] = a1.x; x.k0[5] = a1.y; x.k0[6] = a1.z; x.k0[7] = a1.w;
-    x.k1[0] = b0.x; x.k1[1] = b0.y; x.k1[2] = b0.z; x.k1[3] = b0.w;
-    x.k1[4] = b1.x; x.k1[5] = b1.y; x.k1[6] = b1.z; x.k1[7] = b1.w;
-    x.lo0 = x.hi0 = x.lo1 = x.hi1 = 0;
-  }
-}
-
-// nvalid = valid tokens of the slice (0..16): tokens past it are masked.
-template <int PREC>
-__device__ __forceinline__ void load_v(const uint8_t *stage, const SliceOffsets<PREC> &o, int r, int c, int nvalid,
-                                       VOps<PREC> &x) {
+__device__ __forceinline__ void load_v(const uint8_t *g0, int r, int c, int nvalid, VOps<PREC> &x) {
   const int tA = 2 * c;
+  const int pA = v_row_pos(tA), pB = v_row_pos(tA + 1);  // rows 2c, 2c+1 of both groups
   if constexpr (PREC == NVKV_PREC_NVFP4) {
-    const uint2 A = *reinterpret_cast<const uint2 *>(stage + o.vc + tA * kNvCodeRow + 8 * r);
-    const uint2 B = *reinterpret_cast<const uint2 *>(stage + o.vc + (tA + 1) * kNvCodeRow + 8 * r);
-    const uint2 C = *reinterpret_cast<const uint2 *>(stage + o.vc + (tA + 8) * kNvCodeRow + 8 * r);
-    const uint2 D = *reinterpret_cast<const uint2 *>(stage + o.vc + (tA + 9) * kNvCodeRow + 8 * r);
-    const uint8_t *vs = stage + o.vs + r;
-    uint32_t sv = static_cast<uint32_t>(vs[tA * kNvScaleRow]) | (static_cast<uint32_t>(vs[(tA + 1) * kNvScaleRow]) << 8) |
-                  (static_cast<uint32_t>(vs[(tA + 8) * kNvScaleRow]) << 16) |
-                  (static_cast<uint32_t>(vs[(tA + 9) * kNvScaleRow]) << 24);
-    if (nvalid < kSub) {  // masked tokens get scale 0 -> value 0 (codes are finite)
+    const uint8_t *g1 = g0 + kNvGroup;
+    const uint2 A = *reinterpret_cast<const uint2 *>(g0 + kNvVCodes + pA * 64 + 8 * r);
+    const uint2 B = *reinterpret_cast<const uint2 *>(g0 + kNvVCodes + pB * 64 + 8 * r);
+    const uint2 C = *reinterpret_cast<const uint2 *>(g1 + kNvVCodes + pA * 64 + 8 * r);
+    const uint2 D = *reinterpret_cast<const uint2 *>(g1 + kNvVCodes + pB * 64 + 8 * r);
+    uint32_t sv = static_cast<uint32_t>(g0[kNvVScales + tA * 8 + r]) |
+                  (static_cast<uint32_t>(g0[kNvVScales + (tA + 1) * 8 + r]) << 8) |
+                  (static_cast<uint32_t>(g1[kNvVScales + tA * 8 + r]) << 16) |
+                  (static_cast<uint32_t>(g1[kNvVScales + (tA + 1) * 8 + r]) << 24);
+    if (nvalid < 16) {  // masked tokens get scale 0 -> value 0 (codes are finite)
       if (tA >= nvalid) sv &= 0xFFFFFF00u;
       if (tA + 1 >= nvalid) sv &= 0xFFFF00FFu;
       if (tA + 8 >= nvalid) sv &= 0xFF00FFFFu;
@@ -294,22 +452,23 @@ __device__ __forceinline__ void load_v(const uint8_t *stage, const SliceOffsets<
     const uint32_t a[2] = {A.x, A.y}, b[2] = {B.x, B.y}, cc[2] = {C.x, C.y}, dd[2] = {D.x, D.y};
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
-      // byte j: the token pair's low nibbles (d = 16r + 2j') or high nibbles (d + 1)
+      // byte j: the token pair's low nibbles (d = 16r + 8w + 2j) or high nibbles (d + 1)
       x.w[w][0] = (a[w] & 0x0F0F0F0Fu) | ((b[w] & 0x0F0F0F0Fu) << 4);
       x.w[w][1] = ((a[w] >> 4) & 0x0F0F0F0Fu) | (b[w] & 0xF0F0F0F0u);
       x.w[w][2] = (cc[w] & 0x0F0F0F0Fu) | ((dd[w] & 0x0F0F0F0Fu) << 4);
       x.w[w][3] = ((cc[w] >> 4) & 0x0F0F0F0Fu) | (dd[w] & 0xF0F0F0F0u);
     }
   } else {
-    const uint4 A = *reinterpret_cast<const uint4 *>(stage + o.vc + tA * kF8Row + 16 * r);
-    const uint4 B = *reinterpret_cast<const uint4 *>(stage + o.vc + (tA + 1) * kF8Row + 16 * r);
-    const uint4 C = *reinterpret_cast<const uint4 *>(stage + o.vc + (tA + 8) * kF8Row + 16 * r);
-    const uint4 D = *reinterpret_cast<const uint4 *>(stage + o.vc + (tA + 9) * kF8Row + 16 * r);
+    const uint8_t *g1 = g0 + kF8Group;
+    const uint4 A = *reinterpret_cast<const uint4 *>(g0 + kF8V + pA * 128 + 16 * r);
+    const uint4 B = *reinterpret_cast<const uint4 *>(g0 + kF8V + pB * 128 + 16 * r);
+    const uint4 C = *reinterpret_cast<const uint4 *>(g1 + kF8V + pA * 128 + 16 * r);
+    const uint4 D = *reinterpret_cast<const uint4 *>(g1 + kF8V + pB * 128 + 16 * r);
     x.w[0][0] = A.x; x.w[1][0] = A.y; x.w[2][0] = A.z; x.w[3][0] = A.w;
     x.w[0][1] = B.x; x.w[1][1] = B.y; x.w[2][1] = B.z; x.w[3][1] = B.w;
     x.w[0][2] = C.x; x.w[1][2] = C.y; x.w[2][2] = C.z; x.w[3][2] = C.w;
     x.w[0][3] = D.x; x.w[1][3] = D.y; x.w[2][3] = D.z; x.w[3][3] = D.w;
-    if (nvalid < kSub) {  // masked tokens -> E4M3 zero (stale bytes could be NaN)
+    if (nvalid < 16) {  // masked tokens -> E4M3 zero (stale bytes could be NaN)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         if (tA >= nvalid) x.w[q][0] = 0;
@@ -322,29 +481,10 @@ __device__ __forceinline__ void load_v(const uint8_t *stage, const SliceOffsets<
   }
 }
 
-// Score MMA k-step S (even steps accumulate into e, odd into od).
-template <int PREC, int S>
-__device__ __forceinline__ void qk_step(const KOps<PREC> &x, const uint32_t (&qf)[8][2], float (&e)[4],
-                                        float (&od)[4]) {
-  float(&acc)[4] = (S & 1) ? od : e;
-  if constexpr (PREC == NVKV_PREC_NVFP4) {
-    const uint32_t m0 = S < 4 ? x.lo0 : x.hi0, m1 = S < 4 ? x.lo1 : x.hi1;
-    constexpr int B0 = (S & 1) ? 2 : 0, B1 = B0 + 1;
-    const uint32_t a0 = hmul2_u32(f16x2_from_e2m1x2<B0>(x.k0[S >> 1]), m0);
-    const uint32_t a2 = hmul2_u32(f16x2_from_e2m1x2<B1>(x.k0[S >> 1]), m0);
-    const uint32_t a1 = hmul2_u32(f16x2_from_e2m1x2<B0>(x.k1[S >> 1]), m1);
-    const uint32_t a3 = hmul2_u32(f16x2_from_e2m1x2<B1>(x.k1[S >> 1]), m1);
-    mma_f16_16816(acc, a0, a1, a2, a3, qf[S][0], qf[S][1]);
-  } else {
-    mma_f16_16816(acc, f16x2_from_e4m3x2<0>(x.k0[S]), f16x2_from_e4m3x2<0>(x.k1[S]), f16x2_from_e4m3x2<1>(x.k0[S]),
-                  f16x2_from_e4m3x2<1>(x.k1[S]), qf[S][0], qf[S][1]);
-  }
-}
-
 // P.V MMA for output tile J (NVFP4: half w = J / 4, byte J % 4 of each pair
 // word; FP8: token-pair word J / 2, byte pair J % 2).
 template <int PREC, int J>
-__device__ __forceinline__ void pv_tile(const VOps<PREC> &x, uint32_t b0, uint32_t b1, WarpState &st) {
+__device__ __forceinline__ void pv_tile(const VOps<PREC> &x, uint32_t b0, uint32_t b1, WarpO &st) {
   if constexpr (PREC == NVKV_PREC_NVFP4) {
     constexpr int w = J >> 2, I = J & 3;
     mma_f16_16816(st.o[J], hmul2_u32(f16x2_from_e2m1x2<I>(x.w[w][0]), x.sAB),
@@ -359,128 +499,307 @@ __device__ __forceinline__ void pv_tile(const VOps<PREC> &x, uint32_t b0, uint32
   }
 }
 
-// Step J of the pipeline: score k-step J of the next slice and P.V tile J of
-// the current one, each only when asked for.
-template <int PREC, int J, bool QK, bool PV>
-__device__ __forceinline__ void pipe_step(const KOps<PREC> &kx, const uint32_t (&qf)[8][2], float (&e)[4],
-                                          float (&od)[4], const VOps<PREC> &vx, uint32_t b0, uint32_t b1,
-                                          WarpState &st) {
-  if constexpr (QK) qk_step<PREC, J>(kx, qf, e, od);
-  if constexpr (PV) pv_tile<PREC, J>(vx, b0, b1, st);
-}
-
-template <int PREC, bool QK, bool PV>
-__device__ __forceinline__ void pipe_all(const KOps<PREC> &kx, const uint32_t (&qf)[8][2], float (&e)[4],
-                                         float (&od)[4], const VOps<PREC> &vx, uint32_t b0, uint32_t b1,
-                                         WarpState &st) {
-  pipe_step<PREC, 0, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
-  pipe_step<PREC, 1, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
-  pipe_step<PREC, 2, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
-  pipe_step<PREC, 3, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
-  pipe_step<PREC, 4, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
-  pipe_step<PREC, 5, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
-  pipe_step<PREC, 6, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
-  pipe_step<PREC, 7, QK, PV>(kx, qf, e, od, vx, b0, b1, st);
-}
-
-// Online softmax of one slice's scores (e + od, rows r / r + 8, heads 2c,
-// 2c+1, scaled by cs into log2 units; rows at or past nvalid masked): raises
-// the running max only when a score exceeds it by more than the threshold
-// (then O and l are rescaled), and returns P as the two f16x2 B fragments of
-// the P.V MMA (zero for a slice without valid tokens): b0 = P[tok 2c, 2c+1][head r], b1 = P[tok 2c+8, 2c+9][head r].
-__device__ __forceinline__ void softmax_slice(const float (&e)[4], const float (&od)[4], int nvalid, int r,
-                                              const float (&cs)[2], WarpState &st, uint32_t &b0, uint32_t &b1) {
-  if (nvalid <= 0) {  // warp-uniform: a slice past the end of the sequence adds nothing
-    b0 = b1 = 0;
-    return;
-  }
-  const bool v0 = r < nvalid, v1 = r + 8 < nvalid;
-  const float s0 = v0 ? (e[0] + od[0]) * cs[0] : -INFINITY;
-  const float s1 = v0 ? (e[1] + od[1]) * cs[1] : -INFINITY;
-  const float s2 = v1 ? (e[2] + od[2]) * cs[0] : -INFINITY;
-  const float s3 = v1 ? (e[3] + od[3]) * cs[1] : -INFINITY;
-  const bool need = (s0 > st.m[0] + kRescaleThreshold) | (s2 > st.m[0] + kRescaleThreshold) |
-                    (s1 > st.m[1] + kRescaleThreshold) | (s3 > st.m[1] + kRescaleThreshold);
-  if (__any_sync(0xffffffffu, need)) {
-    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-    }
-    const float n0 = fmaxf(st.m[0], mx0), n1 = fmaxf(st.m[1], mx1);
-    const float al0 = ex2(st.m[0] - n0), al1 = ex2(st.m[1] - n1);
-    st.m[0] = n0;
-    st.m[1] = n1;
-    st.l[0] *= al0;
-    st.l[1] *= al1;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      st.o[j][0] *= al0;
-      st.o[j][1] *= al1;
-      st.o[j][2] *= al0;
-      st.o[j][3] *= al1;
-    }
-  }
-  const float p0 = ex2(s0 - st.m[0]), p1 = ex2(s1 - st.m[1]);
-  const float p2 = ex2(s2 - st.m[0]), p3 = ex2(s3 - st.m[1]);
-  st.l[0] += p0 + p2;
-  st.l[1] += p1 + p3;
-  b0 = movmatrix_trans(pack_f16x2(p0, p1));
-  b1 = movmatrix_trans(pack_f16x2(p2, p3));
-}
-
-// Ring position of the next stage a consumer warp reads.
-struct RingPos {
-  int slot = 0;
-  uint32_t phase = 0;
-  template <int PREC>
-  __device__ __forceinline__ void advance() {
-    if (++slot == Layout<PREC>::kStages) {
-      slot = 0;
-      phase ^= 1u;
-    }
-  }
-};
-
-// Wait for the stage at `p`; false (warp-uniform) after a timeout.
-__device__ __forceinline__ bool wait_stage(uint64_t *full, const RingPos &p, volatile int *abort) {
-  const bool ready = mbar_wait_bounded(&full[p.slot], p.phase, abort);
-  return __all_sync(0xffffffffu, ready);
-}
-
-__device__ __forceinline__ int slice_valid(int64_t rem) {
-  return rem < kSub ? (rem > 0 ? static_cast<int>(rem) : 0) : kSub;
+// Two slices: MMA J of slice 1 follows MMA J of slice 0 (same accumulator),
+// the eight accumulator chains run side by side.
+template <int PREC>
+__device__ __forceinline__ void pv_pair(const VOps<PREC> &x, uint32_t b0, uint32_t b1, const VOps<PREC> &y, uint32_t c0,
+                                        uint32_t c1, WarpO &st) {
+  pv_tile<PREC, 0>(x, b0, b1, st);
+  pv_tile<PREC, 1>(x, b0, b1, st);
+  pv_tile<PREC, 2>(x, b0, b1, st);
+  pv_tile<PREC, 3>(x, b0, b1, st);
+  pv_tile<PREC, 0>(y, c0, c1, st);
+  pv_tile<PREC, 1>(y, c0, c1, st);
+  pv_tile<PREC, 2>(y, c0, c1, st);
+  pv_tile<PREC, 3>(y, c0, c1, st);
+  pv_tile<PREC, 4>(x, b0, b1, st);
+  pv_tile<PREC, 5>(x, b0, b1, st);
+  pv_tile<PREC, 6>(x, b0, b1, st);
+  pv_tile<PREC, 7>(x, b0, b1, st);
+  pv_tile<PREC, 4>(y, c0, c1, st);
+  pv_tile<PREC, 5>(y, c0, c1, st);
+  pv_tile<PREC, 6>(y, c0, c1, st);
+  pv_tile<PREC, 7>(y, c0, c1, st);
 }
 
 template <int PREC>
-__global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_kernel(const DecodeArgs a) {
-  using Lay = Layout<PREC>;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t *ring = smem;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::kStages * Lay::kStageBytes);
-  uint64_t *empty = full + Lay::kStages;
-  int32_t *cum = reinterpret_cast<int32_t *>(empty + Lay::kStages);
-  float *mrg_o = reinterpret_cast<float *>(cum + kMaxBatch + 1);
-  float *mrg_ml = mrg_o + kConsumerWarps * a.G * kD;
-  int *flags = reinterpret_cast<int *>(mrg_ml + kConsumerWarps * kMaxGroup * 2);
-  volatile int *abort = flags;              // flags[0]
-  int *fills = flags + 1;                   // flags[1 .. kStages]: fills issued per slot
+__device__ __forceinline__ void pv_slice(const VOps<PREC> &x, uint32_t b0, uint32_t b1, WarpO &st) {
+  pv_tile<PREC, 0>(x, b0, b1, st);
+  pv_tile<PREC, 1>(x, b0, b1, st);
+  pv_tile<PREC, 2>(x, b0, b1, st);
+  pv_tile<PREC, 3>(x, b0, b1, st);
+  pv_tile<PREC, 4>(x, b0, b1, st);
+  pv_tile<PREC, 5>(x, b0, b1, st);
+  pv_tile<PREC, 6>(x, b0, b1, st);
+  pv_tile<PREC, 7>(x, b0, b1, st);
+}
+
+// ---------------------------------------------------------------------------
+// Consumer warps, three groups of four.  Group g takes the tiles i = g (mod 3)
+// of the CTA's share; per tile each warp reads its 32 rows of the group's
+// score buffer (one token per lane, kTerms columns per head), runs the online
+// softmax per head with the running max shared by the warp, writes P to a
+// per-warp [head][token] FP16 tile in shared memory, then P.V for its two
+// 16-token slices with V straight from the stage.  At the end of a segment
+// the twelve warps merge (m, l, O).
+// ---------------------------------------------------------------------------
+// K block scales of this warp's 32 rows of a staged tile into consumer group
+// grp's TMEM scale-factor columns: row m = 32 qd + lane is read by the MMA
+// from lane m, column sfa_col(grp, mma) + qd.
+template <int PREC, int NH>
+__device__ __forceinline__ void put_scales(const uint8_t *stage, uint32_t tq, int grp, int qd, int lane,
+                                           uint64_t *sfready) {
+  using C = Cfg<PREC, NH>;
+  const int t = 32 * qd + lane;
+  const uint2 sc = *reinterpret_cast<const uint2 *>(stage + (t >> 3) * kNvGroup + kNvKScales + (t & 7) * 8);
+  tmem_st1(tq + C::sfa_col(grp, 0) + qd, sc.x);  // blocks 0..3 (MMA 0)
+  tmem_st1(tq + C::sfa_col(grp, 1) + qd, sc.y);  // blocks 4..7 (MMA 1)
+  tmem_st_wait();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&sfready[grp]);
+}
+
+template <int NH>
+__device__ __forceinline__ float pick(const float (&v)[NH], int i) {  // v[i] for a runtime i < NH
+  float r = v[0];
+#pragma unroll
+  for (int k = 1; k < NH; ++k) r = i == k ? v[k] : r;
+  return r;
+}
+
+template <int PREC, int NH>
+__device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uint64_t *full, uint64_t *empty,
+                              uint64_t *sready, uint64_t *sempty, uint64_t *sfready, uint64_t *qready,
+                              const int32_t *cum, int64_t u0, int64_t u1, volatile int *abort) {
+  using C = Cfg<PREC, NH>;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int grp = warp / kGroupWarps, qd = warp % kGroupWarps;  // consumer group, TMEM lane quadrant
+  const int r = lane >> 2, c = lane & 3;
+  const int Hkv = a.c.Hkv, G = a.G;
+  uint8_t *ring = smem + C::oRing;
+  const float *csb = reinterpret_cast<const float *>(smem + C::oCs);
+  __half *pt = reinterpret_cast<__half *>(smem + C::oPt) + warp * NH * 32;
+  float *mrg_o = reinterpret_cast<float *>(smem + C::oMrgO);
+  float *mrg_ml = reinterpret_cast<float *>(smem + C::oMrgMl);
+  const float vscale = a.c.scale[1];
+  const uint32_t tq = tmem + (static_cast<uint32_t>(32 * qd) << 16);  // this warp's lane quadrant
+  int64_t i = 0;
+  int sidx = 0;
+  bool ok = true;
+  const int64_t ntotal = u1 - u0;  // tiles of the share
+  // The group's first tile: its K scales go to TMEM before anything else.
+  if constexpr (C::kNv) {
+    if (grp < ntotal) {
+      ok = warp_wait(&full[grp % C::kStages], static_cast<uint32_t>(grp / C::kStages) & 1u, abort);
+      if (ok) put_scales<PREC, NH>(ring + static_cast<size_t>(grp % C::kStages) * C::kStageBytes, tq, grp, qd, lane,
+                                   sfready);
+    }
+  }
+  // After a timeout (ok false) the warps skip all work but keep walking the
+  // same segments, so every named barrier of the merge still meets.
+  for (int64_t u = u0; u < u1; ++sidx) {
+    const Seg s = seg_at(u, u1, cum, a.B, Hkv);
+    const int Lb = clamped_len(a, s.b);
+    const int qb = sidx % kQBufs;
+    ok = ok && warp_wait(&qready[qb], static_cast<uint32_t>(sidx / kQBufs) & 1u, abort);
+    float cs[NH], m[NH], l[NH];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      cs[h] = csb[qb * 8 + h];
+      m[h] = -INFINITY;
+      l[h] = 0.0f;
+    }
+    WarpO st;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) st.o[j][0] = st.o[j][1] = st.o[j][2] = st.o[j][3] = 0.0f;
+    const int ntiles = s.t1 - s.t0;
+    for (int k = 0; k < ntiles; ++k, ++i) {
+      if (i % kGroups != grp) continue;  // another group's tile
+      const int slot = static_cast<int>(i % C::kStages), buf = grp;
+      ok = ok && warp_wait(&sready[buf], static_cast<uint32_t>(i / kGroups) & 1u, abort) &&
+           warp_wait(&full[slot], static_cast<uint32_t>(i / C::kStages) & 1u, abort);
+      if (!ok) continue;
+      tc_fence_after();
+      float x[NH * kTerms];
+      tmem_ld16(tq + static_cast<uint32_t>(buf * C::N), *reinterpret_cast<float(*)[16]>(x));
+      if constexpr (NH == 8)
+        tmem_ld16(tq + static_cast<uint32_t>(buf * C::N + 16), *reinterpret_cast<float(*)[16]>(x + 16));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sempty[buf]);
+      if (C::kNv && i + kGroups < ntotal) {  // K scales of the group's next tile (its MMAs have completed)
+        const int64_t nx = i + kGroups;
+        const int ns = static_cast<int>(nx % C::kStages);
+        ok = warp_wait(&full[ns], static_cast<uint32_t>(nx / C::kStages) & 1u, abort);
+        if (ok) put_scales<PREC, NH>(ring + static_cast<size_t>(ns) * C::kStageBytes, tq, grp, qd, lane, sfready);
+        else continue;
+      }
+
+      // scores of this lane's token, log2 units; masked past the sequence end
+      const int t = s.t0 + k;
+      const bool valid = t * kTile + 32 * qd + lane < Lb;
+      float sc[NH];
+      bool need = false;
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const float sum = (x[4 * h] + x[4 * h + 1]) + (x[4 * h + 2] + x[4 * h + 3]);
+        sc[h] = (valid && h < G) ? sum * cs[h] : -INFINITY;
+        need |= sc[h] > m[h] + kRescaleThreshold;
+      }
+      if (__any_sync(0xffffffffu, need)) {  // raise the running max (warp-uniform)
+        float al[NH];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          float mx = sc[h];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          const float nm = fmaxf(m[h], mx);
+          al[h] = nm == -INFINITY ? 1.0f : ex2(m[h] - nm);
+          m[h] = nm;
+          l[h] *= al[h];
+        }
+        const float alo = 2 * c < NH ? pick<NH>(al, 2 * c) : 1.0f;
+        const float ahi = 2 * c + 1 < NH ? pick<NH>(al, 2 * c + 1) : 1.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          st.o[j][0] *= alo;
+          st.o[j][2] *= alo;
+          st.o[j][1] *= ahi;
+          st.o[j][3] *= ahi;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const float p = sc[h] == -INFINITY ? 0.0f : ex2(sc[h] - m[h]);
+        l[h] += p;
+        pt[h * 32 + lane] = __float2half_rn(p);
+      }
+      __syncwarp();
+
+      // P.V over the warp's two 16-token slices, their MMA chains interleaved
+      const uint8_t *stage = ring + static_cast<size_t>(slot) * C::kStageBytes;
+      const int rem = Lb - (t * kTile + 32 * qd);  // warp-uniform
+      if (rem > 0) {
+        uint32_t b[4] = {0u, 0u, 0u, 0u};
+        if (r < NH) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) b[q] = *reinterpret_cast<const uint32_t *>(pt + r * 32 + 8 * q + 2 * c);
+        }
+        VOps<PREC> v0;
+        load_v<PREC>(stage + (4 * qd) * C::P::kGroup, r, c, rem < 16 ? rem : 16, v0);
+        if (rem > 16) {
+          VOps<PREC> v1;
+          load_v<PREC>(stage + (4 * qd + 2) * C::P::kGroup, r, c, rem < 32 ? rem - 16 : 16, v1);
+          pv_pair<PREC>(v0, b[0], b[1], v1, b[2], b[3], st);
+        } else {
+          pv_slice<PREC>(v0, b[0], b[1], st);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+
+    // ---- merge the four warps: (m, l) per head, O per (head, d) ----
+#pragma unroll
+    for (int h = 0; h < NH; ++h)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l[h] += __shfl_xor_sync(0xffffffffu, l[h], o);
+    if (lane == 0) {
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        mrg_ml[(warp * kMaxGroup + h) * 2 + 0] = m[h];
+        mrg_ml[(warp * kMaxGroup + h) * 2 + 1] = l[h];
+      }
+    }
+    const int nb = cum[s.b + 1] - cum[s.b];
+    const bool complete = (s.t0 == 0) && (s.t1 == nb);
+    const int slot_id = (u == u0) ? 0 : 1;
+    float *part = a.partials + (static_cast<int64_t>(blockIdx.x) * 2 + slot_id) * kSlotFloats;
+    for (int hp = 0; hp < G; hp += 2) {  // head pairs (hp, hp + 1): held by lanes with 2c == hp
+      if (2 * c == hp) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float *dst = mrg_o + (warp * 2 + e) * kD + 16 * r;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            dst[2 * j] = st.o[j][e];
+            dst[2 * j + 1] = st.o[j][2 + e];
+          }
+        }
+      }
+      named_bar_sync(1, kConsumerWarps * 32);
+      for (int e2 = tid; e2 < 2 * kD; e2 += kConsumerWarps * 32) {
+        const int e = e2 / kD, d = e2 % kD, hd = hp + e;
+        if (hd < G) {
+          float M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg_ml[(w * kMaxGroup + hd) * 2]);
+          float o = 0.0f, lsum = 0.0f;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float mw = mrg_ml[(w * kMaxGroup + hd) * 2];
+            const float f = (mw == -INFINITY) ? 0.0f : ex2(mw - M);
+            o += f * mrg_o[(w * 2 + e) * kD + d];
+            lsum += f * mrg_ml[(w * kMaxGroup + hd) * 2 + 1];
+          }
+          if (complete) {
+            a.out[(static_cast<int64_t>(s.b) * a.Hq + s.h * G + hd) * kD + d] = __float2bfloat16_rn(o * (vscale / lsum));
+          } else {
+            part[hd * kD + d] = o;
+            if (d == 0) {
+              part[kMaxGroup * kD + hd] = M;
+              part[kMaxGroup * kD + kMaxGroup + hd] = lsum;
+            }
+          }
+        }
+      }
+      named_bar_sync(1, kConsumerWarps * 32);
+    }
+    u += ntiles;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The decode kernel: set-up, role dispatch, teardown.
+// ---------------------------------------------------------------------------
+template <int PREC, int NH>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a) {
+  using C = Cfg<PREC, NH>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::oBars);
+  uint64_t *empty = full + C::kStages;
+  uint64_t *sready = empty + C::kStages;  // score buffer g holds a finished tile
+  uint64_t *sempty = sready + kGroups;    // score buffer g was read by the four warps of group g
+  uint64_t *sfready = sempty + kGroups;   // group g wrote the K scales of its next tile to TMEM
+  uint64_t *qready = sfready + kGroups;   // query image q (and its scale factors) ready
+  int32_t *cum = reinterpret_cast<int32_t *>(smem + C::oCum);
+  int *flags = reinterpret_cast<int *>(smem + C::oFlags);
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(flags);
+  volatile int *abort = flags + 1;
+  int *fills = flags + 2;  // fills issued per ring slot
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int Hkv = a.c.Hkv, B = a.B, G = a.G;
+  const int Hkv = a.c.Hkv, B = a.B;
   const int64_t cap = static_cast<int64_t>(a.max_pages) * a.c.P;
 
-  // ---- prologue: tiles per sequence -> prefix sums (warp 0), barriers ----
+  // ---- set-up: barriers, TMEM, tiles per sequence -> prefix sums ----
   if (tid == 0) {
-    flags[0] = 0;
-    for (int s = 0; s < Lay::kStages; ++s) {
+    flags[1] = 0;
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);  // every consumer warp reads every stage
+      mbar_init(&empty[s], kGroupWarps);  // the four warps of the tile's group read it
       fills[s] = 0;
     }
+    for (int b = 0; b < kGroups; ++b) {
+      mbar_init(&sready[b], 1);
+      mbar_init(&sempty[b], kGroupWarps);
+      mbar_init(&sfready[b], kGroupWarps);
+    }
+    for (int q = 0; q < kQBufs; ++q) mbar_init(&qready[q], 1);
     fence_mbar_init();
   }
+  if (warp == kMmaWarp) tmem_alloc(tmem_holder, C::kTmemCols);
   if (warp == 0) {
     int carry = 0;
     if (lane == 0) cum[0] = 0;
@@ -505,7 +824,10 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
 
   const int64_t W = static_cast<int64_t>(cum[B]) * Hkv;
   // never more shares than units: every active CTA owns at least one unit,
@@ -520,7 +842,6 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
     for (int b = tid; b <= B; b += kThreads) a.meta[b] = cum[b];
     if (tid == 0) a.meta[B + 1] = static_cast<int32_t>(NC);
   }
-
   // zero rows of empty sequences (spread over CTAs)
   for (int b = blockIdx.x; b < B; b += a.num_ctas) {
     if (cum[b + 1] == cum[b]) {
@@ -529,177 +850,39 @@ __global__ void __launch_bounds__(kThreads, Layout<PREC>::kMinBlocks) decode_ker
     }
   }
 
-  if (warp == kConsumerWarps) {
-    producer<PREC>(a, ring, full, empty, cum, u0, u1, abort, fills);
-  } else {
-    const int r = lane >> 2, c = lane & 3;
-    const SliceOffsets<PREC> so(warp, a.c.P);
+  int64_t issued = 0;  // tiles whose MMAs the MMA warp issued
+  if (warp == kProducerWarp) {
+    producer<PREC, NH>(a, smem + C::oRing, full, empty, cum, u0, u1, abort, fills);
+  } else if (warp == kMmaWarp) {
     const float kscale = __fmul_rn(a.c.scale[0], a.sm_scale * 1.4426950408889634f);
-    const float vscale = a.c.scale[1];
-    RingPos pos;  // ring position and parity of the next stage this warp reads
-    for (int64_t u = u0; u < u1;) {
-      const Seg s = seg_at(u, u1, cum, B, Hkv);
-      const int64_t Lb = clamped_len(a, s.b);
-      // query of head j = r of the group, d in [32c, 32c+32), scaled by 2^-e_j into FP16
-      uint32_t qf[8][2];
-      float cs[2];
-      {
-        float qv[32];
-        if (r < G) {
-          const uint4 *qp =
-              reinterpret_cast<const uint4 *>(a.q + (static_cast<int64_t>(s.b) * a.Hq + s.h * G + r) * kD + 32 * c);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            const uint4 w = __ldg(qp + v4);
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              qv[8 * v4 + 2 * e] = __uint_as_float(ww[e] << 16);
-              qv[8 * v4 + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) qv[e] = 0.0f;
-        }
-        float am = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) am = fmaxf(am, fabsf(qv[e]));
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-        // ex = exponent of the head's max minus 14: the scaled max lies in [2^14, 2^15)
-        int ex = 0;
-        if (am > 0.0f) ex = static_cast<int>((__float_as_uint(am) >> 23) & 0xFF) - 127 - 14;
-        ex = max(-110, min(110, ex));
-        const float down = __uint_as_float(static_cast<uint32_t>(127 - ex) << 23);
-#pragma unroll
-        for (int s2 = 0; s2 < 8; ++s2) {
-          qf[s2][0] = pack_f16x2(qv[4 * s2] * down, qv[4 * s2 + 1] * down);
-          qf[s2][1] = pack_f16x2(qv[4 * s2 + 2] * down, qv[4 * s2 + 3] * down);
-        }
-        const int e0 = __shfl_sync(0xffffffffu, ex, 8 * c);
-        const int e1 = __shfl_sync(0xffffffffu, ex, 8 * c + 4);
-        cs[0] = __fmul_rn(kscale, __uint_as_float(static_cast<uint32_t>(127 + e0) << 23));
-        cs[1] = __fmul_rn(kscale, __uint_as_float(static_cast<uint32_t>(127 + e1) << 23));
-      }
-      WarpState st;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) st.o[j][0] = st.o[j][1] = st.o[j][2] = st.o[j][3] = 0.0f;
-      st.m[0] = st.m[1] = -INFINITY;
-      st.l[0] = st.l[1] = 0.0f;
-
-      // two-deep pipeline over the segment's slices (see the consumer notes)
-      const int ntiles = s.t1 - s.t0;
-      const int64_t rem0 = Lb - static_cast<int64_t>(s.t0) * kTile - kSub * warp;
-      bool ok = wait_stage(full, pos, abort);
-      RingPos cur = pos;
-      int nv_cur = slice_valid(rem0);
-      uint32_t b0 = 0, b1 = 0;
-      {
-        KOps<PREC> kx;
-        VOps<PREC> vx;
-        float e[4] = {0.f, 0.f, 0.f, 0.f}, od[4] = {0.f, 0.f, 0.f, 0.f};
-        load_k<PREC>(ring + static_cast<size_t>(cur.slot) * Lay::kStageBytes, so, r, c, kx);
-        pipe_all<PREC, true, false>(kx, qf, e, od, vx, 0, 0, st);
-        softmax_slice(e, od, nv_cur, r, cs, st, b0, b1);
-      }
-      pos.template advance<PREC>();
-      for (int k = 0; k < ntiles && ok; ++k) {
-        const uint8_t *stage_cur = ring + static_cast<size_t>(cur.slot) * Lay::kStageBytes;
-        VOps<PREC> vx;
-        load_v<PREC>(stage_cur, so, r, c, nv_cur, vx);
-        if (k + 1 < ntiles) {
-          ok = wait_stage(full, pos, abort);
-          const int nv_next = slice_valid(rem0 - static_cast<int64_t>(k + 1) * kTile);
-          KOps<PREC> kx;
-          load_k<PREC>(ring + static_cast<size_t>(pos.slot) * Lay::kStageBytes, so, r, c, kx);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[cur.slot]);
-          float e[4] = {0.f, 0.f, 0.f, 0.f}, od[4] = {0.f, 0.f, 0.f, 0.f};
-          pipe_all<PREC, true, true>(kx, qf, e, od, vx, b0, b1, st);
-          softmax_slice(e, od, nv_next, r, cs, st, b0, b1);
-          cur = pos;
-          nv_cur = nv_next;
-          pos.template advance<PREC>();
-        } else {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[cur.slot]);
-          KOps<PREC> kx;
-          float e[4], od[4];
-          pipe_all<PREC, false, true>(kx, qf, e, od, vx, b0, b1, st);
-        }
-      }
-
-      // ---- merge the four warps: (m, l) per head, O per (head, d) ----
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        st.l[0] += __shfl_xor_sync(0xffffffffu, st.l[0], o);
-        st.l[1] += __shfl_xor_sync(0xffffffffu, st.l[1], o);
-      }
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int hd = 2 * c + e;
-        if (hd < G) {
-          float *dst = mrg_o + (warp * G + hd) * kD + 16 * r;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            dst[2 * j] = st.o[j][e];
-            dst[2 * j + 1] = st.o[j][2 + e];
-          }
-          if (r == 0) {
-            mrg_ml[(warp * kMaxGroup + hd) * 2 + 0] = st.m[e];
-            mrg_ml[(warp * kMaxGroup + hd) * 2 + 1] = st.l[e];
-          }
-        }
-      }
-      named_bar_sync(1, kConsumerWarps * 32);
-
-      const int nb = cum[s.b + 1] - cum[s.b];
-      const bool complete = (s.t0 == 0) && (s.t1 == nb);
-      const int slot_id = (u == u0) ? 0 : 1;
-      float *part = a.partials + (static_cast<int64_t>(blockIdx.x) * 2 + slot_id) * kSlotFloats;
-      for (int e = tid; e < G * kD; e += kConsumerWarps * 32) {
-        const int hd = e / kD, d = e % kD;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg_ml[(w * kMaxGroup + hd) * 2]);
-        float o = 0.0f, l = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          const float mw = mrg_ml[(w * kMaxGroup + hd) * 2];
-          const float f = (mw == -INFINITY) ? 0.0f : ex2(mw - M);
-          o += f * mrg_o[(w * G + hd) * kD + d];
-          l += f * mrg_ml[(w * kMaxGroup + hd) * 2 + 1];
-        }
-        if (complete) {
-          a.out[(static_cast<int64_t>(s.b) * a.Hq + s.h * G + hd) * kD + d] = __float2bfloat16_rn(o * (vscale / l));
-        } else {
-          part[hd * kD + d] = o;
-          if (d == 0) {
-            part[kMaxGroup * kD + hd] = M;
-            part[kMaxGroup * kD + kMaxGroup + hd] = l;
-          }
-        }
-      }
-      named_bar_sync(1, kConsumerWarps * 32);
-      u += ntiles;
-    }
+    mma_role<PREC, NH>(a, smem, tmem, full, sready, sempty, sfready, qready, cum, u0, u1, abort, kscale, issued);
+  } else {
+    consumer_role<PREC, NH>(a, smem, tmem, full, empty, sready, sempty, sfready, qready, cum, u0, u1, abort);
   }
 
   // this CTA's partials are written: the combine grid may start launching
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  tc_fence_before();
   __syncthreads();
-  // after a timeout, wait (bounded) for copies still in flight before the CTA exits
+  // after a timeout, wait (bounded) for copies and MMAs still in flight
   if (*abort) {
     if (tid == 0) set_err(a.c.err, NVKV_DEVERR_TIMEOUT);
-    if (tid == kConsumerWarps * 32) {
-      volatile int never = 0;
-      for (int s = 0; s < Lay::kStages; ++s)
+    volatile int never = 0;
+    if (tid == kProducerWarp * 32) {
+      for (int s = 0; s < C::kStages; ++s)
         if (fills[s] > 0) mbar_wait_bounded(&full[s], static_cast<uint32_t>(fills[s] - 1) & 1u, &never);
     }
+    if (tid == kMmaWarp * 32) {
+      for (int64_t j = issued - kGroups; j < issued; ++j)
+        if (j >= 0) mbar_wait_bounded(&sready[j % kGroups], static_cast<uint32_t>(j / kGroups) & 1u, &never);
+    }
+  }
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
-
 
 // ---------------------------------------------------------------------------
 // Split-KV merge (log-sum-exp rule), one CTA per (sequence, KV head, query
@@ -775,19 +958,41 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineA
 // ---------------------------------------------------------------------------
 struct DevInfo {
   int sms = 0;
-  int occ[2][kMaxGroup + 1] = {};
+  int occ[2][2] = {};  // [precision][heads per group slot set: 4, 8]
 };
 
 DevInfo g_info[64];
 std::once_flag g_once[64];
 
-template <int PREC>
-int occupancy_for(int G) {
-  const int smem = smem_bytes_for<PREC>(G);
-  if (cudaFuncSetAttribute(decode_kernel<PREC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+// Resident CTAs per SM, from the kernel's shared memory, registers and TMEM
+// columns.  (The runtime's occupancy query reports one CTA per SM for every
+// kernel that allocates TMEM, whatever its resources; two of these CTAs do
+// fit and run side by side.)
+template <int PREC, int NH>
+int occupancy_for(int dev) {
+  const int smem = Cfg<PREC, NH>::kSmem;
+  if (cudaFuncSetAttribute(decode_kernel<PREC, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return 0;
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<PREC>, kThreads, smem) != cudaSuccess) return 0;
+  // two CTAs of ~110 KB per SM need the largest shared-memory carveout
+  if (cudaFuncSetAttribute(decode_kernel<PREC, NH>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+    return 0;
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, decode_kernel<PREC, NH>) != cudaSuccess) return 0;
+  int sm_smem = 0, reserved = 0, sm_regs = 0, sm_threads = 0;
+  cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  cudaDeviceGetAttribute(&sm_regs, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+  cudaDeviceGetAttribute(&sm_threads, cudaDevAttrMaxThreadsPerMultiProcessor, dev);
+  const int by_smem = sm_smem / (smem + static_cast<int>(fa.sharedSizeBytes) + reserved);
+  const int warp_regs = (fa.numRegs * 32 + 255) / 256 * 256;  // allocation unit: 256 registers per warp
+  const int by_regs = warp_regs > 0 ? sm_regs / (warp_regs * (kThreads / 32)) : 0;
+  const int by_threads = sm_threads / kThreads;
+  const int by_tmem = static_cast<int>(512 / Cfg<PREC, NH>::kTmemCols);  // TMEM columns per SM
+  int n = by_smem;
+  n = by_regs < n ? by_regs : n;
+  n = by_threads < n ? by_threads : n;
+  n = by_tmem < n ? by_tmem : n;
   return n;
 }
 
@@ -797,10 +1002,10 @@ const DevInfo *dev_info() {
   std::call_once(g_once[dev], [dev] {
     DevInfo &d = g_info[dev];
     cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-    for (int G = 1; G <= kMaxGroup; ++G) {
-      d.occ[0][G] = occupancy_for<NVKV_PREC_NVFP4>(G);
-      d.occ[1][G] = occupancy_for<NVKV_PREC_FP8_E4M3>(G);
-    }
+    d.occ[0][0] = occupancy_for<NVKV_PREC_NVFP4, 4>(dev);
+    d.occ[0][1] = occupancy_for<NVKV_PREC_NVFP4, 8>(dev);
+    d.occ[1][0] = occupancy_for<NVKV_PREC_FP8_E4M3, 4>(dev);
+    d.occ[1][1] = occupancy_for<NVKV_PREC_FP8_E4M3, 8>(dev);
   });
   return g_info[dev].sms > 0 ? &g_info[dev] : nullptr;
 }
@@ -814,8 +1019,8 @@ int64_t num_ctas_for(int prec, int32_t batch, int32_t Hkv, int32_t G, int64_t ma
   } else {
     const DevInfo *d = dev_info();
     if (!d) return -1;
-    const int occ = d->occ[prec][G] > 0 ? d->occ[prec][G] : 1;
-    n = static_cast<int64_t>(d->sms) * occ;
+    const int o = d->occ[prec][G > 4 ? 1 : 0];
+    n = static_cast<int64_t>(d->sms) * (o > 0 ? o : 1);
   }
   if (n > max_units) n = max_units;
   return n < 1 ? 1 : n;
@@ -824,9 +1029,13 @@ int64_t num_ctas_for(int prec, int32_t batch, int32_t Hkv, int32_t G, int64_t ma
 // Workspace = schedule (cum[0..B], NC) + two partial slots per CTA.
 size_t meta_bytes(int32_t batch) { return (static_cast<size_t>(batch + 2) * 4 + 255) / 256 * 256; }
 
-size_t workspace_bytes_for(int32_t batch, int32_t Hkv, int64_t nctas) {
-  (void)Hkv;
+size_t workspace_bytes_for(int32_t batch, int64_t nctas) {
   return meta_bytes(batch) + static_cast<size_t>(nctas) * 2 * kSlotFloats * sizeof(float);
+}
+
+template <int PREC, int NH>
+void launch_decode(const DecodeArgs &a, cudaStream_t s) {
+  decode_kernel<PREC, NH><<<static_cast<unsigned>(a.num_ctas), kThreads, Cfg<PREC, NH>::kSmem, s>>>(a);
 }
 
 nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t *block_table, int32_t max_pages,
@@ -849,7 +1058,7 @@ nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t 
   const int64_t nctas = num_ctas_for(prec, batch, Hkv, G, max_units, num_splits);
   if (nctas < 0) return NVKV_ERR_CUDA;
   if (nctas > 0x7fffffff) return NVKV_ERR_UNSUPPORTED;
-  if (workspace_bytes < workspace_bytes_for(batch, Hkv, nctas)) return NVKV_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < workspace_bytes_for(batch, nctas)) return NVKV_ERR_WORKSPACE_TOO_SMALL;
   if (!dev_info()) return NVKV_ERR_CUDA;
 
   DecodeArgs a;
@@ -867,11 +1076,13 @@ nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t 
   a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + meta_bytes(batch));
   a.out = static_cast<__nv_bfloat16 *>(out);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (prec == NVKV_PREC_NVFP4)
-    decode_kernel<NVKV_PREC_NVFP4><<<static_cast<int>(nctas), kThreads, smem_bytes_for<NVKV_PREC_NVFP4>(G), s>>>(a);
-  else
-    decode_kernel<NVKV_PREC_FP8_E4M3>
-        <<<static_cast<int>(nctas), kThreads, smem_bytes_for<NVKV_PREC_FP8_E4M3>(G), s>>>(a);
+  if (prec == NVKV_PREC_NVFP4) {
+    if (G <= 4) launch_decode<NVKV_PREC_NVFP4, 4>(a, s);
+    else launch_decode<NVKV_PREC_NVFP4, 8>(a, s);
+  } else {
+    if (G <= 4) launch_decode<NVKV_PREC_FP8_E4M3, 4>(a, s);
+    else launch_decode<NVKV_PREC_FP8_E4M3, 8>(a, s);
+  }
   st = launch_status();
   if (st != NVKV_OK) return st;
   // split-KV merge, launched as a programmatic dependent of the decode grid
@@ -972,10 +1183,10 @@ size_t nvkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t nu
     const DevInfo *d = dev_info();
     if (!d) return 0;
     int occ = 1;
-    for (int p = 0; p < 2; ++p) occ = d->occ[p][G] > occ ? d->occ[p][G] : occ;
+    for (int p = 0; p < 2; ++p) occ = d->occ[p][G > 4 ? 1 : 0] > occ ? d->occ[p][G > 4 ? 1 : 0] : occ;
     nctas = static_cast<int64_t>(d->sms) * occ;
   }
-  return workspace_bytes_for(batch, num_kv_heads, nctas);
+  return workspace_bytes_for(batch, nctas);
 }
 
 nvkv_status nvkv_decode_workspace_init(void *workspace, size_t bytes, void *stream) {

@@ -20,7 +20,7 @@ inline nvkv_status check_cache(const nvkv_cache *c, int32_t want_prec) {
   if (c->num_pages <= 0 || c->num_kv_heads <= 0 || c->page_size <= 0 || c->head_dim <= 0)
     return NVKV_ERR_INVALID_ARG;
   if (c->head_dim != 128) return NVKV_ERR_UNSUPPORTED;
-  if (c->page_size != 16 && c->page_size != 32 && c->page_size != 64) return NVKV_ERR_UNSUPPORTED;
+  if (c->page_size != 16 && c->page_size != 32 && c->page_size != 64) return NVKV_ERR_UNSUPPORTED;  // multiples of 8
   if (!c->data || !c->kv_scale) return NVKV_ERR_INVALID_ARG;
   if (!aligned16(c->data)) return NVKV_ERR_UNSUPPORTED;
   return NVKV_OK;
@@ -32,29 +32,44 @@ inline nvkv_status launch_status() {
 }
 
 // Device-side view of a cache descriptor (passed by value to kernels).
-// Byte layout of one (page, KV head) block at head_dim 128 (see the header).
-constexpr int kNvCodeRow = 64, kNvScaleRow = 8, kNvTokBytes = 144;  // NVFP4: per token, K+V
-constexpr int kF8Row = 128, kF8TokBytes = 256;                      // FP8
+// Byte layout of one (page, KV head) block at head_dim 128 (see the header):
+// groups of 8 slots; an NVFP4 group is [K codes 512 | K scales 64 | V codes
+// 512 | V scales 64] = 1152 bytes, an FP8 group [K 1024 | V 1024]; K bytes in
+// 16-byte chunks, chunk-major (the tensor-core operand order); V rows in the
+// order 0,2,4,6,1,3,5,7.
+constexpr int kNvTokBytes = 144, kF8TokBytes = 256;  // per token, K + V
+constexpr int kGroupRows = 8;
+constexpr int kNvGroup = kGroupRows * kNvTokBytes;    // 1152
+constexpr int kF8Group = kGroupRows * kF8TokBytes;    // 2048
+constexpr int kNvKScales = 512, kNvVCodes = 576, kNvVScales = 1088;  // offsets inside an NVFP4 group
+constexpr int kF8V = 1024;                                          // offset of V inside an FP8 group
+
+__host__ __device__ constexpr int v_row_pos(int r) { return (r & 1) * 4 + (r >> 1); }
 
 struct CacheDev {
   uint8_t *data;
   const float *scale;
   int32_t *err;
   int32_t num_pages, P, Hkv;
-  // NVFP4 plane offsets inside a block: kind 0 = K, 1 = V
   __host__ __device__ int64_t block(int64_t page, int h, int tok_bytes) const {
     return (page * Hkv + h) * static_cast<int64_t>(P) * tok_bytes;
   }
-  __host__ __device__ int64_t nv_codes(int64_t page, int h, int kind, int off) const {
-    return block(page, h, kNvTokBytes) + static_cast<int64_t>(kind) * P * (kNvCodeRow + kNvScaleRow) +
-           static_cast<int64_t>(off) * kNvCodeRow;
+  // NVFP4: the 8 code bytes of 16-value block `blk` of slot `off` (kind 0 = K, 1 = V)
+  __host__ __device__ int64_t nv_codes(int64_t page, int h, int kind, int off, int blk) const {
+    const int64_t g = block(page, h, kNvTokBytes) + static_cast<int64_t>(off >> 3) * kNvGroup;
+    const int r = off & 7;
+    return kind == 0 ? g + (blk >> 1) * 128 + r * 16 + (blk & 1) * 8 : g + kNvVCodes + v_row_pos(r) * 64 + blk * 8;
   }
-  __host__ __device__ int64_t nv_scales(int64_t page, int h, int kind, int off) const {
-    return block(page, h, kNvTokBytes) + static_cast<int64_t>(kind) * P * (kNvCodeRow + kNvScaleRow) +
-           static_cast<int64_t>(P) * kNvCodeRow + static_cast<int64_t>(off) * kNvScaleRow;
+  // NVFP4: the E4M3 scale byte of block `blk` of slot `off`
+  __host__ __device__ int64_t nv_scale(int64_t page, int h, int kind, int off, int blk) const {
+    return block(page, h, kNvTokBytes) + static_cast<int64_t>(off >> 3) * kNvGroup +
+           (kind == 0 ? kNvKScales : kNvVScales) + (off & 7) * 8 + blk;
   }
-  __host__ __device__ int64_t f8_row(int64_t page, int h, int kind, int off) const {
-    return block(page, h, kF8TokBytes) + static_cast<int64_t>(kind) * P * kF8Row + static_cast<int64_t>(off) * kF8Row;
+  // FP8: the 16 bytes of 16-value block `blk` of slot `off`
+  __host__ __device__ int64_t f8_block(int64_t page, int h, int kind, int off, int blk) const {
+    const int64_t g = block(page, h, kF8TokBytes) + static_cast<int64_t>(off >> 3) * kF8Group;
+    const int r = off & 7;
+    return kind == 0 ? g + blk * 128 + r * 16 : g + kF8V + v_row_pos(r) * 128 + blk * 16;
   }
 };
 

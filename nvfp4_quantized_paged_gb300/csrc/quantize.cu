@@ -137,8 +137,8 @@ __global__ void __launch_bounds__(256)
       hi |= e2m1x2_from_f32(__fdiv_rn(x[8 + 2 * j], den), __fdiv_rn(x[8 + 2 * j + 1], den)) << (8 * j);
     }
   }
-  *reinterpret_cast<uint2 *>(c.data + c.nv_codes(page, h, kind, off) + 8 * blk) = make_uint2(lo, hi);
-  c.data[c.nv_scales(page, h, kind, off) + blk] = static_cast<uint8_t>(sbyte);
+  *reinterpret_cast<uint2 *>(c.data + c.nv_codes(page, h, kind, off, blk)) = make_uint2(lo, hi);
+  c.data[c.nv_scale(page, h, kind, off, blk)] = static_cast<uint8_t>(sbyte);
 }
 
 // ---------------------------------------------------------------------------
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(256)
              (e4m3x2_from_f32(__fdiv_rn(x[4 * j + 2], s8), __fdiv_rn(x[4 * j + 3], s8)) << 16);
     }
   }
-  *reinterpret_cast<uint4 *>(c.data + c.f8_row(page, h, kind, off) + 16 * blk) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4 *>(c.data + c.f8_block(page, h, kind, off, blk)) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // ---------------------------------------------------------------------------
@@ -231,8 +231,8 @@ __global__ void __launch_bounds__(256)
     return;
   }
   const int off = static_cast<int>(t % c.P);
-  const uint2 cw = *reinterpret_cast<const uint2 *>(c.data + c.nv_codes(page, h, kind, off) + 8 * blk);
-  const float S = f32_from_e4m3(c.data[c.nv_scales(page, h, kind, off) + blk]);
+  const uint2 cw = *reinterpret_cast<const uint2 *>(c.data + c.nv_codes(page, h, kind, off, blk));
+  const float S = f32_from_e4m3(c.data[c.nv_scale(page, h, kind, off, blk)]);
   const float ratio = __fdiv_rn(c.scale[kind], ws_scale[kind]);
   const uint32_t words[2] = {cw.x, cw.y};
   uint32_t out[4];

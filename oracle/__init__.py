@@ -65,6 +65,8 @@ def lib():
         L.orc_fp8_quantize_write.restype = ctypes.c_int
         L.orc_fp8_quantize_write.argtypes = [_f32p, _f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _i64p,
                                              _f32p, ctypes.c_int, ctypes.c_int64, _u8p]
+        L.orc_slot_bytes.restype = ctypes.c_int
+        L.orc_slot_bytes.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i64p]
         L.orc_gather_dequant.restype = ctypes.c_int
         L.orc_gather_dequant.argtypes = [ctypes.c_int, _u8p, ctypes.c_int, ctypes.c_float, _i32p, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
@@ -158,33 +160,53 @@ def global_scale(x: np.ndarray, divisor: float = NVFP4_GLOBAL_DIVISOR) -> np.flo
 class Cache:
     """One layer's paged cache: one contiguous block per (page, KV head).
 
-    ``data`` uint8 [num_pages, Hkv, block]: NVFP4 block = [K codes P*D/2 |
-    K scales P*D/16 | V codes P*D/2 | V scales P*D/16] (P*144 bytes at
-    D = 128); FP8 block = [K P*D | V P*D].  ``k_data``/``k_scale``/``v_data``/
-    ``v_scale`` are numpy views of the planes, shaped [num_pages, Hkv, P, D/2]
-    and [num_pages, Hkv, P, D/16] (FP8: [num_pages, Hkv, P, D], no scales).
+    ``data`` uint8 [num_pages, Hkv, block] holds the bytes in the cache layout
+    stated in nvfp4kv_oracle.c (groups of 8 slots; K bytes chunk-major; V rows
+    reordered); the block is P*144 bytes at D = 128 for NVFP4 and P*256 for
+    FP8.  ``k_data``/``k_scale``/``v_data``/``v_scale`` return copies of the
+    logical planes, shaped [num_pages, Hkv, P, D/2] and [num_pages, Hkv, P,
+    D/16] (FP8: [num_pages, Hkv, P, D], no scales); ``positions(name)`` gives
+    the [P, n] byte positions of a plane inside a block, for writes.
     ``g`` = float32[2] (K, V) global (NVFP4) or per-tensor (FP8) scale.
     """
 
     def __init__(self, prec, num_pages, Hkv, P, D, g, fill=0):
         self.prec, self.num_pages, self.Hkv, self.P, self.D = prec, num_pages, Hkv, P, D
         self.g = np.asarray(g, np.float32).reshape(2).copy()
-        if prec == PREC_NVFP4:
-            half = P * (D // 2 + D // 16)
-            self.data = np.full((num_pages, Hkv, 2 * half), fill, np.uint8)
-            cs, ss = P * (D // 2), P * (D // 16)
-            self.k_data = self.data[:, :, :cs].reshape(num_pages, Hkv, P, D // 2)
-            self.k_scale = self.data[:, :, cs:half].reshape(num_pages, Hkv, P, D // 16)
-            self.v_data = self.data[:, :, half:half + cs].reshape(num_pages, Hkv, P, D // 2)
-            self.v_scale = self.data[:, :, half + cs:].reshape(num_pages, Hkv, P, D // 16)
-            del ss
+        block = P * 2 * (D // 2 + D // 16) if prec == PREC_NVFP4 else 2 * P * D
+        self.data = np.full((num_pages, Hkv, block), fill, np.uint8)
+        self._slot_pos = None
+
+    def slot_positions(self) -> np.ndarray:
+        """int64 [P, bytes per slot]: positions of every byte of each slot in a block."""
+        if self._slot_pos is None:
+            n = self.D + self.D // 8 if self.prec == PREC_NVFP4 else 2 * self.D
+            pos = np.empty((self.P, n), np.int64)
+            for off in range(self.P):
+                row = pos[off]
+                assert lib().orc_slot_bytes(self.prec, self.P, self.D, off, _p(row, _i64p)) == 0
+            self._slot_pos = pos
+        return self._slot_pos
+
+    def positions(self, name: str) -> np.ndarray:
+        D, pos = self.D, self.slot_positions()
+        if self.prec == PREC_NVFP4:
+            c, s = D // 2, D // 16
+            cuts = {"k_data": (0, c), "k_scale": (c, c + s), "v_data": (c + s, 2 * c + s), "v_scale": (2 * c + s, 2 * c + 2 * s)}
         else:
-            self.data = np.full((num_pages, Hkv, 2 * P * D), fill, np.uint8)
-            self.k_data = self.data[:, :, :P * D].reshape(num_pages, Hkv, P, D)
-            self.v_data = self.data[:, :, P * D:].reshape(num_pages, Hkv, P, D)
-            self.k_scale = self.v_scale = None
-        for v in (self.k_data, self.v_data, self.k_scale, self.v_scale):
-            assert v is None or np.shares_memory(v, self.data)
+            cuts = {"k_data": (0, D), "v_data": (D, 2 * D)}
+        a, b = cuts[name]
+        return pos[:, a:b]
+
+    def _plane(self, name):
+        if self.prec != PREC_NVFP4 and name.endswith("scale"):
+            return None
+        return self.data[:, :, self.positions(name)]
+
+    k_data = property(lambda self: self._plane("k_data"))
+    k_scale = property(lambda self: self._plane("k_scale"))
+    v_data = property(lambda self: self._plane("v_data"))
+    v_scale = property(lambda self: self._plane("v_scale"))
 
     @property
     def nbytes(self):

@@ -29,9 +29,16 @@
  *   FP8 layers    : s8 = amax / 448; byte = E4M3_RNE_sat(x / s8); s8 == 0 -> 0x00
  *
  * Cache layout (the pages give none): one contiguous block per (page, KV
- * head), pages then heads: NVFP4 block = [K codes P*D/2 | K scales P*D/16 |
- * V codes P*D/2 | V scales P*D/16]; FP8 block = [K P*D | V P*D].  Inside a
- * plane, slot `off` of the page is row `off`.
+ * head), pages then heads.  Inside a block the page's slots form groups of
+ * R rows, R = 8 when the page size is a multiple of 8 (else R = page size):
+ * slot off is row r = off % R of group off / R.  A group holds, in this
+ * order, NVFP4: K codes (R*D/2 bytes), K scales (R*D/16), V codes (R*D/2),
+ * V scales (R*D/16); FP8: K (R*D), V (R*D).  K bytes of a group are stored in
+ * chunks of w = min(16, row bytes) bytes, chunk-major: byte j of row r sits at
+ * (j/w)*R*w + r*w + j%w.  V bytes are row-major, with the rows of an 8-row
+ * group in the order 0,2,4,6,1,3,5,7 (row r at position (r%2)*4 + r/2);
+ * scales are row-major.  Only the byte positions differ from a plain row
+ * layout: every byte's content is the definition below.
  *
  * Every FP32 step is one IEEE-754 binary32 operation with round-to-nearest-even
  * and no fused multiply-add (build with -ffp-contract=off).  Attention runs in
@@ -189,18 +196,53 @@ static void fp8_quantize_vector(const float *x, int D, float s8, uint8_t *out) {
   for (i = 0; i < D; ++i) out[i] = (s8 == 0.0f) ? 0 : orc_e4m3_encode(x[i] / s8);
 }
 
-/* Byte offsets inside the cache (one contiguous block per page and KV head). */
+/* Byte positions inside the cache (layout in the header comment). */
 static int64_t nv_block_bytes(int P, int D) { return (int64_t)P * 2 * (D / 2 + D / 16); }
 static int64_t fp8_block_bytes(int P, int D) { return (int64_t)P * 2 * D; }
 
-/* NVFP4: plane 0 = codes, 1 = scales; kind 0 = K, 1 = V. */
-static int64_t nv_offset(int64_t page, int Hkv, int h, int P, int D, int kind, int plane, int off) {
-  int64_t base = (page * Hkv + h) * nv_block_bytes(P, D) + (int64_t)kind * P * (D / 2 + D / 16);
-  return plane == 0 ? base + (int64_t)off * (D / 2) : base + (int64_t)P * (D / 2) + (int64_t)off * (D / 16);
+/* Rows per group and the position of V row r inside its group. */
+static int group_rows(int P) { return P % 8 == 0 ? 8 : P; }
+static int v_row_pos(int R, int r) { return R == 8 ? (r % 2) * 4 + r / 2 : r; }
+
+/* K byte j of row r inside a group of R rows of `rowbytes` bytes: chunks of
+ * w bytes, chunk-major. */
+static int64_t k_chunked(int R, int rowbytes, int r, int j) {
+  const int w = rowbytes < 16 ? rowbytes : 16;
+  return (int64_t)(j / w) * R * w + (int64_t)r * w + j % w;
 }
 
-static int64_t fp8_offset(int64_t page, int Hkv, int h, int P, int D, int kind, int off) {
-  return (page * Hkv + h) * fp8_block_bytes(P, D) + (int64_t)kind * P * D + (int64_t)off * D;
+/* NVFP4 byte j of slot `off`: plane 0 = codes (j < D/2), 1 = scales (j < D/16);
+ * kind 0 = K, 1 = V. */
+static int64_t nv_byte(int64_t page, int Hkv, int h, int P, int D, int kind, int plane, int off, int j) {
+  const int R = group_rows(P), r = off % R;
+  const int64_t half = (int64_t)R * (D / 2 + D / 16);  /* K (or V) part of a group */
+  const int64_t base = (page * Hkv + h) * nv_block_bytes(P, D) + (int64_t)(off / R) * 2 * half + kind * half;
+  if (plane == 0) return base + (kind == 0 ? k_chunked(R, D / 2, r, j) : (int64_t)v_row_pos(R, r) * (D / 2) + j);
+  return base + (int64_t)R * (D / 2) + (int64_t)r * (D / 16) + j;
+}
+
+/* FP8 byte j (< D) of slot `off`. */
+static int64_t fp8_byte(int64_t page, int Hkv, int h, int P, int D, int kind, int off, int j) {
+  const int R = group_rows(P), r = off % R;
+  const int64_t base = (page * Hkv + h) * fp8_block_bytes(P, D) + (int64_t)(off / R) * 2 * R * D;
+  return base + (kind == 0 ? k_chunked(R, D, r, j) : (int64_t)R * D + (int64_t)v_row_pos(R, r) * D + j);
+}
+
+/* Positions of the bytes of slot `off` inside its (page, KV head) block, in
+ * the order K codes, K scales, V codes, V scales (FP8: K bytes, V bytes);
+ * out holds D + D/8 (FP8: 2*D) entries. */
+int orc_slot_bytes(int prec, int P, int D, int off, int64_t *out) {
+  int kind, j, n = 0;
+  if (off < 0 || off >= P) return -1;
+  for (kind = 0; kind < 2; ++kind) {
+    if (prec == 0) {
+      for (j = 0; j < D / 2; ++j) out[n++] = nv_byte(0, 1, 0, P, D, kind, 0, off, j);
+      for (j = 0; j < D / 16; ++j) out[n++] = nv_byte(0, 1, 0, P, D, kind, 1, off, j);
+    } else {
+      for (j = 0; j < D; ++j) out[n++] = fp8_byte(0, 1, 0, P, D, kind, off, j);
+    }
+  }
+  return 0;
 }
 
 /* Quantized write into paged slots ([P1] 02 "quantized write"; [P2] Three
@@ -222,8 +264,12 @@ int orc_nvfp4_quantize_write(const float *k, const float *v, int64_t T, int Hkv,
     for (h = 0; h < Hkv; ++h)
       for (kind = 0; kind < 2; ++kind) {
         const float *src = (kind ? v : k) + (t * Hkv + h) * D;
-        nvfp4_quantize_vector(src, D, g[kind], cache + nv_offset(page, Hkv, h, P, D, kind, 0, off),
-                              cache + nv_offset(page, Hkv, h, P, D, kind, 1, off));
+        uint8_t codes[512], scales[64];
+        int j;
+        if (D > 1024) return -1;
+        nvfp4_quantize_vector(src, D, g[kind], codes, scales);
+        for (j = 0; j < D / 2; ++j) cache[nv_byte(page, Hkv, h, P, D, kind, 0, off, j)] = codes[j];
+        for (j = 0; j < D / 16; ++j) cache[nv_byte(page, Hkv, h, P, D, kind, 1, off, j)] = scales[j];
       }
   }
   return 0;
@@ -244,9 +290,13 @@ int orc_fp8_quantize_write(const float *k, const float *v, int64_t T, int Hkv, i
     page = slot / P;
     off = (int)(slot % P);
     for (h = 0; h < Hkv; ++h)
-      for (kind = 0; kind < 2; ++kind)
-        fp8_quantize_vector((kind ? v : k) + (t * Hkv + h) * D, D, s8[kind],
-                            cache + fp8_offset(page, Hkv, h, P, D, kind, off));
+      for (kind = 0; kind < 2; ++kind) {
+        uint8_t row[1024];
+        int j;
+        if (D > 1024) return -1;
+        fp8_quantize_vector((kind ? v : k) + (t * Hkv + h) * D, D, s8[kind], row);
+        for (j = 0; j < D; ++j) cache[fp8_byte(page, Hkv, h, P, D, kind, off, j)] = row[j];
+      }
   }
   return 0;
 }
@@ -261,15 +311,14 @@ static void dequant_row(int prec, const uint8_t *cache, int64_t page, int Hkv, i
                         int off, float g, double *out) {
   int d;
   if (prec == 0) {
-    const uint8_t *c = cache + nv_offset(page, Hkv, h, P, D, kind, 0, off);
-    const uint8_t *s = cache + nv_offset(page, Hkv, h, P, D, kind, 1, off);
     for (d = 0; d < D; ++d) {
-      uint8_t code = (d & 1) ? (uint8_t)(c[d / 2] >> 4) : (uint8_t)(c[d / 2] & 15);
-      out[d] = orc_e2m1_value(code) * orc_e4m3_value(s[d / 16]) * (double)g;
+      const uint8_t byte = cache[nv_byte(page, Hkv, h, P, D, kind, 0, off, d / 2)];
+      const uint8_t sc = cache[nv_byte(page, Hkv, h, P, D, kind, 1, off, d / 16)];
+      uint8_t code = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+      out[d] = orc_e2m1_value(code) * orc_e4m3_value(sc) * (double)g;
     }
   } else {
-    const uint8_t *c = cache + fp8_offset(page, Hkv, h, P, D, kind, off);
-    for (d = 0; d < D; ++d) out[d] = orc_e4m3_value(c[d]) * (double)g;
+    for (d = 0; d < D; ++d) out[d] = orc_e4m3_value(cache[fp8_byte(page, Hkv, h, P, D, kind, off, d)]) * (double)g;
   }
 }
 
@@ -401,12 +450,12 @@ int orc_dequant_to_fp8_workspace(const int32_t *block_table, int max_pages, cons
         int64_t page = brow[t / P];
         if (page < 0 || page >= num_pages) return -1;
         for (h = 0; h < Hkv; ++h) {
-          const uint8_t *c = cache + nv_offset(page, Hkv, h, P, D, pass, 0, t % P);
-          const uint8_t *s = cache + nv_offset(page, Hkv, h, P, D, pass, 1, t % P);
           uint8_t *dst = ws + ((cu_prefix[i] + t) * Hkv + h) * D;
           for (d = 0; d < D; ++d) {
-            uint8_t code = (d & 1) ? (uint8_t)(c[d / 2] >> 4) : (uint8_t)(c[d / 2] & 15);
-            float w = (float)(orc_e2m1_value(code) * orc_e4m3_value(s[d / 16]));
+            const uint8_t byte = cache[nv_byte(page, Hkv, h, P, D, pass, 0, t % P, d / 2)];
+            const uint8_t sc = cache[nv_byte(page, Hkv, h, P, D, pass, 1, t % P, d / 16)];
+            uint8_t code = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+            float w = (float)(orc_e2m1_value(code) * orc_e4m3_value(sc));
             dst[d] = orc_e4m3_encode(w * r);
           }
         }

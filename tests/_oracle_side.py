@@ -37,8 +37,9 @@ class OracleLayer:
             self.block_table[i, :n] = [remap[int(p)] for p in wl.block_table[b, :n]]
         prec = oracle.PREC_FP8 if fp8 else oracle.PREC_NVFP4
         self.cache = oracle.Cache(prec, max(1, len(pages)), s.Hkv, s.P, s.D, self.g)
+        self.lens = {b: int(wl.seq_lens[b]) + self.ext[b] for b in self.seqs}
         for i, b in enumerate(self.seqs):
-            L = int(wl.seq_lens[b]) + self.ext[b]
+            L = self.lens[b]
             if L == 0:
                 continue
             t = np.arange(L)
@@ -52,12 +53,27 @@ class OracleLayer:
         return oracle.paged_decode_attention(self.cache, self.q_bits, self.block_table, self.seq_lens,
                                              num_splits=num_splits)
 
-    def planes(self):
+    def compare_bytes(self, gpu_data):
+        """Assert that every byte of every slot the oracle wrote equals the
+        GPU cache's byte at the same position (GPU pages gathered in the
+        compact order; slot byte positions from the oracle's layout)."""
+        import torch
         c = self.cache
-        out = [("k_data", c.k_data), ("v_data", c.v_data)]
-        if c.prec == oracle.PREC_NVFP4:
-            out += [("k_scale", c.k_scale), ("v_scale", c.v_scale)]
-        return out
+        P, pos = c.P, c.slot_positions()
+        blocks = gpu_data[torch.from_numpy(self.global_pages).to(gpu_data.device)].cpu().numpy()
+        hh = np.arange(c.Hkv)[None, :, None]
+        for i, b in enumerate(self.seqs):
+            L = self.lens[b]
+            for t0 in range(0, L, 4096):
+                t = np.arange(t0, min(L, t0 + 4096))
+                lp = self.block_table[i, t // P][:, None, None]
+                idx = pos[t % P][:, None, :]
+                got, want = blocks[lp, hh, idx], c.data[lp, hh, idx]
+                if not np.array_equal(got, want):
+                    bad = np.argwhere(got != want)[0]
+                    raise AssertionError(f"cache bytes differ: sequence {b}, token {t0 + bad[0]}, head {bad[1]}, "
+                                         f"byte {bad[2]} of the slot: gpu {got[tuple(bad)]:#x} oracle "
+                                         f"{want[tuple(bad)]:#x}")
 
 
 def within_tol(got, want, atol=2e-3, rtol=1e-2):

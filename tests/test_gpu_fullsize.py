@@ -21,13 +21,7 @@ def _check_layer(lay, wl, seqs, fp8, with_extend=False):
     assert lay.cache.err.item() == 0
     orc = OracleLayer(wl, lay.layer, seqs, fp8, with_extend=with_extend)
     assert np.array_equal(lay.scale.cpu().numpy(), orc.g)
-    for name, plane in orc.planes():
-        gpu = getattr(lay.cache, name)[torch.from_numpy(orc.global_pages).cuda()].cpu().numpy()
-        for i, b in enumerate(orc.seqs):
-            L = int(wl.seq_lens[b]) + orc.ext[b]
-            t = np.arange(L)
-            lp = orc.block_table[i, t // spec.P]
-            np.testing.assert_array_equal(gpu[lp, :, t % spec.P], plane[lp, :, t % spec.P], err_msg=name)
+    orc.compare_bytes(lay.cache.data)
     if with_extend:
         return orc
     want = orc.attention()

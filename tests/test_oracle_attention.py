@@ -168,8 +168,8 @@ def test_workspace_exact_when_representable(orc):
     E4M3 value maps to exactly that byte."""
     Hkv, D, P = 1, 16, 4
     c = orc.Cache(0, 1, Hkv, P, D, [1.0, 1.0])
-    c.k_data[0, 0, 0] = np.array([0x21, 0x43, 0x65, 0x07, 0x98, 0xBA, 0xDC, 0x0F], np.uint8)
-    c.k_scale[0, 0, 0, 0] = 0x38  # S = 1
+    c.data[0, 0, c.positions("k_data")[0]] = np.array([0x21, 0x43, 0x65, 0x07, 0x98, 0xBA, 0xDC, 0x0F], np.uint8)
+    c.data[0, 0, c.positions("k_scale")[0, 0]] = 0x38  # S = 1
     bt = np.zeros((1, 1), np.int32)
     wk, _ = orc.dequant_to_fp8_workspace(c, bt, [0], [1], np.array([1.0, 1.0], np.float32))
     vals = _e4m3(wk[0, 0])

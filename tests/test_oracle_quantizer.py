@@ -197,19 +197,46 @@ def test_planted_mistakes_are_caught(orc):
 
 
 def test_block_layout_offsets(orc):
-    """One contiguous block per (page, KV head): NVFP4 [K codes | K scales |
-    V codes | V scales], FP8 [K | V]; row = page offset."""
+    """Byte positions of one written slot, stated here independently of the
+    oracle: one contiguous block per (page, KV head); groups of R slots (R = 8
+    when the page size is a multiple of 8, else the page size); per group
+    NVFP4 [K codes | K scales | V codes | V scales], FP8 [K | V]; K bytes in
+    16-byte chunks, chunk-major; V rows of an 8-row group in the order
+    0,2,4,6,1,3,5,7."""
+    # page size 4 (one group of 4 rows), D = 32: K codes 16 B per row (one chunk)
     Hkv, P, D = 2, 4, 32
     c = orc.Cache(orc.PREC_NVFP4, 3, Hkv, P, D, [1.0, 1.0])
     x = np.zeros((1, Hkv, D), np.float32)
     x[0, 1, 0] = 6.0  # head 1, element 0 -> code 7, scale 1.0 (0x38)
     orc.quantize_write(c, x, 0.5 * x, np.array([2 * P + 3], np.int64))  # page 2, offset 3
     blk = c.data[2, 1]
-    cb, sb = P * D // 2, P * D // 16
-    assert blk[3 * (D // 2)] == 0x07 and blk[cb + 3 * (D // 16)] == 0x38              # K: code 7, scale 1
-    assert blk[cb + sb + 3 * (D // 2)] == 0x07 and blk[2 * cb + sb + 3 * (D // 16)] == 0x30  # V: 3 = 6 x 0.5
+    # K codes [0,64): row 3 at 48; K scales [64,72): row 3 at 70; V codes [72,136): row 3 at 120; V scales at 142
+    assert blk[48] == 0x07 and blk[70] == 0x38
+    assert blk[120] == 0x07 and blk[142] == 0x30  # V: 3 = 6 x 0.5 -> scale 0.5
     assert np.count_nonzero(c.data) == 4
     f = orc.Cache(orc.PREC_FP8, 3, Hkv, P, D, [1.0, 1.0])
     orc.quantize_write(f, x, 0.5 * x, np.array([2 * P + 3], np.int64))
-    assert f.data[2, 1, 3 * D] == 0x4C and f.data[2, 1, P * D + 3 * D] == 0x44      # E4M3(6), E4M3(3)
+    # FP8: K [0,128): row 3 byte 0 at 48; V [128,256): row 3 at 128 + 3*32
+    assert f.data[2, 1, 48] == 0x4C and f.data[2, 1, 128 + 96] == 0x44  # E4M3(6), E4M3(3)
     assert np.count_nonzero(f.data) == 2
+    # page size 16, D = 128: slot 11 = group 1 (1152 bytes in), row 3
+    c = orc.Cache(orc.PREC_NVFP4, 1, 1, 16, 128, [1.0, 1.0])
+    x = np.zeros((1, 1, 128), np.float32)
+    x[0, 0, 0] = 6.0    # K byte 0 (chunk 0) and block 0
+    x[0, 0, 35] = 6.0   # byte 17 (chunk 1, high nibble), block 2
+    orc.quantize_write(c, x, 0.5 * x, np.array([11], np.int64))
+    blk = c.data[0, 0]
+    g0 = 1152
+    assert blk[g0 + 3 * 16] == 0x07 and blk[g0 + 128 + 3 * 16 + 1] == 0x70       # K chunks 0 and 1 of row 3
+    assert blk[g0 + 512 + 3 * 8] == 0x38 and blk[g0 + 512 + 3 * 8 + 2] == 0x38   # K scales of blocks 0, 2
+    vrow = 5  # row 3 sits at position (3 % 2) * 4 + 3 // 2
+    assert blk[g0 + 576 + vrow * 64] == 0x07 and blk[g0 + 576 + vrow * 64 + 17] == 0x70
+    assert blk[g0 + 1088 + 3 * 8] == 0x30 and blk[g0 + 1088 + 3 * 8 + 2] == 0x30
+    assert np.count_nonzero(c.data) == 8
+    f = orc.Cache(orc.PREC_FP8, 1, 1, 16, 128, [1.0, 1.0])
+    orc.quantize_write(f, x, 0.5 * x, np.array([11], np.int64))
+    fb = f.data[0, 0]
+    g0 = 2048
+    assert fb[g0 + 3 * 16] == 0x4C and fb[g0 + 2 * 128 + 3 * 16 + 3] == 0x4C   # K bytes 0 and 35
+    assert fb[g0 + 1024 + vrow * 128] == 0x44 and fb[g0 + 1024 + vrow * 128 + 35] == 0x44
+    assert np.count_nonzero(f.data) == 4
