@@ -12,9 +12,11 @@
 //     (sequence, KV head) cut between CTAs leaves split-KV partials that a
 //     second kernel merges with the log-sum-exp rule.
 //   * Warp roles: a producer warp streams tiles into a shared-memory ring with
-//     1-D bulk copies (one per page block, mbarrier transaction counts); an MMA
-//     warp computes the scores of each tile on the 5th-generation tensor cores;
-//     four consumer warps (one per TMEM lane quadrant, 32 tokens each) run the
+//     1-D bulk copies (one per page block, mbarrier transaction counts); a
+//     query warp prepares each segment's query operand; twelve consumer warps
+//     in three groups of four (one warp per TMEM lane quadrant, 32 tokens each)
+//     take the tiles round-robin: a group issues the score MMAs of its next
+//     tile as soon as it has read the scores of its current one, then runs the
 //     softmax and P.V.
 //   * Scores S = K Q^T straight from the packed cache: the K codes of a staged
 //     tile are the A operand of one block-scaled MMA (kind::mxf4nvf4, M = 128
@@ -51,12 +53,14 @@ constexpr int kTile = 128;         // tokens per work unit / ring stage (the MMA
 constexpr int kGroups = 3;         // consumer groups: group g takes the tiles i = g (mod 3) of the CTA
 constexpr int kGroupWarps = 4;     // warp w of a group owns tokens [32w, 32w+32) of a tile = TMEM lane quadrant w
 constexpr int kConsumerWarps = kGroups * kGroupWarps;
-constexpr int kProducerWarp = kConsumerWarps, kMmaWarp = kConsumerWarps + 1;
-constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kProducerWarp = kConsumerWarps;       // producer warps kProducerWarp + g, one per group
+constexpr int kQueryWarp = kConsumerWarps + kGroups;
+constexpr int kThreads = (kConsumerWarps + kGroups + 1) * 32;
 constexpr int kMaxBatch = 1024;    // sequences per call (prefix sums live in shared memory)
 constexpr int kMaxGroup = 8;       // query heads per KV head
 constexpr int kTerms = 4;          // query terms of the score MMA
-constexpr int kQBufs = 3;          // query images in flight (segments)
+constexpr int kQBufs = 4;          // query images in flight: a group issues a tile at most three
+                                   // segments ahead of the one all warps are in (segments of one tile)
 constexpr int kSlotFloats = kMaxGroup * kD + 2 * kMaxGroup;  // one partial (o, m, l)
 constexpr float kRescaleThreshold = 8.0f;                   // log2 units
 
@@ -69,7 +73,7 @@ struct Prec<NVKV_PREC_NVFP4> {
   static constexpr int kGroup = kNvGroup;             // 1152
   static constexpr int kKRow = 64;                    // K bytes per token
   static constexpr int kMmas = 2;                     // K = 64 values per instruction
-  static constexpr int kRing = 10;                    // stages at 4 heads per group
+  static constexpr int kRing = 3;                     // stages per consumer group
 };
 template <>
 struct Prec<NVKV_PREC_FP8_E4M3> {
@@ -77,7 +81,7 @@ struct Prec<NVKV_PREC_FP8_E4M3> {
   static constexpr int kGroup = kF8Group;             // 2048
   static constexpr int kKRow = 128;
   static constexpr int kMmas = 4;                     // K = 32 values per instruction
-  static constexpr int kRing = 6;
+  static constexpr int kRing = 2;
 };
 
 // NH = heads per group slot set (4 or 8), N = NH * kTerms columns of the score MMA.
@@ -87,7 +91,18 @@ struct Cfg {
   static constexpr bool kNv = PREC == NVKV_PREC_NVFP4;
   static constexpr int N = NH * kTerms;
   static constexpr int kStageBytes = kTile / kGroupRows * P::kGroup;     // 18432 / 32768
-  static constexpr int kStages = NH == 4 ? P::kRing : P::kRing - 1;
+  // Each consumer group has its own ring of kStagesG stages, filled by its own
+  // producer warp: tile i (group i % 3, ordinal i / 3 within the group) sits
+  // in slot slot_of(i) of the flat stage array, fill fill_of(i).
+  static constexpr int kStagesG = P::kRing;
+  static constexpr int kStages = kGroups * kStagesG;
+  __host__ __device__ static constexpr int slot_of(int64_t i) {
+    return static_cast<int>(i % kGroups) * kStagesG + static_cast<int>((i / kGroups) % kStagesG);
+  }
+  __host__ __device__ static constexpr uint32_t fill_of(int64_t i) {
+    return static_cast<uint32_t>(i / kGroups / kStagesG);
+  }
+  static constexpr int kMH = (!kNv && NH == 8) ? 1 : 2;  // heads per pass of the segment merge
   static constexpr int kQRow = P::kKRow;                                 // B row bytes
   static constexpr int kQImg = N * kQRow;                                // one query image
   static constexpr int kQSbo = 8 * kQRow;                                // 8-row group stride of B
@@ -101,14 +116,14 @@ struct Cfg {
   // shared memory (bytes)
   static constexpr int oRing = 0;
   static constexpr int oQImg = oRing + kStages * kStageBytes;
-  static constexpr int oSfb = oQImg + kQBufs * kQImg;                       // [3][2][32][16] (NVFP4)
+  static constexpr int oSfb = oQImg + kQBufs * kQImg;                       // [4][2][32][16] (NVFP4)
   static constexpr int oPt = oSfb + (kNv ? kQBufs * 2 * 512 : 0);          // [12 warps][NH][32] f16
-  static constexpr int oCs = oPt + kConsumerWarps * NH * 32 * 2;           // [3][8] f32
-  static constexpr int oMrgO = oCs + kQBufs * 8 * 4;                       // [12 warps][2][128] f32
-  static constexpr int oMrgMl = oMrgO + kConsumerWarps * 2 * kD * 4;       // [12 warps][8][2] f32
+  static constexpr int oCs = oPt + kConsumerWarps * NH * 32 * 2;           // [4][8] f32
+  static constexpr int oMrgO = oCs + kQBufs * 8 * 4;                       // [12 warps][kMH][128] f32
+  static constexpr int oMrgMl = oMrgO + kConsumerWarps * kMH * kD * 4;     // [12 warps][8][2] f32
   static constexpr int oCum = oMrgMl + kConsumerWarps * kMaxGroup * 2 * 4;  // [kMaxBatch + 1] i32
   static constexpr int oBars = (oCum + (kMaxBatch + 1) * 4 + 15) / 16 * 16;
-  static constexpr int kBars = 2 * kStages + 3 * kGroups + kQBufs;  // full, empty, sready, sempty, sfready, qready
+  static constexpr int kBars = 2 * kStages + kGroups + 2 * kQBufs;  // full, empty, sready, qready, qfree
   static constexpr int oFlags = oBars + kBars * 8;                          // tmem holder, abort, fills[kStages]
   static constexpr int kSmem = oFlags + 4 * (2 + kStages);
 };
@@ -171,57 +186,66 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
 }
 
 // ---------------------------------------------------------------------------
-// Producer warp: one bulk copy per page block of each tile of this CTA's
-// share (a tile spans 128 / P whole page blocks, placed back to back, so the
-// stage is 16 groups of 8 tokens at a uniform stride).  Lane j copies block j.
+// Producer warps, one per consumer group: producer g streams the tiles
+// i = g (mod 3) of this CTA's share into group g's ring, one bulk copy per
+// page block (a tile spans 128 / P whole page blocks, placed back to back, so
+// the stage is 16 groups of 8 tokens at a uniform stride).  Lane j copies
+// block j.
 // ---------------------------------------------------------------------------
 template <int PREC, int NH>
 __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uint64_t *empty, const int32_t *cum,
-                         int64_t u0, int64_t u1, volatile int *abort, int *fills) {
+                         int64_t u0, int64_t u1, int grp, volatile int *abort, int *fills) {
   using C = Cfg<PREC, NH>;
   const int lane = threadIdx.x & 31;
   const int Hkv = a.c.Hkv, P = a.c.P;
   const uint64_t policy = policy_evict_first();
   const uint32_t block_bytes = static_cast<uint32_t>(P) * C::P::kTokBytes;
-  int64_t i = 0;  // stage counter
+  int64_t i = 0;  // CTA-local tile index
   for (int64_t u = u0; u < u1;) {
     const Seg s = seg_at(u, u1, cum, a.B, Hkv);
-    const int len = clamped_len(a, s.b);
-    const int32_t *brow = a.block_table + static_cast<int64_t>(s.b) * a.max_pages;
-    // Block-table window: lane l holds the entry of page index wbase + l; the
-    // next window is requested when the current one comes into use.
-    int wbase = (s.t0 * kTile) / P;
-    int32_t pg = wbase + lane < a.max_pages ? brow[wbase + lane] : 0;
-    int32_t pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
-    for (int t = s.t0; t < s.t1; ++t, ++i) {
-      const int slot = static_cast<int>(i % C::kStages);
-      const uint32_t fill = static_cast<uint32_t>(i / C::kStages);
-      if (__any_sync(0xffffffffu, *abort)) return;
-      if (lane == 0 && fill > 0) mbar_wait_bounded(&empty[slot], (fill - 1) & 1u, abort);
-      if (__any_sync(0xffffffffu, *abort)) return;  // warp-uniform exit
-      const int tok0 = t * kTile;
-      const int ntok = min(kTile, len - tok0);
-      const int nblk = (ntok + P - 1) / P;  // page blocks holding the tile's tokens
-      if ((tok0 + ntok - 1) / P >= wbase + 32) {  // the tile leaves the window (warp-uniform)
-        wbase += 32;
-        pg = pg_next;
-        pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nblk) * block_bytes);
-      const int pidx = lane < nblk ? tok0 / P + lane - wbase : 0;
-      const int64_t page_w = __shfl_sync(0xffffffffu, pg, pidx & 31);
-      if (lane < nblk) {
-        int64_t page = page_w;
-        if (page < 0 || page >= a.c.num_pages) {
-          set_err(a.c.err, NVKV_DEVERR_PAGE);
-          page = 0;  // a valid address; the output of this sequence is then undefined
+    const int ntiles = s.t1 - s.t0;
+    const int64_t ifirst = i + ((grp - i % kGroups) + kGroups) % kGroups;  // this group's first tile here
+    if (ifirst < i + ntiles) {
+      const int len = clamped_len(a, s.b);
+      const int32_t *brow = a.block_table + static_cast<int64_t>(s.b) * a.max_pages;
+      // Block-table window: lane l holds the entry of page index wbase + l; the
+      // next window is requested when the current one comes into use.  Window
+      // edges fall on tile edges (32 pages hold whole tiles at P = 16, 32, 64).
+      int wbase = ((s.t0 + static_cast<int>(ifirst - i)) * kTile) / P;
+      int32_t pg = wbase + lane < a.max_pages ? brow[wbase + lane] : 0;
+      int32_t pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
+      for (int64_t x = ifirst; x < i + ntiles; x += kGroups) {
+        const int t = s.t0 + static_cast<int>(x - i);
+        const int slot = C::slot_of(x);
+        const uint32_t fill = C::fill_of(x);
+        if (__any_sync(0xffffffffu, *abort)) return;
+        if (lane == 0 && fill > 0) mbar_wait_bounded(&empty[slot], (fill - 1) & 1u, abort);
+        if (__any_sync(0xffffffffu, *abort)) return;  // warp-uniform exit
+        const int tok0 = t * kTile;
+        const int ntok = min(kTile, len - tok0);
+        const int nblk = (ntok + P - 1) / P;  // page blocks holding the tile's tokens
+        while ((tok0 + ntok - 1) / P >= wbase + 32) {  // the tile leaves the window (warp-uniform)
+          wbase += 32;
+          pg = pg_next;
+          pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
         }
-        bulk_g2s(ring + static_cast<size_t>(slot) * C::kStageBytes + static_cast<size_t>(lane) * block_bytes,
-                 a.c.data + a.c.block(page, s.h, C::P::kTokBytes), block_bytes, &full[slot], policy);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nblk) * block_bytes);
+        const int pidx = lane < nblk ? tok0 / P + lane - wbase : 0;
+        const int64_t page_w = __shfl_sync(0xffffffffu, pg, pidx & 31);
+        if (lane < nblk) {
+          int64_t page = page_w;
+          if (page < 0 || page >= a.c.num_pages) {
+            set_err(a.c.err, NVKV_DEVERR_PAGE);
+            page = 0;  // a valid address; the output of this sequence is then undefined
+          }
+          bulk_g2s(ring + static_cast<size_t>(slot) * C::kStageBytes + static_cast<size_t>(lane) * block_bytes,
+                   a.c.data + a.c.block(page, s.h, C::P::kTokBytes), block_bytes, &full[slot], policy);
+        }
+        if (lane == 0) fills[slot] = static_cast<int>(fill) + 1;
       }
-      if (lane == 0) fills[slot] = static_cast<int>(fill) + 1;
     }
-    u += s.t1 - s.t0;
+    i += ntiles;
+    u += ntiles;
   }
 }
 
@@ -324,86 +348,44 @@ __device__ void prepare_query(const DecodeArgs &a, const Seg &s, uint8_t *img, u
 }
 
 // ---------------------------------------------------------------------------
-// MMA warp.  Per tile i: once consumer group g = i % 3 has read its previous
-// tile's scores and written this tile's K block scales into its TMEM
-// scale-factor columns, issue the score MMAs into group g's score buffer and
-// commit them to sready[g].  The query image of a segment is prepared one
-// segment ahead (ring of three), right after the first MMA of the current
-// segment issues.
+// Query warp: the query images of the CTA's segments, in order, into a ring of
+// four.  Image s overwrites image s - 4 once all consumer warps have merged
+// segment s - 4 (qfree), which means every MMA that read it has completed.  A
+// group issues a tile at most three tiles (so three segments) ahead of the
+// segment it is in, and every warp has finished the segment before that one:
+// the image it waits for never waits for the group itself.
+// qready[q] completes when the image, its scale factors in TMEM (NVFP4: two
+// tcgen05.cp copies, tracked by a commit) and its score factors are in place.
 // ---------------------------------------------------------------------------
 template <int PREC, int NH>
-__device__ void mma_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uint64_t *full, uint64_t *sready,
-                         uint64_t *sempty, uint64_t *sfready, uint64_t *qready, const int32_t *cum, int64_t u0,
-                         int64_t u1, volatile int *abort, float kscale, int64_t &issued) {
+__device__ int query_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uint64_t *qready, uint64_t *qfree,
+                          const int32_t *cum, int64_t u0, int64_t u1, volatile int *abort, float kscale) {
   using C = Cfg<PREC, NH>;
   const int lane = threadIdx.x & 31;
-  uint8_t *ring = smem + C::oRing;
   uint8_t *qimg = smem + C::oQImg;
   uint8_t *sfb = smem + C::oSfb;
   float *cs = reinterpret_cast<float *>(smem + C::oCs);
-  const int Hkv = a.c.Hkv;
-  issued = 0;
-  if (u0 >= u1) return;
-  {
-    const Seg s0 = seg_at(u0, u1, cum, a.B, Hkv);
-    prepare_query<PREC, NH>(a, s0, qimg, sfb, cs, kscale);
+  int sidx = 0;
+  for (int64_t u = u0; u < u1; ++sidx) {
+    const Seg s = seg_at(u, u1, cum, a.B, a.c.Hkv);
+    const int q = sidx % kQBufs;
+    if (sidx >= kQBufs && !warp_wait(&qfree[q], static_cast<uint32_t>(sidx / kQBufs - 1) & 1u, abort)) return sidx;
+    prepare_query<PREC, NH>(a, s, qimg + q * C::kQImg, sfb + q * 1024, cs + q * 8, kscale);
     if (lane == 0) {
       if constexpr (C::kNv) {
         tc_fence_after();
-        tmem_cp_32x128b_x4(tmem + C::sfb_col(0, 0), umma_desc(smem_u32(sfb), 128, 128));
-        tmem_cp_32x128b_x4(tmem + C::sfb_col(0, 1), umma_desc(smem_u32(sfb + 512), 128, 128));
+        tmem_cp_32x128b_x4(tmem + C::sfb_col(q, 0), umma_desc(smem_u32(sfb + q * 1024), 128, 128));
+        tmem_cp_32x128b_x4(tmem + C::sfb_col(q, 1), umma_desc(smem_u32(sfb + q * 1024 + 512), 128, 128));
+        umma_commit(&qready[q]);  // arrives when the copies are done
+      } else {
+        mbar_arrive(&qready[q]);
       }
-      mbar_arrive(&qready[0]);
+      mbar_arrive(&qready[q]);    // the image and score factors (release)
     }
     __syncwarp();
+    u += s.t1 - s.t0;
   }
-  int64_t i = 0;  // tile counter
-  int sidx = 0;   // segment counter
-  for (int64_t u = u0; u < u1; ++sidx) {
-    const Seg s = seg_at(u, u1, cum, a.B, Hkv);
-    const int qb = sidx % kQBufs;
-    const int ntiles = s.t1 - s.t0;
-    for (int k = 0; k < ntiles; ++k, ++i) {
-      const int slot = static_cast<int>(i % C::kStages), buf = static_cast<int>(i % kGroups);
-      const uint8_t *stage = ring + static_cast<size_t>(slot) * C::kStageBytes;
-      if (i >= kGroups && !warp_wait(&sempty[buf], static_cast<uint32_t>(i / kGroups - 1) & 1u, abort)) return;
-      if (!warp_wait(&full[slot], static_cast<uint32_t>(i / C::kStages) & 1u, abort)) return;
-      if (C::kNv && !warp_wait(&sfready[buf], static_cast<uint32_t>(i / kGroups) & 1u, abort)) return;
-      if (lane == 0) {
-        tc_fence_after();
-        const uint32_t d = tmem + static_cast<uint32_t>(buf * C::N);
-        const uint32_t a0 = smem_u32(stage), b0 = smem_u32(qimg + qb * C::kQImg);
-        if constexpr (C::kNv) {
-#pragma unroll
-          for (int kk = 0; kk < C::P::kMmas; ++kk)
-            umma_nvfp4(d, umma_desc(a0 + kk * 256, 128, kNvGroup), umma_desc(b0 + kk * 256, 128, C::kQSbo),
-                       idesc_nvfp4(C::N), tmem + C::sfa_col(buf, kk), tmem + C::sfb_col(qb, kk), kk > 0 ? 1u : 0u);
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < C::P::kMmas; ++kk)
-            umma_e4m3(d, umma_desc(a0 + kk * 256, 128, kF8Group), umma_desc(b0 + kk * 256, 128, C::kQSbo),
-                      idesc_e4m3(C::N), kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&sready[buf]);
-      }
-      __syncwarp();
-      issued = i + 1;
-      if (k == 0 && u + ntiles < u1) {  // the next segment's query image
-        const int nq = (sidx + 1) % kQBufs;
-        const Seg ns = seg_at(u + ntiles, u1, cum, a.B, Hkv);
-        prepare_query<PREC, NH>(a, ns, qimg + nq * C::kQImg, sfb + nq * 1024, cs + nq * 8, kscale);
-        if (lane == 0) {
-          if constexpr (C::kNv) {
-            tc_fence_after();
-            tmem_cp_32x128b_x4(tmem + C::sfb_col(nq, 0), umma_desc(smem_u32(sfb + nq * 1024), 128, 128));
-            tmem_cp_32x128b_x4(tmem + C::sfb_col(nq, 1), umma_desc(smem_u32(sfb + nq * 1024 + 512), 128, 128));
-          }
-          mbar_arrive(&qready[nq]);
-        }
-      }
-    }
-    u += ntiles;
-  }
+  return sidx;  // images prepared
 }
 
 // ---------------------------------------------------------------------------
@@ -543,21 +525,69 @@ __device__ __forceinline__ void pv_slice(const VOps<PREC> &x, uint32_t b0, uint3
 // 16-token slices with V straight from the stage.  At the end of a segment
 // the twelve warps merge (m, l, O).
 // ---------------------------------------------------------------------------
-// K block scales of this warp's 32 rows of a staged tile into consumer group
-// grp's TMEM scale-factor columns: row m = 32 qd + lane is read by the MMA
-// from lane m, column sfa_col(grp, mma) + qd.
+// Index of the segment holding CTA-local tile x, walking forward from the
+// segment that starts at unit u (index sidx, ntiles tiles).
+__device__ __forceinline__ int seg_index_of(int64_t x, int64_t u, int sidx, int ntiles, int64_t u0, int64_t u1,
+                                            const int32_t *cum, int B, int Hkv) {
+  while (x >= (u - u0) + ntiles) {
+    u += ntiles;
+    ++sidx;
+    const Seg ns = seg_at(u, u1, cum, B, Hkv);
+    ntiles = ns.t1 - ns.t0;
+  }
+  return sidx;
+}
+
+// Score MMAs of CTA-local tile x (segment sx) for consumer group grp: each of
+// the group's warps waits for the tile's stage and (NVFP4) writes the K block
+// scales of its 32 rows into the group's TMEM scale-factor columns (row
+// m = 32 qd + lane is read by the MMA from lane m, column sfa_col(grp, mma) +
+// qd); the four warps meet on the group's named barrier; one thread waits for
+// the segment's query image and issues the MMAs into the group's score buffer,
+// committing them to sready[grp].  The caller has read the group's previous
+// scores, so the buffer and the scale columns are free.
 template <int PREC, int NH>
-__device__ __forceinline__ void put_scales(const uint8_t *stage, uint32_t tq, int grp, int qd, int lane,
-                                           uint64_t *sfready) {
+__device__ __forceinline__ bool issue_tile(uint8_t *smem, uint32_t tmem, uint32_t tq, uint64_t *full, uint64_t *sready,
+                                           uint64_t *qready, int64_t x, int sx, int grp, int qd, int lane,
+                                           volatile int *abort) {
   using C = Cfg<PREC, NH>;
-  const int t = 32 * qd + lane;
-  const uint2 sc = *reinterpret_cast<const uint2 *>(stage + (t >> 3) * kNvGroup + kNvKScales + (t & 7) * 8);
-  tmem_st1(tq + C::sfa_col(grp, 0) + qd, sc.x);  // blocks 0..3 (MMA 0)
-  tmem_st1(tq + C::sfa_col(grp, 1) + qd, sc.y);  // blocks 4..7 (MMA 1)
-  tmem_st_wait();
+  const int slot = C::slot_of(x);
+  const uint8_t *stage = smem + C::oRing + static_cast<size_t>(slot) * C::kStageBytes;
+  bool ok = warp_wait(&full[slot], C::fill_of(x) & 1u, abort);
+  if constexpr (C::kNv) {
+    if (ok) {
+      const int t = 32 * qd + lane;
+      const uint2 sc = *reinterpret_cast<const uint2 *>(stage + (t >> 3) * kNvGroup + kNvKScales + (t & 7) * 8);
+      tmem_st1(tq + C::sfa_col(grp, 0) + qd, sc.x);  // blocks 0..3 (MMA 0)
+      tmem_st1(tq + C::sfa_col(grp, 1) + qd, sc.y);  // blocks 4..7 (MMA 1)
+      tmem_st_wait();
+    }
+  }
   tc_fence_before();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&sfready[grp]);
+  named_bar_sync(2 + grp, kGroupWarps * 32);
+  if (qd == 0) {
+    const int qb = sx % kQBufs;
+    ok = ok && warp_wait(&qready[qb], static_cast<uint32_t>(sx / kQBufs) & 1u, abort);
+    if (ok && lane == 0) {
+      tc_fence_after();
+      const uint32_t d = tmem + static_cast<uint32_t>(grp * C::N);
+      const uint32_t a0 = smem_u32(stage), b0 = smem_u32(smem + C::oQImg + qb * C::kQImg);
+      if constexpr (C::kNv) {
+#pragma unroll
+        for (int kk = 0; kk < C::P::kMmas; ++kk)
+          umma_nvfp4(d, umma_desc(a0 + kk * 256, 128, kNvGroup), umma_desc(b0 + kk * 256, 128, C::kQSbo),
+                     idesc_nvfp4(C::N), tmem + C::sfa_col(grp, kk), tmem + C::sfb_col(qb, kk), kk > 0 ? 1u : 0u);
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < C::P::kMmas; ++kk)
+          umma_e4m3(d, umma_desc(a0 + kk * 256, 128, kF8Group), umma_desc(b0 + kk * 256, 128, C::kQSbo),
+                    idesc_e4m3(C::N), kk > 0 ? 1u : 0u);
+      }
+      umma_commit(&sready[grp]);
+    }
+    __syncwarp();
+  }
+  return ok;
 }
 
 template <int NH>
@@ -570,8 +600,8 @@ __device__ __forceinline__ float pick(const float (&v)[NH], int i) {  // v[i] fo
 
 template <int PREC, int NH>
 __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uint64_t *full, uint64_t *empty,
-                              uint64_t *sready, uint64_t *sempty, uint64_t *sfready, uint64_t *qready,
-                              const int32_t *cum, int64_t u0, int64_t u1, volatile int *abort) {
+                              uint64_t *sready, uint64_t *qready, uint64_t *qfree, const int32_t *cum, int64_t u0,
+                              int64_t u1, volatile int *abort, int64_t &last_issued) {
   using C = Cfg<PREC, NH>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = warp / kGroupWarps, qd = warp % kGroupWarps;  // consumer group, TMEM lane quadrant
@@ -588,13 +618,13 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
   int sidx = 0;
   bool ok = true;
   const int64_t ntotal = u1 - u0;  // tiles of the share
-  // The group's first tile: its K scales go to TMEM before anything else.
-  if constexpr (C::kNv) {
-    if (grp < ntotal) {
-      ok = warp_wait(&full[grp % C::kStages], static_cast<uint32_t>(grp / C::kStages) & 1u, abort);
-      if (ok) put_scales<PREC, NH>(ring + static_cast<size_t>(grp % C::kStages) * C::kStageBytes, tq, grp, qd, lane,
-                                   sfready);
-    }
+  last_issued = -1;
+  // The group's first tile is issued before anything else.
+  if (grp < ntotal) {
+    const Seg s0 = seg_at(u0, u1, cum, a.B, Hkv);
+    const int sx = seg_index_of(grp, u0, 0, s0.t1 - s0.t0, u0, u1, cum, a.B, Hkv);
+    ok = issue_tile<PREC, NH>(smem, tmem, tq, full, sready, qready, grp, sx, grp, qd, lane, abort);
+    last_issued = grp;
   }
   // After a timeout (ok false) the warps skip all work but keep walking the
   // same segments, so every named barrier of the merge still meets.
@@ -616,24 +646,19 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
     const int ntiles = s.t1 - s.t0;
     for (int k = 0; k < ntiles; ++k, ++i) {
       if (i % kGroups != grp) continue;  // another group's tile
-      const int slot = static_cast<int>(i % C::kStages), buf = grp;
-      ok = ok && warp_wait(&sready[buf], static_cast<uint32_t>(i / kGroups) & 1u, abort) &&
-           warp_wait(&full[slot], static_cast<uint32_t>(i / C::kStages) & 1u, abort);
+      const int slot = C::slot_of(i), buf = grp;
+      ok = ok && warp_wait(&sready[buf], static_cast<uint32_t>(i / kGroups) & 1u, abort);
       if (!ok) continue;
       tc_fence_after();
       float x[NH * kTerms];
       tmem_ld16(tq + static_cast<uint32_t>(buf * C::N), *reinterpret_cast<float(*)[16]>(x));
       if constexpr (NH == 8)
         tmem_ld16(tq + static_cast<uint32_t>(buf * C::N + 16), *reinterpret_cast<float(*)[16]>(x + 16));
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sempty[buf]);
-      if (C::kNv && i + kGroups < ntotal) {  // K scales of the group's next tile (its MMAs have completed)
-        const int64_t nx = i + kGroups;
-        const int ns = static_cast<int>(nx % C::kStages);
-        ok = warp_wait(&full[ns], static_cast<uint32_t>(nx / C::kStages) & 1u, abort);
-        if (ok) put_scales<PREC, NH>(ring + static_cast<size_t>(ns) * C::kStageBytes, tq, grp, qd, lane, sfready);
-        else continue;
+      if (i + kGroups < ntotal) {  // the group's next tile: its scores can now go to the same buffer
+        const int sx = seg_index_of(i + kGroups, u, sidx, ntiles, u0, u1, cum, a.B, Hkv);
+        ok = issue_tile<PREC, NH>(smem, tmem, tq, full, sready, qready, i + kGroups, sx, grp, qd, lane, abort);
+        last_issued = i + kGroups;
+        if (!ok) continue;
       }
 
       // scores of this lane's token, log2 units; masked past the sequence end
@@ -716,20 +741,21 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
     const bool complete = (s.t0 == 0) && (s.t1 == nb);
     const int slot_id = (u == u0) ? 0 : 1;
     float *part = a.partials + (static_cast<int64_t>(blockIdx.x) * 2 + slot_id) * kSlotFloats;
-    for (int hp = 0; hp < G; hp += 2) {  // head pairs (hp, hp + 1): held by lanes with 2c == hp
-      if (2 * c == hp) {
+    for (int hp = 0; hp < G; hp += C::kMH) {  // kMH heads per pass
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float *dst = mrg_o + (warp * 2 + e) * kD + 16 * r;
+      for (int e = 0; e < C::kMH; ++e) {
+        const int hd = hp + e;  // held by the lanes with c = hd / 2, accumulator column hd % 2
+        if (hd < G && (hd >> 1) == c) {
+          float *dst = mrg_o + (warp * C::kMH + e) * kD + 16 * r;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            dst[2 * j] = st.o[j][e];
-            dst[2 * j + 1] = st.o[j][2 + e];
+            dst[2 * j] = st.o[j][hd & 1];
+            dst[2 * j + 1] = st.o[j][2 + (hd & 1)];
           }
         }
       }
       named_bar_sync(1, kConsumerWarps * 32);
-      for (int e2 = tid; e2 < 2 * kD; e2 += kConsumerWarps * 32) {
+      for (int e2 = tid; e2 < C::kMH * kD; e2 += kConsumerWarps * 32) {
         const int e = e2 / kD, d = e2 % kD, hd = hp + e;
         if (hd < G) {
           float M = -INFINITY;
@@ -740,7 +766,7 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
           for (int w = 0; w < kConsumerWarps; ++w) {
             const float mw = mrg_ml[(w * kMaxGroup + hd) * 2];
             const float f = (mw == -INFINITY) ? 0.0f : ex2(mw - M);
-            o += f * mrg_o[(w * 2 + e) * kD + d];
+            o += f * mrg_o[(w * C::kMH + e) * kD + d];
             lsum += f * mrg_ml[(w * kMaxGroup + hd) * 2 + 1];
           }
           if (complete) {
@@ -756,6 +782,7 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
       }
       named_bar_sync(1, kConsumerWarps * 32);
     }
+    if (lane == 0) mbar_arrive(&qfree[qb]);  // every score of this segment was read: its image may be reused
     u += ntiles;
   }
 }
@@ -770,9 +797,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::oBars);
   uint64_t *empty = full + C::kStages;
   uint64_t *sready = empty + C::kStages;  // score buffer g holds a finished tile
-  uint64_t *sempty = sready + kGroups;    // score buffer g was read by the four warps of group g
-  uint64_t *sfready = sempty + kGroups;   // group g wrote the K scales of its next tile to TMEM
-  uint64_t *qready = sfready + kGroups;   // query image q (and its scale factors) ready
+  uint64_t *qready = sready + kGroups;    // query image q, its scale factors and score factors ready
+  uint64_t *qfree = qready + kQBufs;      // every consumer warp finished the segment of image q
   int32_t *cum = reinterpret_cast<int32_t *>(smem + C::oCum);
   int *flags = reinterpret_cast<int *>(smem + C::oFlags);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(flags);
@@ -793,13 +819,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     }
     for (int b = 0; b < kGroups; ++b) {
       mbar_init(&sready[b], 1);
-      mbar_init(&sempty[b], kGroupWarps);
-      mbar_init(&sfready[b], kGroupWarps);
     }
-    for (int q = 0; q < kQBufs; ++q) mbar_init(&qready[q], 1);
+    for (int q = 0; q < kQBufs; ++q) {
+      mbar_init(&qready[q], 2);  // TMEM copies done + image written
+      mbar_init(&qfree[q], kConsumerWarps);
+    }
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) tmem_alloc(tmem_holder, C::kTmemCols);
+  if (warp == kQueryWarp) tmem_alloc(tmem_holder, C::kTmemCols);
   if (warp == 0) {
     int carry = 0;
     if (lane == 0) cum[0] = 0;
@@ -850,14 +877,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     }
   }
 
-  int64_t issued = 0;  // tiles whose MMAs the MMA warp issued
-  if (warp == kProducerWarp) {
-    producer<PREC, NH>(a, smem + C::oRing, full, empty, cum, u0, u1, abort, fills);
-  } else if (warp == kMmaWarp) {
+  int64_t last_issued = -1;  // consumers: the last tile whose MMAs this thread issued; query warp: images
+  if (warp >= kProducerWarp && warp < kProducerWarp + kGroups) {
+    producer<PREC, NH>(a, smem + C::oRing, full, empty, cum, u0, u1, warp - kProducerWarp, abort, fills);
+  } else if (warp == kQueryWarp) {
     const float kscale = __fmul_rn(a.c.scale[0], a.sm_scale * 1.4426950408889634f);
-    mma_role<PREC, NH>(a, smem, tmem, full, sready, sempty, sfready, qready, cum, u0, u1, abort, kscale, issued);
+    last_issued = query_role<PREC, NH>(a, smem, tmem, qready, qfree, cum, u0, u1, abort, kscale);
   } else {
-    consumer_role<PREC, NH>(a, smem, tmem, full, empty, sready, sempty, sfready, qready, cum, u0, u1, abort);
+    consumer_role<PREC, NH>(a, smem, tmem, full, empty, sready, qready, qfree, cum, u0, u1, abort, last_issued);
   }
 
   // this CTA's partials are written: the combine grid may start launching
@@ -872,12 +899,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
       for (int s = 0; s < C::kStages; ++s)
         if (fills[s] > 0) mbar_wait_bounded(&full[s], static_cast<uint32_t>(fills[s] - 1) & 1u, &never);
     }
-    if (tid == kMmaWarp * 32) {
-      for (int64_t j = issued - kGroups; j < issued; ++j)
-        if (j >= 0) mbar_wait_bounded(&sready[j % kGroups], static_cast<uint32_t>(j / kGroups) & 1u, &never);
+    if (warp < kConsumerWarps && warp % kGroupWarps == 0 && lane == 0 && last_issued >= 0)  // MMA issuers
+      mbar_wait_bounded(&sready[warp / kGroupWarps], static_cast<uint32_t>(last_issued / kGroups) & 1u, &never);
+    if (tid == kQueryWarp * 32 && last_issued > 0) {  // the query warp's last image (its TMEM copies)
+      const int q = static_cast<int>((last_issued - 1) % kQBufs);
+      mbar_wait_bounded(&qready[q], static_cast<uint32_t>((last_issued - 1) / kQBufs) & 1u, &never);
     }
   }
-  if (warp == kMmaWarp) {
+  if (warp == kQueryWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);

@@ -44,6 +44,8 @@ CASES = {
     "gqa2": dict(B=2, Hq=8, Hkv=4, lens=(200, 33)),
     "splits7": dict(B=2, lens=(5000, 1300), num_splits=7),
     "splits64": dict(B=2, lens=(5000, 4096), num_splits=64),
+    # CTA shares that run through many one-tile (sequence, head) segments in a row
+    "short_segments": dict(B=9, lens=(2000, 64, 1, 100, 64, 128, 5, 64, 700), num_splits=1),
     "lognormal_channels": dict(B=3, lens=(600, 333, 64), dist="lognormal_channels", channel_sigma=0.5),
 }
 
