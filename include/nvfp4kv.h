@@ -156,8 +156,10 @@ nvkv_status nvkv_decode_workspace_init(void *workspace, size_t bytes, void *stre
  *   layer_precision must equal cache->prec (else NVKV_ERR_INVALID_ARG)
  *   sm_scale        softmax scale; 0 -> 1/sqrt(head_dim)
  *   num_splits      0: balance the work over the GPU (split-KV wherever it
- *                   helps); > 0: cut every sequence into that many partitions
- *                   (exactly so when all sequences have equal length)
+ *                   helps); > 0: cut every sequence into at most that many
+ *                   partitions (exactly so when all sequences have equal
+ *                   length and batch * num_kv_heads * num_splits CTAs fit on
+ *                   the device at once; a larger request is capped there)
  *   workspace       scratch of nvkv_decode_workspace_size(...) bytes, device
  *   out             [batch][num_q_heads][head_dim] BF16, device
  * Query head h reads KV head h / (num_q_heads / num_kv_heads); every token in
@@ -186,8 +188,10 @@ nvkv_status fp8_paged_decode_attention(const void *q, const nvkv_cache *cache, c
  * pointers.  Same arguments and result as nvfp4_paged_decode_attention without
  * workspace/workspace_bytes; the split-KV scratch lives in a fixed array of
  * NVKV_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the
- * library keeps until the process exits.  A problem whose scratch (see
- * nvkv_decode_workspace_size) exceeds that size is rejected with
+ * library keeps until the process exits.  The scratch a call needs is the
+ * schedule ((batch + 2) int32) plus two 4160-byte partial slots per CTA, and
+ * the CTA count never exceeds one resident wave (152 on a GB300), so every
+ * supported problem fits; a device that would need more is refused with
  * NVKV_ERR_WORKSPACE_TOO_SMALL before any launch.  The first call on a device
  * looks up the array's device address (set-up, once per device, with that
  * device current); make that first call before any stream capture.  Each call

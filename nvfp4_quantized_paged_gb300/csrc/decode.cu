@@ -200,28 +200,29 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
   const int Hkv = a.c.Hkv, P = a.c.P;
   const uint64_t policy = policy_evict_first();
   const uint32_t block_bytes = static_cast<uint32_t>(P) * C::P::kTokBytes;
-  int64_t i = 0;  // CTA-local tile index
+  int slot_l = 0;     // ring position of the group's next tile
+  uint32_t fill = 0;  // fills of that slot so far
+  int ibase = 0;      // CTA-local index of the segment's first tile
   for (int64_t u = u0; u < u1;) {
     const Seg s = seg_at(u, u1, cum, a.B, Hkv);
     const int ntiles = s.t1 - s.t0;
-    const int64_t ifirst = i + ((grp - i % kGroups) + kGroups) % kGroups;  // this group's first tile here
-    if (ifirst < i + ntiles) {
+    const int kfirst = (grp - ibase % kGroups + kGroups) % kGroups;  // this group's first tile here
+    if (kfirst < ntiles) {
       const int len = clamped_len(a, s.b);
       const int32_t *brow = a.block_table + static_cast<int64_t>(s.b) * a.max_pages;
+      const uint8_t *src_h = a.c.data + a.c.block(0, s.h, C::P::kTokBytes);  // page 0 of head h
+      const int64_t page_stride = a.c.block(1, 0, C::P::kTokBytes) - a.c.block(0, 0, C::P::kTokBytes);
       // Block-table window: lane l holds the entry of page index wbase + l; the
       // next window is requested when the current one comes into use.  Window
       // edges fall on tile edges (32 pages hold whole tiles at P = 16, 32, 64).
-      int wbase = ((s.t0 + static_cast<int>(ifirst - i)) * kTile) / P;
+      int wbase = ((s.t0 + kfirst) * kTile) / P;
       int32_t pg = wbase + lane < a.max_pages ? brow[wbase + lane] : 0;
       int32_t pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
-      for (int64_t x = ifirst; x < i + ntiles; x += kGroups) {
-        const int t = s.t0 + static_cast<int>(x - i);
-        const int slot = C::slot_of(x);
-        const uint32_t fill = C::fill_of(x);
-        if (__any_sync(0xffffffffu, *abort)) return;
+      for (int k = kfirst; k < ntiles; k += kGroups) {
+        const int slot = grp * C::kStagesG + slot_l;
         if (lane == 0 && fill > 0) mbar_wait_bounded(&empty[slot], (fill - 1) & 1u, abort);
         if (__any_sync(0xffffffffu, *abort)) return;  // warp-uniform exit
-        const int tok0 = t * kTile;
+        const int tok0 = (s.t0 + k) * kTile;
         const int ntok = min(kTile, len - tok0);
         const int nblk = (ntok + P - 1) / P;  // page blocks holding the tile's tokens
         while ((tok0 + ntok - 1) / P >= wbase + 32) {  // the tile leaves the window (warp-uniform)
@@ -230,21 +231,24 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
           pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
         }
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nblk) * block_bytes);
-        const int pidx = lane < nblk ? tok0 / P + lane - wbase : 0;
-        const int64_t page_w = __shfl_sync(0xffffffffu, pg, pidx & 31);
+        const int page = __shfl_sync(0xffffffffu, pg, (tok0 / P + lane - wbase) & 31);
         if (lane < nblk) {
-          int64_t page = page_w;
+          int64_t pgc = page;
           if (page < 0 || page >= a.c.num_pages) {
             set_err(a.c.err, NVKV_DEVERR_PAGE);
-            page = 0;  // a valid address; the output of this sequence is then undefined
+            pgc = 0;  // a valid address; the output of this sequence is then undefined
           }
-          bulk_g2s(ring + static_cast<size_t>(slot) * C::kStageBytes + static_cast<size_t>(lane) * block_bytes,
-                   a.c.data + a.c.block(page, s.h, C::P::kTokBytes), block_bytes, &full[slot], policy);
+          bulk_g2s(ring + slot * C::kStageBytes + lane * block_bytes, src_h + pgc * page_stride, block_bytes,
+                   &full[slot], policy);
         }
         if (lane == 0) fills[slot] = static_cast<int>(fill) + 1;
+        if (++slot_l == C::kStagesG) {
+          slot_l = 0;
+          ++fill;
+        }
       }
     }
-    i += ntiles;
+    ibase += ntiles;
     u += ntiles;
   }
 }
@@ -538,22 +542,23 @@ __device__ __forceinline__ int seg_index_of(int64_t x, int64_t u, int sidx, int 
   return sidx;
 }
 
-// Score MMAs of CTA-local tile x (segment sx) for consumer group grp: each of
-// the group's warps waits for the tile's stage and (NVFP4) writes the K block
-// scales of its 32 rows into the group's TMEM scale-factor columns (row
-// m = 32 qd + lane is read by the MMA from lane m, column sfa_col(grp, mma) +
-// qd); the four warps meet on the group's named barrier; one thread waits for
-// the segment's query image and issues the MMAs into the group's score buffer,
-// committing them to sready[grp].  The caller has read the group's previous
-// scores, so the buffer and the scale columns are free.
+// Score MMAs of one tile for consumer group grp: its stage is ring slot
+// `slot` (fill parity fpar), its query image qb (parity qpar).  Each of the
+// group's warps waits for the stage and (NVFP4) writes the K block scales of
+// its 32 rows into the group's TMEM scale-factor columns (row m = 32 qd + lane
+// is read by the MMA from lane m, column sfa_col(grp, mma) + qd); the four
+// warps meet on the group's named barrier; one thread waits for the query
+// image and issues the MMAs into the group's score buffer, committing them to
+// sready[grp].  The caller has read the group's previous scores, so the buffer
+// and the scale columns are free.  True (warp-uniform) when the MMAs went out
+// (for the issuing warp) or the stage landed (for the others).
 template <int PREC, int NH>
 __device__ __forceinline__ bool issue_tile(uint8_t *smem, uint32_t tmem, uint32_t tq, uint64_t *full, uint64_t *sready,
-                                           uint64_t *qready, int64_t x, int sx, int grp, int qd, int lane,
-                                           volatile int *abort) {
+                                           uint64_t *qready, int slot, uint32_t fpar, int qb, uint32_t qpar, int grp,
+                                           int qd, int lane, volatile int *abort) {
   using C = Cfg<PREC, NH>;
-  const int slot = C::slot_of(x);
-  const uint8_t *stage = smem + C::oRing + static_cast<size_t>(slot) * C::kStageBytes;
-  bool ok = warp_wait(&full[slot], C::fill_of(x) & 1u, abort);
+  const uint8_t *stage = smem + C::oRing + slot * C::kStageBytes;
+  bool ok = warp_wait(&full[slot], fpar, abort);
   if constexpr (C::kNv) {
     if (ok) {
       const int t = 32 * qd + lane;
@@ -566,8 +571,7 @@ __device__ __forceinline__ bool issue_tile(uint8_t *smem, uint32_t tmem, uint32_
   tc_fence_before();
   named_bar_sync(2 + grp, kGroupWarps * 32);
   if (qd == 0) {
-    const int qb = sx % kQBufs;
-    ok = ok && warp_wait(&qready[qb], static_cast<uint32_t>(sx / kQBufs) & 1u, abort);
+    ok = ok && warp_wait(&qready[qb], qpar, abort);
     if (ok && lane == 0) {
       tc_fence_after();
       const uint32_t d = tmem + static_cast<uint32_t>(grp * C::N);
@@ -614,17 +618,25 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
   float *mrg_ml = reinterpret_cast<float *>(smem + C::oMrgMl);
   const float vscale = a.c.scale[1];
   const uint32_t tq = tmem + (static_cast<uint32_t>(32 * qd) << 16);  // this warp's lane quadrant
-  int64_t i = 0;
+  // The group's tiles are i = grp, grp + 3, ... (CTA-local); its n-th tile
+  // uses ring slot kStagesG * grp + n % kStagesG with fill parity
+  // (n / kStagesG) & 1, and score buffer phase n & 1.  Counters advance
+  // per tile instead of being divided out.
+  const int ntotal = static_cast<int>(u1 - u0);  // tiles of the share
+  int slot_l = 0;          // ring position of the group's current tile
+  uint32_t fpar = 0;       // its fill parity
+  uint32_t spar = 0;       // score buffer phase of the current tile
+  int ibase = 0;           // CTA-local index of the segment's first tile
   int sidx = 0;
   bool ok = true;
-  const int64_t ntotal = u1 - u0;  // tiles of the share
   last_issued = -1;
   // The group's first tile is issued before anything else.
   if (grp < ntotal) {
     const Seg s0 = seg_at(u0, u1, cum, a.B, Hkv);
     const int sx = seg_index_of(grp, u0, 0, s0.t1 - s0.t0, u0, u1, cum, a.B, Hkv);
-    ok = issue_tile<PREC, NH>(smem, tmem, tq, full, sready, qready, grp, sx, grp, qd, lane, abort);
-    last_issued = grp;
+    ok = issue_tile<PREC, NH>(smem, tmem, tq, full, sready, qready, grp * C::kStagesG, 0u, sx % kQBufs,
+                              static_cast<uint32_t>(sx / kQBufs) & 1u, grp, qd, lane, abort);
+    if (ok) last_issued = grp;
   }
   // After a timeout (ok false) the warps skip all work but keep walking the
   // same segments, so every named barrier of the merge still meets.
@@ -644,21 +656,51 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
 #pragma unroll
     for (int j = 0; j < 8; ++j) st.o[j][0] = st.o[j][1] = st.o[j][2] = st.o[j][3] = 0.0f;
     const int ntiles = s.t1 - s.t0;
-    for (int k = 0; k < ntiles; ++k, ++i) {
-      if (i % kGroups != grp) continue;  // another group's tile
-      const int slot = C::slot_of(i), buf = grp;
-      ok = ok && warp_wait(&sready[buf], static_cast<uint32_t>(i / kGroups) & 1u, abort);
-      if (!ok) continue;
-      tc_fence_after();
+    for (int k = (grp - ibase % kGroups + kGroups) % kGroups; k < ntiles; k += kGroups) {
+      const int i = ibase + k;
+      const int slot = grp * C::kStagesG + slot_l;
+      const int nslot_l = slot_l + 1 == C::kStagesG ? 0 : slot_l + 1;  // the group's next tile
+      const uint32_t nfpar = nslot_l == 0 ? fpar ^ 1u : fpar;
+      ok = ok && warp_wait(&sready[grp], spar, abort);
       float x[NH * kTerms];
-      tmem_ld16(tq + static_cast<uint32_t>(buf * C::N), *reinterpret_cast<float(*)[16]>(x));
-      if constexpr (NH == 8)
-        tmem_ld16(tq + static_cast<uint32_t>(buf * C::N + 16), *reinterpret_cast<float(*)[16]>(x + 16));
-      if (i + kGroups < ntotal) {  // the group's next tile: its scores can now go to the same buffer
-        const int sx = seg_index_of(i + kGroups, u, sidx, ntiles, u0, u1, cum, a.B, Hkv);
-        ok = issue_tile<PREC, NH>(smem, tmem, tq, full, sready, qready, i + kGroups, sx, grp, qd, lane, abort);
-        last_issued = i + kGroups;
-        if (!ok) continue;
+      if (ok) {
+        tc_fence_after();
+        tmem_ld16(tq + static_cast<uint32_t>(grp * C::N), *reinterpret_cast<float(*)[16]>(x));
+        if constexpr (NH == 8)
+          tmem_ld16(tq + static_cast<uint32_t>(grp * C::N + 16), *reinterpret_cast<float(*)[16]>(x + 16));
+      }
+      // The group's next tile may now score into the same buffer.  Its MMAs
+      // go out now if its stage has landed for all four warps, else after
+      // this tile's P.V, so the group never waits for data it does not need
+      // yet.  (Every warp of the group takes the same barriers whatever ok is.)
+      const bool has_next = i + kGroups < ntotal;
+      int nqb = qb;
+      uint32_t nqpar = static_cast<uint32_t>(sidx / kQBufs) & 1u;
+      bool issued = false;
+      if (has_next) {
+        if (k + kGroups >= ntiles) {  // the next tile lies in a later segment
+          const int sx = seg_index_of(i + kGroups, u, sidx, ntiles, u0, u1, cum, a.B, Hkv);
+          nqb = sx % kQBufs;
+          nqpar = static_cast<uint32_t>(sx / kQBufs) & 1u;
+        }
+        const bool landed = ok && mbar_test(&full[grp * C::kStagesG + nslot_l], nfpar);
+        if (named_bar_and(2 + grp, kGroupWarps * 32, landed)) {
+          ok = issue_tile<PREC, NH>(smem, tmem, tq, full, sready, qready, grp * C::kStagesG + nslot_l, nfpar, nqb,
+                                    nqpar, grp, qd, lane, abort);
+          if (ok) last_issued = i + kGroups;  // its MMAs went out
+          issued = true;
+        }
+      }
+      slot_l = nslot_l;
+      fpar = nfpar;
+      spar ^= 1u;
+      if (!ok) {
+        if (has_next && !issued) {
+          if (issue_tile<PREC, NH>(smem, tmem, tq, full, sready, qready, grp * C::kStagesG + nslot_l, nfpar, nqb,
+                                   nqpar, grp, qd, lane, abort))
+            last_issued = i + kGroups;
+        }
+        continue;
       }
 
       // scores of this lane's token, log2 units; masked past the sequence end
@@ -703,7 +745,7 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
       __syncwarp();
 
       // P.V over the warp's two 16-token slices, their MMA chains interleaved
-      const uint8_t *stage = ring + static_cast<size_t>(slot) * C::kStageBytes;
+      const uint8_t *stage = ring + slot * C::kStageBytes;
       const int rem = Lb - (t * kTile + 32 * qd);  // warp-uniform
       if (rem > 0) {
         uint32_t b[4] = {0u, 0u, 0u, 0u};
@@ -723,7 +765,13 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
+      if (has_next && !issued) {
+        ok = issue_tile<PREC, NH>(smem, tmem, tq, full, sready, qready, grp * C::kStagesG + slot_l, fpar, nqb, nqpar,
+                                  grp, qd, lane, abort);
+        if (ok) last_issued = i + kGroups;  // its MMAs went out
+      }
     }
+    ibase += ntiles;
 
     // ---- merge the four warps: (m, l) per head, O per (head, d) ----
 #pragma unroll
@@ -1039,17 +1087,19 @@ const DevInfo *dev_info() {
   return g_info[dev].sms > 0 ? &g_info[dev] : nullptr;
 }
 
-// CTAs of the persistent grid.  num_splits > 0: batch * Hkv * num_splits, so
-// equal-length sequences are cut into exactly num_splits shares each.
+// CTAs of the persistent grid, one share each: as many as are resident at
+// once on the device, and with num_splits > 0 at most batch * Hkv *
+// num_splits (equal-length sequences are then cut into exactly num_splits
+// shares each while that fits in one wave; more shares than resident CTAs
+// would only add waves of set-up and merging, so the request is capped there).
 int64_t num_ctas_for(int prec, int32_t batch, int32_t Hkv, int32_t G, int64_t max_units, int32_t num_splits) {
-  int64_t n;
+  const DevInfo *d = dev_info();
+  if (!d) return -1;
+  const int o = d->occ[prec][G > 4 ? 1 : 0];
+  int64_t n = static_cast<int64_t>(d->sms) * (o > 0 ? o : 1);
   if (num_splits > 0) {
-    n = static_cast<int64_t>(batch) * Hkv * num_splits;
-  } else {
-    const DevInfo *d = dev_info();
-    if (!d) return -1;
-    const int o = d->occ[prec][G > 4 ? 1 : 0];
-    n = static_cast<int64_t>(d->sms) * (o > 0 ? o : 1);
+    const int64_t want = static_cast<int64_t>(batch) * Hkv * num_splits;
+    if (want < n) n = want;
   }
   if (n > max_units) n = max_units;
   return n < 1 ? 1 : n;

@@ -175,15 +175,30 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// try_wait that suspends the thread in hardware until the phase completes or
+// about `hint_ns` nanoseconds pass, so a waiting warp takes no issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: true once the phase with `parity` completed; false if *abort
-// became nonzero or the wait exceeded ~2 s (then *abort is raised).
+// became nonzero or the wait exceeded ~2 s (then *abort is raised).  Each
+// try suspends the warp for up to 20 us.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort) return false;
-    if ((it & 255u) == 0 && global_timer_ns() - t0 > 2000000000ull) {
+    if (global_timer_ns() - t0 > 2000000000ull) {
       *abort = 1;
       return false;
     }
@@ -209,6 +224,33 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ANDs a predicate over its nthreads threads.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q; }"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// Non-blocking test: true if the phase with `parity` has completed.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p; }"
+      : "=r"(r)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ void set_err(int32_t *err, int32_t code) {
