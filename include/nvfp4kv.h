@@ -137,9 +137,9 @@ nvkv_status fp8_kv_quantize_write(const void *k, const void *v, nvkv_dtype dtype
 
 /* Bytes of decode workspace for this problem size: num_splits > 0 as passed to
  * the decode call, 0 for the library's choice on the current device.  The
- * workspace holds the split-KV schedule and partial results; every decode call
- * writes all of it that it later reads, so it needs no initialisation.
- * Returns 0 for unsupported sizes. */
+ * workspace holds one merge record per (sequence, KV head) and the split-KV
+ * partial results; every decode call writes all of it that it later reads,
+ * so it needs no initialisation.  Returns 0 for unsupported sizes. */
 size_t nvkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                   int32_t num_splits);
 
@@ -188,8 +188,9 @@ nvkv_status fp8_paged_decode_attention(const void *q, const nvkv_cache *cache, c
  * pointers.  Same arguments and result as nvfp4_paged_decode_attention without
  * workspace/workspace_bytes; the split-KV scratch lives in a fixed array of
  * NVKV_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the
- * library keeps until the process exits.  The scratch a call needs is the
- * schedule ((batch + 2) int32) plus two 4160-byte partial slots per CTA, and
+ * library keeps until the process exits.  The scratch a call needs is an
+ * 8-byte merge record per (sequence, KV head) plus two 4160-byte partial
+ * slots per CTA, and
  * the CTA count never exceeds one resident wave (152 on a GB300), so every
  * supported problem fits; a device that would need more is refused with
  * NVKV_ERR_WORKSPACE_TOO_SMALL before any launch.  The first call on a device

@@ -137,7 +137,7 @@ struct DecodeArgs {
   int32_t B, Hq, G;
   float sm_scale;
   int32_t num_ctas;
-  int32_t *meta;      // written by CTA 0: cum[0..B] (tiles before each sequence), then NC
+  int2 *unit_info;    // [B][Hkv] per call: {partial slot of the first contributor, contributors}
   float *partials;    // [num_ctas][2][kSlotFloats]
   __nv_bfloat16 *out;
 };
@@ -605,7 +605,7 @@ __device__ __forceinline__ float pick(const float (&v)[NH], int i) {  // v[i] fo
 template <int PREC, int NH>
 __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uint64_t *full, uint64_t *empty,
                               uint64_t *sready, uint64_t *qready, uint64_t *qfree, const int32_t *cum, int64_t u0,
-                              int64_t u1, volatile int *abort, int64_t &last_issued) {
+                              int64_t u1, int64_t W, int64_t NC, volatile int *abort, int64_t &last_issued) {
   using C = Cfg<PREC, NH>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = warp / kGroupWarps, qd = warp % kGroupWarps;  // consumer group, TMEM lane quadrant
@@ -788,6 +788,19 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
     const int nb = cum[s.b + 1] - cum[s.b];
     const bool complete = (s.t0 == 0) && (s.t1 == nb);
     const int slot_id = (u == u0) ? 0 : 1;
+    if (tid == 0 && (complete || s.t0 == 0)) {
+      // The CTA holding the first tile of (b, h) tells the merge kernel where
+      // the parts are: contributor k > 0 of the unit left its part in slot 0
+      // of CTA c_first + k (the unit opens its share), contributor 0 in this
+      // CTA's slot slot_id.
+      int2 info = make_int2(0, 1);
+      if (!complete) {
+        const int64_t ubh0 = static_cast<int64_t>(cum[s.b]) * Hkv + static_cast<int64_t>(s.h) * nb;
+        info.x = static_cast<int>(blockIdx.x) * 2 + slot_id;
+        info.y = static_cast<int>(owner_of(ubh0 + nb - 1, W, NC) - blockIdx.x + 1);
+      }
+      a.unit_info[s.b * Hkv + s.h] = info;
+    }
     float *part = a.partials + (static_cast<int64_t>(blockIdx.x) * 2 + slot_id) * kSlotFloats;
     for (int hp = 0; hp < G; hp += C::kMH) {  // kMH heads per pass
 #pragma unroll
@@ -912,16 +925,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
   const int64_t u0 = active ? share_begin(blockIdx.x, W, NC) : 0;
   const int64_t u1 = active ? share_begin(blockIdx.x + 1, W, NC) : 0;
 
-  // the combine kernel needs the same schedule: CTA 0 publishes it
-  if (blockIdx.x == 0) {
-    for (int b = tid; b <= B; b += kThreads) a.meta[b] = cum[b];
-    if (tid == 0) a.meta[B + 1] = static_cast<int32_t>(NC);
-  }
   // zero rows of empty sequences (spread over CTAs)
   for (int b = blockIdx.x; b < B; b += a.num_ctas) {
     if (cum[b + 1] == cum[b]) {
       uint4 *o = reinterpret_cast<uint4 *>(a.out + static_cast<int64_t>(b) * a.Hq * kD);
       for (int i = tid; i < a.Hq * kD / 8; i += kThreads) o[i] = make_uint4(0, 0, 0, 0);
+      if (tid < Hkv) a.unit_info[b * Hkv + tid] = make_int2(0, 0);  // nothing to merge
     }
   }
 
@@ -932,7 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     const float kscale = __fmul_rn(a.c.scale[0], a.sm_scale * 1.4426950408889634f);
     last_issued = query_role<PREC, NH>(a, smem, tmem, qready, qfree, cum, u0, u1, abort, kscale);
   } else {
-    consumer_role<PREC, NH>(a, smem, tmem, full, empty, sready, qready, qfree, cum, u0, u1, abort, last_issued);
+    consumer_role<PREC, NH>(a, smem, tmem, full, empty, sready, qready, qfree, cum, u0, u1, W, NC, abort, last_issued);
   }
 
   // this CTA's partials are written: the combine grid may start launching
@@ -967,14 +976,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
 // (programmatic dependent launch: griddepcontrol.wait returns once the decode
 // grid has completed and its writes are visible).  Contributor k of a
 // (sequence, KV head) left (o_k, m_k, l_k) in log2 units; out = sum_k
-// 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k * g_V, M = max_k m_k.  (Sequence,
-// head) pairs that one CTA covered entirely were written by the decode grid.
+// 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k * g_V, M = max_k m_k.  The decode
+// grid left, per (sequence, KV head), where the parts are and how many; pairs
+// with one contributor (or none) were written by the decode grid itself.
 // ---------------------------------------------------------------------------
 struct CombineArgs {
-  const int32_t *meta;
+  const int2 *unit_info;
   const float *partials;
   const float *scale;
-  int32_t B, Hkv, Hq, G;
+  int32_t Hq, G;
   __nv_bfloat16 *out;
 };
 
@@ -983,27 +993,23 @@ constexpr int kCombineBatch = 16;  // contributors whose loads are in flight tog
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
   const int tid = threadIdx.x;
-  const int hd = blockIdx.x % a.G, bh = blockIdx.x / a.G, h = bh % a.Hkv, b = bh / a.Hkv;
+  const int hd = blockIdx.x % a.G, bh = blockIdx.x / a.G;
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int32_t c0 = a.meta[b], c1 = a.meta[b + 1];
-  const int nb = c1 - c0;
-  if (nb == 0) return;
-  const int64_t W = static_cast<int64_t>(a.meta[a.B]) * a.Hkv, NC = a.meta[a.B + 1];
-  const int64_t ubh0 = static_cast<int64_t>(c0) * a.Hkv + static_cast<int64_t>(h) * nb;
-  const int64_t c_first = owner_of(ubh0, W, NC);
-  const int n = static_cast<int>(owner_of(ubh0 + nb - 1, W, NC) - c_first + 1);
-  if (n == 1) return;  // written directly by the decode grid
+  const int2 info = a.unit_info[bh];
+  const int n = info.y;
+  if (n <= 1) return;  // written directly by the decode grid
   // Every thread (one head_dim element) loads the statistics and its element
   // of a batch of contributors at once and folds them into a running
   // (max, sum, acc) triple: one round trip per batch, no block reductions.
+  const int first_slot = info.x, next_slot = (info.x / 2 + 1) * 2;  // contributor k > 0: slot next_slot + 2 (k - 1)
   float M = -INFINITY, L = 0.0f, acc = 0.0f;
   for (int k0 = 0; k0 < n; k0 += kCombineBatch) {
     float m[kCombineBatch], l[kCombineBatch], o[kCombineBatch];
 #pragma unroll
     for (int q = 0; q < kCombineBatch; ++q) {
-      if (k0 + q < n) {
-        const int64_t cc = c_first + k0 + q;
-        const float *st = a.partials + (cc * 2 + (share_begin(cc, W, NC) >= ubh0 ? 0 : 1)) * kSlotFloats;
+      const int k = k0 + q;
+      if (k < n) {
+        const float *st = a.partials + static_cast<int64_t>(k == 0 ? first_slot : next_slot + 2 * (k - 1)) * kSlotFloats;
         m[q] = st[kMaxGroup * kD + hd];
         l[q] = st[kMaxGroup * kD + kMaxGroup + hd];
         o[q] = st[hd * kD + tid];
@@ -1027,7 +1033,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineA
     }
     M = mb;
   }
-  a.out[(static_cast<int64_t>(b) * a.Hq + h * a.G + hd) * kD + tid] = __float2bfloat16_rn(acc * (a.scale[1] / L));
+  a.out[(static_cast<int64_t>(bh) * a.G + hd) * kD + tid] = __float2bfloat16_rn(acc * (a.scale[1] / L));
 }
 
 // ---------------------------------------------------------------------------
@@ -1094,22 +1100,28 @@ const DevInfo *dev_info() {
 // would only add waves of set-up and merging, so the request is capped there).
 int64_t num_ctas_for(int prec, int32_t batch, int32_t Hkv, int32_t G, int64_t max_units, int32_t num_splits) {
   const DevInfo *d = dev_info();
-  if (!d) return -1;
-  const int o = d->occ[prec][G > 4 ? 1 : 0];
-  int64_t n = static_cast<int64_t>(d->sms) * (o > 0 ? o : 1);
+  int64_t n;
   if (num_splits > 0) {
-    const int64_t want = static_cast<int64_t>(batch) * Hkv * num_splits;
-    if (want < n) n = want;
+    n = static_cast<int64_t>(batch) * Hkv * num_splits;
+    if (d) {
+      const int o = d->occ[prec][G > 4 ? 1 : 0];
+      const int64_t wave = static_cast<int64_t>(d->sms) * (o > 0 ? o : 1);
+      if (wave < n) n = wave;
+    }
+  } else {
+    if (!d) return -1;
+    const int o = d->occ[prec][G > 4 ? 1 : 0];
+    n = static_cast<int64_t>(d->sms) * (o > 0 ? o : 1);
   }
   if (n > max_units) n = max_units;
   return n < 1 ? 1 : n;
 }
 
-// Workspace = schedule (cum[0..B], NC) + two partial slots per CTA.
-size_t meta_bytes(int32_t batch) { return (static_cast<size_t>(batch + 2) * 4 + 255) / 256 * 256; }
+// Workspace = per-(sequence, KV head) merge records + two partial slots per CTA.
+size_t info_bytes(int32_t batch, int32_t Hkv) { return (static_cast<size_t>(batch) * Hkv * 8 + 255) / 256 * 256; }
 
-size_t workspace_bytes_for(int32_t batch, int64_t nctas) {
-  return meta_bytes(batch) + static_cast<size_t>(nctas) * 2 * kSlotFloats * sizeof(float);
+size_t workspace_bytes_for(int32_t batch, int32_t Hkv, int64_t nctas) {
+  return info_bytes(batch, Hkv) + static_cast<size_t>(nctas) * 2 * kSlotFloats * sizeof(float);
 }
 
 template <int PREC, int NH>
@@ -1137,7 +1149,7 @@ nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t 
   const int64_t nctas = num_ctas_for(prec, batch, Hkv, G, max_units, num_splits);
   if (nctas < 0) return NVKV_ERR_CUDA;
   if (nctas > 0x7fffffff) return NVKV_ERR_UNSUPPORTED;
-  if (workspace_bytes < workspace_bytes_for(batch, nctas)) return NVKV_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < workspace_bytes_for(batch, Hkv, nctas)) return NVKV_ERR_WORKSPACE_TOO_SMALL;
   if (!dev_info()) return NVKV_ERR_CUDA;
 
   DecodeArgs a;
@@ -1151,8 +1163,8 @@ nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t 
   a.G = G;
   a.sm_scale = sm_scale > 0.0f ? sm_scale : 1.0f / sqrtf(static_cast<float>(cache->head_dim));
   a.num_ctas = static_cast<int32_t>(nctas);
-  a.meta = static_cast<int32_t *>(workspace);
-  a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + meta_bytes(batch));
+  a.unit_info = static_cast<int2 *>(workspace);
+  a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + info_bytes(batch, Hkv));
   a.out = static_cast<__nv_bfloat16 *>(out);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (prec == NVKV_PREC_NVFP4) {
@@ -1166,11 +1178,9 @@ nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t 
   if (st != NVKV_OK) return st;
   // split-KV merge, launched as a programmatic dependent of the decode grid
   CombineArgs ca;
-  ca.meta = a.meta;
+  ca.unit_info = a.unit_info;
   ca.partials = a.partials;
   ca.scale = a.c.scale;
-  ca.B = batch;
-  ca.Hkv = Hkv;
   ca.Hq = num_q_heads;
   ca.G = G;
   ca.out = a.out;
@@ -1265,7 +1275,7 @@ size_t nvkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t nu
     for (int p = 0; p < 2; ++p) occ = d->occ[p][G > 4 ? 1 : 0] > occ ? d->occ[p][G > 4 ? 1 : 0] : occ;
     nctas = static_cast<int64_t>(d->sms) * occ;
   }
-  return workspace_bytes_for(batch, nctas);
+  return workspace_bytes_for(batch, num_kv_heads, nctas);
 }
 
 nvkv_status nvkv_decode_workspace_init(void *workspace, size_t bytes, void *stream) {

@@ -69,9 +69,11 @@ def test_decode_argument_checks(nv):
 
 
 def test_workspace_size_arithmetic(nv):
-    # explicit splits need no device: schedule (B + 2 ints, rounded to 256 B) + 2 partial slots per CTA
+    # explicit splits need no device: one 8-byte merge record per (sequence, KV
+    # head), rounded up to 256 B, then 2 partial slots per CTA
     slot = (8 * 128 + 16) * 4
-    assert nv.nvkv_decode_workspace_size(16, 32, 8, 128, 4) == 256 + 16 * 8 * 4 * 2 * slot
+    assert nv.nvkv_decode_workspace_size(16, 32, 8, 128, 4) == 1024 + 16 * 8 * 4 * 2 * slot
+    assert nv.nvkv_decode_workspace_size(3, 16, 2, 128, 1) == 256 + 3 * 2 * 1 * 2 * slot
     assert nv.nvkv_decode_workspace_size(16, 32, 8, 64, 4) == 0
     assert nv.nvkv_decode_workspace_size(16, 32, 2, 128, 4) == 0  # group of 16
 
