@@ -543,8 +543,8 @@ __device__ __forceinline__ int seg_index_of(int64_t x, int64_t u, int sidx, int 
 }
 
 // Score MMAs of one tile for consumer group grp: its stage is ring slot
-// `slot` (fill parity fpar), its query image qb (parity qpar).  Each of the
-// group's warps waits for the stage and (NVFP4) writes the K block scales of
+// `slot` (fill parity fpar), its query image qb (parity qpar).  Once the
+// stage has landed each of the group's warps (NVFP4) writes the K block scales of
 // its 32 rows into the group's TMEM scale-factor columns (row m = 32 qd + lane
 // is read by the MMA from lane m, column sfa_col(grp, mma) + qd); the four
 // warps meet on the group's named barrier; one thread waits for the query
@@ -558,7 +558,11 @@ __device__ __forceinline__ bool issue_tile(uint8_t *smem, uint32_t tmem, uint32_
                                            int qd, int lane, volatile int *abort) {
   using C = Cfg<PREC, NH>;
   const uint8_t *stage = smem + C::oRing + slot * C::kStageBytes;
-  bool ok = warp_wait(&full[slot], fpar, abort);
+  // One warp waits for the stage (sleeping between tries); the other three
+  // wait at the group barrier, which takes no issue slots.
+  bool ok = true;
+  if (qd == 0) ok = warp_wait(&full[slot], fpar, abort);
+  ok = named_bar_and(2 + grp, kGroupWarps * 32, ok);
   if constexpr (C::kNv) {
     if (ok) {
       const int t = 32 * qd + lane;

@@ -190,11 +190,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 }
 
 // Bounded wait: true once the phase with `parity` completed; false if *abort
-// became nonzero or the wait exceeded ~2 s (then *abort is raised).  Each
-// try suspends the warp for up to 20 us.
+// became nonzero or the wait exceeded ~2 s (then *abort is raised).  Between
+// tries the warp sleeps (32 ns, doubling up to 256 ns), so a long wait costs
+// few issue slots; the sleep bounds the added wake-up latency.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
+  uint32_t ns = 32;
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort) return false;
@@ -202,6 +204,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
       *abort = 1;
       return false;
     }
+    __nanosleep(ns);
+    if (ns < 256) ns <<= 1;
   }
 }
 
