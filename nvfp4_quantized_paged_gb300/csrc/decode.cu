@@ -11,9 +11,10 @@
 //     streams the same number of bytes whatever the sequence lengths.  A
 //     (sequence, KV head) cut between CTAs leaves split-KV partials that a
 //     second kernel merges with the log-sum-exp rule.
-//   * Warp roles: a producer warp streams tiles into a shared-memory ring with
-//     1-D bulk copies (one per page block, mbarrier transaction counts); a
-//     query warp prepares each segment's query operand; twelve consumer warps
+//   * Warp roles: a producer warp per consumer group streams the group's tiles
+//     into its shared-memory ring with 1-D bulk copies (one per page block,
+//     mbarrier transaction counts); a query warp prepares each segment's query
+//     operand; twelve consumer warps
 //     in three groups of four (one warp per TMEM lane quadrant, 32 tokens each)
 //     take the tiles round-robin: a group issues the score MMAs of its next
 //     tile as soon as it has read the scores of its current one, then runs the
@@ -23,11 +24,12 @@
 //     tokens, K = 64 per instruction) and the E4M3 block scales of K are its
 //     scale factors, so K is never dequantized by a thread.  The BF16 query
 //     enters as the B operand in the same format: each query head is written
-//     as a sum of four NVFP4 terms (E2M1 codes, one E4M3 scale per 16 values),
-//     stacked along N, and the score is the sum of the four columns.  The FP8
-//     variant does the same with kind::f8f6f4 and four E4M3 terms.  Scores land
-//     in TMEM (double-buffered) and are read with tcgen05.ld, one token per
-//     consumer thread.
+//     as a sum of NVFP4 terms (E2M1 codes, one E4M3 scale per 16 values; eight
+//     terms at four heads per KV head, six at eight), stacked along N, and the
+//     score is the sum of the head's columns.  The FP8 variant does the same
+//     with kind::f8f6f4 and four E4M3 terms.  Scores land in TMEM (one buffer
+//     per consumer group) and are read with tcgen05.ld, one token per consumer
+//     thread.
 //   * P.V on warp MMAs (m16n8k16 FP16 -> FP32; tokens = K, GQA heads = N):
 //     E2M1 pairs -> f16x2 by cvt.rn.f16x2.e2m1x2, times the E4M3 block scale
 //     (f16x2 multiply; code * scale has at most 6 significant bits in
@@ -58,7 +60,6 @@ constexpr int kQueryWarp = kConsumerWarps + kGroups;
 constexpr int kThreads = (kConsumerWarps + kGroups + 1) * 32;
 constexpr int kMaxBatch = 1024;    // sequences per call (prefix sums live in shared memory)
 constexpr int kMaxGroup = 8;       // query heads per KV head
-constexpr int kTerms = 4;          // query terms of the score MMA
 constexpr int kQBufs = 4;          // query images in flight: a group issues a tile at most three
                                    // segments ahead of the one all warps are in (segments of one tile)
 constexpr int kSlotFloats = kMaxGroup * kD + 2 * kMaxGroup;  // one partial (o, m, l)
@@ -84,11 +85,21 @@ struct Prec<NVKV_PREC_FP8_E4M3> {
   static constexpr int kRing = 2;
 };
 
-// NH = heads per group slot set (4 or 8), N = NH * kTerms columns of the score MMA.
+// NH = heads per group slot set (4 or 8), N = NH * kTerms columns of the score
+// MMA.  Query terms per head: E4M3 terms keep ~4 more bits each, so four
+// reach FP32-like precision; E2M1 terms keep ~2.6 bits each relative to the
+// residual of their 16-value block, so a block holding one outlier needs more
+// (eight at four heads; six at eight heads, where TMEM columns run short).
 template <int PREC, int NH>
 struct Cfg {
   using P = Prec<PREC>;
   static constexpr bool kNv = PREC == NVKV_PREC_NVFP4;
+  static constexpr int kTerms = !kNv ? 4 : (NH == 4 ? 8 : 6);
+  // The head's largest |q| is scaled into [2^kHeadExp, 2^(kHeadExp+1)) before
+  // the decomposition: E4M3 terms up to 448 (so [128, 256)); E2M1 terms carry
+  // an E4M3 scale, so the top of the range is 6 x 448 = 2688 and [1024, 2048)
+  // leaves the most room above the smallest scale (2^-9) for later terms.
+  static constexpr int kHeadExp = kNv ? 10 : 7;
   static constexpr int N = NH * kTerms;
   static constexpr int kStageBytes = kTile / kGroupRows * P::kGroup;     // 18432 / 32768
   // Each consumer group has its own ring of kStagesG stages, filled by its own
@@ -108,10 +119,13 @@ struct Cfg {
   static constexpr int kQSbo = 8 * kQRow;                                // 8-row group stride of B
   // TMEM columns: scores (one buffer of N per consumer group) from 0; NVFP4
   // scale factors at 16-column boundaries: A (K scales of the group's next
-  // tile) at 128 + 32 * group + 16 * mma, B at 256 + 32 * query image + 16 * mma.
-  // One CTA per SM holds all 512.
+  // tile) at kSfaBase + 32 * group + 16 * mma (kSfaBase >= 3 N), B at 256 +
+  // 32 * query image + 16 * mma.  One CTA per SM holds all 512.
   static constexpr uint32_t kTmemCols = kNv ? 512 : 128;
-  __host__ __device__ static constexpr uint32_t sfa_col(int buf, int k) { return 128 + 32 * buf + 16 * k; }
+  static constexpr uint32_t kSfaBase = 3 * N <= 128 ? 128 : (3 * N + 15) / 16 * 16;
+  static_assert(!kNv || kSfaBase + 32 * 2 + 16 + 4 <= 256, "A scale factors overlap B's");
+  static_assert(kNv || 3 * N <= 128, "score buffers exceed the TMEM allocation");
+  __host__ __device__ static constexpr uint32_t sfa_col(int buf, int k) { return kSfaBase + 32 * buf + 16 * k; }
   __host__ __device__ static constexpr uint32_t sfb_col(int qb, int k) { return 256 + 32 * qb + 16 * k; }
   // shared memory (bytes)
   static constexpr int oRing = 0;
@@ -254,14 +268,14 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
 }
 
 // ---------------------------------------------------------------------------
-// Query images.  Lane (j, kb) of the MMA warp takes head j of the group and
+// Query images.  Lane (j, kb) of the query warp takes head j of the group and
 // values [16 kb, 16 kb + 16); the head is scaled by 2^-e (its max lands in
-// [2^7, 2^8)) and written as kTerms terms, each the residual of the previous
-// ones rounded to the operand format:
+// [2^kHeadExp, 2^(kHeadExp+1))) and written as kTerms terms, each the residual
+// of the previous ones rounded to the operand format:
 //   NVFP4: term = E2M1 codes x one E4M3 scale per 16 values (scale = residual
-//          max / 6, rounded to E4M3); the codes fill B row n = 4 j + term in
-//          the MMA's K-major core-matrix order, the scale goes to the
-//          scale-factor atom of MMA kb / 4, row n, byte kb % 4.
+//          max / 6, rounded to E4M3); the codes fill B row n = kTerms j + term
+//          in the MMA's K-major core-matrix order, the scale goes to the
+//          scale-factor atom of MMA kb / 4, row n % 32, byte 4 (n / 32) + kb % 4.
 //   FP8:   term = E4M3(residual), 16 bytes per lane and term.
 // cs[j] = g_K * sm_scale * log2(e) * 2^e turns a score column sum into log2
 // units.  Heads j >= G get zero terms and cs = 0.
@@ -299,14 +313,14 @@ __device__ void prepare_query(const DecodeArgs &a, const Seg &s, uint8_t *img, u
     am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
     am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
     int ex = 0;
-    if (am > 0.0f) ex = static_cast<int>((__float_as_uint(am) >> 23) & 0xFF) - 127 - 7;
+    if (am > 0.0f) ex = static_cast<int>((__float_as_uint(am) >> 23) & 0xFF) - 127 - C::kHeadExp;
     ex = max(-100, min(100, ex));
     const float down = __uint_as_float(static_cast<uint32_t>(127 - ex) << 23);
 #pragma unroll
     for (int e = 0; e < 16; ++e) v[e] *= down;  // exact (power of two)
 #pragma unroll
-    for (int t = 0; t < kTerms; ++t) {
-      const int n = kTerms * j + t;
+    for (int t = 0; t < C::kTerms; ++t) {
+      const int n = C::kTerms * j + t;
       if constexpr (C::kNv) {
         float m = 0.0f;
 #pragma unroll
@@ -327,7 +341,8 @@ __device__ void prepare_query(const DecodeArgs &a, const Seg &s, uint8_t *img, u
         }
         *reinterpret_cast<uint2 *>(img + (n >> 3) * C::kQSbo + (kb >> 1) * 128 + (n & 7) * 16 + (kb & 1) * 8) =
             make_uint2(w[0], w[1]);
-        sfb[(kb >> 2) * 512 + n * 16 + (kb & 3)] = static_cast<uint8_t>(sb);
+        // row n's four scale bytes of MMA kb / 4: word n / 32 of atom row n % 32
+        sfb[(kb >> 2) * 512 + (n & 31) * 16 + (n >> 5) * 4 + (kb & 3)] = static_cast<uint8_t>(sb);
       } else {
         uint32_t w[4];
 #pragma unroll
@@ -666,12 +681,18 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
       const int nslot_l = slot_l + 1 == C::kStagesG ? 0 : slot_l + 1;  // the group's next tile
       const uint32_t nfpar = nslot_l == 0 ? fpar ^ 1u : fpar;
       ok = ok && warp_wait(&sready[grp], spar, abort);
-      float x[NH * kTerms];
+      float ssum[NH];  // per head: the sum of its kTerms score columns
+#pragma unroll
+      for (int h = 0; h < NH; ++h) ssum[h] = 0.0f;
       if (ok) {
         tc_fence_after();
-        tmem_ld16(tq + static_cast<uint32_t>(grp * C::N), *reinterpret_cast<float(*)[16]>(x));
-        if constexpr (NH == 8)
-          tmem_ld16(tq + static_cast<uint32_t>(grp * C::N + 16), *reinterpret_cast<float(*)[16]>(x + 16));
+#pragma unroll
+        for (int ch = 0; ch < C::N / 16; ++ch) {
+          float x[16];
+          tmem_ld16(tq + static_cast<uint32_t>(grp * C::N + 16 * ch), x);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ssum[(16 * ch + e) / C::kTerms] += x[e];
+        }
       }
       // The group's next tile may now score into the same buffer.  Its MMAs
       // go out now if its stage has landed for all four warps, else after
@@ -714,8 +735,7 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
       bool need = false;
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
-        const float sum = (x[4 * h] + x[4 * h + 1]) + (x[4 * h + 2] + x[4 * h + 3]);
-        sc[h] = (valid && h < G) ? sum * cs[h] : -INFINITY;
+        sc[h] = (valid && h < G) ? ssum[h] * cs[h] : -INFINITY;
         need |= sc[h] > m[h] + kRescaleThreshold;
       }
       if (__any_sync(0xffffffffu, need)) {  // raise the running max (warp-uniform)

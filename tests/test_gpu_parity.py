@@ -81,6 +81,34 @@ def test_fp8_write_and_decode(name):
     _run_case(name, fp8=True)
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_query_with_outliers(fp8):
+    """The score MMA takes the BF16 query as a sum of four NVFP4 (or E4M3)
+    terms; a query whose 16-value blocks hold one large outlier each (the
+    case that leaves the largest residual on the small values beside it)
+    still meets the tolerance."""
+    nv = _nv()
+    from nvfp4_quantized_paged_gb300.runner import Layer
+    from nvfp4_quantized_paged_gb300.workloads import Workload
+    spec = _spec(name="q_outliers", B=3, lens=(900, 130, 64))
+    wl = Workload(spec, seed=21, device="cuda")
+    lay = Layer(wl, 0, prec=nv.PREC_FP8 if fp8 else nv.PREC_NVFP4)
+    gen = torch.Generator().manual_seed(22)
+    q = torch.randn(spec.B, spec.Hq, 128, generator=gen)
+    pos = torch.randint(0, 16, (spec.B, spec.Hq, 8), generator=gen) + 16 * torch.arange(8)
+    q.scatter_(2, pos, 40.0 * torch.sign(torch.randn(spec.B, spec.Hq, 8, generator=gen)))
+    q[:, :, 5] = 300.0  # one channel far above the rest
+    qb = q.to(torch.bfloat16)
+    lay.step()
+    lay.decode(q=qb.cuda())
+    torch.cuda.synchronize()
+    assert lay.cache.err.item() == 0
+    orc = OracleLayer(wl, 0, range(spec.B), fp8)
+    orc.q_bits = qb.view(torch.int16).numpy().view(np.uint16)
+    ok, worst = within_tol(lay.out.float().cpu().numpy(), orc.attention())
+    assert ok, f"max excess over tolerance {worst}"
+
+
 def test_split_count_does_not_change_the_result():
     """Auto schedule, 1 split and many splits agree with each other within
     FP32 rounding (the merge identity), not only within the tolerance."""
