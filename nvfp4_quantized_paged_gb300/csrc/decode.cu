@@ -113,7 +113,7 @@ struct Cfg {
   __host__ __device__ static constexpr uint32_t fill_of(int64_t i) {
     return static_cast<uint32_t>(i / kGroups / kStagesG);
   }
-  static constexpr int kMH = (!kNv && NH == 8) ? 1 : 2;  // heads per pass of the segment merge
+  static constexpr int kMH = kNv ? 4 : (NH == 8 ? 1 : 2);  // heads per pass of the segment merge
   static constexpr int kQRow = P::kKRow;                                 // B row bytes
   static constexpr int kQImg = N * kQRow;                                // one query image
   static constexpr int kQSbo = 8 * kQRow;                                // 8-row group stride of B
@@ -138,8 +138,8 @@ struct Cfg {
   static constexpr int oCum = oMrgMl + kConsumerWarps * kMaxGroup * 2 * 4;  // [kMaxBatch + 1] i32
   static constexpr int oBars = (oCum + (kMaxBatch + 1) * 4 + 15) / 16 * 16;
   static constexpr int kBars = 2 * kStages + kGroups + 2 * kQBufs;  // full, empty, sready, qready, qfree
-  static constexpr int oFlags = oBars + kBars * 8;                          // tmem holder, abort, fills[kStages]
-  static constexpr int kSmem = oFlags + 4 * (2 + kStages);
+  static constexpr int oFlags = oBars + kBars * 8;  // tmem holder, abort, fills[kStages], W, NC, u0, u1
+  static constexpr int kSmem = oFlags + 4 * (6 + kStages);
 };
 
 struct DecodeArgs {
@@ -162,21 +162,23 @@ struct Seg {
 };
 
 // cum[b] = tiles of sequences before b; units before sequence b = Hkv * cum[b].
-__device__ __forceinline__ Seg seg_at(int64_t u, int64_t u_end, const int32_t *cum, int B, int Hkv) {
+// Unit indices fit in 32 bits (the host refuses larger problems).
+__device__ __forceinline__ Seg seg_at(int64_t u64, int64_t u_end, const int32_t *cum, int B, int Hkv) {
+  const int u = static_cast<int>(u64);
   int lo = 0, hi = B - 1;  // last b with Hkv*cum[b] <= u (sequences without tiles are skipped)
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (static_cast<int64_t>(cum[mid]) * Hkv <= u) lo = mid;
+    if (cum[mid] * Hkv <= u) lo = mid;
     else hi = mid - 1;
   }
   const int nb = cum[lo + 1] - cum[lo];
-  const int64_t r = u - static_cast<int64_t>(cum[lo]) * Hkv;
+  const int r = u - cum[lo] * Hkv;
   Seg s;
   s.b = lo;
-  s.h = static_cast<int>(r / nb);
-  s.t0 = static_cast<int>(r % nb);
-  const int64_t left = u_end - u;
-  s.t1 = static_cast<int>(left < nb - s.t0 ? s.t0 + left : nb);
+  s.h = r / nb;
+  s.t0 = r - s.h * nb;
+  const int left = static_cast<int>(u_end - u64);
+  s.t1 = left < nb - s.t0 ? s.t0 + left : nb;
   return s;
 }
 
@@ -935,19 +937,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
       if (b < B) cum[b + 1] = carry + incl;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
+    if (lane == 0) {  // this CTA's share of the units, computed once
+      // never more shares than units: every active CTA owns at least one unit,
+      // which the contributor count of the merge relies on
+      const int64_t W = static_cast<int64_t>(carry) * Hkv;
+      const int64_t NC = W < a.num_ctas ? (W > 0 ? W : 1) : a.num_ctas;
+      const bool active = blockIdx.x < NC;
+      int *sh = flags + 2 + C::kStages;
+      sh[0] = static_cast<int>(W);
+      sh[1] = static_cast<int>(NC);
+      sh[2] = active ? static_cast<int>(share_begin(blockIdx.x, W, NC)) : 0;
+      sh[3] = active ? static_cast<int>(share_begin(blockIdx.x + 1, W, NC)) : 0;
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  const int64_t W = static_cast<int64_t>(cum[B]) * Hkv;
-  // never more shares than units: every active CTA owns at least one unit,
-  // which the contributor count of the merge relies on
-  const int64_t NC = W < a.num_ctas ? (W > 0 ? W : 1) : a.num_ctas;
-  const bool active = blockIdx.x < NC;
-  const int64_t u0 = active ? share_begin(blockIdx.x, W, NC) : 0;
-  const int64_t u1 = active ? share_begin(blockIdx.x + 1, W, NC) : 0;
+  const int *sh = flags + 2 + C::kStages;
+  const int64_t W = sh[0], NC = sh[1], u0 = sh[2], u1 = sh[3];
 
   // zero rows of empty sequences (spread over CTAs)
   for (int b = blockIdx.x; b < B; b += a.num_ctas) {
@@ -1170,6 +1179,7 @@ nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t 
   if (!(sm_scale >= 0.0f)) return NVKV_ERR_INVALID_ARG;
   const int64_t max_units = static_cast<int64_t>(batch) * Hkv *
                             ((static_cast<int64_t>(max_pages) * cache->page_size + kTile - 1) / kTile);
+  if (max_units > 0x7fffffff) return NVKV_ERR_UNSUPPORTED;  // unit indices are 32-bit in the kernel
   const int64_t nctas = num_ctas_for(prec, batch, Hkv, G, max_units, num_splits);
   if (nctas < 0) return NVKV_ERR_CUDA;
   if (nctas > 0x7fffffff) return NVKV_ERR_UNSUPPORTED;
