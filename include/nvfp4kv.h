@@ -39,11 +39,16 @@
  * K bytes are stored in 16-byte chunks, chunk-major: byte j of row r at
  * (j / 16) * 128 + r * 16 + j % 16 (the K-major core-matrix order of a
  * tensor-core operand, so a staged tile of K codes is an MMA operand as it
- * stands).  V rows are stored in the order 0, 2, 4, 6, 1, 3, 5, 7 (row r at
- * position (r % 2) * 4 + r / 2; bank-conflict-free operand loads); scales
- * row-major.  A page of one KV head is one contiguous run of bytes, which
- * decode fetches with a single bulk copy.  The byte contents are the
- * quantizer's output above; only their positions are fixed here.
+ * stands); K scales row-major (block b of row r at r * 8 + b).  V is stored by
+ * row pairs (2c, 2c+1), the register layout of a P.V operand (two tokens of
+ * one value): NVFP4 code of value d = 16 b + j of row r at byte b * 64 +
+ * (r / 2) * 16 + j of the V codes, in the low nibble for even r and the high
+ * nibble for odd r; V scales block-major (b * 8 + r); FP8 byte of value
+ * 16 b + j at (j / 8) * 512 + b * 64 + (r / 2) * 16 + (j % 8) * 2 + r % 2 of
+ * V.  A page of one KV head is one contiguous run of bytes, which decode
+ * fetches with a single bulk copy.  The contents are the quantizer's output
+ * above; only their positions are fixed here (an NVFP4 V write changes only
+ * its own row's nibbles, with atomic byte-lane updates).
  *   Supported: head_dim 128; page_size 16, 32 or 64; every pointer 16-byte
  *   aligned.  Anything else -> NVKV_ERR_UNSUPPORTED.
  *

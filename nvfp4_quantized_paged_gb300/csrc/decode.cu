@@ -419,13 +419,15 @@ struct WarpO {
   float o[8][4];
 };
 
-// V operand of a slice.  NVFP4: per 8-byte half w, the e2m1 pairs of tokens
-// (2c, 2c+1) at d and d + 1 and of tokens (2c+8, 2c+9), and the f16x2 block
-// scales of those token pairs; masked tokens carry scale 0.  FP8: the raw code
-// words of tokens 2c, 2c+1, 2c+8, 2c+9, masked tokens zeroed.
+// V operand of a slice, straight from the pair-interleaved V layout: a[q] /
+// b[q] hold the 16 bytes of token pairs (2c, 2c+1) / (2c+8, 2c+9) for values
+// 16r .. 16r+15 (NVFP4: byte j = both tokens' codes of value 16r + j; FP8:
+// two 8-value chunks, 16-bit half j' = both tokens' bytes of value 16r + 8h +
+// j').  NVFP4 also carries the f16x2 block scales of both pairs; masked
+// tokens get scale 0 (NVFP4) or a zero byte (FP8).
 template <int PREC>
 struct VOps {
-  uint32_t w[PREC == NVKV_PREC_NVFP4 ? 2 : 4][4];
+  uint32_t a[PREC == NVKV_PREC_NVFP4 ? 4 : 8], b[PREC == NVKV_PREC_NVFP4 ? 4 : 8];
   uint32_t sAB, sCD;
 };
 
@@ -433,17 +435,12 @@ struct VOps {
 template <int PREC>
 __device__ __forceinline__ void load_v(const uint8_t *g0, int r, int c, int nvalid, VOps<PREC> &x) {
   const int tA = 2 * c;
-  const int pA = v_row_pos(tA), pB = v_row_pos(tA + 1);  // rows 2c, 2c+1 of both groups
   if constexpr (PREC == NVKV_PREC_NVFP4) {
     const uint8_t *g1 = g0 + kNvGroup;
-    const uint2 A = *reinterpret_cast<const uint2 *>(g0 + kNvVCodes + pA * 64 + 8 * r);
-    const uint2 B = *reinterpret_cast<const uint2 *>(g0 + kNvVCodes + pB * 64 + 8 * r);
-    const uint2 C = *reinterpret_cast<const uint2 *>(g1 + kNvVCodes + pA * 64 + 8 * r);
-    const uint2 D = *reinterpret_cast<const uint2 *>(g1 + kNvVCodes + pB * 64 + 8 * r);
-    uint32_t sv = static_cast<uint32_t>(g0[kNvVScales + tA * 8 + r]) |
-                  (static_cast<uint32_t>(g0[kNvVScales + (tA + 1) * 8 + r]) << 8) |
-                  (static_cast<uint32_t>(g1[kNvVScales + tA * 8 + r]) << 16) |
-                  (static_cast<uint32_t>(g1[kNvVScales + (tA + 1) * 8 + r]) << 24);
+    const uint4 A = *reinterpret_cast<const uint4 *>(g0 + kNvVCodes + r * 64 + c * 16);
+    const uint4 B = *reinterpret_cast<const uint4 *>(g1 + kNvVCodes + r * 64 + c * 16);
+    uint32_t sv = static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(g0 + kNvVScales + r * 8 + tA)) |
+                  (static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(g1 + kNvVScales + r * 8 + tA)) << 16);
     if (nvalid < 16) {  // masked tokens get scale 0 -> value 0 (codes are finite)
       if (tA >= nvalid) sv &= 0xFFFFFF00u;
       if (tA + 1 >= nvalid) sv &= 0xFFFF00FFu;
@@ -452,53 +449,44 @@ __device__ __forceinline__ void load_v(const uint8_t *g0, int r, int c, int nval
     }
     x.sAB = f16x2_from_e4m3x2<0>(sv);
     x.sCD = f16x2_from_e4m3x2<1>(sv);
-    const uint32_t a[2] = {A.x, A.y}, b[2] = {B.x, B.y}, cc[2] = {C.x, C.y}, dd[2] = {D.x, D.y};
-#pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      // byte j: the token pair's low nibbles (d = 16r + 8w + 2j) or high nibbles (d + 1)
-      x.w[w][0] = (a[w] & 0x0F0F0F0Fu) | ((b[w] & 0x0F0F0F0Fu) << 4);
-      x.w[w][1] = ((a[w] >> 4) & 0x0F0F0F0Fu) | (b[w] & 0xF0F0F0F0u);
-      x.w[w][2] = (cc[w] & 0x0F0F0F0Fu) | ((dd[w] & 0x0F0F0F0Fu) << 4);
-      x.w[w][3] = ((cc[w] >> 4) & 0x0F0F0F0Fu) | (dd[w] & 0xF0F0F0F0u);
-    }
+    x.a[0] = A.x; x.a[1] = A.y; x.a[2] = A.z; x.a[3] = A.w;
+    x.b[0] = B.x; x.b[1] = B.y; x.b[2] = B.z; x.b[3] = B.w;
   } else {
     const uint8_t *g1 = g0 + kF8Group;
-    const uint4 A = *reinterpret_cast<const uint4 *>(g0 + kF8V + pA * 128 + 16 * r);
-    const uint4 B = *reinterpret_cast<const uint4 *>(g0 + kF8V + pB * 128 + 16 * r);
-    const uint4 C = *reinterpret_cast<const uint4 *>(g1 + kF8V + pA * 128 + 16 * r);
-    const uint4 D = *reinterpret_cast<const uint4 *>(g1 + kF8V + pB * 128 + 16 * r);
-    x.w[0][0] = A.x; x.w[1][0] = A.y; x.w[2][0] = A.z; x.w[3][0] = A.w;
-    x.w[0][1] = B.x; x.w[1][1] = B.y; x.w[2][1] = B.z; x.w[3][1] = B.w;
-    x.w[0][2] = C.x; x.w[1][2] = C.y; x.w[2][2] = C.z; x.w[3][2] = C.w;
-    x.w[0][3] = D.x; x.w[1][3] = D.y; x.w[2][3] = D.z; x.w[3][3] = D.w;
-    if (nvalid < 16) {  // masked tokens -> E4M3 zero (stale bytes could be NaN)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (tA >= nvalid) x.w[q][0] = 0;
-        if (tA + 1 >= nvalid) x.w[q][1] = 0;
-        if (tA + 8 >= nvalid) x.w[q][2] = 0;
-        if (tA + 9 >= nvalid) x.w[q][3] = 0;
+    for (int hh = 0; hh < 2; ++hh) {
+      const uint4 A = *reinterpret_cast<const uint4 *>(g0 + kF8V + hh * 512 + r * 64 + c * 16);
+      const uint4 B = *reinterpret_cast<const uint4 *>(g1 + kF8V + hh * 512 + r * 64 + c * 16);
+      x.a[4 * hh + 0] = A.x; x.a[4 * hh + 1] = A.y; x.a[4 * hh + 2] = A.z; x.a[4 * hh + 3] = A.w;
+      x.b[4 * hh + 0] = B.x; x.b[4 * hh + 1] = B.y; x.b[4 * hh + 2] = B.z; x.b[4 * hh + 3] = B.w;
+    }
+    if (nvalid < 16) {  // masked tokens -> E4M3 zero (stale bytes could be NaN)
+      const uint32_t ma = (tA >= nvalid ? 0u : 0x00FF00FFu) | (tA + 1 >= nvalid ? 0u : 0xFF00FF00u);
+      const uint32_t mb = (tA + 8 >= nvalid ? 0u : 0x00FF00FFu) | (tA + 9 >= nvalid ? 0u : 0xFF00FF00u);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        x.a[q] &= ma;
+        x.b[q] &= mb;
       }
     }
     x.sAB = x.sCD = 0;
   }
 }
 
-// P.V MMA for output tile J (NVFP4: half w = J / 4, byte J % 4 of each pair
-// word; FP8: token-pair word J / 2, byte pair J % 2).
+// P.V MMA for output tile J (values d = 16r + 2J, 16r + 2J + 1).  NVFP4: bytes
+// 2J, 2J + 1 of each pair, i.e. bytes 2(J%2), 2(J%2)+1 of word J/2.  FP8:
+// chunk J/4, word J%4, halves 0 (d) and 1 (d + 1).
 template <int PREC, int J>
 __device__ __forceinline__ void pv_tile(const VOps<PREC> &x, uint32_t b0, uint32_t b1, WarpO &st) {
   if constexpr (PREC == NVKV_PREC_NVFP4) {
-    constexpr int w = J >> 2, I = J & 3;
-    mma_f16_16816(st.o[J], hmul2_u32(f16x2_from_e2m1x2<I>(x.w[w][0]), x.sAB),
-                  hmul2_u32(f16x2_from_e2m1x2<I>(x.w[w][1]), x.sAB), hmul2_u32(f16x2_from_e2m1x2<I>(x.w[w][2]), x.sCD),
-                  hmul2_u32(f16x2_from_e2m1x2<I>(x.w[w][3]), x.sCD), b0, b1);
+    constexpr int w = J >> 1, I = 2 * (J & 1);
+    mma_f16_16816(st.o[J], hmul2_u32(f16x2_from_e2m1x2<I>(x.a[w]), x.sAB),
+                  hmul2_u32(f16x2_from_e2m1x2<I + 1>(x.a[w]), x.sAB), hmul2_u32(f16x2_from_e2m1x2<I>(x.b[w]), x.sCD),
+                  hmul2_u32(f16x2_from_e2m1x2<I + 1>(x.b[w]), x.sCD), b0, b1);
   } else {
-    constexpr int qd = J >> 1;
-    constexpr uint32_t sel = (J & 1) ? 0x7362u : 0x5140u;
-    const uint32_t ab = prmt(x.w[qd][0], x.w[qd][1], sel), cd = prmt(x.w[qd][2], x.w[qd][3], sel);
-    mma_f16_16816(st.o[J], f16x2_from_e4m3x2<0>(ab), f16x2_from_e4m3x2<1>(ab), f16x2_from_e4m3x2<0>(cd),
-                  f16x2_from_e4m3x2<1>(cd), b0, b1);
+    constexpr int q = 4 * (J >> 2) + (J & 3);
+    mma_f16_16816(st.o[J], f16x2_from_e4m3x2<0>(x.a[q]), f16x2_from_e4m3x2<1>(x.a[q]), f16x2_from_e4m3x2<0>(x.b[q]),
+                  f16x2_from_e4m3x2<1>(x.b[q]), b0, b1);
   }
 }
 

@@ -35,8 +35,11 @@ inline nvkv_status launch_status() {
 // Byte layout of one (page, KV head) block at head_dim 128 (see the header):
 // groups of 8 slots; an NVFP4 group is [K codes 512 | K scales 64 | V codes
 // 512 | V scales 64] = 1152 bytes, an FP8 group [K 1024 | V 1024]; K bytes in
-// 16-byte chunks, chunk-major (the tensor-core operand order); V rows in the
-// order 0,2,4,6,1,3,5,7.
+// 16-byte chunks, chunk-major (the tensor-core operand order).  V is stored by
+// slot pairs (2c, 2c+1), the layout of a P.V operand register (two tokens of
+// one value): NVFP4 code of value 16b + j of slot r at byte b*64 + (r/2)*16 + j
+// of the V codes, nibble r % 2; V scales block-major (b*8 + r); FP8 byte of
+// value 16b + j at (j/8)*512 + b*64 + (r/2)*16 + (j%8)*2 + r%2 of V.
 constexpr int kNvTokBytes = 144, kF8TokBytes = 256;  // per token, K + V
 constexpr int kGroupRows = 8;
 constexpr int kNvGroup = kGroupRows * kNvTokBytes;    // 1152
@@ -44,7 +47,6 @@ constexpr int kF8Group = kGroupRows * kF8TokBytes;    // 2048
 constexpr int kNvKScales = 512, kNvVCodes = 576, kNvVScales = 1088;  // offsets inside an NVFP4 group
 constexpr int kF8V = 1024;                                          // offset of V inside an FP8 group
 
-__host__ __device__ constexpr int v_row_pos(int r) { return (r & 1) * 4 + (r >> 1); }
 
 struct CacheDev {
   uint8_t *data;
@@ -54,22 +56,31 @@ struct CacheDev {
   __host__ __device__ int64_t block(int64_t page, int h, int tok_bytes) const {
     return (page * Hkv + h) * static_cast<int64_t>(P) * tok_bytes;
   }
-  // NVFP4: the 8 code bytes of 16-value block `blk` of slot `off` (kind 0 = K, 1 = V)
-  __host__ __device__ int64_t nv_codes(int64_t page, int h, int kind, int off, int blk) const {
-    const int64_t g = block(page, h, kNvTokBytes) + static_cast<int64_t>(off >> 3) * kNvGroup;
-    const int r = off & 7;
-    return kind == 0 ? g + (blk >> 1) * 128 + r * 16 + (blk & 1) * 8 : g + kNvVCodes + v_row_pos(r) * 64 + blk * 8;
+  // NVFP4 K: the 8 code bytes of 16-value block `blk` of slot `off`
+  __host__ __device__ int64_t nv_kcodes(int64_t page, int h, int off, int blk) const {
+    return block(page, h, kNvTokBytes) + static_cast<int64_t>(off >> 3) * kNvGroup + (blk >> 1) * 128 +
+           (off & 7) * 16 + (blk & 1) * 8;
   }
-  // NVFP4: the E4M3 scale byte of block `blk` of slot `off`
+  // NVFP4 V: the 16 bytes holding block `blk` of slot `off` and of its pair
+  // partner (value 16 blk + j at byte j; this slot's nibble is off % 2)
+  __host__ __device__ int64_t nv_vcodes(int64_t page, int h, int off, int blk) const {
+    return block(page, h, kNvTokBytes) + static_cast<int64_t>(off >> 3) * kNvGroup + kNvVCodes + blk * 64 +
+           ((off & 7) >> 1) * 16;
+  }
+  // NVFP4: the E4M3 scale byte of block `blk` of slot `off` (kind 0 = K, 1 = V)
   __host__ __device__ int64_t nv_scale(int64_t page, int h, int kind, int off, int blk) const {
     return block(page, h, kNvTokBytes) + static_cast<int64_t>(off >> 3) * kNvGroup +
-           (kind == 0 ? kNvKScales : kNvVScales) + (off & 7) * 8 + blk;
+           (kind == 0 ? kNvKScales + (off & 7) * 8 + blk : kNvVScales + blk * 8 + (off & 7));
   }
-  // FP8: the 16 bytes of 16-value block `blk` of slot `off`
-  __host__ __device__ int64_t f8_block(int64_t page, int h, int kind, int off, int blk) const {
-    const int64_t g = block(page, h, kF8TokBytes) + static_cast<int64_t>(off >> 3) * kF8Group;
-    const int r = off & 7;
-    return kind == 0 ? g + blk * 128 + r * 16 : g + kF8V + v_row_pos(r) * 128 + blk * 16;
+  // FP8 K: the 16 bytes of 16-value block `blk` of slot `off`
+  __host__ __device__ int64_t f8_kblock(int64_t page, int h, int off, int blk) const {
+    return block(page, h, kF8TokBytes) + static_cast<int64_t>(off >> 3) * kF8Group + blk * 128 + (off & 7) * 16;
+  }
+  // FP8 V: the 16 bytes holding values 16 blk + 8 half + j' (j' < 8) of slot
+  // `off` and its partner (this slot's byte of value j' is 2 j' + off % 2)
+  __host__ __device__ int64_t f8_vchunk(int64_t page, int h, int off, int blk, int half) const {
+    return block(page, h, kF8TokBytes) + static_cast<int64_t>(off >> 3) * kF8Group + kF8V + half * 512 + blk * 64 +
+           ((off & 7) >> 1) * 16;
   }
 };
 

@@ -137,7 +137,23 @@ __global__ void __launch_bounds__(256)
       hi |= e2m1x2_from_f32(__fdiv_rn(x[8 + 2 * j], den), __fdiv_rn(x[8 + 2 * j + 1], den)) << (8 * j);
     }
   }
-  *reinterpret_cast<uint2 *>(c.data + c.nv_codes(page, h, kind, off, blk)) = make_uint2(lo, hi);
+  if (kind == 0) {
+    *reinterpret_cast<uint2 *>(c.data + c.nv_kcodes(page, h, off, blk)) = make_uint2(lo, hi);
+  } else {
+    // V: value 16 blk + j goes to byte j of the pair's 16 bytes, nibble off % 2;
+    // the partner slot owns the other nibbles, so each word is cleared and set
+    // with atomics on this slot's nibbles only (the partner may be written by
+    // another thread of the same launch)
+    uint32_t *dst = reinterpret_cast<uint32_t *>(c.data + c.nv_vcodes(page, h, off, blk));
+    const int sh = 4 * (off & 1);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t four = ((q < 2 ? lo : hi) >> (16 * (q & 1))) & 0xFFFFu;  // codes 4q .. 4q+3, one per nibble
+      const uint32_t spread = (four & 0xFu) | ((four & 0xF0u) << 4) | ((four & 0xF00u) << 8) | ((four & 0xF000u) << 12);
+      atomicAnd(dst + q, ~(0x0F0F0F0Fu << sh));
+      atomicOr(dst + q, spread << sh);
+    }
+  }
   c.data[c.nv_scale(page, h, kind, off, blk)] = static_cast<uint8_t>(sbyte);
 }
 
@@ -175,7 +191,16 @@ __global__ void __launch_bounds__(256)
              (e4m3x2_from_f32(__fdiv_rn(x[4 * j + 2], s8), __fdiv_rn(x[4 * j + 3], s8)) << 16);
     }
   }
-  *reinterpret_cast<uint4 *>(c.data + c.f8_block(page, h, kind, off, blk)) = make_uint4(w[0], w[1], w[2], w[3]);
+  if (kind == 0) {
+    *reinterpret_cast<uint4 *>(c.data + c.f8_kblock(page, h, off, blk)) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {  // V: value 16 blk + 8 half + j' at byte 2 j' + off % 2 of its chunk (the partner owns the others)
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint8_t *dst = c.data + c.f8_vchunk(page, h, off, blk, half) + (off & 1);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) dst[2 * j] = static_cast<uint8_t>(w[2 * half + (j >> 2)] >> (8 * (j & 3)));
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -231,7 +256,20 @@ __global__ void __launch_bounds__(256)
     return;
   }
   const int off = static_cast<int>(t % c.P);
-  const uint2 cw = *reinterpret_cast<const uint2 *>(c.data + c.nv_codes(page, h, kind, off, blk));
+  uint2 cw;
+  if (kind == 0) {
+    cw = *reinterpret_cast<const uint2 *>(c.data + c.nv_kcodes(page, h, off, blk));
+  } else {  // V: this slot's nibbles of the pair's 16 bytes, back to two codes per byte
+    const uint4 pw = *reinterpret_cast<const uint4 *>(c.data + c.nv_vcodes(page, h, off, blk));
+    const uint32_t ww[4] = {pw.x, pw.y, pw.z, pw.w};
+    uint32_t packed[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t n = (ww[q] >> (4 * (off & 1))) & 0x0F0F0F0Fu;  // code 4q + i in byte i
+      packed[q] = (n & 0xFu) | ((n >> 4) & 0xF0u) | ((n >> 8) & 0xF00u) | ((n >> 12) & 0xF000u);
+    }
+    cw = make_uint2(packed[0] | (packed[1] << 16), packed[2] | (packed[3] << 16));
+  }
   const float S = f32_from_e4m3(c.data[c.nv_scale(page, h, kind, off, blk)]);
   const float ratio = __fdiv_rn(c.scale[kind], ws_scale[kind]);
   const uint32_t words[2] = {cw.x, cw.y};

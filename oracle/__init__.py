@@ -67,6 +67,8 @@ def lib():
                                              _f32p, ctypes.c_int, ctypes.c_int64, _u8p]
         L.orc_slot_bytes.restype = ctypes.c_int
         L.orc_slot_bytes.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i64p]
+        L.orc_v_code_layout.restype = ctypes.c_int
+        L.orc_v_code_layout.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _i64p, _i32p]
         L.orc_gather_dequant.restype = ctypes.c_int
         L.orc_gather_dequant.argtypes = [ctypes.c_int, _u8p, ctypes.c_int, ctypes.c_float, _i32p, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
@@ -178,29 +180,48 @@ class Cache:
         self._slot_pos = None
 
     def slot_positions(self) -> np.ndarray:
-        """int64 [P, bytes per slot]: positions of every byte of each slot in a block."""
+        """int64 [P, n]: positions of the bytes each slot occupies in a block (K
+        codes, K scales, V codes, V scales; FP8: K, V).  NVFP4 V codes of paired
+        rows share bytes with the partner row: the slot's entries are the D
+        bytes holding its D nibbles."""
         if self._slot_pos is None:
-            n = self.D + self.D // 8 if self.prec == PREC_NVFP4 else 2 * self.D
-            pos = np.empty((self.P, n), np.int64)
+            rows = []
             for off in range(self.P):
-                row = pos[off]
-                assert lib().orc_slot_bytes(self.prec, self.P, self.D, off, _p(row, _i64p)) == 0
-            self._slot_pos = pos
+                row = np.empty(2 * self.D + self.D // 8, np.int64)
+                n = lib().orc_slot_bytes(self.prec, self.P, self.D, off, _p(row, _i64p))
+                assert n > 0
+                rows.append(row[:n])
+            self._slot_pos = np.stack(rows)
         return self._slot_pos
 
     def positions(self, name: str) -> np.ndarray:
+        """[P, n] byte positions of a byte plane (k_data, k_scale, v_scale; FP8:
+        k_data, v_data).  NVFP4 v_data is not a byte plane (see v_data)."""
         D, pos = self.D, self.slot_positions()
         if self.prec == PREC_NVFP4:
             c, s = D // 2, D // 16
-            cuts = {"k_data": (0, c), "k_scale": (c, c + s), "v_data": (c + s, 2 * c + s), "v_scale": (2 * c + s, 2 * c + 2 * s)}
+            cuts = {"k_data": (0, c), "k_scale": (c, c + s), "v_scale": (pos.shape[1] - s, pos.shape[1])}
         else:
             cuts = {"k_data": (0, D), "v_data": (D, 2 * D)}
         a, b = cuts[name]
         return pos[:, a:b]
 
+    def _v_codes(self):
+        """NVFP4 V as the logical [pages, Hkv, P, D/2] code bytes (value 2j in
+        the low nibble, 2j+1 in the high), gathered nibble by nibble."""
+        P, D = self.P, self.D
+        pos = np.empty((P, D), np.int64)
+        sh = np.empty((P, D), np.int32)
+        for off in range(P):
+            assert lib().orc_v_code_layout(P, D, off, _p(pos[off], _i64p), _p(sh[off], _i32p)) == 0
+        nib = (self.data[:, :, pos] >> sh.astype(np.uint8)) & 15
+        return (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
+
     def _plane(self, name):
         if self.prec != PREC_NVFP4 and name.endswith("scale"):
             return None
+        if self.prec == PREC_NVFP4 and name == "v_data":
+            return self._v_codes()
         return self.data[:, :, self.positions(name)]
 
     k_data = property(lambda self: self._plane("k_data"))

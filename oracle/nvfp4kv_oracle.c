@@ -35,10 +35,17 @@
  * order, NVFP4: K codes (R*D/2 bytes), K scales (R*D/16), V codes (R*D/2),
  * V scales (R*D/16); FP8: K (R*D), V (R*D).  K bytes of a group are stored in
  * chunks of w = min(16, row bytes) bytes, chunk-major: byte j of row r sits at
- * (j/w)*R*w + r*w + j%w.  V bytes are row-major, with the rows of an 8-row
- * group in the order 0,2,4,6,1,3,5,7 (row r at position (r%2)*4 + r/2);
- * scales are row-major.  Only the byte positions differ from a plain row
- * layout: every byte's content is the definition below.
+ * (j/w)*R*w + r*w + j%w; K scales are row-major (R*D/16: row r, block b at
+ * r*D/16 + b).  In a group of R = 8 rows, V is stored by row pairs (2c, 2c+1),
+ * c = r/2, e = r%2, value d in block b = d/16 at j = d%16:
+ *   NVFP4 codes : byte b*64 + c*16 + j holds value d of row 2c in its low
+ *                 nibble and of row 2c+1 in its high nibble (e = nibble);
+ *   NVFP4 scales: byte b*8 + r (block-major);
+ *   FP8 bytes   : byte (j/8)*(D*4) + b*64 + c*16 + (j%8)*2 + e.
+ * Groups of R != 8 rows (page sizes below 8) keep V row-major: byte d/2 of
+ * row r at r*D/2 (nibble d%2), scales at r*D/16 + b, FP8 at r*D + d.
+ * Only the positions differ from a plain row layout: every value's content is
+ * the definition below.
  *
  * Every FP32 step is one IEEE-754 binary32 operation with round-to-nearest-even
  * and no fused multiply-add (build with -ffp-contract=off).  Attention runs in
@@ -200,9 +207,8 @@ static void fp8_quantize_vector(const float *x, int D, float s8, uint8_t *out) {
 static int64_t nv_block_bytes(int P, int D) { return (int64_t)P * 2 * (D / 2 + D / 16); }
 static int64_t fp8_block_bytes(int P, int D) { return (int64_t)P * 2 * D; }
 
-/* Rows per group and the position of V row r inside its group. */
+/* Rows per group. */
 static int group_rows(int P) { return P % 8 == 0 ? 8 : P; }
-static int v_row_pos(int R, int r) { return R == 8 ? (r % 2) * 4 + r / 2 : r; }
 
 /* K byte j of row r inside a group of R rows of `rowbytes` bytes: chunks of
  * w bytes, chunk-major. */
@@ -211,36 +217,69 @@ static int64_t k_chunked(int R, int rowbytes, int r, int j) {
   return (int64_t)(j / w) * R * w + (int64_t)r * w + j % w;
 }
 
-/* NVFP4 byte j of slot `off`: plane 0 = codes (j < D/2), 1 = scales (j < D/16);
- * kind 0 = K, 1 = V. */
-static int64_t nv_byte(int64_t page, int Hkv, int h, int P, int D, int kind, int plane, int off, int j) {
+/* NVFP4: byte holding code d of slot `off` (kind 0 = K, 1 = V); *shift = its
+ * nibble's bit offset (0 or 4). */
+static int64_t nv_code_at(int64_t page, int Hkv, int h, int P, int D, int kind, int off, int d, int *shift) {
   const int R = group_rows(P), r = off % R;
   const int64_t half = (int64_t)R * (D / 2 + D / 16);  /* K (or V) part of a group */
   const int64_t base = (page * Hkv + h) * nv_block_bytes(P, D) + (int64_t)(off / R) * 2 * half + kind * half;
-  if (plane == 0) return base + (kind == 0 ? k_chunked(R, D / 2, r, j) : (int64_t)v_row_pos(R, r) * (D / 2) + j);
-  return base + (int64_t)R * (D / 2) + (int64_t)r * (D / 16) + j;
+  if (kind == 0 || R != 8) {
+    *shift = 4 * (d & 1);
+    return base + (kind == 0 ? k_chunked(R, D / 2, r, d / 2) : (int64_t)r * (D / 2) + d / 2);
+  }
+  *shift = 4 * (r % 2);
+  return base + (int64_t)(d / 16) * 64 + (r / 2) * 16 + d % 16;
 }
 
-/* FP8 byte j (< D) of slot `off`. */
-static int64_t fp8_byte(int64_t page, int Hkv, int h, int P, int D, int kind, int off, int j) {
+/* NVFP4: byte holding the E4M3 scale of 16-value block b of slot `off`. */
+static int64_t nv_scale_at(int64_t page, int Hkv, int h, int P, int D, int kind, int off, int b) {
+  const int R = group_rows(P), r = off % R;
+  const int64_t half = (int64_t)R * (D / 2 + D / 16);
+  const int64_t base = (page * Hkv + h) * nv_block_bytes(P, D) + (int64_t)(off / R) * 2 * half + kind * half +
+                       (int64_t)R * (D / 2);
+  if (kind == 0 || R != 8) return base + (int64_t)r * (D / 16) + b;
+  return base + (int64_t)b * 8 + r;
+}
+
+/* FP8 byte of value d (< D) of slot `off`. */
+static int64_t fp8_at(int64_t page, int Hkv, int h, int P, int D, int kind, int off, int d) {
   const int R = group_rows(P), r = off % R;
   const int64_t base = (page * Hkv + h) * fp8_block_bytes(P, D) + (int64_t)(off / R) * 2 * R * D;
-  return base + (kind == 0 ? k_chunked(R, D, r, j) : (int64_t)R * D + (int64_t)v_row_pos(R, r) * D + j);
+  if (kind == 0) return base + k_chunked(R, D, r, d);
+  if (R != 8) return base + (int64_t)R * D + (int64_t)r * D + d;
+  return base + (int64_t)R * D + (int64_t)((d % 16) / 8) * D * 4 + (int64_t)(d / 16) * 64 + (r / 2) * 16 +
+         (d % 8) * 2 + r % 2;
 }
 
 /* Positions of the bytes of slot `off` inside its (page, KV head) block, in
- * the order K codes, K scales, V codes, V scales (FP8: K bytes, V bytes);
- * out holds D + D/8 (FP8: 2*D) entries. */
+ * the order K codes (D/2), K scales (D/16), V codes, V scales (D/16) (FP8: K
+ * bytes, V bytes, value order).  V codes: the bytes holding values 0..D-1 in
+ * value order, D bytes when V rows are paired (each byte holds one nibble of
+ * the slot), else D/2.  out holds up to 2*D + D/8 entries; returns how many
+ * were written, or -1. */
 int orc_slot_bytes(int prec, int P, int D, int off, int64_t *out) {
-  int kind, j, n = 0;
+  int kind, j, n = 0, sh;
   if (off < 0 || off >= P) return -1;
   for (kind = 0; kind < 2; ++kind) {
     if (prec == 0) {
-      for (j = 0; j < D / 2; ++j) out[n++] = nv_byte(0, 1, 0, P, D, kind, 0, off, j);
-      for (j = 0; j < D / 16; ++j) out[n++] = nv_byte(0, 1, 0, P, D, kind, 1, off, j);
+      const int paired = kind == 1 && group_rows(P) == 8;
+      for (j = 0; j < (paired ? D : D / 2); ++j) out[n++] = nv_code_at(0, 1, 0, P, D, kind, off, paired ? j : 2 * j, &sh);
+      for (j = 0; j < D / 16; ++j) out[n++] = nv_scale_at(0, 1, 0, P, D, kind, off, j);
     } else {
-      for (j = 0; j < D; ++j) out[n++] = fp8_byte(0, 1, 0, P, D, kind, off, j);
+      for (j = 0; j < D; ++j) out[n++] = fp8_at(0, 1, 0, P, D, kind, off, j);
     }
+  }
+  return n;
+}
+
+/* NVFP4 V: for slot `off` and value d, the byte (inside a block) and nibble
+ * bit offset of its code; pos and shift hold D entries. */
+int orc_v_code_layout(int P, int D, int off, int64_t *pos, int32_t *shift) {
+  int d, sh;
+  if (off < 0 || off >= P) return -1;
+  for (d = 0; d < D; ++d) {
+    pos[d] = nv_code_at(0, 1, 0, P, D, 1, off, d, &sh);
+    shift[d] = sh;
   }
   return 0;
 }
@@ -268,8 +307,13 @@ int orc_nvfp4_quantize_write(const float *k, const float *v, int64_t T, int Hkv,
         int j;
         if (D > 1024) return -1;
         nvfp4_quantize_vector(src, D, g[kind], codes, scales);
-        for (j = 0; j < D / 2; ++j) cache[nv_byte(page, Hkv, h, P, D, kind, 0, off, j)] = codes[j];
-        for (j = 0; j < D / 16; ++j) cache[nv_byte(page, Hkv, h, P, D, kind, 1, off, j)] = scales[j];
+        for (j = 0; j < D; ++j) {  /* each code into its nibble, the other nibble kept */
+          int sh;
+          const int64_t at = nv_code_at(page, Hkv, h, P, D, kind, off, j, &sh);
+          const uint8_t code = (uint8_t)((codes[j / 2] >> (4 * (j & 1))) & 15);
+          cache[at] = (uint8_t)((cache[at] & ~(15 << sh)) | (code << sh));
+        }
+        for (j = 0; j < D / 16; ++j) cache[nv_scale_at(page, Hkv, h, P, D, kind, off, j)] = scales[j];
       }
   }
   return 0;
@@ -295,7 +339,7 @@ int orc_fp8_quantize_write(const float *k, const float *v, int64_t T, int Hkv, i
         int j;
         if (D > 1024) return -1;
         fp8_quantize_vector((kind ? v : k) + (t * Hkv + h) * D, D, s8[kind], row);
-        for (j = 0; j < D; ++j) cache[fp8_byte(page, Hkv, h, P, D, kind, off, j)] = row[j];
+        for (j = 0; j < D; ++j) cache[fp8_at(page, Hkv, h, P, D, kind, off, j)] = row[j];
       }
   }
   return 0;
@@ -312,13 +356,13 @@ static void dequant_row(int prec, const uint8_t *cache, int64_t page, int Hkv, i
   int d;
   if (prec == 0) {
     for (d = 0; d < D; ++d) {
-      const uint8_t byte = cache[nv_byte(page, Hkv, h, P, D, kind, 0, off, d / 2)];
-      const uint8_t sc = cache[nv_byte(page, Hkv, h, P, D, kind, 1, off, d / 16)];
-      uint8_t code = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+      int sh;
+      const uint8_t code = (uint8_t)((cache[nv_code_at(page, Hkv, h, P, D, kind, off, d, &sh)] >> sh) & 15);
+      const uint8_t sc = cache[nv_scale_at(page, Hkv, h, P, D, kind, off, d / 16)];
       out[d] = orc_e2m1_value(code) * orc_e4m3_value(sc) * (double)g;
     }
   } else {
-    for (d = 0; d < D; ++d) out[d] = orc_e4m3_value(cache[fp8_byte(page, Hkv, h, P, D, kind, off, d)]) * (double)g;
+    for (d = 0; d < D; ++d) out[d] = orc_e4m3_value(cache[fp8_at(page, Hkv, h, P, D, kind, off, d)]) * (double)g;
   }
 }
 
@@ -452,9 +496,9 @@ int orc_dequant_to_fp8_workspace(const int32_t *block_table, int max_pages, cons
         for (h = 0; h < Hkv; ++h) {
           uint8_t *dst = ws + ((cu_prefix[i] + t) * Hkv + h) * D;
           for (d = 0; d < D; ++d) {
-            const uint8_t byte = cache[nv_byte(page, Hkv, h, P, D, pass, 0, t % P, d / 2)];
-            const uint8_t sc = cache[nv_byte(page, Hkv, h, P, D, pass, 1, t % P, d / 16)];
-            uint8_t code = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+            int sh;
+            const uint8_t code = (uint8_t)((cache[nv_code_at(page, Hkv, h, P, D, pass, t % P, d, &sh)] >> sh) & 15);
+            const uint8_t sc = cache[nv_scale_at(page, Hkv, h, P, D, pass, t % P, d / 16)];
             float w = (float)(orc_e2m1_value(code) * orc_e4m3_value(sc));
             dst[d] = orc_e4m3_encode(w * r);
           }

@@ -201,8 +201,11 @@ def test_block_layout_offsets(orc):
     oracle: one contiguous block per (page, KV head); groups of R slots (R = 8
     when the page size is a multiple of 8, else the page size); per group
     NVFP4 [K codes | K scales | V codes | V scales], FP8 [K | V]; K bytes in
-    16-byte chunks, chunk-major; V rows of an 8-row group in the order
-    0,2,4,6,1,3,5,7."""
+    16-byte chunks, chunk-major; in an 8-row group V is stored by row pairs
+    (2c, 2c+1): NVFP4 code of value d at byte (d//16)*64 + c*16 + d%16, row
+    2c in the low nibble and 2c+1 in the high one, V scales block-major
+    (block b of row r at b*8 + r); FP8 V byte at ((d%16)//8)*512 +
+    (d//16)*64 + c*16 + (d%8)*2 + r%2.  Smaller groups keep V row-major."""
     # page size 4 (one group of 4 rows), D = 32: K codes 16 B per row (one chunk)
     Hkv, P, D = 2, 4, 32
     c = orc.Cache(orc.PREC_NVFP4, 3, Hkv, P, D, [1.0, 1.0])
@@ -229,14 +232,15 @@ def test_block_layout_offsets(orc):
     g0 = 1152
     assert blk[g0 + 3 * 16] == 0x07 and blk[g0 + 128 + 3 * 16 + 1] == 0x70       # K chunks 0 and 1 of row 3
     assert blk[g0 + 512 + 3 * 8] == 0x38 and blk[g0 + 512 + 3 * 8 + 2] == 0x38   # K scales of blocks 0, 2
-    vrow = 5  # row 3 sits at position (3 % 2) * 4 + 3 // 2
-    assert blk[g0 + 576 + vrow * 64] == 0x07 and blk[g0 + 576 + vrow * 64 + 17] == 0x70
-    assert blk[g0 + 1088 + 3 * 8] == 0x30 and blk[g0 + 1088 + 3 * 8 + 2] == 0x30
+    # V: row 3 = pair 1, high nibble; value 0 -> byte 16, value 35 (block 2, j 3) -> byte 128 + 16 + 3
+    assert blk[g0 + 576 + 16] == 0x70 and blk[g0 + 576 + 2 * 64 + 16 + 3] == 0x70
+    assert blk[g0 + 1088 + 3] == 0x30 and blk[g0 + 1088 + 2 * 8 + 3] == 0x30      # V scales of blocks 0, 2
     assert np.count_nonzero(c.data) == 8
     f = orc.Cache(orc.PREC_FP8, 1, 1, 16, 128, [1.0, 1.0])
     orc.quantize_write(f, x, 0.5 * x, np.array([11], np.int64))
     fb = f.data[0, 0]
     g0 = 2048
     assert fb[g0 + 3 * 16] == 0x4C and fb[g0 + 2 * 128 + 3 * 16 + 3] == 0x4C   # K bytes 0 and 35
-    assert fb[g0 + 1024 + vrow * 128] == 0x44 and fb[g0 + 1024 + vrow * 128 + 35] == 0x44
+    # V: value 0 -> 0*512 + 0*64 + 16 + 0 + 1; value 35 (block 2, j 3) -> 0*512 + 128 + 16 + 6 + 1
+    assert fb[g0 + 1024 + 17] == 0x44 and fb[g0 + 1024 + 151] == 0x44
     assert np.count_nonzero(f.data) == 4
