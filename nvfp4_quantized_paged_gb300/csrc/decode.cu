@@ -560,14 +560,13 @@ __device__ __forceinline__ int seg_index_of(int64_t x, int64_t u, int sidx, int 
 template <int PREC, int NH>
 __device__ __forceinline__ bool issue_tile(uint8_t *smem, uint32_t tmem, uint32_t tq, uint64_t *full, uint64_t *sready,
                                            uint64_t *qready, int slot, uint32_t fpar, int qb, uint32_t qpar, int grp,
-                                           int qd, int lane, volatile int *abort) {
+                                           int qd, int lane, volatile int *abort, bool landed = false) {
   using C = Cfg<PREC, NH>;
   const uint8_t *stage = smem + C::oRing + slot * C::kStageBytes;
-  // One warp waits for the stage (sleeping between tries); the other three
-  // wait at the group barrier, which takes no issue slots.
-  bool ok = true;
-  if (qd == 0) ok = warp_wait(&full[slot], fpar, abort);
-  ok = named_bar_and(2 + grp, kGroupWarps * 32, ok);
+  // Each warp waits for the stage itself (the wait suspends the warp) unless
+  // the caller saw it land already; a warp that gave up still meets the
+  // group barrier below.
+  bool ok = landed || warp_wait(&full[slot], fpar, abort);
   if constexpr (C::kNv) {
     if (ok) {
       const int t = 32 * qd + lane;
@@ -672,8 +671,9 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
       const uint32_t nfpar = nslot_l == 0 ? fpar ^ 1u : fpar;
       ok = ok && warp_wait(&sready[grp], spar, abort);
       float ssum[NH];  // per head: the sum of its kTerms score columns
+      float sp[NH][2];  // per head: partial sums of its even and odd columns
 #pragma unroll
-      for (int h = 0; h < NH; ++h) ssum[h] = 0.0f;
+      for (int h = 0; h < NH; ++h) ssum[h] = sp[h][0] = sp[h][1] = 0.0f;
       if (ok) {
         tc_fence_after();
 #pragma unroll
@@ -681,7 +681,18 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
           float x[16];
           tmem_ld16(tq + static_cast<uint32_t>(grp * C::N + 16 * ch), x);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) ssum[(16 * ch + e) / C::kTerms] += x[e];
+          for (int e = 0; e < 16; e += 2) {
+            if constexpr (C::kTerms % 2 == 0) {  // adjacent columns of one head: packed pairs, folded at the end
+              add_f32x2(sp[(16 * ch + e) / C::kTerms][0], sp[(16 * ch + e) / C::kTerms][1], x[e], x[e + 1]);
+            } else {
+              ssum[(16 * ch + e) / C::kTerms] += x[e];
+              ssum[(16 * ch + e + 1) / C::kTerms] += x[e + 1];
+            }
+          }
+        }
+        if constexpr (C::kTerms % 2 == 0) {
+#pragma unroll
+          for (int h = 0; h < NH; ++h) ssum[h] = sp[h][0] + sp[h][1];
         }
       }
       // The group's next tile may now score into the same buffer.  Its MMAs
@@ -699,9 +710,9 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
           nqpar = static_cast<uint32_t>(sx / kQBufs) & 1u;
         }
         const bool landed = ok && mbar_test(&full[grp * C::kStagesG + nslot_l], nfpar);
-        if (named_bar_and(2 + grp, kGroupWarps * 32, landed)) {
+        if (named_bar_and(2 + grp, kGroupWarps * 32, landed)) {  // every warp of the group saw it land
           ok = issue_tile<PREC, NH>(smem, tmem, tq, full, sready, qready, grp * C::kStagesG + nslot_l, nfpar, nqb,
-                                    nqpar, grp, qd, lane, abort);
+                                    nqpar, grp, qd, lane, abort, true);
           if (ok) last_issued = i + kGroups;  // its MMAs went out
           issued = true;
         }

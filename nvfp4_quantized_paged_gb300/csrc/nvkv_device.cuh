@@ -88,6 +88,17 @@ __device__ __forceinline__ float f32_hi(uint32_t h2) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
 }
 
+// (a0 + b0, a1 + b1) as one packed FP32x2 add (round to nearest even each).
+__device__ __forceinline__ void add_f32x2(float &a0, float &a1, float b0, float b1) {
+  asm("{ .reg .b64 p, q;\n\t"
+      "mov.b64 p, {%0, %1};\n\t"
+      "mov.b64 q, {%2, %3};\n\t"
+      "add.rn.f32x2 p, p, q;\n\t"
+      "mov.b64 {%0, %1}, p; }"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
