@@ -913,6 +913,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     fence_mbar_init();
   }
   if (warp == kQueryWarp) tmem_alloc(tmem_holder, C::kTmemCols);
+  // Launched as a programmatic dependent of the previous kernel on the
+  // stream: everything above touches only this CTA's shared memory and TMEM;
+  // every global access below waits for that kernel to complete.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (warp == 0) {
     int carry = 0;
     if (lane == 0) cum[0] = 0;
@@ -1027,6 +1031,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineA
   const int tid = threadIdx.x;
   const int hd = blockIdx.x % a.G, bh = blockIdx.x / a.G;
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the next kernel may start its set-up
   const int2 info = a.unit_info[bh];
   const int n = info.y;
   if (n <= 1) return;  // written directly by the decode grid
@@ -1156,9 +1161,25 @@ size_t workspace_bytes_for(int32_t batch, int32_t Hkv, int64_t nctas) {
   return info_bytes(batch, Hkv) + static_cast<size_t>(nctas) * 2 * kSlotFloats * sizeof(float);
 }
 
+// Programmatic dependent launch: the grid may start while the previous kernel
+// on the stream finishes (its set-up overlaps that kernel's tail); the kernel
+// waits for it before touching global memory.
 template <int PREC, int NH>
 void launch_decode(const DecodeArgs &a, cudaStream_t s) {
-  decode_kernel<PREC, NH><<<static_cast<unsigned>(a.num_ctas), kThreads, Cfg<PREC, NH>::kSmem, s>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.num_ctas));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<PREC, NH>::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, decode_kernel<PREC, NH>, a) != cudaSuccess) {
+    cudaGetLastError();  // clear, then an ordinary stream-ordered launch
+    decode_kernel<PREC, NH><<<static_cast<unsigned>(a.num_ctas), kThreads, Cfg<PREC, NH>::kSmem, s>>>(a);
+  }
 }
 
 nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t *block_table, int32_t max_pages,

@@ -99,6 +99,10 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     nvfp4_write_kernel(const T *__restrict__ k, const T *__restrict__ v, int64_t num_tokens,
                        const int64_t *__restrict__ slot_mapping, const float *__restrict__ gs, CacheDev c) {
+  // programmatic dependent of the previous kernel: wait for it before any
+  // global access, then let the next kernel start its set-up
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t items = num_tokens * c.Hkv * kBlocksPerRow;
   if (gid >= items) return;
@@ -164,6 +168,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     fp8_write_kernel(const T *__restrict__ k, const T *__restrict__ v, int64_t num_tokens,
                      const int64_t *__restrict__ slot_mapping, const float *__restrict__ gs, CacheDev c) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // as in nvfp4_write_kernel
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t items = num_tokens * c.Hkv * kBlocksPerRow;
   if (gid >= items) return;
@@ -290,6 +296,26 @@ __global__ void __launch_bounds__(256)
   *reinterpret_cast<uint4 *>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+// Launch with programmatic dependent launch (the kernel starts with
+// griddepcontrol.wait); an ordinary launch where that is refused.
+template <typename... KArgs, typename... Args>
+void launch_pdl(void (*kernel)(KArgs...), dim3 grid, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) != cudaSuccess) {
+    cudaGetLastError();
+    kernel<<<grid, 256, 0, s>>>(static_cast<KArgs>(args)...);
+  }
+}
+
 inline int grid_for(int64_t items, int threads) {
   const int64_t b = (items + threads - 1) / threads;
   return static_cast<int>(b < 1 ? 1 : b);
@@ -333,20 +359,18 @@ nvkv_status write_common(const void *k, const void *v, nvkv_dtype dtype, int64_t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (prec == NVKV_PREC_NVFP4) {
     if (dtype == NVKV_DTYPE_F32)
-      nvfp4_write_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(k), static_cast<const float *>(v),
-                                                     num_tokens, slot_mapping, gs, c);
+      launch_pdl(nvfp4_write_kernel<float>, grid, s, static_cast<const float *>(k), static_cast<const float *>(v),
+                 num_tokens, slot_mapping, gs, c);
     else
-      nvfp4_write_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(k),
-                                                             static_cast<const __nv_bfloat16 *>(v), num_tokens,
-                                                             slot_mapping, gs, c);
+      launch_pdl(nvfp4_write_kernel<__nv_bfloat16>, grid, s, static_cast<const __nv_bfloat16 *>(k),
+                 static_cast<const __nv_bfloat16 *>(v), num_tokens, slot_mapping, gs, c);
   } else {
     if (dtype == NVKV_DTYPE_F32)
-      fp8_write_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(k), static_cast<const float *>(v),
-                                                   num_tokens, slot_mapping, gs, c);
+      launch_pdl(fp8_write_kernel<float>, grid, s, static_cast<const float *>(k), static_cast<const float *>(v),
+                 num_tokens, slot_mapping, gs, c);
     else
-      fp8_write_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(k),
-                                                           static_cast<const __nv_bfloat16 *>(v), num_tokens,
-                                                           slot_mapping, gs, c);
+      launch_pdl(fp8_write_kernel<__nv_bfloat16>, grid, s, static_cast<const __nv_bfloat16 *>(k),
+                 static_cast<const __nv_bfloat16 *>(v), num_tokens, slot_mapping, gs, c);
   }
   return launch_status();
 }
