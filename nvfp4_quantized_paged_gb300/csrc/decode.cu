@@ -64,6 +64,7 @@ constexpr int kQBufs = 4;          // query images in flight: a group issues a t
                                    // segments ahead of the one all warps are in (segments of one tile)
 constexpr int kSlotFloats = kMaxGroup * kD + 2 * kMaxGroup;  // one partial (o, m, l)
 constexpr float kRescaleThreshold = 8.0f;                   // log2 units
+constexpr float kNoMax = -1e30f;  // running max before any score: finite, so exp2(-inf - m) = 0
 
 // Per-precision tile geometry (groups of 8 tokens, see nvkv_host.h).
 template <int PREC>
@@ -214,6 +215,7 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
   using C = Cfg<PREC, NH>;
   const int lane = threadIdx.x & 31;
   const int Hkv = a.c.Hkv, P = a.c.P;
+  const int lgP = __ffs(P) - 1;  // page sizes are powers of two (16, 32, 64)
   const uint64_t policy = policy_evict_first();
   const uint32_t block_bytes = static_cast<uint32_t>(P) * C::P::kTokBytes;
   int slot_l = 0;     // ring position of the group's next tile
@@ -231,7 +233,7 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
       // Block-table window: lane l holds the entry of page index wbase + l; the
       // next window is requested when the current one comes into use.  Window
       // edges fall on tile edges (32 pages hold whole tiles at P = 16, 32, 64).
-      int wbase = ((s.t0 + kfirst) * kTile) / P;
+      int wbase = ((s.t0 + kfirst) * kTile) >> lgP;
       int32_t pg = wbase + lane < a.max_pages ? brow[wbase + lane] : 0;
       int32_t pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
       for (int k = kfirst; k < ntiles; k += kGroups) {
@@ -240,14 +242,14 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
         if (__any_sync(0xffffffffu, *abort)) return;  // warp-uniform exit
         const int tok0 = (s.t0 + k) * kTile;
         const int ntok = min(kTile, len - tok0);
-        const int nblk = (ntok + P - 1) / P;  // page blocks holding the tile's tokens
-        while ((tok0 + ntok - 1) / P >= wbase + 32) {  // the tile leaves the window (warp-uniform)
+        const int nblk = (ntok + P - 1) >> lgP;  // page blocks holding the tile's tokens
+        while (((tok0 + ntok - 1) >> lgP) >= wbase + 32) {  // the tile leaves the window (warp-uniform)
           wbase += 32;
           pg = pg_next;
           pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
         }
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nblk) * block_bytes);
-        const int page = __shfl_sync(0xffffffffu, pg, (tok0 / P + lane - wbase) & 31);
+        const int page = __shfl_sync(0xffffffffu, pg, ((tok0 >> lgP) + lane - wbase) & 31);
         if (lane < nblk) {
           int64_t pgc = page;
           if (page < 0 || page >= a.c.num_pages) {
@@ -653,11 +655,11 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
     const int Lb = clamped_len(a, s.b);
     const int qb = sidx % kQBufs;
     ok = ok && warp_wait(&qready[qb], static_cast<uint32_t>(sidx / kQBufs) & 1u, abort);
-    float cs[NH], m[NH], l[NH];
+    float cs[NH], m[NH], mt[NH], l[NH];  // mt = m + the rescale threshold
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
       cs[h] = csb[qb * 8 + h];
-      m[h] = -INFINITY;
+      m[h] = mt[h] = kNoMax;
       l[h] = 0.0f;
     }
     WarpO st;
@@ -732,12 +734,13 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
       // scores of this lane's token, log2 units; masked past the sequence end
       const int t = s.t0 + k;
       const bool valid = t * kTile + 32 * qd + lane < Lb;
+      // heads >= G have cs = 0: finite dummy scores, never written out
       float sc[NH];
       bool need = false;
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
-        sc[h] = (valid && h < G) ? ssum[h] * cs[h] : -INFINITY;
-        need |= sc[h] > m[h] + kRescaleThreshold;
+        sc[h] = valid ? ssum[h] * cs[h] : -INFINITY;
+        need |= sc[h] > mt[h];
       }
       if (__any_sync(0xffffffffu, need)) {  // raise the running max (warp-uniform)
         float al[NH];
@@ -747,8 +750,9 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
           const float nm = fmaxf(m[h], mx);
-          al[h] = nm == -INFINITY ? 1.0f : ex2(m[h] - nm);
+          al[h] = ex2(m[h] - nm);
           m[h] = nm;
+          mt[h] = nm + kRescaleThreshold;
           l[h] *= al[h];
         }
         const float alo = 2 * c < NH ? pick<NH>(al, 2 * c) : 1.0f;
@@ -763,7 +767,7 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
       }
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
-        const float p = sc[h] == -INFINITY ? 0.0f : ex2(sc[h] - m[h]);
+        const float p = ex2(sc[h] - m[h]);  // masked tokens: exp2(-inf) = 0
         l[h] += p;
         pt[h * 32 + lane] = __float2half_rn(p);
       }
