@@ -136,7 +136,8 @@ struct Cfg {
   static constexpr int oCs = oPt + kConsumerWarps * NH * 32 * 2;           // [4][8] f32
   static constexpr int oMrgO = oCs + kQBufs * 8 * 4;                       // [12 warps][kMH][128] f32
   static constexpr int oMrgMl = oMrgO + kConsumerWarps * kMH * kD * 4;     // [12 warps][8][2] f32
-  static constexpr int oCum = oMrgMl + kConsumerWarps * kMaxGroup * 2 * 4;  // [kMaxBatch + 1] i32
+  static constexpr int oMrgHd = oMrgMl + kConsumerWarps * kMaxGroup * 2 * 4;  // [8][M, l] f32 per head
+  static constexpr int oCum = oMrgHd + kMaxGroup * 2 * 4;                     // [kMaxBatch + 1] i32
   static constexpr int oBars = (oCum + (kMaxBatch + 1) * 4 + 15) / 16 * 16;
   static constexpr int kBars = 2 * kStages + kGroups + 2 * kQBufs;  // full, empty, sready, qready, qfree
   static constexpr int oFlags = oBars + kBars * 8;  // tmem holder, abort, fills[kStages], W, NC, u0, u1
@@ -183,6 +184,23 @@ __device__ __forceinline__ Seg seg_at(int64_t u64, int64_t u_end, const int32_t 
   return s;
 }
 
+// The segment after s, which ended at the end of its (b, h), starting at unit
+// u (< u_end): the next KV head, or the next sequence that has tiles.
+__device__ __forceinline__ Seg seg_next(const Seg &s, int64_t u, int64_t u_end, const int32_t *cum, int Hkv) {
+  Seg n;
+  n.b = s.b;
+  n.h = s.h + 1;
+  if (n.h == Hkv) {
+    n.h = 0;
+    do ++n.b; while (cum[n.b + 1] == cum[n.b]);
+  }
+  const int nb = cum[n.b + 1] - cum[n.b];
+  const int64_t left = u_end - u;
+  n.t0 = 0;
+  n.t1 = left < nb ? static_cast<int>(left) : nb;
+  return n;
+}
+
 // Shares: CTA c owns units [floor(c W / NC), floor((c+1) W / NC)); with W >= NC
 // every share is non-empty.  owner_of(u) = the CTA whose share holds unit u.
 __device__ __forceinline__ int64_t share_begin(int64_t c, int64_t W, int64_t NC) { return c * W / NC; }
@@ -221,8 +239,8 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
   int slot_l = 0;     // ring position of the group's next tile
   uint32_t fill = 0;  // fills of that slot so far
   int ibase = 0;      // CTA-local index of the segment's first tile
-  for (int64_t u = u0; u < u1;) {
-    const Seg s = seg_at(u, u1, cum, a.B, Hkv);
+  Seg s = u0 < u1 ? seg_at(u0, u1, cum, a.B, Hkv) : Seg{0, 0, 0, 0};
+  for (int64_t u = u0; u < u1; s = u < u1 ? seg_next(s, u, u1, cum, Hkv) : s) {
     const int ntiles = s.t1 - s.t0;
     const int kfirst = (grp - ibase % kGroups + kGroups) % kGroups;  // this group's first tile here
     if (kfirst < ntiles) {
@@ -389,8 +407,8 @@ __device__ int query_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uin
   uint8_t *sfb = smem + C::oSfb;
   float *cs = reinterpret_cast<float *>(smem + C::oCs);
   int sidx = 0;
-  for (int64_t u = u0; u < u1; ++sidx) {
-    const Seg s = seg_at(u, u1, cum, a.B, a.c.Hkv);
+  Seg s = u0 < u1 ? seg_at(u0, u1, cum, a.B, a.c.Hkv) : Seg{0, 0, 0, 0};
+  for (int64_t u = u0; u < u1; ++sidx, s = u < u1 ? seg_next(s, u, u1, cum, a.c.Hkv) : s) {
     const int q = sidx % kQBufs;
     if (sidx >= kQBufs && !warp_wait(&qfree[q], static_cast<uint32_t>(sidx / kQBufs - 1) & 1u, abort)) return sidx;
     prepare_query<PREC, NH>(a, s, qimg + q * C::kQImg, sfb + q * 1024, cs + q * 8, kscale);
@@ -626,6 +644,7 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
   __half *pt = reinterpret_cast<__half *>(smem + C::oPt) + warp * NH * 32;
   float *mrg_o = reinterpret_cast<float *>(smem + C::oMrgO);
   float *mrg_ml = reinterpret_cast<float *>(smem + C::oMrgMl);
+  float *mrg_hd = reinterpret_cast<float *>(smem + C::oMrgHd);
   const float vscale = a.c.scale[1];
   const uint32_t tq = tmem + (static_cast<uint32_t>(32 * qd) << 16);  // this warp's lane quadrant
   // The group's tiles are i = grp, grp + 3, ... (CTA-local); its n-th tile
@@ -650,8 +669,8 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
   }
   // After a timeout (ok false) the warps skip all work but keep walking the
   // same segments, so every named barrier of the merge still meets.
-  for (int64_t u = u0; u < u1; ++sidx) {
-    const Seg s = seg_at(u, u1, cum, a.B, Hkv);
+  Seg s = u0 < u1 ? seg_at(u0, u1, cum, a.B, Hkv) : Seg{0, 0, 0, 0};
+  for (int64_t u = u0; u < u1; ++sidx, s = u < u1 ? seg_next(s, u, u1, cum, Hkv) : s) {
     const int Lb = clamped_len(a, s.b);
     const int qb = sidx % kQBufs;
     ok = ok && warp_wait(&qready[qb], static_cast<uint32_t>(sidx / kQBufs) & 1u, abort);
@@ -845,26 +864,35 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
         }
       }
       named_bar_sync(1, kConsumerWarps * 32);
+      if (tid < C::kMH && hp + tid < G) {  // per head: M, the warps' factors 2^(m_w - M) (over m_w), l
+        const int hd = hp + tid;
+        float M = kNoMax;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg_ml[(w * kMaxGroup + hd) * 2]);
+        float lsum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float f = ex2(mrg_ml[(w * kMaxGroup + hd) * 2] - M);  // warps without tokens: 0
+          lsum += f * mrg_ml[(w * kMaxGroup + hd) * 2 + 1];
+          mrg_ml[(w * kMaxGroup + hd) * 2] = f;
+        }
+        mrg_hd[2 * hd] = M;
+        mrg_hd[2 * hd + 1] = lsum;
+      }
+      named_bar_sync(1, kConsumerWarps * 32);
       for (int e2 = tid; e2 < C::kMH * kD; e2 += kConsumerWarps * 32) {
         const int e = e2 / kD, d = e2 % kD, hd = hp + e;
         if (hd < G) {
-          float M = -INFINITY;
+          float o = 0.0f;
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg_ml[(w * kMaxGroup + hd) * 2]);
-          float o = 0.0f, lsum = 0.0f;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            const float mw = mrg_ml[(w * kMaxGroup + hd) * 2];
-            const float f = (mw == -INFINITY) ? 0.0f : ex2(mw - M);
-            o += f * mrg_o[(w * C::kMH + e) * kD + d];
-            lsum += f * mrg_ml[(w * kMaxGroup + hd) * 2 + 1];
-          }
+          for (int w = 0; w < kConsumerWarps; ++w) o += mrg_ml[(w * kMaxGroup + hd) * 2] * mrg_o[(w * C::kMH + e) * kD + d];
+          const float lsum = mrg_hd[2 * hd + 1];
           if (complete) {
             a.out[(static_cast<int64_t>(s.b) * a.Hq + s.h * G + hd) * kD + d] = __float2bfloat16_rn(o * (vscale / lsum));
           } else {
             part[hd * kD + d] = o;
             if (d == 0) {
-              part[kMaxGroup * kD + hd] = M;
+              part[kMaxGroup * kD + hd] = mrg_hd[2 * hd];
               part[kMaxGroup * kD + kMaxGroup + hd] = lsum;
             }
           }
