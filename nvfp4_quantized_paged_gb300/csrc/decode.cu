@@ -115,6 +115,9 @@ struct Cfg {
     return static_cast<uint32_t>(i / kGroups / kStagesG);
   }
   static constexpr int kMH = kNv ? 4 : (NH == 8 ? 1 : 2);  // heads per pass of the segment merge
+  // NVFP4 at four heads: the consumers leave a segment's (m, l, O) in shared
+  // memory and go on; the query warp merges it (one pass holds every head)
+  static constexpr bool kAsyncMerge = kNv && NH == 4;
   static constexpr int kQRow = P::kKRow;                                 // B row bytes
   static constexpr int kQImg = N * kQRow;                                // one query image
   static constexpr int kQSbo = 8 * kQRow;                                // 8-row group stride of B
@@ -138,8 +141,9 @@ struct Cfg {
   static constexpr int oMrgMl = oMrgO + kConsumerWarps * kMH * kD * 4;     // [12 warps][8][2] f32
   static constexpr int oMrgHd = oMrgMl + kConsumerWarps * kMaxGroup * 2 * 4;  // [8][M, l] f32 per head
   static constexpr int oCum = oMrgHd + kMaxGroup * 2 * 4;                     // [kMaxBatch + 1] i32
-  static constexpr int oBars = (oCum + (kMaxBatch + 1) * 4 + 15) / 16 * 16;
-  static constexpr int kBars = 2 * kStages + kGroups + 2 * kQBufs;  // full, empty, sready, qready, qfree
+  static constexpr int oLast = oCum + (kMaxBatch + 1) * 4;                // [kMaxBatch] u8
+  static constexpr int oBars = (oLast + kMaxBatch + 15) / 16 * 16;
+  static constexpr int kBars = 2 * kStages + kGroups + 2 * kQBufs + 1;  // full, empty, sready, qready, qfree, mdone
   static constexpr int oFlags = oBars + kBars * 8;  // tmem holder, abort, fills[kStages], W, NC, u0, u1
   static constexpr int kSmem = oFlags + 4 * (6 + kStages);
 };
@@ -208,10 +212,11 @@ __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t W, int64_t NC) {
   return ((u + 1) * NC + W - 1) / W - 1;
 }
 
-__device__ __forceinline__ int clamped_len(const DecodeArgs &a, int b) {
-  const int64_t cap = static_cast<int64_t>(a.max_pages) * a.c.P;
-  const int64_t L = a.seq_lens[b];
-  return static_cast<int>(L < 0 ? 0 : (L > cap ? cap : L));
+// Visible tokens of sequence b, from the set-up's shared-memory copies: its
+// tile count and the tokens in its last tile (the clamped seq_lens[b]).
+__device__ __forceinline__ int seq_len_of(const int32_t *cum, int b) {
+  const int nb = cum[b + 1] - cum[b];
+  return nb > 0 ? (nb - 1) * kTile + reinterpret_cast<const uint8_t *>(cum + kMaxBatch + 1)[b] : 0;
 }
 
 // Wait for `parity` of `bar`; false (warp-uniform) after a timeout or abort.
@@ -244,7 +249,7 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
     const int ntiles = s.t1 - s.t0;
     const int kfirst = (grp - ibase % kGroups + kGroups) % kGroups;  // this group's first tile here
     if (kfirst < ntiles) {
-      const int len = clamped_len(a, s.b);
+      const int len = seq_len_of(cum, s.b);
       const int32_t *brow = a.block_table + static_cast<int64_t>(s.b) * a.max_pages;
       const uint8_t *src_h = a.c.data + a.c.block(0, s.h, C::P::kTokBytes);  // page 0 of head h
       const int64_t page_stride = a.c.block(1, 0, C::P::kTokBytes) - a.c.block(0, 0, C::P::kTokBytes);
@@ -398,35 +403,118 @@ __device__ void prepare_query(const DecodeArgs &a, const Seg &s, uint8_t *img, u
 // qready[q] completes when the image, its scale factors in TMEM (NVFP4: two
 // tcgen05.cp copies, tracked by a commit) and its score factors are in place.
 // ---------------------------------------------------------------------------
+// Merge of one segment by the query warp (async merge): the twelve consumer
+// warps left their (m, l) in mrg_ml and O of every head in mrg_o.  Per head:
+// M = max_w m_w, factors f_w = 2^(m_w - M) (over m_w in place), l = sum f_w
+// l_w; then O = sum_w f_w O_w goes to the output (the CTA held all of (b, h))
+// or to the CTA's partial slot for the merge kernel.
+template <int PREC, int NH>
+__device__ void merge_segment(const DecodeArgs &a, uint8_t *smem, const int32_t *cum, const Seg &s, int slot_id,
+                              int64_t W, int64_t NC) {
+  using C = Cfg<PREC, NH>;
+  const int lane = threadIdx.x & 31;
+  const int G = a.G, Hkv = a.c.Hkv;
+  const float *mrg_o = reinterpret_cast<const float *>(smem + C::oMrgO);
+  float *mrg_ml = reinterpret_cast<float *>(smem + C::oMrgMl);
+  float *mrg_hd = reinterpret_cast<float *>(smem + C::oMrgHd);
+  const int nb = cum[s.b + 1] - cum[s.b];
+  const bool complete = (s.t0 == 0) && (s.t1 == nb);
+  if (lane < G) {
+    const int hd = lane;
+    float M = kNoMax;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg_ml[(w * kMaxGroup + hd) * 2]);
+    float lsum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float f = ex2(mrg_ml[(w * kMaxGroup + hd) * 2] - M);  // warps without tokens: 0
+      lsum += f * mrg_ml[(w * kMaxGroup + hd) * 2 + 1];
+      mrg_ml[(w * kMaxGroup + hd) * 2] = f;
+    }
+    mrg_hd[2 * hd] = M;
+    mrg_hd[2 * hd + 1] = lsum;
+  }
+  __syncwarp();
+  const float vscale = a.c.scale[1];
+  float *part = a.partials + (static_cast<int64_t>(blockIdx.x) * 2 + slot_id) * kSlotFloats;
+  for (int e2 = lane; e2 < G * kD; e2 += 32) {
+    const int hd = e2 / kD, d = e2 % kD;
+    float o = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) o += mrg_ml[(w * kMaxGroup + hd) * 2] * mrg_o[(w * C::kMH + hd) * kD + d];
+    const float lsum = mrg_hd[2 * hd + 1];
+    if (complete) {
+      a.out[(static_cast<int64_t>(s.b) * a.Hq + s.h * G + hd) * kD + d] = __float2bfloat16_rn(o * (vscale / lsum));
+    } else {
+      part[hd * kD + d] = o;
+      if (d == 0) {
+        part[kMaxGroup * kD + hd] = mrg_hd[2 * hd];
+        part[kMaxGroup * kD + kMaxGroup + hd] = lsum;
+      }
+    }
+  }
+  if (lane == 0 && s.t0 == 0) {  // merge record of (b, h), as in the consumers' merge
+    int2 info = make_int2(0, 1);
+    if (!complete) {
+      const int64_t ubh0 = static_cast<int64_t>(cum[s.b]) * Hkv + static_cast<int64_t>(s.h) * nb;
+      info.x = static_cast<int>(blockIdx.x) * 2 + slot_id;
+      info.y = static_cast<int>(owner_of(ubh0 + nb - 1, W, NC) - blockIdx.x + 1);
+    }
+    a.unit_info[s.b * Hkv + s.h] = info;
+  }
+  __syncwarp();
+}
+
+// The query warp: prepares each segment's query image (at most kQBufs
+// segments ahead of the consumers) and, with the async merge, merges each
+// segment the consumers have finished, in order, but the share's last.
 template <int PREC, int NH>
 __device__ int query_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uint64_t *qready, uint64_t *qfree,
-                          const int32_t *cum, int64_t u0, int64_t u1, volatile int *abort, float kscale) {
+                          uint64_t *mdone, const int32_t *cum, int64_t u0, int64_t u1, int64_t W, int64_t NC,
+                          volatile int *abort, float kscale) {
   using C = Cfg<PREC, NH>;
   const int lane = threadIdx.x & 31;
   uint8_t *qimg = smem + C::oQImg;
   uint8_t *sfb = smem + C::oSfb;
   float *cs = reinterpret_cast<float *>(smem + C::oCs);
-  int sidx = 0;
-  Seg s = u0 < u1 ? seg_at(u0, u1, cum, a.B, a.c.Hkv) : Seg{0, 0, 0, 0};
-  for (int64_t u = u0; u < u1; ++sidx, s = u < u1 ? seg_next(s, u, u1, cum, a.c.Hkv) : s) {
-    const int q = sidx % kQBufs;
-    if (sidx >= kQBufs && !warp_wait(&qfree[q], static_cast<uint32_t>(sidx / kQBufs - 1) & 1u, abort)) return sidx;
-    prepare_query<PREC, NH>(a, s, qimg + q * C::kQImg, sfb + q * 1024, cs + q * 8, kscale);
-    if (lane == 0) {
-      if constexpr (C::kNv) {
-        tc_fence_after();
-        tmem_cp_32x128b_x4(tmem + C::sfb_col(q, 0), umma_desc(smem_u32(sfb + q * 1024), 128, 128));
-        tmem_cp_32x128b_x4(tmem + C::sfb_col(q, 1), umma_desc(smem_u32(sfb + q * 1024 + 512), 128, 128));
-        umma_commit(&qready[q]);  // arrives when the copies are done
-      } else {
-        mbar_arrive(&qready[q]);
+  if (u0 >= u1) return 0;
+  int sp = 0, sm = 0;  // images prepared, segments merged
+  Seg s_p = seg_at(u0, u1, cum, a.B, a.c.Hkv), s_m = s_p;
+  int64_t u_p = u0, u_m = u0;
+  for (;;) {
+    if (u_p < u1 && (!C::kAsyncMerge || sp < sm + kQBufs)) {
+      const int q = sp % kQBufs;
+      if (sp >= kQBufs && !warp_wait(&qfree[q], static_cast<uint32_t>(sp / kQBufs - 1) & 1u, abort)) return sp;
+      prepare_query<PREC, NH>(a, s_p, qimg + q * C::kQImg, sfb + q * 1024, cs + q * 8, kscale);
+      if (lane == 0) {
+        if constexpr (C::kNv) {
+          tc_fence_after();
+          tmem_cp_32x128b_x4(tmem + C::sfb_col(q, 0), umma_desc(smem_u32(sfb + q * 1024), 128, 128));
+          tmem_cp_32x128b_x4(tmem + C::sfb_col(q, 1), umma_desc(smem_u32(sfb + q * 1024 + 512), 128, 128));
+          umma_commit(&qready[q]);  // arrives when the copies are done
+        } else {
+          mbar_arrive(&qready[q]);
+        }
+        mbar_arrive(&qready[q]);    // the image and score factors (release)
       }
-      mbar_arrive(&qready[q]);    // the image and score factors (release)
+      __syncwarp();
+      u_p += s_p.t1 - s_p.t0;
+      ++sp;
+      if (u_p < u1) s_p = seg_next(s_p, u_p, u1, cum, a.c.Hkv);
+    } else if (C::kAsyncMerge && u_m + (s_m.t1 - s_m.t0) < u1) {  // the last segment: merged by the consumers
+      const int q = sm % kQBufs;
+      if (!warp_wait(&qfree[q], static_cast<uint32_t>(sm / kQBufs) & 1u, abort)) return sp;  // segment sm done
+      merge_segment<PREC, NH>(a, smem, cum, s_m, u_m == u0 ? 0 : 1, W, NC);
+      if (lane == 0) mbar_arrive(mdone);  // its buffers may be rewritten
+      __syncwarp();
+      u_m += s_m.t1 - s_m.t0;
+      ++sm;
+      if (u_m < u1) s_m = seg_next(s_m, u_m, u1, cum, a.c.Hkv);
+    } else {
+      break;
     }
-    __syncwarp();
-    u += s.t1 - s.t0;
   }
-  return sidx;  // images prepared
+  return sp;  // images prepared
 }
 
 // ---------------------------------------------------------------------------
@@ -632,8 +720,9 @@ __device__ __forceinline__ float pick(const float (&v)[NH], int i) {  // v[i] fo
 
 template <int PREC, int NH>
 __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uint64_t *full, uint64_t *empty,
-                              uint64_t *sready, uint64_t *qready, uint64_t *qfree, const int32_t *cum, int64_t u0,
-                              int64_t u1, int64_t W, int64_t NC, volatile int *abort, int64_t &last_issued) {
+                              uint64_t *sready, uint64_t *qready, uint64_t *qfree, uint64_t *mdone, const int32_t *cum,
+                              int64_t u0, int64_t u1, int64_t W, int64_t NC, volatile int *abort,
+                              int64_t &last_issued) {
   using C = Cfg<PREC, NH>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = warp / kGroupWarps, qd = warp % kGroupWarps;  // consumer group, TMEM lane quadrant
@@ -671,7 +760,7 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
   // same segments, so every named barrier of the merge still meets.
   Seg s = u0 < u1 ? seg_at(u0, u1, cum, a.B, Hkv) : Seg{0, 0, 0, 0};
   for (int64_t u = u0; u < u1; ++sidx, s = u < u1 ? seg_next(s, u, u1, cum, Hkv) : s) {
-    const int Lb = clamped_len(a, s.b);
+    const int Lb = seq_len_of(cum, s.b);
     const int qb = sidx % kQBufs;
     ok = ok && warp_wait(&qready[qb], static_cast<uint32_t>(sidx / kQBufs) & 1u, abort);
     float cs[NH], m[NH], mt[NH], l[NH];  // mt = m + the rescale threshold
@@ -821,6 +910,39 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
     }
     ibase += ntiles;
 
+    // the query warp may still be merging the previous segment out of the
+    // merge buffers
+    if (C::kAsyncMerge && sidx > 0) ok = warp_wait(mdone, static_cast<uint32_t>(sidx - 1) & 1u, abort) && ok;
+    if (C::kAsyncMerge && u + ntiles < u1) {
+      // not the share's last segment: leave (m, l, O) for the query warp and
+      // go on (the last segment is merged by all twelve warps, below)
+#pragma unroll
+      for (int h = 0; h < NH; ++h)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l[h] += __shfl_xor_sync(0xffffffffu, l[h], o);
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          mrg_ml[(warp * kMaxGroup + h) * 2 + 0] = m[h];
+          mrg_ml[(warp * kMaxGroup + h) * 2 + 1] = l[h];
+        }
+      }
+#pragma unroll
+      for (int hd = 0; hd < NH; ++hd) {  // the lanes with c = hd / 2 hold head hd in column hd % 2
+        if (hd < G && (hd >> 1) == c) {
+          float *dst = mrg_o + (warp * C::kMH + hd) * kD + 16 * r;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            dst[2 * j] = st.o[j][hd & 1];
+            dst[2 * j + 1] = st.o[j][2 + (hd & 1)];
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qfree[qb]);  // scores read, merge data written
+      u += ntiles;
+      continue;
+    }
     // ---- merge the four warps: (m, l) per head, O per (head, d) ----
 #pragma unroll
     for (int h = 0; h < NH; ++h)
@@ -917,6 +1039,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
   uint64_t *sready = empty + C::kStages;  // score buffer g holds a finished tile
   uint64_t *qready = sready + kGroups;    // query image q, its scale factors and score factors ready
   uint64_t *qfree = qready + kQBufs;      // every consumer warp finished the segment of image q
+  uint64_t *mdone = qfree + kQBufs;       // the query warp merged a segment (async merge)
   int32_t *cum = reinterpret_cast<int32_t *>(smem + C::oCum);
   int *flags = reinterpret_cast<int *>(smem + C::oFlags);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(flags);
@@ -942,6 +1065,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
       mbar_init(&qready[q], 2);  // TMEM copies done + image written
       mbar_init(&qfree[q], kConsumerWarps);
     }
+    {
+      mbar_init(mdone, 1);
+    }
     fence_mbar_init();
   }
   if (warp == kQueryWarp) tmem_alloc(tmem_holder, C::kTmemCols);
@@ -962,6 +1088,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
           Lb = Lb < 0 ? 0 : cap;
         }
         n = static_cast<int>((Lb + kTile - 1) / kTile);
+        reinterpret_cast<uint8_t *>(cum + kMaxBatch + 1)[b] = static_cast<uint8_t>(Lb - (n > 0 ? (n - 1) * kTile : 0));
       }
       int incl = n;
 #pragma unroll
@@ -1007,9 +1134,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     producer<PREC, NH>(a, smem + C::oRing, full, empty, cum, u0, u1, warp - kProducerWarp, abort, fills);
   } else if (warp == kQueryWarp) {
     const float kscale = __fmul_rn(a.c.scale[0], a.sm_scale * 1.4426950408889634f);
-    last_issued = query_role<PREC, NH>(a, smem, tmem, qready, qfree, cum, u0, u1, abort, kscale);
+    last_issued = query_role<PREC, NH>(a, smem, tmem, qready, qfree, mdone, cum, u0, u1, W, NC, abort, kscale);
   } else {
-    consumer_role<PREC, NH>(a, smem, tmem, full, empty, sready, qready, qfree, cum, u0, u1, W, NC, abort, last_issued);
+    consumer_role<PREC, NH>(a, smem, tmem, full, empty, sready, qready, qfree, mdone, cum, u0, u1, W, NC, abort,
+                            last_issued);
   }
 
   // this CTA's partials are written: the combine grid may start launching
