@@ -82,6 +82,12 @@ def lib():
         L.orc_dequant_to_fp8_workspace.argtypes = [_i32p, ctypes.c_int, _i32p, _i32p, _i64p, ctypes.c_int,
                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                                    _u8p, _f32p, _f32p, _u8p, _u8p]
+        L.orc_fp8_workspace_append.restype = ctypes.c_int
+        L.orc_fp8_workspace_append.argtypes = [_f32p, _f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _i64p,
+                                               _f32p, ctypes.c_int64, _u8p, _u8p]
+        L.orc_fp8_extend_attention.restype = ctypes.c_int
+        L.orc_fp8_extend_attention.argtypes = [_u16p, _i64p, _u8p, _u8p, _i64p, _i32p, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, _f32p, ctypes.c_double, _f64p]
         _LIB = L
     return _LIB
 
@@ -316,3 +322,54 @@ def dequant_to_fp8_workspace(cache: Cache, block_table: np.ndarray, seq_ids, pre
     if rc != 0:
         raise ValueError("bad arguments")
     return wk, wv
+
+
+def fp8_workspace_append(ws_k: np.ndarray, ws_v: np.ndarray, k: np.ndarray, v: np.ndarray, rows: np.ndarray,
+                         ws_scale) -> None:
+    """The current chunk's K/V into FP8 workspace rows ([P2] Three Paths: the
+    prefix is "concatenated with the current chunk's KV for FP8 attention").
+
+    ``k``, ``v``: [T, Hkv, D] (FP32 or BF16-exact values); token t goes to row
+    ``rows[t]`` (negative: skipped) as E4M3_RNE_sat(x / ws_scale) per tensor.
+    ``ws_k`` / ``ws_v`` (uint8 [rows, Hkv, D]) are updated in place.
+    """
+    T, Hkv, D = k.shape
+    kk = _c(k, np.float32)
+    vv = _c(v, np.float32)
+    r = _c(rows, np.int64)
+    ws = _c(ws_scale, np.float32).reshape(2)
+    assert ws_k.flags.c_contiguous and ws_v.flags.c_contiguous and ws_k.dtype == np.uint8
+    rc = lib().orc_fp8_workspace_append(_p(kk, _f32p), _p(vv, _f32p), T, Hkv, D, _p(r, _i64p), _p(ws, _f32p),
+                                        ws_k.shape[0], _p(ws_k, _u8p), _p(ws_v, _u8p))
+    if rc != 0:
+        raise ValueError("bad row or scale")
+
+
+def fp8_extend_attention(q_bf16_bits: np.ndarray, cu_q, ws_k: np.ndarray, ws_v: np.ndarray, cu_kv, kv_lens,
+                         ws_scale, sm_scale: float = 0.0) -> np.ndarray:
+    """Chunked-extend attention over the FP8 workspace in FP64 ([P2] Three
+    Paths, chunked prefill / extend).
+
+    Sequence i's keys and values are workspace rows [cu_kv[i], cu_kv[i] +
+    kv_lens[i]) (prefix, then the chunk); its queries ``q_bf16_bits[cu_q[i]:
+    cu_q[i+1]]`` (uint16 BF16 bits, [Tq, Hq, D]) are the last positions of the
+    sequence and see every position up to their own.  Returns FP64 [Tq, Hq, D].
+    """
+    q = _c(q_bf16_bits, np.uint16)
+    Tq, Hq, D = q.shape
+    Hkv = ws_k.shape[1]
+    cq = _c(cu_q, np.int64)
+    ck = _c(cu_kv, np.int64)
+    kl = _c(kv_lens, np.int32)
+    ws = _c(ws_scale, np.float32).reshape(2)
+    wk = _c(ws_k, np.uint8)
+    wv = _c(ws_v, np.uint8)
+    if sm_scale == 0.0:
+        sm_scale = 1.0 / np.sqrt(D)
+    out = np.zeros((Tq, Hq, D), np.float64)
+    rc = lib().orc_fp8_extend_attention(_p(q, _u16p), _p(cq, _i64p), _p(wk, _u8p), _p(wv, _u8p), _p(ck, _i64p),
+                                        _p(kl, _i32p), len(kl), Hq, Hkv, D, _p(ws, _f32p), float(sm_scale),
+                                        _p(out, _f64p))
+    if rc != 0:
+        raise ValueError("bad arguments")
+    return out

@@ -53,7 +53,9 @@
  *
  * Parity pins (tests, not here): the E2M1 code table, brute-force nearest-value
  * rounding over every FP32 bit pattern, the 9-byte ledger, exact round trips,
- * brute-force dense attention and the split / log-sum-exp merge identity.
+ * brute-force dense attention and the split / log-sum-exp merge identity; for
+ * the chunked extend, a dense causal brute force, closed forms, causality and
+ * the decode attention over an FP8 cache holding the same bytes.
  */
 #include <math.h>
 #include <stdint.h>
@@ -505,6 +507,87 @@ int orc_dequant_to_fp8_workspace(const int32_t *block_table, int max_pages, cons
         }
       }
     }
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The current chunk joins the FP8 workspace ([P2] Three Paths: the prefix in */
+/* the shared FP8 workspace is "concatenated with the current chunk's KV for  */
+/* FP8 attention").  The pages give no rule for the chunk's FP8 bytes; the    */
+/* plainest reading is the per-tensor FP8 quantizer of the FP8 layers with    */
+/* the workspace scale: byte = E4M3_RNE_sat(x / ws_scale) (FP32 divide).      */
+/* Token t of k / v ([T][Hkv][D] FP32) goes to workspace row rows[t]          */
+/* (negative: skipped; >= ws_rows: error).                                    */
+/* ------------------------------------------------------------------------ */
+int orc_fp8_workspace_append(const float *k, const float *v, int64_t T, int Hkv, int D, const int64_t *rows,
+                             const float *ws_scale, int64_t ws_rows, uint8_t *ws_k, uint8_t *ws_v) {
+  int64_t t;
+  int kind;
+  if (!(ws_scale[0] > 0.0f) || !(ws_scale[1] > 0.0f)) return -1;
+  for (t = 0; t < T; ++t) {
+    int64_t r = rows[t];
+    if (r < 0) continue;
+    if (r >= ws_rows) return -1;
+    for (kind = 0; kind < 2; ++kind)
+      fp8_quantize_vector((kind ? v : k) + t * Hkv * D, Hkv * D, ws_scale[kind], (kind ? ws_v : ws_k) + r * Hkv * D);
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Chunked-extend attention over the FP8 workspace ([P2] Three Paths: the     */
+/* chunk's queries attend, in FP8 attention, to the dequantized prefix        */
+/* concatenated with the chunk's own KV).  Sequence i owns workspace rows     */
+/* [cu_kv[i], cu_kv[i] + kv_lens[i]): positions 0 .. kv_lens[i]-1, prefix     */
+/* first, then the chunk.  Its nq = cu_q[i+1] - cu_q[i] queries are the last  */
+/* nq positions: query j sits at position kv_lens[i] - nq + j and sees the    */
+/* positions up to and including its own (causal inside the chunk).  Query   */
+/* head qh reads KV head qh / (Hq / Hkv).  K = E4M3(byte) * ws_scale[0],      */
+/* V = E4M3(byte) * ws_scale[1] (exact in FP64); plain softmax in FP64.      */
+/*   q [Tq][Hq][D] BF16 bits, out [Tq][Hq][D] FP64.                           */
+/* ------------------------------------------------------------------------ */
+int orc_fp8_extend_attention(const uint16_t *q, const int64_t *cu_q, const uint8_t *ws_k, const uint8_t *ws_v,
+                             const int64_t *cu_kv, const int32_t *kv_lens, int n, int Hq, int Hkv, int D,
+                             const float *ws_scale, double sm_scale, double *out) {
+  int i, G;
+  if (Hkv <= 0 || Hq % Hkv != 0) return -1;
+  G = Hq / Hkv;
+  for (i = 0; i < n; ++i) {
+    const int64_t nq = cu_q[i + 1] - cu_q[i];
+    const int L = kv_lens[i];
+    int64_t j;
+    int qh;
+    double *s;
+    if (nq < 0 || nq > L) return -1;
+    s = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    for (j = 0; j < nq; ++j) {
+      const int64_t pos = L - nq + j; /* this query's position; it sees [0, pos] */
+      for (qh = 0; qh < Hq; ++qh) {
+        const int h = qh / G;
+        const uint16_t *qv = q + ((cu_q[i] + j) * Hq + qh) * D;
+        double *o = out + ((cu_q[i] + j) * Hq + qh) * D;
+        double m = -INFINITY, l = 0.0;
+        int64_t t;
+        int d;
+        for (t = 0; t <= pos; ++t) {
+          const uint8_t *kr = ws_k + ((cu_kv[i] + t) * Hkv + h) * D;
+          double acc = 0.0;
+          for (d = 0; d < D; ++d) acc += bf16_bits_to_double(qv[d]) * (orc_e4m3_value(kr[d]) * (double)ws_scale[0]);
+          s[t] = acc * sm_scale;
+          if (s[t] > m) m = s[t];
+        }
+        for (d = 0; d < D; ++d) o[d] = 0.0;
+        for (t = 0; t <= pos; ++t) {
+          const uint8_t *vr = ws_v + ((cu_kv[i] + t) * Hkv + h) * D;
+          const double p = exp(s[t] - m);
+          l += p;
+          for (d = 0; d < D; ++d) o[d] += p * (orc_e4m3_value(vr[d]) * (double)ws_scale[1]);
+        }
+        for (d = 0; d < D; ++d) o[d] /= l;
+      }
+    }
+    free(s);
   }
   return 0;
 }
