@@ -234,6 +234,56 @@ nvkv_status nvfp4_kv_dequant_to_fp8_workspace(const int32_t *block_table, int32_
                                               const float *ws_scale, uint8_t *ws_k, uint8_t *ws_v,
                                               int64_t ws_rows, void *stream);
 
+/* The current chunk's K/V into the shared FP8 workspace ([P2] Three Paths:
+ * the dequantized prefix is "concatenated with the current chunk's KV for FP8
+ * attention").  The pages give no rule for the chunk's bytes; this library
+ * uses the FP8 layers' per-tensor quantizer with the workspace scale:
+ *   byte = E4M3_rne_satfinite(x / ws_scale)          (FP32 divide, per K and V)
+ *   k, v        [num_tokens][num_kv_heads][head_dim] of `dtype`, device,
+ *               16-byte aligned; head_dim a multiple of 16
+ *   rows        [num_tokens] int64 device: the workspace row of each token
+ *               (negative: skipped; >= ws_rows: skipped and
+ *               NVKV_DEVERR_WS_ROWS raised in *err_flag, if given)
+ *   ws_scale    device float[2] {K, V}, > 0 (the scale the prefix dequant used)
+ *   ws_k, ws_v  [ws_rows][num_kv_heads][head_dim] E4M3, device, 16-byte aligned
+ * One kernel on `stream`.  Bytes are identical to the oracle's rule above. */
+nvkv_status fp8_workspace_append_chunk(const void *k, const void *v, nvkv_dtype dtype, int64_t num_tokens,
+                                       const int64_t *rows, int32_t num_kv_heads, int32_t head_dim,
+                                       const float *ws_scale, uint8_t *ws_k, uint8_t *ws_v, int64_t ws_rows,
+                                       int32_t *err_flag, void *stream);
+
+/* Chunked-extend attention over the shared FP8 workspace ([P2] Three Paths:
+ * chunked prefill / extend runs FP8 attention over the dequantized prefix
+ * concatenated with the current chunk).  Sequence i (i < n) owns workspace
+ * rows [cu_kv[i], cu_kv[i] + kv_lens[i]): positions 0 .. kv_lens[i]-1, prefix
+ * first, then the chunk.  Its nq_i = cu_q[i+1] - cu_q[i] queries are the last
+ * nq_i positions: query j sits at position kv_lens[i] - nq_i + j and attends
+ * to positions [0, that position] (causal inside the chunk).  Query head qh
+ * reads KV head qh / (num_q_heads / num_kv_heads).
+ *   out = softmax(sm_scale * q . K) V,  K = E4M3(ws_k) * ws_scale[0],
+ *                                        V = E4M3(ws_v) * ws_scale[1]
+ *   q        [cu_q[n]][num_q_heads][128] BF16, device, 16-byte aligned; used
+ *            at FP16 precision (exact for |q| in [2^-14, 65504])
+ *   cu_q     [n+1] int64 device, non-decreasing; max_q_len (host) >= every
+ *            nq_i (queries beyond it are not computed: NVKV_DEVERR_SEQLEN)
+ *   cu_kv    [n] int64 device; kv_lens [n] int32 device, nq_i <= kv_lens[i]
+ *            and cu_kv[i] + kv_lens[i] <= ws_rows, else the sequence is
+ *            skipped and NVKV_DEVERR_SEQLEN / NVKV_DEVERR_WS_ROWS raised
+ *   ws_k, ws_v  [ws_rows][num_kv_heads][128] E4M3 (finite bytes), device,
+ *            16-byte aligned; ws_scale device float[2] {K, V}
+ *   sm_scale <= 0 -> 1/sqrt(128)
+ *   out      [cu_q[n]][num_q_heads][128] BF16, device, 16-byte aligned
+ *   err_flag optional device int32 (first error code wins)
+ * head_dim must be 128 and num_q_heads / num_kv_heads a power of two <= 128
+ * (else NVKV_ERR_UNSUPPORTED).  QK^T and P.V run on the tensor cores with
+ * FP16 operands (E4M3 converts exactly) and FP32 accumulation; P is rounded
+ * to FP16.  One kernel on `stream`; it allocates nothing. */
+nvkv_status fp8_chunked_extend_attention(const void *q, const int64_t *cu_q, int32_t n, int32_t max_q_len,
+                                         int32_t num_q_heads, const uint8_t *ws_k, const uint8_t *ws_v,
+                                         const int64_t *cu_kv, const int32_t *kv_lens, int32_t num_kv_heads,
+                                         int32_t head_dim, int64_t ws_rows, const float *ws_scale, float sm_scale,
+                                         void *out, int32_t *err_flag, void *stream);
+
 /* Element encoders of the quantizer, one output byte per FP32 input: E2M1
  * code (low nibble, round-to-nearest-even, saturating at 6) and E4M3 byte
  * (round-to-nearest-even, saturating at 448).  x, out: device. */

@@ -11,6 +11,7 @@ Functions keep the C names:
   fp8_kv_quantize_write, nvkv_decode_workspace_size,
   nvkv_decode_workspace_init, nvfp4_paged_decode_attention,
   fp8_paged_decode_attention, nvfp4_kv_dequant_to_fp8_workspace,
+  fp8_workspace_append_chunk, fp8_chunked_extend_attention,
   nvkv_encode_e2m1, nvkv_encode_e4m3.
 ``Cache`` allocates one layer's paged planes with torch and builds the
 ``nvkv_cache`` descriptor.
@@ -88,6 +89,9 @@ SIGNATURES = {
                                                     _vp, _vp]),
     "nvfp4_kv_dequant_to_fp8_workspace": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _cachep, _vp, _vp, _vp, _i64,
                                                  _vp]),
+    "fp8_workspace_append_chunk": (_i32, [_vp, _vp, _i32, _i64, _vp, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp]),
+    "fp8_chunked_extend_attention": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp,
+                                            _f32, _vp, _vp, _vp]),
     "nvkv_encode_e2m1": (_i32, [_vp, _i64, _vp, _vp]),
     "nvkv_encode_e4m3": (_i32, [_vp, _i64, _vp, _vp]),
 }
@@ -270,6 +274,27 @@ def nvfp4_kv_dequant_to_fp8_workspace(block_table, seq_ids, prefix_lens, cu_pref
                                                    _ptr(prefix_lens), _ptr(cu_prefix), seq_ids.numel(),
                                                    ctypes.byref(d), _ptr(ws_scale), _ptr(ws_k), _ptr(ws_v),
                                                    ws_k.shape[0], _stream(stream)))
+
+
+def fp8_workspace_append_chunk(k, v, rows, ws_scale, ws_k, ws_v, err=None, stream=None):
+    """The chunk's K/V ([T, Hkv, D] FP32 or BF16) into workspace rows ``rows``
+    (int64 [T]) as E4M3(x / ws_scale)."""
+    _check("fp8_workspace_append_chunk",
+           lib().fp8_workspace_append_chunk(_ptr(k), _ptr(v), _dtype_code(k), k.shape[0], _ptr(rows), k.shape[1],
+                                            k.shape[2], _ptr(ws_scale), _ptr(ws_k), _ptr(ws_v), ws_k.shape[0],
+                                            _ptr(err), _stream(stream)))
+
+
+def fp8_chunked_extend_attention(q, cu_q, max_q_len, ws_k, ws_v, cu_kv, kv_lens, ws_scale, out, sm_scale=0.0,
+                                 err=None, stream=None):
+    """Causal FP8 attention of the chunk queries ``q`` (BF16 [Tq, Hq, 128],
+    sequence i owns rows cu_q[i]:cu_q[i+1]) over workspace rows
+    [cu_kv[i], cu_kv[i] + kv_lens[i]) (prefix, then the chunk)."""
+    _check("fp8_chunked_extend_attention",
+           lib().fp8_chunked_extend_attention(_ptr(q), _ptr(cu_q), kv_lens.numel(), int(max_q_len), q.shape[1],
+                                              _ptr(ws_k), _ptr(ws_v), _ptr(cu_kv), _ptr(kv_lens), ws_k.shape[1],
+                                              q.shape[2], ws_k.shape[0], _ptr(ws_scale), sm_scale, _ptr(out),
+                                              _ptr(err), _stream(stream)))
 
 
 def nvkv_encode_e2m1(x, out, stream=None):

@@ -330,6 +330,20 @@ __device__ __forceinline__ void umma_e4m3(uint32_t d, uint64_t a, uint64_t b, ui
       : "memory");
 }
 
+// kind::f16 with FP16 x FP16 operands, FP32 accumulator, M = 128, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+// D[128 x n] (+)= A * B with FP16 operands (K = 16 per instruction).
+__device__ __forceinline__ void umma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p;\n\t setp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation this thread issued has completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -363,6 +377,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&x)[16]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(v[i]);
+}
+
+// 16 consecutive 32-bit columns of this warp's 32 TMEM lanes (one row per
+// lane); the caller waits with tmem_st_wait() before the columns are read.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&x)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(x[0])), "r"(__float_as_uint(x[1])), "r"(__float_as_uint(x[2])), "r"(__float_as_uint(x[3])),
+      "r"(__float_as_uint(x[4])), "r"(__float_as_uint(x[5])), "r"(__float_as_uint(x[6])), "r"(__float_as_uint(x[7])),
+      "r"(__float_as_uint(x[8])), "r"(__float_as_uint(x[9])), "r"(__float_as_uint(x[10])), "r"(__float_as_uint(x[11])),
+      "r"(__float_as_uint(x[12])), "r"(__float_as_uint(x[13])), "r"(__float_as_uint(x[14])), "r"(__float_as_uint(x[15]))
+      : "memory");
 }
 
 }  // namespace nvkv
