@@ -101,7 +101,7 @@ struct Tile {            // the CTA's work item, uniform over the CTA
 // phase (dc = 0..7, one rb) write eight different rows of their core
 // matrices: no shared-memory bank conflicts.
 // ---------------------------------------------------------------------------
-__device__ void x_converter(const ExtendArgs &a, const Tile &t, uint8_t *smem, uint64_t *kv_full,
+__device__ __forceinline__ void x_converter(const ExtendArgs &a, const Tile &t, uint8_t *smem, uint64_t *kv_full,
                             uint64_t *pv_done, volatile int *abort) {
   const int ct = static_cast<int>(threadIdx.x) - 128;
   const int rb = ct >> 3, dc = ct & 7;
@@ -189,7 +189,7 @@ __device__ void x_converter(const ExtendArgs &a, const Tile &t, uint8_t *smem, u
 // ---------------------------------------------------------------------------
 // Softmax (warps 0-3): thread r owns TMEM lane r = query row r.
 // ---------------------------------------------------------------------------
-__device__ void x_softmax(const ExtendArgs &a, const Tile &t, uint8_t *smem, uint32_t tmem, uint64_t *s_full,
+__device__ __forceinline__ void x_softmax(const ExtendArgs &a, const Tile &t, uint8_t *smem, uint32_t tmem, uint64_t *s_full,
                           uint64_t *s_free, uint64_t *p_full, uint64_t *pv_done, volatile int *abort) {
   const int r = static_cast<int>(threadIdx.x), warp = r >> 5;
   const int tok = r >> a.lgG, g = r & (a.G - 1);
@@ -204,18 +204,32 @@ __device__ void x_softmax(const ExtendArgs &a, const Tile &t, uint8_t *smem, uin
     ok = warp_wait_x(&s_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort);
     if (!ok) break;
     tc_fence_after();
+    // the row's 128 scores: eight loads in flight, one wait
     const uint32_t sadr = lanes + static_cast<uint32_t>(b * 128);
-    const int lim = qpos - kv0;                             // columns c <= lim are visible
-    const bool diag = kv0 + kXRows - 1 > first_partial;    // some row sees only part of the tile
-    float mx = -INFINITY;
+    uint32_t v[8][16];
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-      float x[16];
-      tmem_ld16(sadr + 16 * ch, x);
+    for (int ch = 0; ch < 8; ++ch) tmem_ld16_async(sadr + 16 * ch, v[ch]);
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-      for (int e = 0; e < 16; ++e) mx = fmaxf(mx, (diag && 16 * ch + e > lim) ? -INFINITY : x[e]);
+    for (int ch = 0; ch < 8; ++ch)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) asm volatile("" : "+r"(v[ch][e]));
+    tc_fence_before();
+    mbar_arrive(&s_free[b]);  // the score buffer may take the next-but-one tile
+    if (kv0 + kXRows - 1 > first_partial) {  // a diagonal tile (uniform): mask columns past the row's position
+      const int lim = qpos - kv0;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          if (16 * ch + e > lim) v[ch][e] = __float_as_uint(-INFINITY);
     }
-    const float mx2 = mx * c2;
+    float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+#pragma unroll
+      for (int e = 0; e < 16; ++e) mq[e & 3] = fmaxf(mq[e & 3], __uint_as_float(v[ch][e]));
+    const float mx2 = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * c2;
     float alpha = 1.0f;
     const bool need = mx2 > mt;
     if (need) {
@@ -224,24 +238,20 @@ __device__ void x_softmax(const ExtendArgs &a, const Tile &t, uint8_t *smem, uin
       mt = mx2 + kXRescale;
       l *= alpha;
     }
+    const float nm = -m;
+    float la[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     uint32_t pk[64];
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-      float x[16];
-      tmem_ld16(sadr + 16 * ch, x);
+    for (int ch = 0; ch < 8; ++ch)
 #pragma unroll
       for (int e = 0; e < 16; e += 2) {
-        float p0 = ex2(fmaf(x[e], c2, -m)), p1 = ex2(fmaf(x[e + 1], c2, -m));
-        if (diag) {
-          p0 = 16 * ch + e > lim ? 0.0f : p0;
-          p1 = 16 * ch + e + 1 > lim ? 0.0f : p1;
-        }
-        l += p0 + p1;
+        float a0, a1;
+        fma_f32x2(a0, a1, __uint_as_float(v[ch][e]), __uint_as_float(v[ch][e + 1]), c2, c2, nm, nm);
+        const float p0 = ex2(a0), p1 = ex2(a1);  // masked: exp2(-inf) = 0
+        add_f32x2(la[(e >> 1) & 2], la[((e >> 1) & 2) + 1], p0, p1);
         pk[8 * ch + e / 2] = pack_f16x2(p0, p1);
       }
-    }
-    tc_fence_before();
-    mbar_arrive(&s_free[b]);  // this tile's scores are read
+    l += (la[0] + la[1]) + (la[2] + la[3]);
     // P and the output are free once the previous tile's P.V is done
     if (j >= 1) {
       ok = warp_wait_x(&pv_done[(j - 1) & 1], static_cast<uint32_t>((j - 1) >> 1) & 1u, abort);
@@ -294,42 +304,57 @@ __device__ void x_softmax(const ExtendArgs &a, const Tile &t, uint8_t *smem, uin
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer (one thread of warp 8): S_b = Q K_b^T as soon as K_b is staged and
-// S_b's previous scores are read; O += P V_b once P is written.  QK^T of the
-// next tile goes out before P.V of this one, so it runs during this softmax.
+// MMA issuer (one thread of warp 8), polling: S_b = Q K_b^T as soon as K_b is
+// staged and S_b's previous scores are read (at most one tile ahead of P.V,
+// so the next tile's scores are computed during this tile's softmax);
+// O += P V_b as soon as P is written.
 // ---------------------------------------------------------------------------
-__device__ void x_issuer(uint8_t *smem, uint32_t tmem, int ntiles, uint64_t *kv_full, uint64_t *s_full,
+__device__ __forceinline__ void x_issuer(uint8_t *smem, uint32_t tmem, int ntiles, uint64_t *kv_full, uint64_t *s_full,
                          uint64_t *s_free, uint64_t *p_full, uint64_t *pv_done, volatile int *abort) {
   const uint32_t qs = smem_u32(smem + oXQ), ps = smem_u32(smem + oXP);
   constexpr uint32_t id = idesc_f16(kXRows);
-  auto qk = [&](int j) -> bool {
-    const int b = j & 1;
-    if (!mbar_wait_bounded(&kv_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort)) return false;
-    if (j >= 2 && !mbar_wait_bounded(&s_free[b], static_cast<uint32_t>((j - 2) >> 1) & 1u, abort)) return false;
-    tc_fence_after();
-    const uint32_t ks = smem_u32(smem + oXK + b * kXTile);
+  int nqk = 0, npv = 0;  // next tile whose QK^T / P.V goes out
+  uint64_t t_last = global_timer_ns();
+  while (npv < ntiles) {
+    bool did = false;
+    // QK^T of tile nqk: K staged, and its score buffer read by the softmax of tile nqk - 2
+    if (nqk < ntiles && nqk <= npv + 1) {
+      const int b = nqk & 1;
+      if (mbar_test(&kv_full[b], static_cast<uint32_t>(nqk >> 1) & 1u) &&
+          (nqk < 2 || mbar_test(&s_free[b], static_cast<uint32_t>((nqk - 2) >> 1) & 1u))) {
+        tc_fence_after();
+        const uint32_t ks = smem_u32(smem + oXK + b * kXTile);
 #pragma unroll
-    for (int kk = 0; kk < kXD / 16; ++kk)
-      umma_f16(tmem + static_cast<uint32_t>(b * 128), umma_desc(qs + kk * 256, 128, kXSbo),
-               umma_desc(ks + kk * 256, 128, kXSbo), id, kk > 0 ? 1u : 0u);
-    umma_commit(&s_full[b]);
-    return true;
-  };
-  auto pv = [&](int j) -> bool {
-    if (!mbar_wait_bounded(p_full, static_cast<uint32_t>(j) & 1u, abort)) return false;
-    tc_fence_after();
-    const uint32_t vt = smem_u32(smem + oXV + (j & 1) * kXTile);
+        for (int kk = 0; kk < kXD / 16; ++kk)
+          umma_f16(tmem + static_cast<uint32_t>(b * 128), umma_desc(qs + kk * 256, 128, kXSbo),
+                   umma_desc(ks + kk * 256, 128, kXSbo), id, kk > 0 ? 1u : 0u);
+        umma_commit(&s_full[b]);
+        ++nqk;
+        did = true;
+      }
+    }
+    // P.V of tile npv once its P is written
+    if (npv < nqk && mbar_test(p_full, static_cast<uint32_t>(npv) & 1u)) {
+      tc_fence_after();
+      const uint32_t vt = smem_u32(smem + oXV + (npv & 1) * kXTile);
 #pragma unroll
-    for (int kk = 0; kk < kXRows / 16; ++kk)
-      umma_f16(tmem + kXColO, umma_desc(ps + kk * 256, 128, kXSbo), umma_desc(vt + kk * 256, 128, kXSbo), id,
-               (j > 0 || kk > 0) ? 1u : 0u);
-    umma_commit(&pv_done[j & 1]);
-    return true;
-  };
-  bool ok = qk(0);
-  for (int j = 0; ok && j < ntiles; ++j) {
-    if (j + 1 < ntiles) ok = qk(j + 1);
-    ok = ok && pv(j);
+      for (int kk = 0; kk < kXRows / 16; ++kk)
+        umma_f16(tmem + kXColO, umma_desc(ps + kk * 256, 128, kXSbo), umma_desc(vt + kk * 256, 128, kXSbo), id,
+                 (npv > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(&pv_done[npv & 1]);
+      ++npv;
+      did = true;
+    }
+    if (did) {
+      t_last = global_timer_ns();
+    } else {
+      if (*abort) return;
+      if (global_timer_ns() - t_last > 2000000000ull) {  // no progress for 2 s
+        *abort = 1;
+        return;
+      }
+      __nanosleep(20);
+    }
   }
 }
 

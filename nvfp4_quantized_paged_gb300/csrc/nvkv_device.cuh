@@ -379,6 +379,40 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&x)[16]) {
   for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(v[i]);
 }
 
+// 16 consecutive FP32 columns of this warp's 32 TMEM lanes without waiting:
+// the registers may be read only after tmem_ld_wait() on the same values.
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Wait for this thread's TMEM loads, then pass each loaded register through
+// an empty statement ordered after the wait, so no use of it can be
+// scheduled before the data is there.
+template <int N>
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&v)[N]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(v[i]));
+}
+
+// (a0, a1) * (b0, b1) + (c0, c1) as one packed FP32x2 fused multiply-add.
+__device__ __forceinline__ void fma_f32x2(float &d0, float &d1, float a0, float a1, float b0, float b1, float c0,
+                                          float c1) {
+  asm("{ .reg .b64 a, b, c;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %5};\n\t"
+      "mov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 a, a, b, c;\n\t"
+      "mov.b64 {%0, %1}, a; }"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 // 16 consecutive 32-bit columns of this warp's 32 TMEM lanes (one row per
 // lane); the caller waits with tmem_st_wait() before the columns are read.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&x)[16]) {
