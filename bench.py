@@ -18,6 +18,9 @@ Multi-GPU: replicas only (one independent copy of the workload per rank, no
 collective on the data path); the barrier and max-over-ranks timing use
 torch.distributed.
 
+--workload extend_b4_chunk2k: the chunked-extend pass instead (the chunk's
+FP8 workspace append and the causal FP8 extend attention), metric TFLOP/s.
+
 --impl reference: the CPU oracle (scalar C, one thread) on a bounded sample of
 the same workload, as the reference arm.
 """
@@ -349,6 +352,174 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+EXTEND_METRIC = "chunked-extend FP8 attention: TFLOP/s (causal, algorithmic)"
+
+
+def _tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (cuBLAS bf16 burst; f16 has the same dense rate)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def extend_flops(prefixes, chunks, Hq, D=128):
+    """Algorithmic FLOPs of the causal extend attention: query j of a chunk
+    over prefix p sees p + j + 1 keys; QK^T and P.V each 2 D per key and head."""
+    keys = sum(p * c + c * (c + 1) // 2 for p, c in zip(prefixes, chunks))
+    return 4 * D * Hq * keys
+
+
+def run_extend(args):
+    """The chunked-extend pass of one layer: the chunk's K/V appended to the
+    FP8 workspace behind the (already dequantized) prefix, then the causal
+    FP8 attention of the chunk's queries over [prefix || chunk]."""
+    dist, rank, ws, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import nvfp4_quantized_paged_gb300 as nv
+    from nvfp4_quantized_paged_gb300.workloads import EXTEND_SPECS, extend_inputs
+    nv.lib()
+    c = EXTEND_SPECS[args.workload]
+    x = extend_inputs(0, **c)
+    Hq, Hkv = c["Hq"], c["Hkv"]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    k_all = torch.from_numpy(x["k"]).to(dev)
+    v_all = torch.from_numpy(x["v"]).to(dev)
+    ws_scale = torch.zeros(2, dtype=torch.float32, device=dev)
+    nv.nvkv_global_scale(k_all, ws_scale[0:1], nv.FP8_GLOBAL_DIVISOR)
+    nv.nvkv_global_scale(v_all, ws_scale[1:2], nv.FP8_GLOBAL_DIVISOR)
+    ci = torch.from_numpy(x["chunk_idx"]).to(dev)
+    k_chunk, v_chunk = k_all[ci].contiguous(), v_all[ci].contiguous()
+    chunk_rows = torch.from_numpy(x["chunk_rows"]).to(dev)
+    cu_q = torch.from_numpy(x["cu_q"]).to(dev)
+    cu_kv = torch.from_numpy(x["cu_kv"]).to(dev)
+    kv_lens = torch.from_numpy(x["kv_lens"]).to(dev)
+    max_q = max(c["chunks"])
+    per = 2 * x["ws_rows"] * Hkv * 128 + x["q"].numel() * 2
+    reps = max(2, -(-3 * l2 // per))  # workspace + queries rotate over >= 3x L2
+    sets = []
+    for _ in range(reps):
+        wk = torch.zeros(x["ws_rows"], Hkv, 128, dtype=torch.uint8, device=dev)
+        wv = torch.zeros_like(wk)
+        nv.fp8_workspace_append_chunk(k_all, v_all, torch.from_numpy(x["rows"]).to(dev), ws_scale, wk, wv)
+        sets.append(dict(wk=wk, wv=wv, q=x["q"].to(dev), out=torch.empty(x["q"].shape, dtype=torch.bfloat16,
+                                                                           device=dev)))
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def attend(r):
+        nv.fp8_chunked_extend_attention(r["q"], cu_q, max_q, r["wk"], r["wv"], cu_kv, kv_lens, ws_scale, r["out"],
+                                        err=err)
+
+    def step(i):
+        r = sets[i % reps]
+        nv.fp8_workspace_append_chunk(k_chunk, v_chunk, chunk_rows, ws_scale, r["wk"], r["wv"], err=err)
+        attend(r)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert err.item() == 0, err.item()
+    g_step = _graph(lambda: [step(i) for i in range(args.steps)])
+    g_att = _graph(lambda: [attend(sets[i % reps]) for i in range(args.steps)])
+    g_step.replay()
+    g_att.replay()
+    torch.cuda.synchronize()
+    _barrier(dist)
+    torch.cuda.synchronize()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    with Clocks(gpu_id) as clk:
+        step_ms = _time_graph(g_step, stream) / args.steps
+        att_ms = _time_graph(g_att, stream) / args.steps
+    _barrier(dist)
+    ms = _max_over_ranks(dist, step_ms, dev)
+    del g_step, g_att
+    flops = extend_flops(c["prefixes"], c["chunks"], Hq)
+    # e2e: the chunk's K/V and queries from pinned host memory, the output back
+    hk, hv = k_chunk.cpu().pin_memory(), v_chunk.cpu().pin_memory()
+    hq = x["q"].pin_memory()
+    hout = torch.empty(x["q"].shape, dtype=torch.bfloat16).pin_memory()
+    dk, dv = torch.empty_like(k_chunk), torch.empty_like(v_chunk)
+
+    def e2e_step(i):
+        r = sets[i % reps]
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        r["q"].copy_(hq, non_blocking=True)
+        nv.fp8_workspace_append_chunk(dk, dv, chunk_rows, ws_scale, r["wk"], r["wv"], err=err)
+        attend(r)
+        hout.copy_(r["out"], non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, dev)
+    peak, peak_kind = _tensor_peak()
+    tot = _sum_over_ranks(dist, float(flops), dev)
+    if rank == 0:
+        line = {
+            "metric": EXTEND_METRIC, "value": round(tot / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16xf16->f32 (E4M3 K/V exact in f16, BF16 queries in f16, P in f16)",
+            "data": "synthetic (seeded; no dataset or weights)",
+            "config": {"workload": args.workload, "prefixes": list(c["prefixes"]), "chunks": list(c["chunks"]),
+                       "Hq": Hq, "Hkv": Hkv, "D": 128,
+                       "l2": f"workspace and queries rotate over {reps} replicas (>= 3x L2, {l2 >> 20} MiB)",
+                       "parallelism": f"replicas x{ws}", "launch": "one CUDA graph of the K timed steps"},
+            "e2e": {"value": round(tot / (e2e_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 5),
+                    "h2d_bytes_per_step": int(hk.numel() * 4 * 2 + hq.numel() * 2),
+                    "d2h_bytes_per_step": int(hout.numel() * 2)},
+            "gpu_launches": 2 * args.steps,
+            "roofline": {"bound": "tensor", "kernel": "extend_attention_kernel", "unit": "TFLOP/s",
+                         "achieved": round(flops / (att_ms * 1e-3) / 1e12, 1), "peak": peak, "peak_kind": peak_kind,
+                         "frac": round(flops / (att_ms * 1e-3) / 1e12 / peak, 4), "traffic": None,
+                         "algorithmic_flops_per_launch": int(flops), "avg_launch_us": round(att_ms * 1e3, 2),
+                         "timed": "CUDA events around one graph of K attention launches, replicas rotated"},
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = extend_cpu_baseline(x, ws_scale.cpu().numpy(), Hq, budget_s=args.cpu_budget)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def extend_cpu_baseline(x, ws_scale, Hq, budget_s=10.0):
+    """The oracle (scalar C, 1 thread) on a bounded sample: single queries
+    of the last sequence, each a one-query problem over its visible keys."""
+    import oracle
+    wk = np.zeros((x["ws_rows"], x["k"].shape[1], 128), np.uint8)
+    wv = np.zeros_like(wk)
+    oracle.fp8_workspace_append(wk, wv, x["k"], x["v"], x["rows"], ws_scale)
+    qb = x["q"].view(torch.int16).numpy().view(np.uint16)
+    i = len(x["chunks"]) - 1
+    done, t, nq = 0, 0.0, 0
+    for j in range(0, x["chunks"][i], 97):
+        pos = x["prefixes"][i] + j
+        row = int(x["cu_q"][i]) + j
+        t0 = time.perf_counter()
+        oracle.fp8_extend_attention(qb[row:row + 1], [0, 1], wk, wv, [int(x["cu_kv"][i])], [pos + 1], ws_scale)
+        t += time.perf_counter() - t0
+        done += 4 * 128 * Hq * (pos + 1)
+        nq += 1
+        if t >= budget_s:
+            break
+    return {"value": round(done / t / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{nq} queries (all heads) of the last sequence, {t:.1f} s", "cpu": _cpu_name(),
+            "host_cores": os.cpu_count()}
+
+
 def _traffic_from_profile(workload):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current decode kernel source (else None)."""
@@ -450,8 +621,11 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    from nvfp4_quantized_paged_gb300.workloads import EXTEND_SPECS
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload in EXTEND_SPECS:
+        run_extend(args)
     else:
         run_ours(args)
 

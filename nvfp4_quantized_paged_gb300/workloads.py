@@ -194,3 +194,45 @@ class Workload:
         s = self.spec
         g = _gen(self.device, self.seed, 6, layer)
         return torch.randn(s.B, s.Hq, s.D, generator=g, device=self.device).to(torch.bfloat16)
+
+
+# ---------------------------------------------------------------------------
+# Chunked-extend workloads: a batch of sequences, each a cached prefix plus a
+# chunk of new tokens whose queries attend over [prefix || chunk].
+# ---------------------------------------------------------------------------
+EXTEND_SPECS = {
+    # four serving sequences (1k-12k token prefixes) extended by 2048 tokens each
+    "extend_b4_chunk2k": dict(prefixes=(1024, 5000, 7000, 12000), chunks=(2048, 2048, 2048, 2048), Hq=32, Hkv=8),
+}
+
+
+def extend_inputs(seed, prefixes, chunks, Hq, Hkv, D=128, gap=16, outlier_p=0.01, outlier_scale=20.0):
+    """Seeded host arrays of one chunked-extend batch: K/V for every position
+    (prefix and chunk) N(0,1) with a fraction `outlier_p` of elements scaled
+    by `outlier_scale` (the element-outlier recipe of the decode workloads),
+    BF16-representable queries N(0,1) for the chunk tokens, and the workspace
+    row layout: sequence i owns rows cu_kv[i] .. cu_kv[i] + prefix + chunk,
+    with `gap` unused rows between sequences."""
+    rng = np.random.default_rng(seed)
+    n = len(prefixes)
+    kv_lens = np.array([p + c for p, c in zip(prefixes, chunks)], np.int32)
+    cu_kv = np.zeros(n, np.int64)
+    r = 0
+    for i in range(n):
+        cu_kv[i] = r
+        r += int(kv_lens[i]) + gap
+    T = int(kv_lens.sum())
+    k = rng.standard_normal((T, Hkv, D)).astype(np.float32)
+    v = rng.standard_normal((T, Hkv, D)).astype(np.float32)
+    for x in (k, v):
+        m = rng.random(x.shape) < outlier_p
+        x[m] *= outlier_scale
+    rows = np.concatenate([cu_kv[i] + np.arange(kv_lens[i]) for i in range(n)]).astype(np.int64)
+    chunk_rows = np.concatenate([cu_kv[i] + prefixes[i] + np.arange(chunks[i]) for i in range(n)]).astype(np.int64)
+    chunk_idx = np.concatenate([int(kv_lens[:i].sum()) + prefixes[i] + np.arange(chunks[i])
+                                for i in range(n)]).astype(np.int64)
+    cu_q = np.zeros(n + 1, np.int64)
+    cu_q[1:] = np.cumsum(chunks)
+    q = torch.from_numpy(rng.standard_normal((int(cu_q[-1]), Hq, D)).astype(np.float32)).to(torch.bfloat16)
+    return dict(k=k, v=v, rows=rows, ws_rows=r, cu_kv=cu_kv, kv_lens=kv_lens, cu_q=cu_q, q=q,
+                chunk_rows=chunk_rows, chunk_idx=chunk_idx, prefixes=tuple(prefixes), chunks=tuple(chunks))

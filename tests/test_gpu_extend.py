@@ -26,34 +26,14 @@ def _nv():
     return nv
 
 
-def _inputs(seed, prefixes, chunks, Hq, Hkv, gap=16, outliers=True):
-    """Seeded K/V/Q for a batch of extends: N(0,1) with sparse x20 outliers
-    (the decode workloads' element-outlier recipe), workspace rows laid out
-    per sequence with `gap` unused rows between sequences."""
-    rng = np.random.default_rng(seed)
-    D = 128
-    n = len(prefixes)
-    kv_lens = np.array([p + c for p, c in zip(prefixes, chunks)], np.int32)
-    cu_kv = np.zeros(n, np.int64)
-    r = 0
-    for i in range(n):
-        cu_kv[i] = r
-        r += int(kv_lens[i]) + gap
-    ws_rows = r
-    T = int(kv_lens.sum())
-    k = rng.standard_normal((T, Hkv, D)).astype(np.float32)
-    v = rng.standard_normal((T, Hkv, D)).astype(np.float32)
-    if outliers:
-        for x in (k, v):
-            m = rng.random(x.shape) < 0.01
-            x[m] *= 20.0
-    rows = np.concatenate([cu_kv[i] + np.arange(kv_lens[i]) for i in range(n)]).astype(np.int64)
-    cu_q = np.zeros(n + 1, np.int64)
-    cu_q[1:] = np.cumsum(chunks)
-    q = rng.standard_normal((int(cu_q[-1]), Hq, D)).astype(np.float32)
-    ws_scale = np.array([np.abs(k).max() / 448.0, np.abs(v).max() / 448.0], np.float32)
-    return dict(k=k, v=v, rows=rows, ws_rows=ws_rows, cu_kv=cu_kv, kv_lens=kv_lens, cu_q=cu_q, q=q,
-                ws_scale=ws_scale, chunks=list(chunks))
+def _inputs(seed, prefixes, chunks, Hq, Hkv):
+    """The seeded chunked-extend generator plus a workspace scale per K and V
+    (amax / 448, the FP8 per-tensor convention) chosen here as an input."""
+    from nvfp4_quantized_paged_gb300.workloads import extend_inputs
+    x = extend_inputs(seed, prefixes, chunks, Hq, Hkv)
+    x["q"] = x["q"].float().numpy()
+    x["ws_scale"] = np.array([np.abs(x["k"]).max() / 448.0, np.abs(x["v"]).max() / 448.0], np.float32)
+    return x
 
 
 def _device(x):
