@@ -90,6 +90,7 @@ typedef enum { NVKV_DTYPE_F32 = 0, NVKV_DTYPE_BF16 = 1 } nvkv_dtype;
 #define NVKV_DEVERR_SEQLEN 3     /* seq_len > max_pages * page_size or < 0   */
 #define NVKV_DEVERR_TIMEOUT 4    /* a bounded wait inside a kernel ran out   */
 #define NVKV_DEVERR_WS_ROWS 5    /* workspace rows smaller than the prefixes */
+#define NVKV_DEVERR_ALIGN 6      /* extend: a sequence's first workspace row not a multiple of 8 */
 
 /* One layer's cache.  The struct itself is host memory read during the call. */
 typedef struct {
@@ -266,23 +267,30 @@ nvkv_status fp8_workspace_append_chunk(const void *k, const void *v, nvkv_dtype 
  *            at FP16 precision (exact for |q| in [2^-14, 65504])
  *   cu_q     [n+1] int64 device, non-decreasing; max_q_len (host) >= every
  *            nq_i (queries beyond it are not computed: NVKV_DEVERR_SEQLEN)
- *   cu_kv    [n] int64 device; kv_lens [n] int32 device, nq_i <= kv_lens[i]
- *            and cu_kv[i] + kv_lens[i] <= ws_rows, else the sequence is
- *            skipped and NVKV_DEVERR_SEQLEN / NVKV_DEVERR_WS_ROWS raised
+ *   cu_kv    [n] int64 device, each a multiple of 8; kv_lens [n] int32
+ *            device, nq_i <= kv_lens[i] and cu_kv[i] + kv_lens[i] <= ws_rows,
+ *            else the sequence is skipped and NVKV_DEVERR_ALIGN /
+ *            NVKV_DEVERR_SEQLEN / NVKV_DEVERR_WS_ROWS raised
  *   ws_k, ws_v  [ws_rows][num_kv_heads][128] E4M3 (finite bytes), device,
  *            16-byte aligned; ws_scale device float[2] {K, V}
  *   sm_scale <= 0 -> 1/sqrt(128)
+ *   scratch  device, 16-byte aligned, >= fp8_extend_scratch_size(ws_rows,
+ *            num_kv_heads, 128) bytes (else NVKV_ERR_WORKSPACE_TOO_SMALL):
+ *            the workspace expanded once into FP16 operand tiles
  *   out      [cu_q[n]][num_q_heads][128] BF16, device, 16-byte aligned
  *   err_flag optional device int32 (first error code wins)
  * head_dim must be 128 and num_q_heads / num_kv_heads a power of two <= 128
  * (else NVKV_ERR_UNSUPPORTED).  QK^T and P.V run on the tensor cores with
  * FP16 operands (E4M3 converts exactly) and FP32 accumulation; P is rounded
- * to FP16.  One kernel on `stream`; it allocates nothing. */
+ * to FP16.  Two kernels on `stream` (the tile expansion, the attention); it
+ * allocates nothing. */
+size_t fp8_extend_scratch_size(int64_t ws_rows, int32_t num_kv_heads, int32_t head_dim);
 nvkv_status fp8_chunked_extend_attention(const void *q, const int64_t *cu_q, int32_t n, int32_t max_q_len,
                                          int32_t num_q_heads, const uint8_t *ws_k, const uint8_t *ws_v,
                                          const int64_t *cu_kv, const int32_t *kv_lens, int32_t num_kv_heads,
                                          int32_t head_dim, int64_t ws_rows, const float *ws_scale, float sm_scale,
-                                         void *out, int32_t *err_flag, void *stream);
+                                         void *scratch, size_t scratch_bytes, void *out, int32_t *err_flag,
+                                         void *stream);
 
 /* Element encoders of the quantizer, one output byte per FP32 input: E2M1
  * code (low nibble, round-to-nearest-even, saturating at 6) and E4M3 byte

@@ -11,7 +11,8 @@ Functions keep the C names:
   fp8_kv_quantize_write, nvkv_decode_workspace_size,
   nvkv_decode_workspace_init, nvfp4_paged_decode_attention,
   fp8_paged_decode_attention, nvfp4_kv_dequant_to_fp8_workspace,
-  fp8_workspace_append_chunk, fp8_chunked_extend_attention,
+  fp8_workspace_append_chunk, fp8_extend_scratch_size,
+  fp8_chunked_extend_attention,
   nvkv_encode_e2m1, nvkv_encode_e4m3.
 ``Cache`` allocates one layer's paged planes with torch and builds the
 ``nvkv_cache`` descriptor.
@@ -90,8 +91,9 @@ SIGNATURES = {
     "nvfp4_kv_dequant_to_fp8_workspace": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _cachep, _vp, _vp, _vp, _i64,
                                                  _vp]),
     "fp8_workspace_append_chunk": (_i32, [_vp, _vp, _i32, _i64, _vp, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp]),
+    "fp8_extend_scratch_size": (_sz, [_i64, _i32, _i32]),
     "fp8_chunked_extend_attention": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp,
-                                            _f32, _vp, _vp, _vp]),
+                                            _f32, _vp, _sz, _vp, _vp, _vp]),
     "nvkv_encode_e2m1": (_i32, [_vp, _i64, _vp, _vp]),
     "nvkv_encode_e4m3": (_i32, [_vp, _i64, _vp, _vp]),
 }
@@ -285,16 +287,29 @@ def fp8_workspace_append_chunk(k, v, rows, ws_scale, ws_k, ws_v, err=None, strea
                                             _ptr(err), _stream(stream)))
 
 
-def fp8_chunked_extend_attention(q, cu_q, max_q_len, ws_k, ws_v, cu_kv, kv_lens, ws_scale, out, sm_scale=0.0,
-                                 err=None, stream=None):
+def fp8_extend_scratch_size(ws_rows, num_kv_heads, head_dim=HEAD_DIM) -> int:
+    return int(lib().fp8_extend_scratch_size(ws_rows, num_kv_heads, head_dim))
+
+
+def alloc_extend_scratch(ws_k: torch.Tensor) -> torch.Tensor:
+    """Scratch (torch) for fp8_chunked_extend_attention over workspace ws_k."""
+    n = fp8_extend_scratch_size(ws_k.shape[0], ws_k.shape[1], ws_k.shape[2])
+    if n == 0:
+        raise NvkvError("fp8_extend_scratch_size", NVKV_ERR_INVALID_ARG)
+    return torch.empty(n, dtype=torch.uint8, device=ws_k.device)
+
+
+def fp8_chunked_extend_attention(q, cu_q, max_q_len, ws_k, ws_v, cu_kv, kv_lens, ws_scale, out, scratch,
+                                 sm_scale=0.0, err=None, stream=None):
     """Causal FP8 attention of the chunk queries ``q`` (BF16 [Tq, Hq, 128],
     sequence i owns rows cu_q[i]:cu_q[i+1]) over workspace rows
-    [cu_kv[i], cu_kv[i] + kv_lens[i]) (prefix, then the chunk)."""
+    [cu_kv[i], cu_kv[i] + kv_lens[i]) (prefix, then the chunk; cu_kv[i] a
+    multiple of 8).  ``scratch``: see alloc_extend_scratch."""
     _check("fp8_chunked_extend_attention",
            lib().fp8_chunked_extend_attention(_ptr(q), _ptr(cu_q), kv_lens.numel(), int(max_q_len), q.shape[1],
                                               _ptr(ws_k), _ptr(ws_v), _ptr(cu_kv), _ptr(kv_lens), ws_k.shape[1],
-                                              q.shape[2], ws_k.shape[0], _ptr(ws_scale), sm_scale, _ptr(out),
-                                              _ptr(err), _stream(stream)))
+                                              q.shape[2], ws_k.shape[0], _ptr(ws_scale), sm_scale, _ptr(scratch),
+                                              scratch.numel(), _ptr(out), _ptr(err), _stream(stream)))
 
 
 def nvkv_encode_e2m1(x, out, stream=None):

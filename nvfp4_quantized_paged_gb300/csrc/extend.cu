@@ -7,24 +7,29 @@
 // FP8 workspace, concatenated with the current chunk's KV, and the chunk's
 // queries run FP8 attention over the concatenation (causal inside the chunk).
 //
-// Work item: (sequence, KV head, M-tile of 128 query rows).  Row r of an
-// M-tile is query token r / G of the tile with query head h G + r % G, so the
-// G query heads that share a KV head share every converted K/V tile.  Per
-// tile of 128 keys, QK^T and P.V run on the tensor cores (tcgen05.mma
-// kind::f16, M = N = 128, K = 16 per instruction, FP32 accumulators in TMEM:
-// scores in two ping-pong buffers, the output in a third); the softmax runs
-// in the registers of the thread that owns the row's TMEM lane.
+// Two kernels per call.  extend_tiles_kernel expands the E4M3 workspace once
+// into FP16 operand tiles in the tensor cores' K-major layout (K by 8-row
+// groups, V transposed so that keys run along K); E4M3 -> FP16 is exact.
+// Every M-tile of a (sequence, KV head) then reads the same tiles from L2
+// instead of converting them again.
 //
-// Roles (288 threads, one CTA per SM):
-//   warps 0-3  softmax: thread r owns query row r; base-2 online softmax with
-//              a lazily raised running max, P to shared memory as FP16, the
-//              output rescaled in TMEM when the max rises, the epilogue.
-//   warps 4-7  converters: the Q tile (BF16 -> FP16) once, then per KV tile
-//              the E4M3 K rows into an FP16 K-major tile and the E4M3 V rows
-//              into an FP16 V^T tile (keys along K), double-buffered.
-//   warp 8     one thread issues the MMAs.
-// E4M3 -> FP16 is exact; BF16 queries convert to FP16 exactly inside the FP16
-// normal range [2^-14, 65504].
+// extend_attention_kernel, work item (sequence, KV head, M-tile of 128 query
+// rows): row r of an M-tile is query token r / G of the tile with query head
+// h G + r % G, so the G query heads that share a KV head share every K/V
+// tile.  Per tile of 128 keys, QK^T and P.V run on the tensor cores
+// (tcgen05.mma kind::f16, M = N = 128, K = 16 per instruction, FP32
+// accumulators in TMEM: scores in two ping-pong buffers, the output in a
+// third); the softmax runs in the registers of the thread that owns the row's
+// TMEM lane.  Roles (192 threads, one CTA per SM):
+//   warps 0-3  the Q tile (BF16 -> FP16) once; then the softmax: thread r owns
+//              query row r; base-2 online softmax with a lazily raised running
+//              max, P to shared memory as FP16, the output rescaled in TMEM
+//              when the max rises, the epilogue.
+//   warp 4     producer: bulk copies of each tile's K (one 32 KB copy) and V^T
+//              (sixteen 2 KB copies) into a double-buffered stage.
+//   warp 5     one thread issues the MMAs.
+// BF16 queries convert to FP16 exactly inside the FP16 normal range
+// [2^-14, 65504].
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -37,15 +42,17 @@ namespace {
 
 constexpr int kXD = 128;                 // head_dim
 constexpr int kXRows = 128;              // query rows per M-tile, keys per KV tile
-constexpr int kXThreads = 288;
-constexpr int kXIssuerWarp = 8;
+constexpr int kXThreads = 192;
+constexpr int kXProducerWarp = 4;
+constexpr int kXIssuerWarp = 5;
 constexpr uint32_t kXTmemCols = 512;     // scores 0..127 and 128..255, output 256..383
 constexpr uint32_t kXColO = 256;
 constexpr int kXTile = kXRows * kXD * 2; // one FP16 operand tile (32 KB)
 constexpr int kXSbo = 2048;              // bytes between 8-row groups of a tile
 // Shared memory: Q | K[2] | V^T[2] | P | barriers | TMEM holder, abort flag.
 constexpr int oXQ = 0, oXK = kXTile, oXV = 3 * kXTile, oXP = 5 * kXTile, oXBar = 6 * kXTile;
-constexpr int kXBars = 10;               // kv_full[2] s_full[2] s_free[2] p_full pv_done[2] fin
+constexpr int kXBars = 11;               // kv_full[2] s_full[2] s_free[2] p_full pv_done[2] fin q_full
+constexpr int kXGroupBytes = 8 * kXD * 2;  // one 8-row group of an FP16 operand tile (2 KB)
 constexpr int oXFlags = oXBar + 8 * kXBars;
 constexpr int kXSmem = oXFlags + 16;
 constexpr float kXNoMax = -1e30f;        // running max before any score (finite: exp2(-inf - m) = 0)
@@ -60,6 +67,8 @@ struct ExtendArgs {
   const float *ws_scale;
   __nv_bfloat16 *out;
   int32_t *err;
+  const uint8_t *tiles;  // expanded FP16 operand tiles
+  int64_t ngroups;       // 8-row groups per head in `tiles`
   int64_t ws_rows;
   int Hq, Hkv, G, lgG, Tm;
   float sm_scale;
@@ -96,17 +105,15 @@ struct Tile {            // the CTA's work item, uniform over the CTA
 };
 
 // ---------------------------------------------------------------------------
-// Converters (warps 4-7).  Thread ct = (rb, dc): 8-row block rb, 16-element
-// column chunk dc.  Stores are rotated so that the eight threads of a store
-// phase (dc = 0..7, one rb) write eight different rows of their core
-// matrices: no shared-memory bank conflicts.
+// The Q tile, by the softmax warps before their loop.  Thread r = (rb, dc):
+// 8-row block rb, 16-element column chunk dc; rows 8 rb + (s + dc) % 8, so
+// the eight threads of a store phase (dc = 0..7) write eight different rows
+// of their core matrices: no shared-memory bank conflicts.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void x_converter(const ExtendArgs &a, const Tile &t, uint8_t *smem, uint64_t *kv_full,
-                            uint64_t *pv_done, volatile int *abort) {
-  const int ct = static_cast<int>(threadIdx.x) - 128;
+__device__ __forceinline__ void x_load_q(const ExtendArgs &a, const Tile &t, uint8_t *smem) {
+  const int ct = static_cast<int>(threadIdx.x);
   const int rb = ct >> 3, dc = ct & 7;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  // Q rows 8 rb + (s + dc) % 8, elements 16 dc .. 16 dc + 15 -> chunks 2 dc, 2 dc + 1
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     const int r = 8 * rb + ((s + dc) & 7);
@@ -124,65 +131,89 @@ __device__ __forceinline__ void x_converter(const ExtendArgs &a, const Tile &t, 
     *reinterpret_cast<uint4 *>(dst + 128) = make_uint4(f16x2_from_bf16x2(hi.x), f16x2_from_bf16x2(hi.y),
                                                        f16x2_from_bf16x2(hi.z), f16x2_from_bf16x2(hi.w));
   }
-  const int rho = dc >> 2, tau = dc & 3;
+}
+
+// ---------------------------------------------------------------------------
+// Producer (warp 4): tile j of keys [128 j, 128 j + 128) of the sequence is
+// row groups g0 .. g0 + 15, g0 = (cu_kv + 128 j) / 8, of the expanded tiles:
+// K as one 32 KB block (groups are contiguous per head), V^T as one 2 KB run
+// per 8-value group d (lane d).  The stage is free once the P.V of tile j - 2
+// is done.  Returns the number of tiles whose copies were issued.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int x_producer(const ExtendArgs &a, const Tile &t, uint8_t *smem, uint64_t *kv_full,
+                                          uint64_t *pv_done, volatile int *abort) {
+  const int lane = static_cast<int>(threadIdx.x) & 31;
+  const uint64_t policy = policy_evict_last();
+  const uint8_t *kt = a.tiles + static_cast<int64_t>(t.h) * a.ngroups * kXGroupBytes;
+  const uint8_t *vt = a.tiles + (static_cast<int64_t>(a.Hkv) + t.h) * a.ngroups * kXGroupBytes;
+  int issued = 0;
   for (int j = 0; j < t.ntiles; ++j) {
-    const int b = j & 1, kv0 = j * kXRows;
-    // loads first (their latency overlaps the wait for the buffer); keys past
-    // the sequence read as zero (never NaN: P is 0 there and 0 * NaN = NaN)
-    uint4 kr[8], vr[8];
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const int key = kv0 + 8 * rb + ((s + dc) & 7);
-      kr[s] = key < t.L ? *reinterpret_cast<const uint4 *>(
-                              a.ws_k + ((t.kv_base + key) * a.Hkv + t.h) * kXD + 16 * dc)
-                        : zero;
+    const int b = j & 1;
+    if (j >= 2 && !warp_wait_x(&pv_done[b], static_cast<uint32_t>((j - 2) >> 1) & 1u, abort)) break;
+    const int64_t g0 = (t.kv_base + static_cast<int64_t>(j) * kXRows) >> 3;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&kv_full[b], 2 * kXTile);
+      bulk_g2s(smem + oXK + b * kXTile, kt + g0 * kXGroupBytes, kXTile, &kv_full[b], policy);
     }
+    __syncwarp();
+    if (lane < 16)
+      bulk_g2s(smem + oXV + b * kXTile + lane * kXGroupBytes, vt + (lane * a.ngroups + g0) * 128, kXGroupBytes,
+               &kv_full[b], policy);
+    ++issued;
+  }
+  return issued;
+}
+
+// ---------------------------------------------------------------------------
+// Expanded tiles: tiles = [K: Hkv][ngroups][2048 B] [V: Hkv][16][ngroups][128 B].
+// K group (h, g): 16-byte chunk c (values 8c .. 8c + 7) of row r (key 8g + r)
+// at c * 128 + r * 16.  V run (h, d, g): value row e (value 8d + e), keys 8g ..
+// 8g + 7 at e * 16 + 2 r.  Rows at or past ws_rows are zero; an E4M3 NaN byte
+// (never written by this library) becomes -448 so that masked keys stay finite.
+// One thread per (g, h, d): an 8 x 8 byte block of the workspace.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t f16x2_finite(uint32_t h2) {
+  return __hmax2_as_u32(h2, 0xDF00DF00u);  // max(x, -448): NaN -> -448, every E4M3 value unchanged
+}
+
+__global__ void __launch_bounds__(256) extend_tiles_kernel(const uint8_t *__restrict__ ws_k,
+                                                           const uint8_t *__restrict__ ws_v, int64_t ws_rows,
+                                                           int Hkv, int64_t ngroups, uint8_t *__restrict__ tiles) {
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= ngroups * Hkv * 16) return;
+  const int d = static_cast<int>(gid & 15);
+  const int h = static_cast<int>((gid >> 4) % Hkv);
+  const int64_t g = (gid >> 4) / Hkv;
+  uint32_t kw[8][2], vw[8][2];
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const int key = kv0 + 8 * rb + s;
-      vr[s] = key < t.L ? *reinterpret_cast<const uint4 *>(
-                              a.ws_v + ((t.kv_base + key) * a.Hkv + t.h) * kXD + 16 * dc)
-                        : zero;
+  for (int r = 0; r < 8; ++r) {
+    const int64_t row = 8 * g + r;
+    uint2 x = make_uint2(0u, 0u), y = x;
+    if (row < ws_rows) {
+      x = *reinterpret_cast<const uint2 *>(ws_k + (row * Hkv + h) * kXD + 8 * d);
+      y = *reinterpret_cast<const uint2 *>(ws_v + (row * Hkv + h) * kXD + 8 * d);
     }
-    // the buffer was last read by the MMAs of tile j - 2
-    if (j >= 2 && !warp_wait_x(&pv_done[b], static_cast<uint32_t>((j - 2) >> 1) & 1u, abort)) return;
-    uint8_t *ks = smem + oXK + b * kXTile;
-    uint8_t *vt = smem + oXV + b * kXTile;
-    // K: row 8 rb + (s + dc) % 8 (the key), chunks 2 dc and 2 dc + 1
+    kw[r][0] = x.x;
+    kw[r][1] = x.y;
+    vw[r][0] = y.x;
+    vw[r][1] = y.y;
+  }
+  uint8_t *kdst = tiles + (static_cast<int64_t>(h) * ngroups + g) * kXGroupBytes + d * 128;
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      uint8_t *dst = ks + kmaj(8 * rb + ((s + dc) & 7), 2 * dc);
-      const uint4 w = kr[s];
-      *reinterpret_cast<uint4 *>(dst) = make_uint4(f16x2_from_e4m3x2<0>(w.x), f16x2_from_e4m3x2<1>(w.x),
-                                                   f16x2_from_e4m3x2<0>(w.y), f16x2_from_e4m3x2<1>(w.y));
-      *reinterpret_cast<uint4 *>(dst + 128) = make_uint4(f16x2_from_e4m3x2<0>(w.z), f16x2_from_e4m3x2<1>(w.z),
-                                                         f16x2_from_e4m3x2<0>(w.w), f16x2_from_e4m3x2<1>(w.w));
-    }
-    // V^T: row = value 16 dc + e, chunk rb = keys 8 rb .. 8 rb + 7.  Word w
-    // of vr[s] holds values 16 dc + 4 w .. + 3 of key 8 rb + s.  Step (sg, bt)
-    // handles e = 4 ((sg + rho) % 4) + (bt + tau) % 4: e % 8 differs across
-    // the eight threads of a store phase.
-    uint32_t wv[8][4];
+  for (int r = 0; r < 8; ++r)
+    *reinterpret_cast<uint4 *>(kdst + r * 16) =
+        make_uint4(f16x2_finite(f16x2_from_e4m3x2<0>(kw[r][0])), f16x2_finite(f16x2_from_e4m3x2<1>(kw[r][0])),
+                   f16x2_finite(f16x2_from_e4m3x2<0>(kw[r][1])), f16x2_finite(f16x2_from_e4m3x2<1>(kw[r][1])));
+  uint8_t *vdst = tiles + ((static_cast<int64_t>(Hkv) + h) * ngroups * kXGroupBytes) +
+                  (static_cast<int64_t>(d) * ngroups + g) * 128;
 #pragma unroll
-    for (int s = 0; s < 8; ++s)
+  for (int e = 0; e < 8; ++e) {
+    const uint32_t sel = static_cast<uint32_t>(e & 3) | (static_cast<uint32_t>(4 + (e & 3)) << 4);
+    uint32_t o[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) wv[s][k] = rho ? word_of(vr[s], (k + 1) & 3) : word_of(vr[s], k);
-#pragma unroll
-    for (int bt = 0; bt < 4; ++bt) {
-      const uint32_t bb = static_cast<uint32_t>((bt + tau) & 3);
-      const uint32_t sel = bb | ((bb + 4u) << 4);  // byte bb of the first word, byte bb of the second
-#pragma unroll
-      for (int sg = 0; sg < 4; ++sg) {
-        const int e = 4 * ((sg + rho) & 3) + static_cast<int>(bb);
-        uint32_t o[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) o[u] = f16x2_from_e4m3x2<0>(prmt(wv[2 * u][sg], wv[2 * u + 1][sg], sel));
-        *reinterpret_cast<uint4 *>(vt + (2 * dc + (e >> 3)) * kXSbo + rb * 128 + (e & 7) * 16) =
-            make_uint4(o[0], o[1], o[2], o[3]);
-      }
-    }
-    fence_proxy_async_smem();  // generic-proxy stores -> visible to the MMAs
-    mbar_arrive(&kv_full[b]);
+    for (int u = 0; u < 4; ++u)
+      o[u] = f16x2_finite(f16x2_from_e4m3x2<0>(prmt(vw[2 * u][e >> 2], vw[2 * u + 1][e >> 2], sel)));
+    *reinterpret_cast<uint4 *>(vdst + e * 16) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -368,9 +399,10 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attention_kernel(const Ex
   const int64_t nq = a.cu_q[i + 1] - t.q0;
   t.L = a.kv_lens[i];
   t.kv_base = a.cu_kv[i];
-  if (nq < 0 || nq > t.L || t.kv_base < 0 || t.kv_base + t.L > a.ws_rows) {
+  if (nq < 0 || nq > t.L || t.kv_base < 0 || t.kv_base + t.L > a.ws_rows || (t.kv_base & 7) != 0) {
     if (tid == 0 && blockIdx.x == 0 && t.h == 0)
-      set_err(a.err, (nq < 0 || nq > t.L) ? NVKV_DEVERR_SEQLEN : NVKV_DEVERR_WS_ROWS);
+      set_err(a.err, (nq < 0 || nq > t.L) ? NVKV_DEVERR_SEQLEN
+                                          : ((t.kv_base & 7) != 0 ? NVKV_DEVERR_ALIGN : NVKV_DEVERR_WS_ROWS));
     return;
   }
   if (tid == 0 && blockIdx.x == 0 && t.h == 0 && nq > static_cast<int64_t>(gridDim.x) * a.Tm)
@@ -384,12 +416,12 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attention_kernel(const Ex
 
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + oXBar);
   uint64_t *kv_full = bars, *s_full = bars + 2, *s_free = bars + 4, *p_full = bars + 6, *pv_done = bars + 7;
-  uint64_t *fin = bars + 9;
+  uint64_t *fin = bars + 9, *q_full = bars + 10;
   uint32_t *holder = reinterpret_cast<uint32_t *>(smem + oXFlags);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + oXFlags + 4);
   if (tid == 0) {
-    mbar_init(&kv_full[0], 128);
-    mbar_init(&kv_full[1], 128);
+    mbar_init(&kv_full[0], 1);  // the producer's expect_tx, then the copies' bytes
+    mbar_init(&kv_full[1], 1);
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
     mbar_init(&s_free[0], 128);
@@ -398,6 +430,7 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attention_kernel(const Ex
     mbar_init(&pv_done[0], 1);
     mbar_init(&pv_done[1], 1);
     mbar_init(fin, 1);
+    mbar_init(q_full, 128);
     *abort = 0;
     fence_mbar_init();
   }
@@ -407,19 +440,32 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attention_kernel(const Ex
   tc_fence_after();
   const uint32_t tmem = *holder;
 
+  int issued = 0;  // producer: tiles whose copies went out
   if (warp < 4) {
+    x_load_q(a, t, smem);
+    fence_proxy_async_smem();  // generic-proxy stores -> visible to the MMAs
+    mbar_arrive(q_full);
     x_softmax(a, t, smem, tmem, s_full, s_free, p_full, pv_done, abort);
-  } else if (warp < 8) {
-    x_converter(a, t, smem, kv_full, pv_done, abort);
+  } else if (warp == kXProducerWarp) {
+    issued = x_producer(a, t, smem, kv_full, pv_done, abort);
   } else if (tid == kXIssuerWarp * 32) {
-    x_issuer(smem, tmem, t.ntiles, kv_full, s_full, s_free, p_full, pv_done, abort);
+    if (mbar_wait_bounded(q_full, 0u, abort))
+      x_issuer(smem, tmem, t.ntiles, kv_full, s_full, s_free, p_full, pv_done, abort);
     umma_commit(fin);  // every MMA issued is complete before TMEM is freed
     volatile int never = 0;
     mbar_wait_bounded(fin, 0u, &never);
   }
   tc_fence_before();
   __syncthreads();
-  if (tid == 0 && *abort) set_err(a.err, NVKV_DEVERR_TIMEOUT);
+  if (*abort) {  // after a timeout: the last copies in flight land before the CTA exits
+    if (tid == 0) set_err(a.err, NVKV_DEVERR_TIMEOUT);
+    if (warp == kXProducerWarp && (threadIdx.x & 31) == 0) {
+      volatile int never = 0;
+      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
+        mbar_wait_bounded(&kv_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, &never);
+    }
+    __syncthreads();
+  }
   if (warp == kXIssuerWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kXTmemCols);
@@ -516,19 +562,29 @@ nvkv_status fp8_workspace_append_chunk(const void *k, const void *v, nvkv_dtype 
   return launch_status();
 }
 
+size_t fp8_extend_scratch_size(int64_t ws_rows, int32_t num_kv_heads, int32_t head_dim) {
+  if (ws_rows < 0 || num_kv_heads <= 0 || head_dim != kXD) return 0;
+  const int64_t ngroups = (ws_rows + 7) / 8 + kXRows / 8;  // + one tile of zero rows past the end
+  return static_cast<size_t>(2 * static_cast<int64_t>(num_kv_heads) * ngroups * kXGroupBytes);
+}
+
 nvkv_status fp8_chunked_extend_attention(const void *q, const int64_t *cu_q, int32_t n, int32_t max_q_len,
                                          int32_t num_q_heads, const uint8_t *ws_k, const uint8_t *ws_v,
                                          const int64_t *cu_kv, const int32_t *kv_lens, int32_t num_kv_heads,
                                          int32_t head_dim, int64_t ws_rows, const float *ws_scale, float sm_scale,
-                                         void *out, int32_t *err_flag, void *stream) {
+                                         void *scratch, size_t scratch_bytes, void *out, int32_t *err_flag,
+                                         void *stream) {
   if (n < 0 || max_q_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || ws_rows < 0) return NVKV_ERR_INVALID_ARG;
   if (num_q_heads % num_kv_heads != 0) return NVKV_ERR_INVALID_ARG;
   if (head_dim != kXD) return NVKV_ERR_UNSUPPORTED;
   const int G = num_q_heads / num_kv_heads;
   if (G > kXRows || (G & (G - 1)) != 0) return NVKV_ERR_UNSUPPORTED;
   if (n == 0 || max_q_len == 0) return NVKV_OK;
-  if (!q || !cu_q || !ws_k || !ws_v || !cu_kv || !kv_lens || !ws_scale || !out) return NVKV_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(ws_k) || !aligned16(ws_v) || !aligned16(out)) return NVKV_ERR_UNSUPPORTED;
+  if (!q || !cu_q || !ws_k || !ws_v || !cu_kv || !kv_lens || !ws_scale || !out || !scratch)
+    return NVKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(ws_k) || !aligned16(ws_v) || !aligned16(out) || !aligned16(scratch))
+    return NVKV_ERR_UNSUPPORTED;
+  if (scratch_bytes < fp8_extend_scratch_size(ws_rows, num_kv_heads, head_dim)) return NVKV_ERR_WORKSPACE_TOO_SMALL;
   if (n > 65535 || num_kv_heads > 65535) return NVKV_ERR_UNSUPPORTED;
   ExtendArgs a;
   a.q = static_cast<const __nv_bfloat16 *>(q);
@@ -540,6 +596,8 @@ nvkv_status fp8_chunked_extend_attention(const void *q, const int64_t *cu_q, int
   a.ws_scale = ws_scale;
   a.out = static_cast<__nv_bfloat16 *>(out);
   a.err = err_flag;
+  a.tiles = static_cast<const uint8_t *>(scratch);
+  a.ngroups = (ws_rows + 7) / 8 + kXRows / 8;
   a.ws_rows = ws_rows;
   a.Hq = num_q_heads;
   a.Hkv = num_kv_heads;
@@ -552,7 +610,12 @@ nvkv_status fp8_chunked_extend_attention(const void *q, const int64_t *cu_q, int
   if (cudaFuncSetAttribute(extend_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kXSmem) !=
       cudaSuccess)
     return NVKV_ERR_CUDA;
-  extend_attention_kernel<<<grid, kXThreads, kXSmem, static_cast<cudaStream_t>(stream)>>>(a);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t items = a.ngroups * num_kv_heads * 16;
+  if ((items + 255) / 256 > 0x7fffffff) return NVKV_ERR_UNSUPPORTED;
+  extend_tiles_kernel<<<static_cast<unsigned>((items + 255) / 256), 256, 0, s>>>(
+      ws_k, ws_v, ws_rows, num_kv_heads, a.ngroups, static_cast<uint8_t *>(scratch));
+  extend_attention_kernel<<<grid, kXThreads, kXSmem, s>>>(a);
   return launch_status();
 }
 

@@ -99,6 +99,13 @@ __device__ __forceinline__ void add_f32x2(float &a0, float &a1, float b0, float 
       : "f"(b0), "f"(b1));
 }
 
+// Elementwise max of two half2 (an input that is NaN yields the other).
+__device__ __forceinline__ uint32_t __hmax2_as_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -229,6 +236,12 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       "%4;" ::"r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {

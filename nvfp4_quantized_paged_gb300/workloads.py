@@ -211,8 +211,9 @@ def extend_inputs(seed, prefixes, chunks, Hq, Hkv, D=128, gap=16, outlier_p=0.01
     (prefix and chunk) N(0,1) with a fraction `outlier_p` of elements scaled
     by `outlier_scale` (the element-outlier recipe of the decode workloads),
     BF16-representable queries N(0,1) for the chunk tokens, and the workspace
-    row layout: sequence i owns rows cu_kv[i] .. cu_kv[i] + prefix + chunk,
-    with `gap` unused rows between sequences."""
+    row layout: sequence i owns rows cu_kv[i] .. cu_kv[i] + prefix + chunk
+    (cu_kv[i] a multiple of 8), with at least `gap` unused rows between
+    sequences."""
     rng = np.random.default_rng(seed)
     n = len(prefixes)
     kv_lens = np.array([p + c for p, c in zip(prefixes, chunks)], np.int32)
@@ -220,7 +221,7 @@ def extend_inputs(seed, prefixes, chunks, Hq, Hkv, D=128, gap=16, outlier_p=0.01
     r = 0
     for i in range(n):
         cu_kv[i] = r
-        r += int(kv_lens[i]) + gap
+        r = (r + int(kv_lens[i]) + gap + 7) // 8 * 8  # each sequence starts on a multiple of 8 rows
     T = int(kv_lens.sum())
     k = rng.standard_normal((T, Hkv, D)).astype(np.float32)
     v = rng.standard_normal((T, Hkv, D)).astype(np.float32)

@@ -53,13 +53,14 @@ def _device(x):
     d["cu_kv"] = torch.from_numpy(x["cu_kv"]).cuda()
     d["kv_lens"] = torch.from_numpy(x["kv_lens"]).cuda()
     d["out"] = torch.full_like(d["q"], float("nan"))
+    d["scratch"] = nv.alloc_extend_scratch(d["ws_k"])
     return d
 
 
 def _attend(d, max_q_len):
     nv = _nv()
     nv.fp8_chunked_extend_attention(d["q"], d["cu_q"], max_q_len, d["ws_k"], d["ws_v"], d["cu_kv"], d["kv_lens"],
-                                    d["ws_scale"], d["out"], err=d["err"])
+                                    d["ws_scale"], d["out"], d["scratch"], err=d["err"])
     torch.cuda.synchronize()
 
 
@@ -137,6 +138,16 @@ def test_full_size_serving_chunk_sampled(orc):
                                             x["ws_scale"])
             ok, worst = within_tol(got[row:row + 1], want)
             assert ok, f"sequence {i} query {j}: max excess {worst}"
+
+
+def test_error_flag_for_unaligned_workspace_offset():
+    x = _inputs(4, (10, 20), (30, 5), 8, 2)
+    d = _device(x)
+    d["cu_kv"][1] += 1  # a sequence must start on a multiple of 8 rows
+    _attend(d, 30)
+    assert d["err"].item() == 6  # NVKV_DEVERR_ALIGN; that sequence is skipped
+    out = d["out"].float()
+    assert torch.isfinite(out[:30]).all() and torch.isnan(out[30:]).all()
 
 
 def test_error_flag_for_more_queries_than_keys():
