@@ -41,18 +41,18 @@ namespace nvkv {
 namespace {
 
 constexpr int kXD = 128;                 // head_dim
-constexpr int kXRows = 128;              // query rows per M-tile, keys per KV tile
-constexpr int kXThreads = 192;
-constexpr int kXProducerWarp = 4;
-constexpr int kXIssuerWarp = 5;
-constexpr uint32_t kXTmemCols = 512;     // scores 0..127 and 128..255, output 256..383
-constexpr uint32_t kXColO = 256;
+constexpr int kXRows = 128;              // query rows per half, keys per KV tile
+constexpr int kXThreads = 352;           // 11 warps
+constexpr int kXKProducerWarp = 8, kXVProducerWarp = 9, kXIssuerWarp = 10;
+constexpr uint32_t kXTmemCols = 512;     // scores of half X at 128 X, its output at 256 + 128 X
 constexpr int kXTile = kXRows * kXD * 2; // one FP16 operand tile (32 KB)
 constexpr int kXSbo = 2048;              // bytes between 8-row groups of a tile
-// Shared memory: Q | K[2] | V^T[2] | P | barriers | TMEM holder, abort flag.
-constexpr int oXQ = 0, oXK = kXTile, oXV = 3 * kXTile, oXP = 5 * kXTile, oXBar = 6 * kXTile;
-constexpr int kXBars = 11;               // kv_full[2] s_full[2] s_free[2] p_full pv_done[2] fin q_full
 constexpr int kXGroupBytes = 8 * kXD * 2;  // one 8-row group of an FP16 operand tile (2 KB)
+// Shared memory: Q[2 halves] | K[2 stages] | V^T | P[2 halves] | barriers | TMEM holder, abort flag.
+constexpr int oXQ = 0, oXK = 2 * kXTile, oXV = 4 * kXTile, oXP = 5 * kXTile, oXBar = 7 * kXTile;
+// barriers: k_full[2] k_free[2] v_full s_full[2] s_free[2] p_full[2] pv_done[2] fin q_full
+constexpr int bKFull = 0, bKFree = 2, bVFull = 4, bSFull = 5, bSFree = 7, bPFull = 9, bPvDone = 11, bFin = 13,
+              bQFull = 14, kXBars = 15;
 constexpr int oXFlags = oXBar + 8 * kXBars;
 constexpr int kXSmem = oXFlags + 16;
 constexpr float kXNoMax = -1e30f;        // running max before any score (finite: exp2(-inf - m) = 0)
@@ -97,35 +97,38 @@ __device__ __forceinline__ bool warp_wait_x(uint64_t *bar, uint32_t parity, vola
 struct Tile {            // the CTA's work item, uniform over the CTA
   int h;                 // KV head
   int64_t q0;            // first query row of the sequence in q / out
-  int tok0, ntok;        // first chunk token of the M-tile, valid tokens in it
+  int tok0;              // first chunk token of the CTA (half 0); half 1 starts Tm tokens later
+  int ntok[2];           // valid tokens of each half (half 1 may have none)
   int L;                 // keys of the sequence (prefix + chunk)
   int p;                 // prefix length: chunk token t sits at position p + t
-  int64_t kv_base;       // workspace row of position 0
-  int ntiles;            // KV tiles that some row of the M-tile sees
+  int64_t kv_base;       // workspace row of position 0 (a multiple of 8)
+  int ntiles;            // KV tiles that some row of the CTA sees
 };
 
 // ---------------------------------------------------------------------------
-// The Q tile, by the softmax warps before their loop.  Thread r = (rb, dc):
-// 8-row block rb, 16-element column chunk dc; rows 8 rb + (s + dc) % 8, so
-// the eight threads of a store phase (dc = 0..7) write eight different rows
-// of their core matrices: no shared-memory bank conflicts.
+// The Q tile of half X, by that half's softmax warps before their loop.
+// Thread r = (rb, dc): 8-row block rb, 16-element column chunk dc; rows
+// 8 rb + (s + dc) % 8, so the eight threads of a store phase (dc = 0..7)
+// write eight different rows of their core matrices: no bank conflicts.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void x_load_q(const ExtendArgs &a, const Tile &t, uint8_t *smem) {
-  const int ct = static_cast<int>(threadIdx.x);
+__device__ __forceinline__ void x_load_q(const ExtendArgs &a, const Tile &t, uint8_t *smem, int X) {
+  const int ct = static_cast<int>(threadIdx.x) & 127;
   const int rb = ct >> 3, dc = ct & 7;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  const int tbase = t.tok0 + X * a.Tm;
+  const int ntok = X ? t.ntok[1] : t.ntok[0];
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     const int r = 8 * rb + ((s + dc) & 7);
     const int tok = r >> a.lgG, g = r & (a.G - 1);
     uint4 lo = zero, hi = zero;
-    if (tok < t.ntok) {
+    if (tok < ntok) {
       const uint4 *src = reinterpret_cast<const uint4 *>(
-          a.q + ((t.q0 + t.tok0 + tok) * a.Hq + static_cast<int64_t>(t.h) * a.G + g) * kXD + 16 * dc);
+          a.q + ((t.q0 + tbase + tok) * a.Hq + static_cast<int64_t>(t.h) * a.G + g) * kXD + 16 * dc);
       lo = src[0];
       hi = src[1];
     }
-    uint8_t *dst = smem + oXQ + kmaj(r, 2 * dc);
+    uint8_t *dst = smem + oXQ + X * kXTile + kmaj(r, 2 * dc);
     *reinterpret_cast<uint4 *>(dst) = make_uint4(f16x2_from_bf16x2(lo.x), f16x2_from_bf16x2(lo.y),
                                                  f16x2_from_bf16x2(lo.z), f16x2_from_bf16x2(lo.w));
     *reinterpret_cast<uint4 *>(dst + 128) = make_uint4(f16x2_from_bf16x2(hi.x), f16x2_from_bf16x2(hi.y),
@@ -134,31 +137,48 @@ __device__ __forceinline__ void x_load_q(const ExtendArgs &a, const Tile &t, uin
 }
 
 // ---------------------------------------------------------------------------
-// Producer (warp 4): tile j of keys [128 j, 128 j + 128) of the sequence is
-// row groups g0 .. g0 + 15, g0 = (cu_kv + 128 j) / 8, of the expanded tiles:
-// K as one 32 KB block (groups are contiguous per head), V^T as one 2 KB run
-// per 8-value group d (lane d).  The stage is free once the P.V of tile j - 2
-// is done.  Returns the number of tiles whose copies were issued.
+// Producers.  Tile j = keys [128 j, 128 j + 128) of the sequence = row groups
+// g0 .. g0 + 15, g0 = (cu_kv + 128 j) / 8, of the expanded tiles.
+//   warp 8: K as one 32 KB copy into stage j % 2, once both halves' QK^T of
+//           tile j - 2 are done (k_free);
+//   warp 9: V^T as one 2 KB copy per 8-value group d (lane d) into the single
+//           V^T buffer, once both halves' P.V of tile j - 1 are done.
+// Each returns the number of tiles whose copies it issued.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int x_producer(const ExtendArgs &a, const Tile &t, uint8_t *smem, uint64_t *kv_full,
-                                          uint64_t *pv_done, volatile int *abort) {
+__device__ __forceinline__ int x_produce_k(const ExtendArgs &a, const Tile &t, uint8_t *smem, uint64_t *bars,
+                                           volatile int *abort) {
   const int lane = static_cast<int>(threadIdx.x) & 31;
   const uint64_t policy = policy_evict_last();
   const uint8_t *kt = a.tiles + static_cast<int64_t>(t.h) * a.ngroups * kXGroupBytes;
-  const uint8_t *vt = a.tiles + (static_cast<int64_t>(a.Hkv) + t.h) * a.ngroups * kXGroupBytes;
   int issued = 0;
   for (int j = 0; j < t.ntiles; ++j) {
     const int b = j & 1;
-    if (j >= 2 && !warp_wait_x(&pv_done[b], static_cast<uint32_t>((j - 2) >> 1) & 1u, abort)) break;
+    if (j >= 2 && !warp_wait_x(&bars[bKFree + b], static_cast<uint32_t>((j - 2) >> 1) & 1u, abort)) break;
     const int64_t g0 = (t.kv_base + static_cast<int64_t>(j) * kXRows) >> 3;
     if (lane == 0) {
-      mbar_arrive_expect_tx(&kv_full[b], 2 * kXTile);
-      bulk_g2s(smem + oXK + b * kXTile, kt + g0 * kXGroupBytes, kXTile, &kv_full[b], policy);
+      mbar_arrive_expect_tx(&bars[bKFull + b], kXTile);
+      bulk_g2s(smem + oXK + b * kXTile, kt + g0 * kXGroupBytes, kXTile, &bars[bKFull + b], policy);
     }
     __syncwarp();
+    ++issued;
+  }
+  return issued;
+}
+
+__device__ __forceinline__ int x_produce_v(const ExtendArgs &a, const Tile &t, uint8_t *smem, uint64_t *bars,
+                                           volatile int *abort) {
+  const int lane = static_cast<int>(threadIdx.x) & 31;
+  const uint64_t policy = policy_evict_last();
+  const uint8_t *vt = a.tiles + (static_cast<int64_t>(a.Hkv) + t.h) * a.ngroups * kXGroupBytes;
+  int issued = 0;
+  for (int j = 0; j < t.ntiles; ++j) {
+    if (j >= 1 && !warp_wait_x(&bars[bPvDone + 1], static_cast<uint32_t>(j - 1) & 1u, abort)) break;
+    const int64_t g0 = (t.kv_base + static_cast<int64_t>(j) * kXRows) >> 3;
+    if (lane == 0) mbar_arrive_expect_tx(&bars[bVFull], kXTile);
+    __syncwarp();
     if (lane < 16)
-      bulk_g2s(smem + oXV + b * kXTile + lane * kXGroupBytes, vt + (lane * a.ngroups + g0) * 128, kXGroupBytes,
-               &kv_full[b], policy);
+      bulk_g2s(smem + oXV + lane * kXGroupBytes, vt + (lane * a.ngroups + g0) * 128, kXGroupBytes, &bars[bVFull],
+               policy);
     ++issued;
   }
   return issued;
@@ -218,35 +238,42 @@ __global__ void __launch_bounds__(256) extend_tiles_kernel(const uint8_t *__rest
 }
 
 // ---------------------------------------------------------------------------
-// Softmax (warps 0-3): thread r owns TMEM lane r = query row r.
+// Softmax of half X (warps 4X .. 4X + 3): thread r owns TMEM lane r = row r
+// of the half.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void x_softmax(const ExtendArgs &a, const Tile &t, uint8_t *smem, uint32_t tmem, uint64_t *s_full,
-                          uint64_t *s_free, uint64_t *p_full, uint64_t *pv_done, volatile int *abort) {
-  const int r = static_cast<int>(threadIdx.x), warp = r >> 5;
+__device__ __forceinline__ void x_softmax(const ExtendArgs &a, const Tile &t, uint8_t *smem, uint32_t tmem,
+                                          uint64_t *bars, int X, volatile int *abort) {
+  const int r = static_cast<int>(threadIdx.x) & 127, quad = r >> 5;
   const int tok = r >> a.lgG, g = r & (a.G - 1);
-  const int qpos = t.p + t.tok0 + (tok < t.ntok ? tok : t.ntok - 1);  // sees positions [0, qpos]
+  const int tbase = t.tok0 + X * a.Tm;
+  const int ntok = X ? t.ntok[1] : t.ntok[0];
+  const int nt = ntok > 0 ? ntok : 1;
+  const int qpos = t.p + tbase + (tok < nt ? tok : nt - 1);  // sees positions [0, qpos]
   const float c2 = a.ws_scale[0] * a.sm_scale * 1.4426950408889634f;  // score -> log2 units
-  const uint32_t lanes = tmem + (static_cast<uint32_t>(32 * warp) << 16);
-  const int first_partial = t.p + t.tok0;  // the smallest qpos of the M-tile
+  const uint32_t lanes = tmem + (static_cast<uint32_t>(32 * quad) << 16);
+  const uint32_t scol = static_cast<uint32_t>(X * 128), ocol = static_cast<uint32_t>(256 + X * 128);
+  const int first_partial = t.p + tbase;  // the smallest position of the half
+  uint64_t *s_full = &bars[bSFull + X], *s_free = &bars[bSFree + X], *p_full = &bars[bPFull + X];
+  uint64_t *pv_done = &bars[bPvDone + X];
+  uint8_t *ps = smem + oXP + X * kXTile;
   float m = kXNoMax, mt = kXNoMax, l = 0.0f;
   bool ok = true;
   for (int j = 0; j < t.ntiles; ++j) {
-    const int b = j & 1, kv0 = j * kXRows;
-    ok = warp_wait_x(&s_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort);
+    const int kv0 = j * kXRows;
+    ok = warp_wait_x(s_full, static_cast<uint32_t>(j) & 1u, abort);
     if (!ok) break;
     tc_fence_after();
     // the row's 128 scores: eight loads in flight, one wait
-    const uint32_t sadr = lanes + static_cast<uint32_t>(b * 128);
     uint32_t v[8][16];
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) tmem_ld16_async(sadr + 16 * ch, v[ch]);
+    for (int ch = 0; ch < 8; ++ch) tmem_ld16_async(lanes + scol + 16 * ch, v[ch]);
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch)
 #pragma unroll
       for (int e = 0; e < 16; ++e) asm volatile("" : "+r"(v[ch][e]));
     tc_fence_before();
-    mbar_arrive(&s_free[b]);  // the score buffer may take the next-but-one tile
+    mbar_arrive(s_free);  // this half's score buffer may take the next tile
     if (kv0 + kXRows - 1 > first_partial) {  // a diagonal tile (uniform): mask columns past the row's position
       const int lim = qpos - kv0;
 #pragma unroll
@@ -269,63 +296,59 @@ __device__ __forceinline__ void x_softmax(const ExtendArgs &a, const Tile &t, ui
       mt = mx2 + kXRescale;
       l *= alpha;
     }
-    const float nm = -m;
-    float la[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    uint32_t pk[64];
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch)
-#pragma unroll
-      for (int e = 0; e < 16; e += 2) {
-        float a0, a1;
-        fma_f32x2(a0, a1, __uint_as_float(v[ch][e]), __uint_as_float(v[ch][e + 1]), c2, c2, nm, nm);
-        const float p0 = ex2(a0), p1 = ex2(a1);  // masked: exp2(-inf) = 0
-        add_f32x2(la[(e >> 1) & 2], la[((e >> 1) & 2) + 1], p0, p1);
-        pk[8 * ch + e / 2] = pack_f16x2(p0, p1);
-      }
-    l += (la[0] + la[1]) + (la[2] + la[3]);
-    // P and the output are free once the previous tile's P.V is done
+    // P and the output of this half are free once its previous P.V is done
     if (j >= 1) {
-      ok = warp_wait_x(&pv_done[(j - 1) & 1], static_cast<uint32_t>((j - 1) >> 1) & 1u, abort);
+      ok = warp_wait_x(pv_done, static_cast<uint32_t>(j - 1) & 1u, abort);
       if (!ok) break;
       tc_fence_after();
       if (__any_sync(0xffffffffu, need)) {  // rescale the output rows whose max rose (warp-uniform)
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           float o[16];
-          tmem_ld16(lanes + kXColO + 16 * ch, o);
+          tmem_ld16(lanes + ocol + 16 * ch, o);
 #pragma unroll
           for (int e = 0; e < 16; ++e) o[e] *= alpha;
-          tmem_st16(lanes + kXColO + 16 * ch, o);
+          tmem_st16(lanes + ocol + 16 * ch, o);
         }
         tmem_st_wait();
       }
     }
-    uint8_t *ps = smem + oXP;
+    const float nm = -m;
+    float la[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int c = 0; c < 16; ++c)
-      *reinterpret_cast<uint4 *>(ps + kmaj(r, c)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    for (int ch = 0; ch < 8; ++ch) {
+      uint32_t pk[8];
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) {
+        float a0, a1;
+        fma_f32x2(a0, a1, __uint_as_float(v[ch][e]), __uint_as_float(v[ch][e + 1]), c2, c2, nm, nm);
+        const float p0 = ex2(a0), p1 = ex2(a1);  // masked: exp2(-inf) = 0
+        add_f32x2(la[(e >> 1) & 2], la[((e >> 1) & 2) + 1], p0, p1);
+        pk[e / 2] = pack_f16x2(p0, p1);
+      }
+      *reinterpret_cast<uint4 *>(ps + kmaj(r, 2 * ch)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      *reinterpret_cast<uint4 *>(ps + kmaj(r, 2 * ch + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    }
+    l += (la[0] + la[1]) + (la[2] + la[3]);
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(p_full);
   }
-  if (ok) {
-    const int jl = t.ntiles - 1;
-    ok = warp_wait_x(&pv_done[jl & 1], static_cast<uint32_t>(jl >> 1) & 1u, abort);
-  }
+  if (ok) ok = warp_wait_x(pv_done, static_cast<uint32_t>(t.ntiles - 1) & 1u, abort);
   if (!ok) return;
   tc_fence_after();
   const float inv = a.ws_scale[1] / l;
-  const bool write = tok < t.ntok;
-  __nv_bfloat16 *dst = a.out + ((t.q0 + t.tok0 + tok) * a.Hq + static_cast<int64_t>(t.h) * a.G + g) * kXD;
+  const bool write = tok < ntok;
+  __nv_bfloat16 *dst = a.out + ((t.q0 + tbase + tok) * a.Hq + static_cast<int64_t>(t.h) * a.G + g) * kXD;
 #pragma unroll
   for (int ch = 0; ch < 8; ++ch) {
     float o[16];
-    tmem_ld16(lanes + kXColO + 16 * ch, o);
+    tmem_ld16(lanes + ocol + 16 * ch, o);
     uint32_t w[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const __nv_bfloat162 v = __floats2bfloat162_rn(o[2 * e] * inv, o[2 * e + 1] * inv);
-      w[e] = *reinterpret_cast<const uint32_t *>(&v);
+      const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[2 * e] * inv, o[2 * e + 1] * inv);
+      w[e] = *reinterpret_cast<const uint32_t *>(&v2);
     }
     if (write) {
       *reinterpret_cast<uint4 *>(dst + 16 * ch) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -335,46 +358,54 @@ __device__ __forceinline__ void x_softmax(const ExtendArgs &a, const Tile &t, ui
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer (one thread of warp 8), polling: S_b = Q K_b^T as soon as K_b is
-// staged and S_b's previous scores are read (at most one tile ahead of P.V,
-// so the next tile's scores are computed during this tile's softmax);
-// O += P V_b as soon as P is written.
+// MMA issuer (one thread of warp 10), polling four in-order streams:
+//   QK_0(j), QK_1(j): S_X = Q_X K_j^T once K_j landed and half X's softmax has
+//                     read S_X of tile j - 1 (QK_0(j) before QK_1(j); the
+//                     commit after QK_1(j) frees K stage j % 2);
+//   PV_0(j), PV_1(j): O_X += P_X V_j once P_X is written and V_j landed
+//                     (PV_0(j) before PV_1(j); the commit after PV_1(j) frees
+//                     the V^T buffer).
+// The tensor cores so run one half's MMAs while the other half's softmax runs.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void x_issuer(uint8_t *smem, uint32_t tmem, int ntiles, uint64_t *kv_full, uint64_t *s_full,
-                         uint64_t *s_free, uint64_t *p_full, uint64_t *pv_done, volatile int *abort) {
-  const uint32_t qs = smem_u32(smem + oXQ), ps = smem_u32(smem + oXP);
+__device__ __forceinline__ void x_issuer(uint8_t *smem, uint32_t tmem, int ntiles, uint64_t *bars,
+                                         volatile int *abort) {
+  const uint32_t qs = smem_u32(smem + oXQ), ps = smem_u32(smem + oXP), vts = smem_u32(smem + oXV);
   constexpr uint32_t id = idesc_f16(kXRows);
-  int nqk = 0, npv = 0;  // next tile whose QK^T / P.V goes out
+  int nqk[2] = {0, 0}, npv[2] = {0, 0};  // next tile whose QK^T / P.V of half X goes out
   uint64_t t_last = global_timer_ns();
-  while (npv < ntiles) {
+  while (npv[1] < ntiles) {
     bool did = false;
-    // QK^T of tile nqk: K staged, and its score buffer read by the softmax of tile nqk - 2
-    if (nqk < ntiles && nqk <= npv + 1) {
-      const int b = nqk & 1;
-      if (mbar_test(&kv_full[b], static_cast<uint32_t>(nqk >> 1) & 1u) &&
-          (nqk < 2 || mbar_test(&s_free[b], static_cast<uint32_t>((nqk - 2) >> 1) & 1u))) {
+#pragma unroll
+    for (int X = 0; X < 2; ++X) {
+      const int j = nqk[X];
+      if (j < ntiles && (X == 0 || j < nqk[0]) && mbar_test(&bars[bKFull + (j & 1)], static_cast<uint32_t>(j >> 1) & 1u) &&
+          (j == 0 || mbar_test(&bars[bSFree + X], static_cast<uint32_t>(j - 1) & 1u))) {
         tc_fence_after();
-        const uint32_t ks = smem_u32(smem + oXK + b * kXTile);
+        const uint32_t ks = smem_u32(smem + oXK + (j & 1) * kXTile);
 #pragma unroll
         for (int kk = 0; kk < kXD / 16; ++kk)
-          umma_f16(tmem + static_cast<uint32_t>(b * 128), umma_desc(qs + kk * 256, 128, kXSbo),
+          umma_f16(tmem + static_cast<uint32_t>(X * 128), umma_desc(qs + X * kXTile + kk * 256, 128, kXSbo),
                    umma_desc(ks + kk * 256, 128, kXSbo), id, kk > 0 ? 1u : 0u);
-        umma_commit(&s_full[b]);
-        ++nqk;
+        umma_commit(&bars[bSFull + X]);
+        if (X == 1) umma_commit(&bars[bKFree + (j & 1)]);
+        ++nqk[X];
         did = true;
       }
     }
-    // P.V of tile npv once its P is written
-    if (npv < nqk && mbar_test(p_full, static_cast<uint32_t>(npv) & 1u)) {
-      tc_fence_after();
-      const uint32_t vt = smem_u32(smem + oXV + (npv & 1) * kXTile);
 #pragma unroll
-      for (int kk = 0; kk < kXRows / 16; ++kk)
-        umma_f16(tmem + kXColO, umma_desc(ps + kk * 256, 128, kXSbo), umma_desc(vt + kk * 256, 128, kXSbo), id,
-                 (npv > 0 || kk > 0) ? 1u : 0u);
-      umma_commit(&pv_done[npv & 1]);
-      ++npv;
-      did = true;
+    for (int X = 0; X < 2; ++X) {
+      const int j = npv[X];
+      if (j < nqk[X] && (X == 0 || j < npv[0]) && mbar_test(&bars[bPFull + X], static_cast<uint32_t>(j) & 1u) &&
+          mbar_test(&bars[bVFull], static_cast<uint32_t>(j) & 1u)) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kXRows / 16; ++kk)
+          umma_f16(tmem + static_cast<uint32_t>(256 + X * 128), umma_desc(ps + X * kXTile + kk * 256, 128, kXSbo),
+                   umma_desc(vts + kk * 256, 128, kXSbo), id, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars[bPvDone + X]);
+        ++npv[X];
+        did = true;
+      }
     }
     if (did) {
       t_last = global_timer_ns();
@@ -405,32 +436,27 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attention_kernel(const Ex
                                           : ((t.kv_base & 7) != 0 ? NVKV_DEVERR_ALIGN : NVKV_DEVERR_WS_ROWS));
     return;
   }
-  if (tid == 0 && blockIdx.x == 0 && t.h == 0 && nq > static_cast<int64_t>(gridDim.x) * a.Tm)
+  if (tid == 0 && blockIdx.x == 0 && t.h == 0 && nq > static_cast<int64_t>(gridDim.x) * 2 * a.Tm)
     set_err(a.err, NVKV_DEVERR_SEQLEN);  // more queries than max_q_len: the rest are not computed
-  const int mtile = static_cast<int>(gridDim.x - 1 - blockIdx.x);  // longest M-tiles launch first
-  t.tok0 = mtile * a.Tm;
+  const int cta = static_cast<int>(gridDim.x - 1 - blockIdx.x);  // longest work items launch first
+  t.tok0 = 2 * cta * a.Tm;
   if (t.tok0 >= nq) return;  // uniform: before any barrier or TMEM allocation
-  t.ntok = static_cast<int>(nq - t.tok0 < a.Tm ? nq - t.tok0 : a.Tm);
+  const int rest = static_cast<int>(nq - t.tok0);
+  t.ntok[0] = rest < a.Tm ? rest : a.Tm;
+  t.ntok[1] = rest - t.ntok[0] < a.Tm ? rest - t.ntok[0] : a.Tm;
   t.p = t.L - static_cast<int>(nq);
-  t.ntiles = (t.p + t.tok0 + t.ntok + kXRows - 1) / kXRows;
+  t.ntiles = (t.p + t.tok0 + t.ntok[0] + t.ntok[1] + kXRows - 1) / kXRows;
 
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + oXBar);
-  uint64_t *kv_full = bars, *s_full = bars + 2, *s_free = bars + 4, *p_full = bars + 6, *pv_done = bars + 7;
-  uint64_t *fin = bars + 9, *q_full = bars + 10;
   uint32_t *holder = reinterpret_cast<uint32_t *>(smem + oXFlags);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + oXFlags + 4);
   if (tid == 0) {
-    mbar_init(&kv_full[0], 1);  // the producer's expect_tx, then the copies' bytes
-    mbar_init(&kv_full[1], 1);
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(&s_free[0], 128);
-    mbar_init(&s_free[1], 128);
-    mbar_init(p_full, 128);
-    mbar_init(&pv_done[0], 1);
-    mbar_init(&pv_done[1], 1);
-    mbar_init(fin, 1);
-    mbar_init(q_full, 128);
+    for (int b = 0; b < kXBars; ++b) {
+      const uint32_t count = (b == bSFree || b == bSFree + 1 || b == bPFull || b == bPFull + 1) ? 128u
+                             : (b == bQFull)                                                  ? 256u
+                                                                                              : 1u;
+      mbar_init(&bars[b], count);  // count 1: an expect_tx arrive or a tcgen05.commit
+    }
     *abort = 0;
     fence_mbar_init();
   }
@@ -440,29 +466,35 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attention_kernel(const Ex
   tc_fence_after();
   const uint32_t tmem = *holder;
 
-  int issued = 0;  // producer: tiles whose copies went out
-  if (warp < 4) {
-    x_load_q(a, t, smem);
+  int issued = 0;  // producers: tiles whose copies went out
+  if (warp < 8) {
+    const int X = warp >> 2;
+    x_load_q(a, t, smem, X);
     fence_proxy_async_smem();  // generic-proxy stores -> visible to the MMAs
-    mbar_arrive(q_full);
-    x_softmax(a, t, smem, tmem, s_full, s_free, p_full, pv_done, abort);
-  } else if (warp == kXProducerWarp) {
-    issued = x_producer(a, t, smem, kv_full, pv_done, abort);
+    mbar_arrive(&bars[bQFull]);
+    x_softmax(a, t, smem, tmem, bars, X, abort);
+  } else if (warp == kXKProducerWarp) {
+    issued = x_produce_k(a, t, smem, bars, abort);
+  } else if (warp == kXVProducerWarp) {
+    issued = x_produce_v(a, t, smem, bars, abort);
   } else if (tid == kXIssuerWarp * 32) {
-    if (mbar_wait_bounded(q_full, 0u, abort))
-      x_issuer(smem, tmem, t.ntiles, kv_full, s_full, s_free, p_full, pv_done, abort);
-    umma_commit(fin);  // every MMA issued is complete before TMEM is freed
+    if (mbar_wait_bounded(&bars[bQFull], 0u, abort)) x_issuer(smem, tmem, t.ntiles, bars, abort);
+    umma_commit(&bars[bFin]);  // every MMA issued is complete before TMEM is freed
     volatile int never = 0;
-    mbar_wait_bounded(fin, 0u, &never);
+    mbar_wait_bounded(&bars[bFin], 0u, &never);
   }
   tc_fence_before();
   __syncthreads();
   if (*abort) {  // after a timeout: the last copies in flight land before the CTA exits
     if (tid == 0) set_err(a.err, NVKV_DEVERR_TIMEOUT);
-    if (warp == kXProducerWarp && (threadIdx.x & 31) == 0) {
+    if ((warp == kXKProducerWarp || warp == kXVProducerWarp) && (tid & 31) == 0) {
       volatile int never = 0;
-      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
-        mbar_wait_bounded(&kv_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, &never);
+      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j) {
+        if (warp == kXKProducerWarp)
+          mbar_wait_bounded(&bars[bKFull + (j & 1)], static_cast<uint32_t>(j >> 1) & 1u, &never);
+        else
+          mbar_wait_bounded(&bars[bVFull], static_cast<uint32_t>(j) & 1u, &never);
+      }
     }
     __syncthreads();
   }
@@ -605,7 +637,7 @@ nvkv_status fp8_chunked_extend_attention(const void *q, const int64_t *cu_q, int
   a.lgG = __builtin_ctz(static_cast<unsigned>(G));
   a.Tm = kXRows / G;
   a.sm_scale = sm_scale > 0.0f ? sm_scale : 1.0f / sqrtf(static_cast<float>(head_dim));
-  const dim3 grid(static_cast<unsigned>((max_q_len + a.Tm - 1) / a.Tm), static_cast<unsigned>(num_kv_heads),
+  const dim3 grid(static_cast<unsigned>((max_q_len + 2 * a.Tm - 1) / (2 * a.Tm)), static_cast<unsigned>(num_kv_heads),
                   static_cast<unsigned>(n));
   if (cudaFuncSetAttribute(extend_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kXSmem) !=
       cudaSuccess)
