@@ -123,8 +123,8 @@ nvkv_status nvkv_global_scale(const void *x, nvkv_dtype dtype, int64_t n, float 
  * this equals the scale of the whole tensor). */
 nvkv_status nvkv_amax_update(const void *x, nvkv_dtype dtype, int64_t n, float *amax, void *stream);
 
-/* NVFP4 quantized write into paged slots ([P1] 02 "quantized write"; [P2] Three
- * Paths: new KV "is quantized into the NVFP4 cache").
+/* NVFP4 quantized write into paged slots ([P1] 02, the quantized write; [P2]
+ * Three Paths: new KV goes into the NVFP4 cache quantized).
  *   k, v          [num_tokens][num_kv_heads][head_dim] of `dtype` (BF16 widens exactly)
  *   slot_mapping  [num_tokens] int64 device; a negative slot skips the token
  *   global_scale  device float[2] {g_K, g_V}; NULL -> cache->kv_scale
@@ -153,8 +153,8 @@ size_t nvkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t nu
 nvkv_status nvkv_decode_workspace_init(void *workspace, size_t bytes, void *stream);
 
 /* Paged GQA decode attention over the NVFP4 or FP8 cache ([P2] Three Paths:
- * decode "reads NVFP4 directly and dequantizes on the fly"; [P1] 03 per-layer
- * precision).
+ * the decode kernel reads the NVFP4 cache itself and dequantizes inside the
+ * kernel; [P1] 03 per-layer precision).
  *   q               [batch][num_q_heads][head_dim] BF16, device
  *   block_table     [batch][max_pages] int32 page ids, device
  *   seq_lens        [batch] int32 visible tokens per sequence (the token written
@@ -215,8 +215,8 @@ nvkv_status nvfp4_paged_decode_attention_noalloc(const void *q, const nvkv_cache
                                                  void *out, void *stream);
 
 /* Chunked-extend prefix dequant into the shared FP8 workspace ([P2] Three
- * Paths: "the cached prefix is gathered out and dequantized into a cross-layer
- * shared FP8 workspace").  For i < n, tokens [0, prefix_lens[i]) of sequence
+ * Paths: for chunked extend the cached prefix is gathered and dequantized into
+ * an FP8 workspace shared by all layers).  For i < n, tokens [0, prefix_lens[i]) of sequence
  * seq_ids[i] land in rows cu_prefix[i] + t of ws_k / ws_v, layout
  * [rows][num_kv_heads][head_dim] E4M3:
  *   byte = E4M3_rne_satfinite((e2m1 * S) * (g / ws_scale))   (FP32, per K and V)
@@ -236,8 +236,8 @@ nvkv_status nvfp4_kv_dequant_to_fp8_workspace(const int32_t *block_table, int32_
                                               int64_t ws_rows, void *stream);
 
 /* The current chunk's K/V into the shared FP8 workspace ([P2] Three Paths:
- * the dequantized prefix is "concatenated with the current chunk's KV for FP8
- * attention").  The pages give no rule for the chunk's bytes; this library
+ * the chunk's KV is appended to the dequantized prefix and FP8 attention runs
+ * over both).  The pages give no rule for the chunk's bytes; this library
  * uses the FP8 layers' per-tensor quantizer with the workspace scale:
  *   byte = E4M3_rne_satfinite(x / ws_scale)          (FP32 divide, per K and V)
  *   k, v        [num_tokens][num_kv_heads][head_dim] of `dtype`, device,

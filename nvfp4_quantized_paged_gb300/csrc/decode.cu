@@ -1,6 +1,6 @@
 // Paged GQA decode attention reading the NVFP4 (or FP8 E4M3) cache straight
 // from HBM ("SGLang x Qwen x NVIDIA ...", Three Paths: decode is memory-bound,
-// so the kernel reads NVFP4 directly and dequantizes on the fly; it must read
+// so the kernel reads the NVFP4 cache itself and dequantizes inside; it must read
 // exactly as much as it computes).  The per-layer FP8 variant serves the
 // sensitive layers ("SOAR Weekly Champion Notes 05", 03).
 //

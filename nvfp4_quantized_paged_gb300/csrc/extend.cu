@@ -2,10 +2,10 @@
 // the current chunk's K/V into that workspace (sm_103a).
 //
 // "SGLang x Qwen x NVIDIA Collaboration: NVFP4 KV Cache Breaks Long-Context
-// and Agentic Inference Bottlenecks", section "Three Paths": in chunked
-// prefill / extend the cached prefix is dequantized into a cross-layer shared
-// FP8 workspace, concatenated with the current chunk's KV, and the chunk's
-// queries run FP8 attention over the concatenation (causal inside the chunk).
+// and Agentic Inference Bottlenecks", section "Three Paths": for chunked
+// prefill / extend the cached prefix is dequantized into an FP8 workspace that
+// all layers share, the current chunk's KV is appended to it, and the chunk's
+// queries run FP8 attention over both (causal inside the chunk).
 //
 // Two kernels per call.  extend_tiles_kernel expands the E4M3 workspace once
 // into FP16 operand tiles in the tensor cores' K-major layout (K by 8-row

@@ -162,7 +162,7 @@ def global_scale(x: np.ndarray, divisor: float = NVFP4_GLOBAL_DIVISOR) -> np.flo
 
 
 # --------------------------------------------------------------------------
-# Paged cache ([P1] 02 "FP4 memory pool"; [P2] Three Paths, paged KV cache)
+# Paged cache ([P1] 02, the FP4 memory pool; [P2] Three Paths, paged KV cache)
 # --------------------------------------------------------------------------
 
 class Cache:
@@ -327,7 +327,7 @@ def dequant_to_fp8_workspace(cache: Cache, block_table: np.ndarray, seq_ids, pre
 def fp8_workspace_append(ws_k: np.ndarray, ws_v: np.ndarray, k: np.ndarray, v: np.ndarray, rows: np.ndarray,
                          ws_scale) -> None:
     """The current chunk's K/V into FP8 workspace rows ([P2] Three Paths: the
-    prefix is "concatenated with the current chunk's KV for FP8 attention").
+    chunk's KV is appended to the dequantized prefix for FP8 attention).
 
     ``k``, ``v``: [T, Hkv, D] (FP32 or BF16-exact values); token t goes to row
     ``rows[t]`` (negative: skipped) as E4M3_RNE_sat(x / ws_scale) per tensor.

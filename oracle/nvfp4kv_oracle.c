@@ -93,8 +93,8 @@ uint8_t orc_e2m1_encode(float y) {
 }
 
 /* ------------------------------------------------------------------------ */
-/* E4M3, the OCP 8-bit "fn" variant ([P2] Core of the Ledger: "FP8 (E4M3)     */
-/* block-level scale"; [P1] 01: FP8 KV cache): bias 7, 3 mantissa bits,       */
+/* E4M3, the OCP 8-bit "fn" variant ([P2] Core of the Ledger: the per-16   */
+/* value block scale is E4M3; [P1] 01: FP8 KV cache): bias 7, 3 mantissa bits, */
 /* subnormals m*2^-9, no infinities, 0x7F/0xFF = NaN, largest finite 448.     */
 /* ------------------------------------------------------------------------ */
 
@@ -153,8 +153,8 @@ void orc_e4m3_encode_bits(uint32_t start, uint32_t count, uint8_t *out) {
 }
 
 /* ------------------------------------------------------------------------ */
-/* Global scale ([P2] Core of the Ledger: "the whole tensor gets one FP32     */
-/* global scale").  g = amax / divisor, divisor 2688 = 6*448 for NVFP4 and    */
+/* Global scale ([P2] Core of the Ledger: one FP32 scale per tensor).        */
+/* g = amax / divisor, divisor 2688 = 6*448 for NVFP4 and                     */
 /* 448 for the FP8 per-tensor scale.                                          */
 /* ------------------------------------------------------------------------ */
 
@@ -286,8 +286,8 @@ int orc_v_code_layout(int P, int D, int off, int64_t *pos, int32_t *shift) {
   return 0;
 }
 
-/* Quantized write into paged slots ([P1] 02 "quantized write"; [P2] Three
- * Paths: the current chunk "is quantized into the NVFP4 cache").
+/* Quantized write into paged slots ([P1] 02, the quantized write; [P2] Three
+ * Paths: new KV goes into the NVFP4 cache quantized).
  * k, v: [T][Hkv][D] FP32.  slot = page*P + offset; slot < 0 skips the token.
  * g[0], g[1] = global scales of K and V.  Returns 0, or -1 on a bad slot. */
 int orc_nvfp4_quantize_write(const float *k, const float *v, int64_t T, int Hkv, int D,
@@ -472,8 +472,8 @@ int orc_paged_decode_attention(const uint16_t *q, int B, int Hq, int Hkv, int D,
 
 /* ------------------------------------------------------------------------ */
 /* Chunked-extend dequant into the shared FP8 workspace ([P2] Three Paths:    */
-/* "the cached prefix is gathered out and dequantized into a cross-layer      */
-/* shared FP8 workspace").  For sequence seq_ids[i], tokens [0, prefix_lens[i]) */
+/* for chunked extend the cached prefix is gathered and dequantized into an   */
+/* FP8 workspace shared by all layers).  For sequence seq_ids[i], tokens [0, prefix_lens[i]) */
 /* go to workspace rows cu_prefix[i] + t, layout [rows][Hkv][D] E4M3:          */
 /*   w = e2m1(code) * S       (exact in FP32)                                 */
 /*   r = g / ws_scale         (FP32 divide, once per K and V)                  */
@@ -512,9 +512,9 @@ int orc_dequant_to_fp8_workspace(const int32_t *block_table, int max_pages, cons
 }
 
 /* ------------------------------------------------------------------------ */
-/* The current chunk joins the FP8 workspace ([P2] Three Paths: the prefix in */
-/* the shared FP8 workspace is "concatenated with the current chunk's KV for  */
-/* FP8 attention").  The pages give no rule for the chunk's FP8 bytes; the    */
+/* The current chunk joins the FP8 workspace ([P2] Three Paths: the chunk's  */
+/* KV is appended to the dequantized prefix in the FP8 workspace and FP8      */
+/* attention runs over both).  The pages give no rule for the chunk's FP8 bytes; the    */
 /* plainest reading is the per-tensor FP8 quantizer of the FP8 layers with    */
 /* the workspace scale: byte = E4M3_RNE_sat(x / ws_scale) (FP32 divide).      */
 /* Token t of k / v ([T][Hkv][D] FP32) goes to workspace row rows[t]          */
