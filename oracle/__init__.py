@@ -88,6 +88,9 @@ def lib():
         L.orc_fp8_extend_attention.restype = ctypes.c_int
         L.orc_fp8_extend_attention.argtypes = [_u16p, _i64p, _u8p, _u8p, _i64p, _i32p, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int, _f32p, ctypes.c_double, _f64p]
+        L.orc_nvfp4_requantize_write_fp8.restype = ctypes.c_int
+        L.orc_nvfp4_requantize_write_fp8.argtypes = [_u8p, _u8p, _f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                                     _i64p, _f32p, ctypes.c_int, ctypes.c_int64, _u8p]
         _LIB = L
     return _LIB
 
@@ -259,6 +262,22 @@ def quantize_write(cache: Cache, k: np.ndarray, v: np.ndarray, slot_mapping: np.
     else:
         rc = L.orc_fp8_quantize_write(_p(k, _f32p), _p(v, _f32p), T, cache.Hkv, cache.D, _p(sm, _i64p),
                                       _p(cache.g, _f32p), cache.P, cache.num_pages, _p(cache.data, _u8p))
+    if rc != 0:
+        raise ValueError("slot out of range")
+
+
+def requantize_write_fp8(cache: Cache, k8: np.ndarray, v8: np.ndarray, s8, slot_mapping: np.ndarray) -> None:
+    """Initial-prefill write from FP8 K/V ([P2] Three Paths: the prefill's FP8
+    KV is requantized into the NVFP4 cache): x = E4M3(byte) * s8 (one FP32
+    multiply), then the NVFP4 quantized write with the cache's global scales."""
+    assert cache.prec == PREC_NVFP4
+    kk = _c(k8, np.uint8)
+    vv = _c(v8, np.uint8)
+    T, Hkv, D = kk.shape
+    sc = _c(s8, np.float32).reshape(2)
+    sm = _c(slot_mapping, np.int64)
+    rc = lib().orc_nvfp4_requantize_write_fp8(_p(kk, _u8p), _p(vv, _u8p), _p(sc, _f32p), T, Hkv, D, _p(sm, _i64p),
+                                              _p(cache.g, _f32p), cache.P, cache.num_pages, _p(cache.data, _u8p))
     if rc != 0:
         raise ValueError("slot out of range")
 

@@ -591,3 +591,29 @@ int orc_fp8_extend_attention(const uint16_t *q, const int64_t *cu_q, const uint8
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Initial-prefill write from FP8 ([P2] Three Paths: in the initial prefill  */
+/* the attention runs on FP8 K/V and the KV is requantized from FP8 into the */
+/* NVFP4 cache).  The FP8 input is decoded with its per-tensor scale, one   */
+/* FP32 multiply per value, x = E4M3(byte) * s8[kind] (exact E4M3 value,    */
+/* rounded once), then written by the NVFP4 quantized write above with the  */
+/* NVFP4 global scales g.  k8, v8: [T][Hkv][D] E4M3 bytes.                  */
+/* ------------------------------------------------------------------------ */
+int orc_nvfp4_requantize_write_fp8(const uint8_t *k8, const uint8_t *v8, const float *s8, int64_t T, int Hkv,
+                                   int D, const int64_t *slot_mapping, const float *g, int P, int64_t num_pages,
+                                   uint8_t *cache) {
+  const int64_t n = T * Hkv * D;
+  float *k = (float *)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1));
+  float *v = (float *)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1));
+  int64_t i;
+  int rc;
+  for (i = 0; i < n; ++i) {
+    k[i] = (float)orc_e4m3_value(k8[i]) * s8[0];
+    v[i] = (float)orc_e4m3_value(v8[i]) * s8[1];
+  }
+  rc = orc_nvfp4_quantize_write(k, v, T, Hkv, D, slot_mapping, g, P, num_pages, cache);
+  free(k);
+  free(v);
+  return rc;
+}
