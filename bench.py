@@ -21,6 +21,9 @@ torch.distributed.
 --workload extend_b4_chunk2k: the chunked-extend pass instead (the chunk's
 FP8 workspace append and the causal FP8 extend attention), metric TFLOP/s.
 
+--workload prefill_write_b4_16k: the initial-prefill write (FP8 K/V
+requantized into the NVFP4 cache), metric HBM GB/s.
+
 --impl reference: the CPU oracle (scalar C, one thread) on a bounded sample of
 the same workload, as the reference arm.
 """
@@ -522,6 +525,103 @@ def extend_cpu_baseline(x, ws_scale, Hq, budget_s=10.0):
             "host_cores": os.cpu_count()}
 
 
+PREFILL_METRIC = "prefill FP8 -> NVFP4 requantize-write: HBM GB/s"
+PREFILL_SPECS = {"prefill_write_b4_16k": dict(tokens=4 * 16384, Hkv=8, P=64)}
+
+
+def run_prefill_write(args):
+    """The initial-prefill write: FP8 K/V of a batch of prompts (4 x 16384
+    tokens, 8 KV heads) requantized into the NVFP4 paged cache."""
+    dist, rank, ws, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import nvfp4_quantized_paged_gb300 as nv
+    nv.lib()
+    c = PREFILL_SPECS[args.workload]
+    T, Hkv, P = c["tokens"], c["Hkv"], c["P"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per = T * Hkv * (2 * 128 + 144)
+    reps = max(2, -(-3 * l2 // per))
+    sets = []
+    for _ in range(reps):
+        k = torch.randn(T, Hkv, 128, device=dev, generator=gen)
+        v = torch.randn(T, Hkv, 128, device=dev, generator=gen)
+        s8 = torch.stack([k.abs().max(), v.abs().max()]).float() / 448.0
+        k8 = (k / s8[0]).to(torch.float8_e4m3fn).view(torch.uint8)  # the prefill's FP8 K/V (input)
+        v8 = (v / s8[1]).to(torch.float8_e4m3fn).view(torch.uint8)
+        g = torch.zeros(2, dtype=torch.float32, device=dev)
+        nv.nvkv_global_scale((k8.view(torch.float8_e4m3fn).float() * s8[0]).contiguous(), g[0:1], nv.NVFP4_GLOBAL_DIVISOR)
+        nv.nvkv_global_scale((v8.view(torch.float8_e4m3fn).float() * s8[1]).contiguous(), g[1:2], nv.NVFP4_GLOBAL_DIVISOR)
+        cache = nv.Cache(nv.PREC_NVFP4, T // P, Hkv, P, device=dev, kv_scale=g)
+        slots = torch.randperm(T, device=dev, generator=gen)  # pages in permuted order
+        sets.append(dict(k8=k8, v8=v8, s8=s8, g=g, cache=cache, slots=slots))
+        del k, v
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        r = sets[i % reps]
+        nv.nvfp4_kv_requantize_write_fp8(r["k8"], r["v8"], r["s8"], r["slots"], r["g"], r["cache"])
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    g_step = _graph(lambda: [step(i) for i in range(args.steps)])
+    g_step.replay()
+    torch.cuda.synchronize()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    with Clocks(gpu_id) as clk:
+        ms = _time_graph(g_step, stream) / args.steps
+    ms = _max_over_ranks(dist, ms, dev)
+    # e2e: FP8 K/V from pinned host memory, a cache page block back
+    hk, hv = sets[0]["k8"].cpu().pin_memory(), sets[0]["v8"].cpu().pin_memory()
+    hb = torch.empty(sets[0]["cache"].data[0].shape, dtype=torch.uint8).pin_memory()
+
+    def e2e_step(i):
+        r = sets[i % reps]
+        r["k8"].copy_(hk, non_blocking=True)
+        r["v8"].copy_(hv, non_blocking=True)
+        step(i)
+        hb.copy_(r["cache"].data[0], non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    peak, peak_kind = _peaks()
+    gbs = per / (ms * 1e-3) / 1e9
+    if rank == 0:
+        line = {"metric": PREFILL_METRIC, "value": round(ws * gbs, 1), "unit": "GB/s", "n_gpus": ws,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32 (E4M3 decode x scale, NVFP4 quantizer)",
+                "data": "synthetic (seeded N(0,1) K/V quantized to FP8 by torch as the input)",
+                "config": {"workload": args.workload, "tokens": T, "Hkv": Hkv, "D": 128, "page": P,
+                           "l2": f"inputs and caches rotate over {reps} replicas (>= 3x L2)",
+                           "parallelism": f"replicas x{ws}", "launch": "one CUDA graph of the K timed steps"},
+                "e2e": {"value": round(per / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+                        "h2d_bytes_per_step": int(hk.numel() * 2), "d2h_bytes_per_step": int(hb.numel())},
+                "gpu_launches": args.steps,
+                "roofline": {"bound": "hbm", "kernel": "nvfp4_write_kernel<uint8_t>", "achieved": round(gbs, 1),
+                             "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(gbs / peak, 4),
+                             "traffic": None, "algorithmic_bytes_per_launch": int(per),
+                             "avg_launch_us": round(ms * 1e3, 2),
+                             "timed": "CUDA events around one graph of K write launches, replicas rotated"},
+                "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def _traffic_from_profile(workload):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current decode kernel source (else None)."""
@@ -628,6 +728,8 @@ def main():
         run_reference(args)
     elif args.workload in EXTEND_SPECS:
         run_extend(args)
+    elif args.workload in PREFILL_SPECS:
+        run_prefill_write(args)
     else:
         run_ours(args)
 

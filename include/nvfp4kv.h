@@ -134,6 +134,21 @@ nvkv_status nvfp4_kv_quantize_write(const void *k, const void *v, nvkv_dtype dty
                                     const int64_t *slot_mapping, const float *global_scale,
                                     const nvkv_cache *cache, void *stream);
 
+/* Initial-prefill write from FP8 K/V into the NVFP4 cache ([P2] Three Paths:
+ * the initial prefill computes on FP8 K/V and requantizes that KV into the
+ * NVFP4 cache; it reads no cache, so no dequant round trip).  Each value is
+ * decoded with its tensor's FP8 scale, x = E4M3(byte) * in_scale[kind] (one
+ * FP32 multiply), then quantized exactly as nvfp4_kv_quantize_write does.
+ *   k8, v8        [num_tokens][num_kv_heads][head_dim] E4M3 bytes, device,
+ *                 16-byte aligned
+ *   in_scale      device float[2] {K, V}: the FP8 per-tensor scales
+ *   slot_mapping, global_scale, cache: as nvfp4_kv_quantize_write (the global
+ *                 scales are those of the decoded values)
+ * One kernel on `stream`. */
+nvkv_status nvfp4_kv_requantize_write_fp8(const uint8_t *k8, const uint8_t *v8, const float *in_scale,
+                                          int64_t num_tokens, const int64_t *slot_mapping, const float *global_scale,
+                                          const nvkv_cache *cache, void *stream);
+
 /* FP8 E4M3 write for the FP8 layers ([P1] 03: sensitive layers keep an FP8 KV
  * cache).  Same arguments; global_scale = per-tensor {s8_K, s8_V}; cache->prec
  * must be NVKV_PREC_FP8_E4M3. */

@@ -8,7 +8,7 @@ if the library is missing, loading it raises.
 
 Functions keep the C names:
   nvkv_global_scale, nvkv_amax_update, nvfp4_kv_quantize_write,
-  fp8_kv_quantize_write, nvkv_decode_workspace_size,
+  fp8_kv_quantize_write, nvfp4_kv_requantize_write_fp8, nvkv_decode_workspace_size,
   nvkv_decode_workspace_init, nvfp4_paged_decode_attention,
   fp8_paged_decode_attention, nvfp4_kv_dequant_to_fp8_workspace,
   fp8_workspace_append_chunk, fp8_extend_scratch_size,
@@ -80,6 +80,7 @@ SIGNATURES = {
     "nvkv_amax_update": (_i32, [_vp, _i32, _i64, _vp, _vp]),
     "nvfp4_kv_quantize_write": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _cachep, _vp]),
     "fp8_kv_quantize_write": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _cachep, _vp]),
+    "nvfp4_kv_requantize_write_fp8": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp, _cachep, _vp]),
     "nvkv_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "nvkv_decode_workspace_init": (_i32, [_vp, _sz, _vp]),
     "nvfp4_paged_decode_attention": (_i32, [_vp, _cachep, _vp, _i32, _vp, _i32, _i32, _i32, _f32, _i32, _vp, _sz,
@@ -213,6 +214,16 @@ def fp8_kv_quantize_write(k, v, slot_mapping, global_scale, cache: Cache, stream
     _check("fp8_kv_quantize_write",
            lib().fp8_kv_quantize_write(_ptr(k), _ptr(v), _dtype_code(k), slot_mapping.numel(), _ptr(slot_mapping),
                                        _ptr(global_scale), ctypes.byref(d), _stream(stream)))
+
+
+def nvfp4_kv_requantize_write_fp8(k8, v8, in_scale, slot_mapping, global_scale, cache: Cache, stream=None):
+    """Initial-prefill write: FP8 K/V bytes (uint8 [T, Hkv, D]) with their
+    per-tensor scales ``in_scale`` (float32[2]) requantized into the NVFP4 cache."""
+    d = cache.desc()
+    _check("nvfp4_kv_requantize_write_fp8",
+           lib().nvfp4_kv_requantize_write_fp8(_ptr(k8), _ptr(v8), _ptr(in_scale), slot_mapping.numel(),
+                                               _ptr(slot_mapping), _ptr(global_scale), ctypes.byref(d),
+                                               _stream(stream)))
 
 
 def nvkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim=HEAD_DIM, num_splits=0) -> int:

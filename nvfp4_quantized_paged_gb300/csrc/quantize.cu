@@ -54,6 +54,21 @@ __device__ __forceinline__ void load16(const __nv_bfloat16 *src, float (&x)[16])
   }
 }
 
+// E4M3 input with its per-tensor scale (the prefill's FP8 K/V): each value
+// decoded exactly, then one FP32 multiply, x = E4M3(byte) * s8.
+__device__ __forceinline__ void load16(const uint8_t *src, float s8, float (&x)[16]) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t lo = f16x2_from_e4m3x2<0>(w[j]), hi = f16x2_from_e4m3x2<1>(w[j]);
+    x[4 * j + 0] = __fmul_rn(f32_lo(lo), s8);
+    x[4 * j + 1] = __fmul_rn(f32_hi(lo), s8);
+    x[4 * j + 2] = __fmul_rn(f32_lo(hi), s8);
+    x[4 * j + 3] = __fmul_rn(f32_hi(hi), s8);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Global scale: amax over the tensor (atomic max on the bit pattern of a
 // non-negative float), then one FP32 divide.
@@ -94,11 +109,13 @@ __global__ void divide_kernel(float *out, float divisor) {
 
 // ---------------------------------------------------------------------------
 // NVFP4 quantized write.  Thread = (token, KV head, 16-block); gridDim.y = K|V.
+// T = uint8_t: E4M3 input decoded with in_scale[kind] (initial prefill).
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(256)
     nvfp4_write_kernel(const T *__restrict__ k, const T *__restrict__ v, int64_t num_tokens,
-                       const int64_t *__restrict__ slot_mapping, const float *__restrict__ gs, CacheDev c) {
+                       const int64_t *__restrict__ slot_mapping, const float *__restrict__ gs, CacheDev c,
+                       const float *__restrict__ in_scale) {
   // programmatic dependent of the previous kernel: wait for it before any
   // global access, then let the next kernel start its set-up
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -120,7 +137,10 @@ __global__ void __launch_bounds__(256)
   const int64_t page = slot / c.P;
   const int off = static_cast<int>(slot % c.P);
   float x[16];
-  load16((kind == 0 ? k : v) + th * kD + 16 * blk, x);
+  if constexpr (sizeof(T) == 1)
+    load16((kind == 0 ? k : v) + th * kD + 16 * blk, in_scale[kind], x);
+  else
+    load16((kind == 0 ? k : v) + th * kD + 16 * blk, x);
   const float g = gs[kind];
   float amax = 0.0f;
 #pragma unroll
@@ -360,10 +380,11 @@ nvkv_status write_common(const void *k, const void *v, nvkv_dtype dtype, int64_t
   if (prec == NVKV_PREC_NVFP4) {
     if (dtype == NVKV_DTYPE_F32)
       launch_pdl(nvfp4_write_kernel<float>, grid, s, static_cast<const float *>(k), static_cast<const float *>(v),
-                 num_tokens, slot_mapping, gs, c);
+                 num_tokens, slot_mapping, gs, c, static_cast<const float *>(nullptr));
     else
       launch_pdl(nvfp4_write_kernel<__nv_bfloat16>, grid, s, static_cast<const __nv_bfloat16 *>(k),
-                 static_cast<const __nv_bfloat16 *>(v), num_tokens, slot_mapping, gs, c);
+                 static_cast<const __nv_bfloat16 *>(v), num_tokens, slot_mapping, gs, c,
+                 static_cast<const float *>(nullptr));
   } else {
     if (dtype == NVKV_DTYPE_F32)
       launch_pdl(fp8_write_kernel<float>, grid, s, static_cast<const float *>(k), static_cast<const float *>(v),
@@ -424,6 +445,23 @@ nvkv_status fp8_kv_quantize_write(const void *k, const void *v, nvkv_dtype dtype
                                   const int64_t *slot_mapping, const float *global_scale, const nvkv_cache *cache,
                                   void *stream) {
   return write_common(k, v, dtype, num_tokens, slot_mapping, global_scale, cache, stream, NVKV_PREC_FP8_E4M3);
+}
+
+nvkv_status nvfp4_kv_requantize_write_fp8(const uint8_t *k8, const uint8_t *v8, const float *in_scale,
+                                          int64_t num_tokens, const int64_t *slot_mapping, const float *global_scale,
+                                          const nvkv_cache *cache, void *stream) {
+  nvkv_status st = check_cache(cache, NVKV_PREC_NVFP4);
+  if (st != NVKV_OK) return st;
+  if (num_tokens < 0) return NVKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return NVKV_OK;
+  if (!k8 || !v8 || !in_scale || !slot_mapping) return NVKV_ERR_INVALID_ARG;
+  if (!aligned16(k8) || !aligned16(v8)) return NVKV_ERR_UNSUPPORTED;
+  const float *gs = global_scale ? global_scale : cache->kv_scale;
+  const int64_t items = num_tokens * cache->num_kv_heads * kBlocksPerRow;
+  dim3 grid(grid_for(items, 256), 2);
+  launch_pdl(nvfp4_write_kernel<uint8_t>, grid, static_cast<cudaStream_t>(stream), k8, v8, num_tokens, slot_mapping,
+             gs, to_dev(cache), in_scale);
+  return launch_status();
 }
 
 nvkv_status nvkv_encode_e2m1(const float *x, int64_t n, uint8_t *out, void *stream) {
