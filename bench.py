@@ -555,7 +555,9 @@ def run_prefill_write(args):
         nv.nvkv_global_scale((k8.view(torch.float8_e4m3fn).float() * s8[0]).contiguous(), g[0:1], nv.NVFP4_GLOBAL_DIVISOR)
         nv.nvkv_global_scale((v8.view(torch.float8_e4m3fn).float() * s8[1]).contiguous(), g[1:2], nv.NVFP4_GLOBAL_DIVISOR)
         cache = nv.Cache(nv.PREC_NVFP4, T // P, Hkv, P, device=dev, kv_scale=g)
-        slots = torch.randperm(T, device=dev, generator=gen)  # pages in permuted order
+        pages = torch.randperm(T // P, device=dev, generator=gen)  # each prompt fills its pages in order,
+        t = torch.arange(T, device=dev)                              # the pages themselves permuted
+        slots = pages[t // P] * P + t % P
         sets.append(dict(k8=k8, v8=v8, s8=s8, g=g, cache=cache, slots=slots))
         del k, v
     stream = torch.cuda.current_stream()

@@ -107,6 +107,35 @@ __global__ void divide_kernel(float *out, float divisor) {
   out[0] = __fdiv_rn(amax, divisor);
 }
 
+// One 16-value block: its E4M3 scale byte and 16 E2M1 codes, two per byte
+// (value 2j in the low nibble of byte j): lo = values 0..7, hi = 8..15.
+__device__ __forceinline__ void quant16(const float (&x)[16], float g, uint32_t &sbyte, uint32_t &lo, uint32_t &hi) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  sbyte = 0;
+  float den = 0.0f;
+  if (g != 0.0f) {
+    const float d = __fmul_rn(6.0f, g);
+    const float sf = __fdiv_rn(amax, d);
+    sbyte = e4m3x2_from_f32(sf, 0.0f) & 0xFFu;
+    den = __fmul_rn(f32_from_e4m3(sbyte), g);
+  }
+  lo = hi = 0;
+  if (den != 0.0f) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      lo |= e2m1x2_from_f32(__fdiv_rn(x[2 * j], den), __fdiv_rn(x[2 * j + 1], den)) << (8 * j);
+      hi |= e2m1x2_from_f32(__fdiv_rn(x[8 + 2 * j], den), __fdiv_rn(x[8 + 2 * j + 1], den)) << (8 * j);
+    }
+  }
+}
+
+// Four 4-bit codes (bits 15:0) -> the low nibbles of four bytes.
+__device__ __forceinline__ uint32_t spread4(uint32_t four) {
+  return (four & 0xFu) | ((four & 0xF0u) << 4) | ((four & 0xF00u) << 8) | ((four & 0xF000u) << 12);
+}
+
 // ---------------------------------------------------------------------------
 // NVFP4 quantized write.  Thread = (token, KV head, 16-block); gridDim.y = K|V.
 // T = uint8_t: E4M3 input decoded with in_scale[kind] (initial prefill).
@@ -128,7 +157,9 @@ __global__ void __launch_bounds__(256)
   const int64_t th = gid / kBlocksPerRow;  // token * Hkv + head
   const int h = static_cast<int>(th % c.Hkv);
   const int64_t t = th / c.Hkv;
+  const int64_t tp = t ^ 1;
   const int64_t slot = slot_mapping[t];
+  const int64_t slot_p = (kind == 1 && tp < num_tokens) ? slot_mapping[tp] : -1;  // loaded together
   if (slot < 0) return;
   if (slot >= static_cast<int64_t>(c.num_pages) * c.P) {
     if (kind == 0 && h == 0 && blk == 0) set_err(c.err, NVKV_DEVERR_SLOT);
@@ -136,47 +167,54 @@ __global__ void __launch_bounds__(256)
   }
   const int64_t page = slot / c.P;
   const int off = static_cast<int>(slot % c.P);
+  // V: value 16 blk + j goes to byte j of the pair's 16 bytes, nibble off % 2.
+  // When the neighbouring token (t ^ 1) holds the partner slot (tokens written
+  // in slot order, as prefill and decode do), the even token's thread writes
+  // both slots' bytes with plain stores and the odd one has nothing to do;
+  // otherwise this slot's nibbles are cleared and set with atomics (the
+  // partner slot may be written by another thread of the same launch).
+  const bool paired = slot_p == (slot ^ 1);
+  if (paired && (t & 1)) return;
   float x[16];
   if constexpr (sizeof(T) == 1)
     load16((kind == 0 ? k : v) + th * kD + 16 * blk, in_scale[kind], x);
   else
     load16((kind == 0 ? k : v) + th * kD + 16 * blk, x);
-  const float g = gs[kind];
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  uint32_t sbyte = 0;
-  float den = 0.0f;
-  if (g != 0.0f) {
-    const float d = __fmul_rn(6.0f, g);
-    const float sf = __fdiv_rn(amax, d);
-    sbyte = e4m3x2_from_f32(sf, 0.0f) & 0xFFu;
-    den = __fmul_rn(f32_from_e4m3(sbyte), g);
-  }
-  uint32_t lo = 0, hi = 0;
-  if (den != 0.0f) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      lo |= e2m1x2_from_f32(__fdiv_rn(x[2 * j], den), __fdiv_rn(x[2 * j + 1], den)) << (8 * j);
-      hi |= e2m1x2_from_f32(__fdiv_rn(x[8 + 2 * j], den), __fdiv_rn(x[8 + 2 * j + 1], den)) << (8 * j);
-    }
-  }
+  uint32_t sbyte, lo, hi;
+  quant16(x, gs[kind], sbyte, lo, hi);
   if (kind == 0) {
     *reinterpret_cast<uint2 *>(c.data + c.nv_kcodes(page, h, off, blk)) = make_uint2(lo, hi);
-  } else {
-    // V: value 16 blk + j goes to byte j of the pair's 16 bytes, nibble off % 2;
-    // the partner slot owns the other nibbles, so each word is cleared and set
-    // with atomics on this slot's nibbles only (the partner may be written by
-    // another thread of the same launch)
-    uint32_t *dst = reinterpret_cast<uint32_t *>(c.data + c.nv_vcodes(page, h, off, blk));
-    const int sh = 4 * (off & 1);
+    c.data[c.nv_scale(page, h, kind, off, blk)] = static_cast<uint8_t>(sbyte);
+    return;
+  }
+  uint32_t *dst = reinterpret_cast<uint32_t *>(c.data + c.nv_vcodes(page, h, off, blk));
+  if (paired) {
+    float y[16];
+    if constexpr (sizeof(T) == 1)
+      load16(v + (tp * c.Hkv + h) * kD + 16 * blk, in_scale[kind], y);
+    else
+      load16(v + (tp * c.Hkv + h) * kD + 16 * blk, y);
+    uint32_t sb2, lo2, hi2;
+    quant16(y, gs[kind], sb2, lo2, hi2);
+    const bool mine_even = (off & 1) == 0;
+    uint32_t w[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint32_t four = ((q < 2 ? lo : hi) >> (16 * (q & 1))) & 0xFFFFu;  // codes 4q .. 4q+3, one per nibble
-      const uint32_t spread = (four & 0xFu) | ((four & 0xF0u) << 4) | ((four & 0xF00u) << 8) | ((four & 0xF000u) << 12);
-      atomicAnd(dst + q, ~(0x0F0F0F0Fu << sh));
-      atomicOr(dst + q, spread << sh);
+      const uint32_t a = spread4(((q < 2 ? lo : hi) >> (16 * (q & 1))) & 0xFFFFu);
+      const uint32_t b = spread4(((q < 2 ? lo2 : hi2) >> (16 * (q & 1))) & 0xFFFFu);
+      w[q] = mine_even ? (a | (b << 4)) : (b | (a << 4));
     }
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    c.data[c.nv_scale(page, h, kind, off, blk)] = static_cast<uint8_t>(sbyte);
+    c.data[c.nv_scale(page, h, kind, off ^ 1, blk)] = static_cast<uint8_t>(sb2);
+    return;
+  }
+  const int sh = 4 * (off & 1);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t spread = spread4(((q < 2 ? lo : hi) >> (16 * (q & 1))) & 0xFFFFu);  // codes 4q .. 4q+3
+    atomicAnd(dst + q, ~(0x0F0F0F0Fu << sh));
+    atomicOr(dst + q, spread << sh);
   }
   c.data[c.nv_scale(page, h, kind, off, blk)] = static_cast<uint8_t>(sbyte);
 }
