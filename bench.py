@@ -24,6 +24,10 @@ FP8 workspace append and the causal FP8 extend attention), metric TFLOP/s.
 --workload prefill_write_b4_16k: the initial-prefill write (FP8 K/V
 requantized into the NVFP4 cache), metric HBM GB/s.
 
+--workload capacity_mixed28: equal-memory capacity (the page pool admits as
+many 4096-token sequences as the KV budget of 44 all-FP8 ones holds, under
+FP8 / mixed / NVFP4 layer maps) and the 28-layer decode step at each batch.
+
 --impl reference: the CPU oracle (scalar C, one thread) on a bounded sample of
 the same workload, as the reference arm.
 """
@@ -624,6 +628,92 @@ def run_prefill_write(args):
         dist.destroy_process_group()
 
 
+CAPACITY_METRIC = "decode tokens/s at equal KV-cache memory (28-layer model, 44 FP8 sequences' budget)"
+CAPACITY_SPECS = {"capacity_mixed28": dict(base="mixed28_b44", fp8_sequences=44)}
+
+
+def run_capacity(args):
+    """Equal-memory capacity: the KV budget of 44 all-FP8 sequences (4096
+    tokens, 28 layers) handed to the library's page pool under three
+    precision maps (all FP8, the mixed map with layers 0, 25, 26, 27 in FP8,
+    all NVFP4); as many sequences as the pool holds are admitted and the
+    28-layer decode step (quantized write + decode per layer) is timed at
+    that batch."""
+    dist, rank, ws, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import nvfp4_quantized_paged_gb300 as nv
+    from nvfp4_quantized_paged_gb300.runner import Layer
+    from nvfp4_quantized_paged_gb300.workloads import SPECS, Workload, scaled
+    nv.lib()
+    c = CAPACITY_SPECS[args.workload]
+    base = SPECS[c["base"]]
+    layers, P, Hkv, L = base.layers, base.P, base.Hkv, base.L
+    pps = -(-L // P)
+    budget = c["fp8_sequences"] * pps * layers * nv.nvkv_cache_page_bytes(nv.PREC_FP8, P, Hkv)
+    maps = {"fp8": tuple(range(layers)), "mixed": tuple(base.fp8_layers), "nvfp4": ()}
+    stream = torch.cuda.current_stream()
+    res = {}
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    with Clocks(gpu_id) as clk:
+        for name, fp8_layers in maps.items():
+            prec_map = [nv.PREC_FP8 if l in fp8_layers else nv.PREC_NVFP4 for l in range(layers)]
+            npages = nv.nvkv_pool_pages_for_budget(budget, prec_map, P, Hkv)
+            pool = nv.PagePool(npages)
+            tables = []
+            while True:
+                ids = pool.alloc(pps)
+                if ids is None:
+                    break
+                tables.append(ids)
+            B = len(tables)
+            wl = Workload(scaled(base, name=f"capacity_{name}", B=B, fp8_layers=fp8_layers), seed=0, device=dev)
+            wl.block_table = np.array(tables, np.int32)  # the pool's pages
+            wl.num_pages = npages
+            lays = [Layer(wl, l, dev) for l in range(layers)]
+            for _ in range(args.warmup):
+                for x in lays:
+                    x.step()
+            torch.cuda.synchronize()
+            g = _graph(_steps_fn([lays], args.steps))
+            g.replay()
+            torch.cuda.synchronize()
+            ms = _max_over_ranks(dist, _time_graph(g, stream) / args.steps, dev)
+            kv = sum(step_bytes(x)["total"] for x in lays)
+            res[name] = {"sequences": B, "pages": npages, "cache_bytes": int(sum(x.cache.nbytes for x in lays)),
+                         "ms_per_step": round(ms, 4), "tokens_per_s": round(B / (ms * 1e-3), 1),
+                         "step_gbs": round(kv / (ms * 1e-3) / 1e9, 1)}
+            del g, lays, wl, pool
+            torch.cuda.empty_cache()
+    peak, peak_kind = _peaks()
+    if rank == 0:
+        m = res["mixed"]
+        line = {"metric": CAPACITY_METRIC, "value": round(ws * m["tokens_per_s"], 1), "unit": "tokens/s",
+                "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f16xf16->f32 (NVFP4/E4M3 dequantized exactly to f16)",
+                "data": "synthetic (seeded; no dataset or weights)",
+                "config": {"workload": args.workload, "layers": layers, "Hkv": Hkv, "Hq": base.Hq, "L": L, "page": P,
+                           "kv_budget_bytes": int(budget), "mixed_fp8_layers": list(base.fp8_layers),
+                           "parallelism": f"replicas x{ws}", "launch": "one CUDA graph of the K timed steps",
+                           "l2": "caches of 10 GB per map (far above L2)"},
+                "capacity": res,
+                "vs_fp8": {k: {"sequences": round(v["sequences"] / res["fp8"]["sequences"], 3),
+                               "tokens_per_s": round(v["tokens_per_s"] / res["fp8"]["tokens_per_s"], 3)}
+                           for k, v in res.items()},
+                "gpu_launches": 3 * layers * args.steps,
+                "roofline": {"bound": "hbm", "kernel": "28-layer decode step (write + decode + merge per layer), mixed map",
+                             "achieved": m["step_gbs"], "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                             "frac": round(m["step_gbs"] / peak, 4), "traffic": None},
+                "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def _traffic_from_profile(workload):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current decode kernel source (else None)."""
@@ -732,6 +822,8 @@ def main():
         run_extend(args)
     elif args.workload in PREFILL_SPECS:
         run_prefill_write(args)
+    elif args.workload in CAPACITY_SPECS:
+        run_capacity(args)
     else:
         run_ours(args)
 

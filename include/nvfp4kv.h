@@ -307,6 +307,36 @@ nvkv_status fp8_chunked_extend_attention(const void *q, const int64_t *cu_q, int
                                          void *scratch, size_t scratch_bytes, void *out, int32_t *err_flag,
                                          void *stream);
 
+/* Page ledger and page pool (host functions, no GPU work).  [P2] The Core of
+ * the Ledger: 16 values take 9 bytes in NVFP4 and 16 in FP8, so the same KV
+ * memory holds more sequences.  Every layer's cache is indexed by the same
+ * page ids, so a KV budget buys
+ *   pages = floor(budget / sum_l nvkv_cache_page_bytes(prec_l, ...))
+ * and a sequence of L tokens holds ceil(L / page_size) pages.
+ *   nvkv_cache_page_bytes       one page of one layer's cache (all KV heads):
+ *                               page_size * Hkv * (NVFP4: head_dim * 9/8 * 2;
+ *                               FP8: head_dim * 2); 0 for bad arguments
+ *   nvkv_pool_pages_for_budget  pages for `budget_bytes` under the per-layer
+ *                               precision map layer_prec[num_layers]; -1 for
+ *                               bad arguments
+ * The pool hands out page ids 0 .. num_pages-1 (lowest first when fresh; a
+ * released page is the next one handed out) and is not thread-safe.
+ *   nvkv_pool_create   NULL if num_pages < 0 or out of host memory
+ *   nvkv_pool_alloc    n pages into out[n], all or nothing: returns n, or -1
+ *                      (nothing taken) when fewer than n are free
+ *   nvkv_pool_release  returns pages to the pool; a page not held, out of
+ *                      range or listed twice -> NVKV_ERR_INVALID_ARG and
+ *                      nothing released */
+typedef struct nvkv_page_pool nvkv_page_pool;
+size_t nvkv_cache_page_bytes(int32_t prec, int32_t page_size, int32_t num_kv_heads, int32_t head_dim);
+int32_t nvkv_pool_pages_for_budget(size_t budget_bytes, const int32_t *layer_prec, int32_t num_layers,
+                                   int32_t page_size, int32_t num_kv_heads, int32_t head_dim);
+nvkv_page_pool *nvkv_pool_create(int32_t num_pages);
+void nvkv_pool_destroy(nvkv_page_pool *pool);
+int32_t nvkv_pool_num_free(const nvkv_page_pool *pool);
+int32_t nvkv_pool_alloc(nvkv_page_pool *pool, int32_t n, int32_t *out);
+nvkv_status nvkv_pool_release(nvkv_page_pool *pool, const int32_t *pages, int32_t n);
+
 /* Element encoders of the quantizer, one output byte per FP32 input: E2M1
  * code (low nibble, round-to-nearest-even, saturating at 6) and E4M3 byte
  * (round-to-nearest-even, saturating at 448).  x, out: device. */

@@ -95,6 +95,13 @@ SIGNATURES = {
     "fp8_extend_scratch_size": (_sz, [_i64, _i32, _i32]),
     "fp8_chunked_extend_attention": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp,
                                             _f32, _vp, _sz, _vp, _vp, _vp]),
+    "nvkv_cache_page_bytes": (_sz, [_i32, _i32, _i32, _i32]),
+    "nvkv_pool_pages_for_budget": (_i32, [_sz, _vp, _i32, _i32, _i32, _i32]),
+    "nvkv_pool_create": (_vp, [_i32]),
+    "nvkv_pool_destroy": (None, [_vp]),
+    "nvkv_pool_num_free": (_i32, [_vp]),
+    "nvkv_pool_alloc": (_i32, [_vp, _i32, _vp]),
+    "nvkv_pool_release": (_i32, [_vp, _vp, _i32]),
     "nvkv_encode_e2m1": (_i32, [_vp, _i64, _vp, _vp]),
     "nvkv_encode_e4m3": (_i32, [_vp, _i64, _vp, _vp]),
 }
@@ -329,3 +336,55 @@ def nvkv_encode_e2m1(x, out, stream=None):
 
 def nvkv_encode_e4m3(x, out, stream=None):
     _check("nvkv_encode_e4m3", lib().nvkv_encode_e4m3(_ptr(x), x.numel(), _ptr(out), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# Page ledger and page pool (host side of the C ABI)
+# ---------------------------------------------------------------------------
+
+def nvkv_cache_page_bytes(prec, page_size, num_kv_heads, head_dim=HEAD_DIM) -> int:
+    return int(lib().nvkv_cache_page_bytes(prec, page_size, num_kv_heads, head_dim))
+
+
+def nvkv_pool_pages_for_budget(budget_bytes, layer_prec, page_size, num_kv_heads, head_dim=HEAD_DIM) -> int:
+    arr = (ctypes.c_int32 * len(layer_prec))(*layer_prec)
+    n = lib().nvkv_pool_pages_for_budget(int(budget_bytes), ctypes.cast(arr, ctypes.c_void_p), len(layer_prec),
+                                         page_size, num_kv_heads, head_dim)
+    if n < 0:
+        raise NvkvError("nvkv_pool_pages_for_budget", NVKV_ERR_INVALID_ARG)
+    return int(n)
+
+
+class PagePool:
+    """The library's page pool (nvkv_pool_*): page ids shared by every layer's cache."""
+
+    def __init__(self, num_pages: int):
+        self._p = lib().nvkv_pool_create(num_pages)
+        if not self._p:
+            raise NvkvError("nvkv_pool_create", NVKV_ERR_INVALID_ARG)
+        self.num_pages = num_pages
+
+    def close(self):
+        if self._p:
+            lib().nvkv_pool_destroy(self._p)
+            self._p = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # pragma: no cover - interpreter shutdown
+            pass
+
+    @property
+    def num_free(self) -> int:
+        return int(lib().nvkv_pool_num_free(self._p))
+
+    def alloc(self, n: int):
+        """n page ids (list) or None when fewer than n are free (nothing taken)."""
+        out = (ctypes.c_int32 * max(n, 1))()
+        r = lib().nvkv_pool_alloc(self._p, n, ctypes.cast(out, ctypes.c_void_p))
+        return None if r < 0 else list(out[:n])
+
+    def release(self, pages):
+        arr = (ctypes.c_int32 * max(len(pages), 1))(*pages)
+        _check("nvkv_pool_release", lib().nvkv_pool_release(self._p, ctypes.cast(arr, ctypes.c_void_p), len(pages)))
