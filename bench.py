@@ -28,6 +28,9 @@ requantized into the NVFP4 cache), metric HBM GB/s.
 many 4096-token sequences as the KV budget of 44 all-FP8 ones holds, under
 FP8 / mixed / NVFP4 layer maps) and the 28-layer decode step at each batch.
 
+--workload calibration_study: the synthetic calibration study (attention
+output error of NVFP4 / FP8 caches against FP32, global-scale factors).
+
 --impl reference: the CPU oracle (scalar C, one thread) on a bounded sample of
 the same workload, as the reference arm.
 """
@@ -714,6 +717,35 @@ def run_capacity(args):
         dist.destroy_process_group()
 
 
+CALIB_METRIC = "attention-output relative L2 error vs FP32, NVFP4 cache at the amax/2688 global scale (element outliers)"
+
+
+def run_calibration(args):
+    """The synthetic calibration study (nvfp4_quantized_paged_gb300.calibration):
+    one JSON line, the table of errors under `rows`."""
+    dist, rank, ws, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import nvfp4_quantized_paged_gb300 as nv
+    from nvfp4_quantized_paged_gb300.calibration import study
+    nv.lib()
+    t0 = time.perf_counter()
+    rows = study(device=dev)
+    elapsed = time.perf_counter() - t0
+    main = next(r for r in rows if r["dist"] == "element_outliers" and r["prec"] == "nvfp4" and r["factor"] == 1.0)
+    if rank == 0:
+        line = {"metric": CALIB_METRIC, "value": round(main["rel_l2"], 6), "unit": "relative L2", "n_gpus": ws,
+                "steps": 1, "warmup": 0, "ms_per_step": round(elapsed * 1e3, 1), "higher_is_better": False,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f16xf16->f32 kernels vs f32 torch reference",
+                "data": "synthetic (seeded; four value distributions)",
+                "config": {"workload": args.workload, "B": 4, "L": 4096, "Hq": 32, "Hkv": 8, "D": 128,
+                           "factors": [0.25, 0.5, 1.0, 2.0, 4.0]},
+                "rows": rows}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def _traffic_from_profile(workload):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current decode kernel source (else None)."""
@@ -824,6 +856,8 @@ def main():
         run_prefill_write(args)
     elif args.workload in CAPACITY_SPECS:
         run_capacity(args)
+    elif args.workload == "calibration_study":
+        run_calibration(args)
     else:
         run_ours(args)
 
