@@ -811,7 +811,30 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    from nvfp4_quantized_paged_gb300.workloads import SPECS
+    from nvfp4_quantized_paged_gb300.workloads import EXTEND_SPECS, SPECS, extend_inputs
+    if args.workload in EXTEND_SPECS:  # the oracle's extend attention on bounded samples
+        c = EXTEND_SPECS[args.workload]
+        x = extend_inputs(0, **c)
+        ws_scale = np.array([np.abs(x["k"]).max() / 448.0, np.abs(x["v"]).max() / 448.0], np.float32)
+        t0 = time.perf_counter()
+        vals = [extend_cpu_baseline(x, ws_scale, c["Hq"], budget_s=args.cpu_budget / max(1, args.steps))
+                for _ in range(args.steps)]
+        elapsed = time.perf_counter() - t0
+        v = statistics.median(cb["value"] for cb in vals)
+        print(json.dumps({"metric": EXTEND_METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+                          "warmup": args.warmup, "ms_per_step": round(1e3 * elapsed / args.steps, 3),
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": "f64 (oracle attention)", "data": "synthetic (seeded)", "impl": "reference",
+                          "config": {"workload": args.workload, **{k: list(v2) if isinstance(v2, tuple) else v2
+                                                                   for k, v2 in c.items()}},
+                          "cpu_baseline": dict(vals[-1], value=v),
+                          "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+    if args.workload not in SPECS:
+        print(json.dumps({"impl": "reference", "unavailable": f"no oracle arm for the {args.workload} measurement"}),
+              flush=True)
+        return
     spec = SPECS[args.workload]
     # each step: a bounded oracle sample of the workload
     for _ in range(args.warmup):
