@@ -423,7 +423,33 @@ __device__ __forceinline__ void x_issuer(uint8_t *smem, uint32_t tmem, int ntile
 __global__ void __launch_bounds__(kXThreads, 1) extend_attention_kernel(const ExtendArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = static_cast<int>(threadIdx.x), warp = tid >> 5;
-  const int i = static_cast<int>(blockIdx.z);
+  // Heaviest sequences first (the longest CTAs start in the first waves, the
+  // tail holds short ones): with at most 64 sequences CTA row z takes the
+  // sequence of rank z by length (ties by index); above that, index order.
+  int i = static_cast<int>(blockIdx.z);
+  const int n = static_cast<int>(gridDim.z);
+  if (n > 1 && n <= 64) {
+    int *pick = reinterpret_cast<int *>(smem + oXFlags + 8);
+    if (warp == 0) {
+      const int lane = tid & 31;
+      int found = -1;
+      for (int c = lane; c < n; c += 32) {
+        const int Lc = a.kv_lens[c];
+        int rank = 0;
+        for (int j = 0; j < n; ++j) {
+          const int Lj = a.kv_lens[j];
+          rank += (Lj > Lc || (Lj == Lc && j < c)) ? 1 : 0;
+        }
+        if (rank == static_cast<int>(blockIdx.z)) found = c;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, found >= 0);
+      const int src = m ? __ffs(m) - 1 : 0;
+      const int v = __shfl_sync(0xffffffffu, found, src);
+      if (lane == 0) *pick = m ? v : static_cast<int>(blockIdx.z);
+    }
+    __syncthreads();
+    i = *pick;
+  }
   Tile t;
   t.h = static_cast<int>(blockIdx.y);
   t.q0 = a.cu_q[i];
