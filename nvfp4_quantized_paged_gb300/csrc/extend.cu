@@ -48,11 +48,11 @@ constexpr uint32_t kXTmemCols = 512;     // scores of half X at 128 X, its outpu
 constexpr int kXTile = kXRows * kXD * 2; // one FP16 operand tile (32 KB)
 constexpr int kXSbo = 2048;              // bytes between 8-row groups of a tile
 constexpr int kXGroupBytes = 8 * kXD * 2;  // one 8-row group of an FP16 operand tile (2 KB)
-// Shared memory: Q[2 halves] | K[2 stages] | V^T | P[2 halves] | barriers | TMEM holder, abort flag.
-constexpr int oXQ = 0, oXK = 2 * kXTile, oXV = 4 * kXTile, oXP = 5 * kXTile, oXBar = 7 * kXTile;
-// barriers: k_full[2] k_free[2] v_full s_full[2] s_free[2] p_full[2] pv_done[2] fin q_full
-constexpr int bKFull = 0, bKFree = 2, bVFull = 4, bSFull = 5, bSFree = 7, bPFull = 9, bPvDone = 11, bFin = 13,
-              bQFull = 14, kXBars = 15;
+// Shared memory: Q[2 halves] | K | V^T[2 stages] | P[2 halves] | barriers | TMEM holder, abort flag, pick.
+constexpr int oXQ = 0, oXK = 2 * kXTile, oXV = 3 * kXTile, oXP = 5 * kXTile, oXBar = 7 * kXTile;
+// barriers: k_full k_free v_full[2] v_free[2] s_full[2] s_free[2] p_full[2] pv_done[2] fin q_full
+constexpr int bKFull = 0, bKFree = 1, bVFull = 2, bVFree = 4, bSFull = 6, bSFree = 8, bPFull = 10, bPvDone = 12,
+              bFin = 14, bQFull = 15, kXBars = 16;
 constexpr int oXFlags = oXBar + 8 * kXBars;
 constexpr int kXSmem = oXFlags + 16;
 constexpr float kXNoMax = -1e30f;        // running max before any score (finite: exp2(-inf - m) = 0)
@@ -139,10 +139,12 @@ __device__ __forceinline__ void x_load_q(const ExtendArgs &a, const Tile &t, uin
 // ---------------------------------------------------------------------------
 // Producers.  Tile j = keys [128 j, 128 j + 128) of the sequence = row groups
 // g0 .. g0 + 15, g0 = (cu_kv + 128 j) / 8, of the expanded tiles.
-//   warp 8: K as one 32 KB copy into stage j % 2, once both halves' QK^T of
-//           tile j - 2 are done (k_free);
-//   warp 9: V^T as one 2 KB copy per 8-value group d (lane d) into the single
-//           V^T buffer, once both halves' P.V of tile j - 1 are done.
+//   warp 8: K as one 32 KB copy into the single K buffer, once both halves'
+//           QK^T of tile j - 1 are done (its latency hides behind the
+//           softmax of tile j - 1);
+//   warp 9: V^T as one 2 KB copy per 8-value group d (lane d) into stage
+//           j % 2, once both halves' P.V of tile j - 2 are done (v_free), so
+//           the P.V of tile j never waits for its copy.
 // Each returns the number of tiles whose copies it issued.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int x_produce_k(const ExtendArgs &a, const Tile &t, uint8_t *smem, uint64_t *bars,
@@ -152,12 +154,11 @@ __device__ __forceinline__ int x_produce_k(const ExtendArgs &a, const Tile &t, u
   const uint8_t *kt = a.tiles + static_cast<int64_t>(t.h) * a.ngroups * kXGroupBytes;
   int issued = 0;
   for (int j = 0; j < t.ntiles; ++j) {
-    const int b = j & 1;
-    if (j >= 2 && !warp_wait_x(&bars[bKFree + b], static_cast<uint32_t>((j - 2) >> 1) & 1u, abort)) break;
+    if (j >= 1 && !warp_wait_x(&bars[bKFree], static_cast<uint32_t>(j - 1) & 1u, abort)) break;
     const int64_t g0 = (t.kv_base + static_cast<int64_t>(j) * kXRows) >> 3;
     if (lane == 0) {
-      mbar_arrive_expect_tx(&bars[bKFull + b], kXTile);
-      bulk_g2s(smem + oXK + b * kXTile, kt + g0 * kXGroupBytes, kXTile, &bars[bKFull + b], policy);
+      mbar_arrive_expect_tx(&bars[bKFull], kXTile);
+      bulk_g2s(smem + oXK, kt + g0 * kXGroupBytes, kXTile, &bars[bKFull], policy);
     }
     __syncwarp();
     ++issued;
@@ -172,13 +173,14 @@ __device__ __forceinline__ int x_produce_v(const ExtendArgs &a, const Tile &t, u
   const uint8_t *vt = a.tiles + (static_cast<int64_t>(a.Hkv) + t.h) * a.ngroups * kXGroupBytes;
   int issued = 0;
   for (int j = 0; j < t.ntiles; ++j) {
-    if (j >= 1 && !warp_wait_x(&bars[bPvDone + 1], static_cast<uint32_t>(j - 1) & 1u, abort)) break;
+    const int b = j & 1;
+    if (j >= 2 && !warp_wait_x(&bars[bVFree + b], static_cast<uint32_t>((j - 2) >> 1) & 1u, abort)) break;
     const int64_t g0 = (t.kv_base + static_cast<int64_t>(j) * kXRows) >> 3;
-    if (lane == 0) mbar_arrive_expect_tx(&bars[bVFull], kXTile);
+    if (lane == 0) mbar_arrive_expect_tx(&bars[bVFull + b], kXTile);
     __syncwarp();
     if (lane < 16)
-      bulk_g2s(smem + oXV + lane * kXGroupBytes, vt + (lane * a.ngroups + g0) * 128, kXGroupBytes, &bars[bVFull],
-               policy);
+      bulk_g2s(smem + oXV + b * kXTile + lane * kXGroupBytes, vt + (lane * a.ngroups + g0) * 128, kXGroupBytes,
+               &bars[bVFull + b], policy);
     ++issued;
   }
   return issued;
@@ -361,10 +363,10 @@ __device__ __forceinline__ void x_softmax(const ExtendArgs &a, const Tile &t, ui
 // MMA issuer (one thread of warp 10), polling four in-order streams:
 //   QK_0(j), QK_1(j): S_X = Q_X K_j^T once K_j landed and half X's softmax has
 //                     read S_X of tile j - 1 (QK_0(j) before QK_1(j); the
-//                     commit after QK_1(j) frees K stage j % 2);
+//                     commit after QK_1(j) frees the K buffer);
 //   PV_0(j), PV_1(j): O_X += P_X V_j once P_X is written and V_j landed
 //                     (PV_0(j) before PV_1(j); the commit after PV_1(j) frees
-//                     the V^T buffer).
+//                     V^T stage j % 2).
 // The tensor cores so run one half's MMAs while the other half's softmax runs.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void x_issuer(uint8_t *smem, uint32_t tmem, int ntiles, uint64_t *bars,
@@ -378,16 +380,16 @@ __device__ __forceinline__ void x_issuer(uint8_t *smem, uint32_t tmem, int ntile
 #pragma unroll
     for (int X = 0; X < 2; ++X) {
       const int j = nqk[X];
-      if (j < ntiles && (X == 0 || j < nqk[0]) && mbar_test(&bars[bKFull + (j & 1)], static_cast<uint32_t>(j >> 1) & 1u) &&
+      if (j < ntiles && (X == 0 || j < nqk[0]) && mbar_test(&bars[bKFull], static_cast<uint32_t>(j) & 1u) &&
           (j == 0 || mbar_test(&bars[bSFree + X], static_cast<uint32_t>(j - 1) & 1u))) {
         tc_fence_after();
-        const uint32_t ks = smem_u32(smem + oXK + (j & 1) * kXTile);
+        const uint32_t ks = smem_u32(smem + oXK);
 #pragma unroll
         for (int kk = 0; kk < kXD / 16; ++kk)
           umma_f16(tmem + static_cast<uint32_t>(X * 128), umma_desc(qs + X * kXTile + kk * 256, 128, kXSbo),
                    umma_desc(ks + kk * 256, 128, kXSbo), id, kk > 0 ? 1u : 0u);
         umma_commit(&bars[bSFull + X]);
-        if (X == 1) umma_commit(&bars[bKFree + (j & 1)]);
+        if (X == 1) umma_commit(&bars[bKFree]);
         ++nqk[X];
         did = true;
       }
@@ -396,13 +398,15 @@ __device__ __forceinline__ void x_issuer(uint8_t *smem, uint32_t tmem, int ntile
     for (int X = 0; X < 2; ++X) {
       const int j = npv[X];
       if (j < nqk[X] && (X == 0 || j < npv[0]) && mbar_test(&bars[bPFull + X], static_cast<uint32_t>(j) & 1u) &&
-          mbar_test(&bars[bVFull], static_cast<uint32_t>(j) & 1u)) {
+          mbar_test(&bars[bVFull + (j & 1)], static_cast<uint32_t>(j >> 1) & 1u)) {
         tc_fence_after();
+        const uint32_t vt = vts + static_cast<uint32_t>((j & 1) * kXTile);
 #pragma unroll
         for (int kk = 0; kk < kXRows / 16; ++kk)
           umma_f16(tmem + static_cast<uint32_t>(256 + X * 128), umma_desc(ps + X * kXTile + kk * 256, 128, kXSbo),
-                   umma_desc(vts + kk * 256, 128, kXSbo), id, (j > 0 || kk > 0) ? 1u : 0u);
+                   umma_desc(vt + kk * 256, 128, kXSbo), id, (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bars[bPvDone + X]);
+        if (X == 1) umma_commit(&bars[bVFree + (j & 1)]);
         ++npv[X];
         did = true;
       }
@@ -517,9 +521,9 @@ __global__ void __launch_bounds__(kXThreads, 1) extend_attention_kernel(const Ex
       volatile int never = 0;
       for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j) {
         if (warp == kXKProducerWarp)
-          mbar_wait_bounded(&bars[bKFull + (j & 1)], static_cast<uint32_t>(j >> 1) & 1u, &never);
+          mbar_wait_bounded(&bars[bKFull], static_cast<uint32_t>(j) & 1u, &never);
         else
-          mbar_wait_bounded(&bars[bVFull], static_cast<uint32_t>(j) & 1u, &never);
+          mbar_wait_bounded(&bars[bVFull + (j & 1)], static_cast<uint32_t>(j >> 1) & 1u, &never);
       }
     }
     __syncthreads();
