@@ -85,10 +85,6 @@ __device__ __forceinline__ uint32_t f16x2_from_bf16x2(uint32_t w) {
   return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-__device__ __forceinline__ uint32_t word_of(const uint4 &v, int k) {
-  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
-}
-
 __device__ __forceinline__ bool warp_wait_x(uint64_t *bar, uint32_t parity, volatile int *abort) {
   const bool ok = mbar_wait_bounded(bar, parity, abort);
   return __all_sync(0xffffffffu, ok);
