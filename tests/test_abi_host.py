@@ -89,3 +89,51 @@ def test_other_entry_points_reject_bad_arguments(nv):
     assert L.nvfp4_kv_dequant_to_fp8_workspace(0x1000, 4, 0x1000, 0x1000, 0x1000, 2, ctypes.byref(d), 0x1000,
                                                0x2000, 0x3000, 10, None) == nv.NVKV_ERR_INVALID_ARG
     assert L.nvkv_status_string(4) == b"workspace too small"
+
+
+def test_extend_and_prefill_argument_checks(nv):
+    L = nv.lib()
+    # scratch size: 2 (K, V) x Hkv x (ceil(rows / 8) + 16 groups) x 2 KB; 0 for a bad head_dim
+    assert nv.fp8_extend_scratch_size(100, 8, 128) == 2 * 8 * (13 + 16) * 2048
+    assert nv.fp8_extend_scratch_size(0, 2, 128) == 2 * 2 * 16 * 2048
+    assert nv.fp8_extend_scratch_size(100, 8, 64) == 0
+
+    def ext(**kw):
+        a = dict(q=0x10000, cu_q=0x20000, n=2, maxq=64, Hq=32, wk=0x30000, wv=0x40000, cu_kv=0x50000,
+                 kl=0x60000, Hkv=8, D=128, rows=100, s=0x70000, sm=0.0, scr=0x80000,
+                 scrb=nv.fp8_extend_scratch_size(100, 8, 128), out=0x90000)
+        a.update(kw)
+        return L.fp8_chunked_extend_attention(a["q"], a["cu_q"], a["n"], a["maxq"], a["Hq"], a["wk"], a["wv"],
+                                              a["cu_kv"], a["kl"], a["Hkv"], a["D"], a["rows"], a["s"], a["sm"],
+                                              a["scr"], a["scrb"], a["out"], None, None)
+    assert ext(D=64) == nv.NVKV_ERR_UNSUPPORTED                 # head_dim 128 only
+    assert ext(Hq=24) == nv.NVKV_ERR_UNSUPPORTED                # group of 3: not a power of two
+    assert ext(Hq=30) == nv.NVKV_ERR_INVALID_ARG                # Hq not a multiple of Hkv
+    assert ext(scrb=1024) == nv.NVKV_ERR_WORKSPACE_TOO_SMALL
+    assert ext(scr=None) == nv.NVKV_ERR_INVALID_ARG
+    assert ext(out=0x90008) == nv.NVKV_ERR_UNSUPPORTED          # 16-byte alignment
+    assert ext(n=-1) == nv.NVKV_ERR_INVALID_ARG
+    assert ext(n=0) == nv.NVKV_OK and ext(maxq=0) == nv.NVKV_OK  # nothing to do
+
+    def app(**kw):
+        a = dict(k=0x10000, v=0x20000, dt=0, T=5, rows=0x30000, Hkv=8, D=128, s=0x40000, wk=0x50000,
+                 wv=0x60000, wr=100)
+        a.update(kw)
+        return L.fp8_workspace_append_chunk(a["k"], a["v"], a["dt"], a["T"], a["rows"], a["Hkv"], a["D"], a["s"],
+                                            a["wk"], a["wv"], a["wr"], None, None)
+    assert app(D=100) == nv.NVKV_ERR_UNSUPPORTED
+    assert app(dt=5) == nv.NVKV_ERR_INVALID_ARG
+    assert app(k=None) == nv.NVKV_ERR_INVALID_ARG
+    assert app(wk=0x50004) == nv.NVKV_ERR_UNSUPPORTED
+    assert app(T=0) == nv.NVKV_OK
+
+    d = _desc(nv)
+    assert L.nvfp4_kv_requantize_write_fp8(0x10000, 0x20000, None, 3, 0x30000, None, ctypes.byref(d),
+                                           None) == nv.NVKV_ERR_INVALID_ARG   # no FP8 scales
+    assert L.nvfp4_kv_requantize_write_fp8(0x10004, 0x20000, 0x40000, 3, 0x30000, None, ctypes.byref(d),
+                                           None) == nv.NVKV_ERR_UNSUPPORTED   # alignment
+    d8 = _desc(nv, prec=1)
+    assert L.nvfp4_kv_requantize_write_fp8(0x10000, 0x20000, 0x40000, 3, 0x30000, None, ctypes.byref(d8),
+                                           None) == nv.NVKV_ERR_INVALID_ARG   # the cache must be NVFP4
+    assert L.nvfp4_kv_requantize_write_fp8(0x10000, 0x20000, 0x40000, 0, 0x30000, None, ctypes.byref(d),
+                                           None) == nv.NVKV_OK
