@@ -47,3 +47,54 @@ def orc_decode(b):
     e, m = (b >> 3) & 15, b & 7
     v = np.where(e > 0, 2.0 ** (e - 7) * (1 + m / 8), 2.0 ** -6 * m / 8)
     return np.where(b & 0x80, -v, v)
+
+
+def test_quantizer_division_at_every_e2m1_rounding_boundary(orc):
+    """Blocks whose scale is exactly 1 (element 0 = 6 g) so den = g, and whose
+    other values sit on and one or two ulps around den * t for every E2M1
+    rounding boundary t (0.25, 0.75, ..., 5) and a few interior values:
+    codes must equal the oracle's, which divides x / den exactly once."""
+    import nvfp4_quantized_paged_gb300 as nv
+    Hkv, D, P = 2, 128, 16
+    rows = []
+    for g in (np.float32(0.0137), np.float32(3.1e-5), np.float32(1.7), np.float32(2.0 ** -20)):
+        d6 = np.float32(6.0) * g
+        bounds = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.5, 1.0, 3.0]
+        vals = []
+        for t in bounds:
+            c = np.float32(g) * np.float32(t)
+            for k in (-2, -1, 0, 1, 2):
+                v = c
+                for _ in range(abs(k)):
+                    v = np.nextafter(v, np.float32(np.inf) if k > 0 else np.float32(-np.inf), dtype=np.float32)
+                vals.append(v)
+                vals.append(-v)
+        vals = np.array(vals, np.float32)
+        for i in range(0, len(vals), 15):
+            blk = np.zeros(16, np.float32)
+            blk[0] = d6
+            part = vals[i:i + 15]
+            blk[1:1 + len(part)] = part
+            rows.append((g, blk))
+    # one token-head row per (g, 8 blocks): pack blocks of the same g into rows of 128 values
+    by_g = {}
+    for g, blk in rows:
+        by_g.setdefault(float(g), []).append(blk)
+    for g, blks in by_g.items():
+        n_rows = (len(blks) + 7) // 8
+        data = np.zeros((n_rows * Hkv, D), np.float32)
+        flat = np.concatenate(blks + [np.zeros(16, np.float32)] * (n_rows * 8 - len(blks)))
+        data[:n_rows].reshape(-1)[:flat.size] = flat
+        data[n_rows:] = data[:n_rows]
+        T = n_rows
+        k = data.reshape(Hkv, T, D).transpose(1, 0, 2).copy()
+        gs = np.array([g, g], np.float32)
+        slots = np.arange(T, dtype=np.int64)
+        npages = (T + P - 1) // P
+        cache = nv.Cache(nv.PREC_NVFP4, npages, Hkv, P, device="cuda")
+        nv.nvfp4_kv_quantize_write(torch.from_numpy(k).cuda(), torch.from_numpy(k).cuda(),
+                                   torch.from_numpy(slots).cuda(), torch.from_numpy(gs).cuda(), cache)
+        torch.cuda.synchronize()
+        oc = orc.Cache(orc.PREC_NVFP4, npages, Hkv, P, D, gs)
+        orc.quantize_write(oc, k, k, slots)
+        assert np.array_equal(cache.data.cpu().numpy(), oc.data), g
