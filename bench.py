@@ -256,24 +256,36 @@ def run_ours(args):
                             for x in sets[0])
     del g_step, g_dec
 
-    # e2e: inputs from pinned host memory, output back to the host, through the C ABI
-    host = []
-    for lay in sets[0]:
-        h = dict(q=lay.q.cpu().pin_memory(), out=torch.empty(lay.out.shape, dtype=lay.out.dtype).pin_memory())
+    # e2e: inputs from pinned host memory, output back to the host, through the
+    # C ABI.  A layer's step inputs (queries, new K/V, their slots) live in one
+    # device buffer that the layer's tensors view, so a step copies them in
+    # with one host-to-device copy and the output back with one copy.
+    def stage(lay):
+        parts = [lay.q] + ([lay.k_new, lay.v_new, lay.slots_new] if lay.k_new is not None else [])
+        sizes = [t.numel() * t.element_size() for t in parts]
+        buf = torch.empty(sum(sizes), dtype=torch.uint8, device=dev)
+        views, off = [], 0
+        for t, n in zip(parts, sizes):  # each part's size is a multiple of 16 bytes but the last
+            v = buf[off:off + n].view(t.dtype).view(t.shape)
+            v.copy_(t)
+            views.append(v)
+            off += n
+        lay.q = views[0]
         if lay.k_new is not None:
-            h.update(k=lay.k_new.cpu().pin_memory(), v=lay.v_new.cpu().pin_memory(),
-                     s=lay.slots_new.cpu().pin_memory())
-        host.append(h)
-    h2d = sum(h["q"].numel() * 2 + (h["k"].numel() * 8 + h["s"].numel() * 8 if "k" in h else 0) for h in host)
+            lay.k_new, lay.v_new, lay.slots_new = views[1], views[2], views[3]
+        return buf
+
+    bufs = [[stage(lay) for lay in lays] for lays in sets]
+    host = [dict(inp=b.cpu().pin_memory(), out=torch.empty(lay.out.shape, dtype=lay.out.dtype).pin_memory())
+            for b, lay in zip(bufs[0], sets[0])]
+    h2d = sum(h["inp"].numel() for h in host)
     d2h = sum(h["out"].numel() * 2 for h in host)
 
     def e2e_step(i):
-        for lay, h in zip(sets[i % len(sets)], host):
-            lay.q.copy_(h["q"], non_blocking=True)
-            if "k" in h:
-                lay.k_new.copy_(h["k"], non_blocking=True)
-                lay.v_new.copy_(h["v"], non_blocking=True)
-                lay.slots_new.copy_(h["s"], non_blocking=True)
+        r = i % len(sets)
+        for lay, buf, h in zip(sets[r], bufs[r], host):
+            buf.copy_(h["inp"], non_blocking=True)
+            if lay.k_new is not None:
                 lay.write(lay.k_new, lay.v_new, lay.slots_new)
             lay.decode()
             if lay.ext is not None:
