@@ -11,10 +11,12 @@
  *   [P2] "SGLang x Qwen x NVIDIA Collaboration: NVFP4 KV Cache Breaks
  *        Long-Context and Agentic Inference Bottlenecks": The Core of the
  *        Ledger (one E4M3 block scale per 16 values, one FP32 global scale per
- *        tensor, 9 bytes per 16 values); Three Paths (decode reads NVFP4 from
- *        the paged cache and dequantizes inside the kernel; chunked extend
- *        dequantizes the cached prefix into a shared FP8 workspace and
- *        quantizes the new chunk into the cache).
+ *        tensor, 9 bytes per 16 values); Three Paths (the initial prefill
+ *        requantizes its FP8 KV into the cache; decode reads NVFP4 from the
+ *        paged cache and dequantizes inside the kernel; chunked extend
+ *        dequantizes the cached prefix into a shared FP8 workspace, runs FP8
+ *        attention over it and the new chunk, and quantizes the new chunk
+ *        into the cache); the equal-capacity comparison (page ledger).
  *
  * Number formats.  E2M1 codes: magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6, bit 3 =
  * sign; byte j of a row holds element 2j in its low nibble and 2j+1 in its
@@ -48,7 +50,8 @@
  * V.  A page of one KV head is one contiguous run of bytes, which decode
  * fetches with a single bulk copy.  The contents are the quantizer's output
  * above; only their positions are fixed here (an NVFP4 V write changes only
- * its own row's nibbles, with atomic byte-lane updates).
+ * its own row's nibbles: with atomic byte-lane updates, or with plain stores
+ * of both rows of a pair when the call writes both).
  *   Supported: head_dim 128; page_size 16, 32 or 64; every pointer 16-byte
  *   aligned.  Anything else -> NVKV_ERR_UNSUPPORTED.
  *
