@@ -239,10 +239,22 @@ nvkv_status nvfp4_paged_decode_attention_noalloc(const void *q, const nvkv_cache
  * [rows][num_kv_heads][head_dim] E4M3:
  *   byte = E4M3_rne_satfinite((e2m1 * S) * (g / ws_scale))   (FP32, per K and V)
  *   seq_ids, prefix_lens  [n] int32 device; each seq_ids[i] must index a row
- *                         of block_table; cu_prefix [n+1] int64 device,
- *                         exclusive prefix sums of prefix_lens; a prefix longer
- *                         than its row (max_pages * page_size) is skipped and
+ *                         of block_table; a prefix longer than its row
+ *                         (max_pages * page_size) is skipped and
  *                         NVKV_DEVERR_SEQLEN raised
+ *   cu_prefix             [n+1] int64 device: cu_prefix[i] (i < n) is the
+ *                         first workspace row of sequence i's prefix; the
+ *                         starts are non-decreasing with room for each prefix,
+ *                         cu_prefix[i] + prefix_lens[i] <= cu_prefix[i+1], and
+ *                         cu_prefix[n] (<= ws_rows) ends the rows the call
+ *                         visits.  Rows between one prefix's end and the next
+ *                         start are not touched, so a caller can reserve the
+ *                         chunk's rows right behind each prefix and start each
+ *                         sequence on a multiple of 8 rows, the layout
+ *                         fp8_chunked_extend_attention reads ([prefix || chunk]
+ *                         per sequence, cu_kv[i] = cu_prefix[i]); the exclusive
+ *                         prefix sums of prefix_lens pack the prefixes back to
+ *                         back
  *   ws_scale              device float[2] {K, V}, > 0 (e.g. 6 * g)
  *   ws_rows               rows allocated in ws_k and ws_v (host value); rows
  *                         past it are skipped and NVKV_DEVERR_WS_ROWS raised

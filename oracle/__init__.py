@@ -319,19 +319,29 @@ def paged_decode_attention(cache: Cache, q_bf16_bits: np.ndarray, block_table: n
 
 
 def dequant_to_fp8_workspace(cache: Cache, block_table: np.ndarray, seq_ids, prefix_lens,
-                             ws_scale) -> tuple:
+                             ws_scale, row_start=None, ws_rows=None) -> tuple:
     """Chunked-extend prefix dequant into the FP8 workspace ([P2] Three Paths).
 
-    Returns (ws_k, ws_v), uint8 [sum(prefix_lens), Hkv, D] E4M3.
+    Token t of sequence i goes to row ``row_start[i] + t`` (default: the
+    sequences back to back, row_start = exclusive sums of prefix_lens).
+    Returns (ws_k, ws_v), uint8 [ws_rows, Hkv, D] E4M3 (default ws_rows: the
+    last prefix's end); rows no prefix token lands on stay 0.
     """
     assert cache.prec == PREC_NVFP4
     bt = _c(block_table, np.int32)
     ids = _c(seq_ids, np.int32)
     pl = _c(prefix_lens, np.int32)
     cu = np.zeros(len(pl) + 1, np.int64)
-    cu[1:] = np.cumsum(pl)
+    if row_start is None:
+        cu[1:] = np.cumsum(pl)
+    else:
+        cu[:-1] = np.asarray(row_start, np.int64)
+        cu[-1] = cu[-2] + pl[-1] if len(pl) else 0
     ws = _c(ws_scale, np.float32).reshape(2)
-    rows = int(cu[-1])
+    rows = max([int(cu[i]) + int(pl[i]) for i in range(len(pl))] + [0])
+    if ws_rows is not None:
+        assert ws_rows >= rows
+        rows = int(ws_rows)
     wk = np.zeros((rows, cache.Hkv, cache.D), np.uint8)
     wv = np.zeros((rows, cache.Hkv, cache.D), np.uint8)
     rc = lib().orc_dequant_to_fp8_workspace(_p(bt, _i32p), bt.shape[1], _p(ids, _i32p), _p(pl, _i32p),

@@ -157,3 +157,95 @@ def test_error_flag_for_more_queries_than_keys():
     _attend(d, 40)
     assert d["err"].item() == 3  # NVKV_DEVERR_SEQLEN; the sequence is skipped
     assert torch.isnan(d["out"].float()).all()
+
+
+def test_chunked_extend_chain_from_the_nvfp4_cache(orc):
+    """The whole chunked-extend path ("SGLang x Qwen x NVIDIA ...", Three
+    Paths): the cached NVFP4 prefix is dequantized into the shared FP8
+    workspace, the chunk's K/V are appended behind it, FP8 attention of the
+    chunk's queries runs over [prefix || chunk], and the chunk is then
+    quantized into the NVFP4 cache.  The workspace is laid out as the
+    attention reads it: each sequence starts on a multiple of 8 rows with its
+    chunk's rows reserved right behind its prefix (cu_prefix = cu_kv).  Every
+    byte (workspace, cache) matches the oracle's chain bit for bit and the
+    attention is within the parity tolerance of the oracle's."""
+    nv = _nv()
+    prefixes, chunks, Hq, Hkv, P = (300, 1000, 64, 0), (130, 77, 200, 9), 32, 8, 64
+    x = _inputs(11, prefixes, chunks, Hq, Hkv)
+    n = len(prefixes)
+    lens = [p + c for p, c in zip(prefixes, chunks)]
+    pages_per = [(L + P - 1) // P for L in lens]
+    max_pages = max(pages_per)
+    num_pages = sum(pages_per) + 3
+    perm = np.random.default_rng(4).permutation(num_pages).astype(np.int32)
+    bt = np.full((n, max_pages), -1, np.int32)
+    off = 0
+    for i in range(n):
+        bt[i, :pages_per[i]] = perm[off:off + pages_per[i]]
+        off += pages_per[i]
+    first = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.int64)  # row of sequence i in x["k"]
+
+    def slots(i, t0, t1):
+        t = np.arange(t0, t1)
+        return bt[i, t // P].astype(np.int64) * P + t % P
+
+    pre_idx = np.concatenate([first[i] + np.arange(prefixes[i]) for i in range(n)]).astype(np.int64)
+    pre_slots = np.concatenate([slots(i, 0, prefixes[i]) for i in range(n)])
+    ch_slots = np.concatenate([slots(i, prefixes[i], lens[i]) for i in range(n)])
+    ci = x["chunk_idx"]
+
+    # ---- GPU chain, through the C ABI
+    dev = "cuda"
+    k_all, v_all = torch.from_numpy(x["k"]).to(dev), torch.from_numpy(x["v"]).to(dev)
+    g = torch.zeros(2, dtype=torch.float32, device=dev)
+    ws_scale = torch.zeros(2, dtype=torch.float32, device=dev)
+    for kind, t in ((0, k_all), (1, v_all)):  # every token the layer holds, prefix and chunk
+        nv.nvkv_global_scale(t, g[kind:kind + 1], nv.NVFP4_GLOBAL_DIVISOR)
+        nv.nvkv_global_scale(t, ws_scale[kind:kind + 1], nv.FP8_GLOBAL_DIVISOR)
+    cache = nv.Cache(nv.PREC_NVFP4, num_pages, Hkv, P, device=dev, kv_scale=g)
+    pi = torch.from_numpy(pre_idx).to(dev)
+    nv.nvfp4_kv_quantize_write(k_all[pi].contiguous(), v_all[pi].contiguous(), torch.from_numpy(pre_slots).to(dev),
+                               g, cache)
+    bt_d = torch.from_numpy(bt).to(dev)
+    cu_prefix = np.concatenate([x["cu_kv"], [x["ws_rows"]]]).astype(np.int64)
+    ws_k = torch.full((x["ws_rows"], Hkv, 128), 0x7F, dtype=torch.uint8, device=dev)  # NaN: rows never read
+    ws_v = torch.full_like(ws_k, 0x7F)
+    nv.nvfp4_kv_dequant_to_fp8_workspace(bt_d, torch.arange(n, dtype=torch.int32, device=dev),
+                                         torch.tensor(prefixes, dtype=torch.int32, device=dev),
+                                         torch.from_numpy(cu_prefix).to(dev), cache, ws_scale, ws_k, ws_v)
+    cidx = torch.from_numpy(ci).to(dev)
+    k_ch, v_ch = k_all[cidx].contiguous(), v_all[cidx].contiguous()
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    nv.fp8_workspace_append_chunk(k_ch, v_ch, torch.from_numpy(x["chunk_rows"]).to(dev), ws_scale, ws_k, ws_v,
+                                  err=err)
+    q = x["q"].to(dev) if isinstance(x["q"], torch.Tensor) else torch.from_numpy(x["q"]).to(dev).to(torch.bfloat16)
+    out = torch.full_like(q, float("nan"))
+    scratch = nv.alloc_extend_scratch(ws_k)
+    nv.fp8_chunked_extend_attention(q, torch.from_numpy(x["cu_q"]).to(dev), max(chunks), ws_k, ws_v,
+                                    torch.from_numpy(x["cu_kv"]).to(dev), torch.from_numpy(x["kv_lens"]).to(dev),
+                                    ws_scale, out, scratch, err=err)
+    nv.nvfp4_kv_quantize_write(k_ch, v_ch, torch.from_numpy(ch_slots).to(dev), g, cache)
+    torch.cuda.synchronize()
+    assert err.item() == 0 and cache.err.item() == 0
+
+    # ---- oracle chain on the same inputs
+    g_o = np.array([orc.global_scale(x["k"], orc.NVFP4_GLOBAL_DIVISOR),
+                    orc.global_scale(x["v"], orc.NVFP4_GLOBAL_DIVISOR)], np.float32)
+    ws_o = np.array([orc.global_scale(x["k"], orc.FP8_GLOBAL_DIVISOR),
+                     orc.global_scale(x["v"], orc.FP8_GLOBAL_DIVISOR)], np.float32)
+    assert np.array_equal(g.cpu().numpy(), g_o) and np.array_equal(ws_scale.cpu().numpy(), ws_o)
+    oc = orc.Cache(orc.PREC_NVFP4, num_pages, Hkv, P, 128, g_o)
+    orc.quantize_write(oc, x["k"][pre_idx], x["v"][pre_idx], pre_slots)
+    wk, wv = orc.dequant_to_fp8_workspace(oc, bt, np.arange(n), prefixes, ws_o, row_start=x["cu_kv"],
+                                          ws_rows=x["ws_rows"])
+    orc.fp8_workspace_append(wk, wv, x["k"][ci], x["v"][ci], x["chunk_rows"], ws_o)
+    used = np.zeros(x["ws_rows"], bool)
+    used[x["rows"]] = True  # every prefix and chunk row; gap rows were never written
+    np.testing.assert_array_equal(ws_k.cpu().numpy()[used], wk[used])
+    np.testing.assert_array_equal(ws_v.cpu().numpy()[used], wv[used])
+    assert np.all(ws_k.cpu().numpy()[~used] == 0x7F)  # the dequant left the reserved gaps alone
+    want = orc.fp8_extend_attention(_bits(q), x["cu_q"], wk, wv, x["cu_kv"], x["kv_lens"], ws_o)
+    ok, worst = within_tol(out.float().cpu().numpy(), want)
+    assert ok, f"max excess over tolerance {worst}"
+    orc.quantize_write(oc, x["k"][ci], x["v"][ci], ch_slots)
+    assert np.array_equal(cache.data.cpu().numpy(), oc.data)

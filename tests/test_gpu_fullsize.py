@@ -53,14 +53,19 @@ def test_longctx_b2_ctx128k_full(num_splits):
     _check_layer(lay, wl, [1], fp8=False)
 
 
-@pytest.mark.parametrize("layer", [0, 1, 27])
-def test_mixed28_b44_sampled_layers(layer):
+# Both batches of the 28-layer mixed-precision workload, on the FP8 layers at
+# either end of the map (0, 25, 26, 27) and NVFP4 layers beside and between
+# them (1, 13), each checked on its first, a middle and its last sequence.
+@pytest.mark.parametrize("layer", [0, 1, 13, 25, 26, 27])
+@pytest.mark.parametrize("name,seqs", [("mixed28_b44", [0, 22, 43]), ("mixed28_b70", [0, 35, 69])])
+def test_mixed28_sampled_layers(name, seqs, layer):
     from nvfp4_quantized_paged_gb300.runner import Layer
-    wl = _wl("mixed28_b44")
+    wl = _wl(name)
     lay = Layer(wl, layer)
+    assert wl.spec.fp8_layers == (0, 25, 26, 27)
     assert (lay.prec == 1) == (layer in (0, 25, 26, 27))
     lay.step()
-    _check_layer(lay, wl, [0, 43], fp8=layer in (0, 25, 26, 27))
+    _check_layer(lay, wl, seqs, fp8=layer in (0, 25, 26, 27))
 
 
 def test_serving_mix_b256_decode_and_extend():
