@@ -161,13 +161,19 @@ nvkv_status fp8_kv_quantize_write(const void *k, const void *v, nvkv_dtype dtype
 
 /* Bytes of decode workspace for this problem size: num_splits > 0 as passed to
  * the decode call, 0 for the library's choice on the current device.  The
- * workspace holds one merge record per (sequence, KV head) and the split-KV
- * partial results; every decode call writes all of it that it later reads,
- * so it needs no initialisation.  Returns 0 for unsupported sizes. */
+ * workspace holds a 4-byte arrival counter per (sequence, KV head) (the
+ * first batch * num_kv_heads * 4 bytes, rounded up to 256) and then two
+ * split-KV partial slots of 4160 bytes per CTA.  The counters must be zero
+ * before the first decode call that uses the workspace (zero it once with
+ * nvkv_decode_workspace_init or any memset); every call leaves them zero
+ * again.  A call that ends with a device error (NVKV_DEVERR_* in the cache's
+ * error word, or a CUDA error) can leave them nonzero: zero the workspace
+ * again before reusing it.  Returns 0 for unsupported sizes. */
 size_t nvkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                   int32_t num_splits);
 
-/* Zero `bytes` of workspace on `stream` (a cudaMemsetAsync); optional. */
+/* Zero `bytes` of workspace on `stream` (a cudaMemsetAsync): once before the
+ * workspace's first decode call, and after a call that failed on the device. */
 nvkv_status nvkv_decode_workspace_init(void *workspace, size_t bytes, void *stream);
 
 /* Paged GQA decode attention over the NVFP4 or FP8 cache ([P2] Three Paths:
@@ -189,9 +195,14 @@ nvkv_status nvkv_decode_workspace_init(void *workspace, size_t bytes, void *stre
  * Query head h reads KV head h / (num_q_heads / num_kv_heads); every token in
  * [0, seq_len) is visible.  out = softmax(q k^T * sm_scale) v with the FP32
  * result rounded to BF16.  Split partitions are merged with the log-sum-exp
- * rule by a second, small kernel chained to the first with programmatic
- * dependent launch (two launches on `stream`).  Requires num_q_heads /
- * num_kv_heads <= 8 and batch <= 1024. */
+ * rule inside the same launch: each contributor of a split (sequence, KV
+ * head) counts itself on the pair's counter and the CTA that arrives last
+ * merges the parts in contributor order (one kernel launch on `stream`,
+ * programmatic dependent launch so its set-up overlaps the previous kernel;
+ * the result does not depend on arrival order).  Requires num_q_heads /
+ * num_kv_heads <= 8, num_kv_heads >= 1 and batch <= 1024; the CTA count is at
+ * most one resident wave.  Calls that share a workspace must be ordered (one
+ * stream). */
 nvkv_status nvfp4_paged_decode_attention(const void *q, const nvkv_cache *cache, const int32_t *block_table,
                                          int32_t max_pages, const int32_t *seq_lens, int32_t batch,
                                          int32_t num_q_heads, int32_t layer_precision, float sm_scale,
@@ -212,19 +223,26 @@ nvkv_status fp8_paged_decode_attention(const void *q, const nvkv_cache *cache, c
  * pointers.  Same arguments and result as nvfp4_paged_decode_attention without
  * workspace/workspace_bytes; the split-KV scratch lives in a fixed array of
  * NVKV_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the
- * library keeps until the process exits.  The scratch a call needs is an
- * 8-byte merge record per (sequence, KV head) plus two 4160-byte partial
- * slots per CTA, and
- * the CTA count never exceeds one resident wave (152 on a GB300), so every
- * supported problem fits; a device that would need more is refused with
- * NVKV_ERR_WORKSPACE_TOO_SMALL before any launch.  The first call on a device
- * looks up the array's device address (set-up, once per device, with that
- * device current); make that first call before any stream capture.  Each call
- * writes all of the array it reads, so nothing needs clearing between calls.
- * All calls share the one array and it keeps the last call's contents, so calls that can
- * overlap on the GPU (different streams, different host threads without
- * ordering) race and give wrong results: order them on one stream.  No
- * cudaMalloc, cudaFree or allocating library routine is called. */
+ * library keeps until the process exits.  The scratch a call needs is a
+ * 4-byte arrival counter per (sequence, KV head) (batch * num_kv_heads * 4
+ * bytes, rounded up to 256) plus two 4160-byte partial slots per CTA, and the
+ * CTA count never exceeds one resident wave (152 on a GB300, 1.27 MB of
+ * slots), so on a GB300 every problem with batch * num_kv_heads <= 1,700,000
+ * fits (batch <= 1024 as for every decode call; num_kv_heads has no other
+ * bound).  A problem whose counters alone exceed the array is refused with
+ * NVKV_ERR_WORKSPACE_TOO_SMALL before any CUDA call, and one whose counters
+ * and slots together exceed it with the same code before any launch.  Each call first clears its counters with one
+ * cudaMemsetAsync on `stream` (so a call after a failed one starts clean), then
+ * launches the decode kernel.  The first call on a device looks up the
+ * array's device address (set-up, once per device, with that device current);
+ * make that first call before any stream capture.  The cached address belongs
+ * to the CUDA context it was looked up in: after cudaDeviceReset (or any
+ * teardown of the primary context) it is stale, so do not call this entry
+ * point again in that process.  All calls share the one array and it keeps
+ * the last call's contents, so calls that can overlap on the GPU (different
+ * streams, different host threads without ordering) race and give wrong
+ * results: order them on one stream.  No cudaMalloc, cudaFree or allocating
+ * library routine is called. */
 #define NVKV_NOALLOC_SCRATCH_BYTES (8u << 20)
 nvkv_status nvfp4_paged_decode_attention_noalloc(const void *q, const nvkv_cache *cache,
                                                  const int32_t *block_table, int32_t max_pages,

@@ -35,6 +35,7 @@ NVKV_ERR_INVALID_ARG = 1
 NVKV_ERR_UNSUPPORTED = 2
 NVKV_ERR_CUDA = 3
 NVKV_ERR_WORKSPACE_TOO_SMALL = 4
+NVKV_NOALLOC_SCRATCH_BYTES = 8 << 20  # the header's fixed scratch array of the no-alloc decode
 
 PREC_NVFP4 = 0
 PREC_FP8 = 1

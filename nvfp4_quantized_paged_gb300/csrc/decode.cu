@@ -9,8 +9,10 @@
 //     the whole batch are laid end to end and cut into equal contiguous shares,
 //     one per CTA of a persistent grid (SMs x resident CTAs), so every CTA
 //     streams the same number of bytes whatever the sequence lengths.  A
-//     (sequence, KV head) cut between CTAs leaves split-KV partials that a
-//     second kernel merges with the log-sum-exp rule.
+//     (sequence, KV head) cut between CTAs leaves split-KV partials; each
+//     contributor counts itself on the pair's arrival counter and the CTA
+//     that arrives last merges the parts with the log-sum-exp rule at its
+//     end (one launch per call, no merge kernel).
 //   * Warp roles: a producer warp per consumer group streams the group's tiles
 //     into its shared-memory ring with 1-D bulk copies (one per page block,
 //     mbarrier transaction counts); a query warp prepares each segment's query
@@ -144,8 +146,9 @@ struct Cfg {
   static constexpr int oLast = oCum + (kMaxBatch + 1) * 4;                // [kMaxBatch] u8
   static constexpr int oBars = (oLast + kMaxBatch + 15) / 16 * 16;
   static constexpr int kBars = 2 * kStages + kGroups + 2 * kQBufs + 1;  // full, empty, sready, qready, qfree, mdone
-  static constexpr int oFlags = oBars + kBars * 8;  // tmem holder, abort, fills[kStages], W, NC, u0, u1
-  static constexpr int kSmem = oFlags + 4 * (6 + kStages);
+  static constexpr int oFlags = oBars + kBars * 8;  // tmem holder, abort, fills[kStages], W, NC, u0, u1, npend
+  static constexpr int oPend = oFlags + 4 * (7 + kStages);  // [2][4] i32: split pairs this CTA merges at its end
+  static constexpr int kSmem = oPend + 4 * 8;
 };
 
 struct DecodeArgs {
@@ -157,8 +160,8 @@ struct DecodeArgs {
   int32_t B, Hq, G;
   float sm_scale;
   int32_t num_ctas;
-  int2 *unit_info;    // [B][Hkv] per call: {partial slot of the first contributor, contributors}
-  float *partials;    // [num_ctas][2][kSlotFloats]
+  uint32_t *counters;  // [B][Hkv] arrivals of split (sequence, KV head) pairs; 0 between calls
+  float *partials;     // [num_ctas][2][kSlotFloats]
   __nv_bfloat16 *out;
 };
 
@@ -210,6 +213,35 @@ __device__ __forceinline__ Seg seg_next(const Seg &s, int64_t u, int64_t u_end, 
 __device__ __forceinline__ int64_t share_begin(int64_t c, int64_t W, int64_t NC) { return c * W / NC; }
 __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t W, int64_t NC) {
   return ((u + 1) * NC + W - 1) / W - 1;
+}
+
+// Split-KV arrival, by one thread once this CTA's partial of segment s is
+// written and fenced.  The contributors of (b, h) are the CTAs owning its
+// first through last unit: contributor 0 left its part in slot 0 of its CTA
+// if the pair opens that CTA's share, else in slot 1; contributor k > 0 in
+// slot 0 of CTA c_first + k (the pair opens its share).  The contributor
+// that arrives last resets the counter for the next call and records the
+// pair {b, h, n, 2 c_first + slot} in the CTA's pending list (at most two:
+// a share cuts at most its first and its last pair).
+__device__ __forceinline__ void split_arrive(const DecodeArgs &a, const int32_t *cum, const Seg &s, int64_t W,
+                                             int64_t NC, int *npend, int *pend) {
+  const int Hkv = a.c.Hkv;
+  const int nb = cum[s.b + 1] - cum[s.b];
+  const int64_t ubh0 = static_cast<int64_t>(cum[s.b]) * Hkv + static_cast<int64_t>(s.h) * nb;
+  const int64_t c_first = owner_of(ubh0, W, NC);
+  const int n = static_cast<int>(owner_of(ubh0 + nb - 1, W, NC) - c_first + 1);
+  uint32_t *cnt = a.counters + static_cast<int64_t>(s.b) * Hkv + s.h;
+  const uint32_t before = atomicAdd(cnt, 1u);
+  if (before == static_cast<uint32_t>(n - 1)) {  // every other part is in place
+    atomicExch(cnt, 0u);
+    const int r = atomicAdd(npend, 1);
+    if (r < 2) {
+      pend[4 * r + 0] = s.b;
+      pend[4 * r + 1] = s.h;
+      pend[4 * r + 2] = n;
+      pend[4 * r + 3] = static_cast<int>(c_first) * 2 + (share_begin(c_first, W, NC) == ubh0 ? 0 : 1);
+    }
+  }
 }
 
 // Visible tokens of sequence b, from the set-up's shared-memory copies: its
@@ -410,10 +442,10 @@ __device__ void prepare_query(const DecodeArgs &a, const Seg &s, uint8_t *img, u
 // or to the CTA's partial slot for the merge kernel.
 template <int PREC, int NH>
 __device__ void merge_segment(const DecodeArgs &a, uint8_t *smem, const int32_t *cum, const Seg &s, int slot_id,
-                              int64_t W, int64_t NC) {
+                              int64_t W, int64_t NC, int *npend) {
   using C = Cfg<PREC, NH>;
   const int lane = threadIdx.x & 31;
-  const int G = a.G, Hkv = a.c.Hkv;
+  const int G = a.G;
   const float *mrg_o = reinterpret_cast<const float *>(smem + C::oMrgO);
   float *mrg_ml = reinterpret_cast<float *>(smem + C::oMrgMl);
   float *mrg_hd = reinterpret_cast<float *>(smem + C::oMrgHd);
@@ -453,14 +485,10 @@ __device__ void merge_segment(const DecodeArgs &a, uint8_t *smem, const int32_t 
       }
     }
   }
-  if (lane == 0 && s.t0 == 0) {  // merge record of (b, h), as in the consumers' merge
-    int2 info = make_int2(0, 1);
-    if (!complete) {
-      const int64_t ubh0 = static_cast<int64_t>(cum[s.b]) * Hkv + static_cast<int64_t>(s.h) * nb;
-      info.x = static_cast<int>(blockIdx.x) * 2 + slot_id;
-      info.y = static_cast<int>(owner_of(ubh0 + nb - 1, W, NC) - blockIdx.x + 1);
-    }
-    a.unit_info[s.b * Hkv + s.h] = info;
+  if (!complete) {
+    __threadfence();  // this lane's part of the partial, visible before the arrival
+    __syncwarp();
+    if (lane == 0) split_arrive(a, cum, s, W, NC, npend, npend + 1);
   }
   __syncwarp();
 }
@@ -471,7 +499,7 @@ __device__ void merge_segment(const DecodeArgs &a, uint8_t *smem, const int32_t 
 template <int PREC, int NH>
 __device__ int query_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uint64_t *qready, uint64_t *qfree,
                           uint64_t *mdone, const int32_t *cum, int64_t u0, int64_t u1, int64_t W, int64_t NC,
-                          volatile int *abort, float kscale) {
+                          volatile int *abort, float kscale, int *npend) {
   using C = Cfg<PREC, NH>;
   const int lane = threadIdx.x & 31;
   uint8_t *qimg = smem + C::oQImg;
@@ -504,7 +532,7 @@ __device__ int query_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uin
     } else if (C::kAsyncMerge && u_m + (s_m.t1 - s_m.t0) < u1) {  // the last segment: merged by the consumers
       const int q = sm % kQBufs;
       if (!warp_wait(&qfree[q], static_cast<uint32_t>(sm / kQBufs) & 1u, abort)) return sp;  // segment sm done
-      merge_segment<PREC, NH>(a, smem, cum, s_m, u_m == u0 ? 0 : 1, W, NC);
+      merge_segment<PREC, NH>(a, smem, cum, s_m, u_m == u0 ? 0 : 1, W, NC, npend);
       if (lane == 0) mbar_arrive(mdone);  // its buffers may be rewritten
       __syncwarp();
       u_m += s_m.t1 - s_m.t0;
@@ -722,7 +750,7 @@ template <int PREC, int NH>
 __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uint64_t *full, uint64_t *empty,
                               uint64_t *sready, uint64_t *qready, uint64_t *qfree, uint64_t *mdone, const int32_t *cum,
                               int64_t u0, int64_t u1, int64_t W, int64_t NC, volatile int *abort,
-                              int64_t &last_issued) {
+                              int64_t &last_issued, int *npend) {
   using C = Cfg<PREC, NH>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = warp / kGroupWarps, qd = warp % kGroupWarps;  // consumer group, TMEM lane quadrant
@@ -958,19 +986,6 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
     const int nb = cum[s.b + 1] - cum[s.b];
     const bool complete = (s.t0 == 0) && (s.t1 == nb);
     const int slot_id = (u == u0) ? 0 : 1;
-    if (tid == 0 && (complete || s.t0 == 0)) {
-      // The CTA holding the first tile of (b, h) tells the merge kernel where
-      // the parts are: contributor k > 0 of the unit left its part in slot 0
-      // of CTA c_first + k (the unit opens its share), contributor 0 in this
-      // CTA's slot slot_id.
-      int2 info = make_int2(0, 1);
-      if (!complete) {
-        const int64_t ubh0 = static_cast<int64_t>(cum[s.b]) * Hkv + static_cast<int64_t>(s.h) * nb;
-        info.x = static_cast<int>(blockIdx.x) * 2 + slot_id;
-        info.y = static_cast<int>(owner_of(ubh0 + nb - 1, W, NC) - blockIdx.x + 1);
-      }
-      a.unit_info[s.b * Hkv + s.h] = info;
-    }
     float *part = a.partials + (static_cast<int64_t>(blockIdx.x) * 2 + slot_id) * kSlotFloats;
     for (int hp = 0; hp < G; hp += C::kMH) {  // kMH heads per pass
 #pragma unroll
@@ -1020,15 +1035,69 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
           }
         }
       }
+      if (!complete) __threadfence();  // this thread's part of the partial, visible before the arrival
       named_bar_sync(1, kConsumerWarps * 32);
     }
+    if (!complete && tid == 0) split_arrive(a, cum, s, W, NC, npend, npend + 1);
     if (lane == 0) mbar_arrive(&qfree[qb]);  // every score of this segment was read: its image may be reused
     u += ntiles;
   }
 }
 
 // ---------------------------------------------------------------------------
-// The decode kernel: set-up, role dispatch, teardown.
+// Split-KV merge (log-sum-exp rule) of one (sequence, KV head) whose parts
+// have all arrived, by every thread of the CTA that arrived last.
+// Contributor k left (o_k, m_k, l_k) in log2 units; out = sum_k 2^(m_k - M)
+// o_k / sum_k 2^(m_k - M) l_k * g_V, M = max_k m_k.  A thread takes one
+// output element (head, value) and folds the parts in contributor order,
+// loading a batch of contributors at once (one round trip per batch); the
+// result does not depend on which CTA arrived last.
+// ---------------------------------------------------------------------------
+constexpr int kMergeBatch = 8;  // contributors whose loads are in flight together
+
+__device__ void final_merge(const DecodeArgs &a, const int *rec) {
+  const int b = rec[0], h = rec[1], n = rec[2], c_first = rec[3] >> 1, slot0 = rec[3] & 1;
+  const float vscale = a.c.scale[1];
+  __threadfence();  // the other contributors' parts were published before their arrivals
+  for (int e = threadIdx.x; e < a.G * kD; e += kThreads) {
+    const int hd = e / kD, d = e % kD;
+    float M = -INFINITY, L = 0.0f, acc = 0.0f;
+    for (int k0 = 0; k0 < n; k0 += kMergeBatch) {
+      float m[kMergeBatch], l[kMergeBatch], o[kMergeBatch];
+#pragma unroll
+      for (int q = 0; q < kMergeBatch; ++q) {
+        const int k = k0 + q;
+        if (k < n) {
+          const float *st = a.partials + (static_cast<int64_t>(c_first + k) * 2 + (k == 0 ? slot0 : 0)) * kSlotFloats;
+          m[q] = __ldcg(st + kMaxGroup * kD + hd);
+          l[q] = __ldcg(st + kMaxGroup * kD + kMaxGroup + hd);
+          o[q] = __ldcg(st + hd * kD + d);
+        } else {
+          m[q] = -INFINITY;
+          l[q] = 0.0f;
+          o[q] = 0.0f;
+        }
+      }
+      float mb = M;
+#pragma unroll
+      for (int q = 0; q < kMergeBatch; ++q) mb = fmaxf(mb, m[q]);
+      const float r = M == -INFINITY ? 0.0f : ex2(M - mb);
+      L *= r;
+      acc *= r;
+#pragma unroll
+      for (int q = 0; q < kMergeBatch; ++q) {
+        const float w = m[q] == -INFINITY ? 0.0f : ex2(m[q] - mb);
+        L += w * l[q];
+        acc += w * o[q];
+      }
+      M = mb;
+    }
+    a.out[(static_cast<int64_t>(b) * a.Hq + h * a.G + hd) * kD + d] = __float2bfloat16_rn(acc * (vscale / L));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The decode kernel: set-up, role dispatch, split-KV merges, teardown.
 // ---------------------------------------------------------------------------
 template <int PREC, int NH>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a) {
@@ -1045,6 +1114,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(flags);
   volatile int *abort = flags + 1;
   int *fills = flags + 2;  // fills issued per ring slot
+  int *npend = flags + 6 + C::kStages;  // split pairs to merge at the end, then their records (oPend)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = a.c.Hkv, B = a.B;
@@ -1053,6 +1123,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
   // ---- set-up: barriers, TMEM, tiles per sequence -> prefix sums ----
   if (tid == 0) {
     flags[1] = 0;
+    *npend = 0;
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kGroupWarps);  // the four warps of the tile's group read it
@@ -1125,7 +1196,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     if (cum[b + 1] == cum[b]) {
       uint4 *o = reinterpret_cast<uint4 *>(a.out + static_cast<int64_t>(b) * a.Hq * kD);
       for (int i = tid; i < a.Hq * kD / 8; i += kThreads) o[i] = make_uint4(0, 0, 0, 0);
-      if (tid < Hkv) a.unit_info[b * Hkv + tid] = make_int2(0, 0);  // nothing to merge
     }
   }
 
@@ -1134,18 +1204,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     producer<PREC, NH>(a, smem + C::oRing, full, empty, cum, u0, u1, warp - kProducerWarp, abort, fills);
   } else if (warp == kQueryWarp) {
     const float kscale = __fmul_rn(a.c.scale[0], a.sm_scale * 1.4426950408889634f);
-    last_issued = query_role<PREC, NH>(a, smem, tmem, qready, qfree, mdone, cum, u0, u1, W, NC, abort, kscale);
+    last_issued = query_role<PREC, NH>(a, smem, tmem, qready, qfree, mdone, cum, u0, u1, W, NC, abort, kscale, npend);
   } else {
     consumer_role<PREC, NH>(a, smem, tmem, full, empty, sready, qready, qfree, mdone, cum, u0, u1, W, NC, abort,
-                            last_issued);
+                            last_issued, npend);
   }
 
-  // this CTA's partials are written: the combine grid may start launching
+  // the next kernel on the stream may start its set-up
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   tc_fence_before();
   __syncthreads();
-  // after a timeout, wait (bounded) for copies and MMAs still in flight
-  if (*abort) {
+  if (!*abort) {  // split pairs whose last part arrived from this CTA
+    const int np = min(*npend, 2);
+    for (int r = 0; r < np; ++r) final_merge(a, npend + 1 + 4 * r);
+  } else {  // after a timeout, wait (bounded) for copies and MMAs still in flight
     if (tid == 0) set_err(a.c.err, NVKV_DEVERR_TIMEOUT);
     volatile int never = 0;
     if (tid == kProducerWarp * 32) {
@@ -1164,73 +1236,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-}
-
-// ---------------------------------------------------------------------------
-// Split-KV merge (log-sum-exp rule), one CTA per (sequence, KV head, query
-// head of the group), thread = head_dim element.  Runs after the decode grid
-// (programmatic dependent launch: griddepcontrol.wait returns once the decode
-// grid has completed and its writes are visible).  Contributor k of a
-// (sequence, KV head) left (o_k, m_k, l_k) in log2 units; out = sum_k
-// 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k * g_V, M = max_k m_k.  The decode
-// grid left, per (sequence, KV head), where the parts are and how many; pairs
-// with one contributor (or none) were written by the decode grid itself.
-// ---------------------------------------------------------------------------
-struct CombineArgs {
-  const int2 *unit_info;
-  const float *partials;
-  const float *scale;
-  int32_t Hq, G;
-  __nv_bfloat16 *out;
-};
-
-constexpr int kCombineThreads = kD;
-constexpr int kCombineBatch = 16;  // contributors whose loads are in flight together
-
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
-  const int tid = threadIdx.x;
-  const int hd = blockIdx.x % a.G, bh = blockIdx.x / a.G;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the next kernel may start its set-up
-  const int2 info = a.unit_info[bh];
-  const int n = info.y;
-  if (n <= 1) return;  // written directly by the decode grid
-  // Every thread (one head_dim element) loads the statistics and its element
-  // of a batch of contributors at once and folds them into a running
-  // (max, sum, acc) triple: one round trip per batch, no block reductions.
-  const int first_slot = info.x, next_slot = (info.x / 2 + 1) * 2;  // contributor k > 0: slot next_slot + 2 (k - 1)
-  float M = -INFINITY, L = 0.0f, acc = 0.0f;
-  for (int k0 = 0; k0 < n; k0 += kCombineBatch) {
-    float m[kCombineBatch], l[kCombineBatch], o[kCombineBatch];
-#pragma unroll
-    for (int q = 0; q < kCombineBatch; ++q) {
-      const int k = k0 + q;
-      if (k < n) {
-        const float *st = a.partials + static_cast<int64_t>(k == 0 ? first_slot : next_slot + 2 * (k - 1)) * kSlotFloats;
-        m[q] = st[kMaxGroup * kD + hd];
-        l[q] = st[kMaxGroup * kD + kMaxGroup + hd];
-        o[q] = st[hd * kD + tid];
-      } else {
-        m[q] = -INFINITY;
-        l[q] = 0.0f;
-        o[q] = 0.0f;
-      }
-    }
-    float mb = M;
-#pragma unroll
-    for (int q = 0; q < kCombineBatch; ++q) mb = fmaxf(mb, m[q]);
-    const float r = M == -INFINITY ? 0.0f : ex2(M - mb);
-    L *= r;
-    acc *= r;
-#pragma unroll
-    for (int q = 0; q < kCombineBatch; ++q) {
-      const float w = m[q] == -INFINITY ? 0.0f : ex2(m[q] - mb);
-      L += w * l[q];
-      acc += w * o[q];
-    }
-    M = mb;
-  }
-  a.out[(static_cast<int64_t>(bh) * a.G + hd) * kD + tid] = __float2bfloat16_rn(acc * (a.scale[1] / L));
 }
 
 // ---------------------------------------------------------------------------
@@ -1314,11 +1319,11 @@ int64_t num_ctas_for(int prec, int32_t batch, int32_t Hkv, int32_t G, int64_t ma
   return n < 1 ? 1 : n;
 }
 
-// Workspace = per-(sequence, KV head) merge records + two partial slots per CTA.
-size_t info_bytes(int32_t batch, int32_t Hkv) { return (static_cast<size_t>(batch) * Hkv * 8 + 255) / 256 * 256; }
+// Workspace = an arrival counter per (sequence, KV head) + two partial slots per CTA.
+size_t counter_bytes(int32_t batch, int32_t Hkv) { return (static_cast<size_t>(batch) * Hkv * 4 + 255) / 256 * 256; }
 
 size_t workspace_bytes_for(int32_t batch, int32_t Hkv, int64_t nctas) {
-  return info_bytes(batch, Hkv) + static_cast<size_t>(nctas) * 2 * kSlotFloats * sizeof(float);
+  return counter_bytes(batch, Hkv) + static_cast<size_t>(nctas) * 2 * kSlotFloats * sizeof(float);
 }
 
 // Programmatic dependent launch: the grid may start while the previous kernel
@@ -1377,8 +1382,8 @@ nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t 
   a.G = G;
   a.sm_scale = sm_scale > 0.0f ? sm_scale : 1.0f / sqrtf(static_cast<float>(cache->head_dim));
   a.num_ctas = static_cast<int32_t>(nctas);
-  a.unit_info = static_cast<int2 *>(workspace);
-  a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + info_bytes(batch, Hkv));
+  a.counters = static_cast<uint32_t *>(workspace);
+  a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + counter_bytes(batch, Hkv));
   a.out = static_cast<__nv_bfloat16 *>(out);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (prec == NVKV_PREC_NVFP4) {
@@ -1387,31 +1392,6 @@ nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t 
   } else {
     if (G <= 4) launch_decode<NVKV_PREC_FP8_E4M3, 4>(a, s);
     else launch_decode<NVKV_PREC_FP8_E4M3, 8>(a, s);
-  }
-  st = launch_status();
-  if (st != NVKV_OK) return st;
-  // split-KV merge, launched as a programmatic dependent of the decode grid
-  CombineArgs ca;
-  ca.unit_info = a.unit_info;
-  ca.partials = a.partials;
-  ca.scale = a.c.scale;
-  ca.Hq = num_q_heads;
-  ca.G = G;
-  ca.out = a.out;
-  const int64_t cgrid = static_cast<int64_t>(batch) * Hkv * G;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(cgrid));
-  cfg.blockDim = dim3(kCombineThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, combine_kernel, ca) != cudaSuccess) {
-    cudaGetLastError();  // clear, then fall back to an ordinary stream-ordered launch
-    combine_kernel<<<static_cast<unsigned>(cgrid), kCombineThreads, 0, s>>>(ca);
   }
   return launch_status();
 }
@@ -1464,9 +1444,16 @@ nvkv_status nvfp4_paged_decode_attention_noalloc(const void *q, const nvkv_cache
   if (st != NVKV_OK) return st;
   if (batch < 0 || batch > kMaxBatch) return batch < 0 ? NVKV_ERR_INVALID_ARG : NVKV_ERR_UNSUPPORTED;
   if (batch == 0) return NVKV_OK;
+  if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0) return NVKV_ERR_INVALID_ARG;
+  // counters plus at least one CTA's two partial slots (refused before any CUDA call)
+  const size_t cb = counter_bytes(batch, cache->num_kv_heads);
+  if (cb + 2 * kSlotFloats * sizeof(float) > NVKV_NOALLOC_SCRATCH_BYTES) return NVKV_ERR_WORKSPACE_TOO_SMALL;
   void *scratch = noalloc_scratch_ptr();
   if (!scratch) return NVKV_ERR_CUDA;
-  // every call rewrites the scratch it later reads (schedule and partials): nothing needs clearing
+  // The arrival counters must start at zero.  A call cut short by a device
+  // error can leave them otherwise, so every call clears them first (one
+  // memset on the stream, no allocation); the partial slots need nothing.
+  if (cudaMemsetAsync(scratch, 0, cb, static_cast<cudaStream_t>(stream)) != cudaSuccess) return NVKV_ERR_CUDA;
   return decode_common(q, cache, block_table, max_pages, seq_lens, batch, num_q_heads, layer_precision, sm_scale,
                        num_splits, scratch, NVKV_NOALLOC_SCRATCH_BYTES, out, stream);
 }

@@ -69,13 +69,28 @@ def test_decode_argument_checks(nv):
 
 
 def test_workspace_size_arithmetic(nv):
-    # explicit splits need no device: one 8-byte merge record per (sequence, KV
-    # head), rounded up to 256 B, then 2 partial slots per CTA
+    # explicit splits need no device: one 4-byte arrival counter per (sequence,
+    # KV head), rounded up to 256 B, then 2 partial slots per CTA
     slot = (8 * 128 + 16) * 4
-    assert nv.nvkv_decode_workspace_size(16, 32, 8, 128, 4) == 1024 + 16 * 8 * 4 * 2 * slot
+    assert nv.nvkv_decode_workspace_size(16, 32, 8, 128, 4) == 512 + 16 * 8 * 4 * 2 * slot
     assert nv.nvkv_decode_workspace_size(3, 16, 2, 128, 1) == 256 + 3 * 2 * 1 * 2 * slot
     assert nv.nvkv_decode_workspace_size(16, 32, 8, 64, 4) == 0
     assert nv.nvkv_decode_workspace_size(16, 32, 2, 128, 4) == 0  # group of 16
+
+
+def test_noalloc_refuses_problems_beyond_its_scratch(nv):
+    # batch x Hkv arrival counters (4 B each) plus one CTA's two partial slots
+    # must fit in the fixed array; larger problems are refused on the host,
+    # before any CUDA call (so this runs without a GPU)
+    L = nv.lib()
+    cap = nv.NVKV_NOALLOC_SCRATCH_BYTES
+    slot = (8 * 128 + 16) * 4
+    hkv = 2048                                   # 1024 x 2048 x 4 B = the whole array
+    assert 1024 * hkv * 4 + 2 * slot > cap
+    d = _desc(nv, num_kv_heads=hkv)
+    st = L.nvfp4_paged_decode_attention_noalloc(0x50000, ctypes.byref(d), 0x60000, 4, 0x70000, 1024, hkv, 0, 0.0,
+                                                0, 0x90000, None)
+    assert st == nv.NVKV_ERR_WORKSPACE_TOO_SMALL
 
 
 def test_other_entry_points_reject_bad_arguments(nv):
