@@ -148,7 +148,8 @@ struct Cfg {
   static constexpr int kBars = 2 * kStages + kGroups + 2 * kQBufs + 1;  // full, empty, sready, qready, qfree, mdone
   static constexpr int oFlags = oBars + kBars * 8;  // tmem holder, abort, fills[kStages], W, NC, u0, u1, npend
   static constexpr int oPend = oFlags + 4 * (7 + kStages);  // [2][4] i32: split pairs this CTA merges at its end
-  static constexpr int kSmem = oPend + 4 * 8;
+  static constexpr int oArm = oPend + 4 * 8;  // [kGroups] i32 arming counters, [kGroups] i32 last tile armed
+  static constexpr int kSmem = oArm + 4 * 2 * kGroups;
 };
 
 struct DecodeArgs {
@@ -469,17 +470,29 @@ __device__ void merge_segment(const DecodeArgs &a, uint8_t *smem, const int32_t 
   __syncwarp();
   const float vscale = a.c.scale[1];
   float *part = a.partials + (static_cast<int64_t>(blockIdx.x) * 2 + slot_id) * kSlotFloats;
-  for (int e2 = lane; e2 < G * kD; e2 += 32) {
-    const int hd = e2 / kD, d = e2 % kD;
-    float o = 0.0f;
+  static_assert(kD == 4 * 32, "one head per pass: four values per lane");
+  for (int hd = 0; hd < G; ++hd) {  // lane: values 4 lane .. 4 lane + 3 of head hd
+    float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) o += mrg_ml[(w * kMaxGroup + hd) * 2] * mrg_o[(w * C::kMH + hd) * kD + d];
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float f = mrg_ml[(w * kMaxGroup + hd) * 2];
+      const float4 x = reinterpret_cast<const float4 *>(mrg_o + (w * C::kMH + hd) * kD)[lane];
+      o.x += f * x.x;
+      o.y += f * x.y;
+      o.z += f * x.z;
+      o.w += f * x.w;
+    }
     const float lsum = mrg_hd[2 * hd + 1];
     if (complete) {
-      a.out[(static_cast<int64_t>(s.b) * a.Hq + s.h * G + hd) * kD + d] = __float2bfloat16_rn(o * (vscale / lsum));
+      const float sc = vscale / lsum;
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(o.x * sc, o.y * sc), hi = __floats2bfloat162_rn(o.z * sc, o.w * sc);
+      uint2 pk;
+      pk.x = *reinterpret_cast<const uint32_t *>(&lo);
+      pk.y = *reinterpret_cast<const uint32_t *>(&hi);
+      reinterpret_cast<uint2 *>(a.out + (static_cast<int64_t>(s.b) * a.Hq + s.h * G + hd) * kD)[lane] = pk;
     } else {
-      part[hd * kD + d] = o;
-      if (d == 0) {
+      reinterpret_cast<float4 *>(part + hd * kD)[lane] = o;
+      if (lane == 0) {
         part[kMaxGroup * kD + hd] = mrg_hd[2 * hd];
         part[kMaxGroup * kD + kMaxGroup + hd] = lsum;
       }
@@ -683,40 +696,40 @@ __device__ __forceinline__ int seg_index_of(int64_t x, int64_t u, int sidx, int 
   return sidx;
 }
 
-// Score MMAs of one tile for consumer group grp: its stage is ring slot
-// `slot` (fill parity fpar), its query image qb (parity qpar).  Once the
-// stage has landed each of the group's warps (NVFP4) writes the K block scales of
-// its 32 rows into the group's TMEM scale-factor columns (row m = 32 qd + lane
-// is read by the MMA from lane m, column sfa_col(grp, mma) + qd); the four
-// warps meet on the group's named barrier; one thread waits for the query
-// image and issues the MMAs into the group's score buffer, committing them to
-// sready[grp].  The caller has read the group's previous scores, so the buffer
-// and the scale columns are free.  True (warp-uniform) when the MMAs went out
-// (for the issuing warp) or the stage landed (for the others).
+// Score MMAs of one tile of consumer group grp (stage = ring slot `slot`,
+// query image qb with parity qpar), armed by the group's four warps without
+// a barrier.  Each warp calls this once the stage has landed and it has read
+// its rows of the group's previous scores (so the score buffer and the scale
+// columns are free for its rows): NVFP4 writes the K block scales of its 32
+// rows into the group's TMEM scale-factor columns (row m = 32 qd + lane is
+// read by the MMA from lane m, column sfa_col(grp, mma) + qd), then the warp
+// counts itself on the group's arming counter in shared memory.  The warp
+// that arrives fourth waits for the query image and issues the MMAs into the
+// group's score buffer, committing them to sready[grp].  The counter only
+// grows: the four arrivals of one tile all come before any arrival for the
+// group's next tile (which needs these MMAs' scores), so the fourth arrival
+// of a tile is the one that finds count = 3 (mod 4).  Returns true (lane 0)
+// when this warp issued the MMAs.
 template <int PREC, int NH>
-__device__ __forceinline__ bool issue_tile(uint8_t *smem, uint32_t tmem, uint32_t tq, uint64_t *full, uint64_t *sready,
-                                           uint64_t *qready, int slot, uint32_t fpar, int qb, uint32_t qpar, int grp,
-                                           int qd, int lane, volatile int *abort, bool landed = false) {
+__device__ __forceinline__ bool arm_tile(uint8_t *smem, uint32_t tmem, uint32_t tq, uint64_t *sready, uint64_t *qready,
+                                         int *arm_cnt, int slot, int qb, uint32_t qpar, int grp, int qd, int lane,
+                                         volatile int *abort) {
   using C = Cfg<PREC, NH>;
   const uint8_t *stage = smem + C::oRing + slot * C::kStageBytes;
-  // Each warp waits for the stage itself (the wait suspends the warp) unless
-  // the caller saw it land already; a warp that gave up still meets the
-  // group barrier below.
-  bool ok = landed || warp_wait(&full[slot], fpar, abort);
   if constexpr (C::kNv) {
-    if (ok) {
-      const int t = 32 * qd + lane;
-      const uint2 sc = *reinterpret_cast<const uint2 *>(stage + (t >> 3) * kNvGroup + kNvKScales + (t & 7) * 8);
-      tmem_st1(tq + C::sfa_col(grp, 0) + qd, sc.x);  // blocks 0..3 (MMA 0)
-      tmem_st1(tq + C::sfa_col(grp, 1) + qd, sc.y);  // blocks 4..7 (MMA 1)
-      tmem_st_wait();
-    }
+    const int t = 32 * qd + lane;
+    const uint2 sc = *reinterpret_cast<const uint2 *>(stage + (t >> 3) * kNvGroup + kNvKScales + (t & 7) * 8);
+    tmem_st1(tq + C::sfa_col(grp, 0) + qd, sc.x);  // blocks 0..3 (MMA 0)
+    tmem_st1(tq + C::sfa_col(grp, 1) + qd, sc.y);  // blocks 4..7 (MMA 1)
+    tmem_st_wait();
   }
   tc_fence_before();
-  named_bar_sync(2 + grp, kGroupWarps * 32);
-  if (qd == 0) {
-    ok = ok && warp_wait(&qready[qb], qpar, abort);
-    if (ok && lane == 0) {
+  __syncwarp();
+  bool issued = false;
+  if (lane == 0) {
+    __threadfence_block();  // this warp's scale columns and score reads, before its arrival
+    if ((atomicAdd(&arm_cnt[grp], 1) & (kGroupWarps - 1)) == kGroupWarps - 1 && mbar_wait_bounded(&qready[qb], qpar, abort)) {
+      __threadfence_block();
       tc_fence_after();
       const uint32_t d = tmem + static_cast<uint32_t>(grp * C::N);
       const uint32_t a0 = smem_u32(stage), b0 = smem_u32(smem + C::oQImg + qb * C::kQImg);
@@ -732,10 +745,11 @@ __device__ __forceinline__ bool issue_tile(uint8_t *smem, uint32_t tmem, uint32_
                     idesc_e4m3(C::N), kk > 0 ? 1u : 0u);
       }
       umma_commit(&sready[grp]);
+      issued = true;
     }
-    __syncwarp();
   }
-  return ok;
+  __syncwarp();
+  return issued;
 }
 
 template <int NH>
@@ -750,7 +764,7 @@ template <int PREC, int NH>
 __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uint64_t *full, uint64_t *empty,
                               uint64_t *sready, uint64_t *qready, uint64_t *qfree, uint64_t *mdone, const int32_t *cum,
                               int64_t u0, int64_t u1, int64_t W, int64_t NC, volatile int *abort,
-                              int64_t &last_issued, int *npend) {
+                              int *arm_cnt, int *last_iss, int *npend) {
   using C = Cfg<PREC, NH>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = warp / kGroupWarps, qd = warp % kGroupWarps;  // consumer group, TMEM lane quadrant
@@ -775,19 +789,23 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
   int ibase = 0;           // CTA-local index of the segment's first tile
   int sidx = 0;
   bool ok = true;
-  last_issued = -1;
-  // The group's first tile is issued before anything else.
+  // The group's first tile is armed before anything else.
   if (grp < ntotal) {
     const Seg s0 = seg_at(u0, u1, cum, a.B, Hkv);
     const int sx = seg_index_of(grp, u0, 0, s0.t1 - s0.t0, u0, u1, cum, a.B, Hkv);
-    ok = issue_tile<PREC, NH>(smem, tmem, tq, full, sready, qready, grp * C::kStagesG, 0u, sx % kQBufs,
-                              static_cast<uint32_t>(sx / kQBufs) & 1u, grp, qd, lane, abort);
-    if (ok) last_issued = grp;
+    ok = warp_wait(&full[grp * C::kStagesG], 0u, abort);
+    if (ok && arm_tile<PREC, NH>(smem, tmem, tq, sready, qready, arm_cnt, grp * C::kStagesG, sx % kQBufs,
+                                 static_cast<uint32_t>(sx / kQBufs) & 1u, grp, qd, lane, abort))
+      last_iss[grp] = grp;
   }
   // After a timeout (ok false) the warps skip all work but keep walking the
   // same segments, so every named barrier of the merge still meets.
   Seg s = u0 < u1 ? seg_at(u0, u1, cum, a.B, Hkv) : Seg{0, 0, 0, 0};
-  for (int64_t u = u0; u < u1; ++sidx, s = u < u1 ? seg_next(s, u, u1, cum, Hkv) : s) {
+  for (int64_t u = u0; u < u1; ++sidx) {
+    // the segment after this one (its length places the group's next tile
+    // when that crosses the boundary)
+    const int ntiles = s.t1 - s.t0;
+    const Seg s_nx = u + ntiles < u1 ? seg_next(s, u + ntiles, u1, cum, Hkv) : s;
     const int Lb = seq_len_of(cum, s.b);
     const int qb = sidx % kQBufs;
     ok = ok && warp_wait(&qready[qb], static_cast<uint32_t>(sidx / kQBufs) & 1u, abort);
@@ -801,7 +819,6 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
     WarpO st;
 #pragma unroll
     for (int j = 0; j < 8; ++j) st.o[j][0] = st.o[j][1] = st.o[j][2] = st.o[j][3] = 0.0f;
-    const int ntiles = s.t1 - s.t0;
     for (int k = (grp - ibase % kGroups + kGroups) % kGroups; k < ntiles; k += kGroups) {
       const int i = ibase + k;
       const int slot = grp * C::kStagesG + slot_l;
@@ -833,39 +850,32 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
           for (int h = 0; h < NH; ++h) ssum[h] = sp[h][0] + sp[h][1];
         }
       }
-      // The group's next tile may now score into the same buffer.  Its MMAs
-      // go out now if its stage has landed for all four warps, else after
-      // this tile's P.V, so the group never waits for data it does not need
-      // yet.  (Every warp of the group takes the same barriers whatever ok is.)
+      // This warp's rows of the group's score buffer are read: it arms the
+      // group's next tile now if that tile's stage has landed, else after
+      // this tile's P.V, so it never waits for data it does not need yet.
       const bool has_next = i + kGroups < ntotal;
       int nqb = qb;
       uint32_t nqpar = static_cast<uint32_t>(sidx / kQBufs) & 1u;
-      bool issued = false;
+      bool armed = false;
       if (has_next) {
         if (k + kGroups >= ntiles) {  // the next tile lies in a later segment
-          const int sx = seg_index_of(i + kGroups, u, sidx, ntiles, u0, u1, cum, a.B, Hkv);
+          int sx = sidx + 1;
+          if (k + kGroups - ntiles >= s_nx.t1 - s_nx.t0)  // beyond the next segment too (short segments)
+            sx = seg_index_of(i + kGroups, u, sidx, ntiles, u0, u1, cum, a.B, Hkv);
           nqb = sx % kQBufs;
           nqpar = static_cast<uint32_t>(sx / kQBufs) & 1u;
         }
-        const bool landed = ok && mbar_test(&full[grp * C::kStagesG + nslot_l], nfpar);
-        if (named_bar_and(2 + grp, kGroupWarps * 32, landed)) {  // every warp of the group saw it land
-          ok = issue_tile<PREC, NH>(smem, tmem, tq, full, sready, qready, grp * C::kStagesG + nslot_l, nfpar, nqb,
-                                    nqpar, grp, qd, lane, abort, true);
-          if (ok) last_issued = i + kGroups;  // its MMAs went out
-          issued = true;
+        if (ok && mbar_test(&full[grp * C::kStagesG + nslot_l], nfpar)) {
+          if (arm_tile<PREC, NH>(smem, tmem, tq, sready, qready, arm_cnt, grp * C::kStagesG + nslot_l, nqb, nqpar,
+                                 grp, qd, lane, abort))
+            last_iss[grp] = i + kGroups;  // its MMAs went out
+          armed = true;
         }
       }
       slot_l = nslot_l;
       fpar = nfpar;
       spar ^= 1u;
-      if (!ok) {
-        if (has_next && !issued) {
-          if (issue_tile<PREC, NH>(smem, tmem, tq, full, sready, qready, grp * C::kStagesG + nslot_l, nfpar, nqb,
-                                   nqpar, grp, qd, lane, abort))
-            last_issued = i + kGroups;
-        }
-        continue;
-      }
+      if (!ok) continue;
 
       // scores of this lane's token, log2 units; masked past the sequence end
       const int t = s.t0 + k;
@@ -930,10 +940,11 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
-      if (has_next && !issued) {
-        ok = issue_tile<PREC, NH>(smem, tmem, tq, full, sready, qready, grp * C::kStagesG + slot_l, fpar, nqb, nqpar,
-                                  grp, qd, lane, abort);
-        if (ok) last_issued = i + kGroups;  // its MMAs went out
+      if (has_next && !armed) {
+        ok = warp_wait(&full[grp * C::kStagesG + slot_l], fpar, abort);
+        if (ok && arm_tile<PREC, NH>(smem, tmem, tq, sready, qready, arm_cnt, grp * C::kStagesG + slot_l, nqb, nqpar,
+                                     grp, qd, lane, abort))
+          last_iss[grp] = i + kGroups;  // its MMAs went out
       }
     }
     ibase += ntiles;
@@ -958,17 +969,15 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
 #pragma unroll
       for (int hd = 0; hd < NH; ++hd) {  // the lanes with c = hd / 2 hold head hd in column hd % 2
         if (hd < G && (hd >> 1) == c) {
-          float *dst = mrg_o + (warp * C::kMH + hd) * kD + 16 * r;
+          float2 *dst = reinterpret_cast<float2 *>(mrg_o + (warp * C::kMH + hd) * kD + 16 * r);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            dst[2 * j] = st.o[j][hd & 1];
-            dst[2 * j + 1] = st.o[j][2 + (hd & 1)];
-          }
+          for (int j = 0; j < 8; ++j) dst[j] = make_float2(st.o[j][hd & 1], st.o[j][2 + (hd & 1)]);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&qfree[qb]);  // scores read, merge data written
       u += ntiles;
+      s = s_nx;
       continue;
     }
     // ---- merge the four warps: (m, l) per head, O per (head, d) ----
@@ -992,12 +1001,9 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
       for (int e = 0; e < C::kMH; ++e) {
         const int hd = hp + e;  // held by the lanes with c = hd / 2, accumulator column hd % 2
         if (hd < G && (hd >> 1) == c) {
-          float *dst = mrg_o + (warp * C::kMH + e) * kD + 16 * r;
+          float2 *dst = reinterpret_cast<float2 *>(mrg_o + (warp * C::kMH + e) * kD + 16 * r);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            dst[2 * j] = st.o[j][hd & 1];
-            dst[2 * j + 1] = st.o[j][2 + (hd & 1)];
-          }
+          for (int j = 0; j < 8; ++j) dst[j] = make_float2(st.o[j][hd & 1], st.o[j][2 + (hd & 1)]);
         }
       }
       named_bar_sync(1, kConsumerWarps * 32);
@@ -1041,6 +1047,7 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
     if (!complete && tid == 0) split_arrive(a, cum, s, W, NC, npend, npend + 1);
     if (lane == 0) mbar_arrive(&qfree[qb]);  // every score of this segment was read: its image may be reused
     u += ntiles;
+    s = s_nx;
   }
 }
 
@@ -1115,6 +1122,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
   volatile int *abort = flags + 1;
   int *fills = flags + 2;  // fills issued per ring slot
   int *npend = flags + 6 + C::kStages;  // split pairs to merge at the end, then their records (oPend)
+  int *arm_cnt = reinterpret_cast<int *>(smem + C::oArm);  // per group: warps that armed its tiles so far
+  int *last_iss = arm_cnt + kGroups;                       // per group: the last tile whose MMAs went out
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = a.c.Hkv, B = a.B;
@@ -1124,6 +1133,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
   if (tid == 0) {
     flags[1] = 0;
     *npend = 0;
+    for (int g = 0; g < kGroups; ++g) {
+      arm_cnt[g] = 0;
+      last_iss[g] = -1;
+    }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kGroupWarps);  // the four warps of the tile's group read it
@@ -1199,7 +1212,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     }
   }
 
-  int64_t last_issued = -1;  // consumers: the last tile whose MMAs this thread issued; query warp: images
+  int64_t last_issued = -1;  // query warp: the images it prepared
   if (warp >= kProducerWarp && warp < kProducerWarp + kGroups) {
     producer<PREC, NH>(a, smem + C::oRing, full, empty, cum, u0, u1, warp - kProducerWarp, abort, fills);
   } else if (warp == kQueryWarp) {
@@ -1207,7 +1220,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     last_issued = query_role<PREC, NH>(a, smem, tmem, qready, qfree, mdone, cum, u0, u1, W, NC, abort, kscale, npend);
   } else {
     consumer_role<PREC, NH>(a, smem, tmem, full, empty, sready, qready, qfree, mdone, cum, u0, u1, W, NC, abort,
-                            last_issued, npend);
+                            arm_cnt, last_iss, npend);
   }
 
   // the next kernel on the stream may start its set-up
@@ -1224,8 +1237,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
       for (int s = 0; s < C::kStages; ++s)
         if (fills[s] > 0) mbar_wait_bounded(&full[s], static_cast<uint32_t>(fills[s] - 1) & 1u, &never);
     }
-    if (warp < kConsumerWarps && warp % kGroupWarps == 0 && lane == 0 && last_issued >= 0)  // MMA issuers
-      mbar_wait_bounded(&sready[warp / kGroupWarps], static_cast<uint32_t>(last_issued / kGroups) & 1u, &never);
+    if (warp < kConsumerWarps && warp % kGroupWarps == 0 && lane == 0) {  // the group's last score MMAs
+      const int li = last_iss[warp / kGroupWarps];
+      if (li >= 0) mbar_wait_bounded(&sready[warp / kGroupWarps], static_cast<uint32_t>(li / kGroups) & 1u, &never);
+    }
     if (tid == kQueryWarp * 32 && last_issued > 0) {  // the query warp's last image (its TMEM copies)
       const int q = static_cast<int>((last_issued - 1) % kQBufs);
       mbar_wait_bounded(&qready[q], static_cast<uint32_t>((last_issued - 1) / kQBufs) & 1u, &never);
