@@ -215,6 +215,30 @@ nvkv_status fp8_paged_decode_attention(const void *q, const nvkv_cache *cache, c
                                        int32_t num_q_heads, float sm_scale, int32_t num_splits, void *workspace,
                                        size_t workspace_bytes, void *out, void *stream);
 
+/* One decode step of a layer in one launch: the quantized write of each
+ * sequence's newest token followed by the paged decode attention over the
+ * cache that now holds it ([P2] Three Paths: in decode each new token's K/V
+ * is quantized into the NVFP4 cache and the decode kernel reads the cache;
+ * [P1] 03 per-layer precision).  The result, cache bytes and output, is that
+ * of nvfp4_kv_quantize_write (or fp8_kv_quantize_write) of k_new / v_new to
+ * the slot of position seq_lens[b] - 1 of each sequence b, i.e. slot
+ * block_table[b][(L - 1) / P] * P + (L - 1) % P, with global_scale =
+ * cache->kv_scale, then nvfp4_paged_decode_attention with the same arguments;
+ * one launch instead of two.  The token is written by the CTA that streams
+ * the sequence's last tile, just before it copies the tile.
+ *   k_new, v_new  [batch][num_kv_heads][head_dim] of `dtype` (FP32 or BF16),
+ *                 device, 16-byte aligned: row b is the newest token of
+ *                 sequence b (rows of sequences with seq_lens[b] == 0 are
+ *                 not read)
+ *   other arguments, workspace contract and errors as for
+ *   nvfp4_paged_decode_attention; a page id out of range sets
+ *   NVKV_DEVERR_PAGE and that token is not written. */
+nvkv_status nvfp4_paged_decode_step(const void *q, const void *k_new, const void *v_new, nvkv_dtype dtype,
+                                    const nvkv_cache *cache, const int32_t *block_table, int32_t max_pages,
+                                    const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                    int32_t layer_precision, float sm_scale, int32_t num_splits, void *workspace,
+                                    size_t workspace_bytes, void *out, void *stream);
+
 /* Decode attention that allocates nothing and takes no workspace (no
  * counterpart in the pages: this is a convenience of this library).  For
  * callers that cannot hand out device memory per call: serving engines that

@@ -88,6 +88,8 @@ SIGNATURES = {
                                             _vp, _vp]),
     "fp8_paged_decode_attention": (_i32, [_vp, _cachep, _vp, _i32, _vp, _i32, _i32, _f32, _i32, _vp, _sz, _vp,
                                           _vp]),
+    "nvfp4_paged_decode_step": (_i32, [_vp, _vp, _vp, _i32, _cachep, _vp, _i32, _vp, _i32, _i32, _i32, _f32, _i32,
+                                       _vp, _sz, _vp, _vp]),
     "nvfp4_paged_decode_attention_noalloc": (_i32, [_vp, _cachep, _vp, _i32, _vp, _i32, _i32, _i32, _f32, _i32,
                                                     _vp, _vp]),
     "nvfp4_kv_dequant_to_fp8_workspace": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _cachep, _vp, _vp, _vp, _i64,
@@ -273,6 +275,19 @@ def fp8_paged_decode_attention(q, cache: Cache, block_table, seq_lens, out, work
                                             _ptr(seq_lens), q.shape[0], q.shape[1], sm_scale, num_splits,
                                             _ptr(workspace), workspace.numel() * workspace.element_size(),
                                             _ptr(out), _stream(stream)))
+
+
+def nvfp4_paged_decode_step(q, k_new, v_new, cache: Cache, block_table, seq_lens, layer_precision, out, workspace,
+                            sm_scale=0.0, num_splits=0, stream=None):
+    """One decode step in one launch: each sequence's newest token (row b of
+    k_new / v_new, [B, Hkv, 128] FP32 or BF16) quantized into the cache at
+    position seq_lens[b] - 1, then decode attention over the cache."""
+    d = cache.desc()
+    _check("nvfp4_paged_decode_step",
+           lib().nvfp4_paged_decode_step(_ptr(q), _ptr(k_new), _ptr(v_new), _dtype_code(k_new), ctypes.byref(d),
+                                         _ptr(block_table), block_table.shape[1], _ptr(seq_lens), q.shape[0],
+                                         q.shape[1], layer_precision, sm_scale, num_splits, _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _ptr(out), _stream(stream)))
 
 
 def nvfp4_paged_decode_attention_noalloc(q, cache: Cache, block_table, seq_lens, layer_precision, out,

@@ -164,6 +164,8 @@ struct DecodeArgs {
   uint32_t *counters;  // [B][Hkv] arrivals of split (sequence, KV head) pairs; 0 between calls
   float *partials;     // [num_ctas][2][kSlotFloats]
   __nv_bfloat16 *out;
+  const void *k_new, *v_new;  // decode step: [B][Hkv][128] newest token of each sequence (null: none)
+  int32_t new_dtype;          // NVKV_DTYPE_F32 or NVKV_DTYPE_BF16
 };
 
 // Segment = run of consecutive units of one (sequence, KV head).
@@ -259,6 +261,84 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
 }
 
 // ---------------------------------------------------------------------------
+// The decode step's new token (nvfp4_paged_decode_step): the token at
+// position len - 1 of (b, h), read from k_new / v_new ([batch][Hkv][128]), is
+// quantized into its cache slot by the producer warp of the tile that holds
+// it, right before that tile is copied, with the layer's write rule and the
+// cache descriptor's global scales g:
+//   NVFP4: per 16-value block, scale byte = E4M3(amax / (6 g)), codes =
+//          E2M1(x / (E4M3 scale x g)); K codes two per byte (value 2j in the
+//          low nibble of byte j), V codes in this slot's nibble of the slot
+//          pair's bytes, the partner slot's nibble kept;
+//   FP8:   E4M3(x / g) per value.
+// Lane = (block blk = lane / 4, values 4 (lane % 4) .. + 3 of it).  No other
+// thread of the launch writes these bytes, so the shared V bytes are read,
+// modified and written with plain accesses.
+// ---------------------------------------------------------------------------
+template <int PREC>
+__device__ void append_token(const DecodeArgs &a, int b, int h, int64_t page, int off) {
+  const int lane = threadIdx.x & 31, blk = lane >> 2, q = lane & 3;
+  const CacheDev &c = a.c;
+  const int64_t e = (static_cast<int64_t>(b) * c.Hkv + h) * kD + 16 * blk + 4 * q;  // first of the lane's values
+#pragma unroll
+  for (int kind = 0; kind < 2; ++kind) {
+    const void *src = kind == 0 ? a.k_new : a.v_new;
+    float x[4];
+    if (a.new_dtype == NVKV_DTYPE_F32) {
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(src) + e));
+      x[0] = v.x;
+      x[1] = v.y;
+      x[2] = v.z;
+      x[3] = v.w;
+    } else {
+      const uint2 v = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(src) + e));
+      x[0] = __uint_as_float(v.x << 16);
+      x[1] = __uint_as_float(v.x & 0xFFFF0000u);
+      x[2] = __uint_as_float(v.y << 16);
+      x[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    }
+    const float g = c.scale[kind];
+    if constexpr (PREC == NVKV_PREC_NVFP4) {
+      float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // the block's four lanes
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      uint32_t sbyte = 0;
+      float den = 0.0f;
+      if (g != 0.0f) {
+        sbyte = e4m3x2_from_f32(__fdiv_rn(amax, __fmul_rn(6.0f, g)), 0.0f) & 0xFFu;
+        den = __fmul_rn(f32_from_e4m3(sbyte), g);
+      }
+      uint32_t codes = 0;  // values 4q .. 4q+3, one nibble each from bit 0
+      if (den != 0.0f)
+        codes = e2m1x2_from_f32(__fdiv_rn(x[0], den), __fdiv_rn(x[1], den)) |
+                (e2m1x2_from_f32(__fdiv_rn(x[2], den), __fdiv_rn(x[3], den)) << 8);
+      if (kind == 0) {
+        *reinterpret_cast<uint16_t *>(c.data + c.nv_kcodes(page, h, off, blk) + 2 * q) = static_cast<uint16_t>(codes);
+      } else {  // value 16 blk + j: byte j of the pair's 16 bytes, nibble off % 2
+        uint32_t *dst = reinterpret_cast<uint32_t *>(c.data + c.nv_vcodes(page, h, off, blk) + 4 * q);
+        const int sh = 4 * (off & 1);
+        const uint32_t spread =
+            (codes & 0xFu) | ((codes & 0xF0u) << 4) | ((codes & 0xF00u) << 8) | ((codes & 0xF000u) << 12);
+        *dst = (*dst & ~(0x0F0F0F0Fu << sh)) | (spread << sh);
+      }
+      if (q == 0) c.data[c.nv_scale(page, h, kind, off, blk)] = static_cast<uint8_t>(sbyte);
+    } else {
+      uint32_t w = 0;
+      if (g != 0.0f)
+        w = e4m3x2_from_f32(__fdiv_rn(x[0], g), __fdiv_rn(x[1], g)) |
+            (e4m3x2_from_f32(__fdiv_rn(x[2], g), __fdiv_rn(x[3], g)) << 16);
+      if (kind == 0) {
+        *reinterpret_cast<uint32_t *>(c.data + c.f8_kblock(page, h, off, blk) + 4 * q) = w;
+      } else {  // value 16 blk + 8 half + j: byte 2 j + off % 2 of chunk `half`
+        uint8_t *dst = c.data + c.f8_vchunk(page, h, off, blk, q >> 1) + (off & 1) + 8 * (q & 1);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[2 * i] = static_cast<uint8_t>(w >> (8 * i));
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Producer warps, one per consumer group: producer g streams the tiles
 // i = g (mod 3) of this CTA's share into group g's ring, one bulk copy per
 // page block (a tile spans 128 / P whole page blocks, placed back to back, so
@@ -303,6 +383,13 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
           wbase += 32;
           pg = pg_next;
           pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
+        }
+        if (a.k_new != nullptr && tok0 + ntok == len) {  // the pair's last tile holds the step's new token
+          const int pos = len - 1;
+          const int pw = __shfl_sync(0xffffffffu, pg, ((pos >> lgP) - wbase) & 31);
+          if (pw >= 0 && pw < a.c.num_pages) append_token<PREC>(a, s.b, s.h, pw, pos & (P - 1));
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // the written bytes, before the copy reads them
+          __syncwarp();
         }
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nblk) * block_bytes);
         const int page = __shfl_sync(0xffffffffu, pg, ((tok0 >> lgP) + lane - wbase) & 31);
@@ -1159,6 +1246,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
   // stream: everything above touches only this CTA's shared memory and TMEM;
   // every global access below waits for that kernel to complete.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // every sequence length in flight at once (one load per thread), then the
+  // prefix sums by warp 0 from shared memory
+  for (int b = tid; b < B; b += kThreads) cum[b + 1] = a.seq_lens[b];
+  __syncthreads();
   if (warp == 0) {
     int carry = 0;
     if (lane == 0) cum[0] = 0;
@@ -1166,7 +1257,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
       const int b = base + lane;
       int n = 0;
       if (b < B) {
-        int64_t Lb = a.seq_lens[b];
+        int64_t Lb = cum[b + 1];
         if (Lb < 0 || Lb > cap) {
           if (blockIdx.x == 0) set_err(a.c.err, NVKV_DEVERR_SEQLEN);
           Lb = Lb < 0 ? 0 : cap;
@@ -1364,7 +1455,9 @@ void launch_decode(const DecodeArgs &a, cudaStream_t s) {
 
 nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t *block_table, int32_t max_pages,
                           const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, int32_t prec, float sm_scale,
-                          int32_t num_splits, void *workspace, size_t workspace_bytes, void *out, void *stream) {
+                          int32_t num_splits, void *workspace, size_t workspace_bytes, void *out, void *stream,
+                          const void *k_new = nullptr, const void *v_new = nullptr,
+                          nvkv_dtype new_dtype = NVKV_DTYPE_F32) {
   nvkv_status st = check_cache(cache, prec);
   if (st != NVKV_OK) return st;
   if (batch < 0 || num_q_heads <= 0 || max_pages <= 0 || num_splits < 0) return NVKV_ERR_INVALID_ARG;
@@ -1400,6 +1493,9 @@ nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t 
   a.counters = static_cast<uint32_t *>(workspace);
   a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + counter_bytes(batch, Hkv));
   a.out = static_cast<__nv_bfloat16 *>(out);
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.new_dtype = new_dtype;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (prec == NVKV_PREC_NVFP4) {
     if (G <= 4) launch_decode<NVKV_PREC_NVFP4, 4>(a, s);
@@ -1453,6 +1549,7 @@ nvkv_status nvfp4_paged_decode_attention_noalloc(const void *q, const nvkv_cache
                                                  const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
                                                  int32_t layer_precision, float sm_scale, int32_t num_splits,
                                                  void *out, void *stream) {
+  NVKV_ABI_RANGE();
   if (!cache || layer_precision != cache->prec) return NVKV_ERR_INVALID_ARG;
   if (layer_precision != NVKV_PREC_NVFP4 && layer_precision != NVKV_PREC_FP8_E4M3) return NVKV_ERR_INVALID_ARG;
   nvkv_status st = check_cache(cache, layer_precision);
@@ -1495,6 +1592,7 @@ size_t nvkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t nu
 }
 
 nvkv_status nvkv_decode_workspace_init(void *workspace, size_t bytes, void *stream) {
+  NVKV_ABI_RANGE();
   if (!workspace && bytes) return NVKV_ERR_INVALID_ARG;
   if (bytes == 0) return NVKV_OK;
   return cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess ? NVKV_OK
@@ -1506,16 +1604,33 @@ nvkv_status nvfp4_paged_decode_attention(const void *q, const nvkv_cache *cache,
                                          int32_t num_q_heads, int32_t layer_precision, float sm_scale,
                                          int32_t num_splits, void *workspace, size_t workspace_bytes, void *out,
                                          void *stream) {
+  NVKV_ABI_RANGE();
   if (!cache || layer_precision != cache->prec) return NVKV_ERR_INVALID_ARG;
   if (layer_precision != NVKV_PREC_NVFP4 && layer_precision != NVKV_PREC_FP8_E4M3) return NVKV_ERR_INVALID_ARG;
   return decode_common(q, cache, block_table, max_pages, seq_lens, batch, num_q_heads, layer_precision, sm_scale,
                        num_splits, workspace, workspace_bytes, out, stream);
 }
 
+nvkv_status nvfp4_paged_decode_step(const void *q, const void *k_new, const void *v_new, nvkv_dtype dtype,
+                                    const nvkv_cache *cache, const int32_t *block_table, int32_t max_pages,
+                                    const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                    int32_t layer_precision, float sm_scale, int32_t num_splits, void *workspace,
+                                    size_t workspace_bytes, void *out, void *stream) {
+  NVKV_ABI_RANGE();
+  if (!cache || layer_precision != cache->prec) return NVKV_ERR_INVALID_ARG;
+  if (layer_precision != NVKV_PREC_NVFP4 && layer_precision != NVKV_PREC_FP8_E4M3) return NVKV_ERR_INVALID_ARG;
+  if (dtype != NVKV_DTYPE_F32 && dtype != NVKV_DTYPE_BF16) return NVKV_ERR_INVALID_ARG;
+  if (batch > 0 && (!k_new || !v_new)) return NVKV_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new)) return NVKV_ERR_UNSUPPORTED;
+  return decode_common(q, cache, block_table, max_pages, seq_lens, batch, num_q_heads, layer_precision, sm_scale,
+                       num_splits, workspace, workspace_bytes, out, stream, k_new, v_new, dtype);
+}
+
 nvkv_status fp8_paged_decode_attention(const void *q, const nvkv_cache *cache, const int32_t *block_table,
                                        int32_t max_pages, const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
                                        float sm_scale, int32_t num_splits, void *workspace, size_t workspace_bytes,
                                        void *out, void *stream) {
+  NVKV_ABI_RANGE();
   return decode_common(q, cache, block_table, max_pages, seq_lens, batch, num_q_heads, NVKV_PREC_FP8_E4M3, sm_scale,
                        num_splits, workspace, workspace_bytes, out, stream);
 }

@@ -598,6 +598,7 @@ nvkv_status fp8_workspace_append_chunk(const void *k, const void *v, nvkv_dtype 
                                        const int64_t *rows, int32_t num_kv_heads, int32_t head_dim,
                                        const float *ws_scale, uint8_t *ws_k, uint8_t *ws_v, int64_t ws_rows,
                                        int32_t *err_flag, void *stream) {
+  NVKV_ABI_RANGE();
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || ws_rows < 0) return NVKV_ERR_INVALID_ARG;
   if (dtype != NVKV_DTYPE_F32 && dtype != NVKV_DTYPE_BF16) return NVKV_ERR_INVALID_ARG;
   if (head_dim % 16 != 0) return NVKV_ERR_UNSUPPORTED;
@@ -632,6 +633,7 @@ nvkv_status fp8_chunked_extend_attention(const void *q, const int64_t *cu_q, int
                                          int32_t head_dim, int64_t ws_rows, const float *ws_scale, float sm_scale,
                                          void *scratch, size_t scratch_bytes, void *out, int32_t *err_flag,
                                          void *stream) {
+  NVKV_ABI_RANGE();
   if (n < 0 || max_q_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || ws_rows < 0) return NVKV_ERR_INVALID_ARG;
   if (num_q_heads % num_kv_heads != 0) return NVKV_ERR_INVALID_ARG;
   if (head_dim != kXD) return NVKV_ERR_UNSUPPORTED;

@@ -3,11 +3,23 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "../../include/nvfp4kv.h"
 
 namespace nvkv {
+
+// NVTX range around one C-ABI call that launches device work, named after the
+// call, so a profiler's timeline and kernel filters can attribute launches to
+// it.  With no tool attached the push and pop return at once.
+struct AbiRange {
+  explicit AbiRange(const char *name) { nvtxRangePushA(name); }
+  ~AbiRange() { nvtxRangePop(); }
+  AbiRange(const AbiRange &) = delete;
+  AbiRange &operator=(const AbiRange &) = delete;
+};
+#define NVKV_ABI_RANGE() ::nvkv::AbiRange nvkv_abi_range_(__func__)
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -454,6 +454,7 @@ const char *nvkv_status_string(nvkv_status s) {
 
 nvkv_status nvkv_global_scale(const void *x, nvkv_dtype dtype, int64_t n, float divisor, float *out,
                               void *stream) {
+  NVKV_ABI_RANGE();
   if (!out || n < 0 || (n > 0 && !x) || !(divisor > 0.0f)) return NVKV_ERR_INVALID_ARG;
   if (dtype != NVKV_DTYPE_F32 && dtype != NVKV_DTYPE_BF16) return NVKV_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -467,6 +468,7 @@ nvkv_status nvkv_global_scale(const void *x, nvkv_dtype dtype, int64_t n, float 
 }
 
 nvkv_status nvkv_amax_update(const void *x, nvkv_dtype dtype, int64_t n, float *amax, void *stream) {
+  NVKV_ABI_RANGE();
   if (!amax || n < 0 || (n > 0 && !x)) return NVKV_ERR_INVALID_ARG;
   if (dtype != NVKV_DTYPE_F32 && dtype != NVKV_DTYPE_BF16) return NVKV_ERR_INVALID_ARG;
   if (n == 0) return NVKV_OK;
@@ -476,18 +478,21 @@ nvkv_status nvkv_amax_update(const void *x, nvkv_dtype dtype, int64_t n, float *
 nvkv_status nvfp4_kv_quantize_write(const void *k, const void *v, nvkv_dtype dtype, int64_t num_tokens,
                                     const int64_t *slot_mapping, const float *global_scale,
                                     const nvkv_cache *cache, void *stream) {
+  NVKV_ABI_RANGE();
   return write_common(k, v, dtype, num_tokens, slot_mapping, global_scale, cache, stream, NVKV_PREC_NVFP4);
 }
 
 nvkv_status fp8_kv_quantize_write(const void *k, const void *v, nvkv_dtype dtype, int64_t num_tokens,
                                   const int64_t *slot_mapping, const float *global_scale, const nvkv_cache *cache,
                                   void *stream) {
+  NVKV_ABI_RANGE();
   return write_common(k, v, dtype, num_tokens, slot_mapping, global_scale, cache, stream, NVKV_PREC_FP8_E4M3);
 }
 
 nvkv_status nvfp4_kv_requantize_write_fp8(const uint8_t *k8, const uint8_t *v8, const float *in_scale,
                                           int64_t num_tokens, const int64_t *slot_mapping, const float *global_scale,
                                           const nvkv_cache *cache, void *stream) {
+  NVKV_ABI_RANGE();
   nvkv_status st = check_cache(cache, NVKV_PREC_NVFP4);
   if (st != NVKV_OK) return st;
   if (num_tokens < 0) return NVKV_ERR_INVALID_ARG;
@@ -503,6 +508,7 @@ nvkv_status nvfp4_kv_requantize_write_fp8(const uint8_t *k8, const uint8_t *v8, 
 }
 
 nvkv_status nvkv_encode_e2m1(const float *x, int64_t n, uint8_t *out, void *stream) {
+  NVKV_ABI_RANGE();
   if (n < 0 || (n > 0 && (!x || !out))) return NVKV_ERR_INVALID_ARG;
   if (n == 0) return NVKV_OK;
   const int64_t b = (n + 255) / 256;
@@ -512,6 +518,7 @@ nvkv_status nvkv_encode_e2m1(const float *x, int64_t n, uint8_t *out, void *stre
 }
 
 nvkv_status nvkv_encode_e4m3(const float *x, int64_t n, uint8_t *out, void *stream) {
+  NVKV_ABI_RANGE();
   if (n < 0 || (n > 0 && (!x || !out))) return NVKV_ERR_INVALID_ARG;
   if (n == 0) return NVKV_OK;
   const int64_t b = (n + 255) / 256;
@@ -525,6 +532,7 @@ nvkv_status nvfp4_kv_dequant_to_fp8_workspace(const int32_t *block_table, int32_
                                               const int64_t *cu_prefix, int32_t n, const nvkv_cache *cache,
                                               const float *ws_scale, uint8_t *ws_k, uint8_t *ws_v,
                                               int64_t ws_rows, void *stream) {
+  NVKV_ABI_RANGE();
   nvkv_status st = check_cache(cache, NVKV_PREC_NVFP4);
   if (st != NVKV_OK) return st;
   if (n < 0 || ws_rows < 0 || max_pages <= 0) return NVKV_ERR_INVALID_ARG;

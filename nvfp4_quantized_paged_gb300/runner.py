@@ -6,7 +6,9 @@ write, decode attention, workspace dequant), and exposes ``step()``: the work
 of one serving step for that layer, i.e. the quantized write of the step's new
 tokens, the paged decode attention over the batch and, for workloads with a
 chunked-extend pass, the prefix dequant into the shared FP8 workspace plus the
-write of the new chunk.  PyTorch only allocates memory and orders streams.
+write of the new chunk.  With one new token per sequence the write and the
+attention run as one launch (nvfp4_paged_decode_step).  PyTorch only
+allocates memory and orders streams.
 """
 from __future__ import annotations
 
@@ -17,7 +19,7 @@ import torch
 
 from . import (Cache, FP8_GLOBAL_DIVISOR, NVFP4_GLOBAL_DIVISOR, PREC_FP8, PREC_NVFP4, alloc_decode_workspace,
                fp8_kv_quantize_write, nvfp4_kv_dequant_to_fp8_workspace, nvfp4_kv_quantize_write,
-               nvfp4_paged_decode_attention, nvkv_amax_update, nvkv_global_scale)
+               nvfp4_paged_decode_attention, nvfp4_paged_decode_step, nvkv_amax_update, nvkv_global_scale)
 from .workloads import Workload
 
 
@@ -25,11 +27,13 @@ class Layer:
     """One layer of a workload: cache, scales and step inputs on the device.
 
     ``prec`` overrides the workload's precision map (the FP8 comparator runs
-    the same workload with every layer in FP8).
+    the same workload with every layer in FP8).  ``fused`` chooses the
+    one-launch decode step where the workload writes one new token per
+    sequence (default) or the separate write and decode calls.
     """
 
     def __init__(self, wl: Workload, layer: int, device="cuda", prec: Optional[int] = None,
-                 num_splits: Optional[int] = None):
+                 num_splits: Optional[int] = None, fused: Optional[bool] = None):
         s = wl.spec
         self.wl, self.layer, self.device = wl, layer, torch.device(device)
         self.prec = prec if prec is not None else (PREC_FP8 if wl.is_fp8(layer) else PREC_NVFP4)
@@ -62,6 +66,15 @@ class Layer:
                 vs.append(wl.kv(layer, 1, b, L - s.step_write, L))
             self.k_new, self.v_new = torch.cat(ks).contiguous(), torch.cat(vs).contiguous()
             self.slots_new = torch.from_numpy(wl.step_slots()).to(self.device)
+        # the one-launch step's inputs: row b = the newest token of sequence b
+        self.k_step = self.v_step = None
+        if s.step_write == 1 and wl.step_seqs():
+            self.k_step = torch.zeros(s.B, s.Hkv, s.D, dtype=torch.float32, device=self.device)
+            self.v_step = torch.zeros_like(self.k_step)
+            rows = torch.tensor(wl.step_seqs(), dtype=torch.int64, device=self.device)
+            self.k_step[rows] = self.k_new
+            self.v_step[rows] = self.v_new
+        self.fused = (self.k_step is not None) if fused is None else (fused and self.k_step is not None)
         self.ext = None
         if s.extend_seqs and self.prec == PREC_NVFP4:
             ids = [b for b in s.extend_seqs if b < s.B]
@@ -106,11 +119,34 @@ class Layer:
         self.write(e["k"], e["v"], e["slots"])
 
     def step(self):
-        if self.k_new is not None:
-            self.write(self.k_new, self.v_new, self.slots_new)
-        self.decode()
+        if self.fused:
+            nvfp4_paged_decode_step(self.q, self.k_step, self.v_step, self.cache, self.block_table, self.seq_lens,
+                                    self.prec, self.out, self.workspace, num_splits=self.num_splits)
+        else:
+            if self.k_new is not None:
+                self.write(self.k_new, self.v_new, self.slots_new)
+            self.decode()
         if self.ext is not None:
             self.extend()
+
+    def step_inputs(self) -> List[torch.Tensor]:
+        """The tensors a step reads that come from the host each step: the
+        queries and the new tokens (with their slots for the separate write)."""
+        if self.fused:
+            return [self.q, self.k_step, self.v_step]
+        return [self.q] + ([self.k_new, self.v_new, self.slots_new] if self.k_new is not None else [])
+
+    def set_step_inputs(self, ts: List[torch.Tensor]):
+        """Rebind the step inputs (same order as step_inputs) to other tensors."""
+        self.q = ts[0]
+        if self.fused:
+            self.k_step, self.v_step = ts[1], ts[2]
+        elif self.k_new is not None:
+            self.k_new, self.v_new, self.slots_new = ts[1], ts[2], ts[3]
+
+    def launches_per_step(self) -> int:
+        n = 1 if self.fused else (1 if self.k_new is not None else 0) + 1
+        return n + (2 if self.ext is not None else 0)
 
     # ------------------------------------------------------------ bookkeeping
     def kv_bytes_read(self) -> int:
