@@ -309,9 +309,14 @@ __device__ void append_token(const DecodeArgs &a, int b, int h, int64_t page, in
         den = __fmul_rn(f32_from_e4m3(sbyte), g);
       }
       uint32_t codes = 0;  // values 4q .. 4q+3, one nibble each from bit 0
-      if (den != 0.0f)
-        codes = e2m1x2_from_f32(__fdiv_rn(x[0], den), __fdiv_rn(x[1], den)) |
-                (e2m1x2_from_f32(__fdiv_rn(x[2], den), __fdiv_rn(x[3], den)) << 8);
+      if (den != 0.0f) {
+        const float r = __frcp_rn(den);
+        if (quot_fast_ok(r))  // codes of fl(x / den) from one reciprocal (exact, see e2m1x2_quot)
+          codes = e2m1x2_quot(x[0], x[1], den, r) | (e2m1x2_quot(x[2], x[3], den, r) << 8);
+        else
+          codes = e2m1x2_from_f32(__fdiv_rn(x[0], den), __fdiv_rn(x[1], den)) |
+                  (e2m1x2_from_f32(__fdiv_rn(x[2], den), __fdiv_rn(x[3], den)) << 8);
+      }
       if (kind == 0) {
         *reinterpret_cast<uint16_t *>(c.data + c.nv_kcodes(page, h, off, blk) + 2 * q) = static_cast<uint16_t>(codes);
       } else {  // value 16 blk + j: byte j of the pair's 16 bytes, nibble off % 2
@@ -324,9 +329,14 @@ __device__ void append_token(const DecodeArgs &a, int b, int h, int64_t page, in
       if (q == 0) c.data[c.nv_scale(page, h, kind, off, blk)] = static_cast<uint8_t>(sbyte);
     } else {
       uint32_t w = 0;
-      if (g != 0.0f)
-        w = e4m3x2_from_f32(__fdiv_rn(x[0], g), __fdiv_rn(x[1], g)) |
-            (e4m3x2_from_f32(__fdiv_rn(x[2], g), __fdiv_rn(x[3], g)) << 16);
+      if (g != 0.0f) {
+        const float r = __frcp_rn(g);
+        if (quot_fast_ok(fabsf(r)))  // bytes of fl(x / g) from one reciprocal (exact, see e4m3x2_quot)
+          w = e4m3x2_quot(x[0], x[1], g, r) | (e4m3x2_quot(x[2], x[3], g, r) << 16);
+        else
+          w = e4m3x2_from_f32(__fdiv_rn(x[0], g), __fdiv_rn(x[1], g)) |
+              (e4m3x2_from_f32(__fdiv_rn(x[2], g), __fdiv_rn(x[3], g)) << 16);
+      }
       if (kind == 0) {
         *reinterpret_cast<uint32_t *>(c.data + c.f8_kblock(page, h, off, blk) + 4 * q) = w;
       } else {  // value 16 blk + 8 half + j: byte 2 j + off % 2 of chunk `half`
@@ -372,24 +382,30 @@ __device__ void producer(const DecodeArgs &a, uint8_t *ring, uint64_t *full, uin
       int wbase = ((s.t0 + kfirst) * kTile) >> lgP;
       int32_t pg = wbase + lane < a.max_pages ? brow[wbase + lane] : 0;
       int32_t pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
+      // The step's new token (position len - 1) lies in the pair's last tile:
+      // if this group copies that tile, the warp writes the token while it
+      // would otherwise wait for a free stage, at the latest just before the
+      // tile's own copy (never before the ring's first fills go out).
+      bool pend = a.k_new != nullptr && s.t1 == cum[s.b + 1] - cum[s.b] && (ntiles - 1 - kfirst) % kGroups == 0;
       for (int k = kfirst; k < ntiles; k += kGroups) {
         const int slot = grp * C::kStagesG + slot_l;
-        if (lane == 0 && fill > 0) mbar_wait_bounded(&empty[slot], (fill - 1) & 1u, abort);
-        if (__any_sync(0xffffffffu, *abort)) return;  // warp-uniform exit
         const int tok0 = (s.t0 + k) * kTile;
         const int ntok = min(kTile, len - tok0);
+        if (pend && (fill > 0 || tok0 + ntok == len)) {
+          const int pos = len - 1;
+          const int32_t pw = __ldg(brow + (pos >> lgP));
+          if (pw >= 0 && pw < a.c.num_pages) append_token<PREC>(a, s.b, s.h, pw, pos & (P - 1));
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // the written bytes, before the copy reads them
+          __syncwarp();
+          pend = false;
+        }
+        if (lane == 0 && fill > 0) mbar_wait_bounded(&empty[slot], (fill - 1) & 1u, abort);
+        if (__any_sync(0xffffffffu, *abort)) return;  // warp-uniform exit
         const int nblk = (ntok + P - 1) >> lgP;  // page blocks holding the tile's tokens
         while (((tok0 + ntok - 1) >> lgP) >= wbase + 32) {  // the tile leaves the window (warp-uniform)
           wbase += 32;
           pg = pg_next;
           pg_next = wbase + 32 + lane < a.max_pages ? brow[wbase + 32 + lane] : 0;
-        }
-        if (a.k_new != nullptr && tok0 + ntok == len) {  // the pair's last tile holds the step's new token
-          const int pos = len - 1;
-          const int pw = __shfl_sync(0xffffffffu, pg, ((pos >> lgP) - wbase) & 31);
-          if (pw >= 0 && pw < a.c.num_pages) append_token<PREC>(a, s.b, s.h, pw, pos & (P - 1));
-          asm volatile("fence.proxy.async.global;" ::: "memory");  // the written bytes, before the copy reads them
-          __syncwarp();
         }
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nblk) * block_bytes);
         const int page = __shfl_sync(0xffffffffu, pg, ((tok0 >> lgP) + lane - wbase) & 31);

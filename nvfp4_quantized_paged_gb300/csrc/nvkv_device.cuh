@@ -75,6 +75,25 @@ __device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t w) {
 }
 
 // Exact FP32 value of an E4M3 byte (never NaN for bytes this library writes).
+// Exact codes of correctly rounded quotients without a division per value.
+// The write rule takes code = RNE(fl(x / den)) (E2M1 or E4M3, saturating).
+// With r = fl(1 / den) and q = fl(x r): q = (x / den)(1 + d1)(1 + d2) and
+// fl(x / den) = (x / den)(1 + d3), |di| <= 2^-24, so fl(x / den) lies within
+// 3 2^-24 |q| of q.  The bracket ends fl(q (1 - 2^-21)) and fl(q (1 + 2^-21))
+// (2^-21 = 8 2^-24, each end rounded once more) lie outside that interval on
+// either side, and rounding to the code grid is monotone in the magnitude, so
+// when both ends give the same code it is the code of fl(x / den).  When a
+// rounding boundary falls inside the bracket (a fraction of about 2^-20 of
+// the values) the quotient is taken exactly.  Requires r normal and finite
+// (den neither tiny nor huge); callers divide otherwise.  Quotients below the
+// normal range give code 0 at both ends whatever their rounding error.
+constexpr float kBracketLo = 1.0f - 0x1p-21f, kBracketHi = 1.0f + 0x1p-21f;
+
+__device__ __forceinline__ bool quot_fast_ok(float r) { return r >= 0x1p-126f && r <= 0x1p127f; }
+
+__device__ __forceinline__ uint32_t e2m1x2_quot(float x0, float x1, float den, float r);
+__device__ __forceinline__ uint32_t e4m3x2_quot(float x0, float x1, float den, float r);
+
 __device__ __forceinline__ float f32_from_e4m3(uint32_t b) {
   const uint32_t h2 = f16x2_from_e4m3x2<0>(b & 0xFFu);
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
@@ -437,6 +456,24 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&x)[16]) 
       "r"(__float_as_uint(x[8])), "r"(__float_as_uint(x[9])), "r"(__float_as_uint(x[10])), "r"(__float_as_uint(x[11])),
       "r"(__float_as_uint(x[12])), "r"(__float_as_uint(x[13])), "r"(__float_as_uint(x[14])), "r"(__float_as_uint(x[15]))
       : "memory");
+}
+
+// E2M1 codes of fl(x0 / den) (low nibble) and fl(x1 / den), r = fl(1 / den).
+__device__ __forceinline__ uint32_t e2m1x2_quot(float x0, float x1, float den, float r) {
+  const float q0 = __fmul_rn(x0, r), q1 = __fmul_rn(x1, r);
+  const uint32_t lo = e2m1x2_from_f32(__fmul_rn(q0, kBracketLo), __fmul_rn(q1, kBracketLo));
+  const uint32_t hi = e2m1x2_from_f32(__fmul_rn(q0, kBracketHi), __fmul_rn(q1, kBracketHi));
+  if (lo == hi) return lo;
+  return e2m1x2_from_f32(__fdiv_rn(x0, den), __fdiv_rn(x1, den));
+}
+
+// E4M3 bytes of fl(x0 / den) (low byte) and fl(x1 / den), r = fl(1 / den).
+__device__ __forceinline__ uint32_t e4m3x2_quot(float x0, float x1, float den, float r) {
+  const float q0 = __fmul_rn(x0, r), q1 = __fmul_rn(x1, r);
+  const uint32_t lo = e4m3x2_from_f32(__fmul_rn(q0, kBracketLo), __fmul_rn(q1, kBracketLo));
+  const uint32_t hi = e4m3x2_from_f32(__fmul_rn(q0, kBracketHi), __fmul_rn(q1, kBracketHi));
+  if (lo == hi) return lo;
+  return e4m3x2_from_f32(__fdiv_rn(x0, den), __fdiv_rn(x1, den));
 }
 
 }  // namespace nvkv

@@ -123,10 +123,19 @@ __device__ __forceinline__ void quant16(const float (&x)[16], float g, uint32_t 
   }
   lo = hi = 0;
   if (den != 0.0f) {
+    const float r = __frcp_rn(den);
+    if (quot_fast_ok(r)) {  // codes of fl(x / den) from one reciprocal (exact, see e2m1x2_quot)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      lo |= e2m1x2_from_f32(__fdiv_rn(x[2 * j], den), __fdiv_rn(x[2 * j + 1], den)) << (8 * j);
-      hi |= e2m1x2_from_f32(__fdiv_rn(x[8 + 2 * j], den), __fdiv_rn(x[8 + 2 * j + 1], den)) << (8 * j);
+      for (int j = 0; j < 4; ++j) {
+        lo |= e2m1x2_quot(x[2 * j], x[2 * j + 1], den, r) << (8 * j);
+        hi |= e2m1x2_quot(x[8 + 2 * j], x[8 + 2 * j + 1], den, r) << (8 * j);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        lo |= e2m1x2_from_f32(__fdiv_rn(x[2 * j], den), __fdiv_rn(x[2 * j + 1], den)) << (8 * j);
+        hi |= e2m1x2_from_f32(__fdiv_rn(x[8 + 2 * j], den), __fdiv_rn(x[8 + 2 * j + 1], den)) << (8 * j);
+      }
     }
   }
 }
@@ -249,10 +258,15 @@ __global__ void __launch_bounds__(256)
   const float s8 = gs[kind];
   uint32_t w[4] = {0, 0, 0, 0};
   if (s8 != 0.0f) {
+    const float r = __frcp_rn(s8);
+    const bool fast = quot_fast_ok(fabsf(r));  // bytes of fl(x / s8) from one reciprocal (exact)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      w[j] = e4m3x2_from_f32(__fdiv_rn(x[4 * j], s8), __fdiv_rn(x[4 * j + 1], s8)) |
-             (e4m3x2_from_f32(__fdiv_rn(x[4 * j + 2], s8), __fdiv_rn(x[4 * j + 3], s8)) << 16);
+      if (fast)
+        w[j] = e4m3x2_quot(x[4 * j], x[4 * j + 1], s8, r) | (e4m3x2_quot(x[4 * j + 2], x[4 * j + 3], s8, r) << 16);
+      else
+        w[j] = e4m3x2_from_f32(__fdiv_rn(x[4 * j], s8), __fdiv_rn(x[4 * j + 1], s8)) |
+               (e4m3x2_from_f32(__fdiv_rn(x[4 * j + 2], s8), __fdiv_rn(x[4 * j + 3], s8)) << 16);
     }
   }
   if (kind == 0) {

@@ -98,3 +98,57 @@ def test_quantizer_division_at_every_e2m1_rounding_boundary(orc):
         oc = orc.Cache(orc.PREC_NVFP4, npages, Hkv, P, D, gs)
         orc.quantize_write(oc, k, k, slots)
         assert np.array_equal(cache.data.cpu().numpy(), oc.data), g
+
+
+E4M3_SCALES = np.array([2.0 ** e * (1 + m / 8) for e in range(-6, 9) for m in range(8)] +
+                       [2.0 ** -6 * m / 8 for m in range(1, 8)], np.float64)
+E4M3_SCALES = E4M3_SCALES[E4M3_SCALES <= 448.0]
+E2M1_POINTS = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _near_boundary_blocks(rng, g, n_blocks):
+    """Blocks whose element 0 fixes an E4M3-representable scale s (so den =
+    fl(s g)) and whose other elements sit a few ulps around den * t for E2M1
+    rounding boundaries and grid points t, plus plain random values."""
+    blks = np.zeros((n_blocks, 16), np.float32)
+    for i in range(n_blocks):
+        s = np.float32(rng.choice(E4M3_SCALES))
+        blks[i, 0] = np.float32(6.0) * g * s if rng.random() < 0.5 else -(np.float32(6.0) * g * s)
+        den = np.float32(s * np.float32(g))
+        for j in range(1, 16):
+            if rng.random() < 0.8:
+                v = np.float32(den * np.float32(rng.choice(E2M1_POINTS)))
+                for _ in range(int(rng.integers(0, 3))):
+                    v = np.nextafter(v, np.float32(np.inf) if rng.random() < 0.5 else np.float32(0), dtype=np.float32)
+            else:
+                v = np.float32(rng.normal() * 6.0 * float(den))
+            blks[i, j] = -v if rng.random() < 0.5 else v
+    return blks
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_quantizer_random_scales_near_boundaries(orc, seed):
+    """Random global scales over 60 decades and values placed on and a few ulps
+    around every E2M1 rounding boundary of random E4M3 block scales: the NVFP4
+    and FP8 writes must give the oracle's bytes (one exact division per value
+    there).  Covers the reciprocal-bracket code selection and its fallback."""
+    import nvfp4_quantized_paged_gb300 as nv
+    rng = np.random.default_rng(seed)
+    Hkv, D, P = 2, 128, 16
+    for g in [np.float32(10.0 ** rng.uniform(-30, 30)) for _ in range(6)] + [np.float32(1.0)]:
+        n_rows = 24
+        blks = _near_boundary_blocks(rng, g, n_rows * Hkv * (D // 16))
+        k = blks.reshape(n_rows, Hkv, D)
+        v = np.ascontiguousarray(k[::-1])
+        slots = rng.permutation(n_rows * 2)[:n_rows].astype(np.int64)
+        npages = (2 * n_rows + P - 1) // P
+        for prec, gs in ((nv.PREC_NVFP4, np.array([g, g], np.float32)),
+                         (nv.PREC_FP8, np.array([g * 7, g * 7], np.float32))):
+            cache = nv.Cache(prec, npages, Hkv, P, device="cuda")
+            write = nv.nvfp4_kv_quantize_write if prec == nv.PREC_NVFP4 else nv.fp8_kv_quantize_write
+            write(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), torch.from_numpy(slots).cuda(),
+                  torch.from_numpy(gs).cuda(), cache)
+            torch.cuda.synchronize()
+            oc = orc.Cache(orc.PREC_NVFP4 if prec == nv.PREC_NVFP4 else orc.PREC_FP8, npages, Hkv, P, D, gs)
+            orc.quantize_write(oc, k, v, slots)
+            assert np.array_equal(cache.data.cpu().numpy(), oc.data), (prec, float(g))
