@@ -197,10 +197,12 @@ def step_bytes(lay) -> dict:
         n = lay.k_new.shape[0] * s.Hkv
         w += n * (2 * 128 * 4 + per_tok_write)
     if lay.ext is not None:
-        rows = lay.ext["ws_k"].shape[0] * s.Hkv
+        rows = int(lay.ext["prefix_lens"].sum().item()) * s.Hkv
         w += rows * (144 + 256)                                    # workspace dequant: read NVFP4, write FP8
         n = lay.ext["k"].shape[0] * s.Hkv
         w += n * (2 * 128 * 4 + per_tok_write)
+        if "q" in lay.ext:  # chunk append (FP32 in, E4M3 out); the attention's work is FLOPs, not counted here
+            w += n * (2 * 128 * 4 + 256)
     return dict(kv=kv, qo=qo, write=w, total=kv + qo + w)
 
 
@@ -213,26 +215,28 @@ TARGET_FRAC_OF_8TBPS = 0.75
 TARGET_FP8_SPEEDUP = 1.5
 
 
-def workload_config(spec, ws=1, l2=None):
+def workload_config(spec, ws=1, extend_attention=False):
     """The `config` dict of a decode workload (both arms print the same one)."""
     return {
         "workload": spec.name, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv, "D": spec.D,
         "L": spec.L or "ragged (lognormal)", "page": spec.P, "layers": spec.layers,
         "fp8_layers": list(spec.fp8_layers), "step_write_tokens_per_seq": spec.step_write,
-        "extend": {"seqs": list(spec.extend_seqs), "tokens": spec.extend_tokens} if spec.extend_seqs else None,
+        "extend": {"seqs": list(spec.extend_seqs), "tokens": spec.extend_tokens,
+                   "attention": bool(extend_attention)} if spec.extend_seqs else None,
         "l2": "inputs rotate over cache replicas totalling >= 3x L2 (or one set larger than that)",
         "parallelism": f"replicas x{ws}",
         "launch": "one CUDA graph of the K timed steps",
     }
 
 
-def _build_sets(wl, layers, dev, l2, prec=None):
+def _build_sets(wl, layers, dev, l2, prec=None, extend_attention=False):
     """Cache replicas of the workload's layers whose total exceeds 3x L2."""
     from nvfp4_quantized_paged_gb300.runner import Layer
-    first = [Layer(wl, l, dev, prec=prec) for l in layers]
+    mk = lambda l: Layer(wl, l, dev, prec=prec, extend_attention=extend_attention)
+    first = [mk(l) for l in layers]
     per = sum(step_bytes(x)["kv"] for x in first)
     reps = max(1, -(-3 * l2 // max(per, 1)))
-    return [first] + [[Layer(wl, l, dev, prec=prec) for l in layers] for _ in range(reps - 1)]
+    return [first] + [[mk(l) for l in layers] for _ in range(reps - 1)]
 
 
 def _decode_graph(sets, steps, keep):
@@ -254,7 +258,7 @@ def measure_workload(name, args, dev, dist, stream, full=True):
     wl = Workload(spec, seed=0, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     layers = list(range(spec.layers)) if not args.layers else [int(x) for x in args.layers.split(",")]
-    sets = _build_sets(wl, layers, dev, l2)
+    sets = _build_sets(wl, layers, dev, l2, extend_attention=args.extend_attention)
     bytes_step = sum(step_bytes(x)["total"] for x in sets[0])
     nv_layers = [x for x in sets[0] if x.prec == nv.PREC_NVFP4]
     dec_bytes = sum(x.kv_bytes_read() + x.qo_bytes() for x in nv_layers)  # per round of NVFP4 decodes
@@ -290,7 +294,7 @@ def measure_workload(name, args, dev, dist, stream, full=True):
     del g_step, g_dec
     res = dict(spec=spec, ms=ms, bytes_step=bytes_step, launches_per_step=launches_per_step, clocks=clk.summary(),
                dec_avg_us=dec_avg_ms * 1e3, dec_bytes_per_launch=dec_bytes / max(1, len(nv_layers)),
-               nv_layers=len(nv_layers), l2=l2)
+               nv_layers=len(nv_layers), l2=l2, extend_attention=args.extend_attention)
     res["dec_gbs"] = res["dec_bytes_per_launch"] / (dec_avg_ms * 1e-3) / 1e9
 
     if full:
@@ -370,7 +374,7 @@ def _targets(res):
 def _extra_line(res, peak):
     """The decode roofline and FP8 ratio of an extra workload (same run)."""
     return {
-        "config": workload_config(res["spec"]),
+        "config": workload_config(res["spec"], 1, res["extend_attention"]),
         "ms_per_step": round(res["ms"], 5),
         "step_gbs": round(res["bytes_step"] / (res["ms"] * 1e-3) / 1e9, 1),
         "roofline": {"bound": "hbm", "kernel": "decode_kernel<NVFP4>", "achieved": round(res["dec_gbs"], 1),
@@ -418,7 +422,7 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": DTYPE,
             "data": "synthetic (seeded; no dataset or weights)",
-            "config": workload_config(spec, ws),
+            "config": workload_config(spec, ws, args.extend_attention),
             "pct_of_8TBps": round(100.0 * gbs / ws / NOMINAL_HBM_GBS, 2),
             "pct_of_measured_hbm": round(100.0 * gbs / ws / peak, 2),
             "decode_tokens_per_s": round(_sum_over_ranks(dist, spec.B, dev) / (ms * 1e-3), 1),
@@ -956,7 +960,7 @@ def run_reference(args):
             "ms_per_step": round(1e3 * elapsed / args.steps, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64 (oracle attention), f32 (oracle quantizer)",
             "data": "synthetic (seeded)", "impl": "reference",
-            "config": workload_config(spec),
+            "config": workload_config(spec, 1, args.extend_attention),
             "cpu_baseline": dict(cb, value=v),
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -972,6 +976,8 @@ def main():
     ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="headline only: skip the long-context and serving-mix keys")
     ap.add_argument("--layers", default="", help="comma list of layer indices to build (profiling runs)")
+    ap.add_argument("--extend-attention", action="store_true",
+                    help="serving mix: the extend pass also appends the chunk and runs its FP8 attention")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()

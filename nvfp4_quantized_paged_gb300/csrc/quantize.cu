@@ -146,26 +146,21 @@ __device__ __forceinline__ uint32_t spread4(uint32_t four) {
 }
 
 // ---------------------------------------------------------------------------
-// NVFP4 quantized write.  Thread = (token, KV head, 16-block); gridDim.y = K|V.
+// NVFP4 quantized write of one item = (kind K|V, token t, KV head h, 16-block).
 // T = uint8_t: E4M3 input decoded with in_scale[kind] (initial prefill).
+// V: value 16 blk + j goes to byte j of the pair's 16 bytes, nibble off % 2.
+// When the neighbouring token (t ^ 1) holds the partner slot (tokens written
+// in slot order, as prefill and decode do), the even token's item writes both
+// slots' bytes with plain stores and the odd one has nothing to do;
+// otherwise this slot's nibbles are cleared and set with atomics (the partner
+// slot may be written by another thread of the same launch).
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(256)
-    nvfp4_write_kernel(const T *__restrict__ k, const T *__restrict__ v, int64_t num_tokens,
-                       const int64_t *__restrict__ slot_mapping, const float *__restrict__ gs, CacheDev c,
-                       const float *__restrict__ in_scale) {
-  // programmatic dependent of the previous kernel: wait for it before any
-  // global access, then let the next kernel start its set-up
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t items = num_tokens * c.Hkv * kBlocksPerRow;
-  if (gid >= items) return;
-  const int kind = blockIdx.y;
-  const int blk = static_cast<int>(gid % kBlocksPerRow);
-  const int64_t th = gid / kBlocksPerRow;  // token * Hkv + head
-  const int h = static_cast<int>(th % c.Hkv);
-  const int64_t t = th / c.Hkv;
+__device__ void nvfp4_write_item(const T *__restrict__ k, const T *__restrict__ v, int64_t num_tokens,
+                                 const int64_t *__restrict__ slot_mapping, const float *__restrict__ gs,
+                                 const CacheDev &c, const float *__restrict__ in_scale, int kind, int64_t t, int h,
+                                 int blk) {
+  const int64_t th = t * c.Hkv + h;
   const int64_t tp = t ^ 1;
   const int64_t slot = slot_mapping[t];
   const int64_t slot_p = (kind == 1 && tp < num_tokens) ? slot_mapping[tp] : -1;  // loaded together
@@ -176,12 +171,6 @@ __global__ void __launch_bounds__(256)
   }
   const int64_t page = slot / c.P;
   const int off = static_cast<int>(slot % c.P);
-  // V: value 16 blk + j goes to byte j of the pair's 16 bytes, nibble off % 2.
-  // When the neighbouring token (t ^ 1) holds the partner slot (tokens written
-  // in slot order, as prefill and decode do), the even token's thread writes
-  // both slots' bytes with plain stores and the odd one has nothing to do;
-  // otherwise this slot's nibbles are cleared and set with atomics (the
-  // partner slot may be written by another thread of the same launch).
   const bool paired = slot_p == (slot ^ 1);
   if (paired && (t & 1)) return;
   float x[16];
@@ -226,6 +215,93 @@ __global__ void __launch_bounds__(256)
     atomicOr(dst + q, spread << sh);
   }
   c.data[c.nv_scale(page, h, kind, off, blk)] = static_cast<uint8_t>(sbyte);
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 quantized write, one warp per (8 consecutive input tokens, KV head).
+// When the 8 tokens go to the 8 slots of one 8-slot group in order (as a
+// prefill or a chunk fills its pages), the warp builds the group's whole
+// 1152-byte image in shared memory and stores it with 16-byte coalesced
+// stores: lane = (token lane / 4, K blocks 2 (lane % 4), + 1) for K and
+// (slot pair lane / 8, block lane % 8) for V, whose two tokens' codes share
+// bytes.  Any other pattern (decode steps, skipped or scattered slots, a
+// ragged last group) takes the item path above, 4 items per lane.
+// ---------------------------------------------------------------------------
+constexpr int kWriteWarps = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(kWriteWarps * 32)
+    nvfp4_write_kernel(const T *__restrict__ k, const T *__restrict__ v, int64_t num_tokens,
+                       const int64_t *__restrict__ slot_mapping, const float *__restrict__ gs, CacheDev c,
+                       const float *__restrict__ in_scale) {
+  __shared__ __align__(16) uint8_t img[kWriteWarps][kNvGroup];
+  // programmatic dependent of the previous kernel: wait for it before any
+  // global access, then let the next kernel start its set-up
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWriteWarps + warp;
+  const int64_t ngroups = (num_tokens + 7) / 8;
+  if (wid >= ngroups * c.Hkv) return;
+  const int h = static_cast<int>(wid % c.Hkv);
+  const int64_t t0 = (wid / c.Hkv) * 8;
+  const int64_t sl = t0 + (lane & 7) < num_tokens ? slot_mapping[t0 + (lane & 7)] : -1;
+  const int64_t s0 = __shfl_sync(0xffffffffu, sl, 0);
+  const bool whole = __all_sync(0xffffffffu, s0 >= 0 && (s0 & 7) == 0 && sl == s0 + (lane & 7) &&
+                                                 s0 + 7 < static_cast<int64_t>(c.num_pages) * c.P);
+  if (!whole) {
+    for (int it = lane; it < 2 * 8 * kBlocksPerRow; it += 32) {
+      const int kind = it / (8 * kBlocksPerRow), tt = (it / kBlocksPerRow) % 8, blk = it % kBlocksPerRow;
+      if (t0 + tt < num_tokens) nvfp4_write_item<T>(k, v, num_tokens, slot_mapping, gs, c, in_scale, kind, t0 + tt, h, blk);
+    }
+    return;
+  }
+  uint8_t *im = img[warp];
+  {  // K: token tk, blocks 2 (lane % 4) and 2 (lane % 4) + 1
+    const int tk = lane >> 2;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int blk = 2 * (lane & 3) + j;
+      float x[16];
+      const int64_t e = ((t0 + tk) * c.Hkv + h) * kD + 16 * blk;
+      if constexpr (sizeof(T) == 1)
+        load16(k + e, in_scale[0], x);
+      else
+        load16(k + e, x);
+      uint32_t sb, lo, hi;
+      quant16(x, gs[0], sb, lo, hi);
+      *reinterpret_cast<uint2 *>(im + (blk >> 1) * 128 + tk * 16 + (blk & 1) * 8) = make_uint2(lo, hi);
+      im[kNvKScales + tk * 8 + blk] = static_cast<uint8_t>(sb);
+    }
+  }
+  {  // V: slots 2p and 2p + 1, block blk (value 16 blk + j at byte j, slot 2p in the low nibble)
+    const int p = lane >> 3, blk = lane & 7;
+    uint32_t sb[2], lo[2], hi[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float x[16];
+      const int64_t e = ((t0 + 2 * p + u) * c.Hkv + h) * kD + 16 * blk;
+      if constexpr (sizeof(T) == 1)
+        load16(v + e, in_scale[1], x);
+      else
+        load16(v + e, x);
+      quant16(x, gs[1], sb[u], lo[u], hi[u]);
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      w[q] = spread4(((q < 2 ? lo[0] : hi[0]) >> (16 * (q & 1))) & 0xFFFFu) |
+             (spread4(((q < 2 ? lo[1] : hi[1]) >> (16 * (q & 1))) & 0xFFFFu) << 4);
+    *reinterpret_cast<uint4 *>(im + kNvVCodes + blk * 64 + p * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    im[kNvVScales + blk * 8 + 2 * p] = static_cast<uint8_t>(sb[0]);
+    im[kNvVScales + blk * 8 + 2 * p + 1] = static_cast<uint8_t>(sb[1]);
+  }
+  __syncwarp();
+  const int64_t page = s0 / c.P;
+  const int off = static_cast<int>(s0 % c.P);
+  uint4 *dst = reinterpret_cast<uint4 *>(c.data + c.block(page, h, kNvTokBytes) + static_cast<int64_t>(off >> 3) * kNvGroup);
+  const uint4 *src = reinterpret_cast<const uint4 *>(im);
+  for (int i = lane; i < kNvGroup / 16; i += 32) dst[i] = src[i];
 }
 
 // ---------------------------------------------------------------------------
@@ -428,13 +504,15 @@ nvkv_status write_common(const void *k, const void *v, nvkv_dtype dtype, int64_t
   CacheDev c = to_dev(cache);
   const int64_t items = num_tokens * cache->num_kv_heads * kBlocksPerRow;
   dim3 grid(grid_for(items, 256), 2);
+  // NVFP4: one warp per (8 tokens, KV head)
+  const dim3 ngrid(grid_for((num_tokens + 7) / 8 * cache->num_kv_heads, kWriteWarps));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (prec == NVKV_PREC_NVFP4) {
     if (dtype == NVKV_DTYPE_F32)
-      launch_pdl(nvfp4_write_kernel<float>, grid, s, static_cast<const float *>(k), static_cast<const float *>(v),
+      launch_pdl(nvfp4_write_kernel<float>, ngrid, s, static_cast<const float *>(k), static_cast<const float *>(v),
                  num_tokens, slot_mapping, gs, c, static_cast<const float *>(nullptr));
     else
-      launch_pdl(nvfp4_write_kernel<__nv_bfloat16>, grid, s, static_cast<const __nv_bfloat16 *>(k),
+      launch_pdl(nvfp4_write_kernel<__nv_bfloat16>, ngrid, s, static_cast<const __nv_bfloat16 *>(k),
                  static_cast<const __nv_bfloat16 *>(v), num_tokens, slot_mapping, gs, c,
                  static_cast<const float *>(nullptr));
   } else {
@@ -514,8 +592,7 @@ nvkv_status nvfp4_kv_requantize_write_fp8(const uint8_t *k8, const uint8_t *v8, 
   if (!k8 || !v8 || !in_scale || !slot_mapping) return NVKV_ERR_INVALID_ARG;
   if (!aligned16(k8) || !aligned16(v8)) return NVKV_ERR_UNSUPPORTED;
   const float *gs = global_scale ? global_scale : cache->kv_scale;
-  const int64_t items = num_tokens * cache->num_kv_heads * kBlocksPerRow;
-  dim3 grid(grid_for(items, 256), 2);
+  const dim3 grid(grid_for((num_tokens + 7) / 8 * cache->num_kv_heads, kWriteWarps));  // one warp per (8 tokens, KV head)
   launch_pdl(nvfp4_write_kernel<uint8_t>, grid, static_cast<cudaStream_t>(stream), k8, v8, num_tokens, slot_mapping,
              gs, to_dev(cache), in_scale);
   return launch_status();

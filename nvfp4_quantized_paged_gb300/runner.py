@@ -18,7 +18,8 @@ import numpy as np
 import torch
 
 from . import (Cache, FP8_GLOBAL_DIVISOR, NVFP4_GLOBAL_DIVISOR, PREC_FP8, PREC_NVFP4, alloc_decode_workspace,
-               fp8_kv_quantize_write, nvfp4_kv_dequant_to_fp8_workspace, nvfp4_kv_quantize_write,
+               alloc_extend_scratch, fp8_chunked_extend_attention, fp8_kv_quantize_write,
+               fp8_workspace_append_chunk, nvfp4_kv_dequant_to_fp8_workspace, nvfp4_kv_quantize_write,
                nvfp4_paged_decode_attention, nvfp4_paged_decode_step, nvkv_amax_update, nvkv_global_scale)
 from .workloads import Workload
 
@@ -30,10 +31,14 @@ class Layer:
     the same workload with every layer in FP8).  ``fused`` chooses the
     one-launch decode step where the workload writes one new token per
     sequence (default) or the separate write and decode calls.
+    ``extend_attention`` adds, to a workload's chunked-extend pass, the chunk's
+    append to the FP8 workspace and the FP8 attention of its queries over
+    [prefix || chunk] (the workspace then reserves each chunk's rows behind its
+    prefix, every sequence starting on a multiple of 8 rows).
     """
 
     def __init__(self, wl: Workload, layer: int, device="cuda", prec: Optional[int] = None,
-                 num_splits: Optional[int] = None, fused: Optional[bool] = None):
+                 num_splits: Optional[int] = None, fused: Optional[bool] = None, extend_attention: bool = False):
         s = wl.spec
         self.wl, self.layer, self.device = wl, layer, torch.device(device)
         self.prec = prec if prec is not None else (PREC_FP8 if wl.is_fp8(layer) else PREC_NVFP4)
@@ -79,9 +84,13 @@ class Layer:
         if s.extend_seqs and self.prec == PREC_NVFP4:
             ids = [b for b in s.extend_seqs if b < s.B]
             pref = [int(wl.seq_lens[b]) for b in ids]
-            cu = np.zeros(len(ids) + 1, np.int64)
-            cu[1:] = np.cumsum(pref)
             n_ext = s.extend_tokens
+            cu = np.zeros(len(ids) + 1, np.int64)
+            if extend_attention:  # [prefix || chunk] per sequence, starts on multiples of 8 rows
+                for i, p in enumerate(pref):
+                    cu[i + 1] = cu[i] + (p + n_ext + 7) // 8 * 8
+            else:  # the prefixes back to back
+                cu[1:] = np.cumsum(pref)
             ws_scale = torch.zeros(2, dtype=torch.float32, device=self.device)
             for kind in (0, 1):  # FP8 per-tensor convention: amax / 448
                 nvkv_global_scale(self.amax[kind:kind + 1], ws_scale[kind:kind + 1], FP8_GLOBAL_DIVISOR)
@@ -97,6 +106,20 @@ class Layer:
                 slots=torch.from_numpy(np.concatenate([wl.slots(b, pref[i], pref[i] + n_ext)
                                                        for i, b in enumerate(ids)])).to(self.device),
             )
+            if extend_attention:
+                e = self.ext
+                nq = len(ids) * n_ext
+                e.update(
+                    rows=torch.from_numpy(np.concatenate([cu[i] + pref[i] + np.arange(n_ext) for i in range(len(ids))])
+                                          .astype(np.int64)).to(self.device),
+                    q=wl.ext_q_bf16(layer, nq),
+                    cu_q=torch.arange(0, nq + 1, max(n_ext, 1), dtype=torch.int64, device=self.device)[:len(ids) + 1],
+                    cu_kv=torch.from_numpy(cu[:-1].copy()).to(self.device),
+                    kv_lens=torch.tensor([p + n_ext for p in pref], dtype=torch.int32, device=self.device),
+                    max_q=n_ext,
+                    out=torch.empty(nq, s.Hq, s.D, dtype=torch.bfloat16, device=self.device),
+                    scratch=alloc_extend_scratch(e["ws_k"]),
+                    err=torch.zeros(1, dtype=torch.int32, device=self.device))
         self.out = torch.empty(s.B, s.Hq, s.D, dtype=torch.bfloat16, device=self.device)
         self.workspace = alloc_decode_workspace(s.B, s.Hq, s.Hkv, self.num_splits, device=self.device)
 
@@ -113,9 +136,16 @@ class Layer:
                                      num_splits=self.num_splits)
 
     def extend(self):
+        """The chunked-extend pass: the cached prefix into the FP8 workspace,
+        (with extend_attention) the chunk behind it and the chunk's attention,
+        then the chunk quantized into the cache."""
         e = self.ext
         nvfp4_kv_dequant_to_fp8_workspace(self.block_table, e["seq_ids"], e["prefix_lens"], e["cu_prefix"],
                                           self.cache, e["ws_scale"], e["ws_k"], e["ws_v"])
+        if "q" in e:
+            fp8_workspace_append_chunk(e["k"], e["v"], e["rows"], e["ws_scale"], e["ws_k"], e["ws_v"], err=e["err"])
+            fp8_chunked_extend_attention(e["q"], e["cu_q"], e["max_q"], e["ws_k"], e["ws_v"], e["cu_kv"],
+                                         e["kv_lens"], e["ws_scale"], e["out"], e["scratch"], err=e["err"])
         self.write(e["k"], e["v"], e["slots"])
 
     def step(self):
@@ -146,7 +176,9 @@ class Layer:
 
     def launches_per_step(self) -> int:
         n = 1 if self.fused else (1 if self.k_new is not None else 0) + 1
-        return n + (2 if self.ext is not None else 0)
+        if self.ext is not None:
+            n += 2 + (3 if "q" in self.ext else 0)  # dequant, chunk write (+ append, tile expansion, attention)
+        return n
 
     # ------------------------------------------------------------ bookkeeping
     def kv_bytes_read(self) -> int:

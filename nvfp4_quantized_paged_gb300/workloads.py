@@ -189,6 +189,12 @@ class Workload:
             x = x * std
         return x[t0:t1].contiguous()
 
+    def ext_q_bf16(self, layer: int, n: int) -> torch.Tensor:
+        """BF16 queries [n, Hq, D] of the chunked-extend tokens (N(0,1) drawn in FP32, cast by torch)."""
+        s = self.spec
+        g = _gen(self.device, self.seed, 7, layer)
+        return torch.randn(n, s.Hq, s.D, generator=g, device=self.device).to(torch.bfloat16)
+
     def q_bf16(self, layer: int = 0) -> torch.Tensor:
         """BF16 queries [B, Hq, D] (N(0,1) drawn in FP32, cast by torch)."""
         s = self.spec

@@ -1,22 +1,44 @@
-"""The calibration study on a small case: errors finite and bounded, FP8
-closer to FP32 than NVFP4 on every distribution, and on sparse x20 outliers
-the amax-based global scale at least as good as a scale four times smaller
-(which saturates the outliers)."""
+"""The calibration study at the size its table is stated for (B = 4, L = 4096,
+32 q / 8 KV heads, seed 0): errors finite, FP8 closer to FP32 than NVFP4 on
+every distribution, on sparse x20 outliers the amax-based global scale at least
+as good as a scale four times smaller (which saturates the outliers), and each
+relative L2 error under a per-distribution bound.
+
+The bounds are the study's measured errors (B = 4, L = 4096, seed 0: NVFP4 at
+the amax rule 0.138 normal, 0.222 element outliers, 0.412 channel outliers,
+0.284 log-normal channels; FP8 0.038, 0.117, 0.212, 0.095) plus 15 %.  The
+study is deterministic for a fixed seed, so the margin only absorbs changes
+of the kernels' rounding order (query decomposition, accumulation order)
+that stay inside the parity tolerance; a change of the quantizer or of the
+cache format that moved an error by more would fail here.
+"""
 import pytest
 
 pytestmark = pytest.mark.gpu
 
+MEASURED = {  # (distribution, precision) -> relative L2 error of the output at the amax rule
+    ("normal", "nvfp4"): 0.138, ("element_outliers", "nvfp4"): 0.222,
+    ("channel_outliers", "nvfp4"): 0.412, ("lognormal_channels", "nvfp4"): 0.284,
+    ("normal", "fp8"): 0.038, ("element_outliers", "fp8"): 0.117,
+    ("channel_outliers", "fp8"): 0.212, ("lognormal_channels", "fp8"): 0.095,
+}
+SLACK = 1.15
 
-def test_calibration_study_small():
+
+def test_calibration_study_bounds():
     from nvfp4_quantized_paged_gb300.calibration import study
-    rows = study(device="cuda", B=2, L=1024, Hq=8, Hkv=2, factors=(0.25, 1.0, 4.0))
+    rows = study(device="cuda", factors=(0.25, 1.0, 4.0))
     assert len(rows) == 4 * (1 + 3)
+    by = {}
     for r in rows:
         assert r["cache_err"] == 0
         assert 0.0 < r["rel_l2"] < float("inf"), r
-        if r["factor"] == 1.0:  # the amax rule; moved scales may saturate (x0.25 on outliers: ~0.7)
-            assert r["rel_l2"] < 0.5, r
-    by = {(r["dist"], r["prec"], r["factor"]): r["rel_l2"] for r in rows}
+        by[(r["dist"], r["prec"], r["factor"])] = r["rel_l2"]
+    for (d, p), want in MEASURED.items():
+        assert by[(d, p, 1.0)] < want * SLACK, (d, p, by[(d, p, 1.0)], want)
     for d in ("normal", "element_outliers", "channel_outliers", "lognormal_channels"):
         assert by[(d, "fp8", 1.0)] < by[(d, "nvfp4", 1.0)], d
+        # a global scale 4x larger divides every block scale by 4, exactly while it stays an E4M3
+        # normal: the same codes and the same dequantized products (rare subnormal scales excepted)
+        assert by[(d, "nvfp4", 4.0)] == pytest.approx(by[(d, "nvfp4", 1.0)], rel=1e-2), d
     assert by[("element_outliers", "nvfp4", 1.0)] <= by[("element_outliers", "nvfp4", 0.25)]

@@ -249,3 +249,46 @@ def test_chunked_extend_chain_from_the_nvfp4_cache(orc):
     assert ok, f"max excess over tolerance {worst}"
     orc.quantize_write(oc, x["k"][ci], x["v"][ci], ch_slots)
     assert np.array_equal(cache.data.cpu().numpy(), oc.data)
+
+
+def test_serving_mix_layer_runs_the_extend_attention(orc):
+    """The serving-mix layer driver with the extend attention on: each extend
+    sequence's cached NVFP4 prefix is dequantized into the workspace, its
+    chunk appended behind it (rows reserved per sequence on 8-row starts), the
+    chunk's queries attend over [prefix || chunk], and the chunk is written
+    into the cache.  The attention output matches the oracle's chain on the
+    same inputs within the parity tolerance, and the workspace rows it read
+    match the oracle's bytes."""
+    from _oracle_side import OracleLayer, oracle_global_scales
+    from nvfp4_quantized_paged_gb300.runner import Layer
+    from nvfp4_quantized_paged_gb300.workloads import Spec, Workload
+    nv = _nv()
+    spec = Spec("mix_extend", B=3, Hq=32, Hkv=8, D=128, P=64, lens=(700, 90, 1300), dist="normal", step_write=1,
+                extend_seqs=(0, 2), extend_tokens=150)
+    wl = Workload(spec, seed=17, device="cuda")
+    lay = Layer(wl, 0, extend_attention=True)
+    lay.extend()
+    torch.cuda.synchronize()
+    e = lay.ext
+    assert e["err"].item() == 0 and lay.cache.err.item() == 0
+    # oracle chain: prefix cache -> workspace rows at the same starts -> chunk append -> attention
+    ids = [0, 2]
+    orl = OracleLayer(wl, 0, ids, False)
+    ws_o = oracle_global_scales(wl, 0, True)
+    assert np.array_equal(e["ws_scale"].cpu().numpy(), ws_o)
+    cu = e["cu_prefix"].cpu().numpy()
+    prefixes = [int(wl.seq_lens[b]) for b in ids]
+    wk, wv = orc.dequant_to_fp8_workspace(orl.cache, orl.block_table, np.arange(len(ids)), prefixes, ws_o,
+                                          row_start=cu[:-1], ws_rows=int(cu[-1]))
+    kc = np.concatenate([wl.kv(0, 0, b, p, p + 150).cpu().numpy() for b, p in zip(ids, prefixes)])
+    vc = np.concatenate([wl.kv(0, 1, b, p, p + 150).cpu().numpy() for b, p in zip(ids, prefixes)])
+    rows = e["rows"].cpu().numpy()
+    orc.fp8_workspace_append(wk, wv, kc, vc, rows, ws_o)
+    for i, p in enumerate(prefixes):
+        r = slice(int(cu[i]), int(cu[i]) + p + 150)
+        np.testing.assert_array_equal(e["ws_k"].cpu().numpy()[r], wk[r])
+        np.testing.assert_array_equal(e["ws_v"].cpu().numpy()[r], wv[r])
+    want = orc.fp8_extend_attention(_bits(e["q"].cpu()), e["cu_q"].cpu().numpy(), wk, wv, cu[:-1],
+                                    e["kv_lens"].cpu().numpy(), ws_o)
+    ok, worst = within_tol(e["out"].float().cpu().numpy(), want)
+    assert ok, f"max excess over tolerance {worst}"
