@@ -18,9 +18,12 @@
 //     mbarrier transaction counts); a query warp prepares each segment's query
 //     operand; twelve consumer warps
 //     in three groups of four (one warp per TMEM lane quadrant, 32 tokens each)
-//     take the tiles round-robin: a group issues the score MMAs of its next
-//     tile as soon as it has read the scores of its current one, then runs the
-//     softmax and P.V.
+//     take the tiles round-robin: each warp arms its group's next tile (its
+//     rows' scale factors, a count on the group's arming counter) as soon as
+//     it has read its rows of the current scores, the fourth warp to arm
+//     issues the score MMAs, and every warp then runs the softmax and P.V.
+//     In the decode step (nvfp4_paged_decode_step) the producer that copies a
+//     sequence's last tile first quantizes the step's new token into it.
 //   * Scores S = K Q^T straight from the packed cache: the K codes of a staged
 //     tile are the A operand of one block-scaled MMA (kind::mxf4nvf4, M = 128
 //     tokens, K = 64 per instruction) and the E4M3 block scales of K are its
