@@ -379,6 +379,7 @@ def _extra_line(res, peak):
         "step_gbs": round(res["bytes_step"] / (res["ms"] * 1e-3) / 1e9, 1),
         "roofline": {"bound": "hbm", "kernel": "decode_kernel<NVFP4>", "achieved": round(res["dec_gbs"], 1),
                      "peak": peak, "unit": "GB/s", "frac": round(res["dec_gbs"] / peak, 4),
+                     "traffic": _traffic_from_profile(res["spec"].name),
                      "algorithmic_bytes_per_launch": int(res["dec_bytes_per_launch"]),
                      "avg_launch_us": round(res["dec_avg_us"], 3)},
         "fp8_comparator": None if res["fp8_ms"] is None else {
