@@ -60,6 +60,29 @@ def test_decode_step_equals_write_then_decode(prec, P, dtype):
 
 
 @pytest.mark.parametrize("prec", ["nvfp4", "fp8"])
+@pytest.mark.parametrize("Hq,Hkv,P", [(16, 2, 32), (4, 4, 64), (64, 8, 16)])
+def test_decode_step_other_groups_and_pages(prec, Hq, Hkv, P):
+    """The same equality for 8 query heads per KV head (the kernel's second
+    instantiation), one head per KV head and page size 32."""
+    nv, wl, lay = _layer(prec, P, zlib.crc32(f"{prec}{Hq}{Hkv}{P}".encode()) % 1000, lens=(5, 128, 700, 1, 257),
+                         Hq=Hq, Hkv=Hkv)
+    pristine = lay.cache.data.clone()
+    lay.write(lay.k_new, lay.v_new, lay.slots_new)
+    lay.decode()
+    torch.cuda.synchronize()
+    want_bytes, want_out = lay.cache.data.clone(), lay.out.clone()
+    lay.cache.data.copy_(pristine)
+    lay.write(lay.k_new * 1.5 - 2.0, lay.v_new * -0.75, lay.slots_new)
+    out = torch.full_like(lay.out, float("nan"))
+    nv.nvfp4_paged_decode_step(lay.q, lay.k_step, lay.v_step, lay.cache, lay.block_table, lay.seq_lens, lay.prec,
+                               out, lay.workspace)
+    torch.cuda.synchronize()
+    assert lay.cache.err.item() == 0
+    assert torch.equal(lay.cache.data, want_bytes)
+    assert torch.equal(out, want_out)
+
+
+@pytest.mark.parametrize("prec", ["nvfp4", "fp8"])
 def test_decode_step_against_the_oracle(prec):
     nv, wl, lay = _layer(prec, 64, 321)
     lay.write(lay.k_new * 4.0, lay.v_new * -4.0, lay.slots_new)  # stale bytes the step must replace
