@@ -16,6 +16,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "nvkv_device.cuh"
 #include "nvkv_host.h"
 
@@ -305,6 +307,161 @@ __global__ void __launch_bounds__(kWriteWarps * 32)
 }
 
 // ---------------------------------------------------------------------------
+// Initial-prefill write from FP8 K/V ([P2] Three Paths: the prefill's FP8 KV is
+// requantized into the NVFP4 cache) by tables instead of per-value
+// arithmetic.  Every value is x = fl(E4M3(byte) s8) and every block's divisor
+// is den = fl(E4M3(sbyte) g), so a code depends only on (sbyte, byte):
+// code[sbyte][byte] = E2M1_RNE(fl(x_byte / den_sbyte)), built once per CTA
+// with the write rule's own IEEE operations (for the positive bytes; a
+// negative byte's x is the exact negation, so its code is the positive one's
+// with the sign bit: E2M1 rounding is symmetric).  x grows with the byte's
+// magnitude, so a block's amax is x of its largest magnitude and its scale
+// byte is sb[e_max] = E4M3_RNE(fl(x_emax / fl(6 g))).  A block whose den is 0
+// (g = 0, or the scale byte 0) writes code 0 everywhere, as the rule does.
+// NaN input bytes are outside the rule (undefined), as for every write.
+// One warp per (8 tokens, KV head) as in nvfp4_write_kernel (whole 8-slot
+// groups assembled in shared memory, other patterns through the item path),
+// in a persistent grid of one CTA of 32 warps per SM that builds the tables
+// once.  Per value: one byte extract, one table load, one multiply-add into
+// the packed codes.
+// ---------------------------------------------------------------------------
+constexpr int kRqWarps = 32;
+constexpr int kRqScales = 127;                      // scale bytes 0 .. 0x7E (sf <= 448)
+constexpr int kRqRow = 256;                         // one code per input byte
+constexpr int kRqLut = kRqScales * kRqRow;          // [scale byte][byte] -> E2M1 code
+constexpr int kRqOffX = kRqWarps * kNvGroup;        // after the group images: [2][128] f32 x of each magnitude
+constexpr int kRqOffDen = kRqOffX + 2 * 128 * 4;    // [2][127] f32 den of each scale byte (padded to 128)
+constexpr int kRqOffSb = kRqOffDen + 2 * 128 * 4;   // [2][128] u8 scale byte of a block's largest magnitude
+constexpr int kRqOffLut = kRqOffSb + 2 * 128;       // [2][kRqLut] u8
+constexpr int kRqSmem = kRqOffLut + 2 * kRqLut;
+
+// A row's entries are stored at byte ^ rq_swizzle(scale byte): an input
+// tensor's bytes cluster in a few dozen values, and without the swizzle the
+// lanes of a warp (each on its own block's row) would read the same few
+// banks at different rows; the XOR moves equal bytes of different rows onto
+// different banks (a permutation inside the row's 256 bytes).
+__device__ __forceinline__ uint32_t rq_swizzle(uint32_t sbyte) { return (sbyte & 31u) << 2; }
+
+// Codes of one 16-byte E4M3 block from the tables of its tensor: the scale
+// byte, then lo = values 0..7 and hi = values 8..15 (value 2j in the low
+// nibble of byte j), as quant16 gives them for the decoded values.
+__device__ __forceinline__ void requant16(const uint4 w, const uint8_t *lut, const uint8_t *sbl, const float *dens,
+                                          uint32_t &sbyte, uint32_t &lo, uint32_t &hi) {
+  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  uint32_t m4 = __vmaxu4(__vmaxu4(ww[0] & 0x7F7F7F7Fu, ww[1] & 0x7F7F7F7Fu),
+                         __vmaxu4(ww[2] & 0x7F7F7F7Fu, ww[3] & 0x7F7F7F7Fu));
+  m4 = __vmaxu4(m4, m4 >> 16);
+  m4 = __vmaxu4(m4, m4 >> 8);
+  sbyte = sbl[m4 & 0x7Fu];
+  lo = hi = 0;
+  if (dens[sbyte] == 0.0f) return;
+  const uint8_t *row = lut + sbyte * kRqRow;
+  const uint32_t swz = rq_swizzle(sbyte);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t c = row[((ww[i >> 2] >> (8 * (i & 3))) & 0xFFu) ^ swz];
+    if (i < 8)
+      lo += c << (4 * i);  // disjoint nibbles: the add is an or
+    else
+      hi += c << (4 * (i - 8));
+  }
+}
+
+__global__ void __launch_bounds__(kRqWarps * 32, 1)
+    nvfp4_requant_kernel(const uint8_t *__restrict__ k8, const uint8_t *__restrict__ v8, int64_t num_tokens,
+                         const int64_t *__restrict__ slot_mapping, const float *__restrict__ gs, CacheDev c,
+                         const float *__restrict__ in_scale) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  float *xs = reinterpret_cast<float *>(sm + kRqOffX);
+  float *dens = reinterpret_cast<float *>(sm + kRqOffDen);
+  uint8_t *sbl = sm + kRqOffSb;
+  uint8_t *lut = sm + kRqOffLut;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the tables of K (kind 0) and V (kind 1)
+  for (int i = tid; i < 2 * 128; i += blockDim.x) {
+    const int kind = i >> 7, e = i & 127;
+    xs[i] = __fmul_rn(f32_from_e4m3(static_cast<uint32_t>(e)), in_scale[kind]);
+    dens[i] = e < kRqScales ? __fmul_rn(f32_from_e4m3(static_cast<uint32_t>(e)), gs[kind]) : 0.0f;
+  }
+  __syncthreads();
+  for (int i = tid; i < 2 * 128; i += blockDim.x) {
+    const int kind = i >> 7;
+    const float g = gs[kind];
+    uint32_t sb = 0;
+    if (g != 0.0f) sb = e4m3x2_from_f32(__fdiv_rn(xs[i], __fmul_rn(6.0f, g)), 0.0f) & 0xFFu;
+    sbl[i] = static_cast<uint8_t>(sb);
+  }
+  for (int i = tid; i < 2 * kRqScales * 128; i += blockDim.x) {  // positive bytes; negative ones mirror them
+    const int kind = i / (kRqScales * 128), j = i % (kRqScales * 128), sb = j >> 7, e = j & 127;
+    const float den = dens[kind * 128 + sb];
+    uint32_t code = 0;
+    if (den != 0.0f) code = e2m1x2_from_f32(__fdiv_rn(xs[kind * 128 + e], den), 0.0f) & 0xFu;
+    uint8_t *row = lut + kind * kRqLut + sb * kRqRow;
+    row[e ^ rq_swizzle(sb)] = static_cast<uint8_t>(code);
+    row[(e | 0x80) ^ rq_swizzle(sb)] = static_cast<uint8_t>(code | 0x8u);
+  }
+  __syncthreads();
+  const int64_t ngroups = (num_tokens + 7) / 8;
+  for (int64_t wid = static_cast<int64_t>(blockIdx.x) * kRqWarps + warp; wid < ngroups * c.Hkv;
+       wid += static_cast<int64_t>(gridDim.x) * kRqWarps) {
+    const int h = static_cast<int>(wid % c.Hkv);
+    const int64_t t0 = (wid / c.Hkv) * 8;
+    const int64_t sl = t0 + (lane & 7) < num_tokens ? slot_mapping[t0 + (lane & 7)] : -1;
+    const int64_t s0 = __shfl_sync(0xffffffffu, sl, 0);
+    const bool whole = __all_sync(0xffffffffu, s0 >= 0 && (s0 & 7) == 0 && sl == s0 + (lane & 7) &&
+                                                   s0 + 7 < static_cast<int64_t>(c.num_pages) * c.P);
+    if (!whole) {
+      for (int it = lane; it < 2 * 8 * kBlocksPerRow; it += 32) {
+        const int kind = it / (8 * kBlocksPerRow), tt = (it / kBlocksPerRow) % 8, blk = it % kBlocksPerRow;
+        if (t0 + tt < num_tokens)
+          nvfp4_write_item<uint8_t>(k8, v8, num_tokens, slot_mapping, gs, c, in_scale, kind, t0 + tt, h, blk);
+      }
+      continue;
+    }
+    uint8_t *im = sm + warp * kNvGroup;
+    {  // K: token tk, blocks 2 (lane % 4) and 2 (lane % 4) + 1
+      const int tk = lane >> 2;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int blk = 2 * (lane & 3) + j;
+        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(k8 + ((t0 + tk) * c.Hkv + h) * kD + 16 * blk));
+        uint32_t sb, lo, hi;
+        requant16(w, lut, sbl, dens, sb, lo, hi);
+        *reinterpret_cast<uint2 *>(im + (blk >> 1) * 128 + tk * 16 + (blk & 1) * 8) = make_uint2(lo, hi);
+        im[kNvKScales + tk * 8 + blk] = static_cast<uint8_t>(sb);
+      }
+    }
+    {  // V: slots 2p and 2p + 1, block blk (slot 2p in the low nibble)
+      const int p = lane >> 3, blk = lane & 7;
+      uint32_t sb[2], lo[2], hi[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(v8 + ((t0 + 2 * p + u) * c.Hkv + h) * kD + 16 * blk));
+        requant16(w, lut + kRqLut, sbl + 128, dens + 128, sb[u], lo[u], hi[u]);
+      }
+      uint32_t w4[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        w4[q] = spread4(((q < 2 ? lo[0] : hi[0]) >> (16 * (q & 1))) & 0xFFFFu) |
+                (spread4(((q < 2 ? lo[1] : hi[1]) >> (16 * (q & 1))) & 0xFFFFu) << 4);
+      *reinterpret_cast<uint4 *>(im + kNvVCodes + blk * 64 + p * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      im[kNvVScales + blk * 8 + 2 * p] = static_cast<uint8_t>(sb[0]);
+      im[kNvVScales + blk * 8 + 2 * p + 1] = static_cast<uint8_t>(sb[1]);
+    }
+    __syncwarp();
+    const int64_t page = s0 / c.P;
+    const int off = static_cast<int>(s0 % c.P);
+    uint4 *dst =
+        reinterpret_cast<uint4 *>(c.data + c.block(page, h, kNvTokBytes) + static_cast<int64_t>(off >> 3) * kNvGroup);
+    const uint4 *src = reinterpret_cast<const uint4 *>(im);
+    for (int i = lane; i < kNvGroup / 16; i += 32) dst[i] = src[i];
+    __syncwarp();  // the image is rewritten by the warp's next item
+  }
+}
+
+// ---------------------------------------------------------------------------
 // FP8 E4M3 write: byte = E4M3(x / s8).
 // ---------------------------------------------------------------------------
 template <typename T>
@@ -464,6 +621,25 @@ void launch_pdl(void (*kernel)(KArgs...), dim3 grid, cudaStream_t s, Args... arg
   }
 }
 
+// As launch_pdl, with a block size and dynamic shared memory of the caller's.
+template <typename... KArgs, typename... Args>
+void launch_pdl_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) != cudaSuccess) {
+    cudaGetLastError();
+    kernel<<<grid, block, smem, s>>>(static_cast<KArgs>(args)...);
+  }
+}
+
 inline int grid_for(int64_t items, int threads) {
   const int64_t b = (items + threads - 1) / threads;
   return static_cast<int>(b < 1 ? 1 : b);
@@ -592,9 +768,20 @@ nvkv_status nvfp4_kv_requantize_write_fp8(const uint8_t *k8, const uint8_t *v8, 
   if (!k8 || !v8 || !in_scale || !slot_mapping) return NVKV_ERR_INVALID_ARG;
   if (!aligned16(k8) || !aligned16(v8)) return NVKV_ERR_UNSUPPORTED;
   const float *gs = global_scale ? global_scale : cache->kv_scale;
-  const dim3 grid(grid_for((num_tokens + 7) / 8 * cache->num_kv_heads, kWriteWarps));  // one warp per (8 tokens, KV head)
-  launch_pdl(nvfp4_write_kernel<uint8_t>, grid, static_cast<cudaStream_t>(stream), k8, v8, num_tokens, slot_mapping,
-             gs, to_dev(cache), in_scale);
+  // a persistent grid of one 32-warp CTA per SM (each builds the tables once), at most one warp per item
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 1;
+  static std::once_flag attr_once;
+  std::call_once(attr_once, [] {
+    cudaFuncSetAttribute(nvfp4_requant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRqSmem);
+  });
+  const int64_t items = (num_tokens + 7) / 8 * cache->num_kv_heads;
+  const int64_t ctas = (items + kRqWarps - 1) / kRqWarps;
+  const dim3 grid(static_cast<unsigned>(ctas < sms ? ctas : sms));
+  launch_pdl_ex(nvfp4_requant_kernel, grid, dim3(kRqWarps * 32), kRqSmem, static_cast<cudaStream_t>(stream), k8, v8,
+                num_tokens, slot_mapping, gs, to_dev(cache), in_scale);
   return launch_status();
 }
 
