@@ -201,8 +201,11 @@ nvkv_status nvkv_decode_workspace_init(void *workspace, size_t bytes, void *stre
  * programmatic dependent launch so its set-up overlaps the previous kernel;
  * the result does not depend on arrival order).  Requires num_q_heads /
  * num_kv_heads <= 8, num_kv_heads >= 1 and batch <= 1024; the CTA count is at
- * most one resident wave.  Calls that share a workspace must be ordered (one
- * stream). */
+ * most one resident wave and at most 184.  Each CTA streams one contiguous
+ * run of 128-token tiles; when batch * num_kv_heads is at least four per CTA
+ * the runs are balanced on tiles plus a charge of three tiles per (sequence,
+ * KV head) they hold, else on tiles alone.  Calls that share a workspace must
+ * be ordered (one stream). */
 nvkv_status nvfp4_paged_decode_attention(const void *q, const nvkv_cache *cache, const int32_t *block_table,
                                          int32_t max_pages, const int32_t *seq_lens, int32_t batch,
                                          int32_t num_q_heads, int32_t layer_precision, float sm_scale,

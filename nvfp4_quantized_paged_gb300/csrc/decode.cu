@@ -64,6 +64,7 @@ constexpr int kProducerWarp = kConsumerWarps;       // producer warps kProducerW
 constexpr int kQueryWarp = kConsumerWarps + kGroups;
 constexpr int kThreads = (kConsumerWarps + kGroups + 1) * 32;
 constexpr int kMaxBatch = 1024;    // sequences per call (prefix sums live in shared memory)
+constexpr int kMaxShares = 184;    // CTAs per launch (weighted shares keep every share's start in shared memory)
 constexpr int kMaxGroup = 8;       // query heads per KV head
 constexpr int kQBufs = 4;          // query images in flight: a group issues a tile at most three
                                    // segments ahead of the one all warps are in (segments of one tile)
@@ -153,6 +154,10 @@ struct Cfg {
   static constexpr int oPend = oFlags + 4 * (7 + kStages);  // [2][4] i32: split pairs this CTA merges at its end
   static constexpr int oArm = oPend + 4 * 8;  // [kGroups] i32 arming counters, [kGroups] i32 last tile armed
   static constexpr int kSmem = oArm + 4 * 2 * kGroups;
+  // weighted shares (see tile_at): every share's first unit, after the rest
+  static constexpr int oStarts = kSmem;  // [kMaxShares + 1] i32
+  static constexpr int kSmemW = oStarts + 4 * (kMaxShares + 1);
+  static_assert(kSmemW <= 232448, "shared memory exceeds the per-block limit");
 };
 
 struct DecodeArgs {
@@ -221,6 +226,87 @@ __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t W, int64_t NC) {
   return ((u + 1) * NC + W - 1) / W - 1;
 }
 
+// Shares weighted by pairs, for batches of many (sequence, KV head) pairs
+// per CTA.  A pair costs a CTA more than its tiles: its query image, the
+// merge of its partial results and the restart of the tile pipeline
+// (measured ~1.2 us per pair a share holds on a batch of many short
+// sequences, ~3 tiles' worth).  So the tiles are laid on a "virtual" line on
+// which tile u of pair q = b Hkv + h starts at kVTile u + vk (q + 1): every
+// pair (empty sequences' pairs included, which hold no tile) is preceded by
+// vk units.  The line's length is V = kVTile W + vk B Hkv, CTA c's range is
+// [floor(c V / NC), floor((c+1) V / NC)) and it owns the tiles whose start
+// lies in it; a share is still a contiguous run of tiles.  With NC <= W a
+// range is at least one tile long, so inside a pair (no gaps between its
+// tiles) every CTA between the pair's first and last owner owns some of its
+// tiles (the merge's contributor count relies on it); a range that falls
+// between two pairs may hold no tile: that CTA has nothing to do.  vk =
+// kVPair when the batch has at least kVPairMin pairs with tiles per CTA,
+// else 0 (the equal split floor(c W / NC)).  The kernel that weighs shares
+// is launched when batch x Hkv reaches kVPairMin per CTA; with fewer pairs
+// per share the weight measured slower.
+constexpr int64_t kVTile = 8, kVPair = 24, kVPairMin = 4;
+
+__device__ __forceinline__ int64_t vpos(int64_t u, int b, int h, int Hkv, int64_t vk) {
+  return kVTile * u + vk * (static_cast<int64_t>(b) * Hkv + h + 1);
+}
+
+// floor(n / d) for 0 <= n < 2^52 and 0 < d < 2^11, by two 32-bit divisions:
+// n = hi 2^20 + lo, floor(n / d) = floor(hi / d) 2^20 +
+// floor(((hi mod d) 2^20 + lo) / d), the second numerator < 2^31.
+__device__ __forceinline__ int64_t div_small(int64_t n, uint32_t d) {
+  const uint32_t hi = static_cast<uint32_t>(n >> 20), lo = static_cast<uint32_t>(n) & 0xFFFFFu;
+  const uint32_t qh = hi / d;
+  const uint32_t ql = (((hi - qh * d) << 20) | lo) / d;
+  return (static_cast<int64_t>(qh) << 20) + ql;
+}
+
+// floor(n / d) for 0 <= n, 0 < d, when the quotient is known to be < 2^16:
+// a single-precision estimate (relative error < 2^-20, so within one of the
+// quotient) corrected by exact integer comparisons.
+__device__ __forceinline__ int64_t div_est(int64_t n, int64_t d) {
+  int64_t q = static_cast<int64_t>(__fdividef(static_cast<float>(n), static_cast<float>(d)));
+  if (q < 0) q = 0;
+  while (q > 0 && q * d > n) --q;
+  while ((q + 1) * d <= n) ++q;
+  return q;
+}
+
+// The first tile whose virtual start is >= vt (W when none is).  Sequence b's
+// pairs start at base_b + h (kVTile nb + vk), base_b = vpos(Hkv cum[b], b,
+// 0): a search over sequences, then the head by a short division.
+__device__ __forceinline__ int64_t tile_at(int64_t vt, const int32_t *cum, int B, int Hkv, int64_t vk) {
+  int lo = 0, hi = B - 1;  // the last sequence whose first position is <= vt
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (vpos(static_cast<int64_t>(cum[mid]) * Hkv, mid, 0, Hkv, vk) <= vt) lo = mid;
+    else hi = mid - 1;
+  }
+  const int nb = cum[lo + 1] - cum[lo];
+  const int64_t u_b = static_cast<int64_t>(cum[lo]) * Hkv;
+  const int64_t base = vpos(u_b, lo, 0, Hkv, vk);
+  if (base >= vt) return u_b;
+  const int64_t step = kVTile * nb + vk;  // from one pair's first position to the next's
+  if (step == 0) return u_b;            // (an empty sequence without weights: no tile here)
+  int64_t h = div_est(vt - base, step);
+  if (h > Hkv - 1) h = Hkv - 1;
+  const int64_t p0 = base + h * step, u = u_b + h * nb;
+  const int64_t t = (vt - p0 + kVTile - 1) / kVTile;
+  return t < nb ? u + t : u + nb;  // past the pair: the next pair's first tile
+}
+
+// Weighted shares: the CTA whose share holds unit u (0 <= u < W), the last
+// share starting at or before u (shares without tiles start where the next
+// one does).
+__device__ __forceinline__ int64_t owner_in(int64_t u, const int *starts, int64_t NC) {
+  int lo = 0, hi = static_cast<int>(NC) - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (starts[mid] <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
 // Split-KV arrival, by one thread once this CTA's partial of segment s is
 // written and fenced.  The contributors of (b, h) are the CTAs owning its
 // first through last unit: contributor 0 left its part in slot 0 of its CTA
@@ -229,13 +315,15 @@ __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t W, int64_t NC) {
 // that arrives last resets the counter for the next call and records the
 // pair {b, h, n, 2 c_first + slot} in the CTA's pending list (at most two:
 // a share cuts at most its first and its last pair).
+template <bool WT>
 __device__ __forceinline__ void split_arrive(const DecodeArgs &a, const int32_t *cum, const Seg &s, int64_t W,
-                                             int64_t NC, int *npend, int *pend) {
+                                             int64_t NC, const int *starts, int *npend, int *pend) {
   const int Hkv = a.c.Hkv;
   const int nb = cum[s.b + 1] - cum[s.b];
   const int64_t ubh0 = static_cast<int64_t>(cum[s.b]) * Hkv + static_cast<int64_t>(s.h) * nb;
-  const int64_t c_first = owner_of(ubh0, W, NC);
-  const int n = static_cast<int>(owner_of(ubh0 + nb - 1, W, NC) - c_first + 1);
+  const int64_t c_first = WT ? owner_in(ubh0, starts, NC) : owner_of(ubh0, W, NC);
+  const int n = static_cast<int>((WT ? owner_in(ubh0 + nb - 1, starts, NC) : owner_of(ubh0 + nb - 1, W, NC)) -
+                                 c_first + 1);
   uint32_t *cnt = a.counters + static_cast<int64_t>(s.b) * Hkv + s.h;
   const uint32_t before = atomicAdd(cnt, 1u);
   if (before == static_cast<uint32_t>(n - 1)) {  // every other part is in place
@@ -245,7 +333,8 @@ __device__ __forceinline__ void split_arrive(const DecodeArgs &a, const int32_t 
       pend[4 * r + 0] = s.b;
       pend[4 * r + 1] = s.h;
       pend[4 * r + 2] = n;
-      pend[4 * r + 3] = static_cast<int>(c_first) * 2 + (share_begin(c_first, W, NC) == ubh0 ? 0 : 1);
+      const int64_t first = WT ? starts[c_first] : share_begin(c_first, W, NC);
+      pend[4 * r + 3] = static_cast<int>(c_first) * 2 + (first == ubh0 ? 0 : 1);
     }
   }
 }
@@ -547,7 +636,7 @@ __device__ void prepare_query(const DecodeArgs &a, const Seg &s, uint8_t *img, u
 // M = max_w m_w, factors f_w = 2^(m_w - M) (over m_w in place), l = sum f_w
 // l_w; then O = sum_w f_w O_w goes to the output (the CTA held all of (b, h))
 // or to the CTA's partial slot for the merge kernel.
-template <int PREC, int NH>
+template <int PREC, int NH, bool WT>
 __device__ void merge_segment(const DecodeArgs &a, uint8_t *smem, const int32_t *cum, const Seg &s, int slot_id,
                               int64_t W, int64_t NC, int *npend) {
   using C = Cfg<PREC, NH>;
@@ -607,7 +696,8 @@ __device__ void merge_segment(const DecodeArgs &a, uint8_t *smem, const int32_t 
   if (!complete) {
     __threadfence();  // this lane's part of the partial, visible before the arrival
     __syncwarp();
-    if (lane == 0) split_arrive(a, cum, s, W, NC, npend, npend + 1);
+    if (lane == 0)
+      split_arrive<WT>(a, cum, s, W, NC, reinterpret_cast<const int *>(smem + C::oStarts), npend, npend + 1);
   }
   __syncwarp();
 }
@@ -615,7 +705,7 @@ __device__ void merge_segment(const DecodeArgs &a, uint8_t *smem, const int32_t 
 // The query warp: prepares each segment's query image (at most kQBufs
 // segments ahead of the consumers) and, with the async merge, merges each
 // segment the consumers have finished, in order, but the share's last.
-template <int PREC, int NH>
+template <int PREC, int NH, bool WT>
 __device__ int query_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uint64_t *qready, uint64_t *qfree,
                           uint64_t *mdone, const int32_t *cum, int64_t u0, int64_t u1, int64_t W, int64_t NC,
                           volatile int *abort, float kscale, int *npend) {
@@ -651,7 +741,7 @@ __device__ int query_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uin
     } else if (C::kAsyncMerge && u_m + (s_m.t1 - s_m.t0) < u1) {  // the last segment: merged by the consumers
       const int q = sm % kQBufs;
       if (!warp_wait(&qfree[q], static_cast<uint32_t>(sm / kQBufs) & 1u, abort)) return sp;  // segment sm done
-      merge_segment<PREC, NH>(a, smem, cum, s_m, u_m == u0 ? 0 : 1, W, NC, npend);
+      merge_segment<PREC, NH, WT>(a, smem, cum, s_m, u_m == u0 ? 0 : 1, W, NC, npend);
       if (lane == 0) mbar_arrive(mdone);  // its buffers may be rewritten
       __syncwarp();
       u_m += s_m.t1 - s_m.t0;
@@ -866,7 +956,7 @@ __device__ __forceinline__ float pick(const float (&v)[NH], int i) {  // v[i] fo
   return r;
 }
 
-template <int PREC, int NH>
+template <int PREC, int NH, bool WT>
 __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem, uint64_t *full, uint64_t *empty,
                               uint64_t *sready, uint64_t *qready, uint64_t *qfree, uint64_t *mdone, const int32_t *cum,
                               int64_t u0, int64_t u1, int64_t W, int64_t NC, volatile int *abort,
@@ -1150,7 +1240,8 @@ __device__ void consumer_role(const DecodeArgs &a, uint8_t *smem, uint32_t tmem,
       if (!complete) __threadfence();  // this thread's part of the partial, visible before the arrival
       named_bar_sync(1, kConsumerWarps * 32);
     }
-    if (!complete && tid == 0) split_arrive(a, cum, s, W, NC, npend, npend + 1);
+    if (!complete && tid == 0)
+      split_arrive<WT>(a, cum, s, W, NC, reinterpret_cast<const int *>(smem + C::oStarts), npend, npend + 1);
     if (lane == 0) mbar_arrive(&qfree[qb]);  // every score of this segment was read: its image may be reused
     u += ntiles;
     s = s_nx;
@@ -1212,7 +1303,7 @@ __device__ void final_merge(const DecodeArgs &a, const int *rec) {
 // ---------------------------------------------------------------------------
 // The decode kernel: set-up, role dispatch, split-KV merges, teardown.
 // ---------------------------------------------------------------------------
-template <int PREC, int NH>
+template <int PREC, int NH, bool WT>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a) {
   using C = Cfg<PREC, NH>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -1269,11 +1360,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
   // prefix sums by warp 0 from shared memory
   for (int b = tid; b < B; b += kThreads) cum[b + 1] = a.seq_lens[b];
   __syncthreads();
-  if (warp == 0) {
-    int carry = 0;
-    if (lane == 0) cum[0] = 0;
-    for (int base = 0; base < B; base += 32) {
-      const int b = base + lane;
+  if constexpr (WT) {
+    // Prefix sums, kThreads sequences per pass: a scan within each warp, then
+    // over the warps' totals (in the merge scratch, which only the set-up
+    // uses at this point).  Then thread c finds the start of share c on the
+    // virtual line (thread NC: W).
+    int *wsum = reinterpret_cast<int *>(smem + C::oMrgO);
+    if (tid == 0) cum[0] = 0;
+    int carry = 0, nonempty = 0;  // tiles and sequences with tiles so far
+    for (int base = 0; base < B; base += kThreads) {
+      const int b = base + tid;
       int n = 0;
       if (b < B) {
         int64_t Lb = cum[b + 1];
@@ -1290,20 +1386,78 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      if (b < B) cum[b + 1] = carry + incl;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
+      if (lane == 31) wsum[warp] = incl;
+      nonempty += __syncthreads_count(n > 0);
+      int wv = lane < kThreads / 32 ? wsum[lane] : 0;  // the warps' totals, scanned
+#pragma unroll
+      for (int o = 1; o < kThreads / 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wv, o);
+        if (lane >= o) wv += y;
+      }
+      const int before = warp > 0 ? __shfl_sync(0xffffffffu, wv, warp - 1) : 0;
+      if (b < B) cum[b + 1] = carry + before + incl;
+      carry += __shfl_sync(0xffffffffu, wv, kThreads / 32 - 1);
+      __syncthreads();  // the totals are read before the next pass writes them
     }
-    if (lane == 0) {  // this CTA's share of the units, computed once
-      // never more shares than units: every active CTA owns at least one unit,
-      // which the contributor count of the merge relies on
-      const int64_t W = static_cast<int64_t>(carry) * Hkv;
-      const int64_t NC = W < a.num_ctas ? (W > 0 ? W : 1) : a.num_ctas;
-      const bool active = blockIdx.x < NC;
+    // never more shares than units, so a share is at least one tile long on
+    // the virtual line (see tile_at)
+    const int64_t W = static_cast<int64_t>(carry) * Hkv;
+    const int NC = static_cast<int>(W < a.num_ctas ? (W > 0 ? W : 1) : a.num_ctas);
+    const int64_t vk = static_cast<int64_t>(nonempty) * Hkv >= kVPairMin * NC ? kVPair : 0;
+    int *starts = reinterpret_cast<int *>(smem + C::oStarts);
+    if (tid <= NC) {
+      int64_t st = 0;
+      if (W > 0 && tid == NC) st = W;
+      else if (W > 0 && vk == 0) st = div_small(tid * W, NC);
+      else if (W > 0) st = tile_at(div_small(tid * (kVTile * W + vk * static_cast<int64_t>(B) * Hkv), NC), cum, B, Hkv, vk);
+      starts[tid] = static_cast<int>(st);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const bool active = static_cast<int>(blockIdx.x) < NC;
       int *sh = flags + 2 + C::kStages;
       sh[0] = static_cast<int>(W);
-      sh[1] = static_cast<int>(NC);
-      sh[2] = active ? static_cast<int>(share_begin(blockIdx.x, W, NC)) : 0;
-      sh[3] = active ? static_cast<int>(share_begin(blockIdx.x + 1, W, NC)) : 0;
+      sh[1] = NC;
+      sh[2] = active ? starts[blockIdx.x] : 0;
+      sh[3] = active ? starts[blockIdx.x + 1] : 0;
+    }
+  } else {
+    if (warp == 0) {
+      int carry = 0;
+      if (lane == 0) cum[0] = 0;
+      for (int base = 0; base < B; base += 32) {
+        const int b = base + lane;
+        int n = 0;
+        if (b < B) {
+          int64_t Lb = cum[b + 1];
+          if (Lb < 0 || Lb > cap) {
+            if (blockIdx.x == 0) set_err(a.c.err, NVKV_DEVERR_SEQLEN);
+            Lb = Lb < 0 ? 0 : cap;
+          }
+          n = static_cast<int>((Lb + kTile - 1) / kTile);
+          reinterpret_cast<uint8_t *>(cum + kMaxBatch + 1)[b] = static_cast<uint8_t>(Lb - (n > 0 ? (n - 1) * kTile : 0));
+        }
+        int incl = n;
+  #pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (b < B) cum[b + 1] = carry + incl;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) {  // this CTA's share of the units, computed once
+        // never more shares than units: every active CTA owns at least one unit,
+        // which the contributor count of the merge relies on
+        const int64_t W = static_cast<int64_t>(carry) * Hkv;
+        const int64_t NC = W < a.num_ctas ? (W > 0 ? W : 1) : a.num_ctas;
+        const bool active = blockIdx.x < NC;
+        int *sh = flags + 2 + C::kStages;
+        sh[0] = static_cast<int>(W);
+        sh[1] = static_cast<int>(NC);
+        sh[2] = active ? static_cast<int>(share_begin(blockIdx.x, W, NC)) : 0;
+        sh[3] = active ? static_cast<int>(share_begin(blockIdx.x + 1, W, NC)) : 0;
+      }
     }
   }
   tc_fence_before();
@@ -1327,9 +1481,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     producer<PREC, NH>(a, smem + C::oRing, full, empty, cum, u0, u1, warp - kProducerWarp, abort, fills);
   } else if (warp == kQueryWarp) {
     const float kscale = __fmul_rn(a.c.scale[0], a.sm_scale * 1.4426950408889634f);
-    last_issued = query_role<PREC, NH>(a, smem, tmem, qready, qfree, mdone, cum, u0, u1, W, NC, abort, kscale, npend);
+    last_issued = query_role<PREC, NH, WT>(a, smem, tmem, qready, qfree, mdone, cum, u0, u1, W, NC, abort, kscale, npend);
   } else {
-    consumer_role<PREC, NH>(a, smem, tmem, full, empty, sready, qready, qfree, mdone, cum, u0, u1, W, NC, abort,
+    consumer_role<PREC, NH, WT>(a, smem, tmem, full, empty, sready, qready, qfree, mdone, cum, u0, u1, W, NC, abort,
                             arm_cnt, last_iss, npend);
   }
 
@@ -1381,14 +1535,20 @@ std::once_flag g_once[64];
 template <int PREC, int NH>
 int occupancy_for(int dev) {
   const int smem = Cfg<PREC, NH>::kSmem;
-  if (cudaFuncSetAttribute(decode_kernel<PREC, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(decode_kernel<PREC, NH, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(decode_kernel<PREC, NH, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<PREC, NH>::kSmemW) != cudaSuccess)
     return 0;
   // two CTAs of ~110 KB per SM need the largest shared-memory carveout
-  if (cudaFuncSetAttribute(decode_kernel<PREC, NH>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  if (cudaFuncSetAttribute(decode_kernel<PREC, NH, false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+      cudaFuncSetAttribute(decode_kernel<PREC, NH, true>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared) != cudaSuccess)
     return 0;
+  // (the weighted-share kernel holds kSmemW - kSmem bytes more: one CTA per SM either way)
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, decode_kernel<PREC, NH>) != cudaSuccess) return 0;
+  if (cudaFuncGetAttributes(&fa, decode_kernel<PREC, NH, false>) != cudaSuccess) return 0;
   int sm_smem = 0, reserved = 0, sm_regs = 0, sm_threads = 0;
   cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
@@ -1441,6 +1601,7 @@ int64_t num_ctas_for(int prec, int32_t batch, int32_t Hkv, int32_t G, int64_t ma
     n = static_cast<int64_t>(d->sms) * (o > 0 ? o : 1);
   }
   if (n > max_units) n = max_units;
+  if (n > kMaxShares) n = kMaxShares;
   return n < 1 ? 1 : n;
 }
 
@@ -1454,21 +1615,22 @@ size_t workspace_bytes_for(int32_t batch, int32_t Hkv, int64_t nctas) {
 // Programmatic dependent launch: the grid may start while the previous kernel
 // on the stream finishes (its set-up overlaps that kernel's tail); the kernel
 // waits for it before touching global memory.
-template <int PREC, int NH>
+template <int PREC, int NH, bool WT>
 void launch_decode(const DecodeArgs &a, cudaStream_t s) {
+  constexpr int smem = WT ? Cfg<PREC, NH>::kSmemW : Cfg<PREC, NH>::kSmem;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.num_ctas));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<PREC, NH>::kSmem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, decode_kernel<PREC, NH>, a) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, decode_kernel<PREC, NH, WT>, a) != cudaSuccess) {
     cudaGetLastError();  // clear, then an ordinary stream-ordered launch
-    decode_kernel<PREC, NH><<<static_cast<unsigned>(a.num_ctas), kThreads, Cfg<PREC, NH>::kSmem, s>>>(a);
+    decode_kernel<PREC, NH, WT><<<static_cast<unsigned>(a.num_ctas), kThreads, smem, s>>>(a);
   }
 }
 
@@ -1516,12 +1678,14 @@ nvkv_status decode_common(const void *q, const nvkv_cache *cache, const int32_t 
   a.v_new = v_new;
   a.new_dtype = new_dtype;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // shares weighted by pairs when the batch has many pairs per CTA
+  const bool wt = static_cast<int64_t>(batch) * Hkv >= kVPairMin * nctas;
   if (prec == NVKV_PREC_NVFP4) {
-    if (G <= 4) launch_decode<NVKV_PREC_NVFP4, 4>(a, s);
-    else launch_decode<NVKV_PREC_NVFP4, 8>(a, s);
+    if (G <= 4) wt ? launch_decode<NVKV_PREC_NVFP4, 4, true>(a, s) : launch_decode<NVKV_PREC_NVFP4, 4, false>(a, s);
+    else wt ? launch_decode<NVKV_PREC_NVFP4, 8, true>(a, s) : launch_decode<NVKV_PREC_NVFP4, 8, false>(a, s);
   } else {
-    if (G <= 4) launch_decode<NVKV_PREC_FP8_E4M3, 4>(a, s);
-    else launch_decode<NVKV_PREC_FP8_E4M3, 8>(a, s);
+    if (G <= 4) wt ? launch_decode<NVKV_PREC_FP8_E4M3, 4, true>(a, s) : launch_decode<NVKV_PREC_FP8_E4M3, 4, false>(a, s);
+    else wt ? launch_decode<NVKV_PREC_FP8_E4M3, 8, true>(a, s) : launch_decode<NVKV_PREC_FP8_E4M3, 8, false>(a, s);
   }
   return launch_status();
 }

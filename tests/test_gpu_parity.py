@@ -47,6 +47,12 @@ CASES = {
     # CTA shares that run through many one-tile (sequence, head) segments in a row
     "short_segments": dict(B=9, lens=(2000, 64, 1, 100, 64, 128, 5, 64, 700), num_splits=1),
     "lognormal_channels": dict(B=3, lens=(600, 333, 64), dist="lognormal_channels", channel_sigma=0.5),
+    # at least four (sequence, KV head) pairs per CTA: the launch weighs shares by
+    # pairs (88 of 96 sequences hold tiles) ...
+    "many_pairs_weighted": dict(B=96, lens=(1, 64, 65, 129, 200, 300, 511, 0, 700, 128, 127, 40) * 8),
+    # ... and the same launch with too few non-empty sequences for the weight
+    # (16 of 96), which then splits the tiles equally
+    "many_pairs_mostly_empty": dict(B=96, lens=(0, 0, 0, 0, 0, 300) * 16),
 }
 
 
@@ -76,7 +82,7 @@ def test_nvfp4_write_and_decode(name):
     _run_case(name, fp8=False)
 
 
-@pytest.mark.parametrize("name", ["ragged_p64", "ragged_p16", "empty_seqs", "gqa8", "splits7"])
+@pytest.mark.parametrize("name", ["ragged_p64", "ragged_p16", "empty_seqs", "gqa8", "splits7", "many_pairs_weighted"])
 def test_fp8_write_and_decode(name):
     _run_case(name, fp8=True)
 
