@@ -719,7 +719,7 @@ def run_prefill_write(args):
                 "e2e": {"value": round(per / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                         "h2d_bytes_per_step": int(hk.numel() * 2), "d2h_bytes_per_step": int(hb.numel())},
                 "gpu_launches": args.steps,
-                "roofline": {"bound": "hbm", "kernel": "nvfp4_write_kernel<uint8_t>", "achieved": round(gbs, 1),
+                "roofline": {"bound": "hbm", "kernel": "nvfp4_requant_kernel", "achieved": round(gbs, 1),
                              "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(gbs / peak, 4),
                              "traffic": None, "algorithmic_bytes_per_launch": int(per),
                              "avg_launch_us": round(ms * 1e3, 2),

@@ -16,6 +16,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cfloat>
 #include <mutex>
 
 #include "nvkv_device.cuh"
@@ -308,44 +309,42 @@ __global__ void __launch_bounds__(kWriteWarps * 32)
 
 // ---------------------------------------------------------------------------
 // Initial-prefill write from FP8 K/V ([P2] Three Paths: the prefill's FP8 KV is
-// requantized into the NVFP4 cache) by tables instead of per-value
+// requantized into the NVFP4 cache) by thresholds instead of per-value
 // arithmetic.  Every value is x = fl(E4M3(byte) s8) and every block's divisor
 // is den = fl(E4M3(sbyte) g), so a code depends only on (sbyte, byte):
-// code[sbyte][byte] = E2M1_RNE(fl(x_byte / den_sbyte)), built once per CTA
-// with the write rule's own IEEE operations (for the positive bytes; a
-// negative byte's x is the exact negation, so its code is the positive one's
-// with the sign bit: E2M1 rounding is symmetric).  x grows with the byte's
-// magnitude, so a block's amax is x of its largest magnitude and its scale
-// byte is sb[e_max] = E4M3_RNE(fl(x_emax / fl(6 g))).  A block whose den is 0
+// code = E2M1_RNE(fl(x_byte / den_sbyte)).  For s8 > 0 (finite) x grows with
+// the byte's magnitude e = byte & 0x7F and is +-|x_e| with the byte's sign,
+// and fl(. / den) and E2M1_RNE are monotone and odd, so the code is the
+// byte's sign over a magnitude code that steps up at seven magnitudes:
+// T_k(sbyte) = the least e whose magnitude code is >= k (k = 1..7; 128 when
+// none).  These are found once per CTA by bisection with the write rule's
+// own IEEE operations; a value's magnitude code is then #{k : e >= T_k}.  A
+// block's amax is x of its largest magnitude and its scale byte is
+// sb[e_max] = E4M3_RNE(fl(x_emax / fl(6 g))).  A block whose den is 0
 // (g = 0, or the scale byte 0) writes code 0 everywhere, as the rule does.
+// An input scale that is not a positive finite number, or a global scale that
+// is negative or not finite, sends every item through the per-value path.
 // NaN input bytes are outside the rule (undefined), as for every write.
 // One warp per (8 tokens, KV head) as in nvfp4_write_kernel (whole 8-slot
 // groups assembled in shared memory, other patterns through the item path),
-// in a persistent grid of one CTA of 32 warps per SM that builds the tables
-// once.  Per value: one byte extract, one table load, one multiply-add into
-// the packed codes.
+// in a persistent grid of one CTA of 32 warps per SM.
 // ---------------------------------------------------------------------------
 constexpr int kRqWarps = 32;
 constexpr int kRqScales = 127;                      // scale bytes 0 .. 0x7E (sf <= 448)
-constexpr int kRqRow = 256;                         // one code per input byte
-constexpr int kRqLut = kRqScales * kRqRow;          // [scale byte][byte] -> E2M1 code
 constexpr int kRqOffX = kRqWarps * kNvGroup;        // after the group images: [2][128] f32 x of each magnitude
 constexpr int kRqOffDen = kRqOffX + 2 * 128 * 4;    // [2][127] f32 den of each scale byte (padded to 128)
-constexpr int kRqOffSb = kRqOffDen + 2 * 128 * 4;   // [2][128] u8 scale byte of a block's largest magnitude
-constexpr int kRqOffLut = kRqOffSb + 2 * 128;       // [2][kRqLut] u8
-constexpr int kRqSmem = kRqOffLut + 2 * kRqLut;
+constexpr int kRqOffThr = kRqOffDen + 2 * 128 * 4;  // [2][128] u8x8 T_1..T_7 of each scale byte (byte 7 unused)
+constexpr int kRqOffSb = kRqOffThr + 2 * 128 * 8;   // [2][128] u8 scale byte of a block's largest magnitude
+constexpr int kRqSmem = kRqOffSb + 2 * 128;
 
-// A row's entries are stored at byte ^ rq_swizzle(scale byte): an input
-// tensor's bytes cluster in a few dozen values, and without the swizzle the
-// lanes of a warp (each on its own block's row) would read the same few
-// banks at different rows; the XOR moves equal bytes of different rows onto
-// different banks (a permutation inside the row's 256 bytes).
-__device__ __forceinline__ uint32_t rq_swizzle(uint32_t sbyte) { return (sbyte & 31u) << 2; }
-
-// Codes of one 16-byte E4M3 block from the tables of its tensor: the scale
-// byte, then lo = values 0..7 and hi = values 8..15 (value 2j in the low
-// nibble of byte j), as quant16 gives them for the decoded values.
-__device__ __forceinline__ void requant16(const uint4 w, const uint8_t *lut, const uint8_t *sbl, const float *dens,
+// Codes of one 16-byte E4M3 block from the thresholds of its tensor: the
+// scale byte, then lo = values 0..7 and hi = values 8..15 (value 2j in the
+// low nibble of byte j), as quant16 gives them for the decoded values.  Four
+// values at a time: with a = byte | 0x80 in each byte lane, a - T_k (T_k <=
+// 0x80, so no lane borrows from the next) has bit 7 set exactly when
+// e >= T_k.  The seven flags are monotone in k, so the magnitude code's bits
+// are f4 (bit 2), f2 ^ f4 ^ f6 (bit 1) and f1 ^ ... ^ f7 (bit 0).
+__device__ __forceinline__ void requant16(const uint4 w, const uint2 *thr, const uint8_t *sbl, const float *dens,
                                           uint32_t &sbyte, uint32_t &lo, uint32_t &hi) {
   const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
   uint32_t m4 = __vmaxu4(__vmaxu4(ww[0] & 0x7F7F7F7Fu, ww[1] & 0x7F7F7F7Fu),
@@ -355,15 +354,24 @@ __device__ __forceinline__ void requant16(const uint4 w, const uint8_t *lut, con
   sbyte = sbl[m4 & 0x7Fu];
   lo = hi = 0;
   if (dens[sbyte] == 0.0f) return;
-  const uint8_t *row = lut + sbyte * kRqRow;
-  const uint32_t swz = rq_swizzle(sbyte);
+  const uint2 t = thr[sbyte];
+  const uint32_t t1 = __byte_perm(t.x, 0, 0x0000), t2 = __byte_perm(t.x, 0, 0x1111), t3 = __byte_perm(t.x, 0, 0x2222),
+                 t4 = __byte_perm(t.x, 0, 0x3333), t5 = __byte_perm(t.y, 0, 0x0000), t6 = __byte_perm(t.y, 0, 0x1111),
+                 t7 = __byte_perm(t.y, 0, 0x2222);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const uint32_t c = row[((ww[i >> 2] >> (8 * (i & 3))) & 0xFFu) ^ swz];
-    if (i < 8)
-      lo += c << (4 * i);  // disjoint nibbles: the add is an or
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t a = ww[q] | 0x80808080u;
+    const uint32_t f1 = a - t1, f2 = a - t2, f3 = a - t3, f4 = a - t4, f5 = a - t5, f6 = a - t6, f7 = a - t7;
+    const uint32_t b0 = f1 ^ f2 ^ f3 ^ f4 ^ f5 ^ f6 ^ f7, b1 = f2 ^ f4 ^ f6;
+    // the code of byte j in bits 4..7 of byte j: sign, f4, b1, b0
+    const uint32_t c = (ww[q] & 0x80808080u) | ((f4 >> 1) & 0x40404040u) | ((b1 >> 2) & 0x20202020u) |
+                       ((b0 >> 3) & 0x10101010u);
+    const uint32_t x = c >> 4;                                // code j in the low nibble of byte j
+    const uint32_t n = __byte_perm(x | (x >> 4), 0, 0x4420);  // codes 0..3 in nibbles 0..3
+    if (q < 2)
+      lo |= n << (16 * q);
     else
-      hi += c << (4 * (i - 8));
+      hi |= n << (16 * (q - 2));
   }
 }
 
@@ -374,11 +382,15 @@ __global__ void __launch_bounds__(kRqWarps * 32, 1)
   extern __shared__ __align__(16) uint8_t sm[];
   float *xs = reinterpret_cast<float *>(sm + kRqOffX);
   float *dens = reinterpret_cast<float *>(sm + kRqOffDen);
+  uint8_t *thr = sm + kRqOffThr;
   uint8_t *sbl = sm + kRqOffSb;
-  uint8_t *lut = sm + kRqOffLut;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the thresholds hold for a positive finite input scale and a finite global
+  // scale >= 0 (each comparison is false for NaN)
+  const bool by_thr = in_scale[0] > 0.0f && in_scale[1] > 0.0f && in_scale[0] <= FLT_MAX && in_scale[1] <= FLT_MAX &&
+                      gs[0] >= 0.0f && gs[1] >= 0.0f && gs[0] <= FLT_MAX && gs[1] <= FLT_MAX;
   // the tables of K (kind 0) and V (kind 1)
   for (int i = tid; i < 2 * 128; i += blockDim.x) {
     const int kind = i >> 7, e = i & 127;
@@ -393,14 +405,21 @@ __global__ void __launch_bounds__(kRqWarps * 32, 1)
     if (g != 0.0f) sb = e4m3x2_from_f32(__fdiv_rn(xs[i], __fmul_rn(6.0f, g)), 0.0f) & 0xFFu;
     sbl[i] = static_cast<uint8_t>(sb);
   }
-  for (int i = tid; i < 2 * kRqScales * 128; i += blockDim.x) {  // positive bytes; negative ones mirror them
-    const int kind = i / (kRqScales * 128), j = i % (kRqScales * 128), sb = j >> 7, e = j & 127;
+  // T_k of (kind, scale byte): the least e in [0, 127) whose magnitude code
+  // is >= k, by bisection (127: none below the NaN byte, stored as 128)
+  for (int i = tid; i < 2 * 128 * 8; i += blockDim.x) {
+    const int kind = i >> 10, sb = (i >> 3) & 127, k = (i & 7) + 1;
     const float den = dens[kind * 128 + sb];
-    uint32_t code = 0;
-    if (den != 0.0f) code = e2m1x2_from_f32(__fdiv_rn(xs[kind * 128 + e], den), 0.0f) & 0xFu;
-    uint8_t *row = lut + kind * kRqLut + sb * kRqRow;
-    row[e ^ rq_swizzle(sb)] = static_cast<uint8_t>(code);
-    row[(e | 0x80) ^ rq_swizzle(sb)] = static_cast<uint8_t>(code | 0x8u);
+    int lo_e = 0, hi_e = 127;
+    if (k <= 7 && den != 0.0f) {
+      while (lo_e < hi_e) {
+        const int mid = (lo_e + hi_e) >> 1;
+        const uint32_t mag = e2m1x2_from_f32(__fdiv_rn(xs[kind * 128 + mid], den), 0.0f) & 0x7u;
+        if (mag >= static_cast<uint32_t>(k)) hi_e = mid;
+        else lo_e = mid + 1;
+      }
+    }
+    thr[i] = static_cast<uint8_t>(lo_e == 127 ? 128 : lo_e);
   }
   __syncthreads();
   const int64_t ngroups = (num_tokens + 7) / 8;
@@ -412,7 +431,7 @@ __global__ void __launch_bounds__(kRqWarps * 32, 1)
     const int64_t s0 = __shfl_sync(0xffffffffu, sl, 0);
     const bool whole = __all_sync(0xffffffffu, s0 >= 0 && (s0 & 7) == 0 && sl == s0 + (lane & 7) &&
                                                    s0 + 7 < static_cast<int64_t>(c.num_pages) * c.P);
-    if (!whole) {
+    if (!whole || !by_thr) {
       for (int it = lane; it < 2 * 8 * kBlocksPerRow; it += 32) {
         const int kind = it / (8 * kBlocksPerRow), tt = (it / kBlocksPerRow) % 8, blk = it % kBlocksPerRow;
         if (t0 + tt < num_tokens)
@@ -428,7 +447,7 @@ __global__ void __launch_bounds__(kRqWarps * 32, 1)
         const int blk = 2 * (lane & 3) + j;
         const uint4 w = __ldg(reinterpret_cast<const uint4 *>(k8 + ((t0 + tk) * c.Hkv + h) * kD + 16 * blk));
         uint32_t sb, lo, hi;
-        requant16(w, lut, sbl, dens, sb, lo, hi);
+        requant16(w, reinterpret_cast<const uint2 *>(thr), sbl, dens, sb, lo, hi);
         *reinterpret_cast<uint2 *>(im + (blk >> 1) * 128 + tk * 16 + (blk & 1) * 8) = make_uint2(lo, hi);
         im[kNvKScales + tk * 8 + blk] = static_cast<uint8_t>(sb);
       }
@@ -439,7 +458,7 @@ __global__ void __launch_bounds__(kRqWarps * 32, 1)
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const uint4 w = __ldg(reinterpret_cast<const uint4 *>(v8 + ((t0 + 2 * p + u) * c.Hkv + h) * kD + 16 * blk));
-        requant16(w, lut + kRqLut, sbl + 128, dens + 128, sb[u], lo[u], hi[u]);
+        requant16(w, reinterpret_cast<const uint2 *>(thr) + 128, sbl + 128, dens + 128, sb[u], lo[u], hi[u]);
       }
       uint32_t w4[4];
 #pragma unroll
