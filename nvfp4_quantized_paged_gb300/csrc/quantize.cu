@@ -335,44 +335,48 @@ constexpr int kRqOffX = kRqWarps * kNvGroup;        // after the group images: [
 constexpr int kRqOffDen = kRqOffX + 2 * 128 * 4;    // [2][127] f32 den of each scale byte (padded to 128)
 constexpr int kRqOffThr = kRqOffDen + 2 * 128 * 4;  // [2][128] u8x8 T_1..T_7 of each scale byte (byte 7 unused)
 constexpr int kRqOffSb = kRqOffThr + 2 * 128 * 8;   // [2][128] u8 scale byte of a block's largest magnitude
-constexpr int kRqSmem = kRqOffSb + 2 * 128;
+constexpr int kRqOffTab = kRqOffSb + 2 * 128;       // [2][128] of 32 B: the block entry of each largest magnitude
+constexpr int kRqSmem = kRqOffTab + 2 * 128 * 32;
 
-// Codes of one 16-byte E4M3 block from the thresholds of its tensor: the
-// scale byte, then lo = values 0..7 and hi = values 8..15 (value 2j in the
-// low nibble of byte j), as quant16 gives them for the decoded values.  Four
-// values at a time: with a = byte | 0x80 in each byte lane, a - T_k (T_k <=
-// 0x80, so no lane borrows from the next) has bit 7 set exactly when
-// e >= T_k.  The seven flags are monotone in k, so the magnitude code's bits
-// are f4 (bit 2), f2 ^ f4 ^ f6 (bit 1) and f1 ^ ... ^ f7 (bit 0).
-__device__ __forceinline__ void requant16(const uint4 w, const uint2 *thr, const uint8_t *sbl, const float *dens,
-                                          uint32_t &sbyte, uint32_t &lo, uint32_t &hi) {
+// A block's entry, indexed by its largest magnitude m: the seven thresholds
+// of its scale byte sb[m], each repeated in the four bytes of a word, then
+// sb[m] in byte 0 and the sign mask (0x80, or 0 when den is 0: every code 0)
+// in byte 1 of the last word.  When den is 0 the thresholds are all 128.
+struct RqEntry {
+  uint4 a, b;  // a = T1..T4, b = T5, T6, T7, meta
+};
+
+// Codes of one 16-byte E4M3 block: the scale byte, and X[q] = the codes of
+// values 4q..4q+3 in the low nibbles of bytes 0..3.  Four values at a time:
+// with a = byte | 0x80 in each byte lane, a - T_k (T_k <= 0x80, so no lane
+// borrows from the next) has bit 7 set exactly when e >= T_k.  The seven
+// flags are monotone in k, so the magnitude code's bits are f4 (bit 2),
+// f2 ^ f4 ^ f6 (bit 1) and f1 ^ ... ^ f7 (bit 0).  The largest magnitude is
+// the byte maximum of the four a words (bit 7 set in all of them).
+__device__ __forceinline__ void requant_codes(const uint4 w, const RqEntry *tab, uint32_t &sbyte, uint32_t X[4]) {
   const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-  uint32_t m4 = __vmaxu4(__vmaxu4(ww[0] & 0x7F7F7F7Fu, ww[1] & 0x7F7F7F7Fu),
-                         __vmaxu4(ww[2] & 0x7F7F7F7Fu, ww[3] & 0x7F7F7F7Fu));
+  uint32_t a[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) a[q] = ww[q] | 0x80808080u;
+  uint32_t m4 = __vmaxu4(__vmaxu4(a[0], a[1]), __vmaxu4(a[2], a[3]));
   m4 = __vmaxu4(m4, m4 >> 16);
   m4 = __vmaxu4(m4, m4 >> 8);
-  sbyte = sbl[m4 & 0x7Fu];
-  lo = hi = 0;
-  if (dens[sbyte] == 0.0f) return;
-  const uint2 t = thr[sbyte];
-  const uint32_t t1 = __byte_perm(t.x, 0, 0x0000), t2 = __byte_perm(t.x, 0, 0x1111), t3 = __byte_perm(t.x, 0, 0x2222),
-                 t4 = __byte_perm(t.x, 0, 0x3333), t5 = __byte_perm(t.y, 0, 0x0000), t6 = __byte_perm(t.y, 0, 0x1111),
-                 t7 = __byte_perm(t.y, 0, 0x2222);
+  const RqEntry e = tab[m4 & 0x7Fu];
+  sbyte = e.b.w & 0xFFu;
+  const uint32_t smask = __byte_perm(e.b.w, 0, 0x1111);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint32_t a = ww[q] | 0x80808080u;
-    const uint32_t f1 = a - t1, f2 = a - t2, f3 = a - t3, f4 = a - t4, f5 = a - t5, f6 = a - t6, f7 = a - t7;
+    const uint32_t f1 = a[q] - e.a.x, f2 = a[q] - e.a.y, f3 = a[q] - e.a.z, f4 = a[q] - e.a.w, f5 = a[q] - e.b.x,
+                   f6 = a[q] - e.b.y, f7 = a[q] - e.b.z;
     const uint32_t b0 = f1 ^ f2 ^ f3 ^ f4 ^ f5 ^ f6 ^ f7, b1 = f2 ^ f4 ^ f6;
-    // the code of byte j in bits 4..7 of byte j: sign, f4, b1, b0
-    const uint32_t c = (ww[q] & 0x80808080u) | ((f4 >> 1) & 0x40404040u) | ((b1 >> 2) & 0x20202020u) |
-                       ((b0 >> 3) & 0x10101010u);
-    const uint32_t x = c >> 4;                                // code j in the low nibble of byte j
-    const uint32_t n = __byte_perm(x | (x >> 4), 0, 0x4420);  // codes 0..3 in nibbles 0..3
-    if (q < 2)
-      lo |= n << (16 * q);
-    else
-      hi |= n << (16 * (q - 2));
+    X[q] = ((ww[q] & smask) >> 4) | ((f4 >> 5) & 0x04040404u) | ((b1 >> 6) & 0x02020202u) | ((b0 >> 7) & 0x01010101u);
   }
+}
+
+// Four codes in the low nibbles of bytes 0..3 of x and y -> the 8 nibbles of
+// one word (x's codes first, code i in nibble i).
+__device__ __forceinline__ uint32_t pack8(uint32_t x, uint32_t y) {
+  return __byte_perm(x | (x >> 4), y | (y >> 4), 0x6420);
 }
 
 __global__ void __launch_bounds__(kRqWarps * 32, 1)
@@ -384,6 +388,7 @@ __global__ void __launch_bounds__(kRqWarps * 32, 1)
   float *dens = reinterpret_cast<float *>(sm + kRqOffDen);
   uint8_t *thr = sm + kRqOffThr;
   uint8_t *sbl = sm + kRqOffSb;
+  RqEntry *tab = reinterpret_cast<RqEntry *>(sm + kRqOffTab);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -422,14 +427,48 @@ __global__ void __launch_bounds__(kRqWarps * 32, 1)
     thr[i] = static_cast<uint8_t>(lo_e == 127 ? 128 : lo_e);
   }
   __syncthreads();
+  for (int i = tid; i < 2 * 128; i += blockDim.x) {  // the entry of each largest magnitude
+    const int kind = i >> 7;
+    const uint32_t sb = sbl[i];
+    const bool zero = !(sb < static_cast<uint32_t>(kRqScales)) || dens[kind * 128 + sb] == 0.0f;
+    uint32_t t[8];
+#pragma unroll
+    for (int k = 0; k < 7; ++k) t[k] = zero ? 0x80808080u : thr[(kind * 128 + sb) * 8 + k] * 0x01010101u;
+    t[7] = (sb & 0xFFu) | (zero ? 0u : 0x8000u);
+    tab[i].a = make_uint4(t[0], t[1], t[2], t[3]);
+    tab[i].b = make_uint4(t[4], t[5], t[6], t[7]);
+  }
+  __syncthreads();
   const int64_t ngroups = (num_tokens + 7) / 8;
-  for (int64_t wid = static_cast<int64_t>(blockIdx.x) * kRqWarps + warp; wid < ngroups * c.Hkv;
+  const int64_t items = ngroups * c.Hkv;
+  for (int64_t wid = static_cast<int64_t>(blockIdx.x) * kRqWarps + warp; wid < items;
        wid += static_cast<int64_t>(gridDim.x) * kRqWarps) {
-    const int h = static_cast<int>(wid % c.Hkv);
-    const int64_t t0 = (wid / c.Hkv) * 8;
+    int h;
+    int64_t t0;
+    if (items <= 0x7fffffff) {  // 32-bit index arithmetic when it fits
+      const uint32_t w32 = static_cast<uint32_t>(wid), hk = static_cast<uint32_t>(c.Hkv);
+      h = static_cast<int>(w32 % hk);
+      t0 = static_cast<int64_t>(w32 / hk) * 8;
+    } else {
+      h = static_cast<int>(wid % c.Hkv);
+      t0 = (wid / c.Hkv) * 8;
+    }
+    // this lane's K and V blocks, loaded before the slots are known (tokens past
+    // the end are not read: such an item takes the per-value path)
+    const int tk = lane >> 2, p = lane >> 3, vb = lane & 7;
+    uint4 kw[2], vw[2];
+    const bool full8 = t0 + 8 <= num_tokens;
+    if (full8) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        kw[j] = __ldg(reinterpret_cast<const uint4 *>(k8 + ((t0 + tk) * c.Hkv + h) * kD + 16 * (2 * (lane & 3) + j)));
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+        vw[u] = __ldg(reinterpret_cast<const uint4 *>(v8 + ((t0 + 2 * p + u) * c.Hkv + h) * kD + 16 * vb));
+    }
     const int64_t sl = t0 + (lane & 7) < num_tokens ? slot_mapping[t0 + (lane & 7)] : -1;
     const int64_t s0 = __shfl_sync(0xffffffffu, sl, 0);
-    const bool whole = __all_sync(0xffffffffu, s0 >= 0 && (s0 & 7) == 0 && sl == s0 + (lane & 7) &&
+    const bool whole = __all_sync(0xffffffffu, full8 && s0 >= 0 && (s0 & 7) == 0 && sl == s0 + (lane & 7) &&
                                                    s0 + 7 < static_cast<int64_t>(c.num_pages) * c.P);
     if (!whole || !by_thr) {
       for (int it = lane; it < 2 * 8 * kBlocksPerRow; it += 32) {
@@ -441,37 +480,36 @@ __global__ void __launch_bounds__(kRqWarps * 32, 1)
     }
     uint8_t *im = sm + warp * kNvGroup;
     {  // K: token tk, blocks 2 (lane % 4) and 2 (lane % 4) + 1
-      const int tk = lane >> 2;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int blk = 2 * (lane & 3) + j;
-        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(k8 + ((t0 + tk) * c.Hkv + h) * kD + 16 * blk));
-        uint32_t sb, lo, hi;
-        requant16(w, reinterpret_cast<const uint2 *>(thr), sbl, dens, sb, lo, hi);
-        *reinterpret_cast<uint2 *>(im + (blk >> 1) * 128 + tk * 16 + (blk & 1) * 8) = make_uint2(lo, hi);
+        uint32_t sb, X[4];
+        requant_codes(kw[j], tab, sb, X);
+        *reinterpret_cast<uint2 *>(im + (blk >> 1) * 128 + tk * 16 + (blk & 1) * 8) =
+            make_uint2(pack8(X[0], X[1]), pack8(X[2], X[3]));
         im[kNvKScales + tk * 8 + blk] = static_cast<uint8_t>(sb);
       }
     }
-    {  // V: slots 2p and 2p + 1, block blk (slot 2p in the low nibble)
-      const int p = lane >> 3, blk = lane & 7;
-      uint32_t sb[2], lo[2], hi[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(v8 + ((t0 + 2 * p + u) * c.Hkv + h) * kD + 16 * blk));
-        requant16(w, reinterpret_cast<const uint2 *>(thr) + 128, sbl + 128, dens + 128, sb[u], lo[u], hi[u]);
-      }
-      uint32_t w4[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        w4[q] = spread4(((q < 2 ? lo[0] : hi[0]) >> (16 * (q & 1))) & 0xFFFFu) |
-                (spread4(((q < 2 ? lo[1] : hi[1]) >> (16 * (q & 1))) & 0xFFFFu) << 4);
-      *reinterpret_cast<uint4 *>(im + kNvVCodes + blk * 64 + p * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      im[kNvVScales + blk * 8 + 2 * p] = static_cast<uint8_t>(sb[0]);
-      im[kNvVScales + blk * 8 + 2 * p + 1] = static_cast<uint8_t>(sb[1]);
+    {  // V: slots 2p and 2p + 1, block vb (slot 2p in the low nibble)
+      uint32_t sb[2], X0[4], X1[4];
+      requant_codes(vw[0], tab + 128, sb[0], X0);
+      requant_codes(vw[1], tab + 128, sb[1], X1);
+      *reinterpret_cast<uint4 *>(im + kNvVCodes + vb * 64 + p * 16) =
+          make_uint4(X0[0] | (X1[0] << 4), X0[1] | (X1[1] << 4), X0[2] | (X1[2] << 4), X0[3] | (X1[3] << 4));
+      im[kNvVScales + vb * 8 + 2 * p] = static_cast<uint8_t>(sb[0]);
+      im[kNvVScales + vb * 8 + 2 * p + 1] = static_cast<uint8_t>(sb[1]);
     }
     __syncwarp();
-    const int64_t page = s0 / c.P;
-    const int off = static_cast<int>(s0 % c.P);
+    int64_t page;
+    int off;
+    if (s0 <= 0x7fffffff) {
+      const uint32_t s32 = static_cast<uint32_t>(s0), pp = static_cast<uint32_t>(c.P);
+      page = s32 / pp;
+      off = static_cast<int>(s32 - static_cast<uint32_t>(page) * pp);
+    } else {
+      page = s0 / c.P;
+      off = static_cast<int>(s0 % c.P);
+    }
     uint4 *dst =
         reinterpret_cast<uint4 *>(c.data + c.block(page, h, kNvTokBytes) + static_cast<int64_t>(off >> 3) * kNvGroup);
     const uint4 *src = reinterpret_cast<const uint4 *>(im);
