@@ -721,7 +721,7 @@ def run_prefill_write(args):
                 "gpu_launches": args.steps,
                 "roofline": {"bound": "hbm", "kernel": "nvfp4_requant_kernel", "achieved": round(gbs, 1),
                              "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(gbs / peak, 4),
-                             "traffic": None, "algorithmic_bytes_per_launch": int(per),
+                             "traffic": _prefill_traffic(args.workload), "algorithmic_bytes_per_launch": int(per),
                              "avg_launch_us": round(ms * 1e3, 2),
                              "timed": "CUDA events around one graph of K write launches, replicas rotated"},
                 "clocks": clk.summary()}
@@ -846,15 +846,28 @@ def run_calibration(args):
 
 
 DECODE_SOURCES = ("decode.cu", "nvkv_device.cuh", "nvkv_host.h")
+WRITE_SOURCES = ("quantize.cu", "nvkv_device.cuh", "nvkv_host.h")
 
 
-def decode_sources_sha256():
-    """Hash of the decode kernel's sources (the kernel file and the headers it includes)."""
+def decode_sources_sha256(names=DECODE_SOURCES):
+    """Hash of a kernel's sources (the kernel file and the headers it includes)."""
     import hashlib
     h = hashlib.sha256()
-    for name in DECODE_SOURCES:
+    for name in names:
         h.update(open(os.path.join(ROOT, "nvfp4_quantized_paged_gb300", "csrc", name), "rb").read())
     return h.hexdigest()
+
+
+def _prefill_traffic(workload):
+    """DRAM bytes per prefill-write launch from the committed ncu summary, if it
+    was taken on the current write kernel sources (else None)."""
+    try:
+        prof = json.load(open(os.path.join(ROOT, "profiles", f"prefill_write_{workload}.json")))
+        if prof.get("write_sources_sha256") != decode_sources_sha256(WRITE_SOURCES):
+            return None
+        return prof.get("dram_bytes_per_launch")
+    except Exception:
+        return None
 
 
 def _traffic_from_profile(workload):

@@ -358,10 +358,15 @@ __device__ __forceinline__ void requant_codes(const uint4 w, const RqEntry *tab,
   uint32_t a[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) a[q] = ww[q] | 0x80808080u;
-  uint32_t m4 = __vmaxu4(__vmaxu4(a[0], a[1]), __vmaxu4(a[2], a[3]));
-  m4 = __vmaxu4(m4, m4 >> 16);
-  m4 = __vmaxu4(m4, m4 >> 8);
-  const RqEntry e = tab[m4 & 0x7Fu];
+  uint32_t mx = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t ev = ww[q] & 0x007F007Fu, od = (ww[q] >> 8) & 0x007F007Fu, t;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(t) : "r"(ev), "r"(od));
+    asm("max.u16x2 %0, %1, %2;" : "=r"(mx) : "r"(mx), "r"(t));
+  }
+  const uint32_t m4 = max(mx & 0xFFFFu, mx >> 16);
+  const RqEntry e = tab[m4];
   sbyte = e.b.w & 0xFFu;
   const uint32_t smask = __byte_perm(e.b.w, 0, 0x1111);
 #pragma unroll
