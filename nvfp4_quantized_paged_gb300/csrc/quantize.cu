@@ -446,11 +446,17 @@ __global__ void __launch_bounds__(kRqWarps * 32, 1)
   __syncthreads();
   const int64_t ngroups = (num_tokens + 7) / 8;
   const int64_t items = ngroups * c.Hkv;
+  const int lgP = __ffs(c.P) - 1;  // page sizes are powers of two (16, 32, 64)
+  const bool hk_pow2 = (c.Hkv & (c.Hkv - 1)) == 0;
+  const int lgH = __ffs(c.Hkv) - 1;
   for (int64_t wid = static_cast<int64_t>(blockIdx.x) * kRqWarps + warp; wid < items;
        wid += static_cast<int64_t>(gridDim.x) * kRqWarps) {
     int h;
     int64_t t0;
-    if (items <= 0x7fffffff) {  // 32-bit index arithmetic when it fits
+    if (hk_pow2) {
+      h = static_cast<int>(wid & (c.Hkv - 1));
+      t0 = (wid >> lgH) * 8;
+    } else if (items <= 0x7fffffff) {  // 32-bit index arithmetic when it fits
       const uint32_t w32 = static_cast<uint32_t>(wid), hk = static_cast<uint32_t>(c.Hkv);
       h = static_cast<int>(w32 % hk);
       t0 = static_cast<int64_t>(w32 / hk) * 8;
@@ -505,16 +511,8 @@ __global__ void __launch_bounds__(kRqWarps * 32, 1)
       im[kNvVScales + vb * 8 + 2 * p + 1] = static_cast<uint8_t>(sb[1]);
     }
     __syncwarp();
-    int64_t page;
-    int off;
-    if (s0 <= 0x7fffffff) {
-      const uint32_t s32 = static_cast<uint32_t>(s0), pp = static_cast<uint32_t>(c.P);
-      page = s32 / pp;
-      off = static_cast<int>(s32 - static_cast<uint32_t>(page) * pp);
-    } else {
-      page = s0 / c.P;
-      off = static_cast<int>(s0 % c.P);
-    }
+    const int64_t page = s0 >> lgP;
+    const int off = static_cast<int>(s0 & (c.P - 1));
     uint4 *dst =
         reinterpret_cast<uint4 *>(c.data + c.block(page, h, kNvTokBytes) + static_cast<int64_t>(off >> 3) * kNvGroup);
     const uint4 *src = reinterpret_cast<const uint4 *>(im);
