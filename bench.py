@@ -17,7 +17,9 @@ the step (GB/s; bytes of NVFP4/FP8 K/V codes + scales read, Q read, output
 written, new tokens read and their codes written) over the device-timed step;
 ``roofline`` times the NVFP4 layers' decode calls alone;
 ``e2e`` is the same metric with the step's inputs copied from pinned host
-memory and the output copied back inside the timed region.  The FP8-KV
+memory and the output copied back inside the timed region (one copy in and
+one copy out per layer and step, on two copy streams, each ordered against
+its layer's step by events so that copies overlap other layers' steps).  The FP8-KV
 variant of the same workload is timed beside it as the comparator.  Between
 timed steps the caches rotate over replicas whose total exceeds L2.
 
@@ -321,12 +323,40 @@ def measure_workload(name, args, dev, dist, stream, full=True):
         h2d = sum(h["inp"].numel() for h in host)
         d2h = sum(h["out"].numel() * 2 for h in host)
 
+        # The copies run on two copy streams, a layer's input copy and its
+        # output copy ordered against that layer's step by events, so the
+        # copies of one layer overlap the steps of the others (as a serving
+        # loop pipelines them).  Every step still copies every input in and
+        # every output out inside the timed region.
+        h2d_stream, d2h_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        in_free = [[None] * len(host) for _ in sets]   # the layer's last step that read this input buffer
+        out_free = [[None] * len(host) for _ in sets]  # the copy-out that last read this output
+
         def e2e_step(i):
             r = i % len(sets)
-            for lay, buf, h in zip(sets[r], bufs[r], host):
-                buf.copy_(h["inp"], non_blocking=True)
+            ready = []
+            with torch.cuda.stream(h2d_stream):
+                for j, (buf, h) in enumerate(zip(bufs[r], host)):
+                    if in_free[r][j] is not None:
+                        h2d_stream.wait_event(in_free[r][j])
+                    buf.copy_(h["inp"], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(h2d_stream)
+                    ready.append(ev)
+            for j, (lay, h) in enumerate(zip(sets[r], host)):
+                stream.wait_event(ready[j])
+                if out_free[r][j] is not None:
+                    stream.wait_event(out_free[r][j])
                 lay.step()
-                h["out"].copy_(lay.out, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                in_free[r][j] = ev
+                with torch.cuda.stream(d2h_stream):
+                    d2h_stream.wait_event(ev)
+                    h["out"].copy_(lay.out, non_blocking=True)
+                    ev_out = torch.cuda.Event()
+                    ev_out.record(d2h_stream)
+                    out_free[r][j] = ev_out
 
         for i in range(args.warmup):
             e2e_step(i)
@@ -334,8 +364,10 @@ def measure_workload(name, args, dev, dist, stream, full=True):
         _barrier(dist)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        h2d_stream.wait_event(e0)  # no copy of the timed steps starts before the region does
         for i in range(args.steps):
             e2e_step(i)
+        stream.wait_stream(d2h_stream)  # the region ends after the last copy-out
         e1.record(stream)
         torch.cuda.synchronize()
         res.update(e2e_ms=_max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, dev), h2d=h2d, d2h=d2h)
