@@ -172,8 +172,8 @@ __device__ void nvfp4_write_item(const T *__restrict__ k, const T *__restrict__ 
     if (kind == 0 && h == 0 && blk == 0) set_err(c.err, NVKV_DEVERR_SLOT);
     return;
   }
-  const int64_t page = slot / c.P;
-  const int off = static_cast<int>(slot % c.P);
+  const int64_t page = slot >> (__ffs(c.P) - 1);  // page sizes are powers of two (16, 32, 64)
+  const int off = static_cast<int>(slot & (c.P - 1));
   const bool paired = slot_p == (slot ^ 1);
   if (paired && (t & 1)) return;
   float x[16];
@@ -246,8 +246,15 @@ __global__ void __launch_bounds__(kWriteWarps * 32)
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWriteWarps + warp;
   const int64_t ngroups = (num_tokens + 7) / 8;
   if (wid >= ngroups * c.Hkv) return;
-  const int h = static_cast<int>(wid % c.Hkv);
-  const int64_t t0 = (wid / c.Hkv) * 8;
+  int h;
+  int64_t t0;
+  if ((c.Hkv & (c.Hkv - 1)) == 0) {  // shifts for power-of-two head counts
+    h = static_cast<int>(wid & (c.Hkv - 1));
+    t0 = (wid >> (__ffs(c.Hkv) - 1)) * 8;
+  } else {
+    h = static_cast<int>(wid % c.Hkv);
+    t0 = (wid / c.Hkv) * 8;
+  }
   const int64_t sl = t0 + (lane & 7) < num_tokens ? slot_mapping[t0 + (lane & 7)] : -1;
   const int64_t s0 = __shfl_sync(0xffffffffu, sl, 0);
   const bool whole = __all_sync(0xffffffffu, s0 >= 0 && (s0 & 7) == 0 && sl == s0 + (lane & 7) &&
@@ -300,8 +307,8 @@ __global__ void __launch_bounds__(kWriteWarps * 32)
     im[kNvVScales + blk * 8 + 2 * p + 1] = static_cast<uint8_t>(sb[1]);
   }
   __syncwarp();
-  const int64_t page = s0 / c.P;
-  const int off = static_cast<int>(s0 % c.P);
+  const int64_t page = s0 >> (__ffs(c.P) - 1);  // page sizes are powers of two (16, 32, 64)
+  const int off = static_cast<int>(s0 & (c.P - 1));
   uint4 *dst = reinterpret_cast<uint4 *>(c.data + c.block(page, h, kNvTokBytes) + static_cast<int64_t>(off >> 3) * kNvGroup);
   const uint4 *src = reinterpret_cast<const uint4 *>(im);
   for (int i = lane; i < kNvGroup / 16; i += 32) dst[i] = src[i];
@@ -536,16 +543,23 @@ __global__ void __launch_bounds__(256)
   const int kind = blockIdx.y;
   const int blk = static_cast<int>(gid % kBlocksPerRow);
   const int64_t th = gid / kBlocksPerRow;
-  const int h = static_cast<int>(th % c.Hkv);
-  const int64_t t = th / c.Hkv;
+  int h;
+  int64_t t;
+  if ((c.Hkv & (c.Hkv - 1)) == 0) {  // shifts for power-of-two head counts
+    h = static_cast<int>(th & (c.Hkv - 1));
+    t = th >> (__ffs(c.Hkv) - 1);
+  } else {
+    h = static_cast<int>(th % c.Hkv);
+    t = th / c.Hkv;
+  }
   const int64_t slot = slot_mapping[t];
   if (slot < 0) return;
   if (slot >= static_cast<int64_t>(c.num_pages) * c.P) {
     if (kind == 0 && h == 0 && blk == 0) set_err(c.err, NVKV_DEVERR_SLOT);
     return;
   }
-  const int64_t page = slot / c.P;
-  const int off = static_cast<int>(slot % c.P);
+  const int64_t page = slot >> (__ffs(c.P) - 1);
+  const int off = static_cast<int>(slot & (c.P - 1));
   float x[16];
   load16((kind == 0 ? k : v) + th * kD + 16 * blk, x);
   const float s8 = gs[kind];
@@ -604,8 +618,15 @@ __global__ void __launch_bounds__(256)
   const int kind = blockIdx.y;
   const int blk = static_cast<int>(gid % kBlocksPerRow);
   const int64_t rh = gid / kBlocksPerRow;
-  const int h = static_cast<int>(rh % c.Hkv);
-  const int64_t r = rh / c.Hkv;
+  int h;
+  int64_t r;
+  if ((c.Hkv & (c.Hkv - 1)) == 0) {  // shifts for power-of-two head counts (a 64-bit division is a long subroutine)
+    h = static_cast<int>(rh & (c.Hkv - 1));
+    r = rh >> (__ffs(c.Hkv) - 1);
+  } else {
+    h = static_cast<int>(rh % c.Hkv);
+    r = rh / c.Hkv;
+  }
   const int64_t total = cu_prefix[n];
   if (r == 0 && h == 0 && blk == 0 && kind == 0 && total > ws_rows) set_err(c.err, NVKV_DEVERR_WS_ROWS);
   if (r >= total) return;
@@ -617,16 +638,17 @@ __global__ void __launch_bounds__(256)
   }
   const int64_t t = r - cu_prefix[lo];
   if (t >= prefix_lens[lo]) return;
-  if (t / c.P >= max_pages) {  // prefix longer than its block-table row
+  const int lgP = __ffs(c.P) - 1;  // page sizes are powers of two (16, 32, 64)
+  if ((t >> lgP) >= max_pages) {  // prefix longer than its block-table row
     set_err(c.err, NVKV_DEVERR_SEQLEN);
     return;
   }
-  const int64_t page = block_table[static_cast<int64_t>(seq_ids[lo]) * max_pages + t / c.P];
+  const int64_t page = block_table[static_cast<int64_t>(seq_ids[lo]) * max_pages + (t >> lgP)];
   if (page < 0 || page >= c.num_pages) {
     set_err(c.err, NVKV_DEVERR_PAGE);
     return;
   }
-  const int off = static_cast<int>(t % c.P);
+  const int off = static_cast<int>(t & (c.P - 1));
   uint2 cw;
   if (kind == 0) {
     cw = *reinterpret_cast<const uint2 *>(c.data + c.nv_kcodes(page, h, off, blk));
